@@ -1,0 +1,279 @@
+"""Float64 CPU oracle for paged-KV extend attention and its companions.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference leg of ``bench.py`` may import this package.  The
+product library (``paged_kv_extend_gb300``) never imports, loads or calls it,
+and this package imports nothing from the product library.
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision, loops over
+sequence -> head -> query -> key).  This module only compiles it with gcc and
+marshals torch CPU tensors into it.  Each wrapper names the page section whose
+definition it restates; the C file states the definition itself.
+
+Pins: every function here is checked against something other than itself in
+``tests/test_oracle_pins.py`` (library routines, closed forms, invariants the
+pages fix, and hand-derived golden values under ``tests/golden/``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_p = ctypes.c_void_p
+_l = ctypes.c_long
+_i = ctypes.c_int
+_d = ctypes.c_double
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, -O2, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+           "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _configure(lib):
+    lib.oracle_num_threads.restype = _i
+    lib.oracle_extend_attention.restype = _i
+    lib.oracle_extend_attention.argtypes = [
+        _p, _p, _l, _l, _p, _l, _l, _p, _l, _l, _p, _l, _l,
+        _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _l, _p, _l, _p, _p]
+    lib.oracle_extend_attention_unified.restype = _i
+    lib.oracle_extend_attention_unified.argtypes = [
+        _p, _p, _l, _l, _p, _l, _l, _p, _p, _p, _p,
+        _i, _i, _i, _i, _i, _d, _d, _l, _p, _l, _p, _p]
+    lib.oracle_decode_attention.restype = _i
+    lib.oracle_decode_attention.argtypes = [
+        _p, _p, _l, _l, _p, _l, _l, _p, _p,
+        _i, _i, _i, _i, _i, _d, _d, _l, _p, _p]
+    lib.oracle_merge_state.restype = None
+    lib.oracle_merge_state.argtypes = [_p, _p, _p, _p, _l, _i, _i, _p, _p]
+    lib.oracle_build_unified_kv_indices.restype = None
+    lib.oracle_build_unified_kv_indices.argtypes = [
+        _p, _p, _p, _p, _p, _i, _p, _p, _p]
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _configure(ctypes.CDLL(build()))
+    return _lib
+
+
+class use_library:
+    """Context manager for tests: run the wrappers against another build of
+    the oracle (e.g. one with a deliberately planted mistake)."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self._saved = _lib
+        _lib = None
+        _lib = _configure(ctypes.CDLL(self.path))
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self._saved
+        return False
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle runs on."""
+    return int(_load().oracle_num_threads())
+
+
+# ---------------------------------------------------------------- marshalling
+def _bf16_bits(t: torch.Tensor) -> torch.Tensor:
+    """A CPU bf16 tensor reinterpreted as its int16 bit patterns (no copy of
+    values, strides preserved)."""
+    assert t.dtype == torch.bfloat16, t.dtype
+    return t.detach().cpu().view(torch.int16)
+
+
+def _ptr(t) -> int:
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _i32(t: torch.Tensor) -> torch.Tensor:
+    return t.detach().cpu().to(torch.int32).contiguous()
+
+
+def _i64(t: torch.Tensor) -> torch.Tensor:
+    return t.detach().cpu().to(torch.int64).contiguous()
+
+
+def _row_strides(t: torch.Tensor):
+    """(token/slot stride, head stride) in elements of a [n, h, d] view whose
+    last dim is contiguous."""
+    assert t.dim() == 3 and t.stride(2) == 1, (t.shape, t.stride())
+    return t.stride(0), t.stride(1)
+
+
+def _rows_arg(rows):
+    if rows is None:
+        return None, 0
+    r = _i64(torch.as_tensor(rows))
+    return r, r.numel()
+
+
+# ------------------------------------------------------------------ functions
+def extend_attention(q_extend, k_extend, v_extend, k_buffer, v_buffer,
+                     qo_indptr, kv_indptr, kv_indices, sm_scale, logit_cap=0.0,
+                     sliding_window=-1, rows=None):
+    """Two-stage extend attention (sglang extend_attention.py,
+    extend_attention_fwd): prefix K/V through kv_indptr/kv_indices into the
+    pool, extend K/V contiguous at qo_indptr.
+
+    q_extend [N, Hq, Lq] bf16; k_extend [N, Hkv, Lq]; v_extend [N, Hkv, Lv];
+    k_buffer [S, Hkv, Lq]; v_buffer [S, Hkv, Lv] (views with a contiguous last
+    dim; v may alias k).  sm_scale <= 0 means 1/sqrt(Lq).
+    Returns (o [N, Hq, Lv] float64, lse [N, Hq] float64), or for ``rows`` (a
+    list of token*Hq + head) o [R, Lv] and lse [R].
+    """
+    lib = _load()
+    n, hq, lq = q_extend.shape
+    hkv = k_buffer.shape[1]
+    lv = v_buffer.shape[2]
+    if sm_scale is None or sm_scale <= 0:
+        sm_scale = 1.0 / (lq ** 0.5)
+    q = _bf16_bits(q_extend).contiguous()
+    ke, ve = _bf16_bits(k_extend), _bf16_bits(v_extend)
+    kb, vb = _bf16_bits(k_buffer), _bf16_bits(v_buffer)
+    qo, kvp, kvi = _i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices)
+    batch = qo.numel() - 1
+    rws, nr = _rows_arg(rows)
+    count = nr if rws is not None else n * hq
+    o = torch.empty(count, lv, dtype=torch.float64)
+    lse = torch.empty(count, dtype=torch.float64)
+    rc = lib.oracle_extend_attention(
+        _ptr(q), _ptr(ke), *_row_strides(ke), _ptr(ve), *_row_strides(ve),
+        _ptr(kb), *_row_strides(kb), _ptr(vb), *_row_strides(vb),
+        _ptr(qo), _ptr(kvp), _ptr(kvi) if kvi.numel() else None,
+        batch, hq, hkv, lq, lv, float(sm_scale), float(logit_cap),
+        int(sliding_window), _ptr(rws) if rws is not None else None, nr,
+        _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_extend_attention: bad arguments")
+    if rws is None:
+        return o.view(n, hq, lv), lse.view(n, hq)
+    return o, lse
+
+
+def extend_attention_unified(q, k_buffer, v_buffer, qo_indptr, kv_indptr,
+                             kv_indices, prefix_lens, sm_scale, logit_cap=0.0,
+                             sliding_window=-1, rows=None):
+    """Unified extend attention (sglang extend_attention.py,
+    extend_attention_fwd_unified): all keys through the unified int64
+    kv_indices; the first prefix_lens[b] keys of sequence b are its prefix.
+    Shapes and returns as :func:`extend_attention`."""
+    lib = _load()
+    n, hq, lq = q.shape
+    hkv = k_buffer.shape[1]
+    lv = v_buffer.shape[2]
+    if sm_scale is None or sm_scale <= 0:
+        sm_scale = 1.0 / (lq ** 0.5)
+    qb = _bf16_bits(q).contiguous()
+    kb, vb = _bf16_bits(k_buffer), _bf16_bits(v_buffer)
+    qo, kvp, kvi, pl = _i32(qo_indptr), _i32(kv_indptr), _i64(kv_indices), _i32(prefix_lens)
+    batch = qo.numel() - 1
+    rws, nr = _rows_arg(rows)
+    count = nr if rws is not None else n * hq
+    o = torch.empty(count, lv, dtype=torch.float64)
+    lse = torch.empty(count, dtype=torch.float64)
+    rc = lib.oracle_extend_attention_unified(
+        _ptr(qb), _ptr(kb), *_row_strides(kb), _ptr(vb), *_row_strides(vb),
+        _ptr(qo), _ptr(kvp), _ptr(kvi) if kvi.numel() else None, _ptr(pl),
+        batch, hq, hkv, lq, lv, float(sm_scale), float(logit_cap),
+        int(sliding_window), _ptr(rws) if rws is not None else None, nr,
+        _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_extend_attention_unified: bad arguments")
+    if rws is None:
+        return o.view(n, hq, lv), lse.view(n, hq)
+    return o, lse
+
+
+def decode_attention(q, k_buffer, v_buffer, kv_indptr, kv_indices, sm_scale,
+                     logit_cap=0.0, sliding_window=-1):
+    """Decode attention (sglang flashinfer_backend.py, forward_decode): one
+    query per sequence over all of its pooled keys.
+    q [B, Hq, Lq] bf16 -> (o [B, Hq, Lv] float64, lse [B, Hq] float64)."""
+    lib = _load()
+    b, hq, lq = q.shape
+    hkv = k_buffer.shape[1]
+    lv = v_buffer.shape[2]
+    if sm_scale is None or sm_scale <= 0:
+        sm_scale = 1.0 / (lq ** 0.5)
+    qb = _bf16_bits(q).contiguous()
+    kb, vb = _bf16_bits(k_buffer), _bf16_bits(v_buffer)
+    kvp, kvi = _i32(kv_indptr), _i32(kv_indices)
+    o = torch.empty(b, hq, lv, dtype=torch.float64)
+    lse = torch.empty(b, hq, dtype=torch.float64)
+    rc = lib.oracle_decode_attention(
+        _ptr(qb), _ptr(kb), *_row_strides(kb), _ptr(vb), *_row_strides(vb),
+        _ptr(kvp), _ptr(kvi) if kvi.numel() else None, b, hq, hkv, lq, lv,
+        float(sm_scale), float(logit_cap), int(sliding_window), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_decode_attention: bad arguments")
+    return o, lse
+
+
+def merge_state(v_a, s_a, v_b, s_b):
+    """merge_state (sglang flashinfer_backend.py, forward_extend ragged +
+    paged split).  v_* [N, H, Dv] bf16, s_* [N, H] fp32 ->
+    (v [N, H, Dv] float64, s [N, H] float64)."""
+    lib = _load()
+    n, h, dv = v_a.shape
+    va, vb = _bf16_bits(v_a).contiguous(), _bf16_bits(v_b).contiguous()
+    sa = s_a.detach().cpu().to(torch.float32).contiguous()
+    sb = s_b.detach().cpu().to(torch.float32).contiguous()
+    v = torch.empty(n, h, dv, dtype=torch.float64)
+    s = torch.empty(n, h, dtype=torch.float64)
+    lib.oracle_merge_state(_ptr(va), _ptr(sa), _ptr(vb), _ptr(sb), n, h, dv,
+                           _ptr(v), _ptr(s))
+    return v, s
+
+
+def build_unified_kv_indices(prefix_kv_indptr, prefix_kv_indices,
+                             extend_start_loc, extend_seq_lens,
+                             extend_kv_indices, bs, fill=-1):
+    """Unified KV-index build (sglang extend_attention.py,
+    build_unified_kv_indices).  Returns (unified_kv_indptr int32 [bs+1],
+    unified_kv_indices int64 [len(prefix)+len(extend)], prefix_lens int32
+    [bs]); entries past unified_kv_indptr[bs] keep the value ``fill``."""
+    lib = _load()
+    pip, pix = _i32(prefix_kv_indptr), _i32(prefix_kv_indices)
+    esl, eln, eix = _i32(extend_start_loc), _i32(extend_seq_lens), _i32(extend_kv_indices)
+    uptr = torch.empty(bs + 1, dtype=torch.int32)
+    uidx = torch.full((pix.numel() + eix.numel(),), fill, dtype=torch.int64)
+    plen = torch.empty(bs, dtype=torch.int32)
+    lib.oracle_build_unified_kv_indices(
+        _ptr(pip), _ptr(pix) if pix.numel() else None, _ptr(esl), _ptr(eln),
+        _ptr(eix) if eix.numel() else None, int(bs), _ptr(uptr),
+        _ptr(uidx) if uidx.numel() else None, _ptr(plen))
+    return uptr, uidx, plen

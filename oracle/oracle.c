@@ -1,0 +1,372 @@
+/*
+ * oracle.c -- plain, slow, float64 CPU restatement of extend attention over a
+ * page-size-1 KV pool, decode attention, merge_state and the unified
+ * KV-index build.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file.  It exists so that tests, the smoke check and the CPU
+ * baseline leg of the benchmark have an obviously correct answer to compare
+ * the CUDA kernels against.  It shares no code, header, table or helper with
+ * the CUDA library.
+ *
+ * Sources (the web pages this method is taken from):
+ *   [EXT]  sglang extend_attention.py (diff 0.5.3rc2 -> 0.5.4.post1):
+ *          _fwd_kernel_unified, extend_attention_fwd_unified,
+ *          extend_attention_fwd, redundant_attention,
+ *          _copy_unified_indices_kernel, build_unified_kv_indices.
+ *   [FI]   sglang flashinfer_backend.py: forward_extend (ragged + paged +
+ *          merge_state split), forward_decode, the sliding-window index
+ *          updaters.
+ *   [CPU]  sglang cpu_graph_runner.py: the MLA K/V layout (V is the first
+ *          kv_lora_rank dims of K) in the qkv_proj_with_rope fake.
+ *
+ * Every floating-point step runs in double on the exact bf16 input values.
+ * Loops are in the order sequence -> head -> query -> key, with no tiling,
+ * no online softmax and no reordering beyond the definition:
+ *
+ *   s_j   = sm_scale * sum_d q[d] * k_j[d]                ([EXT] QK, scale)
+ *   s_j   = cap * tanh(s_j / cap)           if cap > 0     ([EXT] logit cap)
+ *   vis_j = (j <= qpos) && (W <= 0 || qpos - j <= W)       ([EXT] causal
+ *           mask on the extend part; sliding-window mask)
+ *   m     = max_{vis} s_j ;  l = sum_{vis} exp(s_j - m)
+ *   o     = sum_{vis} exp(s_j - m) v_j / l ;  lse = m + log(l)
+ *
+ * where a sequence's keys are its P prefix keys followed by its E extend keys,
+ * and extend query i sits at position qpos = P + i.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 bit pattern -> double (bf16 is the top half of an IEEE float). */
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Attention of one query row over one sequence's key list.
+ *   krow[j], vrow[j]: the j-th key / value row of the sequence (position j).
+ *   qpos: the query's position in the sequence.  window <= 0: no window.
+ *   s: scratch of n_keys doubles.
+ * Writes o[0..lv) and *lse.  A query that sees no key (cannot happen for a
+ * valid extend or decode query, which always sees itself) gets o = 0 and
+ * lse = -inf.
+ */
+static void attend_one_query(const uint16_t *q, int lq, int lv, long n_keys,
+                             const uint16_t *const *krow,
+                             const uint16_t *const *vrow, long qpos,
+                             long window, double sm_scale, double logit_cap,
+                             double *s, double *o, double *lse)
+{
+    double m = -INFINITY;
+    for (long j = 0; j < n_keys; ++j) {
+        int visible = (j <= qpos) && (window <= 0 || qpos - j <= window);
+        if (!visible) {
+            s[j] = -INFINITY;
+            continue;
+        }
+        double dot = 0.0;
+        for (int d = 0; d < lq; ++d)
+            dot += bf16_to_double(q[d]) * bf16_to_double(krow[j][d]);
+        double sj = sm_scale * dot;
+        if (logit_cap > 0.0)
+            sj = logit_cap * tanh(sj / logit_cap);
+        s[j] = sj;
+        if (sj > m)
+            m = sj;
+    }
+    for (int d = 0; d < lv; ++d)
+        o[d] = 0.0;
+    if (m == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double l = 0.0;
+    for (long j = 0; j < n_keys; ++j) {
+        if (s[j] == -INFINITY)
+            continue;
+        double p = exp(s[j] - m);
+        l += p;
+        for (int d = 0; d < lv; ++d)
+            o[d] += p * bf16_to_double(vrow[j][d]);
+    }
+    for (int d = 0; d < lv; ++d)
+        o[d] /= l;
+    *lse = m + log(l);
+}
+
+/* Index b of the sequence whose extend rows [qo_indptr[b], qo_indptr[b+1])
+ * contain token t, or -1. */
+static int sequence_of_token(const int32_t *qo_indptr, int batch, long t)
+{
+    for (int b = 0; b < batch; ++b)
+        if (t >= qo_indptr[b] && t < qo_indptr[b + 1])
+            return b;
+    return -1;
+}
+
+/*
+ * Extend attention, two-stage form ([EXT] extend_attention_fwd and its
+ * _fwd_kernel): prefix K/V come from the pool through
+ * kv_indices[kv_indptr[b] .. kv_indptr[b+1]), extend K/V are the contiguous
+ * rows k_extend/v_extend[qo_indptr[b] .. qo_indptr[b+1]).
+ *
+ * Layouts (element strides; the last dim is contiguous):
+ *   q_extend [n_tokens, hq, lq] contiguous
+ *   k_extend row (t, h) at k_ext + t*k_ext_ts + h*k_ext_hs  (lq elements)
+ *   v_extend row (t, h) at v_ext + t*v_ext_ts + h*v_ext_hs  (lv elements)
+ *   k_buffer row (slot, h) at k_buf + slot*k_buf_ss + h*k_buf_hs
+ *   v_buffer row (slot, h) at v_buf + slot*v_buf_ss + h*v_buf_hs
+ * rows: NULL -> every (token, head) and o_out is [n_tokens, hq, lv],
+ *       lse_out [n_tokens, hq];
+ *       else rows[r] = token*hq + head for r < n_rows, and o_out is
+ *       [n_rows, lv], lse_out [n_rows].
+ * Returns 0, or -1 on an argument error.
+ */
+int oracle_extend_attention(
+    const uint16_t *q_extend, const uint16_t *k_ext, long k_ext_ts,
+    long k_ext_hs, const uint16_t *v_ext, long v_ext_ts, long v_ext_hs,
+    const uint16_t *k_buf, long k_buf_ss, long k_buf_hs, const uint16_t *v_buf,
+    long v_buf_ss, long v_buf_hs, const int32_t *qo_indptr,
+    const int32_t *kv_indptr, const int32_t *kv_indices, int batch, int hq,
+    int hkv, int lq, int lv, double sm_scale, double logit_cap,
+    long sliding_window, const int64_t *rows, long n_rows, double *o_out,
+    double *lse_out)
+{
+    if (batch < 0 || hkv <= 0 || hq % hkv != 0)
+        return -1;
+    int group = hq / hkv; /* [EXT] kv_group_num: q heads per kv head */
+    long n_tokens = batch > 0 ? qo_indptr[batch] : 0;
+    long total = rows ? n_rows : n_tokens * hq;
+    int bad = 0;
+
+#pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
+    for (long r = 0; r < total; ++r) {
+        long row = rows ? rows[r] : r;
+        long t = row / hq;
+        int h = (int)(row % hq);
+        int b = sequence_of_token(qo_indptr, batch, t);
+        if (b < 0) {
+            bad = 1;
+            continue;
+        }
+        int hk = h / group;
+        long p_len = kv_indptr[b + 1] - kv_indptr[b];
+        long e_len = qo_indptr[b + 1] - qo_indptr[b];
+        long n_keys = p_len + e_len;
+        const uint16_t **krow = malloc(sizeof(*krow) * (size_t)(n_keys + 1));
+        const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)(n_keys + 1));
+        double *s = malloc(sizeof(double) * (size_t)(n_keys + 1));
+        /* Key j of sequence b: prefix keys through the page table, then the
+         * sequence's own extend tokens. */
+        for (long j = 0; j < p_len; ++j) {
+            long slot = kv_indices[kv_indptr[b] + j];
+            krow[j] = k_buf + slot * k_buf_ss + (long)hk * k_buf_hs;
+            vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;
+        }
+        for (long e = 0; e < e_len; ++e) {
+            long te = qo_indptr[b] + e;
+            krow[p_len + e] = k_ext + te * k_ext_ts + (long)hk * k_ext_hs;
+            vrow[p_len + e] = v_ext + te * v_ext_ts + (long)hk * v_ext_hs;
+        }
+        long i = t - qo_indptr[b];
+        attend_one_query(q_extend + (t * hq + h) * (long)lq, lq, lv, n_keys,
+                         krow, vrow, p_len + i, sliding_window, sm_scale,
+                         logit_cap, s, o_out + r * (long)lv, lse_out + r);
+        free(krow);
+        free(vrow);
+        free(s);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Extend attention, unified form ([EXT] extend_attention_fwd_unified and
+ * _fwd_kernel_unified): every key of sequence b, prefix and extend alike, is
+ * pool slot kv_indices[kv_indptr[b] + j]; the first prefix_lens[b] of them are
+ * the prefix.  Extend query i sits at position prefix_lens[b] + i.  The window
+ * start position is 0 for every sequence (the launcher's default).
+ * q [n_tokens, hq, lq] contiguous; rows / outputs as in
+ * oracle_extend_attention.
+ */
+int oracle_extend_attention_unified(
+    const uint16_t *q, const uint16_t *k_buf, long k_buf_ss, long k_buf_hs,
+    const uint16_t *v_buf, long v_buf_ss, long v_buf_hs,
+    const int32_t *qo_indptr, const int32_t *kv_indptr,
+    const int64_t *kv_indices, const int32_t *prefix_lens, int batch, int hq,
+    int hkv, int lq, int lv, double sm_scale, double logit_cap,
+    long sliding_window, const int64_t *rows, long n_rows, double *o_out,
+    double *lse_out)
+{
+    if (batch < 0 || hkv <= 0 || hq % hkv != 0)
+        return -1;
+    int group = hq / hkv;
+    long n_tokens = batch > 0 ? qo_indptr[batch] : 0;
+    long total = rows ? n_rows : n_tokens * hq;
+    int bad = 0;
+
+#pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
+    for (long r = 0; r < total; ++r) {
+        long row = rows ? rows[r] : r;
+        long t = row / hq;
+        int h = (int)(row % hq);
+        int b = sequence_of_token(qo_indptr, batch, t);
+        if (b < 0) {
+            bad = 1;
+            continue;
+        }
+        int hk = h / group;
+        long n_keys = kv_indptr[b + 1] - kv_indptr[b];
+        const uint16_t **krow = malloc(sizeof(*krow) * (size_t)(n_keys + 1));
+        const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)(n_keys + 1));
+        double *s = malloc(sizeof(double) * (size_t)(n_keys + 1));
+        for (long j = 0; j < n_keys; ++j) {
+            long slot = (long)kv_indices[kv_indptr[b] + j];
+            krow[j] = k_buf + slot * k_buf_ss + (long)hk * k_buf_hs;
+            vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;
+        }
+        long i = t - qo_indptr[b];
+        attend_one_query(q + (t * hq + h) * (long)lq, lq, lv, n_keys, krow,
+                         vrow, (long)prefix_lens[b] + i, sliding_window,
+                         sm_scale, logit_cap, s, o_out + r * (long)lv,
+                         lse_out + r);
+        free(krow);
+        free(vrow);
+        free(s);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Decode attention ([FI] forward_decode): one query per sequence; the
+ * sequence's K/V, the current token's included, are all in the pool at
+ * kv_indices[kv_indptr[b] .. kv_indptr[b+1]).  The query sits at the last
+ * position T_b - 1, so with a window W > 0 it sees the last W + 1 keys ([FI]
+ * sliding-window decode updater keeps min(seq_len, W + 1) keys).
+ * q [batch, hq, lq] contiguous; o_out [batch, hq, lv]; lse_out [batch, hq].
+ * A sequence with T_b = 0 gets o = 0, lse = -inf.
+ */
+int oracle_decode_attention(const uint16_t *q, const uint16_t *k_buf,
+                            long k_buf_ss, long k_buf_hs, const uint16_t *v_buf,
+                            long v_buf_ss, long v_buf_hs,
+                            const int32_t *kv_indptr, const int32_t *kv_indices,
+                            int batch, int hq, int hkv, int lq, int lv,
+                            double sm_scale, double logit_cap,
+                            long sliding_window, double *o_out,
+                            double *lse_out)
+{
+    if (batch < 0 || hkv <= 0 || hq % hkv != 0)
+        return -1;
+    int group = hq / hkv;
+    long total = (long)batch * hq;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long r = 0; r < total; ++r) {
+        int b = (int)(r / hq);
+        int h = (int)(r % hq);
+        int hk = h / group;
+        long n_keys = kv_indptr[b + 1] - kv_indptr[b];
+        const uint16_t **krow = malloc(sizeof(*krow) * (size_t)(n_keys + 1));
+        const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)(n_keys + 1));
+        double *s = malloc(sizeof(double) * (size_t)(n_keys + 1));
+        for (long j = 0; j < n_keys; ++j) {
+            long slot = kv_indices[kv_indptr[b] + j];
+            krow[j] = k_buf + slot * k_buf_ss + (long)hk * k_buf_hs;
+            vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;
+        }
+        attend_one_query(q + r * (long)lq, lq, lv, n_keys, krow, vrow,
+                         n_keys - 1, sliding_window, sm_scale, logit_cap, s,
+                         o_out + r * (long)lv, lse_out + r);
+        free(krow);
+        free(vrow);
+        free(s);
+    }
+    return 0;
+}
+
+/*
+ * merge_state ([FI] forward_extend, ragged + paged split): two partial
+ * attention states (v_a, s_a) and (v_b, s_b) of the same queries over
+ * disjoint key sets, with s the natural-log sum of exp of the scaled (and
+ * capped) logits, combine into the state over the union:
+ *   s = log(exp(s_a) + exp(s_b))
+ *   v = exp(s_a - s) * v_a + exp(s_b - s) * v_b
+ * A side with s = -inf holds no key and has weight 0; both -inf gives v = 0,
+ * s = -inf.
+ * v_* [n, h, dv] bf16; s_* [n, h] fp32; outputs double.
+ */
+void oracle_merge_state(const uint16_t *v_a, const float *s_a,
+                        const uint16_t *v_b, const float *s_b, long n, int h,
+                        int dv, double *v_out, double *s_out)
+{
+    long total = n * (long)h;
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < total; ++r) {
+        double sa = s_a[r], sb = s_b[r];
+        if (sa == -INFINITY && sb == -INFINITY) {
+            for (int d = 0; d < dv; ++d)
+                v_out[r * dv + d] = 0.0;
+            s_out[r] = -INFINITY;
+            continue;
+        }
+        double m = sa > sb ? sa : sb;
+        double s = m + log(exp(sa - m) + exp(sb - m));
+        double wa = exp(sa - s), wb = exp(sb - s);
+        for (int d = 0; d < dv; ++d)
+            v_out[r * dv + d] = wa * bf16_to_double(v_a[r * dv + d]) +
+                                wb * bf16_to_double(v_b[r * dv + d]);
+        s_out[r] = s;
+    }
+}
+
+/*
+ * Unified KV-index build ([EXT] build_unified_kv_indices and
+ * _copy_unified_indices_kernel):
+ *   prefix_lens[b]            = prefix_kv_indptr[b+1] - prefix_kv_indptr[b]
+ *   unified_kv_indptr[0]      = 0
+ *   unified_kv_indptr[b+1]    = unified_kv_indptr[b] + prefix_lens[b]
+ *                               + extend_seq_lens[b]
+ *   unified_kv_indices[unified_kv_indptr[b] + j]
+ *       = prefix_kv_indices[prefix_kv_indptr[b] + j]           j < P_b
+ *       = extend_kv_indices[extend_start_loc[b] + j - P_b]     P_b <= j < T_b
+ * Entries of unified_kv_indices past unified_kv_indptr[bs] are not written.
+ */
+void oracle_build_unified_kv_indices(
+    const int32_t *prefix_kv_indptr, const int32_t *prefix_kv_indices,
+    const int32_t *extend_start_loc, const int32_t *extend_seq_lens,
+    const int32_t *extend_kv_indices, int bs, int32_t *unified_kv_indptr,
+    int64_t *unified_kv_indices, int32_t *prefix_lens)
+{
+    unified_kv_indptr[0] = 0;
+    for (int b = 0; b < bs; ++b) {
+        prefix_lens[b] = prefix_kv_indptr[b + 1] - prefix_kv_indptr[b];
+        unified_kv_indptr[b + 1] =
+            unified_kv_indptr[b] + prefix_lens[b] + extend_seq_lens[b];
+    }
+    for (int b = 0; b < bs; ++b) {
+        long dst = unified_kv_indptr[b];
+        for (long j = 0; j < prefix_lens[b]; ++j)
+            unified_kv_indices[dst + j] =
+                prefix_kv_indices[prefix_kv_indptr[b] + j];
+        for (long e = 0; e < extend_seq_lens[b]; ++e)
+            unified_kv_indices[dst + prefix_lens[b] + e] =
+                extend_kv_indices[extend_start_loc[b] + e];
+    }
+}

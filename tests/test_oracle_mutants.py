@@ -1,0 +1,97 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch every one of them.
+
+Each mutant is oracle.c with one textual change (an off-by-one in a mask, a
+dropped scale, a wrong head mapping, a reversed index, a wrong merge weight),
+compiled with gcc into a temporary library.  The pins of
+``test_oracle_pins.py`` are run against it; at least one must fail.  Nothing
+here touches a GPU.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text in oracle.c, replacement, occurrence index or None for all)
+MUTANTS = [
+    ("causal_off_by_one", "(j <= qpos)", "(j < qpos)", None),
+    ("causal_dropped", "(j <= qpos) && ", "", None),
+    ("window_off_by_one", "qpos - j <= window", "qpos - j < window", None),
+    ("window_sign", "qpos - j <= window", "j - qpos <= window", None),
+    ("scale_dropped", "double sj = sm_scale * dot;", "double sj = dot;", None),
+    ("cap_inside_out", "logit_cap * tanh(sj / logit_cap)", "tanh(sj * logit_cap) / logit_cap", None),
+    ("cap_before_scale", "double sj = sm_scale * dot;\n        if (logit_cap > 0.0)\n            sj = logit_cap * tanh(sj / logit_cap);",
+     "double sj = dot;\n        if (logit_cap > 0.0)\n            sj = logit_cap * tanh(sj / logit_cap);\n        sj *= sm_scale;", None),
+    ("lse_drops_max", "*lse = m + log(l);", "*lse = log(l);", None),
+    ("no_normalise", "o[d] /= l;", "o[d] /= 1.0;", None),
+    ("v_is_k", "bf16_to_double(vrow[j][d])", "bf16_to_double(krow[j][d])", None),
+    ("gqa_modulo", "int hk = h / group;", "int hk = h % hkv;", None),
+    ("extend_qpos_no_prefix", "p_len + i, sliding_window", "i, sliding_window", None),
+    ("unified_qpos_no_prefix", "(long)prefix_lens[b] + i", "(long)i", None),
+    ("extend_rows_reversed", "long te = qo_indptr[b] + e;", "long te = qo_indptr[b] + (e_len - 1 - e);", None),
+    ("prefix_reversed", "long slot = kv_indices[kv_indptr[b] + j];\n            krow[j] = k_buf + slot * k_buf_ss + (long)hk * k_buf_hs;\n            vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;\n        }\n        for (long e = 0",
+     "long slot = kv_indices[kv_indptr[b] + (p_len - 1 - j)];\n            krow[j] = k_buf + slot * k_buf_ss + (long)hk * k_buf_hs;\n            vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;\n        }\n        for (long e = 0", None),
+    ("decode_qpos", "n_keys - 1, sliding_window", "n_keys - 2, sliding_window", None),
+    ("merge_weight_uses_max", "double wa = exp(sa - s), wb = exp(sb - s);", "double wa = exp(sa - m), wb = exp(sb - m);", None),
+    ("merge_lse_drops_max", "double s = m + log(exp(sa - m) + exp(sb - m));", "double s = log(exp(sa - m) + exp(sb - m));", None),
+    ("merge_swapped", "wa * bf16_to_double(v_a[r * dv + d]) +\n                                wb * bf16_to_double(v_b[r * dv + d]);",
+     "wb * bf16_to_double(v_a[r * dv + d]) +\n                                wa * bf16_to_double(v_b[r * dv + d]);", None),
+    ("unified_extend_start_ignored", "extend_kv_indices[extend_start_loc[b] + e]", "extend_kv_indices[unified_kv_indptr[b] - prefix_kv_indptr[b] + e]", None),
+    ("unified_indptr_drops_extend", "+ prefix_lens[b] + extend_seq_lens[b];", "+ prefix_lens[b];\n        unified_kv_indptr[b + 1] += extend_seq_lens[b] * (b > 0);", None),
+]
+
+# The pins, cheapest first; a mutant is caught by the first one that fails.
+BATTERY = [
+    lambda: pins.test_unified_indices_hand_fixture(),
+    lambda: pins.test_merge_closed_forms(),
+    lambda: pins.test_merge_weights_are_softmax_of_lse(),
+    lambda: pins.test_no_prefix_is_torch_causal_sdpa(64, 64, 4, 2),
+    lambda: pins.test_no_prefix_window_is_sdpa_band_mask(),
+    lambda: pins.test_matches_dense_library_formulation(2.5, 40, 4),
+    lambda: pins.test_matches_dense_library_formulation(0.0, 9, 3),
+    lambda: pins.test_gqa_head_mapping(),
+    lambda: pins.test_cap_two_key_closed_form(),
+    lambda: pins.test_one_and_two_visible_keys_closed_forms(),
+    lambda: pins.test_decode_equals_extend_of_last_token(),
+    lambda: pins.test_decode_window_keeps_last_w_plus_one_keys(),
+    lambda: pins.test_two_stage_equals_unified(),
+    lambda: pins.test_unified_indices_are_per_sequence_concatenation(0),
+    lambda: pins.test_merge_of_two_key_halves_equals_attention_over_all(),
+]
+
+
+def _build_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert old in src, f"mutation {name}: pattern not found in oracle.c"
+    mutated = src.replace(old, new)
+    c = tmp_path / f"{name}.c"
+    so = tmp_path / f"{name}.so"
+    c.write_text(mutated)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-w",
+                    "-o", str(so), str(c), "-lm"], check=True)
+    return str(so)
+
+
+def test_unmutated_copy_passes_battery(tmp_path):
+    """Control: the battery passes on an unmodified rebuild."""
+    so = _build_mutant(tmp_path, "control", "#include <math.h>", "#include <math.h>")
+    with oracle.use_library(so):
+        for check in BATTERY:
+            check()
+
+
+@pytest.mark.parametrize("name,old,new,_", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new, _):
+    so = _build_mutant(tmp_path, name, old, new)
+    with oracle.use_library(so):
+        for check in BATTERY:
+            try:
+                check()
+            except Exception:
+                return  # caught
+    pytest.fail(f"no pin caught the planted mistake {name!r}")

@@ -1,0 +1,479 @@
+"""Pins of the float64 oracle against things other than itself.
+
+Each test checks one oracle function against a library routine, a closed
+form, an invariant the pages fix, or a hand-derived fixture, so that a
+plausible slip in the oracle (a dropped term, an off-by-one in a mask, a wrong
+sign, a transposed operand, a wrong head mapping) fails at least one of them.
+``tests/test_oracle_mutants.py`` plants such slips and checks exactly that.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from paged_kv_extend_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+TOL = 1e-10
+
+
+def _spec(**kw):
+    return W.small_spec(**kw)
+
+
+def _run_oracle(wl, cap=None, window=None, rows=None):
+    k_ext, v_ext = wl.extend_kv()
+    kb, vb = wl.pool()
+    s = wl.spec
+    return oracle.extend_attention(
+        wl.q, k_ext, v_ext, kb, vb, wl.qo_indptr, wl.kv_indptr, wl.kv_indices,
+        wl.sm_scale, s.logit_cap if cap is None else cap,
+        s.sliding_window if window is None else window, rows=rows)
+
+
+def _dense_reference(wl, cap, window):
+    """Second formulation with library primitives: per sequence, the full
+    [E, T] score matrix by matmul, tanh cap, a boolean mask from explicit
+    position tables, softmax and matmul.  Returns (o, lse) float64."""
+    s = wl.spec
+    g = s.hq // s.hkv
+    outs, lses = [], []
+    for b in range(wl.batch):
+        t0 = int(wl.token_offsets[b])
+        T = wl.prefix_lens[b] + wl.extend_lens[b]
+        E = wl.extend_lens[b]
+        if E == 0:
+            continue
+        k = wl.k_rows[t0:t0 + T].double().repeat_interleave(g, dim=1)  # [T,Hq,Lq]
+        v = wl.v_rows[t0:t0 + T].double().repeat_interleave(g, dim=1)
+        q0 = int(wl.qo_indptr[b])
+        q = wl.q[q0:q0 + E].double()                                     # [E,Hq,Lq]
+        sc = torch.einsum("ehd,thd->het", q, k) * wl.sm_scale
+        if cap > 0:
+            sc = cap * torch.tanh(sc / cap)
+        qpos = torch.arange(E).view(E, 1) + wl.prefix_lens[b]
+        kpos = torch.arange(T).view(1, T)
+        vis = kpos <= qpos
+        if window > 0:
+            vis = vis & (qpos - kpos <= window)
+        sc = sc.masked_fill(~vis.unsqueeze(0), float("-inf"))
+        lse = torch.logsumexp(sc, dim=-1)                                # [Hq,E]
+        o = torch.einsum("het,thd->ehd", torch.softmax(sc, dim=-1), v)
+        outs.append(o)
+        lses.append(lse.transpose(0, 1))
+    return torch.cat(outs), torch.cat(lses)
+
+
+# ------------------------------------------------------------ prefix = 0 case
+@pytest.mark.parametrize("lq,lv,hq,hkv", [(64, 64, 4, 2), (128, 128, 8, 2), (96, 80, 6, 3)])
+def test_no_prefix_is_torch_causal_sdpa(lq, lv, hq, hkv):
+    """With no cached prefix, extend attention is plain causal attention
+    (flashinfer_backend.py, forward_extend: the ragged result alone when no
+    sequence has a prefix).  Library pin: torch SDPA, is_causal, float64."""
+    wl = W.draw(_spec(batch=3, hq=hq, hkv=hkv, lq=lq, lv=lv, prefix=[0, 0, 0],
+                      extend=[1, 7, 33], seed=11))
+    o, _ = _run_oracle(wl, cap=0.0, window=-1)
+    g = hq // hkv
+    for b in range(wl.batch):
+        a, e = int(wl.qo_indptr[b]), int(wl.qo_indptr[b + 1])
+        q = wl.q[a:e].double().transpose(0, 1)[None]
+        k = wl.k_rows[a:e].double().repeat_interleave(g, 1).transpose(0, 1)[None]
+        v = wl.v_rows[a:e].double().repeat_interleave(g, 1).transpose(0, 1)[None]
+        ref = F.scaled_dot_product_attention(q, k, v, is_causal=True, scale=wl.sm_scale)
+        torch.testing.assert_close(o[a:e], ref[0].transpose(0, 1), rtol=0, atol=TOL)
+
+
+def test_no_prefix_window_is_sdpa_band_mask():
+    """Sliding window with no prefix: query i sees keys i-W .. i
+    (extend_attention.py, _fwd_kernel_unified, sliding-window mask).  Library
+    pin: SDPA with a band mask built by tril/triu."""
+    W_ = 5
+    wl = W.draw(_spec(batch=1, hq=2, hkv=1, lq=64, lv=64, prefix=[0], extend=[23], seed=3))
+    o, _ = _run_oracle(wl, cap=0.0, window=W_)
+    E = wl.extend_lens[0]
+    band = torch.ones(E, E, dtype=torch.bool).tril().triu(-W_)
+    q = wl.q.double().transpose(0, 1)[None]
+    k = wl.k_rows.double().repeat_interleave(2, 1).transpose(0, 1)[None]
+    v = wl.v_rows.double().repeat_interleave(2, 1).transpose(0, 1)[None]
+    ref = F.scaled_dot_product_attention(q, k, v, attn_mask=band, scale=wl.sm_scale)
+    torch.testing.assert_close(o, ref[0].transpose(0, 1), rtol=0, atol=TOL)
+
+
+# ------------------------------------------------------- dense brute force
+@pytest.mark.parametrize("cap,window,seed", [(0.0, -1, 1), (30.0, -1, 2), (0.0, 9, 3),
+                                             (2.5, 40, 4), (0.5, 1, 5)])
+def test_matches_dense_library_formulation(cap, window, seed):
+    """Brute force on small ragged batches with prefix, GQA, cap and window:
+    the oracle's per-key loops equal a dense matmul/tanh/mask/softmax
+    formulation built from torch library routines."""
+    wl = W.draw(_spec(batch=4, hq=6, hkv=2, lq=64, lv=32, prefix=[0, 13, 70, 4],
+                      extend=[9, 1, 20, 0], seed=seed, std=2.0))
+    o, lse = _run_oracle(wl, cap=cap, window=window)
+    ro, rl = _dense_reference(wl, cap, window)
+    torch.testing.assert_close(o, ro, rtol=0, atol=TOL)
+    torch.testing.assert_close(lse, rl, rtol=0, atol=TOL)
+
+
+def test_mla_shape_matches_dense_formulation():
+    """MLA layout (Lq=576 = 512 latent + 64 rope, Lv=512, V = first 512 dims
+    of K, one KV head): the score is the full 576-dim dot product."""
+    wl = W.draw(_spec(batch=2, hq=4, hkv=1, lq=576, lv=512, prefix=[6, 0],
+                      extend=[3, 4], seed=21, std=0.5, v_aliases_k=True,
+                      sm_scale=1 / math.sqrt(192)))
+    o, lse = _run_oracle(wl)
+    ro, rl = _dense_reference(wl, 0.0, -1)
+    torch.testing.assert_close(o, ro, rtol=0, atol=TOL)
+    torch.testing.assert_close(lse, rl, rtol=0, atol=TOL)
+
+
+# ------------------------------------------------------ split invariance
+@pytest.mark.parametrize("cap,window", [(0.0, -1), (30.0, -1), (0.0, 6)])
+def test_any_prefix_split_equals_full_causal(cap, window):
+    """redundant_attention (extend_attention.py): laying prefix and extend
+    out contiguously and running full causal attention gives the extend rows.
+    So for one sequence of T tokens, every cut c (prefix c, extend T-c) must
+    give rows c..T-1 of the cut-0 result."""
+    T = 29
+    base = W.draw(_spec(batch=1, hq=4, hkv=2, lq=64, lv=64, prefix=[0], extend=[T], seed=8))
+    # Whole sequence as extend (cut 0): reference rows.
+    full_o, full_lse = _run_oracle(base, cap=cap, window=window)
+    kb, vb = base.pool()
+    slots = base.slots
+    for c in [1, 5, 17, 28]:
+        q = base.q[c:]
+        k_ext, v_ext = base.k_rows[c:], base.v_rows[c:]
+        qo = torch.tensor([0, T - c], dtype=torch.int32)
+        kvp = torch.tensor([0, c], dtype=torch.int32)
+        o, lse = oracle.extend_attention(q, k_ext, v_ext, kb, vb, qo, kvp, slots[:c],
+                                         base.sm_scale, cap, window)
+        torch.testing.assert_close(o, full_o[c:], rtol=0, atol=TOL)
+        torch.testing.assert_close(lse, full_lse[c:], rtol=0, atol=TOL)
+
+
+# ------------------------------------------------------------ closed forms
+def test_zero_query_gives_mean_of_visible_values():
+    """q = 0 makes every visible score 0: o is the plain mean of the visible
+    values and lse = log(#visible).  Checked with and without a window."""
+    wl = W.draw(_spec(batch=2, hq=2, hkv=1, lq=64, lv=64, prefix=[10, 0], extend=[4, 6], seed=4))
+    wl.q.zero_()
+    for window in (-1, 3):
+        o, lse = _run_oracle(wl, cap=0.0, window=window)
+        r = 0
+        for b in range(wl.batch):
+            t0, P = int(wl.token_offsets[b]), wl.prefix_lens[b]
+            for i in range(wl.extend_lens[b]):
+                qpos = P + i
+                lo = 0 if window <= 0 else max(0, qpos - window)
+                vis = wl.v_rows[t0 + lo: t0 + qpos + 1, 0].double()
+                for h in range(2):
+                    torch.testing.assert_close(o[r, h], vis.mean(0), rtol=0, atol=TOL)
+                    assert abs(lse[r, h].item() - math.log(vis.shape[0])) < TOL
+                r += 1
+
+
+def test_constant_values_give_that_constant():
+    """Softmax weights sum to one: if every V row is the same vector c, o = c
+    whatever the scores."""
+    wl = W.draw(_spec(batch=2, hq=4, hkv=2, lq=64, lv=64, prefix=[7, 3], extend=[5, 2], seed=6))
+    c = torch.randn(64, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    wl.v_rows[:] = c
+    o, _ = _run_oracle(wl, cap=30.0, window=4)
+    torch.testing.assert_close(o, c.double().expand_as(o), rtol=0, atol=1e-12)
+
+
+def test_one_and_two_visible_keys_closed_forms():
+    """A query that sees a single key returns that key's V row, with lse its
+    own score; with W = 1 a query sees exactly itself and the key before it,
+    and the output is the sigmoid blend of the two V rows."""
+    # One key visible: decode over a single-token sequence.
+    wl = W.draw(_spec(batch=1, hq=2, hkv=1, lq=64, lv=64, prefix=[0], extend=[1], seed=9))
+    kb, vb = wl.pool()
+    o, lse = oracle.decode_attention(wl.q, kb, vb, torch.tensor([0, 1], dtype=torch.int32),
+                                     wl.slots, wl.sm_scale)
+    for h in range(2):
+        torch.testing.assert_close(o[0, h], wl.v_rows[0, 0].double(), rtol=0, atol=TOL)
+        s = wl.sm_scale * (wl.q[0, h].double() @ wl.k_rows[0, 0].double())
+        assert abs(lse[0, h].item() - s.item()) < TOL
+    # W = 1: two keys visible (self and the one before).  Hand-worked:
+    # weights sigma(s_prev - s_self), sigma(s_self - s_prev).
+    wl = W.draw(_spec(batch=1, hq=1, hkv=1, lq=64, lv=64, prefix=[4], extend=[3], seed=10))
+    o, lse = _run_oracle(wl, cap=0.0, window=1)
+    for i in range(3):
+        qpos = 4 + i
+        qv = wl.q[i, 0].double()
+        s_self = wl.sm_scale * (qv @ wl.k_rows[qpos, 0].double()).item()
+        s_prev = wl.sm_scale * (qv @ wl.k_rows[qpos - 1, 0].double()).item()
+        w_prev = 1.0 / (1.0 + math.exp(s_self - s_prev))
+        ref = w_prev * wl.v_rows[qpos - 1, 0].double() + (1 - w_prev) * wl.v_rows[qpos, 0].double()
+        torch.testing.assert_close(o[i, 0], ref, rtol=0, atol=TOL)
+        m = max(s_self, s_prev)
+        assert abs(lse[i, 0].item() - (m + math.log(math.exp(s_self - m) + math.exp(s_prev - m)))) < TOL
+
+
+def test_large_window_and_large_cap_change_nothing():
+    """W >= T keeps every causal key; cap -> infinity makes cap*tanh(s/cap)
+    -> s.  Both must reproduce the plain result."""
+    wl = W.draw(_spec(batch=2, hq=4, hkv=2, lq=64, lv=64, prefix=[12, 30], extend=[9, 4], seed=12))
+    o0, l0 = _run_oracle(wl, cap=0.0, window=-1)
+    o1, l1 = _run_oracle(wl, cap=0.0, window=1000)
+    torch.testing.assert_close(o1, o0, rtol=0, atol=TOL)
+    torch.testing.assert_close(l1, l0, rtol=0, atol=TOL)
+    o2, l2 = _run_oracle(wl, cap=1e9, window=-1)
+    torch.testing.assert_close(o2, o0, rtol=0, atol=1e-9)
+    torch.testing.assert_close(l2, l0, rtol=0, atol=1e-9)
+
+
+def test_tiny_cap_flattens_scores():
+    """cap -> 0 squeezes every score into (-cap, cap): the weights become
+    uniform, o -> mean of visible V, lse -> log(#visible)."""
+    wl = W.draw(_spec(batch=1, hq=2, hkv=1, lq=64, lv=64, prefix=[6], extend=[5], seed=13, std=3.0))
+    cap = 1e-9
+    o, lse = _run_oracle(wl, cap=cap, window=-1)
+    for i in range(5):
+        vis = wl.v_rows[: 6 + i + 1, 0].double()
+        for h in range(2):
+            torch.testing.assert_close(o[i, h], vis.mean(0), rtol=0, atol=1e-8)
+            assert abs(lse[i, h].item() - math.log(vis.shape[0])) < 1e-8
+
+
+def test_cap_two_key_closed_form():
+    """With two visible keys the output is a sigmoid blend of their values;
+    with the cap, the blend weight uses cap*tanh(score/cap)."""
+    wl = W.draw(_spec(batch=1, hq=1, hkv=1, lq=64, lv=64, prefix=[1], extend=[1], seed=14, std=2.0))
+    cap = 1.5
+    o, _ = _run_oracle(wl, cap=cap, window=-1)
+    qv = wl.q[0, 0].double()
+    s = [cap * math.tanh(wl.sm_scale * (qv @ wl.k_rows[j, 0].double()).item() / cap) for j in (0, 1)]
+    w0 = 1.0 / (1.0 + math.exp(s[1] - s[0]))
+    ref = w0 * wl.v_rows[0, 0].double() + (1 - w0) * wl.v_rows[1, 0].double()
+    torch.testing.assert_close(o[0, 0], ref, rtol=0, atol=TOL)
+
+
+def test_gqa_head_mapping():
+    """q head h reads kv head h // (Hq/Hkv) (kv_group_num): zeroing every V
+    row of kv head 1 must zero exactly q heads 2 and 3 when Hq=4, Hkv=2."""
+    wl = W.draw(_spec(batch=1, hq=4, hkv=2, lq=64, lv=64, prefix=[5], extend=[4], seed=15))
+    wl.v_rows[:, 1] = 0
+    o, _ = _run_oracle(wl)
+    assert torch.all(o[:, 2:] == 0)
+    assert torch.all(o[:, :2].abs().sum(-1) > 0)
+
+
+def test_sample_rows_equal_full_rows():
+    """Row-sampled mode returns exactly the rows of the full run."""
+    wl = W.draw(_spec(batch=3, hq=4, hkv=2, lq=64, lv=64, prefix=[3, 0, 9], extend=[2, 5, 3], seed=16))
+    o, lse = _run_oracle(wl, cap=5.0, window=4)
+    rows = [0, 5, 17, 39, 22]
+    so, sl = _run_oracle(wl, cap=5.0, window=4, rows=rows)
+    hq = 4
+    for r, row in enumerate(rows):
+        assert torch.equal(so[r], o[row // hq, row % hq])
+        assert sl[r] == lse[row // hq, row % hq]
+
+
+# --------------------------------------------------------------------- decode
+def test_decode_equals_extend_of_last_token():
+    """Decode (flashinfer_backend.py, forward_decode: the token's K/V are
+    saved first, then one query attends to all T keys) equals extend with
+    prefix T-1 and the last token as the one extend token."""
+    wl = W.draw(W.WorkloadSpec("dec", batch=3, hq=8, hkv=2, lq=128, lv=128,
+                               prefix=[0, 6, 40], extend=[1, 1, 1], num_slots=128,
+                               seed=17, decode=True))
+    kb, vb = wl.pool()
+    o, lse = oracle.decode_attention(wl.q, kb, vb, wl.kv_indptr, wl.kv_indices, wl.sm_scale,
+                                     logit_cap=4.0, sliding_window=5)
+    for b in range(3):
+        T = wl.prefix_lens[b] + 1
+        t0 = int(wl.token_offsets[b])
+        slots = wl.slots[t0:t0 + T]
+        eo, el = oracle.extend_attention(
+            wl.q[b:b + 1], wl.k_rows[t0 + T - 1:t0 + T], wl.v_rows[t0 + T - 1:t0 + T], kb, vb,
+            torch.tensor([0, 1], dtype=torch.int32), torch.tensor([0, T - 1], dtype=torch.int32),
+            slots[:T - 1], wl.sm_scale, 4.0, 5)
+        torch.testing.assert_close(o[b], eo[0], rtol=0, atol=TOL)
+        torch.testing.assert_close(lse[b], el[0], rtol=0, atol=TOL)
+
+
+def test_decode_window_keeps_last_w_plus_one_keys():
+    """Sliding-window decode keeps min(T, W+1) keys (flashinfer_backend.py,
+    sliding-window decode index updater): equal to plain decode over only
+    the last W+1 slots."""
+    wl = W.draw(W.WorkloadSpec("dec", batch=2, hq=4, hkv=1, lq=64, lv=64,
+                               prefix=[20, 3], extend=[1, 1], num_slots=64, seed=18, decode=True))
+    kb, vb = wl.pool()
+    Wn = 6
+    o, lse = oracle.decode_attention(wl.q, kb, vb, wl.kv_indptr, wl.kv_indices, wl.sm_scale,
+                                     sliding_window=Wn)
+    sub_idx, sub_ptr = [], [0]
+    for b in range(2):
+        a, e = int(wl.kv_indptr[b]), int(wl.kv_indptr[b + 1])
+        keep = wl.kv_indices[max(a, e - (Wn + 1)):e]
+        sub_idx.append(keep)
+        sub_ptr.append(sub_ptr[-1] + keep.numel())
+    o2, l2 = oracle.decode_attention(wl.q, kb, vb, torch.tensor(sub_ptr, dtype=torch.int32),
+                                     torch.cat(sub_idx), wl.sm_scale)
+    torch.testing.assert_close(o, o2, rtol=0, atol=TOL)
+    torch.testing.assert_close(lse, l2, rtol=0, atol=TOL)
+
+
+def test_empty_sequences_are_harmless():
+    """Padding sequences (length 0, as the CUDA-graph runner pads with
+    seq_len 0) produce no rows and do not disturb their neighbours."""
+    a = W.draw(_spec(batch=3, hq=4, hkv=2, lq=64, lv=64, prefix=[4, 0, 6], extend=[3, 0, 2], seed=19))
+    o, lse = _run_oracle(a)
+    assert o.shape[0] == 5
+    ro, rl = _dense_reference(a, 0.0, -1)
+    torch.testing.assert_close(o, ro, rtol=0, atol=TOL)
+    kb, vb = a.pool()
+    od, ld = oracle.decode_attention(a.q[:2], kb, vb, torch.tensor([0, 0, 0], dtype=torch.int32),
+                                     torch.zeros(0, dtype=torch.int32), a.sm_scale)
+    assert torch.all(od == 0) and torch.all(torch.isneginf(ld))
+
+
+# ---------------------------------------------------------------- merge_state
+def test_merge_of_two_key_halves_equals_attention_over_all():
+    """merge_state of attention over key set A and over key set B equals
+    attention over A u B (flashinfer_backend.py, forward_extend: ragged
+    extend result merged with the non-causal paged prefix result).  The
+    partial outputs are rounded to bf16 before merging, so the bound is the
+    largest rounding error of the merged inputs (a convex combination cannot
+    amplify it) plus fp32 rounding of the lse inputs."""
+    wl = W.draw(W.WorkloadSpec("dec", batch=4, hq=8, hkv=2, lq=128, lv=128,
+                               prefix=[9, 30, 1, 63], extend=[1, 1, 1, 1], num_slots=256,
+                               seed=20, decode=True))
+    kb, vb = wl.pool()
+    full_o, full_l = oracle.decode_attention(wl.q, kb, vb, wl.kv_indptr, wl.kv_indices, wl.sm_scale)
+    ia, ib, pa, pb = [], [], [0], [0]
+    for b in range(4):
+        a, e = int(wl.kv_indptr[b]), int(wl.kv_indptr[b + 1])
+        cut = a + (e - a) // 3
+        ia.append(wl.kv_indices[a:cut]); ib.append(wl.kv_indices[cut:e])
+        pa.append(pa[-1] + cut - a); pb.append(pb[-1] + e - cut)
+    oa, la = oracle.decode_attention(wl.q, kb, vb, torch.tensor(pa, dtype=torch.int32),
+                                     torch.cat(ia), wl.sm_scale)
+    ob, lb = oracle.decode_attention(wl.q, kb, vb, torch.tensor(pb, dtype=torch.int32),
+                                     torch.cat(ib), wl.sm_scale)
+    va, vb_ = oa.to(torch.bfloat16), ob.to(torch.bfloat16)
+    v, s = oracle.merge_state(va, la.float(), vb_, lb.float())
+    bound = max((va.double() - oa).abs().max().item(), (vb_.double() - ob).abs().max().item())
+    assert (v - full_o).abs().max().item() <= bound + 1e-6
+    torch.testing.assert_close(s, full_l, rtol=0, atol=1e-5)
+
+
+def test_merge_closed_forms():
+    """An empty side (lse = -inf) has weight 0; equal lse halves average
+    and add log 2; both empty gives 0 and -inf."""
+    g = torch.Generator().manual_seed(2)
+    va = torch.randn(3, 2, 16, generator=g).to(torch.bfloat16)
+    vb = torch.randn(3, 2, 16, generator=g).to(torch.bfloat16)
+    sa = torch.tensor([[float("-inf"), 1.0], [0.5, float("-inf")], [float("-inf"), -2.0]])
+    sb = torch.tensor([[0.25, 1.0], [float("-inf"), float("-inf")], [3.0, -2.0]])
+    v, s = oracle.merge_state(va, sa, vb, sb)
+    torch.testing.assert_close(v[0, 0], vb[0, 0].double(), rtol=0, atol=0)
+    assert s[0, 0] == 0.25
+    torch.testing.assert_close(v[0, 1], (va[0, 1].double() + vb[0, 1].double()) / 2, rtol=0, atol=1e-15)
+    assert abs(s[0, 1].item() - (1.0 + math.log(2))) < 1e-15
+    torch.testing.assert_close(v[1, 0], va[1, 0].double(), rtol=0, atol=0)
+    assert torch.all(v[1, 1] == 0) and torch.isneginf(s[1, 1])
+    torch.testing.assert_close(v[2, 0], vb[2, 0].double(), rtol=0, atol=0)
+
+
+def test_merge_weights_are_softmax_of_lse():
+    """Library pin: the merged value equals softmax([s_a, s_b]) . [v_a, v_b]
+    and the merged lse equals torch.logsumexp([s_a, s_b])."""
+    g = torch.Generator().manual_seed(3)
+    va = torch.randn(50, 4, 32, generator=g).to(torch.bfloat16)
+    vb = torch.randn(50, 4, 32, generator=g).to(torch.bfloat16)
+    sa = torch.randn(50, 4, generator=g) * 10
+    sb = torch.randn(50, 4, generator=g) * 10
+    v, s = oracle.merge_state(va, sa, vb, sb)
+    st = torch.stack([sa.double(), sb.double()], -1)
+    w = torch.softmax(st, -1)
+    ref = w[..., :1] * va.double() + w[..., 1:] * vb.double()
+    torch.testing.assert_close(v, ref, rtol=0, atol=1e-12)
+    torch.testing.assert_close(s, torch.logsumexp(st, -1), rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------ unified indices
+def test_unified_indices_hand_fixture():
+    """Hand-derived worked example (tests/golden/unified_indices_hand.json)."""
+    with open(os.path.join(GOLDEN, "unified_indices_hand.json")) as f:
+        fx = json.load(f)
+    i, e = fx["inputs"], fx["expected"]
+    t = lambda k: torch.tensor(i[k], dtype=torch.int32)
+    uptr, uidx, plen = oracle.build_unified_kv_indices(
+        t("prefix_kv_indptr"), t("prefix_kv_indices"), t("extend_start_loc"),
+        t("extend_seq_lens"), t("extend_kv_indices"), i["bs"], fill=-7)
+    assert uptr.tolist() == e["unified_kv_indptr"]
+    n = e["unified_kv_indptr"][-1]
+    assert uidx[:n].tolist() == e["unified_kv_indices_prefix"]
+    assert torch.all(uidx[n:] == -7)
+    assert plen.tolist() == e["prefix_lens"]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_unified_indices_are_per_sequence_concatenation(seed):
+    """Random ragged batches with arbitrary extend_start_loc: the unified
+    list equals numpy concatenation of each sequence's prefix slice and
+    extend slice, the indptr equals numpy cumsum, bit for bit."""
+    rng = np.random.default_rng(seed)
+    bs = int(rng.integers(1, 40))
+    plens = rng.integers(0, 300, bs)
+    plens[rng.random(bs) < 0.2] = 0
+    elens = rng.integers(0, 200, bs)
+    pptr = np.concatenate([[0], np.cumsum(plens)]).astype(np.int32)
+    pidx = rng.integers(0, 2**31 - 1, int(plens.sum())).astype(np.int32)
+    # extend buffer in a shuffled order with gaps
+    order = rng.permutation(bs)
+    starts = np.zeros(bs, np.int64)
+    pos = 0
+    for b in order:
+        pos += int(rng.integers(0, 4))
+        starts[b] = pos
+        pos += int(elens[b])
+    eidx = rng.integers(0, 2**31 - 1, pos + 3).astype(np.int32)
+    uptr, uidx, plen = oracle.build_unified_kv_indices(
+        torch.from_numpy(pptr), torch.from_numpy(pidx), torch.from_numpy(starts.astype(np.int32)),
+        torch.from_numpy(elens.astype(np.int32)), torch.from_numpy(eidx), bs, fill=-1)
+    ref = np.concatenate([np.concatenate([pidx[pptr[b]:pptr[b + 1]],
+                                          eidx[starts[b]:starts[b] + elens[b]]])
+                          for b in range(bs)]).astype(np.int64)
+    n = int(plens.sum() + elens.sum())
+    assert np.array_equal(uidx[:n].numpy(), ref)
+    assert torch.all(uidx[n:] == -1)
+    assert np.array_equal(uptr.numpy(), np.concatenate([[0], np.cumsum(plens + elens)]))
+    assert np.array_equal(plen.numpy(), plens)
+
+
+def test_two_stage_equals_unified():
+    """The two-stage form (prefix through indices, extend contiguous) and the
+    unified form (everything through unified indices) compute the same
+    thing on the same data (extend_attention.py: extend_attention_fwd vs
+    extend_attention_fwd_unified)."""
+    wl = W.draw(_spec(batch=4, hq=8, hkv=2, lq=128, lv=128, prefix=[0, 17, 3, 60],
+                      extend=[12, 1, 0, 33], seed=22))
+    o, lse = _run_oracle(wl, cap=20.0, window=15)
+    uptr, uidx, plen = oracle.build_unified_kv_indices(
+        wl.kv_indptr, wl.kv_indices, wl.extend_start_loc, wl.extend_seq_lens,
+        wl.extend_kv_indices, wl.batch)
+    kb, vb = wl.pool()
+    uo, ul = oracle.extend_attention_unified(wl.q, kb, vb, wl.qo_indptr, uptr, uidx, plen,
+                                             wl.sm_scale, 20.0, 15)
+    assert torch.equal(o, uo) and torch.equal(lse, ul)
+
+
+def test_default_scale_is_inverse_sqrt_lq():
+    """sm_scale <= 0 means 1/sqrt(Lq) (the launcher's 'sm_scale or
+    1/sqrt(Lq)')."""
+    wl = W.draw(_spec(batch=1, hq=2, hkv=1, lq=64, lv=64, prefix=[3], extend=[2], seed=23))
+    k_ext, v_ext = wl.extend_kv()
+    kb, vb = wl.pool()
+    args = (wl.q, k_ext, v_ext, kb, vb, wl.qo_indptr, wl.kv_indptr, wl.kv_indices)
+    o0, _ = oracle.extend_attention(*args, 0.0)
+    o1, _ = oracle.extend_attention(*args, 1.0 / 8.0)
+    assert torch.equal(o0, o1)
