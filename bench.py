@@ -1,0 +1,517 @@
+#!/usr/bin/env python
+"""Benchmark of the extend-attention hot path on one GB300 (or N replicas).
+
+One step = one pass of the extend hot path over one batch of the
+Llama-3-8B-shaped workload (16 sequences, Hq=32, Hkv=8, D=128, prefix lens
+uniform[0,4096], extend lens uniform[1,1024], 262144-slot pool with permuted
+slots, bf16 N(0,1), sm_scale 1/sqrt(128)):
+  1. build_unified_kv_indices (prefix slots + extend slots -> unified list)
+  2. extend_attention_fwd_unified (device scheduler, paged gather, QK^T,
+     mask, online softmax, PV, split-KV combine)
+Inputs are resident in HBM when the timed region starts; L2 is flushed
+(a 512 MiB buffer is written) before every timed step, outside the timing.
+
+value = algorithmic FLOPs of all ranks / max over ranks of the device time
+(TFLOP/s); FLOPs = 2 (Lq + Lv) per visible (query head, key) pair.
+
+--impl reference times the float64 CPU oracle instead (the reference arm of
+this build), on a bounded row sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_extend_gb300 import workloads as W  # noqa: E402
+
+WORKLOAD = "llama3_8b"
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------ work counters
+def visible_pairs(spec: W.WorkloadSpec, prefix, extend, rows=None, qo_indptr=None):
+    """Number of visible (query, key) pairs per query token (summed over the
+    batch, or for the given token rows): causal over prefix + extend, cut by
+    the sliding window."""
+    total = 0
+    win = spec.sliding_window
+    per_token = []
+    for p, e in zip(prefix, extend):
+        if e == 0:
+            continue
+        qpos = torch.arange(p, p + e, dtype=torch.int64)
+        n = qpos + 1
+        if win > 0:
+            n = torch.clamp(n, max=win + 1)
+        per_token.append(n)
+    if not per_token:
+        return 0
+    allv = torch.cat(per_token)
+    if rows is None:
+        return int(allv.sum())
+    return int(allv[rows].sum())
+
+
+def extend_flops(wl: W.Workload) -> float:
+    s = wl.spec
+    return 2.0 * (s.lq + s.lv) * s.hq * visible_pairs(s, wl.prefix_lens, wl.extend_lens)
+
+
+def extend_bytes(wl: W.Workload, unified: bool) -> float:
+    """Algorithmic bytes: every visible K/V row once per (sequence, KV head),
+    4 B per prefix index (8 B per unified index), Q read, O write, lse."""
+    s = wl.spec
+    kv_row = (s.lq if s.v_aliases_k else s.lq + s.lv) * 2
+    keys = 0
+    for p, e in zip(wl.prefix_lens, wl.extend_lens):
+        if e == 0:
+            continue
+        lo = 0 if s.sliding_window <= 0 else max(0, p - s.sliding_window)
+        keys += p + e - lo
+    idx = (8 if unified else 4) * sum(wl.prefix_lens) + (8 * sum(wl.extend_lens) if unified else 0)
+    n = sum(wl.extend_lens)
+    qo = n * s.hq * (s.lq + s.lv) * 2 + n * s.hq * 4
+    return keys * s.hkv * kv_row + idx + qo
+
+
+def decode_bytes(wl: W.Workload) -> float:
+    s = wl.spec
+    kv_row = (s.lq if s.v_aliases_k else s.lq + s.lv) * 2
+    keys = 0
+    for p in wl.prefix_lens:
+        T = p + 1
+        keys += T if s.sliding_window <= 0 else min(T, s.sliding_window + 1)
+    return keys * s.hkv * kv_row + 4 * keys + wl.batch * s.hq * ((s.lq + s.lv) * 2 + 4)
+
+
+# ------------------------------------------------------------------ peaks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------ clock sampler
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms while the
+    timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.window = None
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        t0, t1 = self.window or (0, 1e30)
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        inside = [s for t, s in self.samples if t0 - 0.025 <= t <= t1 + 0.025]
+        if not inside:  # timed region shorter than the sampling period
+            inside = [s for _, s in self.samples][-3:]
+        for s in inside:
+            parts = [x.strip() for x in s.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# -------------------------------------------------------------- distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, dev) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ reference arm
+def oracle_sample_rows(wl, count, seed):
+    g = torch.Generator().manual_seed(seed)
+    total = wl.n_q_tokens * wl.spec.hq
+    return torch.randperm(total, generator=g)[:min(count, total)].sort().values
+
+
+def oracle_rate(wl, rows, k_ext, v_ext, kb, vb):
+    """Run the oracle on the given (token*Hq + head) rows; return (seconds,
+    flops)."""
+    import oracle
+    s = wl.spec
+    t0 = time.perf_counter()
+    oracle.extend_attention(wl.q, k_ext, v_ext, kb, vb, wl.qo_indptr, wl.kv_indptr,
+                            wl.kv_indices, wl.sm_scale, s.logit_cap, s.sliding_window, rows=rows)
+    dt = time.perf_counter() - t0
+    tok = rows // s.hq
+    pairs = visible_pairs(s, wl.prefix_lens, wl.extend_lens, rows=tok)
+    return dt, 2.0 * (s.lq + s.lv) * pairs
+
+
+def calibrate_rows(wl, k_ext, v_ext, kb, vb, target_s):
+    rows = oracle_sample_rows(wl, 256, seed=1)
+    dt, fl = oracle_rate(wl, rows, k_ext, v_ext, kb, vb)
+    per_row = dt / rows.numel()
+    return max(64, min(wl.n_q_tokens * wl.spec.hq, int(target_s / max(per_row, 1e-9))))
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    wl = W.draw(W.SPECS[WORKLOAD])
+    k_ext, v_ext = wl.extend_kv()
+    kb, vb = wl.pool()
+    # size each step so the whole run stays within about two minutes
+    nrows = calibrate_rows(wl, k_ext, v_ext, kb, vb,
+                           target_s=min(4.0, 120.0 / max(1, args.steps)))
+    for w in range(args.warmup):
+        oracle_rate(wl, oracle_sample_rows(wl, max(64, nrows // 8), seed=100 + w), k_ext, v_ext, kb, vb)
+    tot_t = tot_f = 0.0
+    for k in range(args.steps):
+        dt, fl = oracle_rate(wl, oracle_sample_rows(wl, nrows, seed=1000 + k), k_ext, v_ext, kb, vb)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    cores = oracle.num_threads()
+    sample = (f"{nrows} random (token, q-head) rows of the {WORKLOAD} workload per step "
+              f"(of {wl.n_q_tokens * wl.spec.hq}); float64 oracle")
+    line = {
+        "impl": "reference", "metric": "extend-attn TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(wl),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(wl):
+    s = wl.spec
+    return {"workload": (f"{s.name}: batch={s.batch} Hq={s.hq} Hkv={s.hkv} D={s.lq} "
+                         f"prefix~U[0,4096] extend~U[1,1024] pool={s.num_slots} slots "
+                         f"(permuted) bf16 N(0,1) sm_scale=1/sqrt(128)"),
+            "batch": s.batch, "q_tokens": wl.n_q_tokens,
+            "kv_tokens": int(sum(wl.prefix_lens) + sum(wl.extend_lens)),
+            "seed": s.seed, "l2": "flushed before every timed step (512 MiB write)",
+            "step": "build_unified_kv_indices + extend_attention_fwd_unified"}
+
+
+# ------------------------------------------------------------- our arm
+class ExtendStep:
+    """Device-resident inputs and the one-step call sequence."""
+
+    def __init__(self, wl: W.Workload, dev):
+        from paged_kv_extend_gb300 import pkx
+        self.pkx = pkx
+        s = wl.spec
+        self.wl = wl
+        self.dev = dev
+        self.kb, self.vb = wl.pool(dev)
+        self.q = wl.q.to(dev)
+        self.prefix_indptr = wl.kv_indptr.to(dev)
+        self.prefix_indices = wl.kv_indices.to(dev)
+        self.extend_start = wl.extend_start_loc.to(dev)
+        self.extend_lens = wl.extend_seq_lens.to(dev)
+        self.extend_indices = wl.extend_kv_indices.to(dev)
+        self.qo_indptr = wl.qo_indptr.to(dev)
+        n = wl.n_q_tokens
+        self.uptr = torch.empty(wl.batch + 1, dtype=torch.int32, device=dev)
+        self.uidx = torch.empty(self.prefix_indices.numel() + self.extend_indices.numel(),
+                                dtype=torch.int64, device=dev)
+        self.plen = torch.empty(wl.batch, dtype=torch.int32, device=dev)
+        self.o = torch.empty(n, s.hq, s.lv, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(n, s.hq, dtype=torch.float32, device=dev)
+        nbytes = pkx.extend_workspace_size(wl.batch, n, s.hq, s.hkv, s.lq, s.lv)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.launches = 4  # index build, scheduler, attention, combine
+
+    def __call__(self):
+        s = self.wl.spec
+        self.pkx.build_unified_kv_indices(self.prefix_indptr, self.prefix_indices,
+                                          self.extend_start, self.extend_lens,
+                                          self.extend_indices, self.wl.batch,
+                                          out=(self.uptr, self.uidx, self.plen))
+        self.pkx.extend_attention_fwd_unified(
+            self.q, self.o, self.kb, self.vb, self.qo_indptr, self.uptr, self.uidx, self.plen,
+            self.wl.sm_scale, s.logit_cap, s.sliding_window, lse=self.lse, workspace=self.ws)
+
+
+def time_steps(step, steps, flush, dev, attn_events=False, pkx=None):
+    """Per-step device time (ms) with CUDA events on the current stream, L2
+    flushed before each step outside the events; optionally the attention
+    kernel's own time."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ab = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ae = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in ab + ae:
+        e.record()
+    torch.cuda.synchronize(dev)
+    for k in range(steps):
+        flush.zero_()
+        if attn_events:
+            pkx.set_attention_events(ab[k], ae[k])
+        starts[k].record()
+        step()
+        ends[k].record()
+    if attn_events:
+        pkx.set_attention_events(None, None)
+    torch.cuda.synchronize(dev)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    attn_ms = [s.elapsed_time(e) for s, e in zip(ab, ae)] if attn_events else None
+    return step_ms, attn_ms
+
+
+def measure_e2e(step: ExtendStep, steps, warmup, flush, dev):
+    """Same metric through the public API with host buffers: every step
+    copies its inputs (q, prefix indptr/indices, extend starts/lens/indices,
+    qo_indptr) from pinned host memory, runs the step and reads o back into
+    pinned host memory.  The KV pool is device-resident state (it is the
+    cache), as in serving."""
+    pin = lambda t: t.cpu().pin_memory()
+    host_in = [pin(t) for t in (step.q, step.prefix_indptr, step.prefix_indices, step.extend_start,
+                                step.extend_lens, step.extend_indices, step.qo_indptr)]
+    dev_in = [step.q, step.prefix_indptr, step.prefix_indices, step.extend_start,
+              step.extend_lens, step.extend_indices, step.qo_indptr]
+    host_o = torch.empty(step.o.shape, dtype=step.o.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_o.numel() * host_o.element_size()
+
+    def e2e_step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        host_o.copy_(step.o, non_blocking=True)
+
+    for _ in range(warmup):
+        e2e_step()
+    ms, _ = time_steps(e2e_step, steps, flush, dev)
+    return sum(ms) / len(ms), h2d, d2h
+
+
+def measure_decode(dev, flush, steps):
+    from paged_kv_extend_gb300 import pkx
+    wl = W.draw(W.SPECS["decode_gqa"])
+    s = wl.spec
+    kb, vb = wl.pool(dev)
+    q = wl.q.to(dev)
+    kvp, kvi = wl.kv_indptr.to(dev), wl.kv_indices.to(dev)
+    o = torch.empty(s.batch, s.hq, s.lv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(s.batch, s.hq, dtype=torch.float32, device=dev)
+    ws = torch.empty(pkx.decode_workspace_size(s.batch, s.hq, s.hkv, s.lq, s.lv),
+                     dtype=torch.uint8, device=dev)
+    fn = lambda: pkx.decode_attention_fwd(q, o, kb, vb, kvp, kvi, wl.sm_scale, lse=lse, workspace=ws)
+    for _ in range(3):
+        fn()
+    ms, attn = time_steps(fn, steps, flush, dev, attn_events=True, pkx=pkx)
+    b = decode_bytes(wl)
+    out = {"workload": "decode_gqa: batch=64 Hq=32 Hkv=8 D=128 T=8193 pool=2^20",
+           "GB/s": b / (sum(ms) / len(ms) * 1e-3) / 1e9,
+           "attn_kernel_GB/s": b / (sum(attn) / len(attn) * 1e-3) / 1e9,
+           "bytes": b, "ms": sum(ms) / len(ms)}
+    del kb, vb
+    return out
+
+
+def run_ours(args, ws, rank, local):
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the CUDA library has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from paged_kv_extend_gb300 import build as pkx_build
+    from paged_kv_extend_gb300 import pkx
+    if rank == 0:
+        pkx_build.build()
+    barrier(ws)
+    pkx.load_library()
+    hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
+
+    wl = W.draw(W.SPECS[WORKLOAD])
+    step = ExtendStep(wl, dev)
+    flops = extend_flops(wl)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if pkx.workspace_status(step.ws) != 0:
+        raise SystemExit(f"device status {pkx.workspace_status(step.ws)} after warm-up")
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.2)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    step_ms, attn_ms = time_steps(step, args.steps, flush, dev, attn_events=True, pkx=pkx)
+    t1 = time.time()
+    barrier(ws)
+    if clocks:
+        clocks.mark(t0, t1)
+    clock_info = clocks.stop() if clocks else None
+
+    ms = sum(step_ms) / len(step_ms)
+    ms_max = max_over_ranks(ms, ws, dev)
+    attn_avg = sum(attn_ms) / len(attn_ms)
+    value = flops * ws / (ms_max * 1e-3) / 1e12
+    achieved = flops / (attn_avg * 1e-3) / 1e12
+
+    e2e_ms, h2d, d2h = measure_e2e(step, args.steps, 2, flush, dev)
+    e2e_ms = max_over_ranks(e2e_ms, ws, dev)
+
+    components = {}
+    if not args.no_components:
+        components["decode"] = measure_decode(dev, flush, max(5, min(args.steps, 20)))
+        components["decode"]["frac_of_hbm"] = components["decode"]["attn_kernel_GB/s"] / hbm_peak
+        components["extend_attn_kernel_share"] = attn_avg / ms
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        k_ext, v_ext = wl.extend_kv()
+        kb, vb = wl.pool()
+        nrows = calibrate_rows(wl, k_ext, v_ext, kb, vb, target_s=10.0)
+        rows = oracle_sample_rows(wl, nrows, seed=4242)
+        dt, fl = oracle_rate(wl, rows, k_ext, v_ext, kb, vb)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+               "kind": "oracle",
+               "sample": f"{nrows} random (token, q-head) rows of {wl.n_q_tokens * wl.spec.hq}, "
+                         f"{dt:.1f} s of float64 CPU work"}
+
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "attn_kernel_llama3_8b.md")
+    if os.path.exists(prof):
+        import hashlib
+        src = b"".join(open(os.path.join(ROOT, "paged_kv_extend_gb300", "csrc", f), "rb").read()
+                       for f in ("attention.cu", "ptx.cuh"))
+        h = hashlib.sha1(src).hexdigest()[:12]
+        for line in open(prof):
+            if line.startswith("traffic_bytes_per_launch:"):
+                parts = line.split()
+                if len(parts) >= 4 and parts[3] == h:
+                    traffic = float(parts[1])
+
+    line = {
+        "metric": "extend-attn TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_dict(wl),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak,
+                     "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": traffic,
+                     "peak_source": f"bf16_tflops burst, of {peak_src}",
+                     "kernel": "attn_kernel<128, unified>",
+                     "algorithmic_flops_per_launch": flops,
+                     "algorithmic_bytes_per_launch": extend_bytes(wl, unified=True)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches * args.steps,
+        "clocks": clock_info,
+        "components": components,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-components", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        rc = run_reference(args, ws, rank)
+    else:
+        rc = run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

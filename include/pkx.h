@@ -1,0 +1,223 @@
+/*
+ * pkx.h -- C ABI of libpkx: extend attention over a page-size-1 KV pool and
+ * its companions (decode attention, unified KV-index build, merge_state),
+ * as hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * Conventions for every call below
+ * --------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  Outputs
+ *    are preallocated by the caller and written in place.  A call never
+ *    allocates device memory and never synchronises the host with the
+ *    device; everything is enqueued on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).
+ *  - bf16 means IEEE bfloat16 (16 bits).  Shapes are written outermost
+ *    first; the last dimension is always contiguous.  Strides are in
+ *    ELEMENTS.
+ *  - Alignment: every bf16 tensor base pointer must be 16-byte aligned, and
+ *    every row stride must be a multiple of 8 elements (16 bytes); index and
+ *    indptr arrays must be 4-byte (int32) / 8-byte (int64) aligned.
+ *  - Return value: PKX_OK (0) or an error code.  Argument errors are found
+ *    on the host before anything is enqueued (nothing is written then).
+ *    pkx_last_error_string() gives a human-readable reason for the last
+ *    failing call on the calling thread.  No call aborts or throws.
+ *  - Index values that point outside the pool ([0, num_slots)) are not
+ *    dereferenced: the kernel reads a zero row instead and records
+ *    PKX_EDEVICE in the workspace's status word, which
+ *    pkx_workspace_status() reads back.
+ *  - Every wait inside a kernel is bounded (about two seconds); a wait that
+ *    runs out records PKX_ETIMEOUT in the same status word and the kernel
+ *    returns instead of hanging.
+ *
+ * Notation (the pages' own): per sequence b, P_b prefix (cached) tokens and
+ * E_b extend (new) tokens, T_b = P_b + E_b keys at positions 0..T_b-1; extend
+ * query i sits at position P_b + i.  Hq query heads, Hkv KV heads, query head
+ * h reads KV head h / (Hq / Hkv).  Lq = query/key head dim, Lv = value head
+ * dim.
+ */
+#ifndef PKX_H
+#define PKX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define PKX_OK 0
+#define PKX_EINVAL 1        /* bad argument: null, misaligned, inconsistent */
+#define PKX_EUNSUPPORTED 2  /* valid but not built: head dims, group size   */
+#define PKX_ECUDA 3         /* a CUDA runtime call or a launch failed        */
+#define PKX_ETIMEOUT 4      /* a bounded device wait ran out (status word)   */
+#define PKX_EDEVICE 5       /* device-side index check failed (status word)  */
+#define PKX_EWORKSPACE 6    /* workspace null or smaller than required       */
+
+/* Reason for the last failing call on this thread ("" if none). */
+const char *pkx_last_error_string(void);
+
+/* Library version string. */
+const char *pkx_version(void);
+
+/*
+ * Workspace bytes the attention calls need for the given problem on the
+ * CURRENT device (it depends on the device's SM count).  The workspace holds
+ * the device-built work list and the split-KV partial results; it must be
+ * 256-byte aligned.  Its content need not be initialised and may be reused
+ * by later calls on the same stream.  Returns 0 on bad arguments.
+ *   num_q_tokens: rows of q_extend (sum of E_b) for extend; batch for decode.
+ */
+size_t pkx_extend_workspace_size(int batch, int num_q_tokens, int hq, int hkv,
+                                 int lq, int lv);
+size_t pkx_decode_workspace_size(int batch, int hq, int hkv, int lq, int lv);
+
+/*
+ * Device status word of the last attention call that used `workspace`:
+ * copies it to the host (synchronising `stream`) and returns PKX_OK,
+ * PKX_EDEVICE or PKX_ETIMEOUT.  Returns PKX_ECUDA if the copy fails.
+ */
+int pkx_workspace_status(const void *workspace, void *stream);
+
+/*
+ * Profiling hook: when `before` / `after` are non-null cudaEvent_t handles,
+ * every later attention call made on this thread records `before` on its
+ * stream immediately before the attention kernel launch and `after`
+ * immediately after it (the scheduler and split-KV combine launches fall
+ * outside the pair), so the caller can time the attention kernel alone with
+ * cudaEventElapsedTime.  Pass NULL, NULL to stop.  Events are owned by the
+ * caller.
+ */
+void pkx_set_attention_events(void *before, void *after);
+
+/*
+ * Extend attention, two-stage form.
+ * Source: sglang extend_attention.py (diff 0.5.3rc2 -> 0.5.4.post1),
+ * extend_attention_fwd and its _fwd_kernel (prefix K/V read from the pool
+ * through kv_indptr/kv_indices, extend K/V read from k_extend/v_extend); the
+ * masks, cap and online softmax follow _fwd_kernel_unified on the same page.
+ *
+ * For every sequence b, q head h and extend query i (position P_b + i):
+ *   keys j <  P_b: k_buffer/v_buffer row (kv_indices[kv_indptr[b] + j], h_kv)
+ *   keys j >= P_b: k_extend/v_extend row (qo_indptr[b] + j - P_b, h_kv)
+ *   s_j = sm_scale * <q, k_j>;  s_j = logit_cap * tanh(s_j / logit_cap) if
+ *   logit_cap > 0; key j is visible iff j <= P_b + i and, if
+ *   sliding_window > 0, (P_b + i) - j <= sliding_window;
+ *   o = softmax over visible keys of s, applied to v;  lse = log sum exp s.
+ *
+ *   q_extend   bf16 [num_q_tokens, hq, lq] contiguous
+ *   k_extend   bf16 row (t, h) at k_extend + t*ke_st + h*ke_sh, lq elements
+ *   v_extend   bf16 row (t, h) at v_extend + t*ve_st + h*ve_sh, lv elements
+ *   o_extend   bf16 [num_q_tokens, hq, lv] contiguous (written)
+ *   k_buffer   bf16 row (slot, h) at k_buffer + slot*kb_ss + h*kb_sh (lq)
+ *   v_buffer   bf16 row (slot, h) at v_buffer + slot*vb_ss + h*vb_sh (lv);
+ *              may alias k_buffer (MLA: V is the first lv dims of K)
+ *   qo_indptr  int32 [batch+1], qo_indptr[0] = 0, non-decreasing,
+ *              qo_indptr[batch] = num_q_tokens
+ *   kv_indptr  int32 [batch+1] over kv_indices: the PREFIX keys only
+ *   kv_indices int32 [kv_indptr[batch]] pool slots
+ *   sm_scale   <= 0 selects 1/sqrt(lq)
+ *   logit_cap  <= 0: no cap
+ *   sliding_window <= 0: no window
+ *   lse_out    nullable fp32 [num_q_tokens, hq] (natural log)
+ *   workspace  >= pkx_extend_workspace_size(...) bytes
+ * Supported (lq, lv): (64, 64), (128, 128), (576, 512); hq % hkv == 0 and
+ * hq / hkv <= 128.
+ */
+int pkx_extend_attention_fwd(
+    const void *q_extend, const void *k_extend, const void *v_extend,
+    void *o_extend, const void *k_buffer, const void *v_buffer,
+    const int32_t *qo_indptr, const int32_t *kv_indptr,
+    const int32_t *kv_indices, int batch, int num_q_tokens, int hq, int hkv,
+    int lq, int lv, int64_t ke_st, int64_t ke_sh, int64_t ve_st,
+    int64_t ve_sh, int64_t kb_ss, int64_t kb_sh, int64_t vb_ss, int64_t vb_sh,
+    int64_t num_slots, float sm_scale, float logit_cap, int sliding_window,
+    float *lse_out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Extend attention, unified form.
+ * Source: sglang extend_attention.py, extend_attention_fwd_unified and
+ * _fwd_kernel_unified: prefix and extend keys alike are pool slots
+ * kv_indices[kv_indptr[b] + j], j < T_b = kv_indptr[b+1] - kv_indptr[b]; the
+ * first prefix_lens[b] of them are the prefix, so extend query i sits at
+ * position prefix_lens[b] + i.  The window start position is 0 for every
+ * sequence (the launcher's default).  Same math and arguments as the
+ * two-stage form, except:
+ *   q, o       as q_extend / o_extend
+ *   kv_indptr  int32 [batch+1] over ALL keys of each sequence
+ *   kv_indices int64 [kv_indptr[batch]] (as build_unified_kv_indices makes)
+ *   prefix_lens int32 [batch]
+ */
+int pkx_extend_attention_fwd_unified(
+    const void *q, void *o, const void *k_buffer, const void *v_buffer,
+    const int32_t *qo_indptr, const int32_t *kv_indptr,
+    const int64_t *kv_indices, const int32_t *prefix_lens, int batch,
+    int num_q_tokens, int hq, int hkv, int lq, int lv, int64_t kb_ss,
+    int64_t kb_sh, int64_t vb_ss, int64_t vb_sh, int64_t num_slots,
+    float sm_scale, float logit_cap, int sliding_window, float *lse_out,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Decode attention.
+ * Source: sglang flashinfer_backend.py, forward_decode (the token's K/V are
+ * saved into the pool first, then one query per sequence attends to all
+ * T_b = kv_indptr[b+1] - kv_indptr[b] keys) and the sliding-window decode
+ * index updater (the last min(T_b, W + 1) keys).  Same math as extend with
+ * the query at position T_b - 1.  A sequence with T_b = 0 (padding) gets
+ * o = 0 and lse = -inf.
+ *   q  bf16 [batch, hq, lq] contiguous;  o  bf16 [batch, hq, lv] contiguous
+ *   kv_indptr int32 [batch+1]; kv_indices int32 [kv_indptr[batch]]
+ *   workspace >= pkx_decode_workspace_size(...) bytes
+ */
+int pkx_decode_attention_fwd(
+    const void *q, void *o, const void *k_buffer, const void *v_buffer,
+    const int32_t *kv_indptr, const int32_t *kv_indices, int batch, int hq,
+    int hkv, int lq, int lv, int64_t kb_ss, int64_t kb_sh, int64_t vb_ss,
+    int64_t vb_sh, int64_t num_slots, float sm_scale, float logit_cap,
+    int sliding_window, float *lse_out, void *workspace,
+    size_t workspace_bytes, void *stream);
+
+/*
+ * merge_state.
+ * Source: sglang flashinfer_backend.py, forward_extend (the ragged causal
+ * extend result and the non-causal paged prefix result, each with its
+ * log-sum-exp, combined into one).  For every row r = (token, head):
+ *   s = log(exp(s_a) + exp(s_b))
+ *   v = exp(s_a - s) * v_a + exp(s_b - s) * v_b
+ * A side with s = -inf has weight 0; both -inf gives v = 0, s = -inf.
+ *   v_a, v_b, v_out  bf16 [n_tokens, h, dv] contiguous; dv % 8 == 0
+ *   s_a, s_b         fp32 [n_tokens, h] (natural log)
+ *   s_out            nullable fp32 [n_tokens, h]
+ * v_out may alias v_a or v_b (and s_out s_a or s_b): each row is read
+ * before it is written.
+ */
+int pkx_merge_state(const void *v_a, const float *s_a, const void *v_b,
+                    const float *s_b, void *v_out, float *s_out,
+                    int64_t n_tokens, int h, int dv, void *stream);
+
+/*
+ * Unified KV-index build.
+ * Source: sglang extend_attention.py, build_unified_kv_indices and
+ * _copy_unified_indices_kernel.  For b < batch:
+ *   prefix_lens[b]           = prefix_kv_indptr[b+1] - prefix_kv_indptr[b]
+ *   unified_kv_indptr[0]     = 0
+ *   unified_kv_indptr[b+1]   = unified_kv_indptr[b] + prefix_lens[b]
+ *                              + extend_seq_lens[b]
+ *   unified_kv_indices[unified_kv_indptr[b] + j]
+ *       = prefix_kv_indices[prefix_kv_indptr[b] + j]          (j < P_b)
+ *       = extend_kv_indices[extend_start_loc[b] + j - P_b]    (P_b <= j < T_b)
+ * Entries of unified_kv_indices past unified_kv_indptr[batch] are left as
+ * they were.  Inputs int32; unified_kv_indptr and prefix_lens int32 (written);
+ * unified_kv_indices int64 (written), sized >= len(prefix) + len(extend).
+ * extend_start_loc[b] is any start offset (it need not be a running sum).
+ */
+int pkx_build_unified_kv_indices(
+    const int32_t *prefix_kv_indptr, const int32_t *prefix_kv_indices,
+    const int32_t *extend_start_loc, const int32_t *extend_seq_lens,
+    const int32_t *extend_kv_indices, int batch, int32_t *unified_kv_indptr,
+    int64_t *unified_kv_indices, int32_t *prefix_lens, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKX_H */

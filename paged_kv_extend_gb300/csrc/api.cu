@@ -1,0 +1,260 @@
+// api.cu -- the extern "C" entry points of libpkx (declared in include/pkx.h):
+// host-side argument validation, then the launchers.  No entry point
+// allocates device memory or synchronises the stream (except
+// pkx_workspace_status, whose job is to read the device status word).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cuda_runtime.h>
+
+#include "pkx_internal.h"
+
+namespace pkx {
+
+static thread_local char g_err[512] = "";
+static thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+
+void attention_events(cudaEvent_t *before, cudaEvent_t *after) {
+  *before = g_ev_before;
+  *after = g_ev_after;
+}
+
+int set_error(int code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static int check_heads(int hq, int hkv, int lq, int lv) {
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0)
+    return set_error(PKX_EINVAL, "hq=%d must be a positive multiple of hkv=%d", hq, hkv);
+  if (hq / hkv > kBlockM)
+    return set_error(PKX_EUNSUPPORTED, "group size hq/hkv=%d > %d not built", hq / hkv, kBlockM);
+  const bool ok = (lq == 64 && lv == 64) || (lq == 128 && lv == 128);
+  if (!ok) return set_error(PKX_EUNSUPPORTED, "head dims (lq=%d, lv=%d) not built", lq, lv);
+  return PKX_OK;
+}
+
+static int check_rows(const char *name, const void *p, int64_t s0, int64_t s1) {
+  if (!p) return set_error(PKX_EINVAL, "%s is null", name);
+  if (!aligned(p, 16)) return set_error(PKX_EINVAL, "%s must be 16-byte aligned", name);
+  if (s0 < 0 || s1 < 0 || s0 % 8 || s1 % 8)
+    return set_error(PKX_EINVAL, "%s strides (%lld, %lld) must be non-negative multiples of 8",
+                     name, (long long)s0, (long long)s1);
+  return PKX_OK;
+}
+
+static int check_scalars(float sm_scale, float logit_cap) {
+  if (!std::isfinite(sm_scale) || !std::isfinite(logit_cap))
+    return set_error(PKX_EINVAL, "sm_scale and logit_cap must be finite");
+  return PKX_OK;
+}
+
+}  // namespace pkx
+
+using namespace pkx;
+
+extern "C" {
+
+const char *pkx_last_error_string(void) { return g_err; }
+
+const char *pkx_version(void) { return "pkx 0.1 (sm_103a)"; }
+
+void pkx_set_attention_events(void *before, void *after) {
+  g_ev_before = static_cast<cudaEvent_t>(before);
+  g_ev_after = static_cast<cudaEvent_t>(after);
+}
+
+size_t pkx_extend_workspace_size(int batch, int num_q_tokens, int hq, int hkv, int lq, int lv) {
+  if (batch < 0 || num_q_tokens < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM ||
+      lv <= 0)
+    return 0;
+  (void)lq;
+  return ws_layout(batch, num_q_tokens, hkv, hq / hkv, lv, num_sms_current_device()).total;
+}
+
+size_t pkx_decode_workspace_size(int batch, int hq, int hkv, int lq, int lv) {
+  return pkx_extend_workspace_size(batch, batch, hq, hkv, lq, lv);
+}
+
+int pkx_workspace_status(const void *workspace, void *stream) {
+  if (!workspace) return set_error(PKX_EINVAL, "workspace is null");
+  int32_t st = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&st, workspace, sizeof st, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error(PKX_ECUDA, "status read: %s", cudaGetErrorString(e));
+  if (st == PKX_EDEVICE) return set_error(PKX_EDEVICE, "device-side index or indptr check failed");
+  if (st == PKX_ETIMEOUT) return set_error(PKX_ETIMEOUT, "a device wait ran out of time");
+  if (st != 0) return set_error(st, "device status %d", st);
+  return PKX_OK;
+}
+
+int pkx_extend_attention_fwd(const void *q_extend, const void *k_extend, const void *v_extend,
+                             void *o_extend, const void *k_buffer, const void *v_buffer,
+                             const int32_t *qo_indptr, const int32_t *kv_indptr,
+                             const int32_t *kv_indices, int batch, int num_q_tokens, int hq,
+                             int hkv, int lq, int lv, int64_t ke_st, int64_t ke_sh,
+                             int64_t ve_st, int64_t ve_sh, int64_t kb_ss, int64_t kb_sh,
+                             int64_t vb_ss, int64_t vb_sh, int64_t num_slots, float sm_scale,
+                             float logit_cap, int sliding_window, float *lse_out,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+  int rc;
+  if (batch < 0 || num_q_tokens < 0) return set_error(PKX_EINVAL, "negative batch or token count");
+  if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
+  if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
+  if (batch == 0 || num_q_tokens == 0) return PKX_OK;
+  if ((rc = check_rows("q_extend", q_extend, 8, 8))) return rc;
+  if ((rc = check_rows("o_extend", o_extend, 8, 8))) return rc;
+  if ((rc = check_rows("k_extend", k_extend, ke_st, ke_sh))) return rc;
+  if ((rc = check_rows("v_extend", v_extend, ve_st, ve_sh))) return rc;
+  if ((rc = check_rows("k_buffer", k_buffer, kb_ss, kb_sh))) return rc;
+  if ((rc = check_rows("v_buffer", v_buffer, vb_ss, vb_sh))) return rc;
+  if (!qo_indptr || !kv_indptr || !aligned(qo_indptr, 4) || !aligned(kv_indptr, 4))
+    return set_error(PKX_EINVAL, "qo_indptr / kv_indptr null or misaligned");
+  if (kv_indices && !aligned(kv_indices, 4)) return set_error(PKX_EINVAL, "kv_indices misaligned");
+  if (lse_out && !aligned(lse_out, 4)) return set_error(PKX_EINVAL, "lse_out misaligned");
+  if (num_slots <= 0) return set_error(PKX_EINVAL, "num_slots must be positive");
+  AttnArgs a{};
+  a.mode = kTwoStage;
+  a.q = q_extend;
+  a.o = o_extend;
+  a.lse = lse_out;
+  a.k_ext = k_extend;
+  a.v_ext = v_extend;
+  a.ke_st = ke_st; a.ke_sh = ke_sh; a.ve_st = ve_st; a.ve_sh = ve_sh;
+  a.k_buf = k_buffer;
+  a.v_buf = v_buffer;
+  a.kb_ss = kb_ss; a.kb_sh = kb_sh; a.vb_ss = vb_ss; a.vb_sh = vb_sh;
+  a.num_slots = num_slots;
+  a.qo_indptr = qo_indptr;
+  a.kv_indptr = kv_indptr;
+  a.prefix_lens = nullptr;
+  a.kv_indices = kv_indices;
+  a.batch = batch; a.num_q_tokens = num_q_tokens; a.hq = hq; a.hkv = hkv; a.lq = lq; a.lv = lv;
+  a.sm_scale = sm_scale; a.logit_cap = logit_cap; a.window = sliding_window;
+  a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_attention(a);
+}
+
+int pkx_extend_attention_fwd_unified(const void *q, void *o, const void *k_buffer,
+                                     const void *v_buffer, const int32_t *qo_indptr,
+                                     const int32_t *kv_indptr, const int64_t *kv_indices,
+                                     const int32_t *prefix_lens, int batch, int num_q_tokens,
+                                     int hq, int hkv, int lq, int lv, int64_t kb_ss,
+                                     int64_t kb_sh, int64_t vb_ss, int64_t vb_sh,
+                                     int64_t num_slots, float sm_scale, float logit_cap,
+                                     int sliding_window, float *lse_out, void *workspace,
+                                     size_t workspace_bytes, void *stream) {
+  int rc;
+  if (batch < 0 || num_q_tokens < 0) return set_error(PKX_EINVAL, "negative batch or token count");
+  if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
+  if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
+  if (batch == 0 || num_q_tokens == 0) return PKX_OK;
+  if ((rc = check_rows("q", q, 8, 8))) return rc;
+  if ((rc = check_rows("o", o, 8, 8))) return rc;
+  if ((rc = check_rows("k_buffer", k_buffer, kb_ss, kb_sh))) return rc;
+  if ((rc = check_rows("v_buffer", v_buffer, vb_ss, vb_sh))) return rc;
+  if (!qo_indptr || !kv_indptr || !prefix_lens || !aligned(qo_indptr, 4) ||
+      !aligned(kv_indptr, 4) || !aligned(prefix_lens, 4))
+    return set_error(PKX_EINVAL, "qo_indptr / kv_indptr / prefix_lens null or misaligned");
+  if (kv_indices && !aligned(kv_indices, 8)) return set_error(PKX_EINVAL, "kv_indices misaligned");
+  if (lse_out && !aligned(lse_out, 4)) return set_error(PKX_EINVAL, "lse_out misaligned");
+  if (num_slots <= 0) return set_error(PKX_EINVAL, "num_slots must be positive");
+  AttnArgs a{};
+  a.mode = kUnified;
+  a.q = q;
+  a.o = o;
+  a.lse = lse_out;
+  a.k_buf = k_buffer;
+  a.v_buf = v_buffer;
+  a.kb_ss = kb_ss; a.kb_sh = kb_sh; a.vb_ss = vb_ss; a.vb_sh = vb_sh;
+  a.num_slots = num_slots;
+  a.qo_indptr = qo_indptr;
+  a.kv_indptr = kv_indptr;
+  a.prefix_lens = prefix_lens;
+  a.kv_indices = kv_indices;
+  a.batch = batch; a.num_q_tokens = num_q_tokens; a.hq = hq; a.hkv = hkv; a.lq = lq; a.lv = lv;
+  a.sm_scale = sm_scale; a.logit_cap = logit_cap; a.window = sliding_window;
+  a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_attention(a);
+}
+
+int pkx_decode_attention_fwd(const void *q, void *o, const void *k_buffer, const void *v_buffer,
+                             const int32_t *kv_indptr, const int32_t *kv_indices, int batch,
+                             int hq, int hkv, int lq, int lv, int64_t kb_ss, int64_t kb_sh,
+                             int64_t vb_ss, int64_t vb_sh, int64_t num_slots, float sm_scale,
+                             float logit_cap, int sliding_window, float *lse_out,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+  int rc;
+  if (batch < 0) return set_error(PKX_EINVAL, "negative batch");
+  if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
+  if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
+  if (batch == 0) return PKX_OK;
+  if ((rc = check_rows("q", q, 8, 8))) return rc;
+  if ((rc = check_rows("o", o, 8, 8))) return rc;
+  if ((rc = check_rows("k_buffer", k_buffer, kb_ss, kb_sh))) return rc;
+  if ((rc = check_rows("v_buffer", v_buffer, vb_ss, vb_sh))) return rc;
+  if (!kv_indptr || !aligned(kv_indptr, 4))
+    return set_error(PKX_EINVAL, "kv_indptr null or misaligned");
+  if (kv_indices && !aligned(kv_indices, 4)) return set_error(PKX_EINVAL, "kv_indices misaligned");
+  if (lse_out && !aligned(lse_out, 4)) return set_error(PKX_EINVAL, "lse_out misaligned");
+  if (num_slots <= 0) return set_error(PKX_EINVAL, "num_slots must be positive");
+  AttnArgs a{};
+  a.mode = kDecode;
+  a.q = q;
+  a.o = o;
+  a.lse = lse_out;
+  a.k_buf = k_buffer;
+  a.v_buf = v_buffer;
+  a.kb_ss = kb_ss; a.kb_sh = kb_sh; a.vb_ss = vb_ss; a.vb_sh = vb_sh;
+  a.num_slots = num_slots;
+  a.qo_indptr = nullptr;
+  a.kv_indptr = kv_indptr;
+  a.prefix_lens = nullptr;
+  a.kv_indices = kv_indices;
+  a.batch = batch; a.num_q_tokens = batch; a.hq = hq; a.hkv = hkv; a.lq = lq; a.lv = lv;
+  a.sm_scale = sm_scale; a.logit_cap = logit_cap; a.window = sliding_window;
+  a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_attention(a);
+}
+
+int pkx_merge_state(const void *v_a, const float *s_a, const void *v_b, const float *s_b,
+                    void *v_out, float *s_out, int64_t n_tokens, int h, int dv, void *stream) {
+  if (n_tokens < 0 || h <= 0 || dv <= 0 || dv % 8)
+    return set_error(PKX_EINVAL, "merge_state: n_tokens >= 0, h > 0, dv a positive multiple of 8");
+  if (n_tokens == 0) return PKX_OK;
+  if (!v_a || !v_b || !v_out || !s_a || !s_b)
+    return set_error(PKX_EINVAL, "merge_state: null input or output");
+  if (!aligned(v_a, 16) || !aligned(v_b, 16) || !aligned(v_out, 16) || !aligned(s_a, 4) ||
+      !aligned(s_b, 4) || (s_out && !aligned(s_out, 4)))
+    return set_error(PKX_EINVAL, "merge_state: misaligned pointer");
+  return launch_merge_state(v_a, s_a, v_b, s_b, v_out, s_out, n_tokens, h, dv,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int pkx_build_unified_kv_indices(const int32_t *prefix_kv_indptr,
+                                 const int32_t *prefix_kv_indices,
+                                 const int32_t *extend_start_loc, const int32_t *extend_seq_lens,
+                                 const int32_t *extend_kv_indices, int batch,
+                                 int32_t *unified_kv_indptr, int64_t *unified_kv_indices,
+                                 int32_t *prefix_lens, void *stream) {
+  if (batch < 0) return set_error(PKX_EINVAL, "negative batch");
+  if (!prefix_kv_indptr || !unified_kv_indptr)
+    return set_error(PKX_EINVAL, "prefix_kv_indptr / unified_kv_indptr null");
+  if (batch > 0 && (!extend_start_loc || !extend_seq_lens || !prefix_lens || !unified_kv_indices))
+    return set_error(PKX_EINVAL, "null argument");
+  if (!aligned(unified_kv_indices, 8)) return set_error(PKX_EINVAL, "unified_kv_indices misaligned");
+  return launch_build_unified(prefix_kv_indptr, prefix_kv_indices, extend_start_loc,
+                              extend_seq_lens, extend_kv_indices, batch, unified_kv_indptr,
+                              unified_kv_indices, prefix_lens, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+// pkx_internal.h -- declarations shared by the translation units of libpkx
+// (host side): error reporting, workspace layout and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/pkx.h"
+
+namespace pkx {
+
+// Per-thread error message (pkx_last_error_string).
+int set_error(int code, const char *fmt, ...);
+
+// Which key source an attention launch reads.
+enum KeyMode : int {
+  kTwoStage = 0,  // prefix via int32 kv_indices, extend rows from k/v_extend
+  kUnified = 1,   // every key via int64 kv_indices, prefix_lens given
+  kDecode = 2,    // every key via int32 kv_indices, query at position T-1
+};
+
+// Rows of one query tile (tcgen05 M) and keys of one KV tile.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+// Smallest number of KV tiles a split-KV chunk holds.
+constexpr int kMinSplitTiles = 4;
+
+// One unit of attention work: a block of query tokens of one sequence and one
+// KV head (all of that head's query heads stacked in the tile's rows, row =
+// token * group + head-in-group), over the key range [k_begin, k_end).
+struct WorkUnit {
+  int32_t q_tok0;   // first query row in q/o (token index)
+  int32_t n_tok;    // tokens in the block
+  int32_t qpos0;    // position of the first query token in its sequence
+  int32_t kvh;      // KV head
+  int32_t k_begin;  // key positions [k_begin, k_end)
+  int32_t k_end;
+  int32_t b;        // sequence
+  int32_t slot;     // -1: write o/lse; else split-KV partial slot
+};
+
+// A query block whose key range was split: its partials live in slots
+// [slot0, slot0 + n_split).
+struct CombineEntry {
+  int32_t q_tok0;
+  int32_t n_tok;
+  int32_t kvh;
+  int32_t slot0;
+  int32_t n_split;
+  int32_t pad[3];
+};
+
+// Header at the start of every attention workspace.
+struct WsHeader {
+  int32_t status;      // PKX_OK / PKX_EDEVICE / PKX_ETIMEOUT (first error wins)
+  int32_t n_units;
+  int32_t n_combine;
+  int32_t split_tiles; // chunk size chosen by the scheduler (tiles)
+  int32_t pad[60];
+};
+
+// Byte offsets of the workspace regions for one problem.
+struct WsLayout {
+  size_t seq_off;      // int32 [8][batch + 1] per-sequence scratch
+  size_t qb_off;       // int32 [qb_max] per-query-block tile counts
+  size_t units_off;    // WorkUnit [unit_max]
+  size_t comb_off;     // CombineEntry [comb_max]
+  size_t plse_off;     // float [slot_max][kBlockM]
+  size_t po_off;       // float [slot_max][kBlockM][lv]
+  size_t total;
+  int qb_max, unit_max, comb_max, slot_max, unit_target;
+};
+
+int num_sms_current_device();
+// Events set by pkx_set_attention_events for this thread (may be null).
+void attention_events(cudaEvent_t *before, cudaEvent_t *after);
+int tokens_per_block(int group);
+WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int num_sms);
+
+// Arguments of one attention launch (any key mode).
+struct AttnArgs {
+  int mode;
+  const void *q;
+  void *o;
+  float *lse;
+  const void *k_ext, *v_ext;
+  int64_t ke_st, ke_sh, ve_st, ve_sh;
+  const void *k_buf, *v_buf;
+  int64_t kb_ss, kb_sh, vb_ss, vb_sh;
+  int64_t num_slots;
+  const int32_t *qo_indptr, *kv_indptr, *prefix_lens;
+  const void *kv_indices;
+  int batch, num_q_tokens, hq, hkv, lq, lv;
+  float sm_scale, logit_cap;
+  int window;
+  void *workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+};
+
+int launch_attention(const AttnArgs &a);
+int launch_merge_state(const void *v_a, const float *s_a, const void *v_b, const float *s_b,
+                       void *v_out, float *s_out, int64_t n, int h, int dv, cudaStream_t s);
+int launch_build_unified(const int32_t *prefix_kv_indptr, const int32_t *prefix_kv_indices,
+                         const int32_t *extend_start_loc, const int32_t *extend_seq_lens,
+                         const int32_t *extend_kv_indices, int batch, int32_t *unified_kv_indptr,
+                         int64_t *unified_kv_indices, int32_t *prefix_lens, cudaStream_t s);
+
+}  // namespace pkx

@@ -1,0 +1,261 @@
+"""Python binding of libpkx (include/pkx.h): argument marshalling only.
+
+Every function here takes torch CUDA tensors, checks dtypes and shapes,
+passes raw device pointers, element strides and the current CUDA stream to
+the C entry point of the same name (``pkx_`` prefix dropped), and raises
+:class:`PkxError` on a non-zero status.  All computation happens in the CUDA
+kernels of libpkx.so; there is no fallback path.  If the library is missing
+the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkx.so")
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_lock = threading.Lock()
+_lib = None
+
+# status codes (include/pkx.h)
+PKX_OK, PKX_EINVAL, PKX_EUNSUPPORTED, PKX_ECUDA, PKX_ETIMEOUT, PKX_EDEVICE, PKX_EWORKSPACE = range(7)
+
+
+class PkxError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"pkx error {code}: {msg}")
+        self.code = code
+
+
+# argtypes of every exported symbol, in header order
+_SIGS = {
+    "pkx_last_error_string": (ctypes.c_char_p, []),
+    "pkx_version": (ctypes.c_char_p, []),
+    "pkx_extend_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "pkx_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "pkx_workspace_status": (_i, [_p, _p]),
+    "pkx_set_attention_events": (None, [_p, _p]),
+    "pkx_extend_attention_fwd": (_i, [
+        _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
+        _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _sz, _p]),
+    "pkx_extend_attention_fwd_unified": (_i, [
+        _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
+        _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _sz, _p]),
+    "pkx_decode_attention_fwd": (_i, [
+        _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i,
+        _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _sz, _p]),
+    "pkx_merge_state": (_i, [_p, _p, _p, _p, _p, _p, _i64, _i, _i, _p]),
+    "pkx_build_unified_kv_indices": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _p, _p]),
+}
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libpkx.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = path or LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libpkx.so not found at {path}: build it first "
+                    "(python -m paged_kv_extend_gb300.build)")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _check(rc: int):
+    if rc != PKX_OK:
+        msg = load_library().pkx_last_error_string().decode(errors="replace")
+        raise PkxError(rc, msg)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(dev: torch.device):
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _rows(t: torch.Tensor, name: str):
+    if t.dim() != 3 or t.stride(2) != 1:
+        raise ValueError(f"{name} must be [n, heads, dim] with a contiguous last dim")
+    if t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA bf16 tensor")
+    return t.stride(0), t.stride(1)
+
+
+def _i32(t: torch.Tensor, name: str):
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
+    return t
+
+
+def version() -> str:
+    return load_library().pkx_version().decode()
+
+
+def extend_workspace_size(batch, num_q_tokens, hq, hkv, lq, lv) -> int:
+    return int(load_library().pkx_extend_workspace_size(batch, num_q_tokens, hq, hkv, lq, lv))
+
+
+def decode_workspace_size(batch, hq, hkv, lq, lv) -> int:
+    return int(load_library().pkx_decode_workspace_size(batch, hq, hkv, lq, lv))
+
+
+def workspace_status(workspace: torch.Tensor) -> int:
+    """Status word of the last attention call that used ``workspace``
+    (synchronises the current stream).  Returns the code; does not raise."""
+    return int(load_library().pkx_workspace_status(_ptr(workspace), _stream(workspace.device)))
+
+
+def set_attention_events(before=None, after=None):
+    """Record CUDA events ``before``/``after`` (torch.cuda.Event, already
+    recorded once so that they exist) around the attention kernel of every
+    later attention call on this thread; ``None, None`` stops."""
+    load_library().pkx_set_attention_events(
+        None if before is None else before.cuda_event,
+        None if after is None else after.cuda_event)
+
+
+def _workspace(ws, nbytes, dev):
+    """The caller's workspace (its size is checked by the library), or a new
+    one of the size the library asks for."""
+    if ws is None:
+        return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    return ws
+
+
+def extend_attention_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffer,
+                         qo_indptr, kv_indptr, kv_indices, sm_scale=None, logit_cap=0.0,
+                         sliding_window=-1, lse=None, workspace=None):
+    """Two-stage extend attention (pkx_extend_attention_fwd); writes o_extend
+    (and lse if given) in place.  Returns the workspace used."""
+    lib = load_library()
+    n, hq, lq = q_extend.shape
+    hkv = k_buffer.shape[1]
+    lv = v_buffer.shape[2]
+    batch = qo_indptr.numel() - 1
+    ke = _rows(k_extend, "k_extend")
+    ve = _rows(v_extend, "v_extend")
+    kb = _rows(k_buffer, "k_buffer")
+    vb = _rows(v_buffer, "v_buffer")
+    for t, nm in ((q_extend, "q_extend"), (o_extend, "o_extend")):
+        if not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{nm} must be contiguous bf16")
+    _i32(qo_indptr, "qo_indptr"), _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
+    ws = _workspace(workspace, extend_workspace_size(batch, n, hq, hkv, lq, lv), q_extend.device)
+    _check(lib.pkx_extend_attention_fwd(
+        _ptr(q_extend), _ptr(k_extend), _ptr(v_extend), _ptr(o_extend), _ptr(k_buffer),
+        _ptr(v_buffer), _ptr(qo_indptr), _ptr(kv_indptr),
+        _ptr(kv_indices) if kv_indices.numel() else None, batch, n, hq, hkv, lq, lv,
+        ke[0], ke[1], ve[0], ve[1], kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0],
+        float(sm_scale or 0.0), float(logit_cap or 0.0), int(sliding_window), _ptr(lse),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(q_extend.device)))
+    return ws
+
+
+def extend_attention_fwd_unified(q, o, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices,
+                                 prefix_lens, sm_scale=None, logit_cap=0.0, sliding_window=-1,
+                                 lse=None, workspace=None):
+    """Unified extend attention (pkx_extend_attention_fwd_unified); int64
+    kv_indices over every key.  Writes o (and lse) in place."""
+    lib = load_library()
+    n, hq, lq = q.shape
+    hkv = k_buffer.shape[1]
+    lv = v_buffer.shape[2]
+    batch = qo_indptr.numel() - 1
+    kb = _rows(k_buffer, "k_buffer")
+    vb = _rows(v_buffer, "v_buffer")
+    if kv_indices.dtype != torch.int64 or not kv_indices.is_contiguous():
+        raise ValueError("kv_indices must be contiguous int64")
+    _i32(qo_indptr, "qo_indptr"), _i32(kv_indptr, "kv_indptr"), _i32(prefix_lens, "prefix_lens")
+    ws = _workspace(workspace, extend_workspace_size(batch, n, hq, hkv, lq, lv), q.device)
+    _check(lib.pkx_extend_attention_fwd_unified(
+        _ptr(q), _ptr(o), _ptr(k_buffer), _ptr(v_buffer), _ptr(qo_indptr), _ptr(kv_indptr),
+        _ptr(kv_indices) if kv_indices.numel() else None, _ptr(prefix_lens), batch, n, hq, hkv,
+        lq, lv, kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0], float(sm_scale or 0.0),
+        float(logit_cap or 0.0), int(sliding_window), _ptr(lse), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(q.device)))
+    return ws
+
+
+def decode_attention_fwd(q, o, k_buffer, v_buffer, kv_indptr, kv_indices, sm_scale=None,
+                         logit_cap=0.0, sliding_window=-1, lse=None, workspace=None):
+    """Decode attention (pkx_decode_attention_fwd): q [B, Hq, Lq] -> o."""
+    lib = load_library()
+    b, hq, lq = q.shape
+    hkv = k_buffer.shape[1]
+    lv = v_buffer.shape[2]
+    kb = _rows(k_buffer, "k_buffer")
+    vb = _rows(v_buffer, "v_buffer")
+    _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
+    ws = _workspace(workspace, decode_workspace_size(b, hq, hkv, lq, lv), q.device)
+    _check(lib.pkx_decode_attention_fwd(
+        _ptr(q), _ptr(o), _ptr(k_buffer), _ptr(v_buffer), _ptr(kv_indptr),
+        _ptr(kv_indices) if kv_indices.numel() else None, b, hq, hkv, lq, lv,
+        kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0], float(sm_scale or 0.0),
+        float(logit_cap or 0.0), int(sliding_window), _ptr(lse), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(q.device)))
+    return ws
+
+
+def merge_state(v_a, s_a, v_b, s_b, v_out=None, s_out=None):
+    """merge_state (pkx_merge_state).  Returns (v_out, s_out)."""
+    lib = load_library()
+    n, h, dv = v_a.shape
+    if v_out is None:
+        v_out = torch.empty_like(v_a)
+    if s_out is None:
+        s_out = torch.empty_like(s_a)
+    for t in (v_a, v_b, v_out):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("v tensors must be contiguous bf16")
+    for t in (s_a, s_b, s_out):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("s tensors must be contiguous fp32")
+    _check(lib.pkx_merge_state(_ptr(v_a), _ptr(s_a), _ptr(v_b), _ptr(s_b), _ptr(v_out),
+                               _ptr(s_out), n, h, dv, _stream(v_a.device)))
+    return v_out, s_out
+
+
+def build_unified_kv_indices(prefix_kv_indptr, prefix_kv_indices, extend_start_loc,
+                             extend_seq_lens, extend_kv_indices, bs, out=None):
+    """Unified KV-index build (pkx_build_unified_kv_indices).  Returns
+    (unified_kv_indptr int32 [bs+1], unified_kv_indices int64, prefix_lens
+    int32 [bs]); pass ``out`` = that triple to write into existing tensors."""
+    lib = load_library()
+    dev = prefix_kv_indptr.device
+    for t, nm in ((prefix_kv_indptr, "prefix_kv_indptr"), (prefix_kv_indices, "prefix_kv_indices"),
+                  (extend_start_loc, "extend_start_loc"), (extend_seq_lens, "extend_seq_lens"),
+                  (extend_kv_indices, "extend_kv_indices")):
+        _i32(t, nm)
+    if out is None:
+        uptr = torch.empty(bs + 1, dtype=torch.int32, device=dev)
+        uidx = torch.empty(prefix_kv_indices.numel() + extend_kv_indices.numel(),
+                           dtype=torch.int64, device=dev)
+        plen = torch.empty(bs, dtype=torch.int32, device=dev)
+    else:
+        uptr, uidx, plen = out
+    _check(lib.pkx_build_unified_kv_indices(
+        _ptr(prefix_kv_indptr), _ptr(prefix_kv_indices) if prefix_kv_indices.numel() else None,
+        _ptr(extend_start_loc), _ptr(extend_seq_lens),
+        _ptr(extend_kv_indices) if extend_kv_indices.numel() else None, int(bs), _ptr(uptr),
+        _ptr(uidx) if uidx.numel() else None, _ptr(plen), _stream(dev)))
+    return uptr, uidx, plen

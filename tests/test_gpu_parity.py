@@ -1,0 +1,287 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the float64
+oracle on the same seeded inputs.
+
+Bar: unified indices bit-exact; bf16 attention outputs within max|err| 2e-2
+and mean|err| 2e-3, fp32 lse within 1e-3 (tests/gpu_cases.py).
+"""
+import json
+import math
+import os
+
+import pytest
+import torch
+
+import oracle
+from paged_kv_extend_gb300 import pkx
+from paged_kv_extend_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from gpu_cases import (DEV, DeviceWorkload, assert_close, oracle_decode, oracle_extend,
+                           sample_rows)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkx.load_library()
+
+
+# --------------------------------------------------------- unified indices
+def _unified_gpu(pptr, pidx, start, elen, eidx, bs, fill=-5):
+    d = lambda t: t.to(DEV)
+    uptr = torch.full((bs + 1,), fill, dtype=torch.int32, device=DEV)
+    uidx = torch.full((pidx.numel() + eidx.numel(),), fill, dtype=torch.int64, device=DEV)
+    plen = torch.full((bs,), fill, dtype=torch.int32, device=DEV)
+    pkx.build_unified_kv_indices(d(pptr.to(torch.int32)), d(pidx), d(start), d(elen), d(eidx), bs,
+                                 out=(uptr, uidx, plen))
+    torch.cuda.synchronize()
+    return uptr.cpu(), uidx.cpu(), plen.cpu()
+
+
+def test_unified_indices_hand_fixture_bit_exact():
+    fx = json.load(open(os.path.join(GOLDEN, "unified_indices_hand.json")))
+    i, e = fx["inputs"], fx["expected"]
+    t = lambda k: torch.tensor(i[k], dtype=torch.int32)
+    uptr, uidx, plen = _unified_gpu(t("prefix_kv_indptr"), t("prefix_kv_indices"),
+                                    t("extend_start_loc"), t("extend_seq_lens"),
+                                    t("extend_kv_indices"), i["bs"])
+    n = e["unified_kv_indptr"][-1]
+    assert uptr.tolist() == e["unified_kv_indptr"]
+    assert uidx[:n].tolist() == e["unified_kv_indices_prefix"]
+    assert torch.all(uidx[n:] == -5)
+    assert plen.tolist() == e["prefix_lens"]
+
+
+@pytest.mark.parametrize("seed,bs", [(0, 1), (1, 7), (2, 64), (3, 300)])
+def test_unified_indices_bit_exact_vs_oracle(seed, bs):
+    g = torch.Generator().manual_seed(seed)
+    plens = torch.randint(0, 700, (bs,), generator=g)
+    plens[torch.rand(bs, generator=g) < 0.2] = 0
+    elens = torch.randint(0, 300, (bs,), generator=g).to(torch.int32)
+    pptr = torch.zeros(bs + 1, dtype=torch.int32)
+    pptr[1:] = torch.cumsum(plens, 0)
+    pidx = torch.randint(0, 2**31 - 1, (int(plens.sum()),), generator=g, dtype=torch.int32)
+    perm = torch.randperm(bs, generator=g)
+    start = torch.zeros(bs, dtype=torch.int32)
+    pos = 0
+    for b in perm.tolist():
+        pos += int(torch.randint(0, 3, (1,), generator=g))
+        start[b] = pos
+        pos += int(elens[b])
+    eidx = torch.randint(0, 2**31 - 1, (pos + 2,), generator=g, dtype=torch.int32)
+    uptr, uidx, plen = _unified_gpu(pptr, pidx, start, elens, eidx, bs)
+    rptr, ridx, rplen = oracle.build_unified_kv_indices(pptr, pidx, start, elens, eidx, bs, fill=-5)
+    assert torch.equal(uptr, rptr)
+    assert torch.equal(uidx, ridx)   # includes the untouched tail
+    assert torch.equal(plen, rplen)
+
+
+def test_unified_indices_empty_batch():
+    uptr, uidx, plen = _unified_gpu(torch.zeros(1, dtype=torch.int32), torch.zeros(0, dtype=torch.int32),
+                                    torch.zeros(0, dtype=torch.int32), torch.zeros(0, dtype=torch.int32),
+                                    torch.zeros(0, dtype=torch.int32), 0)
+    assert uptr.tolist() == [0]
+
+
+# ---------------------------------------------------------------- merge_state
+@pytest.mark.parametrize("n,h,dv", [(1, 1, 8), (37, 8, 128), (1000, 16, 512), (5, 3, 64)])
+def test_merge_state_vs_oracle(n, h, dv):
+    g = torch.Generator().manual_seed(n * 31 + dv)
+    va = torch.randn(n, h, dv, generator=g).to(torch.bfloat16)
+    vb = torch.randn(n, h, dv, generator=g).to(torch.bfloat16)
+    sa = torch.randn(n, h, generator=g) * 8
+    sb = torch.randn(n, h, generator=g) * 8
+    # empty sides
+    sa.view(-1)[::7] = float("-inf")
+    sb.view(-1)[::11] = float("-inf")
+    v, s = pkx.merge_state(va.to(DEV), sa.to(DEV), vb.to(DEV), sb.to(DEV))
+    torch.cuda.synchronize()
+    rv, rs = oracle.merge_state(va, sa, vb, sb)
+    err = (v.double().cpu() - rv).abs()
+    assert err.max().item() <= 2e-2 and err.mean().item() <= 2e-3
+    fin = torch.isfinite(rs)
+    assert torch.equal(torch.isfinite(s.cpu()), fin)
+    assert (s.double().cpu()[fin] - rs[fin]).abs().max().item() <= 1e-5 if fin.any() else True
+
+
+def test_merge_state_in_place():
+    g = torch.Generator().manual_seed(5)
+    va = torch.randn(64, 4, 128, generator=g).to(torch.bfloat16)
+    vb = torch.randn(64, 4, 128, generator=g).to(torch.bfloat16)
+    sa, sb = torch.randn(64, 4, generator=g), torch.randn(64, 4, generator=g)
+    rv, rs = oracle.merge_state(va, sa, vb, sb)
+    a, s_a = va.to(DEV), sa.to(DEV)
+    pkx.merge_state(a, s_a, vb.to(DEV), sb.to(DEV), v_out=a, s_out=s_a)
+    torch.cuda.synchronize()
+    assert (a.double().cpu() - rv).abs().max().item() <= 2e-2
+    assert (s_a.double().cpu() - rs).abs().max().item() <= 1e-5
+
+
+# ------------------------------------------------------------ extend attention
+def test_tiny_config():
+    """The tiny correctness workload: B=2, Hq=4, Hkv=2, D=64, prefix {16,0},
+    extend {8,5}, 64 shuffled slots, scale 1/8."""
+    wl = W.draw(W.SPECS["tiny"])
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.extend()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_extend(wl)
+    assert_close(o, lse, ro, rl, "tiny")
+
+
+SMALL = [
+    # (lq, hq, hkv, prefix, extend, cap, window)
+    (128, 32, 8, [0, 5, 300, 1000], [1, 40, 77, 130], 0.0, -1),
+    (128, 32, 8, [17, 0, 2000], [129, 3, 64], 30.0, -1),
+    (128, 28, 4, [600, 0, 90, 3000], [200, 1, 19, 5], 0.0, 100),
+    (128, 8, 8, [40, 1300], [70, 33], 0.0, -1),
+    (128, 16, 1, [250, 7], [9, 260], 5.0, 31),
+    (64, 4, 2, [16, 0], [8, 5], 0.0, -1),
+    (64, 12, 3, [0, 999, 45], [500, 2, 129], 0.0, 250),
+    (64, 64, 4, [128, 1], [16, 256], 12.0, -1),
+    (128, 32, 8, [0, 0, 0], [0, 5, 0], 0.0, -1),   # empty sequences around one
+]
+
+
+@pytest.mark.parametrize("lq,hq,hkv,prefix,extend,cap,window", SMALL)
+def test_extend_small_vs_oracle(lq, hq, hkv, prefix, extend, cap, window):
+    spec = W.small_spec(batch=len(prefix), hq=hq, hkv=hkv, lq=lq, lv=lq, prefix=prefix,
+                        extend=extend, logit_cap=cap, sliding_window=window,
+                        seed=sum(prefix) + 3 * sum(extend) + hq)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.extend()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_extend(wl)
+    assert_close(o, lse, ro, rl, f"extend {lq} {hq}/{hkv}")
+    # unified form on the same data gives the same answer
+    uo, ul, ws2 = dw.unified()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws2) == 0
+    assert_close(uo, ul, ro, rl, "unified")
+
+
+def test_repeat_calls_are_bitwise_identical():
+    wl = W.draw(W.small_spec(batch=3, hq=32, hkv=8, prefix=[700, 30, 0], extend=[90, 300, 17], seed=4))
+    dw = DeviceWorkload(wl)
+    o1, l1, ws = dw.extend()
+    o2, l2, _ = dw.extend()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_no_lse_output_is_fine():
+    wl = W.draw(W.small_spec(batch=2, hq=8, hkv=2, prefix=[10, 600], extend=[20, 40], seed=9))
+    dw = DeviceWorkload(wl)
+    o, _ = dw.out()
+    pkx.extend_attention_fwd(dw.q, dw.k_extend, dw.v_extend, o, dw.k_buffer, dw.v_buffer,
+                             dw.qo_indptr, dw.kv_indptr, dw.kv_indices, wl.sm_scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle_extend(wl)
+    assert_close(o, rl.float(), ro, rl, "no lse")
+
+
+# --------------------------------------------------------------------- decode
+@pytest.mark.parametrize("lq,hq,hkv,lens,cap,window", [
+    (128, 32, 8, [1, 2, 130, 4000, 777], 0.0, -1),
+    (128, 32, 8, [300, 1, 9000], 30.0, 64),
+    (64, 16, 16, [5, 1000], 0.0, -1),
+    (128, 16, 1, [513, 2], 0.0, -1),
+])
+def test_decode_small_vs_oracle(lq, hq, hkv, lens, cap, window):
+    spec = W.WorkloadSpec("dec", batch=len(lens), hq=hq, hkv=hkv, lq=lq, lv=lq,
+                          prefix=[x - 1 for x in lens], extend=[1] * len(lens),
+                          num_slots=2 * sum(lens) + 16, logit_cap=cap, sliding_window=window,
+                          seed=sum(lens), decode=True)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.decode()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_decode(wl)
+    assert_close(o, lse, ro, rl, "decode")
+
+
+def test_decode_padding_sequence_gives_zero():
+    """A padded decode slot (T = 0, as CUDA-graph padding produces) yields
+    o = 0 and lse = -inf and leaves its neighbours alone."""
+    spec = W.WorkloadSpec("dec", batch=3, hq=8, hkv=2, lq=128, lv=128, prefix=[50, 0, 9],
+                          extend=[1, 1, 1], num_slots=256, seed=3, decode=True)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    kvp = torch.tensor([0, 51, 51, 61], dtype=torch.int32)
+    idx = torch.cat([wl.kv_indices[:51], wl.kv_indices[52:62]])
+    dw.kv_indptr, dw.kv_indices = kvp.to(DEV), idx.to(DEV)
+    o, lse, _ = dw.decode()
+    torch.cuda.synchronize()
+    kb, vb = wl.pool()
+    ro, rl = oracle.decode_attention(wl.q, kb, vb, kvp, idx, wl.sm_scale)
+    assert torch.all(o[1].cpu() == 0) and torch.all(torch.isneginf(lse[1].cpu()))
+    assert_close(o, lse, ro, rl, "decode padding")
+
+
+# ------------------------------------------------------------- error paths
+def test_out_of_range_index_is_reported_not_dereferenced():
+    wl = W.draw(W.small_spec(batch=2, hq=8, hkv=2, prefix=[40, 9], extend=[5, 7], seed=12))
+    dw = DeviceWorkload(wl)
+    bad = dw.kv_indices.clone()
+    bad[3] = wl.spec.num_slots + 1000
+    bad[7] = -4
+    dw.kv_indices = bad
+    o, lse, ws = dw.extend()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == pkx.PKX_EDEVICE
+    assert torch.isfinite(o.float()).all()
+    # the next good call clears the status word
+    dw.kv_indices = wl.kv_indices.to(DEV)
+    o, lse, ws = dw.extend()
+    assert pkx.workspace_status(ws) == pkx.PKX_OK
+
+
+def test_workspace_too_small_is_rejected():
+    wl = W.draw(W.small_spec(batch=1, hq=8, hkv=2, prefix=[4], extend=[4], seed=1))
+    dw = DeviceWorkload(wl)
+    o, lse = dw.out()
+    ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(pkx.PkxError) as e:
+        pkx.extend_attention_fwd(dw.q, dw.k_extend, dw.v_extend, o, dw.k_buffer, dw.v_buffer,
+                                 dw.qo_indptr, dw.kv_indptr, dw.kv_indices, wl.sm_scale,
+                                 lse=lse, workspace=ws)
+    assert e.value.code == pkx.PKX_EWORKSPACE
+
+
+# ------------------------------------------------- full-size sampled parity
+@pytest.mark.parametrize("name", ["llama3_8b", "long_prefix", "heavy_tail"])
+def test_full_size_sampled_rows(name):
+    """The full-size workloads, in the launch configuration the benchmark
+    times; the oracle computes a seeded sample of (token, head) rows."""
+    wl = W.draw(W.SPECS[name])
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.extend()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    rows = sample_rows(wl.n_q_tokens, wl.spec.hq, 3072, seed=77)
+    ro, rl = oracle_extend(wl, rows=rows)
+    hq = wl.spec.hq
+    go = o.view(-1, o.shape[-1])[rows.to(DEV)]
+    gl = lse.view(-1)[rows.to(DEV)]
+    assert_close(go, gl, ro, rl, name)
+    assert torch.isfinite(o.float()).all()
+    del dw
+
+
+def test_full_size_decode():
+    wl = W.draw(W.SPECS["decode_gqa"])
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.decode()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_decode(wl)
+    assert_close(o, lse, ro, rl, "decode_gqa")
