@@ -177,6 +177,28 @@ int pkx_decode_attention_fwd(
     size_t workspace_bytes, void *stream);
 
 /*
+ * Decode attention without a workspace argument, for callers that cannot
+ * allocate device memory: a plugin whose host framework owns every device
+ * allocation and offers it no allocator, or a latency-critical decode loop
+ * that must not call cudaMalloc (which synchronises the device).  The pages
+ * have no counterpart to this call; it is this library's own addition.
+ * Same arguments and results as pkx_decode_attention_fwd minus
+ * workspace/workspace_bytes.  Its scratch is a fixed 96 MiB device array
+ * inside the library that every GPU loading the library holds until exit.
+ * The first call on each device looks up that array's address (make it
+ * before any stream capture).  Calls share the array: calls that overlap on
+ * the GPU race and must be serialised.  A problem whose scratch
+ * (pkx_decode_workspace_size) exceeds 96 MiB returns PKX_EWORKSPACE before
+ * anything is enqueued.  Nothing is allocated.
+ */
+int pkx_decode_attention_fwd_no_alloc(
+    const void *q, void *o, const void *k_buffer, const void *v_buffer,
+    const int32_t *kv_indptr, const int32_t *kv_indices, int batch, int hq,
+    int hkv, int lq, int lv, int64_t kb_ss, int64_t kb_sh, int64_t vb_ss,
+    int64_t vb_sh, int64_t num_slots, float sm_scale, float logit_cap,
+    int sliding_window, float *lse_out, void *stream);
+
+/*
  * merge_state.
  * Source: sglang flashinfer_backend.py, forward_extend (the ragged causal
  * extend result and the non-causal paged prefix result, each with its

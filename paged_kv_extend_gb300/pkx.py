@@ -55,6 +55,9 @@ _SIGS = {
     "pkx_decode_attention_fwd": (_i, [
         _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i,
         _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _sz, _p]),
+    "pkx_decode_attention_fwd_no_alloc": (_i, [
+        _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i,
+        _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p]),
     "pkx_merge_state": (_i, [_p, _p, _p, _p, _p, _p, _i64, _i, _i, _p]),
     "pkx_build_unified_kv_indices": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _p, _p]),
 }
@@ -214,6 +217,25 @@ def decode_attention_fwd(q, o, k_buffer, v_buffer, kv_indptr, kv_indices, sm_sca
         float(logit_cap or 0.0), int(sliding_window), _ptr(lse), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(q.device)))
     return ws
+
+
+def decode_attention_fwd_no_alloc(q, o, k_buffer, v_buffer, kv_indptr, kv_indices,
+                                  sm_scale=None, logit_cap=0.0, sliding_window=-1, lse=None):
+    """Decode attention with the library's built-in scratch instead of a
+    workspace (pkx_decode_attention_fwd_no_alloc), for callers that cannot
+    allocate device memory.  Calls that overlap on the GPU must not be made."""
+    lib = load_library()
+    b, hq, lq = q.shape
+    hkv = k_buffer.shape[1]
+    lv = v_buffer.shape[2]
+    kb = _rows(k_buffer, "k_buffer")
+    vb = _rows(v_buffer, "v_buffer")
+    _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
+    _check(lib.pkx_decode_attention_fwd_no_alloc(
+        _ptr(q), _ptr(o), _ptr(k_buffer), _ptr(v_buffer), _ptr(kv_indptr),
+        _ptr(kv_indices) if kv_indices.numel() else None, b, hq, hkv, lq, lv,
+        kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0], float(sm_scale or 0.0),
+        float(logit_cap or 0.0), int(sliding_window), _ptr(lse), _stream(q.device)))
 
 
 def merge_state(v_a, s_a, v_b, s_b, v_out=None, s_out=None):
