@@ -697,8 +697,26 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1) attn_kernel(const KParams
         const int kb = w.k_begin + j * C::BN;
         const uint32_t sK = sbase + C::OFF_K + stage * C::K_BYTES;
         const uint32_t sV = sbase + C::OFF_V + stage * C::V_BYTES;
-#pragma unroll 4
-        for (int key = row0; key < C::BN; key += KPP) {
+        // All of this thread's slot indices first (independent loads in
+        // flight together), then the row copies.
+        constexpr int NK = (C::BN + KPP - 1) / KPP;
+        int64_t slot[NK];
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+          const int key = row0 + i * KPP;
+          const int jpos = kb + key;
+          slot[i] = -1;
+          if (key < C::BN && jpos < w.k_end && !(MODE == kTwoStage && jpos >= P_pool)) {
+            if (MODE == kUnified)
+              slot[i] = __ldg(static_cast<const int64_t *>(p.kv_indices) + kv_base + jpos);
+            else
+              slot[i] = __ldg(static_cast<const int32_t *>(p.kv_indices) + kv_base + jpos);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+          const int key = row0 + i * KPP;
+          if (key >= C::BN) break;
           const int jpos = kb + key;
           bool v = jpos < w.k_end;
           const bf16 *krow = p.k_buf, *vrow = p.v_buf;
@@ -707,19 +725,12 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1) attn_kernel(const KParams
               const int64_t te = ext_base + (jpos - P_pool);
               krow = p.k_ext + te * p.ke_st + (int64_t)w.kvh * p.ke_sh;
               vrow = p.v_ext + te * p.ve_st + (int64_t)w.kvh * p.ve_sh;
+            } else if (slot[i] < 0 || slot[i] >= p.num_slots) {
+              record_status(p.status, PKX_EDEVICE);
+              v = false;
             } else {
-              int64_t slot;
-              if (MODE == kUnified)
-                slot = static_cast<const int64_t *>(p.kv_indices)[kv_base + jpos];
-              else
-                slot = static_cast<const int32_t *>(p.kv_indices)[kv_base + jpos];
-              if (slot < 0 || slot >= p.num_slots) {
-                record_status(p.status, PKX_EDEVICE);
-                v = false;
-              } else {
-                krow = p.k_buf + slot * p.kb_ss + (int64_t)w.kvh * p.kb_sh;
-                vrow = p.v_buf + slot * p.vb_ss + (int64_t)w.kvh * p.vb_sh;
-              }
+              krow = p.k_buf + slot[i] * p.kb_ss + (int64_t)w.kvh * p.kb_sh;
+              vrow = p.v_buf + slot[i] * p.vb_ss + (int64_t)w.kvh * p.vb_sh;
             }
           }
           const uint32_t off = (ch >> 3) * (C::BN * 128) + sw128_off(key, ch & 7);
