@@ -74,11 +74,13 @@ size_t pkx_extend_workspace_size(int batch, int num_q_tokens, int hq, int hkv, i
       lv <= 0)
     return 0;
   (void)lq;
-  return ws_layout(batch, num_q_tokens, hkv, hq / hkv, lv, num_sms_current_device()).total;
+  return ws_layout(batch, num_q_tokens, hkv, hq / hkv, lv, num_sms_current_device(), false).total;
 }
 
 size_t pkx_decode_workspace_size(int batch, int hq, int hkv, int lq, int lv) {
-  return pkx_extend_workspace_size(batch, batch, hq, hkv, lq, lv);
+  if (batch < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM || lv <= 0) return 0;
+  (void)lq;
+  return ws_layout(batch, batch, hkv, hq / hkv, lv, num_sms_current_device(), true).total;
 }
 
 int pkx_workspace_status(const void *workspace, void *stream) {

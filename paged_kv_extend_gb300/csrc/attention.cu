@@ -1,6 +1,6 @@
 // attention.cu -- extend and decode attention over a page-size-1 KV pool for
 // sm_103a: a device-side work scheduler, a warp-specialised tcgen05/TMEM
-// attention kernel with a cp.async paged gather, and the split-KV combine.
+// attention kernel fed by TMA gathers, and the split-KV combine.
 //
 // Method (sglang extend_attention.py, _fwd_kernel_unified and
 // extend_attention_fwd; flashinfer_backend.py, forward_decode):
@@ -12,20 +12,31 @@
 //
 // GB300 design (differs from the pages' Triton kernel, which launches one
 // program per (sequence, q head, 128-row block) and re-reads K/V per q head):
-//  * one tile = 128 rows = (tokens x the Hq/Hkv query heads of one KV head),
-//    so K/V of a KV head are gathered once for all of its query heads;
-//  * QK^T and PV are tcgen05.mma (M=128, bf16 in, fp32 accumulate in TMEM);
-//    S is double-buffered in TMEM so the tensor core computes S_{j+1} while
-//    the softmax warps work on S_j;
+//  * a Q tile = 128 rows = (tokens x the Hq/Hkv query heads of one KV head),
+//    and a CTA runs two Q tiles of consecutive tokens against each K/V tile:
+//    K/V of a KV head are gathered once for 2 x 128 query rows;
+//  * K and V tiles are gathered from the pool by TMA (tile::gather4, four
+//    pool rows per instruction, 128-byte swizzle) into two smem rings; one
+//    warp issues them, completion is counted in bytes on mbarriers;
+//  * QK^T and PV are tcgen05.mma (M=128, bf16 in, fp32 accumulate in TMEM).
+//    TMEM holds S and O of both Q tiles (4 x 128 columns).  The softmax
+//    warpgroup of a tile writes P (bf16) back over its S columns and PV
+//    reads A = P straight from TMEM.  While one warpgroup runs its softmax,
+//    the tensor core runs the other tile's PV and QK^T;
 //  * the KV loop stops at the causal diagonal and starts at the window edge
 //    (the Triton kernel walks every tile and masks);
 //  * a device-built work list (no host sync, graph-safe) splits long key
-//    ranges across CTAs (split-KV) and a combine kernel merges the partial
+//    ranges across CTAs (split-KV); a combine kernel merges the partial
 //    (o, lse) pairs with the merge_state formula;
 //  * a persistent grid of one CTA per SM walks the work list.
+#include <algorithm>
+#include <climits>
 #include <cstdio>
+#include <cstring>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "pkx_internal.h"
 #include "ptx.cuh"
@@ -103,6 +114,15 @@ __device__ __forceinline__ void qblock_range(const SchedParams &p, const SeqDims
   if (hi < lo) hi = lo;
 }
 
+// Number of K/V tiles of the key range [kb, ke) when tiles may not straddle
+// `split` (the prefix / extend boundary of the two-stage form).
+__device__ __forceinline__ int range_tiles(int kb, int ke, int split) {
+  const int pe = min(ke, split), eb = max(kb, split);
+  const int n_pre = pe > kb ? (pe - kb + kBlockN - 1) / kBlockN : 0;
+  const int n_ext = ke > eb ? (ke - eb + kBlockN - 1) / kBlockN : 0;
+  return n_pre + n_ext;
+}
+
 // Exclusive scan of in[0..n) into out[0..n) by the whole 1024-thread block;
 // returns the total.  in and out may alias.
 __device__ int block_exclusive_scan(const int32_t *in, int32_t *out, int n, int *sh) {
@@ -176,8 +196,6 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     my_tiles += w;
   }
   __syncthreads();
-  // block reduce of the tile count (as 64-bit via two 32-bit halves is
-  // unnecessary: tiles of any sane problem fit in 31 bits)
   sh[tid] = (int)min(my_tiles, (long long)0x3fffffff);
   __syncthreads();
   for (int off = 512; off > 0; off >>= 1) {
@@ -247,6 +265,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   for (int rk = tid; rk < B; rk += 1024) {
     const int b = order[rk];
     SeqDims d = seq_dims(p, b);
+    const int split_at = p.mode == kTwoStage ? d.P : INT_MAX;
     int uo = ucnt[rk], so = scnt[rk], co = ccnt[rk];
     for (int kvh = 0; kvh < p.hkv; ++kvh) {
       for (int qb = d.nqb - 1; qb >= 0; --qb) {
@@ -273,8 +292,11 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
           w.kvh = kvh;
           w.k_begin = min(hi, lo + s * tps * kBlockN);
           w.k_end = min(hi, lo + (s + 1) * tps * kBlockN);
+          w.k_split = split_at;
+          w.n_tiles = range_tiles(w.k_begin, w.k_end, split_at);
           w.b = b;
           w.slot = S > 1 ? so + s : -1;
+          w.pad[0] = w.pad[1] = 0;
           p.units[uo++] = w;
         }
         if (S > 1) so += S;
@@ -289,17 +311,13 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
 
 // ============================================================ attention ====
 struct KParams {
-  const bf16 *q;
   bf16 *o;
   float *lse;
-  const bf16 *k_ext, *v_ext;
-  int64_t ke_st, ke_sh, ve_st, ve_sh;
-  const bf16 *k_buf, *v_buf;
-  int64_t kb_ss, kb_sh, vb_ss, vb_sh;
+  int64_t kb_sh, vb_sh, ke_sh, ve_sh;  // head strides (elements) of the maps' rows
   int64_t num_slots;
   const int32_t *qo_indptr, *kv_indptr;
   const void *kv_indices;
-  int hq, group, window, use_cap;
+  int hq, group, tok, q_box_tok, window, use_cap, rows_per_slot;
   float scale_log2;  // sm_scale * log2(e)           (no cap)
   float cap_pre;     // sm_scale / cap                (cap)
   float cap_log2;    // cap * log2(e)                 (cap)
@@ -309,44 +327,55 @@ struct KParams {
   float *plse, *po;
 };
 
+// TMA descriptors: q (3-D: dim, head, token), K/V pool rows (2-D: element of
+// a slot row, slot) and K/V extend rows (2-D: element of a token row, token).
+struct TMaps {
+  CUtensorMap q, kp, vp, ke, ve;
+};
+
 template <int HD>
 struct Cfg {
   static constexpr int BM = kBlockM, BN = kBlockN, HDV = HD;
-  static constexpr int NS = HD == 128 ? 2 : 4;  // K/V pipeline stages
-  static constexpr int Q_BYTES = BM * HD * 2;
+  static constexpr int NK = HD == 128 ? 3 : 6;  // K ring stages
+  static constexpr int NV = HD == 128 ? 2 : 6;  // V ring stages
+  static constexpr int Q_BYTES = BM * HD * 2;   // one Q tile
   static constexpr int K_BYTES = BN * HD * 2;
   static constexpr int V_BYTES = BN * HDV * 2;
-  static constexpr int P_BYTES = BM * BN * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + NS * K_BYTES;
-  static constexpr int OFF_P = OFF_V + NS * V_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  static constexpr int N_BARS = 8 + 2 * NS;
+  static constexpr int OFF_Q = 0;  // two Q tiles
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * K_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NV * V_BYTES;
+  static constexpr int N_BARS = 16 + 2 * NK + 2 * NV;
   static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 1024;  // + alignment slack
-  static constexpr int S_COL = 0;       // two S buffers: columns 0 and 128
-  static constexpr int O_COL = 2 * BN;  // O accumulator
-  static constexpr int TMEM_COLS = 512;
+  static constexpr int TMEM_COLS = 512;  // S0 | S1 | O0 | O1, 128 columns each
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HDV, 1);
-  static constexpr int THREADS = 256;  // 4 softmax warps, 1 MMA warp, 3 load warps
-  static constexpr int LOAD_THREADS = 96;
+  static constexpr int THREADS = 320;  // 2 softmax warpgroups, MMA warp, TMA warp
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 // barrier indices
 enum {
   B_Q_FULL = 0,
   B_Q_EMPTY = 1,
-  B_S_FULL0 = 2,
-  B_S_FULL1 = 3,
-  B_P_FULL = 4,
-  B_O_DONE = 5,
-  B_FINAL = 6,
-  B_KV_FULL = 8,  // + stage
+  B_S_FULL = 2,  // + Q tile
+  B_P_FULL = 4,  // + Q tile
+  B_O_DONE = 6,  // + Q tile
+  B_FINAL = 8,
+  B_RING = 16,  // K full[NK], K empty[NK], V full[NV], V empty[NV]
 };
 
-__device__ __forceinline__ int unit_tiles(const WorkUnit &w) {
-  return w.k_end > w.k_begin ? (w.k_end - w.k_begin + kBlockN - 1) / kBlockN : 0;
+// Key range [kb, ke) of tile j of a unit (tiles never straddle k_split).
+__device__ __forceinline__ void tile_keys(const WorkUnit &w, int j, int &kb, int &ke) {
+  const int pe = min(w.k_end, w.k_split);
+  const int n_pre = pe > w.k_begin ? (pe - w.k_begin + kBlockN - 1) / kBlockN : 0;
+  if (j < n_pre) {
+    kb = w.k_begin + j * kBlockN;
+    ke = min(kb + kBlockN, pe);
+  } else {
+    kb = max(w.k_begin, w.k_split) + (j - n_pre) * kBlockN;
+    ke = min(kb + kBlockN, w.k_end);
+  }
 }
 
 __device__ __forceinline__ void abort_cta(volatile int *abort_flag, int32_t *status, int code) {
@@ -355,7 +384,8 @@ __device__ __forceinline__ void abort_cta(volatile int *abort_flag, int32_t *sta
 }
 
 template <int HD, int MODE>
-__global__ void __launch_bounds__(Cfg<HD>::THREADS, 1) attn_kernel(const KParams p) {
+__global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
+    attn_kernel(const __grid_constant__ TMaps tm, const KParams p) {
   using C = Cfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
@@ -365,29 +395,36 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1) attn_kernel(const KParams
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-  uint64_t *bar_kv_full = bars + B_KV_FULL;
-  uint64_t *bar_kv_empty = bars + B_KV_FULL + C::NS;
+  uint64_t *k_full = bars + B_RING;
+  uint64_t *k_empty = k_full + C::NK;
+  uint64_t *v_full = k_empty + C::NK;
+  uint64_t *v_empty = v_full + C::NV;
   volatile int *abort_flag = &s_abort;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    mbar_init(&bars[B_Q_FULL], C::LOAD_THREADS);
+    mbar_init(&bars[B_Q_FULL], 1);
     mbar_init(&bars[B_Q_EMPTY], 1);
-    mbar_init(&bars[B_S_FULL0], 1);
-    mbar_init(&bars[B_S_FULL1], 1);
-    mbar_init(&bars[B_P_FULL], 128);
-    mbar_init(&bars[B_O_DONE], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[B_S_FULL + i], 1);
+      mbar_init(&bars[B_P_FULL + i], 128);
+      mbar_init(&bars[B_O_DONE + i], 1);
+    }
     mbar_init(&bars[B_FINAL], 1);
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&bar_kv_full[s], C::LOAD_THREADS);
-      mbar_init(&bar_kv_empty[s], 1);
+    for (int s = 0; s < C::NK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < C::NV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     s_abort = 0;
     fence_barrier_init();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     tmem_alloc(&s_tmem, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -396,57 +433,73 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1) attn_kernel(const KParams
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   const int n_units = p.hdr->n_units;
+  const int G = p.group, TOK = p.tok;
 
-  if (warp < 4) {
-    // ------------------------------------------------ softmax + epilogue
-    const int r = tid;  // TMEM lane == tile row
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  if (warp < 8) {
+    // ------------------------------------------- softmax + epilogue (x2)
+    const int wg = warp >> 2;  // Q tile of this warpgroup
+    const int wq = warp & 3;   // TMEM lane quarter
+    const int r = tid & 127;   // tile row == TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t s_col = wg * C::BN;
+    const uint32_t o_col = 2 * C::BN + wg * C::HDV;
     uint32_t s_cnt = 0, o_cnt = 0;
     for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
       const WorkUnit w = p.units[u];
-      const int nt = unit_tiles(w);
-      const int rows_valid = w.n_tok * p.group;
+      const int nt = w.n_tiles;
+      const int tok0 = wg * TOK;  // first token of this Q tile in the block
+      if (wg == 1 && w.n_tok <= TOK) continue;
+      const int n_tok_i = min(TOK, w.n_tok - tok0);
+      const int rows_valid = n_tok_i * G;
       const bool valid = r < rows_valid;
-      const bool warp_active = warp * 32 < rows_valid;
-      const int t = r / p.group, g = r - (r / p.group) * p.group;
+      const bool warp_active = wq * 32 < rows_valid;
+      const int t = tok0 + r / G, g = r - (r / G) * G;
       const int qpos = w.qpos0 + t;
-      const int qpos_max = w.qpos0 + w.n_tok - 1;
+      const int qmin = w.qpos0 + tok0, qmax = w.qpos0 + tok0 + n_tok_i - 1;
+      const int64_t orow_idx = (int64_t)(w.q_tok0 + t) * p.hq + w.kvh * G + g;
+      const int64_t prow_idx = (int64_t)w.slot * p.rows_per_slot + tok0 * G + r;
       if (nt == 0) {
         if (valid) {
           if (w.slot < 0) {
-            bf16 *orow = p.o + ((int64_t)(w.q_tok0 + t) * p.hq + w.kvh * p.group + g) * C::HDV;
+            bf16 *orow = p.o + orow_idx * C::HDV;
             for (int c = 0; c < C::HDV; c += 8)
               *reinterpret_cast<uint4 *>(orow + c) = make_uint4(0, 0, 0, 0);
-            if (p.lse) p.lse[(int64_t)(w.q_tok0 + t) * p.hq + w.kvh * p.group + g] = -INFINITY;
+            if (p.lse) p.lse[orow_idx] = -INFINITY;
           } else {
-            float *prow = p.po + ((int64_t)w.slot * C::BM + r) * C::HDV;
+            float *prow = p.po + prow_idx * C::HDV;
             for (int c = 0; c < C::HDV; c += 4)
               *reinterpret_cast<float4 *>(prow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-            p.plse[(int64_t)w.slot * C::BM + r] = -INFINITY;
+            p.plse[prow_idx] = -INFINITY;
           }
         }
         continue;
       }
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j) {
-        const int kb = w.k_begin + j * C::BN;
-        const uint32_t sb = s_cnt & 1u;
-        if (!mbar_wait(&bars[B_S_FULL0 + sb], (s_cnt >> 1) & 1u, abort_flag)) {
+        int kb, ke;
+        tile_keys(w, j, kb, ke);
+        if (!mbar_wait(&bars[B_S_FULL + wg], s_cnt & 1u, abort_flag)) {
           abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
           break;
         }
         ++s_cnt;
         tc_fence_after();
-        float x[C::BN];
-        float mt = -INFINITY;
         if (warp_active) {
-          uint32_t v[32];
-#pragma unroll
-          for (int c = 0; c < C::BN / 32; ++c) {
-            tmem_ld32(lane_base + C::S_COL + sb * C::BN + c * 32, v);
+          float x[C::BN];
+          {
+            uint32_t v0[32], v1[32], v2[32], v3[32];
+            tmem_ld32(lane_base + s_col + 0, v0);
+            tmem_ld32(lane_base + s_col + 32, v1);
+            tmem_ld32(lane_base + s_col + 64, v2);
+            tmem_ld32(lane_base + s_col + 96, v3);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(v[i]);
+            for (int i = 0; i < 32; ++i) {
+              x[i] = __uint_as_float(v0[i]);
+              x[32 + i] = __uint_as_float(v1[i]);
+              x[64 + i] = __uint_as_float(v2[i]);
+              x[96 + i] = __uint_as_float(v3[i]);
+            }
           }
           if (p.use_cap) {
 #pragma unroll
@@ -455,32 +508,31 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1) attn_kernel(const KParams
 #pragma unroll
             for (int i = 0; i < C::BN; ++i) x[i] *= p.scale_log2;
           }
-          const bool need_mask = (kb + C::BN - 1 > w.qpos0) || (kb + C::BN > w.k_end) ||
-                                 (p.window > 0 && kb < qpos_max - p.window);
+          const bool need_mask = (ke - 1 > qmin) || (ke - kb < C::BN) ||
+                                 (p.window > 0 && kb < qmax - p.window);
           if (need_mask) {
 #pragma unroll
             for (int i = 0; i < C::BN; ++i) {
               const int kpos = kb + i;
-              const bool vis = kpos < w.k_end && kpos <= qpos &&
-                               (p.window <= 0 || qpos - kpos <= p.window);
+              const bool vis =
+                  kpos < ke && kpos <= qpos && (p.window <= 0 || qpos - kpos <= p.window);
               if (!vis) x[i] = -INFINITY;
             }
           }
+          float mt0 = x[0], mt1 = x[1], mt2 = x[2], mt3 = x[3];
 #pragma unroll
-          for (int i = 0; i < C::BN; ++i) mt = fmaxf(mt, x[i]);
-        }
-        if (j > 0) {
-          if (!mbar_wait(&bars[B_O_DONE], o_cnt & 1u, abort_flag)) {
-            abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
-            break;
+          for (int i = 4; i < C::BN; i += 4) {
+            mt0 = fmaxf(mt0, x[i]);
+            mt1 = fmaxf(mt1, x[i + 1]);
+            mt2 = fmaxf(mt2, x[i + 2]);
+            mt3 = fmaxf(mt3, x[i + 3]);
           }
-          ++o_cnt;
-          tc_fence_after();
-        }
-        if (warp_active) {
+          const float mt = fmaxf(fmaxf(mt0, mt1), fmaxf(mt2, mt3));
           const float m_new = fmaxf(m, mt);
           // Rescale only when the max grows by more than 2^8: exponents of
           // the stale max stay below 256, which fp32 sums and bf16 P hold.
+          // (S_full of this tile completes after the previous PV, so O is
+          // quiescent here.)
           const bool grow = m_new > m + 8.0f;
           const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
           const bool o_needs = grow && j > 0 && l > 0.f;
@@ -489,47 +541,49 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1) attn_kernel(const KParams
             m = m_new;
           }
           const float mref = m == -INFINITY ? 0.f : m;
-          uint8_t *prow_base = smem + C::OFF_P;
+          float l0 = 0.f, l1 = 0.f;
+          uint32_t pk[C::BN / 2];
 #pragma unroll
-          for (int c = 0; c < C::BN / 8; ++c) {
-            float e[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              e[i] = ex2_approx(x[c * 8 + i] - mref);
-              l += e[i];
-            }
-            uint4 pk;
-            pk.x = pack_bf16(e[0], e[1]);
-            pk.y = pack_bf16(e[2], e[3]);
-            pk.z = pack_bf16(e[4], e[5]);
-            pk.w = pack_bf16(e[6], e[7]);
-            const uint32_t off = (c >> 3) * (C::BM * 128) + sw128_off(r, c & 7);
-            *reinterpret_cast<uint4 *>(prow_base + off) = pk;
+          for (int i = 0; i < C::BN; i += 2) {
+            const float e0 = ex2_approx(x[i] - mref);
+            const float e1 = ex2_approx(x[i + 1] - mref);
+            l0 += e0;
+            l1 += e1;
+            pk[i / 2] = pack_bf16(e0, e1);
           }
-          // O *= alpha once P is out of registers (PV_j is issued only after
-          // this warp arrives on the P barrier below).
+          l += l0 + l1;
+          // P (bf16 pairs) over the first 64 columns of this tile's S.
+          {
+            uint32_t a[32], b[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              a[i] = pk[i];
+              b[i] = pk[32 + i];
+            }
+            tmem_st32(lane_base + s_col + 0, a);
+            tmem_st32(lane_base + s_col + 32, b);
+          }
           if (__any_sync(0xffffffffu, o_needs)) {
             const float a = o_needs ? alpha : 1.0f;
             uint32_t v[32];
 #pragma unroll
             for (int c = 0; c < C::HDV / 32; ++c) {
-              const uint32_t ta = lane_base + C::O_COL + c * 32;
+              const uint32_t ta = lane_base + o_col + c * 32;
               tmem_ld32(ta, v);
               tmem_wait_ld();
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
               tmem_st32(ta, v);
             }
-            tmem_wait_st();
           }
+          tmem_wait_st();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bars[B_P_FULL]);
+        mbar_arrive(&bars[B_P_FULL + wg]);
       }
       if (*abort_flag) break;
-      // epilogue: wait for the last PV, normalise, store
-      if (!mbar_wait(&bars[B_O_DONE], o_cnt & 1u, abort_flag)) {
+      // epilogue: wait for the last PV of this tile, normalise, store
+      if (!mbar_wait(&bars[B_O_DONE + wg], o_cnt & 1u, abort_flag)) {
         abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
         break;
       }
@@ -538,26 +592,25 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1) attn_kernel(const KParams
       if (warp_active) {
         const float inv = l > 0.f ? 1.0f / l : 0.f;
         const float lse_v = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        const int64_t orow_idx = (int64_t)(w.q_tok0 + t) * p.hq + w.kvh * p.group + g;
         uint32_t v[32];
 #pragma unroll
         for (int c = 0; c < C::HDV / 32; ++c) {
-          tmem_ld32(lane_base + C::O_COL + c * 32, v);
+          tmem_ld32(lane_base + o_col + c * 32, v);
           tmem_wait_ld();
           if (valid) {
             if (w.slot < 0) {
               bf16 *orow = p.o + orow_idx * C::HDV + c * 32;
 #pragma unroll
               for (int i = 0; i < 32; i += 8) {
-                uint4 pk;
-                pk.x = pack_bf16(__uint_as_float(v[i + 0]) * inv, __uint_as_float(v[i + 1]) * inv);
-                pk.y = pack_bf16(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
-                pk.z = pack_bf16(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv);
-                pk.w = pack_bf16(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
-                *reinterpret_cast<uint4 *>(orow + i) = pk;
+                uint4 q4;
+                q4.x = pack_bf16(__uint_as_float(v[i + 0]) * inv, __uint_as_float(v[i + 1]) * inv);
+                q4.y = pack_bf16(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+                q4.z = pack_bf16(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv);
+                q4.w = pack_bf16(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
+                *reinterpret_cast<uint4 *>(orow + i) = q4;
               }
             } else {
-              float *prow = p.po + ((int64_t)w.slot * C::BM + r) * C::HDV + c * 32;
+              float *prow = p.po + prow_idx * C::HDV + c * 32;
 #pragma unroll
               for (int i = 0; i < 32; i += 4)
                 *reinterpret_cast<float4 *>(prow + i) =
@@ -570,62 +623,101 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1) attn_kernel(const KParams
           if (w.slot < 0) {
             if (p.lse) p.lse[orow_idx] = lse_v;
           } else {
-            p.plse[(int64_t)w.slot * C::BM + r] = lse_v;
+            p.plse[prow_idx] = lse_v;
           }
         }
       }
       tc_fence_before();
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ------------------------------------------------ MMA issue (one thread)
     if (lane == 0) {
-      uint32_t q_cnt = 0, kv_cnt = 0, s_cnt = 0, p_cnt = 0;
-      const uint32_t sQ = sbase + C::OFF_Q, sP = sbase + C::OFF_P;
+      uint32_t q_cnt = 0, kc = 0, vc = 0, p_cnt0 = 0, p_cnt1 = 0;
+      const uint32_t sQ0 = sbase + C::OFF_Q, sQ1 = sQ0 + C::Q_BYTES;
       bool ok = true;
-      auto issue_pv = [&](int jj, int stage) -> bool {
-        if (!mbar_wait(&bars[B_P_FULL], p_cnt & 1u, abort_flag)) return false;
-        ++p_cnt;
-        tc_fence_after();
-        const uint32_t sV = sbase + C::OFF_V + stage * C::V_BYTES;
+      auto issue_s = [&](int qt, uint32_t sK) {
+        const uint32_t sQ = qt ? sQ1 : sQ0;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t ad = sw128_desc(sQ + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 0, 1024);
+          const uint64_t bd = sw128_desc(sK + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 0, 1024);
+          tc_mma_ss(tmem + qt * C::BN, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&bars[B_S_FULL + qt]);
+      };
+      auto issue_pv = [&](int qt, uint32_t sV, bool acc_first) {
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
-          const uint64_t ad = sw128_desc(sP + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 0, 1024);
           const uint64_t bd = sw128_desc(sV + kk * 2048, C::BN * 128, 1024);
-          tc_mma_ss(tmem + C::O_COL, ad, bd, C::IDESC_PV, (jj > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + 2 * C::BN + qt * C::HDV, tmem + qt * C::BN + kk * 8, bd, C::IDESC_PV,
+                    (acc_first || kk > 0) ? 1u : 0u);
         }
-        tc_commit(&bars[B_O_DONE]);
-        tc_commit(&bar_kv_empty[stage]);
-        return true;
       };
       for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
         const WorkUnit w = p.units[u];
-        const int nt = unit_tiles(w);
+        const int nt = w.n_tiles;
         if (nt == 0) continue;
+        const bool q1 = w.n_tok > TOK;
         if (!mbar_wait(&bars[B_Q_FULL], q_cnt & 1u, abort_flag)) { ok = false; break; }
         ++q_cnt;
         tc_fence_after();
-        int prev_stage = -1;
-        for (int j = 0; j < nt; ++j) {
-          const int stage = kv_cnt % C::NS;
-          if (!mbar_wait(&bar_kv_full[stage], (kv_cnt / C::NS) & 1u, abort_flag)) { ok = false; break; }
-          ++kv_cnt;
+        // tile 0: S of both Q tiles
+        {
+          const int ks = kc % C::NK;
+          if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sb = s_cnt & 1u;
-          ++s_cnt;
-          const uint32_t sK = sbase + C::OFF_K + stage * C::K_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint64_t ad = sw128_desc(sQ + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 0, 1024);
-            const uint64_t bd = sw128_desc(sK + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 0, 1024);
-            tc_mma_ss(tmem + C::S_COL + sb * C::BN, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
+          issue_s(0, sK);
+          if (q1) issue_s(1, sK);
+          tc_commit(&k_empty[ks]);
+          ++kc;
+          if (nt == 1) tc_commit(&bars[B_Q_EMPTY]);
+        }
+        for (int j = 1; j < nt && ok; ++j) {
+          const int ks = kc % C::NK, vs = vc % C::NV;
+          if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&bars[B_P_FULL + 0], p_cnt0 & 1u, abort_flag)) { ok = false; break; }
+          ++p_cnt0;
+          tc_fence_after();
+          const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
+          const uint32_t sV = sbase + C::OFF_V + vs * C::V_BYTES;
+          issue_pv(0, sV, j > 1);
+          issue_s(0, sK);
+          if (q1) {
+            if (!mbar_wait(&bars[B_P_FULL + 1], p_cnt1 & 1u, abort_flag)) { ok = false; break; }
+            ++p_cnt1;
+            tc_fence_after();
+            issue_pv(1, sV, j > 1);
+            issue_s(1, sK);
           }
-          tc_commit(&bars[B_S_FULL0 + sb]);
+          tc_commit(&v_empty[vs]);
+          ++vc;
+          tc_commit(&k_empty[ks]);
+          ++kc;
           if (j == nt - 1) tc_commit(&bars[B_Q_EMPTY]);
-          if (j > 0 && !issue_pv(j - 1, prev_stage)) { ok = false; break; }
-          prev_stage = stage;
         }
         if (!ok) break;
-        if (!issue_pv(nt - 1, prev_stage)) { ok = false; break; }
+        // last PV of both Q tiles
+        {
+          const int vs = vc % C::NV;
+          if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&bars[B_P_FULL + 0], p_cnt0 & 1u, abort_flag)) { ok = false; break; }
+          ++p_cnt0;
+          tc_fence_after();
+          const uint32_t sV = sbase + C::OFF_V + vs * C::V_BYTES;
+          issue_pv(0, sV, nt > 1);
+          tc_commit(&bars[B_O_DONE + 0]);
+          if (q1) {
+            if (!mbar_wait(&bars[B_P_FULL + 1], p_cnt1 & 1u, abort_flag)) { ok = false; break; }
+            ++p_cnt1;
+            tc_fence_after();
+            issue_pv(1, sV, nt > 1);
+            tc_commit(&bars[B_O_DONE + 1]);
+          }
+          tc_commit(&v_empty[vs]);
+          ++vc;
+        }
       }
       if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
       // drain: every MMA issued above must finish before TMEM is freed
@@ -633,131 +725,126 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1) attn_kernel(const KParams
       if (!mbar_wait_drain(&bars[B_FINAL], 0)) record_status(p.status, PKX_ETIMEOUT);
     }
   } else {
-    // ------------------------------------------------ paged K/V gather
-    const int lt = tid - 160;
-    uint32_t q_cnt = 0, kv_cnt = 0;
-    constexpr int CPR = HD / 8;                  // 16-byte chunks per row
-    constexpr int KPP = C::LOAD_THREADS / CPR;   // rows per pass of the load warps
-    const int ch = lt % CPR;
-    const int row0 = lt / CPR;
-    for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
-      const WorkUnit w = p.units[u];
-      const int nt = unit_tiles(w);
-      if (nt == 0) continue;
-      if (q_cnt > 0 && !mbar_wait(&bars[B_Q_EMPTY], (q_cnt - 1) & 1u, abort_flag)) {
-        abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
-        break;
-      }
-      // Q tile: row r = token * group + head-in-group; rows past the block
-      // are zero-filled.
-      {
-        const uint32_t sQ = sbase + C::OFF_Q;
-        const int rows_valid = w.n_tok * p.group;
-#pragma unroll 4
-        for (int rr = row0; rr < C::BM; rr += KPP) {
-          const bool v = rr < rows_valid;
-          const int t = rr / p.group, g = rr - t * p.group;
-          const bf16 *src = v ? p.q + ((int64_t)(w.q_tok0 + t) * p.hq + w.kvh * p.group + g) * HD + ch * 8
-                              : p.q;
-          cp_async_16(sQ + (ch >> 3) * (C::BM * 128) + sw128_off(rr, ch & 7), src, v ? 16u : 0u);
-        }
-        cp_async_commit();
-        cp_async_wait_group<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[B_Q_FULL]);
-        ++q_cnt;
-      }
-      // key sources of this sequence
-      int64_t kv_base = p.kv_indptr[w.b];
-      int P_pool;  // keys [0, P_pool) are pool slots, the rest extend rows
-      int64_t ext_base = 0;
+    // ------------------------------------------------ TMA loads (one warp)
+    uint32_t q_cnt = 0, kc = 0, vc = 0;
+    const CUtensorMap *kmap_pool = &tm.kp, *vmap_pool = &tm.vp;
+    const CUtensorMap *kmap_ext = &tm.ke, *vmap_ext = &tm.ve;
+    if (lane == 0) {
+      prefetch_tensormap(&tm.q);
+      prefetch_tensormap(kmap_pool);
+      prefetch_tensormap(vmap_pool);
       if (MODE == kTwoStage) {
-        P_pool = p.kv_indptr[w.b + 1] - (int)kv_base;
-        ext_base = p.qo_indptr[w.b];
-      } else {
-        P_pool = 0x7fffffff;
-      }
-      int pending = -1;
-      for (int j = 0; j < nt; ++j) {
-        const int stage = kv_cnt % C::NS;
-        if (kv_cnt >= (uint32_t)C::NS) {
-          // Publish the tile still in flight before blocking on a free stage:
-          // the MMA warp frees this stage only after it has consumed that tile.
-          if (pending >= 0) {
-            cp_async_wait_group<0>();
-            fence_proxy_async_smem();
-            mbar_arrive(&bar_kv_full[pending]);
-            pending = -1;
-          }
-          if (!mbar_wait(&bar_kv_empty[stage], ((kv_cnt / C::NS) - 1) & 1u, abort_flag)) {
-            abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
-            break;
-          }
-        }
-        const int kb = w.k_begin + j * C::BN;
-        const uint32_t sK = sbase + C::OFF_K + stage * C::K_BYTES;
-        const uint32_t sV = sbase + C::OFF_V + stage * C::V_BYTES;
-        // All of this thread's slot indices first (independent loads in
-        // flight together), then the row copies.
-        constexpr int NK = (C::BN + KPP - 1) / KPP;
-        int64_t slot[NK];
-#pragma unroll
-        for (int i = 0; i < NK; ++i) {
-          const int key = row0 + i * KPP;
-          const int jpos = kb + key;
-          slot[i] = -1;
-          if (key < C::BN && jpos < w.k_end && !(MODE == kTwoStage && jpos >= P_pool)) {
-            if (MODE == kUnified)
-              slot[i] = __ldg(static_cast<const int64_t *>(p.kv_indices) + kv_base + jpos);
-            else
-              slot[i] = __ldg(static_cast<const int32_t *>(p.kv_indices) + kv_base + jpos);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < NK; ++i) {
-          const int key = row0 + i * KPP;
-          if (key >= C::BN) break;
-          const int jpos = kb + key;
-          bool v = jpos < w.k_end;
-          const bf16 *krow = p.k_buf, *vrow = p.v_buf;
-          if (v) {
-            if (MODE == kTwoStage && jpos >= P_pool) {
-              const int64_t te = ext_base + (jpos - P_pool);
-              krow = p.k_ext + te * p.ke_st + (int64_t)w.kvh * p.ke_sh;
-              vrow = p.v_ext + te * p.ve_st + (int64_t)w.kvh * p.ve_sh;
-            } else if (slot[i] < 0 || slot[i] >= p.num_slots) {
-              record_status(p.status, PKX_EDEVICE);
-              v = false;
-            } else {
-              krow = p.k_buf + slot[i] * p.kb_ss + (int64_t)w.kvh * p.kb_sh;
-              vrow = p.v_buf + slot[i] * p.vb_ss + (int64_t)w.kvh * p.vb_sh;
-            }
-          }
-          const uint32_t off = (ch >> 3) * (C::BN * 128) + sw128_off(key, ch & 7);
-          cp_async_16(sK + off, v ? krow + ch * 8 : p.k_buf, v ? 16u : 0u);
-          cp_async_16(sV + off, v ? vrow + ch * 8 : p.v_buf, v ? 16u : 0u);
-        }
-        cp_async_commit();
-        if (pending >= 0) {
-          cp_async_wait_group<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(&bar_kv_full[pending]);
-        }
-        pending = stage;
-        ++kv_cnt;
-      }
-      if (pending >= 0) {
-        cp_async_wait_group<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(&bar_kv_full[pending]);
+        prefetch_tensormap(kmap_ext);
+        prefetch_tensormap(vmap_ext);
       }
     }
-    cp_async_wait_group<0>();
+    const uint32_t q_box_bytes = 64u * 2u * G * p.q_box_tok;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
+      const WorkUnit w = p.units[u];
+      const int nt = w.n_tiles;
+      if (nt == 0) continue;
+      const bool q1 = w.n_tok > TOK;
+      // Q tiles: box (64 dims, G heads, q_box_tok tokens), rows t * G + g.
+      if (lane == 0) {
+        if (q_cnt > 0 && !mbar_wait(&bars[B_Q_EMPTY], (q_cnt - 1) & 1u, abort_flag)) ok = false;
+        if (ok) {
+          const int nq = q1 ? 2 : 1;
+          mbar_arrive_expect_tx(&bars[B_Q_FULL], q_box_bytes * (HD / 64) * nq);
+          for (int qt = 0; qt < nq; ++qt)
+            for (int h = 0; h < HD / 64; ++h)
+              tma_load_3d(sbase + C::OFF_Q + qt * C::Q_BYTES + h * (C::BM * 128), &tm.q, h * 64,
+                          w.kvh * G, w.q_tok0 + qt * TOK, &bars[B_Q_FULL]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ++q_cnt;
+      const int64_t kv_base = p.kv_indptr[w.b];
+      const int64_t ext_base = MODE == kTwoStage ? p.qo_indptr[w.b] : 0;
+      for (int j = 0; j < nt && ok; ++j) {
+        int kb, ke;
+        tile_keys(w, j, kb, ke);
+        const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
+        // rows of this lane's four keys (invalid keys repeat the tile's
+        // first row: their scores are masked, so P = 0 for them)
+        int rows[4];
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int jpos = kb + 4 * lane + i;
+          int64_t row = -1;
+          if (jpos < ke) {
+            if (from_ext) {
+              row = ext_base + (jpos - w.k_split);
+            } else {
+              row = MODE == kUnified
+                        ? static_cast<const int64_t *>(p.kv_indices)[kv_base + jpos]
+                        : (int64_t) static_cast<const int32_t *>(p.kv_indices)[kv_base + jpos];
+              if (row < 0 || row >= p.num_slots) {
+                bad = true;
+                row = -1;
+              }
+            }
+          }
+          rows[i] = (int)row;
+        }
+        if (bad) record_status(p.status, PKX_EDEVICE);
+        int first = __shfl_sync(0xffffffffu, rows[0], 0);
+        if (first < 0) first = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (rows[i] < 0) rows[i] = first;
+        const CUtensorMap *km = from_ext ? kmap_ext : kmap_pool;
+        const CUtensorMap *vm = from_ext ? vmap_ext : vmap_pool;
+        const int kx = w.kvh * (int)(from_ext ? p.ke_sh : p.kb_sh);
+        const int vx = w.kvh * (int)(from_ext ? p.ve_sh : p.vb_sh);
+        // K tile
+        const int ks = kc % C::NK;
+        if (lane == 0) {
+          if (kc >= (uint32_t)C::NK &&
+              !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag))
+            ok = false;
+          else
+            mbar_arrive_expect_tx(&k_full[ks], C::K_BYTES);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        {
+          const uint32_t dst = sbase + C::OFF_K + ks * C::K_BYTES + lane * 4 * 128;
+#pragma unroll
+          for (int h = 0; h < HD / 64; ++h)
+            tma_gather4(dst + h * (C::BN * 128), km, kx + h * 64, rows[0], rows[1], rows[2],
+                        rows[3], &k_full[ks]);
+        }
+        ++kc;
+        // V tile
+        const int vs = vc % C::NV;
+        if (lane == 0) {
+          if (vc >= (uint32_t)C::NV &&
+              !mbar_wait(&v_empty[vs], ((vc / C::NV) - 1) & 1u, abort_flag))
+            ok = false;
+          else
+            mbar_arrive_expect_tx(&v_full[vs], C::V_BYTES);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        {
+          const uint32_t dst = sbase + C::OFF_V + vs * C::V_BYTES + lane * 4 * 128;
+#pragma unroll
+          for (int h = 0; h < C::HDV / 64; ++h)
+            tma_gather4(dst + h * (C::BN * 128), vm, vx + h * 64, rows[0], rows[1], rows[2],
+                        rows[3], &v_full[vs]);
+        }
+        ++vc;
+      }
+    }
+    if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -772,17 +859,18 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1) attn_kernel(const KParams
 __global__ void __launch_bounds__(256) combine_kernel(const WsHeader *hdr, const CombineEntry *ce,
                                                       const float *plse, const float *po,
                                                       bf16 *o, float *lse, int hq, int group,
-                                                      int hdv) {
+                                                      int hdv, int rows_per_slot) {
   const int n_comb = hdr->n_combine;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
-  for (int64_t idx = gw; idx < (int64_t)n_comb * kBlockM; idx += nw) {
-    const int e = (int)(idx / kBlockM), r = (int)(idx % kBlockM);
+  for (int64_t idx = gw; idx < (int64_t)n_comb * rows_per_slot; idx += nw) {
+    const int e = (int)(idx / rows_per_slot), r = (int)(idx % rows_per_slot);
     const CombineEntry E = ce[e];
     if (r >= E.n_tok * group) continue;
     float mx = -INFINITY;
-    for (int i = 0; i < E.n_split; ++i) mx = fmaxf(mx, plse[(int64_t)(E.slot0 + i) * kBlockM + r]);
+    for (int i = 0; i < E.n_split; ++i)
+      mx = fmaxf(mx, plse[(int64_t)(E.slot0 + i) * rows_per_slot + r]);
     const int t = r / group, g = r - t * group;
     const int64_t orow = (int64_t)(E.q_tok0 + t) * hq + E.kvh * group + g;
     if (mx == -INFINITY) {
@@ -793,14 +881,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const WsHeader *hdr, const
     }
     float wsum = 0.f;
     for (int i = 0; i < E.n_split; ++i)
-      wsum += exp2f((plse[(int64_t)(E.slot0 + i) * kBlockM + r] - mx) * 1.4426950408889634f);
+      wsum += exp2f((plse[(int64_t)(E.slot0 + i) * rows_per_slot + r] - mx) * 1.4426950408889634f);
     const float inv = 1.0f / wsum;
     for (int c = lane * 8; c < hdv; c += 256) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       for (int i = 0; i < E.n_split; ++i) {
-        const float wi =
-            exp2f((plse[(int64_t)(E.slot0 + i) * kBlockM + r] - mx) * 1.4426950408889634f) * inv;
-        const float *src = po + ((int64_t)(E.slot0 + i) * kBlockM + r) * hdv + c;
+        const int64_t sr = (int64_t)(E.slot0 + i) * rows_per_slot + r;
+        const float wi = exp2f((plse[sr] - mx) * 1.4426950408889634f) * inv;
+        const float *src = po + sr * hdv + c;
         const float4 a = *reinterpret_cast<const float4 *>(src);
         const float4 b = *reinterpret_cast<const float4 *>(src + 4);
         acc[0] += wi * a.x; acc[1] += wi * a.y; acc[2] += wi * a.z; acc[3] += wi * a.w;
@@ -829,14 +917,22 @@ int tokens_per_block(int group) { return group >= 1 && group <= kBlockM ? kBlock
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int num_sms) {
+// Rows of one split-KV partial slot: both Q tiles of an extend block, or the
+// group's rows of a decode query.
+int rows_per_slot(bool decode, int group) {
+  return decode ? group : 2 * tokens_per_block(group) * group;
+}
+
+WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int num_sms,
+                   bool decode) {
   WsLayout L{};
-  const int tok = tokens_per_block(group);
+  const int tok = 2 * tokens_per_block(group);  // tokens of a two-Q-tile block
   L.unit_target = 4 * (num_sms > 0 ? num_sms : 160);
   L.qb_max = (tok > 0 ? (num_q_tokens + tok - 1) / tok : 0) + batch + 1;
   L.unit_max = L.unit_target + hkv * L.qb_max;
   L.slot_max = 2 * L.unit_target;
   L.comb_max = L.unit_target;
+  L.rows_per_slot = rows_per_slot(decode, group);
   size_t off = align256(sizeof(WsHeader));
   L.seq_off = off;
   off = align256(off + sizeof(int32_t) * 8 * (size_t)(batch + 1));
@@ -847,15 +943,65 @@ WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int 
   L.comb_off = off;
   off = align256(off + sizeof(CombineEntry) * (size_t)L.comb_max);
   L.plse_off = off;
-  off = align256(off + sizeof(float) * (size_t)L.slot_max * kBlockM);
+  off = align256(off + sizeof(float) * (size_t)L.slot_max * L.rows_per_slot);
   L.po_off = off;
-  off = align256(off + sizeof(float) * (size_t)L.slot_max * kBlockM * lv);
+  off = align256(off + sizeof(float) * (size_t)L.slot_max * L.rows_per_slot * lv);
   L.total = off;
   return L;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once.
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// 2-D map over rows of `row_elems` bf16 (row stride `row_stride` elements),
+// box = 64 elements x 1 row, 128-byte swizzle (gather4 rows).
+static int make_row_map(CUtensorMap *m, const void *base, int64_t row_elems, int64_t rows,
+                        int64_t row_stride) {
+  auto fn = encode_fn();
+  if (!fn) return set_error(PKX_ECUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_stride * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(PKX_EINVAL, "tensor map (rows=%lld, row=%lld, stride=%lld) rejected: %d",
+                     (long long)rows, (long long)row_elems, (long long)row_stride, (int)r);
+  return PKX_OK;
+}
+
+// 3-D map over q [n, hq, lq]: box = 64 dims x G heads x tok tokens.
+static int make_q_map(CUtensorMap *m, const void *q, int64_t n, int hq, int lq, int G, int tok) {
+  auto fn = encode_fn();
+  if (!fn) return set_error(PKX_ECUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)lq, (cuuint64_t)hq, (cuuint64_t)n};
+  cuuint64_t strides[2] = {(cuuint64_t)lq * 2, (cuuint64_t)hq * lq * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)tok};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(PKX_EINVAL, "q tensor map rejected: %d", (int)r);
+  return PKX_OK;
+}
+
 template <int HD, int MODE>
-static int launch_attn_kernel(const KParams &kp, int grid, cudaStream_t s) {
+static int launch_attn_kernel(const TMaps &tmaps, const KParams &kp, int grid, cudaStream_t s) {
   using C = Cfg<HD>;
   static bool configured = false;  // per instantiation; attribute is per device
   if (!configured) {
@@ -865,7 +1011,7 @@ static int launch_attn_kernel(const KParams &kp, int grid, cudaStream_t s) {
       return set_error(PKX_ECUDA, "cudaFuncSetAttribute(attn_kernel): %s", cudaGetErrorString(e));
     configured = true;
   }
-  attn_kernel<HD, MODE><<<grid, C::THREADS, C::SMEM, s>>>(kp);
+  attn_kernel<HD, MODE><<<grid, C::THREADS, C::SMEM, s>>>(tmaps, kp);
   return PKX_OK;
 }
 
@@ -873,15 +1019,38 @@ int launch_attention(const AttnArgs &a) {
   const int group = a.hq / a.hkv;
   const int nsm = num_sms_current_device();
   if (nsm <= 0) return set_error(PKX_ECUDA, "cannot query the current device");
-  const int nq = a.mode == kDecode ? a.batch : a.num_q_tokens;
-  WsLayout L = ws_layout(a.batch, nq, a.hkv, group, a.lv, nsm);
+  const bool decode = a.mode == kDecode;
+  const int nq = decode ? a.batch : a.num_q_tokens;
+  WsLayout L = ws_layout(a.batch, nq, a.hkv, group, a.lv, nsm, decode);
   if (a.workspace == nullptr || a.workspace_bytes < L.total)
     return set_error(PKX_EWORKSPACE, "workspace of %zu bytes given, %zu needed",
                      a.workspace_bytes, L.total);
   if (reinterpret_cast<uintptr_t>(a.workspace) & 255)
     return set_error(PKX_EINVAL, "workspace must be 256-byte aligned");
+  if (a.num_slots >= (int64_t)INT_MAX)
+    return set_error(PKX_EUNSUPPORTED, "more than 2^31 pool slots");
   uint8_t *ws = static_cast<uint8_t *>(a.workspace);
   WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+  const int tok = tokens_per_block(group);
+
+  // tensor maps
+  TMaps tm;
+  memset(&tm, 0, sizeof tm);
+  int rc = make_q_map(&tm.q, a.q, nq, a.hq, a.lq, group, decode ? 1 : tok);
+  if (rc != PKX_OK) return rc;
+  const int64_t krow = std::max<int64_t>(a.kb_ss, (int64_t)(a.hkv - 1) * a.kb_sh + a.lq);
+  const int64_t vrow = std::max<int64_t>(a.vb_ss, (int64_t)(a.hkv - 1) * a.vb_sh + a.lv);
+  if ((rc = make_row_map(&tm.kp, a.k_buf, krow, a.num_slots, a.kb_ss))) return rc;
+  if ((rc = make_row_map(&tm.vp, a.v_buf, vrow, a.num_slots, a.vb_ss))) return rc;
+  if (a.mode == kTwoStage) {
+    const int64_t kr = std::max<int64_t>(a.ke_st, (int64_t)(a.hkv - 1) * a.ke_sh + a.lq);
+    const int64_t vr = std::max<int64_t>(a.ve_st, (int64_t)(a.hkv - 1) * a.ve_sh + a.lv);
+    if ((rc = make_row_map(&tm.ke, a.k_ext, kr, nq, a.ke_st))) return rc;
+    if ((rc = make_row_map(&tm.ve, a.v_ext, vr, nq, a.ve_st))) return rc;
+  } else {
+    tm.ke = tm.kp;
+    tm.ve = tm.vp;
+  }
 
   SchedParams sp;
   sp.mode = a.mode;
@@ -890,7 +1059,7 @@ int launch_attention(const AttnArgs &a) {
   sp.prefix_lens = a.prefix_lens;
   sp.batch = a.batch;
   sp.hkv = a.hkv;
-  sp.tok = tokens_per_block(group);
+  sp.tok = 2 * tok;
   sp.window = a.window;
   sp.num_q_tokens = nq;
   sp.unit_target = L.unit_target;
@@ -906,28 +1075,22 @@ int launch_attention(const AttnArgs &a) {
   sched_kernel<<<1, 1024, 0, a.stream>>>(sp);
 
   KParams kp;
-  kp.q = static_cast<const bf16 *>(a.q);
   kp.o = static_cast<bf16 *>(a.o);
   kp.lse = a.lse;
-  kp.k_ext = static_cast<const bf16 *>(a.k_ext);
-  kp.v_ext = static_cast<const bf16 *>(a.v_ext);
-  kp.ke_st = a.ke_st;
-  kp.ke_sh = a.ke_sh;
-  kp.ve_st = a.ve_st;
-  kp.ve_sh = a.ve_sh;
-  kp.k_buf = static_cast<const bf16 *>(a.k_buf);
-  kp.v_buf = static_cast<const bf16 *>(a.v_buf);
-  kp.kb_ss = a.kb_ss;
   kp.kb_sh = a.kb_sh;
-  kp.vb_ss = a.vb_ss;
   kp.vb_sh = a.vb_sh;
+  kp.ke_sh = a.ke_sh;
+  kp.ve_sh = a.ve_sh;
   kp.num_slots = a.num_slots;
   kp.qo_indptr = a.qo_indptr;
   kp.kv_indptr = a.kv_indptr;
   kp.kv_indices = a.kv_indices;
   kp.hq = a.hq;
   kp.group = group;
+  kp.tok = tok;
+  kp.q_box_tok = decode ? 1 : tok;
   kp.window = a.window;
+  kp.rows_per_slot = L.rows_per_slot;
   const float log2e = 1.4426950408889634f;
   const float sm_scale = a.sm_scale > 0.f ? a.sm_scale : 1.0f / sqrtf((float)a.lq);
   kp.use_cap = a.logit_cap > 0.f;
@@ -940,26 +1103,25 @@ int launch_attention(const AttnArgs &a) {
   kp.plse = reinterpret_cast<float *>(ws + L.plse_off);
   kp.po = reinterpret_cast<float *>(ws + L.po_off);
 
-  int rc;
   const int grid = nsm;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
   attention_events(&ev_before, &ev_after);
   if (ev_before) cudaEventRecord(ev_before, a.stream);
   if (a.lq == 128 && a.lv == 128) {
-    if (a.mode == kTwoStage) rc = launch_attn_kernel<128, kTwoStage>(kp, grid, a.stream);
-    else if (a.mode == kUnified) rc = launch_attn_kernel<128, kUnified>(kp, grid, a.stream);
-    else rc = launch_attn_kernel<128, kDecode>(kp, grid, a.stream);
+    if (a.mode == kTwoStage) rc = launch_attn_kernel<128, kTwoStage>(tm, kp, grid, a.stream);
+    else if (a.mode == kUnified) rc = launch_attn_kernel<128, kUnified>(tm, kp, grid, a.stream);
+    else rc = launch_attn_kernel<128, kDecode>(tm, kp, grid, a.stream);
   } else if (a.lq == 64 && a.lv == 64) {
-    if (a.mode == kTwoStage) rc = launch_attn_kernel<64, kTwoStage>(kp, grid, a.stream);
-    else if (a.mode == kUnified) rc = launch_attn_kernel<64, kUnified>(kp, grid, a.stream);
-    else rc = launch_attn_kernel<64, kDecode>(kp, grid, a.stream);
+    if (a.mode == kTwoStage) rc = launch_attn_kernel<64, kTwoStage>(tm, kp, grid, a.stream);
+    else if (a.mode == kUnified) rc = launch_attn_kernel<64, kUnified>(tm, kp, grid, a.stream);
+    else rc = launch_attn_kernel<64, kDecode>(tm, kp, grid, a.stream);
   } else {
     return set_error(PKX_EUNSUPPORTED, "head dims (%d, %d) not built", a.lq, a.lv);
   }
   if (rc != PKX_OK) return rc;
   if (ev_after) cudaEventRecord(ev_after, a.stream);
   combine_kernel<<<nsm * 2, 256, 0, a.stream>>>(hdr, sp.comb, kp.plse, kp.po, kp.o, a.lse, a.hq,
-                                               group, a.lv);
+                                               group, a.lv, L.rows_per_slot);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(PKX_ECUDA, "attention launch: %s", cudaGetErrorString(e));
   return PKX_OK;

@@ -27,8 +27,8 @@ constexpr int kBlockN = 128;
 constexpr int kMinSplitTiles = 4;
 
 // One unit of attention work: a block of query tokens of one sequence and one
-// KV head (all of that head's query heads stacked in the tile's rows, row =
-// token * group + head-in-group), over the key range [k_begin, k_end).
+// KV head (up to two Q tiles; in a tile, row = token * group + head-in-group),
+// over the key range [k_begin, k_end).
 struct WorkUnit {
   int32_t q_tok0;   // first query row in q/o (token index)
   int32_t n_tok;    // tokens in the block
@@ -36,8 +36,11 @@ struct WorkUnit {
   int32_t kvh;      // KV head
   int32_t k_begin;  // key positions [k_begin, k_end)
   int32_t k_end;
+  int32_t k_split;  // keys >= k_split come from the extend rows (two-stage)
+  int32_t n_tiles;  // K/V tiles (no tile straddles k_split)
   int32_t b;        // sequence
   int32_t slot;     // -1: write o/lse; else split-KV partial slot
+  int32_t pad[2];
 };
 
 // A query block whose key range was split: its partials live in slots
@@ -66,17 +69,19 @@ struct WsLayout {
   size_t qb_off;       // int32 [qb_max] per-query-block tile counts
   size_t units_off;    // WorkUnit [unit_max]
   size_t comb_off;     // CombineEntry [comb_max]
-  size_t plse_off;     // float [slot_max][kBlockM]
-  size_t po_off;       // float [slot_max][kBlockM][lv]
+  size_t plse_off;     // float [slot_max][rows_per_slot]
+  size_t po_off;       // float [slot_max][rows_per_slot][lv]
   size_t total;
-  int qb_max, unit_max, comb_max, slot_max, unit_target;
+  int qb_max, unit_max, comb_max, slot_max, unit_target, rows_per_slot;
 };
 
 int num_sms_current_device();
 // Events set by pkx_set_attention_events for this thread (may be null).
 void attention_events(cudaEvent_t *before, cudaEvent_t *after);
 int tokens_per_block(int group);
-WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int num_sms);
+int rows_per_slot(bool decode, int group);
+WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int num_sms,
+                   bool decode);
 
 // Arguments of one attention launch (any key mode).
 struct AttnArgs {
