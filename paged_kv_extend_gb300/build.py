@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import glob
 import os
+import re
 import subprocess
 import sys
 
@@ -42,6 +43,34 @@ def needs_build() -> bool:
     return any(os.path.getmtime(f) > t for f in srcs + hdrs + [__file__])
 
 
+def check_attention_registers(ptxas_log: str) -> None:
+    """The attention kernel hands registers between warpgroups with
+    setmaxnreg; the split adds up only if every instantiation launches with
+    exactly the register count the kernel source assumes (REGS_LAUNCH).
+    Refuse to build otherwise: a wrong split would stall the kernel."""
+    src = open(os.path.join(CSRC, "attention.cu")).read()
+    m = re.search(r"REGS_LAUNCH = (\d+)", src)
+    if not m:
+        raise RuntimeError("attention.cu: REGS_LAUNCH not found")
+    want = int(m.group(1))
+    found = 0
+    current = None
+    for line in ptxas_log.splitlines():
+        fm = re.search(r"Compiling entry function '(\S+)'", line) or \
+            re.search(r"Function properties for (\S+)", line)
+        if fm:
+            current = fm.group(1)
+        rm = re.search(r"Used (\d+) registers", line)
+        if rm and current and "attn_kernel" in current:
+            found += 1
+            if int(rm.group(1)) != want:
+                raise RuntimeError(
+                    f"{current} uses {rm.group(1)} registers at launch, the register split "
+                    f"assumes {want}; not building")
+    if found == 0:
+        raise RuntimeError("no attn_kernel register report from ptxas; not building")
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile and link libpkx.so; returns its path."""
     if not force and not needs_build():
@@ -55,6 +84,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         cmd = [nvcc, *NVCC_FLAGS, "-c", src, "-o", obj]
+        if os.path.basename(src) == "attention.cu":
+            cmd.insert(1, "-Xptxas=-v")
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -63,8 +94,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
         out, _ = p.communicate()
         if p.returncode != 0:
             failed.append((src, out.decode(errors="replace")))
-        elif verbose and out:
-            print(out.decode(errors="replace"), file=sys.stderr)
+        else:
+            if os.path.basename(src) == "attention.cu":
+                check_attention_registers(out.decode(errors="replace"))
+            if verbose and out:
+                print(out.decode(errors="replace"), file=sys.stderr)
     if failed:
         msg = "\n".join(f"{s}:\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")

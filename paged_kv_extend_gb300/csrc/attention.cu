@@ -15,9 +15,15 @@
 //  * a Q tile = 128 rows = (tokens x the Hq/Hkv query heads of one KV head),
 //    and a CTA runs two Q tiles of consecutive tokens against each K/V tile:
 //    K/V of a KV head are gathered once for 2 x 128 query rows;
-//  * K and V tiles are gathered from the pool by TMA (tile::gather4, four
-//    pool rows per instruction, 128-byte swizzle) into two smem rings; one
-//    warp issues them, completion is counted in bytes on mbarriers;
+//  * K and V rows are gathered from the pool by six warps with 16-byte
+//    cp.async copies placed straight into the 128-byte-swizzled layout the
+//    MMA descriptors read (random 256-byte rows need many copying threads
+//    to reach HBM bandwidth; a TMA gather4 moves only four 128-byte rows
+//    per instruction and stalls on its issue rate); each copying thread
+//    arrives on the stage barrier when its own copies land.  An index warp
+//    resolves every tile's slot indices into a small smem ring ahead of the
+//    copy warps and loads the Q tiles (3-D TMA boxes).  setmaxnreg moves
+//    registers from these warps to the softmax warpgroups;
 //  * QK^T and PV are tcgen05.mma (M=128, bf16 in, fp32 accumulate in TMEM).
 //    TMEM holds S and O of both Q tiles (4 x 128 columns).  The softmax
 //    warpgroup of a tile writes P (bf16) back over its S columns and PV
@@ -313,7 +319,9 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
 struct KParams {
   bf16 *o;
   float *lse;
-  int64_t kb_sh, vb_sh, ke_sh, ve_sh;  // head strides (elements) of the maps' rows
+  const bf16 *k_pool, *v_pool, *k_ext, *v_ext;
+  int64_t kb_ss, vb_ss, ke_st, ve_st;  // row strides (elements): slot / token
+  int64_t kb_sh, vb_sh, ke_sh, ve_sh;  // head strides (elements)
   int64_t num_slots;
   const int32_t *qo_indptr, *kv_indptr;
   const void *kv_indices;
@@ -327,30 +335,40 @@ struct KParams {
   float *plse, *po;
 };
 
-// TMA descriptors: q (3-D: dim, head, token), K/V pool rows (2-D: element of
-// a slot row, slot) and K/V extend rows (2-D: element of a token row, token).
+// TMA descriptor of q (3-D: dim, head, token).
 struct TMaps {
-  CUtensorMap q, kp, vp, ke, ve;
+  CUtensorMap q;
 };
 
 template <int HD>
 struct Cfg {
   static constexpr int BM = kBlockM, BN = kBlockN, HDV = HD;
-  static constexpr int NK = HD == 128 ? 3 : 6;  // K ring stages
-  static constexpr int NV = HD == 128 ? 2 : 6;  // V ring stages
+  static constexpr int NK = HD == 128 ? 3 : 5;  // K ring stages
+  static constexpr int NV = HD == 128 ? 2 : 5;  // V ring stages
+  static constexpr int NI = HD == 128 ? 3 : 4;  // row-index ring stages
   static constexpr int Q_BYTES = BM * HD * 2;   // one Q tile
   static constexpr int K_BYTES = BN * HD * 2;
   static constexpr int V_BYTES = BN * HDV * 2;
+  static constexpr int I_BYTES = BN * 4;        // int32 row of each key
   static constexpr int OFF_Q = 0;  // two Q tiles
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NK * K_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NV * V_BYTES;
-  static constexpr int N_BARS = 16 + 2 * NK + 2 * NV;
+  static constexpr int OFF_I = OFF_V + NV * V_BYTES;
+  static constexpr int OFF_BAR = OFF_I + NI * I_BYTES;
+  static constexpr int N_BARS = 16 + 2 * NK + 2 * NV + 2 * NI;
   static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 1024;  // + alignment slack
   static constexpr int TMEM_COLS = 512;  // S0 | S1 | O0 | O1, 128 columns each
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HDV, 1);
-  static constexpr int THREADS = 320;  // 2 softmax warpgroups, MMA warp, TMA warp
+  // warps 0-7: two softmax warpgroups; 8: MMA; 9: row indices + Q; 10-15: copies
+  static constexpr int THREADS = 512;
+  static constexpr int COPY_THREADS = 192;
+  // Registers: the kernel launches with REGS_LAUNCH per thread (checked at
+  // build time); the softmax warpgroups take REGS_SOFTMAX, the other two
+  // give back down to REGS_OTHER.  The split must add up exactly.
+  static constexpr int REGS_LAUNCH = 128, REGS_SOFTMAX = 168, REGS_OTHER = 88;
+  static_assert(256 * REGS_SOFTMAX + 256 * REGS_OTHER == THREADS * REGS_LAUNCH,
+                "register split must match the launch allocation");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -362,7 +380,8 @@ enum {
   B_P_FULL = 4,  // + Q tile
   B_O_DONE = 6,  // + Q tile
   B_FINAL = 8,
-  B_RING = 16,  // K full[NK], K empty[NK], V full[NV], V empty[NV]
+  B_RING = 16,  // K full[NK], K empty[NK], V full[NV], V empty[NV],
+                // I full[NI], I empty[NI]
 };
 
 // Key range [kb, ke) of tile j of a unit (tiles never straddle k_split).
@@ -399,6 +418,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
   uint64_t *k_empty = k_full + C::NK;
   uint64_t *v_full = k_empty + C::NK;
   uint64_t *v_empty = v_full + C::NV;
+  uint64_t *i_full = v_empty + C::NV;
+  uint64_t *i_empty = i_full + C::NI;
   volatile int *abort_flag = &s_abort;
 
   const int tid = threadIdx.x;
@@ -414,12 +435,16 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     }
     mbar_init(&bars[B_FINAL], 1);
     for (int s = 0; s < C::NK; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&k_full[s], C::COPY_THREADS);
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < C::NV; ++s) {
-      mbar_init(&v_full[s], 1);
+      mbar_init(&v_full[s], C::COPY_THREADS);
       mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < C::NI; ++s) {
+      mbar_init(&i_full[s], 32);
+      mbar_init(&i_empty[s], C::COPY_THREADS);
     }
     s_abort = 0;
     fence_barrier_init();
@@ -436,6 +461,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
   const int G = p.group, TOK = p.tok;
 
   if (warp < 8) {
+    regs_increase<C::REGS_SOFTMAX>();
     // ------------------------------------------- softmax + epilogue (x2)
     const int wg = warp >> 2;  // Q tile of this warpgroup
     const int wq = warp & 3;   // TMEM lane quarter
@@ -629,7 +655,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       }
       tc_fence_before();
     }
-  } else if (warp == 8) {
+  } else {
+  regs_decrease<C::REGS_OTHER>();
+  if (warp == 8) {
     // ------------------------------------------------ MMA issue (one thread)
     if (lane == 0) {
       uint32_t q_cnt = 0, kc = 0, vc = 0, p_cnt0 = 0, p_cnt1 = 0;
@@ -637,7 +665,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       bool ok = true;
       auto issue_s = [&](int qt, uint32_t sK) {
         const uint32_t sQ = qt ? sQ1 : sQ0;
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint64_t ad = sw128_desc(sQ + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 0, 1024);
           const uint64_t bd = sw128_desc(sK + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 0, 1024);
@@ -646,7 +674,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         tc_commit(&bars[B_S_FULL + qt]);
       };
       auto issue_pv = [&](int qt, uint32_t sV, bool acc_first) {
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           const uint64_t bd = sw128_desc(sV + kk * 2048, C::BN * 128, 1024);
           tc_mma_ts(tmem + 2 * C::BN + qt * C::HDV, tmem + qt * C::BN + kk * 8, bd, C::IDESC_PV,
@@ -665,6 +693,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         {
           const int ks = kc % C::NK;
           if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag)) { ok = false; break; }
+          fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.mma reads
           tc_fence_after();
           const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
           issue_s(0, sK);
@@ -679,6 +708,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag)) { ok = false; break; }
           if (!mbar_wait(&bars[B_P_FULL + 0], p_cnt0 & 1u, abort_flag)) { ok = false; break; }
           ++p_cnt0;
+          fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
           const uint32_t sV = sbase + C::OFF_V + vs * C::V_BYTES;
@@ -704,6 +734,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag)) { ok = false; break; }
           if (!mbar_wait(&bars[B_P_FULL + 0], p_cnt0 & 1u, abort_flag)) { ok = false; break; }
           ++p_cnt0;
+          fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t sV = sbase + C::OFF_V + vs * C::V_BYTES;
           issue_pv(0, sV, nt > 1);
@@ -724,20 +755,15 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       tc_commit(&bars[B_FINAL]);
       if (!mbar_wait_drain(&bars[B_FINAL], 0)) record_status(p.status, PKX_ETIMEOUT);
     }
-  } else {
-    // ------------------------------------------------ TMA loads (one warp)
-    uint32_t q_cnt = 0, kc = 0, vc = 0;
-    const CUtensorMap *kmap_pool = &tm.kp, *vmap_pool = &tm.vp;
-    const CUtensorMap *kmap_ext = &tm.ke, *vmap_ext = &tm.ve;
-    if (lane == 0) {
-      prefetch_tensormap(&tm.q);
-      prefetch_tensormap(kmap_pool);
-      prefetch_tensormap(vmap_pool);
-      if (MODE == kTwoStage) {
-        prefetch_tensormap(kmap_ext);
-        prefetch_tensormap(vmap_ext);
-      }
-    }
+  } else if (warp == 9) {
+    // --------------------------------------- Q tiles and row indices
+    // Lane 0 loads each unit's Q tiles (3-D TMA box: 64 dims, G heads,
+    // q_box_tok tokens; rows t * G + g).  Every lane resolves 4 keys of each
+    // tile to a pool slot (or extend row) into the index ring, ahead of the
+    // copy warps; -1 marks a key to zero-fill (past the tile's end, or an
+    // out-of-range slot, which is also recorded).
+    uint32_t q_cnt = 0, ic = 0;
+    if (lane == 0) prefetch_tensormap(&tm.q);
     const uint32_t q_box_bytes = 64u * 2u * G * p.q_box_tok;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
@@ -745,7 +771,6 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       const int nt = w.n_tiles;
       if (nt == 0) continue;
       const bool q1 = w.n_tok > TOK;
-      // Q tiles: box (64 dims, G heads, q_box_tok tokens), rows t * G + g.
       if (lane == 0) {
         if (q_cnt > 0 && !mbar_wait(&bars[B_Q_EMPTY], (q_cnt - 1) & 1u, abort_flag)) ok = false;
         if (ok) {
@@ -762,12 +787,10 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       ++q_cnt;
       const int64_t kv_base = p.kv_indptr[w.b];
       const int64_t ext_base = MODE == kTwoStage ? p.qo_indptr[w.b] : 0;
-      for (int j = 0; j < nt && ok; ++j) {
+      for (int j = 0; j < nt; ++j) {
         int kb, ke;
         tile_keys(w, j, kb, ke);
         const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
-        // rows of this lane's four keys (invalid keys repeat the tile's
-        // first row: their scores are masked, so P = 0 for them)
         int rows[4];
         bool bad = false;
 #pragma unroll
@@ -779,8 +802,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
               row = ext_base + (jpos - w.k_split);
             } else {
               row = MODE == kUnified
-                        ? static_cast<const int64_t *>(p.kv_indices)[kv_base + jpos]
-                        : (int64_t) static_cast<const int32_t *>(p.kv_indices)[kv_base + jpos];
+                        ? __ldg(static_cast<const int64_t *>(p.kv_indices) + kv_base + jpos)
+                        : (int64_t)__ldg(static_cast<const int32_t *>(p.kv_indices) + kv_base + jpos);
               if (row < 0 || row >= p.num_slots) {
                 bad = true;
                 row = -1;
@@ -790,56 +813,106 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           rows[i] = (int)row;
         }
         if (bad) record_status(p.status, PKX_EDEVICE);
-        int first = __shfl_sync(0xffffffffu, rows[0], 0);
-        if (first < 0) first = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (rows[i] < 0) rows[i] = first;
-        const CUtensorMap *km = from_ext ? kmap_ext : kmap_pool;
-        const CUtensorMap *vm = from_ext ? vmap_ext : vmap_pool;
-        const int kx = w.kvh * (int)(from_ext ? p.ke_sh : p.kb_sh);
-        const int vx = w.kvh * (int)(from_ext ? p.ve_sh : p.vb_sh);
+        const int is = ic % C::NI;
+        if (ic >= (uint32_t)C::NI &&
+            !mbar_wait(&i_empty[is], ((ic / C::NI) - 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        *reinterpret_cast<int4 *>(smem + C::OFF_I + is * C::I_BYTES + lane * 16) =
+            make_int4(rows[0], rows[1], rows[2], rows[3]);
+        mbar_arrive(&i_full[is]);
+        ++ic;
+      }
+    }
+    if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+  } else {
+    // ------------------------------------------------ K/V copies (6 warps)
+    // Thread ct copies 16-byte chunk (ct % CPR) of every KPP-th key of a
+    // tile into the swizzled K (then V) stage, then arrives (noinc) on the
+    // stage barrier when its own copies have landed: no thread ever blocks
+    // on its copies.
+    const int ct = tid - 10 * 32;
+    constexpr int CPR = HD / 8;                 // 16-byte chunks per row
+    constexpr int KPP = C::COPY_THREADS / CPR;  // keys per pass
+    constexpr int NKEYS = (C::BN + KPP - 1) / KPP;
+    const int ch = ct % CPR;
+    const int key0 = ct / CPR;
+    uint32_t kc = 0, vc = 0, ic = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
+      const WorkUnit w = p.units[u];
+      const int nt = w.n_tiles;
+      if (nt == 0) continue;
+      const bf16 *kp = p.k_pool + (int64_t)w.kvh * p.kb_sh + ch * 8;
+      const bf16 *vp = p.v_pool + (int64_t)w.kvh * p.vb_sh + ch * 8;
+      const bf16 *kx = p.k_ext + (int64_t)w.kvh * p.ke_sh + ch * 8;
+      const bf16 *vx = p.v_ext + (int64_t)w.kvh * p.ve_sh + ch * 8;
+      for (int j = 0; j < nt; ++j) {
+        int kb, ke;
+        tile_keys(w, j, kb, ke);
+        const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
+        // this thread's rows from the index ring
+        const int is = ic % C::NI;
+        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int *ring = reinterpret_cast<const int *>(smem + C::OFF_I + is * C::I_BYTES);
+        ++ic;
+        const bf16 *kbase = from_ext ? kx : kp;
+        const bf16 *vbase = from_ext ? vx : vp;
+        const int64_t kst = from_ext ? p.ke_st : p.kb_ss, vst = from_ext ? p.ve_st : p.vb_ss;
         // K tile
         const int ks = kc % C::NK;
-        if (lane == 0) {
-          if (kc >= (uint32_t)C::NK &&
-              !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag))
-            ok = false;
-          else
-            mbar_arrive_expect_tx(&k_full[ks], C::K_BYTES);
+        if (kc >= (uint32_t)C::NK &&
+            !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
         {
-          const uint32_t dst = sbase + C::OFF_K + ks * C::K_BYTES + lane * 4 * 128;
+          const uint32_t dst = sbase + C::OFF_K + ks * C::K_BYTES + (ch >> 3) * (C::BN * 128);
 #pragma unroll
-          for (int h = 0; h < HD / 64; ++h)
-            tma_gather4(dst + h * (C::BN * 128), km, kx + h * 64, rows[0], rows[1], rows[2],
-                        rows[3], &k_full[ks]);
+          for (int i = 0; i < NKEYS; ++i) {
+            const int key = key0 + i * KPP;
+            if (key < C::BN) {
+              const int row = ring[key];
+              const bool v = row >= 0;
+              cp_async_16(dst + sw128_off(key, ch & 7), v ? kbase + (int64_t)row * kst : p.k_pool,
+                          v ? 16u : 0u);
+            }
+          }
+          cp_async_arrive_noinc(&k_full[ks]);
         }
         ++kc;
         // V tile
         const int vs = vc % C::NV;
-        if (lane == 0) {
-          if (vc >= (uint32_t)C::NV &&
-              !mbar_wait(&v_empty[vs], ((vc / C::NV) - 1) & 1u, abort_flag))
-            ok = false;
-          else
-            mbar_arrive_expect_tx(&v_full[vs], C::V_BYTES);
+        if (vc >= (uint32_t)C::NV &&
+            !mbar_wait(&v_empty[vs], ((vc / C::NV) - 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
         {
-          const uint32_t dst = sbase + C::OFF_V + vs * C::V_BYTES + lane * 4 * 128;
+          const uint32_t dst = sbase + C::OFF_V + vs * C::V_BYTES + (ch >> 3) * (C::BN * 128);
 #pragma unroll
-          for (int h = 0; h < C::HDV / 64; ++h)
-            tma_gather4(dst + h * (C::BN * 128), vm, vx + h * 64, rows[0], rows[1], rows[2],
-                        rows[3], &v_full[vs]);
+          for (int i = 0; i < NKEYS; ++i) {
+            const int key = key0 + i * KPP;
+            if (key < C::BN) {
+              const int row = ring[key];
+              const bool v = row >= 0;
+              cp_async_16(dst + sw128_off(key, ch & 7), v ? vbase + (int64_t)row * vst : p.v_pool,
+                          v ? 16u : 0u);
+            }
+          }
+          cp_async_arrive_noinc(&v_full[vs]);
         }
         ++vc;
+        mbar_arrive(&i_empty[is]);  // this thread is done with the ring slot
       }
     }
     if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+    cp_async_wait_all();
+  }
   }
 
   tc_fence_before();
@@ -966,25 +1039,6 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D map over rows of `row_elems` bf16 (row stride `row_stride` elements),
-// box = 64 elements x 1 row, 128-byte swizzle (gather4 rows).
-static int make_row_map(CUtensorMap *m, const void *base, int64_t row_elems, int64_t rows,
-                        int64_t row_stride) {
-  auto fn = encode_fn();
-  if (!fn) return set_error(PKX_ECUDA, "cuTensorMapEncodeTiled unavailable");
-  cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)row_stride * 2};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return set_error(PKX_EINVAL, "tensor map (rows=%lld, row=%lld, stride=%lld) rejected: %d",
-                     (long long)rows, (long long)row_elems, (long long)row_stride, (int)r);
-  return PKX_OK;
-}
-
 // 3-D map over q [n, hq, lq]: box = 64 dims x G heads x tok tokens.
 static int make_q_map(CUtensorMap *m, const void *q, int64_t n, int hq, int lq, int G, int tok) {
   auto fn = encode_fn();
@@ -1038,19 +1092,6 @@ int launch_attention(const AttnArgs &a) {
   memset(&tm, 0, sizeof tm);
   int rc = make_q_map(&tm.q, a.q, nq, a.hq, a.lq, group, decode ? 1 : tok);
   if (rc != PKX_OK) return rc;
-  const int64_t krow = std::max<int64_t>(a.kb_ss, (int64_t)(a.hkv - 1) * a.kb_sh + a.lq);
-  const int64_t vrow = std::max<int64_t>(a.vb_ss, (int64_t)(a.hkv - 1) * a.vb_sh + a.lv);
-  if ((rc = make_row_map(&tm.kp, a.k_buf, krow, a.num_slots, a.kb_ss))) return rc;
-  if ((rc = make_row_map(&tm.vp, a.v_buf, vrow, a.num_slots, a.vb_ss))) return rc;
-  if (a.mode == kTwoStage) {
-    const int64_t kr = std::max<int64_t>(a.ke_st, (int64_t)(a.hkv - 1) * a.ke_sh + a.lq);
-    const int64_t vr = std::max<int64_t>(a.ve_st, (int64_t)(a.hkv - 1) * a.ve_sh + a.lv);
-    if ((rc = make_row_map(&tm.ke, a.k_ext, kr, nq, a.ke_st))) return rc;
-    if ((rc = make_row_map(&tm.ve, a.v_ext, vr, nq, a.ve_st))) return rc;
-  } else {
-    tm.ke = tm.kp;
-    tm.ve = tm.vp;
-  }
 
   SchedParams sp;
   sp.mode = a.mode;
@@ -1077,6 +1118,14 @@ int launch_attention(const AttnArgs &a) {
   KParams kp;
   kp.o = static_cast<bf16 *>(a.o);
   kp.lse = a.lse;
+  kp.k_pool = static_cast<const bf16 *>(a.k_buf);
+  kp.v_pool = static_cast<const bf16 *>(a.v_buf);
+  kp.k_ext = static_cast<const bf16 *>(a.mode == kTwoStage ? a.k_ext : a.k_buf);
+  kp.v_ext = static_cast<const bf16 *>(a.mode == kTwoStage ? a.v_ext : a.v_buf);
+  kp.kb_ss = a.kb_ss;
+  kp.vb_ss = a.vb_ss;
+  kp.ke_st = a.ke_st;
+  kp.ve_st = a.ve_st;
   kp.kb_sh = a.kb_sh;
   kp.vb_sh = a.vb_sh;
   kp.ke_sh = a.ke_sh;
