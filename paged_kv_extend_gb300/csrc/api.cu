@@ -34,7 +34,7 @@ static int check_heads(int hq, int hkv, int lq, int lv) {
     return set_error(PKX_EINVAL, "hq=%d must be a positive multiple of hkv=%d", hq, hkv);
   if (hq / hkv > kBlockM)
     return set_error(PKX_EUNSUPPORTED, "group size hq/hkv=%d > %d not built", hq / hkv, kBlockM);
-  const bool ok = (lq == 64 && lv == 64) || (lq == 128 && lv == 128);
+  const bool ok = (lq == 64 && lv == 64) || (lq == 128 && lv == 128) || (lq == 576 && lv == 512);
   if (!ok) return set_error(PKX_EUNSUPPORTED, "head dims (lq=%d, lv=%d) not built", lq, lv);
   return PKX_OK;
 }
@@ -73,14 +73,16 @@ size_t pkx_extend_workspace_size(int batch, int num_q_tokens, int hq, int hkv, i
   if (batch < 0 || num_q_tokens < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM ||
       lv <= 0)
     return 0;
-  (void)lq;
-  return ws_layout(batch, num_q_tokens, hkv, hq / hkv, lv, num_sms_current_device(), false).total;
+  return ws_layout(batch, num_q_tokens, hkv, hq / hkv, lv, num_sms_current_device(), false,
+                   lq == 576 && lv == 512)
+      .total;
 }
 
 size_t pkx_decode_workspace_size(int batch, int hq, int hkv, int lq, int lv) {
   if (batch < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM || lv <= 0) return 0;
-  (void)lq;
-  return ws_layout(batch, batch, hkv, hq / hkv, lv, num_sms_current_device(), true).total;
+  return ws_layout(batch, batch, hkv, hq / hkv, lv, num_sms_current_device(), true,
+                   lq == 576 && lv == 512)
+      .total;
 }
 
 int pkx_workspace_status(const void *workspace, void *stream) {

@@ -56,6 +56,8 @@ struct SchedParams {
   int mode;
   const int32_t *qo_indptr, *kv_indptr, *prefix_lens;
   int batch, hkv, tok, window, num_q_tokens;
+  int bn;        // keys per K/V tile
+  int n_dsplit;  // units per (block, split): value-dim slices (1, or 4 for MLA)
   int unit_target, qb_max, unit_max, comb_max, slot_max;
   int32_t *seq;  // 8 arrays of batch+1 ints
   int32_t *qbt;  // tiles per query block
@@ -122,10 +124,10 @@ __device__ __forceinline__ void qblock_range(const SchedParams &p, const SeqDims
 
 // Number of K/V tiles of the key range [kb, ke) when tiles may not straddle
 // `split` (the prefix / extend boundary of the two-stage form).
-__device__ __forceinline__ int range_tiles(int kb, int ke, int split) {
+__device__ __forceinline__ int range_tiles(int kb, int ke, int split, int bn) {
   const int pe = min(ke, split), eb = max(kb, split);
-  const int n_pre = pe > kb ? (pe - kb + kBlockN - 1) / kBlockN : 0;
-  const int n_ext = ke > eb ? (ke - eb + kBlockN - 1) / kBlockN : 0;
+  const int n_pre = pe > kb ? (pe - kb + bn - 1) / bn : 0;
+  const int n_ext = ke > eb ? (ke - eb + bn - 1) / bn : 0;
   return n_pre + n_ext;
 }
 
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     for (int qb = 0; qb < d.nqb; ++qb) {
       int lo, hi, i0, i1;
       qblock_range(p, d, qb, lo, hi, i0, i1);
-      int nt = (hi - lo + kBlockN - 1) / kBlockN;
+      int nt = (hi - lo + p.bn - 1) / p.bn;
       p.qbt[qboff[b] + qb] = nt;
       w += nt;
     }
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     if (tid < off) sh[tid] = min(sh[tid] + sh[tid + off], 0x3fffffff);
     __syncthreads();
   }
-  const long long total_tiles = (long long)sh[0] * p.hkv;
+  const long long total_tiles = (long long)sh[0] * p.hkv * p.n_dsplit;
   __syncthreads();
   if (tid == 0) {
     long long c = (total_tiles + p.unit_target - 1) / p.unit_target;
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
         c += 1;
       }
     }
-    ucnt[rk] = u * p.hkv;
+    ucnt[rk] = u * p.hkv * p.n_dsplit;
     scnt[rk] = s * p.hkv;
     ccnt[rk] = c * p.hkv;
   }
@@ -291,19 +293,22 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
           p.comb[co++] = e;
         }
         for (int s = 0; s < S; ++s) {
-          WorkUnit w;
-          w.q_tok0 = d.qbase + i0;
-          w.n_tok = i1 - i0;
-          w.qpos0 = d.P + i0;
-          w.kvh = kvh;
-          w.k_begin = min(hi, lo + s * tps * kBlockN);
-          w.k_end = min(hi, lo + (s + 1) * tps * kBlockN);
-          w.k_split = split_at;
-          w.n_tiles = range_tiles(w.k_begin, w.k_end, split_at);
-          w.b = b;
-          w.slot = S > 1 ? so + s : -1;
-          w.pad[0] = w.pad[1] = 0;
-          p.units[uo++] = w;
+          for (int dq = 0; dq < p.n_dsplit; ++dq) {
+            WorkUnit w;
+            w.q_tok0 = d.qbase + i0;
+            w.n_tok = i1 - i0;
+            w.qpos0 = d.P + i0;
+            w.kvh = kvh;
+            w.k_begin = min(hi, lo + s * tps * p.bn);
+            w.k_end = min(hi, lo + (s + 1) * tps * p.bn);
+            w.k_split = split_at;
+            w.n_tiles = range_tiles(w.k_begin, w.k_end, split_at, p.bn);
+            w.b = b;
+            w.slot = S > 1 ? so + s : -1;
+            w.dq = dq;
+            w.pad = 0;
+            p.units[uo++] = w;
+          }
         }
         if (S > 1) so += S;
       }
@@ -317,6 +322,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
 
 // ============================================================ attention ====
 struct KParams {
+  const bf16 *q;  // read directly by the MLA kernel (the GQA kernel uses the TMA map)
   bf16 *o;
   float *lse;
   const bf16 *k_pool, *v_pool, *k_ext, *v_ext;
@@ -385,15 +391,16 @@ enum {
 };
 
 // Key range [kb, ke) of tile j of a unit (tiles never straddle k_split).
+template <int BN = kBlockN>
 __device__ __forceinline__ void tile_keys(const WorkUnit &w, int j, int &kb, int &ke) {
   const int pe = min(w.k_end, w.k_split);
-  const int n_pre = pe > w.k_begin ? (pe - w.k_begin + kBlockN - 1) / kBlockN : 0;
+  const int n_pre = pe > w.k_begin ? (pe - w.k_begin + BN - 1) / BN : 0;
   if (j < n_pre) {
-    kb = w.k_begin + j * kBlockN;
-    ke = min(kb + kBlockN, pe);
+    kb = w.k_begin + j * BN;
+    ke = min(kb + BN, pe);
   } else {
-    kb = max(w.k_begin, w.k_split) + (j - n_pre) * kBlockN;
-    ke = min(kb + kBlockN, w.k_end);
+    kb = max(w.k_begin, w.k_split) + (j - n_pre) * BN;
+    ke = min(kb + BN, w.k_end);
   }
 }
 
@@ -924,6 +931,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
   }
 }
 
+// ================================================================== MLA ====
+#include "mla_kernel.cuh"
+
 // ============================================================== combine ====
 // Merge the split-KV partials of every split query block: with lse_i the
 // partial log-sum-exps and o_i the partial (normalised) outputs,
@@ -992,20 +1002,21 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Rows of one split-KV partial slot: both Q tiles of an extend block, or the
 // group's rows of a decode query.
-int rows_per_slot(bool decode, int group) {
-  return decode ? group : 2 * tokens_per_block(group) * group;
+int rows_per_slot(bool decode, int group, bool mla) {
+  return decode ? group : (mla ? 1 : 2) * tokens_per_block(group) * group;
 }
 
 WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int num_sms,
-                   bool decode) {
+                   bool decode, bool mla) {
   WsLayout L{};
-  const int tok = 2 * tokens_per_block(group);  // tokens of a two-Q-tile block
+  // tokens of a query block: two Q tiles (GQA kernel) or one (MLA kernel)
+  const int tok = (mla ? 1 : 2) * tokens_per_block(group);
   L.unit_target = 4 * (num_sms > 0 ? num_sms : 160);
   L.qb_max = (tok > 0 ? (num_q_tokens + tok - 1) / tok : 0) + batch + 1;
-  L.unit_max = L.unit_target + hkv * L.qb_max;
+  L.unit_max = (L.unit_target + hkv * L.qb_max) * (mla ? 4 : 1);
   L.slot_max = 2 * L.unit_target;
   L.comb_max = L.unit_target;
-  L.rows_per_slot = rows_per_slot(decode, group);
+  L.rows_per_slot = rows_per_slot(decode, group, mla);
   size_t off = align256(sizeof(WsHeader));
   L.seq_off = off;
   off = align256(off + sizeof(int32_t) * 8 * (size_t)(batch + 1));
@@ -1069,13 +1080,38 @@ static int launch_attn_kernel(const TMaps &tmaps, const KParams &kp, int grid, c
   return PKX_OK;
 }
 
+template <int MODE>
+static int launch_mla_kernel(const KParams &kp, int grid, cudaStream_t s) {
+  using C = MlaCfg<MODE>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(mla_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess)
+      return set_error(PKX_ECUDA, "cudaFuncSetAttribute(mla_kernel): %s", cudaGetErrorString(e));
+    configured = true;
+  }
+  mla_kernel<MODE><<<grid, C::THREADS, C::SMEM, s>>>(kp);
+  return PKX_OK;
+}
+
 int launch_attention(const AttnArgs &a) {
   const int group = a.hq / a.hkv;
   const int nsm = num_sms_current_device();
   if (nsm <= 0) return set_error(PKX_ECUDA, "cannot query the current device");
   const bool decode = a.mode == kDecode;
+  const bool mla = a.lq == 576 && a.lv == 512;
   const int nq = decode ? a.batch : a.num_q_tokens;
-  WsLayout L = ws_layout(a.batch, nq, a.hkv, group, a.lv, nsm, decode);
+  WsLayout L = ws_layout(a.batch, nq, a.hkv, group, a.lv, nsm, decode, mla);
+  if (mla) {
+    // V must be the first 512 dims of each K row (the MLA layout).
+    const bool pool_alias = a.v_buf == a.k_buf && a.vb_ss == a.kb_ss && a.vb_sh == a.kb_sh;
+    const bool ext_alias = a.mode != kTwoStage ||
+                           (a.v_ext == a.k_ext && a.ve_st == a.ke_st && a.ve_sh == a.ke_sh);
+    if (!pool_alias || !ext_alias)
+      return set_error(PKX_EUNSUPPORTED,
+                       "Lq=576/Lv=512 needs V to be the first 512 dims of each K row");
+  }
   if (a.workspace == nullptr || a.workspace_bytes < L.total)
     return set_error(PKX_EWORKSPACE, "workspace of %zu bytes given, %zu needed",
                      a.workspace_bytes, L.total);
@@ -1090,8 +1126,9 @@ int launch_attention(const AttnArgs &a) {
   // tensor maps
   TMaps tm;
   memset(&tm, 0, sizeof tm);
-  int rc = make_q_map(&tm.q, a.q, nq, a.hq, a.lq, group, decode ? 1 : tok);
-  if (rc != PKX_OK) return rc;
+  int rc = PKX_OK;
+  if (!mla && (rc = make_q_map(&tm.q, a.q, nq, a.hq, a.lq, group, decode ? 1 : tok)) != PKX_OK)
+    return rc;
 
   SchedParams sp;
   sp.mode = a.mode;
@@ -1100,7 +1137,9 @@ int launch_attention(const AttnArgs &a) {
   sp.prefix_lens = a.prefix_lens;
   sp.batch = a.batch;
   sp.hkv = a.hkv;
-  sp.tok = 2 * tok;
+  sp.tok = (mla ? 1 : 2) * tok;
+  sp.bn = mla ? MlaCfg<0>::BN : kBlockN;
+  sp.n_dsplit = mla ? MlaCfg<0>::LV / MlaCfg<0>::DVS : 1;
   sp.window = a.window;
   sp.num_q_tokens = nq;
   sp.unit_target = L.unit_target;
@@ -1116,6 +1155,7 @@ int launch_attention(const AttnArgs &a) {
   sched_kernel<<<1, 1024, 0, a.stream>>>(sp);
 
   KParams kp;
+  kp.q = static_cast<const bf16 *>(a.q);
   kp.o = static_cast<bf16 *>(a.o);
   kp.lse = a.lse;
   kp.k_pool = static_cast<const bf16 *>(a.k_buf);
@@ -1164,6 +1204,10 @@ int launch_attention(const AttnArgs &a) {
     if (a.mode == kTwoStage) rc = launch_attn_kernel<64, kTwoStage>(tm, kp, grid, a.stream);
     else if (a.mode == kUnified) rc = launch_attn_kernel<64, kUnified>(tm, kp, grid, a.stream);
     else rc = launch_attn_kernel<64, kDecode>(tm, kp, grid, a.stream);
+  } else if (mla) {
+    if (a.mode == kTwoStage) rc = launch_mla_kernel<kTwoStage>(kp, grid, a.stream);
+    else if (a.mode == kUnified) rc = launch_mla_kernel<kUnified>(kp, grid, a.stream);
+    else rc = launch_mla_kernel<kDecode>(kp, grid, a.stream);
   } else {
     return set_error(PKX_EUNSUPPORTED, "head dims (%d, %d) not built", a.lq, a.lv);
   }

@@ -1,0 +1,434 @@
+// mla_kernel.cuh -- extend / decode attention for the MLA head shape
+// (Lq = 576 = 512 latent + 64 rope dims, Lv = 512, one KV head, V = the first
+// 512 dims of each K row), included by attention.cu.
+//
+// The MLA layout (sglang cpu_graph_runner.py, qkv_proj_with_rope fake: V is a
+// narrow view of K; extend_attention.py, _get_block_sizes_for_extend_attention:
+// 576 = 512 + 64) makes the score a single 576-dim dot product, and V need not
+// be loaded separately: the K tile in shared memory is also the V operand.
+//
+// TMEM holds 512 columns of 32 bits.  A 128-row tile of O over all 512 value
+// dims would fill it, leaving no room for S, so each work unit produces one
+// 128-dim slice of the value dims (w.dq) and recomputes S for it:
+//   TMEM  [0, 288)   Q tile, bf16 pairs (A operand of QK^T, TMEM form)
+//         [320, 384) S (fp32); P (bf16 pairs) is written over its first 32
+//         [384, 512) O slice (fp32)
+//   SMEM  three stages of a 64-key K tile (64 x 576 bf16, 128-byte swizzle,
+//         nine 64-dim blocks) + a ring of resolved row indices.
+// QK^T reads A = Q from TMEM and B = K from SMEM; PV reads A = P from TMEM and
+// B = columns [128 dq, 128 dq + 128) of the same K tile, as an MN-major
+// operand.  Warps: 0-3 softmax (one row per thread; they also write Q into
+// TMEM), 4 MMA issue, 5 row indices, 6-11 K-row copies (cp.async).
+
+template <int MODE>
+struct MlaCfg {
+  static constexpr int BM = kBlockM, BN = 64;
+  static constexpr int LQ = 576, LV = 512, DVS = 128;  // value dims per unit
+  static constexpr int NK = 3, NI = 4;
+  static constexpr int K_BYTES = BN * LQ * 2;  // 73728
+  static constexpr int I_BYTES = BN * 4;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_I = NK * K_BYTES;
+  static constexpr int OFF_BAR = OFF_I + NI * I_BYTES;
+  static constexpr int N_BARS = 8 + 2 * NK + 2 * NI;
+  static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 1024;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int Q_COL = 0, S_COL = 320, O_COL = 384;
+  static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DVS, 1);
+  static constexpr int THREADS = 384;
+  static constexpr int COPY_THREADS = 192;
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+enum { M_Q_FULL = 0, M_S_FULL = 1, M_P_FULL = 2, M_O_DONE = 3, M_FINAL = 4, M_RING = 8 };
+
+template <int MODE>
+__global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KParams p) {
+  using C = MlaCfg<MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *k_full = bars + M_RING;
+  uint64_t *k_empty = k_full + C::NK;
+  uint64_t *i_full = k_empty + C::NK;
+  uint64_t *i_empty = i_full + C::NI;
+  volatile int *abort_flag = &s_abort;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    mbar_init(&bars[M_Q_FULL], 128);
+    mbar_init(&bars[M_S_FULL], 1);
+    mbar_init(&bars[M_P_FULL], 128);
+    mbar_init(&bars[M_O_DONE], 1);
+    mbar_init(&bars[M_FINAL], 1);
+    for (int s = 0; s < C::NK; ++s) {
+      mbar_init(&k_full[s], C::COPY_THREADS);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < C::NI; ++s) {
+      mbar_init(&i_full[s], 32);
+      mbar_init(&i_empty[s], C::COPY_THREADS);
+    }
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(&s_tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int n_units = p.hdr->n_units;
+  const int G = p.group;
+
+  if (warp < 4) {
+    // ------------------------------------------- Q -> TMEM, softmax, epilogue
+    const int r = tid;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    uint32_t s_cnt = 0, o_cnt = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+      const WorkUnit w = p.units[u];
+      const int nt = w.n_tiles;
+      const int rows_valid = w.n_tok * G;
+      const bool valid = r < rows_valid;
+      const bool warp_active = warp * 32 < rows_valid;
+      const int t = r / G, g = r - (r / G) * G;
+      const int qpos = w.qpos0 + t;
+      const int qmax = w.qpos0 + w.n_tok - 1;
+      const int64_t orow_idx = (int64_t)(w.q_tok0 + t) * p.hq + w.kvh * G + g;
+      const int64_t prow_idx = (int64_t)w.slot * p.rows_per_slot + r;
+      const int dv0 = w.dq * C::DVS;
+      if (nt == 0) {
+        if (valid) {
+          if (w.slot < 0) {
+            bf16 *orow = p.o + orow_idx * C::LV + dv0;
+            for (int c = 0; c < C::DVS; c += 8)
+              *reinterpret_cast<uint4 *>(orow + c) = make_uint4(0, 0, 0, 0);
+            if (p.lse && w.dq == 0) p.lse[orow_idx] = -INFINITY;
+          } else {
+            float *prow = p.po + prow_idx * C::LV + dv0;
+            for (int c = 0; c < C::DVS; c += 4)
+              *reinterpret_cast<float4 *>(prow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (w.dq == 0) p.plse[prow_idx] = -INFINITY;
+          }
+        }
+        continue;
+      }
+      // Q row (576 bf16) into TMEM columns [0, 288) as bf16 pairs; rows past
+      // the block get zeros.  The previous unit's MMAs have all completed
+      // (its epilogue waited for them), so Q's columns are free.
+      {
+        const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + orow_idx * C::LQ);
+#pragma unroll 1
+        for (int c = 0; c < C::LQ / 64; ++c) {
+          uint32_t v[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 x = valid ? __ldg(qrow + c * 8 + i) : make_uint4(0, 0, 0, 0);
+            v[4 * i + 0] = x.x;
+            v[4 * i + 1] = x.y;
+            v[4 * i + 2] = x.z;
+            v[4 * i + 3] = x.w;
+          }
+          tmem_st32(lane_base + C::Q_COL + c * 32, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars[M_Q_FULL]);
+      }
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nt; ++j) {
+        int kb, ke;
+        tile_keys<C::BN>(w, j, kb, ke);
+        if (!mbar_wait(&bars[M_S_FULL], s_cnt & 1u, abort_flag)) {
+          abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+          break;
+        }
+        ++s_cnt;
+        tc_fence_after();
+        if (warp_active) {
+          float x[C::BN];
+          {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(lane_base + C::S_COL + 0, v0);
+            tmem_ld32(lane_base + C::S_COL + 32, v1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              x[i] = __uint_as_float(v0[i]);
+              x[32 + i] = __uint_as_float(v1[i]);
+            }
+          }
+          if (p.use_cap) {
+#pragma unroll
+            for (int i = 0; i < C::BN; ++i) x[i] = p.cap_log2 * tanh_approx(x[i] * p.cap_pre);
+          } else {
+#pragma unroll
+            for (int i = 0; i < C::BN; ++i) x[i] *= p.scale_log2;
+          }
+          const bool need_mask = (ke - 1 > w.qpos0) || (ke - kb < C::BN) ||
+                                 (p.window > 0 && kb < qmax - p.window);
+          if (need_mask) {
+#pragma unroll
+            for (int i = 0; i < C::BN; ++i) {
+              const int kpos = kb + i;
+              const bool vis =
+                  kpos < ke && kpos <= qpos && (p.window <= 0 || qpos - kpos <= p.window);
+              if (!vis) x[i] = -INFINITY;
+            }
+          }
+          float mt0 = x[0], mt1 = x[1];
+#pragma unroll
+          for (int i = 2; i < C::BN; i += 2) {
+            mt0 = fmaxf(mt0, x[i]);
+            mt1 = fmaxf(mt1, x[i + 1]);
+          }
+          const float m_new = fmaxf(m, fmaxf(mt0, mt1));
+          const bool grow = m_new > m + 8.0f;
+          const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
+          const bool o_needs = grow && j > 0 && l > 0.f;
+          if (grow) {
+            l *= alpha;
+            m = m_new;
+          }
+          const float mref = m == -INFINITY ? 0.f : m;
+          uint32_t pk[32];
+          float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < C::BN; i += 2) {
+            const float e0 = ex2_approx(x[i] - mref);
+            const float e1 = ex2_approx(x[i + 1] - mref);
+            l0 += e0;
+            l1 += e1;
+            pk[i / 2] = pack_bf16(e0, e1);
+          }
+          l += l0 + l1;
+          tmem_st32(lane_base + C::S_COL, pk);
+          if (__any_sync(0xffffffffu, o_needs)) {
+            const float a = o_needs ? alpha : 1.0f;
+            uint32_t v[32];
+#pragma unroll
+            for (int c = 0; c < C::DVS / 32; ++c) {
+              const uint32_t ta = lane_base + C::O_COL + c * 32;
+              tmem_ld32(ta, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+              tmem_st32(ta, v);
+            }
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars[M_P_FULL]);
+      }
+      if (*abort_flag) break;
+      if (!mbar_wait(&bars[M_O_DONE], o_cnt & 1u, abort_flag)) {
+        abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+        break;
+      }
+      ++o_cnt;
+      tc_fence_after();
+      if (warp_active) {
+        const float inv = l > 0.f ? 1.0f / l : 0.f;
+        const float lse_v = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        uint32_t v[32];
+#pragma unroll
+        for (int c = 0; c < C::DVS / 32; ++c) {
+          tmem_ld32(lane_base + C::O_COL + c * 32, v);
+          tmem_wait_ld();
+          if (valid) {
+            if (w.slot < 0) {
+              bf16 *orow = p.o + orow_idx * C::LV + dv0 + c * 32;
+#pragma unroll
+              for (int i = 0; i < 32; i += 8) {
+                uint4 q4;
+                q4.x = pack_bf16(__uint_as_float(v[i + 0]) * inv, __uint_as_float(v[i + 1]) * inv);
+                q4.y = pack_bf16(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+                q4.z = pack_bf16(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv);
+                q4.w = pack_bf16(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
+                *reinterpret_cast<uint4 *>(orow + i) = q4;
+              }
+            } else {
+              float *prow = p.po + prow_idx * C::LV + dv0 + c * 32;
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4 *>(prow + i) =
+                    make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
+                                __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+            }
+          }
+        }
+        if (valid && w.dq == 0) {
+          if (w.slot < 0) {
+            if (p.lse) p.lse[orow_idx] = lse_v;
+          } else {
+            p.plse[prow_idx] = lse_v;
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------ MMA issue (one thread)
+    if (lane == 0) {
+      uint32_t q_cnt = 0, kc = 0, p_cnt = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
+        const WorkUnit w = p.units[u];
+        const int nt = w.n_tiles;
+        if (nt == 0) continue;
+        if (!mbar_wait(&bars[M_Q_FULL], q_cnt & 1u, abort_flag)) { ok = false; break; }
+        ++q_cnt;
+        tc_fence_after();
+        for (int j = 0; j < nt; ++j) {
+          const int ks = kc % C::NK;
+          if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag)) { ok = false; break; }
+          fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.mma reads
+          tc_fence_after();
+          const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
+#pragma unroll 1
+          for (int kk = 0; kk < C::LQ / 16; ++kk) {
+            const uint64_t bd = sw128_desc(sK + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 0, 1024);
+            tc_mma_ts(tmem + C::S_COL, tmem + C::Q_COL + kk * 8, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&bars[M_S_FULL]);
+          if (!mbar_wait(&bars[M_P_FULL], p_cnt & 1u, abort_flag)) { ok = false; break; }
+          ++p_cnt;
+          tc_fence_after();
+          const uint32_t sV = sK + (w.dq * (C::DVS / 64)) * (C::BN * 128);
+#pragma unroll 1
+          for (int kk = 0; kk < C::BN / 16; ++kk) {
+            const uint64_t bd = sw128_desc(sV + kk * 2048, C::BN * 128, 1024);
+            tc_mma_ts(tmem + C::O_COL, tmem + C::S_COL + kk * 8, bd, C::IDESC_PV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&k_empty[ks]);
+          ++kc;
+        }
+        if (!ok) break;
+        tc_commit(&bars[M_O_DONE]);
+      }
+      if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+      tc_commit(&bars[M_FINAL]);
+      if (!mbar_wait_drain(&bars[M_FINAL], 0)) record_status(p.status, PKX_ETIMEOUT);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------ row indices (one warp)
+    uint32_t ic = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
+      const WorkUnit w = p.units[u];
+      const int nt = w.n_tiles;
+      if (nt == 0) continue;
+      const int64_t kv_base = p.kv_indptr[w.b];
+      const int64_t ext_base = MODE == kTwoStage ? p.qo_indptr[w.b] : 0;
+      for (int j = 0; j < nt; ++j) {
+        int kb, ke;
+        tile_keys<C::BN>(w, j, kb, ke);
+        const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
+        int rows[2];
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int jpos = kb + 2 * lane + i;
+          int64_t row = -1;
+          if (jpos < ke) {
+            if (from_ext) {
+              row = ext_base + (jpos - w.k_split);
+            } else {
+              row = MODE == kUnified
+                        ? __ldg(static_cast<const int64_t *>(p.kv_indices) + kv_base + jpos)
+                        : (int64_t)__ldg(static_cast<const int32_t *>(p.kv_indices) + kv_base + jpos);
+              if (row < 0 || row >= p.num_slots) {
+                bad = true;
+                row = -1;
+              }
+            }
+          }
+          rows[i] = (int)row;
+        }
+        if (bad) record_status(p.status, PKX_EDEVICE);
+        const int is = ic % C::NI;
+        if (ic >= (uint32_t)C::NI &&
+            !mbar_wait(&i_empty[is], ((ic / C::NI) - 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        *reinterpret_cast<int2 *>(smem + C::OFF_I + is * C::I_BYTES + lane * 8) =
+            make_int2(rows[0], rows[1]);
+        mbar_arrive(&i_full[is]);
+        ++ic;
+      }
+    }
+    if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+  } else {
+    // ------------------------------------------------ K-row copies (6 warps)
+    const int ct = tid - 6 * 32;
+    constexpr int CPR = C::LQ / 8;  // 72 chunks of 16 bytes per row
+    constexpr int NCH = C::BN * CPR / C::COPY_THREADS;  // 24 chunks per thread
+    static_assert(C::BN * CPR % C::COPY_THREADS == 0, "even split of a tile");
+    uint32_t kc = 0, ic = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
+      const WorkUnit w = p.units[u];
+      const int nt = w.n_tiles;
+      if (nt == 0) continue;
+      const bf16 *kp = p.k_pool + (int64_t)w.kvh * p.kb_sh;
+      const bf16 *kx = p.k_ext + (int64_t)w.kvh * p.ke_sh;
+      for (int j = 0; j < nt; ++j) {
+        int kb, ke;
+        tile_keys<C::BN>(w, j, kb, ke);
+        const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
+        const int is = ic % C::NI;
+        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int *ring = reinterpret_cast<const int *>(smem + C::OFF_I + is * C::I_BYTES);
+        ++ic;
+        const int ks = kc % C::NK;
+        if (kc >= (uint32_t)C::NK &&
+            !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const bf16 *base = from_ext ? kx : kp;
+        const int64_t st = from_ext ? p.ke_st : p.kb_ss;
+        const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
+#pragma unroll 4
+        for (int i = 0; i < NCH; ++i) {
+          const int c = ct + i * C::COPY_THREADS;
+          const int key = c / CPR, ch = c - (c / CPR) * CPR;
+          const int row = ring[key];
+          const bool v = row >= 0;
+          cp_async_16(sK + (ch >> 3) * (C::BN * 128) + sw128_off(key, ch & 7),
+                      v ? base + (int64_t)row * st + ch * 8 : p.k_pool, v ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(&k_full[ks]);
+        mbar_arrive(&i_empty[is]);
+        ++kc;
+      }
+    }
+    if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+    cp_async_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}

@@ -40,7 +40,8 @@ struct WorkUnit {
   int32_t n_tiles;  // K/V tiles (no tile straddles k_split)
   int32_t b;        // sequence
   int32_t slot;     // -1: write o/lse; else split-KV partial slot
-  int32_t pad[2];
+  int32_t dq;       // value-dim slice (MLA: 128 of the 512 value dims)
+  int32_t pad;
 };
 
 // A query block whose key range was split: its partials live in slots
@@ -79,9 +80,9 @@ int num_sms_current_device();
 // Events set by pkx_set_attention_events for this thread (may be null).
 void attention_events(cudaEvent_t *before, cudaEvent_t *after);
 int tokens_per_block(int group);
-int rows_per_slot(bool decode, int group);
+int rows_per_slot(bool decode, int group, bool mla);
 WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int num_sms,
-                   bool decode);
+                   bool decode, bool mla);
 
 // Arguments of one attention launch (any key mode).
 struct AttnArgs {

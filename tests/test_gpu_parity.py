@@ -285,3 +285,86 @@ def test_full_size_decode():
     assert pkx.workspace_status(ws) == 0
     ro, rl = oracle_decode(wl)
     assert_close(o, lse, ro, rl, "decode_gqa")
+
+
+# ------------------------------------------------------------------ MLA
+MLA_SMALL = [
+    # (prefix, extend, cap, window)
+    ([0, 70, 300], [9, 1, 130], 0.0, -1),
+    ([33, 0], [64, 200], 0.0, 50),
+    ([129, 5, 2], [17, 40, 3], 20.0, -1),
+]
+
+
+@pytest.mark.parametrize("prefix,extend,cap,window", MLA_SMALL)
+def test_mla_small_vs_oracle(prefix, extend, cap, window):
+    """MLA head (Lq=576 = 512 latent + 64 rope, Lv=512, V = the first 512
+    dims of K, one KV head, 16 query heads)."""
+    spec = W.small_spec(batch=len(prefix), hq=16, hkv=1, lq=576, lv=512, prefix=prefix,
+                        extend=extend, logit_cap=cap, sliding_window=window, std=0.5,
+                        v_aliases_k=True, sm_scale=1.0 / math.sqrt(192.0),
+                        seed=sum(prefix) + 5 * sum(extend))
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.extend()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_extend(wl)
+    assert_close(o, lse, ro, rl, "mla extend")
+    uo, ul, ws2 = dw.unified()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws2) == 0
+    assert_close(uo, ul, ro, rl, "mla unified")
+
+
+def test_mla_decode_small_vs_oracle():
+    lens = [1, 64, 65, 1000, 3]
+    spec = W.WorkloadSpec("dec", batch=len(lens), hq=16, hkv=1, lq=576, lv=512,
+                          prefix=[x - 1 for x in lens], extend=[1] * len(lens),
+                          num_slots=4096, sm_scale=1.0 / math.sqrt(192.0), std=0.5,
+                          seed=31, v_aliases_k=True, decode=True)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.decode()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_decode(wl)
+    assert_close(o, lse, ro, rl, "mla decode")
+
+
+def test_mla_requires_v_alias():
+    """Lq=576/Lv=512 with a V pool that is not a view of K is refused."""
+    spec = W.small_spec(batch=1, hq=16, hkv=1, lq=576, lv=512, prefix=[4], extend=[4],
+                        seed=2, v_aliases_k=True)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    dw.v_buffer = dw.v_buffer.clone()
+    o, lse = dw.out()
+    with pytest.raises(pkx.PkxError) as e:
+        dw.extend()
+    assert e.value.code == pkx.PKX_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("name", ["mla"])
+def test_full_size_mla_sampled_rows(name):
+    wl = W.draw(W.SPECS[name])
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.extend()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    rows = sample_rows(wl.n_q_tokens, wl.spec.hq, 2048, seed=78)
+    ro, rl = oracle_extend(wl, rows=rows)
+    go = o.view(-1, o.shape[-1])[rows.to(DEV)]
+    gl = lse.view(-1)[rows.to(DEV)]
+    assert_close(go, gl, ro, rl, name)
+    assert torch.isfinite(o.float()).all()
+
+
+def test_full_size_decode_mla():
+    wl = W.draw(W.SPECS["decode_mla"])
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.decode()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_decode(wl)
+    assert_close(o, lse, ro, rl, "decode_mla")
