@@ -231,7 +231,8 @@ def run_reference(args, ws, rank):
         return 0
     import oracle
     oracle.build()
-    wl = W.draw(W.SPECS[WORKLOAD])
+    name = args.workload if not W.SPECS[args.workload].decode else WORKLOAD
+    wl = W.draw(W.SPECS[name])
     k_ext, v_ext = wl.extend_kv()
     kb, vb = wl.pool()
     # size each step so the whole run stays within about two minutes
@@ -246,7 +247,7 @@ def run_reference(args, ws, rank):
         tot_f += fl
     value = tot_f / tot_t / 1e12
     cores = oracle.num_threads()
-    sample = (f"{nrows} random (token, q-head) rows of the {WORKLOAD} workload per step "
+    sample = (f"{nrows} random (token, q-head) rows of the {name} workload per step "
               f"(of {wl.n_q_tokens * wl.spec.hq}); float64 oracle")
     line = {
         "impl": "reference", "metric": "extend-attn TFLOP/s", "value": value, "unit": "TFLOP/s",
@@ -262,20 +263,36 @@ def run_reference(args, ws, rank):
     return 0
 
 
+WORKLOAD_TEXT = {
+    "llama3_8b": "batch=16 Hq=32 Hkv=8 D=128 prefix~U[0,4096] extend~U[1,1024] pool=2^18 slots "
+                 "(permuted) bf16 N(0,1) sm_scale=1/sqrt(128)",
+    "long_prefix": "batch=64 Hq=32 Hkv=8 D=128 prefix=8192 extend=16 pool=2^20 slots (permuted) "
+                   "bf16 N(0,1) logit_cap=30",
+    "mla": "batch=8 Hq=16 Hkv=1 Lq=576 (512+64 rope) Lv=512 (V aliases K) prefix=2048 extend=512 "
+           "pool=65536 slots (permuted) bf16 N(0,0.5) sm_scale=1/sqrt(192)",
+    "heavy_tail": "256 seqs Hq=28 Hkv=4 D=128 prefix,extend~lognormal(6,1.2) clipped [0,16384]/"
+                  "[1,4096] sliding_window=4096 pool=2^22 slots (permuted) bf16 N(0,1)",
+    "tiny": "batch=2 Hq=4 Hkv=2 D=64 prefix={16,0} extend={8,5} pool=64 slots sm_scale=1/8",
+    "decode_gqa": "decode: batch=64 Hq=32 Hkv=8 D=128 T=8193 pool=2^20 slots (permuted)",
+    "decode_mla": "decode: batch=64 Hq=16 Hkv=1 Lq=576 Lv=512 (V aliases K) T=4096 pool=2^20 slots",
+}
+
+
 def config_dict(wl):
     s = wl.spec
-    return {"workload": (f"{s.name}: batch={s.batch} Hq={s.hq} Hkv={s.hkv} D={s.lq} "
-                         f"prefix~U[0,4096] extend~U[1,1024] pool={s.num_slots} slots "
-                         f"(permuted) bf16 N(0,1) sm_scale=1/sqrt(128)"),
+    step = ("decode_attention_fwd" if s.decode else
+            "build_unified_kv_indices + extend_attention_fwd_unified")
+    return {"workload": f"{s.name}: {WORKLOAD_TEXT.get(s.name, '')}",
             "batch": s.batch, "q_tokens": wl.n_q_tokens,
             "kv_tokens": int(sum(wl.prefix_lens) + sum(wl.extend_lens)),
             "seed": s.seed, "l2": "flushed before every timed step (512 MiB write)",
-            "step": "build_unified_kv_indices + extend_attention_fwd_unified"}
+            "step": step}
 
 
 # ------------------------------------------------------------- our arm
 class ExtendStep:
-    """Device-resident inputs and the one-step call sequence."""
+    """Device-resident inputs and the one-step call sequence (unified
+    index build + unified extend attention)."""
 
     def __init__(self, wl: W.Workload, dev):
         from paged_kv_extend_gb300 import pkx
@@ -301,6 +318,12 @@ class ExtendStep:
         nbytes = pkx.extend_workspace_size(wl.batch, n, s.hq, s.hkv, s.lq, s.lv)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.launches = 4  # index build, scheduler, attention, combine
+        self.flops = extend_flops(wl)
+        self.bytes = extend_bytes(wl, unified=True)
+
+    def inputs(self):
+        return [self.q, self.prefix_indptr, self.prefix_indices, self.extend_start,
+                self.extend_lens, self.extend_indices, self.qo_indptr]
 
     def __call__(self):
         s = self.wl.spec
@@ -311,6 +334,42 @@ class ExtendStep:
         self.pkx.extend_attention_fwd_unified(
             self.q, self.o, self.kb, self.vb, self.qo_indptr, self.uptr, self.uidx, self.plen,
             self.wl.sm_scale, s.logit_cap, s.sliding_window, lse=self.lse, workspace=self.ws)
+
+
+class DecodeStep:
+    """One decode step over a decode workload (one query per sequence)."""
+
+    def __init__(self, wl: W.Workload, dev):
+        from paged_kv_extend_gb300 import pkx
+        self.pkx = pkx
+        s = wl.spec
+        self.wl = wl
+        self.kb, self.vb = wl.pool(dev)
+        self.q = wl.q.to(dev)
+        self.kvp, self.kvi = wl.kv_indptr.to(dev), wl.kv_indices.to(dev)
+        self.o = torch.empty(s.batch, s.hq, s.lv, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(s.batch, s.hq, dtype=torch.float32, device=dev)
+        self.ws = torch.empty(pkx.decode_workspace_size(s.batch, s.hq, s.hkv, s.lq, s.lv),
+                              dtype=torch.uint8, device=dev)
+        self.launches = 3  # scheduler, attention, combine
+        self.flops = 2.0 * (s.lq + s.lv) * s.hq * sum(
+            min(p + 1, s.sliding_window + 1) if s.sliding_window > 0 else p + 1
+            for p in wl.prefix_lens)
+        self.bytes = decode_bytes(wl)
+
+    def inputs(self):
+        return [self.q, self.kvp, self.kvi]
+
+    def __call__(self):
+        s = self.wl.spec
+        self.pkx.decode_attention_fwd(self.q, self.o, self.kb, self.vb, self.kvp, self.kvi,
+                                      self.wl.sm_scale, s.logit_cap, s.sliding_window,
+                                      lse=self.lse, workspace=self.ws)
+
+
+def make_step(name, dev):
+    wl = W.draw(W.SPECS[name])
+    return (DecodeStep if wl.spec.decode else ExtendStep)(wl, dev)
 
 
 def time_steps(step, steps, flush, dev, attn_events=False, pkx=None):
@@ -346,10 +405,8 @@ def measure_e2e(step: ExtendStep, steps, warmup, flush, dev):
     pinned host memory.  The KV pool is device-resident state (it is the
     cache), as in serving."""
     pin = lambda t: t.cpu().pin_memory()
-    host_in = [pin(t) for t in (step.q, step.prefix_indptr, step.prefix_indices, step.extend_start,
-                                step.extend_lens, step.extend_indices, step.qo_indptr)]
-    dev_in = [step.q, step.prefix_indptr, step.prefix_indices, step.extend_start,
-              step.extend_lens, step.extend_indices, step.qo_indptr]
+    dev_in = step.inputs()
+    host_in = [pin(t) for t in dev_in]
     host_o = torch.empty(step.o.shape, dtype=step.o.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = host_o.numel() * host_o.element_size()
@@ -366,27 +423,27 @@ def measure_e2e(step: ExtendStep, steps, warmup, flush, dev):
     return sum(ms) / len(ms), h2d, d2h
 
 
-def measure_decode(dev, flush, steps):
+def measure_component(name, dev, flush, steps, hbm_peak, bf16_peak):
+    """One workload's step, device-timed, with the attention kernel's own
+    time; TFLOP/s and GB/s of algorithmic work and the roofline fractions."""
     from paged_kv_extend_gb300 import pkx
-    wl = W.draw(W.SPECS["decode_gqa"])
-    s = wl.spec
-    kb, vb = wl.pool(dev)
-    q = wl.q.to(dev)
-    kvp, kvi = wl.kv_indptr.to(dev), wl.kv_indices.to(dev)
-    o = torch.empty(s.batch, s.hq, s.lv, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(s.batch, s.hq, dtype=torch.float32, device=dev)
-    ws = torch.empty(pkx.decode_workspace_size(s.batch, s.hq, s.hkv, s.lq, s.lv),
-                     dtype=torch.uint8, device=dev)
-    fn = lambda: pkx.decode_attention_fwd(q, o, kb, vb, kvp, kvi, wl.sm_scale, lse=lse, workspace=ws)
+    step = make_step(name, dev)
     for _ in range(3):
-        fn()
-    ms, attn = time_steps(fn, steps, flush, dev, attn_events=True, pkx=pkx)
-    b = decode_bytes(wl)
-    out = {"workload": "decode_gqa: batch=64 Hq=32 Hkv=8 D=128 T=8193 pool=2^20",
-           "GB/s": b / (sum(ms) / len(ms) * 1e-3) / 1e9,
-           "attn_kernel_GB/s": b / (sum(attn) / len(attn) * 1e-3) / 1e9,
-           "bytes": b, "ms": sum(ms) / len(ms)}
-    del kb, vb
+        step()
+    ms, attn = time_steps(step, steps, flush, dev, attn_events=True, pkx=pkx)
+    status = pkx.workspace_status(step.ws)
+    m, a = sum(ms) / len(ms), sum(attn) / len(attn)
+    out = {"workload": f"{name}: {WORKLOAD_TEXT.get(name, '')}", "ms": m, "attn_kernel_ms": a,
+           "TFLOP/s": step.flops / (m * 1e-3) / 1e12,
+           "attn_kernel_TFLOP/s": step.flops / (a * 1e-3) / 1e12,
+           "GB/s": step.bytes / (m * 1e-3) / 1e9,
+           "attn_kernel_GB/s": step.bytes / (a * 1e-3) / 1e9,
+           "frac_of_bf16_peak": step.flops / (a * 1e-3) / 1e12 / bf16_peak,
+           "frac_of_hbm": step.bytes / (a * 1e-3) / 1e9 / hbm_peak,
+           "algorithmic_flops": step.flops, "algorithmic_bytes": step.bytes,
+           "status": status}
+    del step
+    torch.cuda.empty_cache()
     return out
 
 
@@ -403,9 +460,9 @@ def run_ours(args, ws, rank, local):
     pkx.load_library()
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
 
-    wl = W.draw(W.SPECS[WORKLOAD])
-    step = ExtendStep(wl, dev)
-    flops = extend_flops(wl)
+    step = make_step(args.workload, dev)
+    wl = step.wl
+    flops = step.flops
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     for _ in range(args.warmup):
@@ -435,14 +492,19 @@ def run_ours(args, ws, rank, local):
     e2e_ms, h2d, d2h = measure_e2e(step, args.steps, 2, flush, dev)
     e2e_ms = max_over_ranks(e2e_ms, ws, dev)
 
-    components = {}
+    components = {"attn_kernel_share_of_step": attn_avg / ms}
     if not args.no_components:
-        components["decode"] = measure_decode(dev, flush, max(5, min(args.steps, 20)))
-        components["decode"]["frac_of_hbm"] = components["decode"]["attn_kernel_GB/s"] / hbm_peak
-        components["extend_attn_kernel_share"] = attn_avg / ms
+        names = ["decode_gqa", "mla"]
+        if args.all_workloads:
+            names = ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla"]
+        for name in names:
+            if name == args.workload:
+                continue
+            components[name] = measure_component(name, dev, flush, max(5, min(args.steps, 20)),
+                                                 hbm_peak, bf16_peak)
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not wl.spec.decode:
         import oracle
         oracle.build()
         k_ext, v_ext = wl.extend_kv()
@@ -456,7 +518,7 @@ def run_ours(args, ws, rank, local):
                          f"{dt:.1f} s of float64 CPU work"}
 
     traffic = None
-    prof = os.path.join(ROOT, "profiles", "attn_kernel_llama3_8b.md")
+    prof = os.path.join(ROOT, "profiles", f"attn_kernel_{args.workload}.md")
     if os.path.exists(prof):
         import hashlib
         src = b"".join(open(os.path.join(ROOT, "paged_kv_extend_gb300", "csrc", f), "rb").read()
@@ -468,19 +530,32 @@ def run_ours(args, ws, rank, local):
                 if len(parts) >= 4 and parts[3] == h:
                     traffic = float(parts[1])
 
+    if wl.spec.decode:
+        metric, unit = "decode-shape HBM GB/s", "GB/s"
+        value = step.bytes * ws / (ms_max * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": step.bytes / (attn_avg * 1e-3) / 1e9,
+                "peak": hbm_peak, "unit": "GB/s",
+                "frac": step.bytes / (attn_avg * 1e-3) / 1e9 / hbm_peak, "traffic": None,
+                "peak_source": f"hbm_gbs copy bandwidth, of {peak_src}",
+                "kernel": "attn_kernel (decode)", "algorithmic_bytes_per_launch": step.bytes}
+        e2e_value = step.bytes * ws / (e2e_ms * 1e-3) / 1e9
+    else:
+        metric, unit = "extend-attn TFLOP/s", "TFLOP/s"
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak,
+                "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": traffic,
+                "peak_source": f"bf16_tflops burst, of {peak_src}",
+                "kernel": "mla_kernel<unified>" if wl.spec.lq == 576 else "attn_kernel<unified>",
+                "algorithmic_flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": step.bytes}
+        e2e_value = flops * ws / (e2e_ms * 1e-3) / 1e12
     line = {
-        "metric": "extend-attn TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "metric": metric, "value": value, "unit": unit, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_dict(wl),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak,
-                     "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": traffic,
-                     "peak_source": f"bf16_tflops burst, of {peak_src}",
-                     "kernel": "attn_kernel<128, unified>",
-                     "algorithmic_flops_per_launch": flops,
-                     "algorithmic_bytes_per_launch": extend_bytes(wl, unified=True)},
+        "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": e2e_value, "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches * args.steps,
         "clocks": clock_info,
@@ -499,6 +574,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-components", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(W.SPECS),
+                    help="workload of the timed step (default: the Llama-3-8B-shaped layer)")
+    ap.add_argument("--all-workloads", action="store_true",
+                    help="also measure every other workload as a component")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
