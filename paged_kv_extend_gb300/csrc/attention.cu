@@ -159,9 +159,14 @@ __device__ int block_exclusive_scan(const int32_t *in, int32_t *out, int n, int 
   return total;
 }
 
+// Per-block tile counts live in shared memory when they fit (they are read
+// back many times while the units are emitted).
+constexpr int kSchedSmemBlocks = 8192;
+
 __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   __shared__ int sh[1024];
   __shared__ int s_c;
+  __shared__ int s_qbt[kSchedSmemBlocks];
   const int tid = threadIdx.x;
   const int B = p.batch;
   int32_t *nqb = p.seq;                 // [B]  query blocks per sequence
@@ -188,6 +193,8 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     return;
   }
 
+  int32_t *qbt = total_qb <= kSchedSmemBlocks ? s_qbt : p.qbt;
+
   // 2. KV tiles per query block and per sequence; total tiles
   long long my_tiles = 0;
   for (int b = tid; b < B; b += 1024) {
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
       int lo, hi, i0, i1;
       qblock_range(p, d, qb, lo, hi, i0, i1);
       int nt = (hi - lo + p.bn - 1) / p.bn;
-      p.qbt[qboff[b] + qb] = nt;
+      qbt[qboff[b] + qb] = nt;
       w += nt;
     }
     work[b] = w;
@@ -243,7 +250,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     const int n = nqb[b];
     int u = 0, s = 0, c = 0;
     for (int qb = 0; qb < n; ++qb) {
-      const int nt = p.qbt[qboff[b] + qb];
+      const int nt = qbt[qboff[b] + qb];
       const int S = nt > 0 ? (nt + C - 1) / C : 1;
       u += S;
       if (S > 1) {
@@ -268,50 +275,61 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     return;
   }
 
-  // 5. emit: for each sequence (largest first), each KV head, each query
-  //    block from the last (longest key range) to the first, each split.
-  for (int rk = tid; rk < B; rk += 1024) {
+  // 5. emit, one (sequence, KV head) pair per thread: sequences largest
+  //    first, then KV heads, then query blocks from the last (longest key
+  //    range) to the first, then splits.
+  for (int idx = tid; idx < B * p.hkv; idx += 1024) {
+    const int rk = idx / p.hkv, kvh = idx - (idx / p.hkv) * p.hkv;
     const int b = order[rk];
     SeqDims d = seq_dims(p, b);
     const int split_at = p.mode == kTwoStage ? d.P : INT_MAX;
-    int uo = ucnt[rk], so = scnt[rk], co = ccnt[rk];
-    for (int kvh = 0; kvh < p.hkv; ++kvh) {
-      for (int qb = d.nqb - 1; qb >= 0; --qb) {
-        int lo, hi, i0, i1;
-        qblock_range(p, d, qb, lo, hi, i0, i1);
-        const int nt = p.qbt[qboff[b] + qb];
-        const int S = nt > 0 ? (nt + C - 1) / C : 1;
-        const int tps = nt > 0 ? (nt + S - 1) / S : 0;
-        if (S > 1) {
-          CombineEntry e;
-          e.q_tok0 = d.qbase + i0;
-          e.n_tok = i1 - i0;
-          e.kvh = kvh;
-          e.slot0 = so;
-          e.n_split = S;
-          e.pad[0] = e.pad[1] = e.pad[2] = 0;
-          p.comb[co++] = e;
-        }
-        for (int s = 0; s < S; ++s) {
-          for (int dq = 0; dq < p.n_dsplit; ++dq) {
-            WorkUnit w;
-            w.q_tok0 = d.qbase + i0;
-            w.n_tok = i1 - i0;
-            w.qpos0 = d.P + i0;
-            w.kvh = kvh;
-            w.k_begin = min(hi, lo + s * tps * p.bn);
-            w.k_end = min(hi, lo + (s + 1) * tps * p.bn);
-            w.k_split = split_at;
-            w.n_tiles = range_tiles(w.k_begin, w.k_end, split_at, p.bn);
-            w.b = b;
-            w.slot = S > 1 ? so + s : -1;
-            w.dq = dq;
-            w.pad = 0;
-            p.units[uo++] = w;
-          }
-        }
-        if (S > 1) so += S;
+    // this sequence's units, slots and combine entries per KV head
+    int u1 = 0, s1 = 0, c1 = 0;
+    for (int qb = 0; qb < d.nqb; ++qb) {
+      const int nt = qbt[qboff[b] + qb];
+      const int S = nt > 0 ? (nt + C - 1) / C : 1;
+      u1 += S * p.n_dsplit;
+      if (S > 1) {
+        s1 += S;
+        c1 += 1;
       }
+    }
+    int uo = ucnt[rk] + kvh * u1, so = scnt[rk] + kvh * s1, co = ccnt[rk] + kvh * c1;
+    for (int qb = d.nqb - 1; qb >= 0; --qb) {
+      int lo, hi, i0, i1;
+      qblock_range(p, d, qb, lo, hi, i0, i1);
+      const int nt = qbt[qboff[b] + qb];
+      const int S = nt > 0 ? (nt + C - 1) / C : 1;
+      const int tps = nt > 0 ? (nt + S - 1) / S : 0;
+      if (S > 1) {
+        CombineEntry e;
+        e.q_tok0 = d.qbase + i0;
+        e.n_tok = i1 - i0;
+        e.kvh = kvh;
+        e.slot0 = so;
+        e.n_split = S;
+        e.pad[0] = e.pad[1] = e.pad[2] = 0;
+        p.comb[co++] = e;
+      }
+      for (int s = 0; s < S; ++s) {
+        for (int dq = 0; dq < p.n_dsplit; ++dq) {
+          WorkUnit w;
+          w.q_tok0 = d.qbase + i0;
+          w.n_tok = i1 - i0;
+          w.qpos0 = d.P + i0;
+          w.kvh = kvh;
+          w.k_begin = min(hi, lo + s * tps * p.bn);
+          w.k_end = min(hi, lo + (s + 1) * tps * p.bn);
+          w.k_split = split_at;
+          w.n_tiles = range_tiles(w.k_begin, w.k_end, split_at, p.bn);
+          w.b = b;
+          w.slot = S > 1 ? so + s : -1;
+          w.dq = dq;
+          w.pad = 0;
+          p.units[uo++] = w;
+        }
+      }
+      if (S > 1) so += S;
     }
   }
   if (tid == 0) {
