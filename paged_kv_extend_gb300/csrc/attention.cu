@@ -688,23 +688,30 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       uint32_t q_cnt = 0, kc = 0, vc = 0, p_cnt0 = 0, p_cnt1 = 0;
       const uint32_t sQ0 = sbase + C::OFF_Q, sQ1 = sQ0 + C::Q_BYTES;
       bool ok = true;
+      // Descriptors are built once per tile and stepped by constants: the
+      // issue path is a single thread, and a per-MMA dependent chain of
+      // address arithmetic starves the tensor pipe.
+      constexpr uint32_t K_LO = sw128_desc_lo(0), K_HI = sw128_desc_hi(1024);
+      constexpr uint32_t V_LO = sw128_desc_lo(C::BN * 128), V_HI = sw128_desc_hi(1024);
       auto issue_s = [&](int qt, uint32_t sK) {
-        const uint32_t sQ = qt ? sQ1 : sQ0;
-#pragma unroll 1
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t ad = sw128_desc(sQ + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 0, 1024);
-          const uint64_t bd = sw128_desc(sK + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 0, 1024);
-          tc_mma_ss(tmem + qt * C::BN, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
-        }
+        const uint32_t a_lo = K_LO | ((qt ? sQ1 : sQ0) >> 4), b_lo = K_LO | (sK >> 4);
+        const uint32_t d = tmem + qt * C::BN;
+        static_for<0, HD / 16>([&](auto kk_c) {
+          constexpr int kk = decltype(kk_c)::value;
+          constexpr uint32_t ao = ((kk / 4) * (C::BM * 128) + (kk % 4) * 32) / 16;
+          constexpr uint32_t bo = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) / 16;
+          tc_mma_ss_step<ao, bo>(d, a_lo, b_lo, K_HI, C::IDESC_QK, kk > 0 ? 1u : 0u);
+        });
         tc_commit(&bars[B_S_FULL + qt]);
       };
       auto issue_pv = [&](int qt, uint32_t sV, bool acc_first) {
-#pragma unroll 1
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          const uint64_t bd = sw128_desc(sV + kk * 2048, C::BN * 128, 1024);
-          tc_mma_ts(tmem + 2 * C::BN + qt * C::HDV, tmem + qt * C::BN + kk * 8, bd, C::IDESC_PV,
-                    (acc_first || kk > 0) ? 1u : 0u);
-        }
+        const uint32_t b_lo = V_LO | (sV >> 4);
+        const uint32_t d = tmem + 2 * C::BN + qt * C::HDV, a = tmem + qt * C::BN;
+        const uint32_t acc0 = acc_first ? 1u : 0u;
+        static_for<0, C::BN / 16>([&](auto kk_c) {
+          constexpr int kk = decltype(kk_c)::value;
+          tc_mma_ts_step<kk * 8, kk * 128>(d, a, b_lo, V_HI, C::IDESC_PV, kk > 0 ? 1u : acc0);
+        });
       };
       for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
         const WorkUnit w = p.units[u];

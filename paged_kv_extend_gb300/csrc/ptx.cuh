@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -244,6 +245,55 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr, uint32_t lbo,
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M x N.
 //   b_mn_major: 0 = B is K-major (K contiguous), 1 = B is N-major.
+// The same descriptor with start address 0, as two 32-bit words.  The start
+// address field is bits 0-13 of the low word, so the descriptor of address a
+// is (lo | a >> 4, hi) and stepping it by b bytes adds b >> 4 to the low
+// word, with no carry while a + b stays inside shared memory (< 256 KB).
+__host__ __device__ constexpr uint32_t sw128_desc_lo(uint32_t lbo) {
+  return ((lbo >> 4) & 0x3FFFu) << 16;
+}
+__host__ __device__ constexpr uint32_t sw128_desc_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
+// One tcgen05.mma (kind::f16, cta_group::1, D in TMEM) whose smem operands
+// are (a_lo + AO, hi) and (b_lo + BO, hi): the steps are immediates inside
+// the instruction block, so the compiler keeps only the base words live.
+template <uint32_t AO, uint32_t BO>
+__device__ __forceinline__ void tc_mma_ss_step(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                               uint32_t hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 al, bl;\n\t.reg .b64 ad, bd;\n\t"
+      "add.u32 al, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+      "mov.b64 ad, {al, %3};\n\tmov.b64 bd, {bl, %3};\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(AO), "n"(BO), "r"(accumulate)
+      : "memory");
+}
+// Same with A in TMEM at a_tmem + AO columns.
+template <uint32_t AO, uint32_t BO>
+__device__ __forceinline__ void tc_mma_ts_step(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                               uint32_t hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 at, bl;\n\t.reg .b64 bd;\n\t"
+      "add.u32 at, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+      "mov.b64 bd, {bl, %3};\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(AO), "n"(BO), "r"(accumulate)
+      : "memory");
+}
+
+// f(std::integral_constant<int, I>) for I = 0 .. N-1, unrolled at compile time.
+template <int I, int N, typename F>
+__device__ __forceinline__ void static_for(F &&f) {
+  if constexpr (I < N) {
+    f(std::integral_constant<int, I>{});
+    static_for<I + 1, N>(f);
+  }
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_major) {
   return (1u << 4)                      // D format: f32
          | (1u << 7)                    // A format: bf16
