@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[B_S_FULL + i], 1);
-      mbar_init(&bars[B_P_FULL + i], 128);
+      mbar_init(&bars[B_P_FULL + i], 4);  // one arrival per softmax warp
       mbar_init(&bars[B_O_DONE + i], 1);
     }
     mbar_init(&bars[B_FINAL], 1);
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     }
     for (int s = 0; s < C::NI; ++s) {
       mbar_init(&i_full[s], 32);
-      mbar_init(&i_empty[s], C::COPY_THREADS);
+      mbar_init(&i_empty[s], C::COPY_THREADS / 32);
     }
     s_abort = 0;
     fence_barrier_init();
@@ -552,12 +552,14 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
               x[96 + i] = __uint_as_float(v3[i]);
             }
           }
+          // Logits in the log2 domain are sc * x.  The plain path keeps the
+          // raw dot products and folds sc into the exponent's FMA; a capped
+          // or masked tile is first mapped into the log2 domain (sc = 1).
+          float sc = p.scale_log2;
           if (p.use_cap) {
 #pragma unroll
             for (int i = 0; i < C::BN; ++i) x[i] = p.cap_log2 * tanh_approx(x[i] * p.cap_pre);
-          } else {
-#pragma unroll
-            for (int i = 0; i < C::BN; ++i) x[i] *= p.scale_log2;
+            sc = 1.0f;
           }
           const bool need_mask = (ke - 1 > qmin) || (ke - kb < C::BN) ||
                                  (p.window > 0 && kb < qmax - p.window);
@@ -567,18 +569,33 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
               const int kpos = kb + i;
               const bool vis =
                   kpos < ke && kpos <= qpos && (p.window <= 0 || qpos - kpos <= p.window);
-              if (!vis) x[i] = -INFINITY;
+              x[i] = vis ? x[i] * sc : -INFINITY;
             }
+            sc = 1.0f;
           }
-          float mt0 = x[0], mt1 = x[1], mt2 = x[2], mt3 = x[3];
+          // row max of sc * x: sc * max(x), or sc * min(x) for a negative sc
+          float mt;
+          if (sc >= 0.f) {
+            float mt0 = x[0], mt1 = x[1], mt2 = x[2], mt3 = x[3];
 #pragma unroll
-          for (int i = 4; i < C::BN; i += 4) {
-            mt0 = fmaxf(mt0, x[i]);
-            mt1 = fmaxf(mt1, x[i + 1]);
-            mt2 = fmaxf(mt2, x[i + 2]);
-            mt3 = fmaxf(mt3, x[i + 3]);
+            for (int i = 4; i < C::BN; i += 4) {
+              mt0 = fmaxf(mt0, x[i]);
+              mt1 = fmaxf(mt1, x[i + 1]);
+              mt2 = fmaxf(mt2, x[i + 2]);
+              mt3 = fmaxf(mt3, x[i + 3]);
+            }
+            mt = fmaxf(fmaxf(mt0, mt1), fmaxf(mt2, mt3)) * sc;
+          } else {
+            float mt0 = x[0], mt1 = x[1], mt2 = x[2], mt3 = x[3];
+#pragma unroll
+            for (int i = 4; i < C::BN; i += 4) {
+              mt0 = fminf(mt0, x[i]);
+              mt1 = fminf(mt1, x[i + 1]);
+              mt2 = fminf(mt2, x[i + 2]);
+              mt3 = fminf(mt3, x[i + 3]);
+            }
+            mt = fminf(fminf(mt0, mt1), fminf(mt2, mt3)) * sc;
           }
-          const float mt = fmaxf(fmaxf(mt0, mt1), fmaxf(mt2, mt3));
           const float m_new = fmaxf(m, mt);
           // Rescale only when the max grows by more than 2^8: exponents of
           // the stale max stay below 256, which fp32 sums and bf16 P hold.
@@ -592,12 +609,14 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             m = m_new;
           }
           const float mref = m == -INFINITY ? 0.f : m;
+          // p = 2^(sc * x - m): one FMA into each exp2
+          const float nm = -mref;
           float l0 = 0.f, l1 = 0.f;
           uint32_t pk[C::BN / 2];
 #pragma unroll
           for (int i = 0; i < C::BN; i += 2) {
-            const float e0 = ex2_approx(x[i] - mref);
-            const float e1 = ex2_approx(x[i + 1] - mref);
+            const float e0 = ex2_approx(fmaf(x[i], sc, nm));
+            const float e1 = ex2_approx(fmaf(x[i + 1], sc, nm));
             l0 += e0;
             l1 += e1;
             pk[i / 2] = pack_bf16(e0, e1);
@@ -630,7 +649,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(&bars[B_P_FULL + wg]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_P_FULL + wg]);
       }
       if (*abort_flag) break;
       // epilogue: wait for the last PV of this tile, normalise, store
@@ -939,7 +959,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           cp_async_arrive_noinc(&v_full[vs]);
         }
         ++vc;
-        mbar_arrive(&i_empty[is]);  // this thread is done with the ring slot
+        __syncwarp();  // the warp is done with the ring slot
+        if (lane == 0) mbar_arrive(&i_empty[is]);
       }
     }
     if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);

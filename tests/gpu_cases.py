@@ -48,7 +48,7 @@ class DeviceWorkload:
             s.sliding_window if window is None else window, lse=lse)
         return o, lse, ws
 
-    def unified(self, cap=None, window=None):
+    def unified(self, cap=None, window=None, scale=None):
         s = self.wl.spec
         uptr, uidx, plen = pkx.build_unified_kv_indices(
             self.kv_indptr, self.kv_indices, self.extend_start_loc, self.extend_seq_lens,
@@ -56,7 +56,7 @@ class DeviceWorkload:
         o, lse = self.out()
         ws = pkx.extend_attention_fwd_unified(
             self.q, o, self.k_buffer, self.v_buffer, self.qo_indptr, uptr, uidx, plen,
-            self.wl.sm_scale, s.logit_cap if cap is None else cap,
+            self.wl.sm_scale if scale is None else scale, s.logit_cap if cap is None else cap,
             s.sliding_window if window is None else window, lse=lse)
         return o, lse, ws
 
@@ -70,12 +70,13 @@ class DeviceWorkload:
         return o, lse, ws
 
 
-def oracle_extend(wl: W.Workload, cap=None, window=None, rows=None):
+def oracle_extend(wl: W.Workload, cap=None, window=None, rows=None, scale=None):
     s = wl.spec
     k_ext, v_ext = wl.extend_kv()
     kb, vb = wl.pool()
     return oracle.extend_attention(
-        wl.q, k_ext, v_ext, kb, vb, wl.qo_indptr, wl.kv_indptr, wl.kv_indices, wl.sm_scale,
+        wl.q, k_ext, v_ext, kb, vb, wl.qo_indptr, wl.kv_indptr, wl.kv_indices,
+        wl.sm_scale if scale is None else scale,
         s.logit_cap if cap is None else cap, s.sliding_window if window is None else window,
         rows=rows)
 

@@ -168,6 +168,24 @@ def test_extend_small_vs_oracle(lq, hq, hkv, prefix, extend, cap, window):
     assert_close(uo, ul, ro, rl, "unified")
 
 
+@pytest.mark.parametrize("scale,cap,window", [
+    (-0.09, 0.0, -1),   # negative scale: the row max is scale * min(q.k)
+    (0.0, 0.0, -1),     # uniform weights over the visible keys
+    (0.6, 0.0, -1),     # large logits: many lazy rescales
+    (-0.2, 20.0, 50),   # negative scale through the cap, with a window
+])
+def test_extend_scale_values(scale, cap, window):
+    spec = W.small_spec(batch=3, hq=16, hkv=4, prefix=[0, 260, 1100], extend=[140, 7, 300],
+                        logit_cap=cap, sliding_window=window, seed=77)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.unified(scale=scale)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_extend(wl, scale=scale)
+    assert_close(o, lse, ro, rl, f"scale {scale}")
+
+
 def test_repeat_calls_are_bitwise_identical():
     wl = W.draw(W.small_spec(batch=3, hq=32, hkv=8, prefix=[700, 30, 0], extend=[90, 300, 17], seed=4))
     dw = DeviceWorkload(wl)
