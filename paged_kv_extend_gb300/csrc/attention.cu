@@ -384,9 +384,11 @@ struct Cfg {
   static constexpr int TMEM_COLS = 512;  // S0 | S1 | O0 | O1, 128 columns each
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HDV, 1);
-  // warps 0-7: two softmax warpgroups; 8: MMA; 9: row indices + Q; 10-15: copies
+  // warps 0-7: two softmax warpgroups; 8: MMA; 9: row indices + Q;
+  // 10-13: copies; 14-15: idle
   static constexpr int THREADS = 512;
-  static constexpr int COPY_THREADS = 192;
+  static constexpr int COPY_WARP0 = 10;
+  static constexpr int COPY_THREADS = 128;
   // Registers: the kernel launches with REGS_LAUNCH per thread (checked at
   // build time); the softmax warpgroups take REGS_SOFTMAX, the other two
   // give back down to REGS_OTHER.  The split must add up exactly.
@@ -871,25 +873,47 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           ok = false;
           break;
         }
-        *reinterpret_cast<int4 *>(smem + C::OFF_I + is * C::I_BYTES + lane * 16) =
-            make_int4(rows[0], rows[1], rows[2], rows[3]);
+        {
+          // ring[key % KPP][key / KPP]: each copy thread's rows contiguous
+          constexpr int KPP = C::COPY_THREADS / (HD / 8), NK_T = C::BN / KPP;
+          int *ring = reinterpret_cast<int *>(smem + C::OFF_I + is * C::I_BYTES);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int key = 4 * lane + i;
+            ring[(key % KPP) * NK_T + key / KPP] = rows[i];
+          }
+        }
         mbar_arrive(&i_full[is]);
         ++ic;
       }
     }
     if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
-  } else {
-    // ------------------------------------------------ K/V copies (6 warps)
-    // Thread ct copies 16-byte chunk (ct % CPR) of every KPP-th key of a
-    // tile into the swizzled K (then V) stage, then arrives (noinc) on the
-    // stage barrier when its own copies have landed: no thread ever blocks
-    // on its copies.
-    const int ct = tid - 10 * 32;
-    constexpr int CPR = HD / 8;                 // 16-byte chunks per row
+  } else if (warp < C::COPY_WARP0 + C::COPY_THREADS / 32) {
+    // ------------------------------------------------ K/V copies (4 warps)
+    // Thread ct copies 16-byte chunk ch = ct % CPR of keys key0 + KPP * i
+    // (key0 = ct / CPR): every copy instruction of a warp reads whole rows.
+    // KPP is a multiple of 8, so the swizzle term (ch ^ key % 8) is fixed
+    // per thread and key i lands at a constant offset from the thread's
+    // destination base.  The index warp stores each thread's rows
+    // contiguously (ring[key0][i]).  A thread arrives (noinc) on the stage
+    // barrier when its own copies have landed.
+    const int ct = tid - C::COPY_WARP0 * 32;
+    constexpr int CPR = HD / 8;                 // chunks of a row
     constexpr int KPP = C::COPY_THREADS / CPR;  // keys per pass
-    constexpr int NKEYS = (C::BN + KPP - 1) / KPP;
-    const int ch = ct % CPR;
-    const int key0 = ct / CPR;
+    constexpr int NKEYS = C::BN / KPP;          // keys per thread
+    static_assert(KPP % 8 == 0 && C::BN % KPP == 0, "constant swizzle per thread");
+    const int ch = ct % CPR, key0 = ct / CPR;
+    const uint32_t dthr = (uint32_t)(ch >> 3) * (C::BN * 128) + (uint32_t)key0 * 128u +
+                          ((uint32_t)((ch & 7) ^ (key0 & 7)) << 4);
+    auto copy_rows = [&](uint32_t stage, const bf16 *base, int64_t stride, const int *rows) {
+      static_for<0, NKEYS>([&](auto i_c) {
+        constexpr int i = decltype(i_c)::value;
+        const int r = rows[i];
+        const uint32_t bytes = r >= 0 ? 16u : 0u;
+        const bf16 *src = base + (int64_t)max(r, 0) * stride;
+        cp_async_16_at<i * KPP * 128, 0>(stage + dthr, src, bytes);
+      });
+    };
     uint32_t kc = 0, vc = 0, ic = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
@@ -910,11 +934,22 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           ok = false;
           break;
         }
-        const int *ring = reinterpret_cast<const int *>(smem + C::OFF_I + is * C::I_BYTES);
+        int rows[NKEYS];
+        {
+          const int4 *ring =
+              reinterpret_cast<const int4 *>(smem + C::OFF_I + is * C::I_BYTES) + key0 * (NKEYS / 4);
+#pragma unroll
+          for (int q = 0; q < NKEYS / 4; ++q) {
+            const int4 v = ring[q];
+            rows[4 * q] = v.x;
+            rows[4 * q + 1] = v.y;
+            rows[4 * q + 2] = v.z;
+            rows[4 * q + 3] = v.w;
+          }
+        }
+        __syncwarp();  // the warp is done with the ring slot
+        if (lane == 0) mbar_arrive(&i_empty[is]);
         ++ic;
-        const bf16 *kbase = from_ext ? kx : kp;
-        const bf16 *vbase = from_ext ? vx : vp;
-        const int64_t kst = from_ext ? p.ke_st : p.kb_ss, vst = from_ext ? p.ve_st : p.vb_ss;
         // K tile
         const int ks = kc % C::NK;
         if (kc >= (uint32_t)C::NK &&
@@ -922,20 +957,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           ok = false;
           break;
         }
-        {
-          const uint32_t dst = sbase + C::OFF_K + ks * C::K_BYTES + (ch >> 3) * (C::BN * 128);
-#pragma unroll
-          for (int i = 0; i < NKEYS; ++i) {
-            const int key = key0 + i * KPP;
-            if (key < C::BN) {
-              const int row = ring[key];
-              const bool v = row >= 0;
-              cp_async_16(dst + sw128_off(key, ch & 7), v ? kbase + (int64_t)row * kst : p.k_pool,
-                          v ? 16u : 0u);
-            }
-          }
-          cp_async_arrive_noinc(&k_full[ks]);
-        }
+        copy_rows(sbase + C::OFF_K + ks * C::K_BYTES, from_ext ? kx : kp,
+                  from_ext ? p.ke_st : p.kb_ss, rows);
+        cp_async_arrive_noinc(&k_full[ks]);
         ++kc;
         // V tile
         const int vs = vc % C::NV;
@@ -944,23 +968,10 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           ok = false;
           break;
         }
-        {
-          const uint32_t dst = sbase + C::OFF_V + vs * C::V_BYTES + (ch >> 3) * (C::BN * 128);
-#pragma unroll
-          for (int i = 0; i < NKEYS; ++i) {
-            const int key = key0 + i * KPP;
-            if (key < C::BN) {
-              const int row = ring[key];
-              const bool v = row >= 0;
-              cp_async_16(dst + sw128_off(key, ch & 7), v ? vbase + (int64_t)row * vst : p.v_pool,
-                          v ? 16u : 0u);
-            }
-          }
-          cp_async_arrive_noinc(&v_full[vs]);
-        }
+        copy_rows(sbase + C::OFF_V + vs * C::V_BYTES, from_ext ? vx : vp,
+                  from_ext ? p.ve_st : p.vb_ss, rows);
+        cp_async_arrive_noinc(&v_full[vs]);
         ++vc;
-        __syncwarp();  // the warp is done with the ring slot
-        if (lane == 0) mbar_arrive(&i_empty[is]);
       }
     }
     if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);

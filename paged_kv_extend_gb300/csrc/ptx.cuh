@@ -124,6 +124,13 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint3
                "r"(src_bytes)
                : "memory");
 }
+// The same with compile-time byte offsets added to both addresses.
+template <uint32_t DOFF, uint32_t SOFF>
+__device__ __forceinline__ void cp_async_16_at(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0+%3], [%1+%4], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "n"(DOFF), "n"(SOFF)
+               : "memory");
+}
 // Arrive on `bar` (counted as one of its expected arrivals) once every
 // cp.async this thread has issued so far has landed.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
