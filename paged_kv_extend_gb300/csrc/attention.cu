@@ -57,11 +57,13 @@ struct SchedParams {
   const int32_t *qo_indptr, *kv_indptr, *prefix_lens;
   int batch, hkv, tok, window, num_q_tokens;
   int bn;        // keys per K/V tile
+  int q_tile_tok;  // query tokens of one Q tile
   int n_dsplit;  // units per (block, split): value-dim slices (1, or 4 for MLA)
   int unit_target, qb_max, unit_max, comb_max, slot_max;
   int32_t *seq;  // 8 arrays of batch+1 ints
   int32_t *qbt;  // tiles per query block
   WorkUnit *units;
+  int32_t *uorder;  // units by cost, largest first
   CombineEntry *comb;
   WsHeader *hdr;
 };
@@ -162,11 +164,21 @@ __device__ int block_exclusive_scan(const int32_t *in, int32_t *out, int n, int 
 // Per-block tile counts live in shared memory when they fit (they are read
 // back many times while the units are emitted).
 constexpr int kSchedSmemBlocks = 8192;
+// Buckets of the counting sort of units by cost.
+constexpr int kCostBuckets = 2048;
+
+// Relative cost of a unit: its K/V tiles times its Q tiles, plus one for the
+// per-unit prologue and epilogue (clamped to the sort's bucket range).
+__device__ __forceinline__ int unit_cost(const WorkUnit &w, int q_tile_tok) {
+  const int nq = (w.n_tok + q_tile_tok - 1) / q_tile_tok;
+  return min(w.n_tiles * max(nq, 1) + 1, kCostBuckets - 1);
+}
 
 __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   __shared__ int sh[1024];
   __shared__ int s_c;
   __shared__ int s_qbt[kSchedSmemBlocks];
+  __shared__ int s_hist[kCostBuckets];
   const int tid = threadIdx.x;
   const int B = p.batch;
   int32_t *nqb = p.seq;                 // [B]  query blocks per sequence
@@ -177,7 +189,10 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   int32_t *scnt = p.seq + 5 * (B + 1);  // [B]  by rank: partial slots
   int32_t *ccnt = p.seq + 6 * (B + 1);  // [B]  by rank: combine entries
 
-  if (tid == 0) p.hdr->status = 0;
+  if (tid == 0) {
+    p.hdr->status = 0;
+    p.hdr->next_unit = 0;
+  }
   __syncthreads();
 
   // 1. query blocks per sequence and their offsets
@@ -332,6 +347,20 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
       if (S > 1) so += S;
     }
   }
+
+  // 6. order the units by cost, largest first (counting sort; the order
+  //    within a cost is arbitrary).  The attention kernels hand them to
+  //    CTAs in serpentine order, which balances the work per CTA.
+  for (int i = tid; i < kCostBuckets; i += 1024) s_hist[i] = 0;
+  __syncthreads();
+  for (int u = tid; u < n_units; u += 1024)
+    atomicAdd(&s_hist[kCostBuckets - 1 - unit_cost(p.units[u], p.q_tile_tok)], 1);
+  __syncthreads();
+  block_exclusive_scan(s_hist, s_hist, kCostBuckets, sh);
+  for (int u = tid; u < n_units; u += 1024) {
+    const int pos = atomicAdd(&s_hist[kCostBuckets - 1 - unit_cost(p.units[u], p.q_tile_tok)], 1);
+    p.uorder[pos] = u;
+  }
   if (tid == 0) {
     p.hdr->n_units = n_units;
     p.hdr->n_combine = n_comb;
@@ -354,7 +383,9 @@ struct KParams {
   float cap_pre;     // sm_scale / cap                (cap)
   float cap_log2;    // cap * log2(e)                 (cap)
   const WorkUnit *units;
+  const int32_t *uorder;  // units by cost, largest first
   const WsHeader *hdr;
+  int32_t *next_unit;     // claim counter over uorder (zeroed by the scheduler)
   int32_t *status;
   float *plse, *po;
 };
@@ -406,6 +437,8 @@ enum {
   B_P_FULL = 4,  // + Q tile
   B_O_DONE = 6,  // + Q tile
   B_FINAL = 8,
+  B_U_FULL = 9,    // + unit ring slot (kUnitRing)
+  B_U_EMPTY = 12,  // + unit ring slot
   B_RING = 16,  // K full[NK], K empty[NK], V full[NV], V empty[NV],
                 // I full[NI], I empty[NI]
 };
@@ -424,9 +457,44 @@ __device__ __forceinline__ void tile_keys(const WorkUnit &w, int j, int &kb, int
   }
 }
 
+// The CTA's r-th work unit: round r covers units r * G .. r * G + G - 1 (G
+// CTAs), forward on even rounds and backward on odd ones.  Over a work list
+// ordered largest first this evens out the total work per CTA.  Every role
+// of a CTA walks the same sequence.
+__device__ __forceinline__ int cta_unit(int r) {
+  const int G = (int)gridDim.x, base = r * G;
+  return (r & 1) ? base + (G - 1 - (int)blockIdx.x) : base + (int)blockIdx.x;
+}
+
 __device__ __forceinline__ void abort_cta(volatile int *abort_flag, int32_t *status, int code) {
   *abort_flag = 1;
   record_status(status, code);
+}
+
+// Units are claimed at run time: the index warp takes the next position of
+// the cost order (largest first) from a global counter and passes the unit
+// to the CTA's other warps through a small ring in shared memory (-1 ends
+// the stream).  A CTA that finishes early simply claims more, so the work
+// evens out without a cost model.
+constexpr int kUnitRing = 3;
+// Consumer side: the uc-th unit of this CTA, or -1 at the end or on a
+// timeout (then *ok is cleared).  The slot is released as soon as it is
+// read: by every lane of a warp (lane 0 arrives) or by a lone thread.
+__device__ __forceinline__ int ring_unit(uint64_t *bars, const volatile int *ring, uint32_t uc,
+                                         volatile int *abort_flag, bool whole_warp, bool &ok) {
+  const int slot = uc % kUnitRing;
+  if (!mbar_wait(&bars[B_U_FULL + slot], (uc / kUnitRing) & 1u, abort_flag)) {
+    ok = false;
+    return -1;
+  }
+  const int u = ring[slot];
+  if (whole_warp) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&bars[B_U_EMPTY + slot]);
+  } else {
+    mbar_arrive(&bars[B_U_EMPTY + slot]);
+  }
+  return u;
 }
 
 template <int HD, int MODE>
@@ -436,6 +504,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_unit[kUnitRing];
 
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -461,6 +530,10 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       mbar_init(&bars[B_O_DONE + i], 1);
     }
     mbar_init(&bars[B_FINAL], 1);
+    for (int i = 0; i < kUnitRing; ++i) {
+      mbar_init(&bars[B_U_FULL + i], 1);
+      mbar_init(&bars[B_U_EMPTY + i], 8 + 1 + C::COPY_THREADS / 32);
+    }
     for (int s = 0; s < C::NK; ++s) {
       mbar_init(&k_full[s], C::COPY_THREADS);
       mbar_init(&k_empty[s], 1);
@@ -497,8 +570,14 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     const uint32_t s_col = wg * C::BN;
     const uint32_t o_col = 2 * C::BN + wg * C::HDV;
     uint32_t s_cnt = 0, o_cnt = 0;
-    for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
-      const WorkUnit w = p.units[u];
+    bool ring_ok = true;
+    for (uint32_t uc = 0; !*abort_flag; ++uc) {
+      const int u = ring_unit(bars, s_unit, uc, abort_flag, true, ring_ok);
+      if (u < 0) {
+        if (!ring_ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+        break;
+      }
+      const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
       const int tok0 = wg * TOK;  // first token of this Q tile in the block
       if (wg == 1 && w.n_tok <= TOK) continue;
@@ -735,8 +814,10 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           tc_mma_ts_step<kk * 8, kk * 128>(d, a, b_lo, V_HI, C::IDESC_PV, kk > 0 ? 1u : acc0);
         });
       };
-      for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
-        const WorkUnit w = p.units[u];
+      for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+        const int u = ring_unit(bars, s_unit, uc, abort_flag, false, ok);
+        if (u < 0) break;
+        const WorkUnit w = p.units[p.uorder[u]];
         const int nt = w.n_tiles;
         if (nt == 0) continue;
         const bool q1 = w.n_tok > TOK;
@@ -820,8 +901,28 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     if (lane == 0) prefetch_tensormap(&tm.q);
     const uint32_t q_box_bytes = 64u * 2u * G * p.q_box_tok;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
-      const WorkUnit w = p.units[u];
+    for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+      // claim the next unit and hand it to the other warps
+      int u = -1;
+      if (lane == 0) {
+        const int pos = atomicAdd(p.next_unit, 1);
+        u = pos < n_units ? pos : -1;
+      }
+      u = __shfl_sync(0xffffffffu, u, 0);
+      {
+        const int slot = uc % kUnitRing;
+        if (uc >= (uint32_t)kUnitRing &&
+            !mbar_wait(&bars[B_U_EMPTY + slot], ((uc / kUnitRing) - 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          s_unit[slot] = u;
+          mbar_arrive(&bars[B_U_FULL + slot]);
+        }
+      }
+      if (u < 0) break;
+      const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
       if (nt == 0) continue;
       const bool q1 = w.n_tok > TOK;
@@ -916,8 +1017,10 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     };
     uint32_t kc = 0, vc = 0, ic = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
-      const WorkUnit w = p.units[u];
+    for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+      const int u = ring_unit(bars, s_unit, uc, abort_flag, true, ok);
+      if (u < 0) break;
+      const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
       if (nt == 0) continue;
       const bf16 *kp = p.k_pool + (int64_t)w.kvh * p.kb_sh + ch * 8;
@@ -1081,6 +1184,8 @@ WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int 
   off = align256(off + sizeof(int32_t) * (size_t)L.qb_max);
   L.units_off = off;
   off = align256(off + sizeof(WorkUnit) * (size_t)L.unit_max);
+  L.uorder_off = off;
+  off = align256(off + sizeof(int32_t) * (size_t)L.unit_max);
   L.comb_off = off;
   off = align256(off + sizeof(CombineEntry) * (size_t)L.comb_max);
   L.plse_off = off;
@@ -1196,6 +1301,7 @@ int launch_attention(const AttnArgs &a) {
   sp.hkv = a.hkv;
   sp.tok = (mla ? 1 : 2) * tok;
   sp.bn = mla ? MlaCfg<0>::BN : kBlockN;
+  sp.q_tile_tok = tok > 0 ? tok : 1;
   sp.n_dsplit = mla ? MlaCfg<0>::LV / MlaCfg<0>::DVS : 1;
   sp.window = a.window;
   sp.num_q_tokens = nq;
@@ -1207,6 +1313,7 @@ int launch_attention(const AttnArgs &a) {
   sp.seq = reinterpret_cast<int32_t *>(ws + L.seq_off);
   sp.qbt = reinterpret_cast<int32_t *>(ws + L.qb_off);
   sp.units = reinterpret_cast<WorkUnit *>(ws + L.units_off);
+  sp.uorder = reinterpret_cast<int32_t *>(ws + L.uorder_off);
   sp.comb = reinterpret_cast<CombineEntry *>(ws + L.comb_off);
   sp.hdr = hdr;
   sched_kernel<<<1, 1024, 0, a.stream>>>(sp);
@@ -1244,6 +1351,8 @@ int launch_attention(const AttnArgs &a) {
   kp.cap_pre = kp.use_cap ? sm_scale / a.logit_cap : 0.f;
   kp.cap_log2 = kp.use_cap ? a.logit_cap * log2e : 0.f;
   kp.units = sp.units;
+  kp.uorder = sp.uorder;
+  kp.next_unit = &hdr->next_unit;
   kp.hdr = hdr;
   kp.status = &hdr->status;
   kp.plse = reinterpret_cast<float *>(ws + L.plse_off);

@@ -96,8 +96,10 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     const int r = tid;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     uint32_t s_cnt = 0, o_cnt = 0;
-    for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
-      const WorkUnit w = p.units[u];
+    for (int ur = 0; ur * (int)gridDim.x < n_units && !*abort_flag; ++ur) {
+      const int u = cta_unit(ur);
+      if (u >= n_units) continue;
+      const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
       const int rows_valid = w.n_tok * G;
       const bool valid = r < rows_valid;
@@ -284,8 +286,10 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     if (lane == 0) {
       uint32_t q_cnt = 0, kc = 0, p_cnt = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
-        const WorkUnit w = p.units[u];
+      for (int ur = 0; ur * (int)gridDim.x < n_units && ok && !*abort_flag; ++ur) {
+        const int u = cta_unit(ur);
+        if (u >= n_units) continue;
+        const WorkUnit w = p.units[p.uorder[u]];
         const int nt = w.n_tiles;
         if (nt == 0) continue;
         if (!mbar_wait(&bars[M_Q_FULL], q_cnt & 1u, abort_flag)) { ok = false; break; }
@@ -327,8 +331,10 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     // ------------------------------------------------ row indices (one warp)
     uint32_t ic = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
-      const WorkUnit w = p.units[u];
+    for (int ur = 0; ur * (int)gridDim.x < n_units && ok && !*abort_flag; ++ur) {
+      const int u = cta_unit(ur);
+      if (u >= n_units) continue;
+      const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
       if (nt == 0) continue;
       const int64_t kv_base = p.kv_indptr[w.b];
@@ -380,8 +386,10 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     static_assert(C::BN * CPR % C::COPY_THREADS == 0, "even split of a tile");
     uint32_t kc = 0, ic = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok && !*abort_flag; u += gridDim.x) {
-      const WorkUnit w = p.units[u];
+    for (int ur = 0; ur * (int)gridDim.x < n_units && ok && !*abort_flag; ++ur) {
+      const int u = cta_unit(ur);
+      if (u >= n_units) continue;
+      const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
       if (nt == 0) continue;
       const bf16 *kp = p.k_pool + (int64_t)w.kvh * p.kb_sh;

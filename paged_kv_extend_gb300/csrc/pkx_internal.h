@@ -61,7 +61,8 @@ struct WsHeader {
   int32_t n_units;
   int32_t n_combine;
   int32_t split_tiles; // chunk size chosen by the scheduler (tiles)
-  int32_t pad[60];
+  int32_t next_unit;   // position in the cost order of the next unclaimed unit
+  int32_t pad[59];
 };
 
 // Byte offsets of the workspace regions for one problem.
@@ -69,6 +70,7 @@ struct WsLayout {
   size_t seq_off;      // int32 [8][batch + 1] per-sequence scratch
   size_t qb_off;       // int32 [qb_max] per-query-block tile counts
   size_t units_off;    // WorkUnit [unit_max]
+  size_t uorder_off;   // int32 [unit_max] units by cost, largest first
   size_t comb_off;     // CombineEntry [comb_max]
   size_t plse_off;     // float [slot_max][rows_per_slot]
   size_t po_off;       // float [slot_max][rows_per_slot][lv]
