@@ -457,15 +457,6 @@ __device__ __forceinline__ void tile_keys(const WorkUnit &w, int j, int &kb, int
   }
 }
 
-// The CTA's r-th work unit: round r covers units r * G .. r * G + G - 1 (G
-// CTAs), forward on even rounds and backward on odd ones.  Over a work list
-// ordered largest first this evens out the total work per CTA.  Every role
-// of a CTA walks the same sequence.
-__device__ __forceinline__ int cta_unit(int r) {
-  const int G = (int)gridDim.x, base = r * G;
-  return (r & 1) ? base + (G - 1 - (int)blockIdx.x) : base + (int)blockIdx.x;
-}
-
 __device__ __forceinline__ void abort_cta(volatile int *abort_flag, int32_t *status, int code) {
   *abort_flag = 1;
   record_status(status, code);
@@ -480,19 +471,20 @@ constexpr int kUnitRing = 3;
 // Consumer side: the uc-th unit of this CTA, or -1 at the end or on a
 // timeout (then *ok is cleared).  The slot is released as soon as it is
 // read: by every lane of a warp (lane 0 arrives) or by a lone thread.
-__device__ __forceinline__ int ring_unit(uint64_t *bars, const volatile int *ring, uint32_t uc,
+__device__ __forceinline__ int ring_unit(uint64_t *u_full, uint64_t *u_empty,
+                                         const volatile int *ring, uint32_t uc,
                                          volatile int *abort_flag, bool whole_warp, bool &ok) {
   const int slot = uc % kUnitRing;
-  if (!mbar_wait(&bars[B_U_FULL + slot], (uc / kUnitRing) & 1u, abort_flag)) {
+  if (!mbar_wait(&u_full[slot], (uc / kUnitRing) & 1u, abort_flag)) {
     ok = false;
     return -1;
   }
   const int u = ring[slot];
   if (whole_warp) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&bars[B_U_EMPTY + slot]);
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&u_empty[slot]);
   } else {
-    mbar_arrive(&bars[B_U_EMPTY + slot]);
+    mbar_arrive(&u_empty[slot]);
   }
   return u;
 }
@@ -572,7 +564,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ring_ok = true;
     for (uint32_t uc = 0; !*abort_flag; ++uc) {
-      const int u = ring_unit(bars, s_unit, uc, abort_flag, true, ring_ok);
+      const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ring_ok);
       if (u < 0) {
         if (!ring_ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
         break;
@@ -815,7 +807,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         });
       };
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-        const int u = ring_unit(bars, s_unit, uc, abort_flag, false, ok);
+        const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, false, ok);
         if (u < 0) break;
         const WorkUnit w = p.units[p.uorder[u]];
         const int nt = w.n_tiles;
@@ -1018,7 +1010,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     uint32_t kc = 0, vc = 0, ic = 0;
     bool ok = true;
     for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-      const int u = ring_unit(bars, s_unit, uc, abort_flag, true, ok);
+      const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ok);
       if (u < 0) break;
       const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;

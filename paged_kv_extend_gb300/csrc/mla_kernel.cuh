@@ -11,8 +11,11 @@
 // dims would fill it, leaving no room for S, so each work unit produces one
 // 128-dim slice of the value dims (w.dq) and recomputes S for it:
 //   TMEM  [0, 288)   Q tile, bf16 pairs (A operand of QK^T, TMEM form)
-//         [320, 384) S (fp32); P (bf16 pairs) is written over its first 32
+//         [288, 320) P (bf16 pairs, 64 keys)
+//         [320, 384) S (fp32)
 //         [384, 512) O slice (fp32)
+// The softmax releases S as soon as it holds the tile in registers, so QK^T
+// of the next K tile runs while it computes P and while PV runs.
 //   SMEM  three stages of a 64-key K tile (64 x 576 bf16, 128-byte swizzle,
 //         nine 64-dim blocks) + a ring of resolved row indices.
 // QK^T reads A = Q from TMEM and B = K from SMEM; PV reads A = P from TMEM and
@@ -30,10 +33,10 @@ struct MlaCfg {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_I = NK * K_BYTES;
   static constexpr int OFF_BAR = OFF_I + NI * I_BYTES;
-  static constexpr int N_BARS = 8 + 2 * NK + 2 * NI;
+  static constexpr int N_BARS = 16 + 2 * NK + 2 * NI;
   static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 1024;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int Q_COL = 0, S_COL = 320, O_COL = 384;
+  static constexpr int Q_COL = 0, P_COL = 288, S_COL = 320, O_COL = 384;
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DVS, 1);
   static constexpr int THREADS = 384;
@@ -41,7 +44,18 @@ struct MlaCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-enum { M_Q_FULL = 0, M_S_FULL = 1, M_P_FULL = 2, M_O_DONE = 3, M_FINAL = 4, M_RING = 8 };
+enum {
+  M_Q_FULL = 0,
+  M_S_FULL = 1,   // S landed
+  M_P_FULL = 2,   // P written
+  M_O_DONE = 3,   // last PV of a unit landed
+  M_FINAL = 4,
+  M_S_FREE = 5,   // S read into registers: the next QK^T may overwrite it
+  M_PV_DONE = 6,  // one phase per PV: P and O are free again
+  M_U_FULL = 8,   // + unit ring slot
+  M_U_EMPTY = 11, // + unit ring slot
+  M_RING = 16
+};
 
 template <int MODE>
 __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KParams p) {
@@ -49,6 +63,7 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_unit[kUnitRing];
 
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -66,9 +81,15 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
   if (tid == 0) {
     mbar_init(&bars[M_Q_FULL], 128);
     mbar_init(&bars[M_S_FULL], 1);
-    mbar_init(&bars[M_P_FULL], 128);
+    mbar_init(&bars[M_P_FULL], 4);  // one arrival per softmax warp
     mbar_init(&bars[M_O_DONE], 1);
     mbar_init(&bars[M_FINAL], 1);
+    mbar_init(&bars[M_S_FREE], 4);  // one arrival per softmax warp
+    mbar_init(&bars[M_PV_DONE], 1);
+    for (int i = 0; i < kUnitRing; ++i) {
+      mbar_init(&bars[M_U_FULL + i], 1);
+      mbar_init(&bars[M_U_EMPTY + i], 4 + 1 + C::COPY_THREADS / 32);
+    }
     for (int s = 0; s < C::NK; ++s) {
       mbar_init(&k_full[s], C::COPY_THREADS);
       mbar_init(&k_empty[s], 1);
@@ -96,9 +117,15 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     const int r = tid;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     uint32_t s_cnt = 0, o_cnt = 0;
-    for (int ur = 0; ur * (int)gridDim.x < n_units && !*abort_flag; ++ur) {
-      const int u = cta_unit(ur);
-      if (u >= n_units) continue;
+    uint32_t pv_base = 0;  // PVs of earlier units (M_PV_DONE phases)
+    bool ring_ok = true;
+    for (uint32_t uc = 0; !*abort_flag; ++uc) {
+      const int u = ring_unit(&bars[M_U_FULL], &bars[M_U_EMPTY], s_unit, uc, abort_flag, true,
+                              ring_ok);
+      if (u < 0) {
+        if (!ring_ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+        break;
+      }
       const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
       const int rows_valid = w.n_tok * G;
@@ -158,25 +185,33 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
         }
         ++s_cnt;
         tc_fence_after();
+        float x[C::BN];
         if (warp_active) {
-          float x[C::BN];
-          {
-            uint32_t v0[32], v1[32];
-            tmem_ld32(lane_base + C::S_COL + 0, v0);
-            tmem_ld32(lane_base + C::S_COL + 32, v1);
-            tmem_wait_ld();
+          uint32_t v0[32], v1[32];
+          tmem_ld32(lane_base + C::S_COL + 0, v0);
+          tmem_ld32(lane_base + C::S_COL + 32, v1);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              x[i] = __uint_as_float(v0[i]);
-              x[32 + i] = __uint_as_float(v1[i]);
-            }
+          for (int i = 0; i < 32; ++i) {
+            x[i] = __uint_as_float(v0[i]);
+            x[32 + i] = __uint_as_float(v1[i]);
           }
+        }
+        // S is in registers: the next QK^T may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[M_S_FREE]);
+        float alpha = 1.0f;
+        bool o_needs = false;
+        uint32_t pk[32];
+        if (warp_active) {
+          // Logits in the log2 domain are sc * x; a capped or masked tile
+          // is first mapped into the log2 domain (sc = 1).
+          float sc = p.scale_log2;
           if (p.use_cap) {
 #pragma unroll
             for (int i = 0; i < C::BN; ++i) x[i] = p.cap_log2 * tanh_approx(x[i] * p.cap_pre);
-          } else {
-#pragma unroll
-            for (int i = 0; i < C::BN; ++i) x[i] *= p.scale_log2;
+            sc = 1.0f;
           }
           const bool need_mask = (ke - 1 > w.qpos0) || (ke - kb < C::BN) ||
                                  (p.window > 0 && kb < qmax - p.window);
@@ -186,40 +221,63 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
               const int kpos = kb + i;
               const bool vis =
                   kpos < ke && kpos <= qpos && (p.window <= 0 || qpos - kpos <= p.window);
-              if (!vis) x[i] = -INFINITY;
+              x[i] = vis ? x[i] * sc : -INFINITY;
             }
+            sc = 1.0f;
           }
-          float mt0 = x[0], mt1 = x[1];
+          // row max of sc * x: sc * max(x), or sc * min(x) for a negative sc
+          float mt;
+          if (sc >= 0.f) {
+            float mt0 = x[0], mt1 = x[1];
 #pragma unroll
-          for (int i = 2; i < C::BN; i += 2) {
-            mt0 = fmaxf(mt0, x[i]);
-            mt1 = fmaxf(mt1, x[i + 1]);
+            for (int i = 2; i < C::BN; i += 2) {
+              mt0 = fmaxf(mt0, x[i]);
+              mt1 = fmaxf(mt1, x[i + 1]);
+            }
+            mt = fmaxf(mt0, mt1) * sc;
+          } else {
+            float mt0 = x[0], mt1 = x[1];
+#pragma unroll
+            for (int i = 2; i < C::BN; i += 2) {
+              mt0 = fminf(mt0, x[i]);
+              mt1 = fminf(mt1, x[i + 1]);
+            }
+            mt = fminf(mt0, mt1) * sc;
           }
-          const float m_new = fmaxf(m, fmaxf(mt0, mt1));
+          const float m_new = fmaxf(m, mt);
           const bool grow = m_new > m + 8.0f;
-          const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
-          const bool o_needs = grow && j > 0 && l > 0.f;
+          alpha = grow ? ex2_approx(m - m_new) : 1.0f;
+          o_needs = grow && j > 0 && l > 0.f;
           if (grow) {
             l *= alpha;
             m = m_new;
           }
-          const float mref = m == -INFINITY ? 0.f : m;
-          uint32_t pk[32];
+          const float nm = m == -INFINITY ? 0.f : -m;
           float l0 = 0.f, l1 = 0.f;
 #pragma unroll
           for (int i = 0; i < C::BN; i += 2) {
-            const float e0 = ex2_approx(x[i] - mref);
-            const float e1 = ex2_approx(x[i + 1] - mref);
+            const float e0 = ex2_approx(fmaf(x[i], sc, nm));
+            const float e1 = ex2_approx(fmaf(x[i + 1], sc, nm));
             l0 += e0;
             l1 += e1;
             pk[i / 2] = pack_bf16(e0, e1);
           }
           l += l0 + l1;
-          tmem_st32(lane_base + C::S_COL, pk);
+        }
+        // P's columns and O are free once the previous tile's PV has landed.
+        // Every warp waits, also one without rows: S of the next tile can
+        // land before this tile's P, and a warp that ran ahead would arrive
+        // on P_FULL twice in one phase.
+        if (j > 0 && !mbar_wait(&bars[M_PV_DONE], (pv_base + j - 1) & 1u, abort_flag)) {
+          abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+        }
+        tc_fence_after();
+        if (warp_active) {
+          tmem_st32(lane_base + C::P_COL, pk);
           if (__any_sync(0xffffffffu, o_needs)) {
             const float a = o_needs ? alpha : 1.0f;
             uint32_t v[32];
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < C::DVS / 32; ++c) {
               const uint32_t ta = lane_base + C::O_COL + c * 32;
               tmem_ld32(ta, v);
@@ -232,7 +290,8 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(&bars[M_P_FULL]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[M_P_FULL]);
       }
       if (*abort_flag) break;
       if (!mbar_wait(&bars[M_O_DONE], o_cnt & 1u, abort_flag)) {
@@ -240,6 +299,7 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
         break;
       }
       ++o_cnt;
+      pv_base += nt;
       tc_fence_after();
       if (warp_active) {
         const float inv = l > 0.f ? 1.0f / l : 0.f;
@@ -283,44 +343,70 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     }
   } else if (warp == 4) {
     // ------------------------------------------------ MMA issue (one thread)
+    // Per K tile j: S(j+1) = Q K(j+1)^T as soon as the softmax has read S(j),
+    // then O += P(j) V(j) once P(j) is written.  Descriptors are formed once
+    // per tile and stepped by constants.
     if (lane == 0) {
-      uint32_t q_cnt = 0, kc = 0, p_cnt = 0;
+      uint32_t q_cnt = 0, kc = 0, p_cnt = 0, f_cnt = 0;
       bool ok = true;
-      for (int ur = 0; ur * (int)gridDim.x < n_units && ok && !*abort_flag; ++ur) {
-        const int u = cta_unit(ur);
-        if (u >= n_units) continue;
+      constexpr uint32_t K_LO = sw128_desc_lo(0), K_HI = sw128_desc_hi(1024);
+      constexpr uint32_t V_LO = sw128_desc_lo(C::BN * 128), V_HI = sw128_desc_hi(1024);
+      auto issue_s = [&](uint32_t sK) {
+        const uint32_t b_lo = K_LO | (sK >> 4);
+        static_for<0, C::LQ / 16>([&](auto kk_c) {
+          constexpr int kk = decltype(kk_c)::value;
+          constexpr uint32_t bo = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) / 16;
+          tc_mma_ts_step<kk * 8, bo>(tmem + C::S_COL, tmem + C::Q_COL, b_lo, K_HI, C::IDESC_QK,
+                                     kk > 0 ? 1u : 0u);
+        });
+        tc_commit(&bars[M_S_FULL]);
+      };
+      auto issue_pv = [&](uint32_t sV, bool acc_first) {
+        const uint32_t b_lo = V_LO | (sV >> 4);
+        const uint32_t acc0 = acc_first ? 1u : 0u;
+        static_for<0, C::BN / 16>([&](auto kk_c) {
+          constexpr int kk = decltype(kk_c)::value;
+          tc_mma_ts_step<kk * 8, kk * 128>(tmem + C::O_COL, tmem + C::P_COL, b_lo, V_HI,
+                                           C::IDESC_PV, kk > 0 ? 1u : acc0);
+        });
+        tc_commit(&bars[M_PV_DONE]);
+      };
+      auto k_tile = [&](uint32_t kpos) { return sbase + C::OFF_K + (kpos % C::NK) * C::K_BYTES; };
+      for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+        const int u = ring_unit(&bars[M_U_FULL], &bars[M_U_EMPTY], s_unit, uc, abort_flag, false,
+                                ok);
+        if (u < 0) break;
         const WorkUnit w = p.units[p.uorder[u]];
         const int nt = w.n_tiles;
         if (nt == 0) continue;
         if (!mbar_wait(&bars[M_Q_FULL], q_cnt & 1u, abort_flag)) { ok = false; break; }
         ++q_cnt;
         tc_fence_after();
+        const uint32_t k0 = kc;  // ring position of this unit's first K tile
+        if (!mbar_wait(&k_full[k0 % C::NK], (k0 / C::NK) & 1u, abort_flag)) { ok = false; break; }
+        fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.mma reads
+        tc_fence_after();
+        issue_s(k_tile(k0));
+        const uint32_t dv_off = (w.dq * (C::DVS / 64)) * (C::BN * 128);
         for (int j = 0; j < nt; ++j) {
-          const int ks = kc % C::NK;
-          if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag)) { ok = false; break; }
-          fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.mma reads
+          if (!mbar_wait(&bars[M_S_FREE], f_cnt & 1u, abort_flag)) { ok = false; break; }
+          ++f_cnt;
           tc_fence_after();
-          const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
-#pragma unroll 1
-          for (int kk = 0; kk < C::LQ / 16; ++kk) {
-            const uint64_t bd = sw128_desc(sK + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 0, 1024);
-            tc_mma_ts(tmem + C::S_COL, tmem + C::Q_COL + kk * 8, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          if (j + 1 < nt) {
+            const uint32_t kn = k0 + j + 1;
+            if (!mbar_wait(&k_full[kn % C::NK], (kn / C::NK) & 1u, abort_flag)) { ok = false; break; }
+            fence_proxy_async_smem();
+            tc_fence_after();
+            issue_s(k_tile(kn));
           }
-          tc_commit(&bars[M_S_FULL]);
           if (!mbar_wait(&bars[M_P_FULL], p_cnt & 1u, abort_flag)) { ok = false; break; }
           ++p_cnt;
           tc_fence_after();
-          const uint32_t sV = sK + (w.dq * (C::DVS / 64)) * (C::BN * 128);
-#pragma unroll 1
-          for (int kk = 0; kk < C::BN / 16; ++kk) {
-            const uint64_t bd = sw128_desc(sV + kk * 2048, C::BN * 128, 1024);
-            tc_mma_ts(tmem + C::O_COL, tmem + C::S_COL + kk * 8, bd, C::IDESC_PV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(&k_empty[ks]);
-          ++kc;
+          issue_pv(k_tile(k0 + j) + dv_off, j > 0);
+          tc_commit(&k_empty[(k0 + j) % C::NK]);
         }
         if (!ok) break;
+        kc = k0 + nt;
         tc_commit(&bars[M_O_DONE]);
       }
       if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
@@ -331,9 +417,27 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     // ------------------------------------------------ row indices (one warp)
     uint32_t ic = 0;
     bool ok = true;
-    for (int ur = 0; ur * (int)gridDim.x < n_units && ok && !*abort_flag; ++ur) {
-      const int u = cta_unit(ur);
-      if (u >= n_units) continue;
+    for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+      // claim the next unit and hand it to the other warps
+      int u = -1;
+      if (lane == 0) {
+        const int pos = atomicAdd(p.next_unit, 1);
+        u = pos < n_units ? pos : -1;
+      }
+      u = __shfl_sync(0xffffffffu, u, 0);
+      {
+        const int slot = uc % kUnitRing;
+        if (uc >= (uint32_t)kUnitRing &&
+            !mbar_wait(&bars[M_U_EMPTY + slot], ((uc / kUnitRing) - 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          s_unit[slot] = u;
+          mbar_arrive(&bars[M_U_FULL + slot]);
+        }
+      }
+      if (u < 0) break;
       const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
       if (nt == 0) continue;
@@ -386,9 +490,9 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     static_assert(C::BN * CPR % C::COPY_THREADS == 0, "even split of a tile");
     uint32_t kc = 0, ic = 0;
     bool ok = true;
-    for (int ur = 0; ur * (int)gridDim.x < n_units && ok && !*abort_flag; ++ur) {
-      const int u = cta_unit(ur);
-      if (u >= n_units) continue;
+    for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+      const int u = ring_unit(&bars[M_U_FULL], &bars[M_U_EMPTY], s_unit, uc, abort_flag, true, ok);
+      if (u < 0) break;
       const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
       if (nt == 0) continue;
