@@ -484,10 +484,26 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
   } else {
     // ------------------------------------------------ K-row copies (6 warps)
+    // Thread ct copies flat chunks c = ct + 192 i (key c / 72, 16-byte chunk
+    // c % 72), so consecutive lanes read consecutive bytes of a row.  Since
+    // 3 x 192 = 8 rows, steps i and i + 3 share the chunk and the key mod 8:
+    // three destination bases cover all steps, the rest is a constant
+    // offset of 1024 bytes per 3 steps.
     const int ct = tid - 6 * 32;
     constexpr int CPR = C::LQ / 8;  // 72 chunks of 16 bytes per row
     constexpr int NCH = C::BN * CPR / C::COPY_THREADS;  // 24 chunks per thread
-    static_assert(C::BN * CPR % C::COPY_THREADS == 0, "even split of a tile");
+    static_assert(C::BN * CPR % C::COPY_THREADS == 0 && 3 * C::COPY_THREADS == 8 * CPR &&
+                      NCH % 3 == 0,
+                  "copy steps repeat every 8 rows");
+    int kq[3], cq[3];
+    uint32_t dq[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const int c = ct + q * C::COPY_THREADS;
+      kq[q] = c / CPR;
+      cq[q] = c - kq[q] * CPR;
+      dq[q] = (uint32_t)(cq[q] >> 3) * (C::BN * 128) + sw128_off(kq[q], cq[q] & 7);
+    }
     uint32_t kc = 0, ic = 0;
     bool ok = true;
     for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
@@ -518,15 +534,13 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
         const bf16 *base = from_ext ? kx : kp;
         const int64_t st = from_ext ? p.ke_st : p.kb_ss;
         const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
-#pragma unroll 4
-        for (int i = 0; i < NCH; ++i) {
-          const int c = ct + i * C::COPY_THREADS;
-          const int key = c / CPR, ch = c - (c / CPR) * CPR;
-          const int row = ring[key];
+        static_for<0, NCH>([&](auto i_c) {
+          constexpr int i = decltype(i_c)::value, q = i % 3, step = i / 3;
+          const int row = ring[kq[q] + 8 * step];
           const bool v = row >= 0;
-          cp_async_16(sK + (ch >> 3) * (C::BN * 128) + sw128_off(key, ch & 7),
-                      v ? base + (int64_t)row * st + ch * 8 : p.k_pool, v ? 16u : 0u);
-        }
+          cp_async_16_at<step * 1024, 0>(sK + dq[q], (v ? base + (int64_t)row * st : base) + cq[q] * 8,
+                                         v ? 16u : 0u);
+        });
         cp_async_arrive_noinc(&k_full[ks]);
         mbar_arrive(&i_empty[is]);
         ++kc;
