@@ -61,7 +61,7 @@ struct SchedParams {
   int n_dsplit;  // units per (block, split): value-dim slices (1, or 4 for MLA)
   int unit_target, qb_max, unit_max, comb_max, slot_max;
   int32_t *seq;  // 8 arrays of batch+1 ints
-  int32_t *qbt;  // tiles per query block
+  int32_t *qbt;  // [5][qb_max]: tiles, sequence, unit / slot / combine offsets per block
   WorkUnit *units;
   int32_t *uorder;  // units by cost, largest first
   CombineEntry *comb;
@@ -161,6 +161,25 @@ __device__ int block_exclusive_scan(const int32_t *in, int32_t *out, int n, int 
   return total;
 }
 
+// Exclusive scan of one value per thread over the 1024-thread block; the
+// total goes to *total.
+__device__ int block_scan_value(int v, int *sh, int &total) {
+  const int tid = threadIdx.x;
+  __syncthreads();
+  sh[tid] = v;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int x = tid >= off ? sh[tid - off] : 0;
+    __syncthreads();
+    sh[tid] += x;
+    __syncthreads();
+  }
+  const int incl = sh[tid];
+  total = sh[1023];
+  __syncthreads();
+  return incl - v;
+}
+
 // Per-block tile counts live in shared memory when they fit (they are read
 // back many times while the units are emitted).
 constexpr int kSchedSmemBlocks = 8192;
@@ -183,11 +202,6 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   const int B = p.batch;
   int32_t *nqb = p.seq;                 // [B]  query blocks per sequence
   int32_t *qboff = p.seq + 1 * (B + 1); // [B]  first query block of sequence
-  int32_t *work = p.seq + 2 * (B + 1);  // [B]  KV tiles of the sequence
-  int32_t *order = p.seq + 3 * (B + 1); // [B]  rank -> sequence
-  int32_t *ucnt = p.seq + 4 * (B + 1);  // [B]  by rank: units, then offsets
-  int32_t *scnt = p.seq + 5 * (B + 1);  // [B]  by rank: partial slots
-  int32_t *ccnt = p.seq + 6 * (B + 1);  // [B]  by rank: combine entries
 
   if (tid == 0) {
     p.hdr->status = 0;
@@ -209,21 +223,23 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   }
 
   int32_t *qbt = total_qb <= kSchedSmemBlocks ? s_qbt : p.qbt;
+  int32_t *qbs = p.qbt + p.qb_max;      // [total_qb] sequence of the block
+  int32_t *quo = p.qbt + 2 * p.qb_max;  // first unit of the block (one KV head)
+  int32_t *qso = p.qbt + 3 * p.qb_max;  // first partial slot
+  int32_t *qco = p.qbt + 4 * p.qb_max;  // combine entry
 
-  // 2. KV tiles per query block and per sequence; total tiles
+  // 2. KV tiles per query block; total tiles
   long long my_tiles = 0;
   for (int b = tid; b < B; b += 1024) {
     SeqDims d = seq_dims(p, b);
-    int w = 0;
     for (int qb = 0; qb < d.nqb; ++qb) {
       int lo, hi, i0, i1;
       qblock_range(p, d, qb, lo, hi, i0, i1);
-      int nt = (hi - lo + p.bn - 1) / p.bn;
+      const int nt = (hi - lo + p.bn - 1) / p.bn;
       qbt[qboff[b] + qb] = nt;
-      w += nt;
+      qbs[qboff[b] + qb] = b;
+      my_tiles += nt;
     }
-    work[b] = w;
-    my_tiles += w;
   }
   __syncthreads();
   sh[tid] = (int)min(my_tiles, (long long)0x3fffffff);
@@ -242,46 +258,40 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   __syncthreads();
   const int C = s_c;
 
-  // 3. order sequences by work, largest first (ties by index); identity for
-  //    very large batches
-  if (B <= 8192) {
-    for (int b = tid; b < B; b += 1024) {
-      const int wb = work[b];
-      int rank = 0;
-      for (int c = 0; c < B; ++c) {
-        const int wc = work[c];
-        rank += (wc > wb) || (wc == wb && c < b);
-      }
-      order[rank] = b;
+  // 3. per query block (of one KV head): units (splits x value slices),
+  //    partial slots and combine entries, and their offsets (each thread
+  //    scans a contiguous chunk of blocks)
+  const int nd = p.n_dsplit;
+  auto splits = [&](int nt) { return nt > 0 ? (nt + C - 1) / C : 1; };
+  const int chunk = (total_qb + 1023) / 1024;
+  const int qb_beg = min(total_qb, tid * chunk), qb_end = min(total_qb, qb_beg + chunk);
+  int lu = 0, ls = 0, lc = 0;
+  for (int qb = qb_beg; qb < qb_end; ++qb) {
+    const int S = splits(qbt[qb]);
+    lu += S * nd;
+    if (S > 1) {
+      ls += S;
+      lc += 1;
     }
-  } else {
-    for (int b = tid; b < B; b += 1024) order[b] = b;
   }
-  __syncthreads();
-
-  // 4. units, partial slots and combine entries per sequence (by rank)
-  for (int rk = tid; rk < B; rk += 1024) {
-    const int b = order[rk];
-    const int n = nqb[b];
-    int u = 0, s = 0, c = 0;
-    for (int qb = 0; qb < n; ++qb) {
-      const int nt = qbt[qboff[b] + qb];
-      const int S = nt > 0 ? (nt + C - 1) / C : 1;
-      u += S;
-      if (S > 1) {
-        s += S;
-        c += 1;
-      }
+  int tu, ts, tcm;
+  int u0 = block_scan_value(lu, sh, tu);
+  int s0 = block_scan_value(ls, sh, ts);
+  int c0 = block_scan_value(lc, sh, tcm);
+  for (int qb = qb_beg; qb < qb_end; ++qb) {
+    quo[qb] = u0;
+    qso[qb] = s0;
+    qco[qb] = c0;
+    const int S = splits(qbt[qb]);
+    u0 += S * nd;
+    if (S > 1) {
+      s0 += S;
+      c0 += 1;
     }
-    ucnt[rk] = u * p.hkv * p.n_dsplit;
-    scnt[rk] = s * p.hkv;
-    ccnt[rk] = c * p.hkv;
   }
-  __syncthreads();
-  const int n_units = block_exclusive_scan(ucnt, ucnt, B, sh);
-  const int n_slots = block_exclusive_scan(scnt, scnt, B, sh);
-  const int n_comb = block_exclusive_scan(ccnt, ccnt, B, sh);
-  if (n_units > p.unit_max || n_slots > p.slot_max || n_comb > p.comb_max) {
+  const long long n_units_l = (long long)tu * p.hkv, n_slots_l = (long long)ts * p.hkv,
+                  n_comb_l = (long long)tcm * p.hkv;
+  if (n_units_l > p.unit_max || n_slots_l > p.slot_max || n_comb_l > p.comb_max) {
     if (tid == 0) {
       record_status(&p.hdr->status, PKX_EDEVICE);
       p.hdr->n_units = 0;
@@ -289,62 +299,49 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     }
     return;
   }
+  const int n_units = (int)n_units_l, n_comb = (int)n_comb_l;
+  __syncthreads();
 
-  // 5. emit, one (sequence, KV head) pair per thread: sequences largest
-  //    first, then KV heads, then query blocks from the last (longest key
-  //    range) to the first, then splits.
-  for (int idx = tid; idx < B * p.hkv; idx += 1024) {
-    const int rk = idx / p.hkv, kvh = idx - (idx / p.hkv) * p.hkv;
-    const int b = order[rk];
+  // 4. emit, one (KV head, query block) pair at a time per thread
+  for (int idx = tid; idx < p.hkv * total_qb; idx += 1024) {
+    const int kvh = idx / total_qb, qb = idx - kvh * total_qb;
+    const int b = qbs[qb];
     SeqDims d = seq_dims(p, b);
     const int split_at = p.mode == kTwoStage ? d.P : INT_MAX;
-    // this sequence's units, slots and combine entries per KV head
-    int u1 = 0, s1 = 0, c1 = 0;
-    for (int qb = 0; qb < d.nqb; ++qb) {
-      const int nt = qbt[qboff[b] + qb];
-      const int S = nt > 0 ? (nt + C - 1) / C : 1;
-      u1 += S * p.n_dsplit;
-      if (S > 1) {
-        s1 += S;
-        c1 += 1;
-      }
+    int lo, hi, i0, i1;
+    qblock_range(p, d, qb - qboff[b], lo, hi, i0, i1);
+    const int nt = qbt[qb];
+    const int S = splits(nt);
+    const int tps = nt > 0 ? (nt + S - 1) / S : 0;
+    int uo = kvh * tu + quo[qb];
+    const int so = kvh * ts + qso[qb];
+    if (S > 1) {
+      CombineEntry e;
+      e.q_tok0 = d.qbase + i0;
+      e.n_tok = i1 - i0;
+      e.kvh = kvh;
+      e.slot0 = so;
+      e.n_split = S;
+      e.pad[0] = e.pad[1] = e.pad[2] = 0;
+      p.comb[kvh * tcm + qco[qb]] = e;
     }
-    int uo = ucnt[rk] + kvh * u1, so = scnt[rk] + kvh * s1, co = ccnt[rk] + kvh * c1;
-    for (int qb = d.nqb - 1; qb >= 0; --qb) {
-      int lo, hi, i0, i1;
-      qblock_range(p, d, qb, lo, hi, i0, i1);
-      const int nt = qbt[qboff[b] + qb];
-      const int S = nt > 0 ? (nt + C - 1) / C : 1;
-      const int tps = nt > 0 ? (nt + S - 1) / S : 0;
-      if (S > 1) {
-        CombineEntry e;
-        e.q_tok0 = d.qbase + i0;
-        e.n_tok = i1 - i0;
-        e.kvh = kvh;
-        e.slot0 = so;
-        e.n_split = S;
-        e.pad[0] = e.pad[1] = e.pad[2] = 0;
-        p.comb[co++] = e;
+    for (int sp = 0; sp < S; ++sp) {
+      for (int dq = 0; dq < nd; ++dq) {
+        WorkUnit w;
+        w.q_tok0 = d.qbase + i0;
+        w.n_tok = i1 - i0;
+        w.qpos0 = d.P + i0;
+        w.kvh = kvh;
+        w.k_begin = min(hi, lo + sp * tps * p.bn);
+        w.k_end = min(hi, lo + (sp + 1) * tps * p.bn);
+        w.k_split = split_at;
+        w.n_tiles = range_tiles(w.k_begin, w.k_end, split_at, p.bn);
+        w.b = b;
+        w.slot = S > 1 ? so + sp : -1;
+        w.dq = dq;
+        w.pad = 0;
+        p.units[uo++] = w;
       }
-      for (int s = 0; s < S; ++s) {
-        for (int dq = 0; dq < p.n_dsplit; ++dq) {
-          WorkUnit w;
-          w.q_tok0 = d.qbase + i0;
-          w.n_tok = i1 - i0;
-          w.qpos0 = d.P + i0;
-          w.kvh = kvh;
-          w.k_begin = min(hi, lo + s * tps * p.bn);
-          w.k_end = min(hi, lo + (s + 1) * tps * p.bn);
-          w.k_split = split_at;
-          w.n_tiles = range_tiles(w.k_begin, w.k_end, split_at, p.bn);
-          w.b = b;
-          w.slot = S > 1 ? so + s : -1;
-          w.dq = dq;
-          w.pad = 0;
-          p.units[uo++] = w;
-        }
-      }
-      if (S > 1) so += S;
     }
   }
 
@@ -1173,7 +1170,7 @@ WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int 
   L.seq_off = off;
   off = align256(off + sizeof(int32_t) * 8 * (size_t)(batch + 1));
   L.qb_off = off;
-  off = align256(off + sizeof(int32_t) * (size_t)L.qb_max);
+  off = align256(off + sizeof(int32_t) * 5 * (size_t)L.qb_max);
   L.units_off = off;
   off = align256(off + sizeof(WorkUnit) * (size_t)L.unit_max);
   L.uorder_off = off;

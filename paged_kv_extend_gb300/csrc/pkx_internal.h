@@ -67,8 +67,8 @@ struct WsHeader {
 
 // Byte offsets of the workspace regions for one problem.
 struct WsLayout {
-  size_t seq_off;      // int32 [8][batch + 1] per-sequence scratch
-  size_t qb_off;       // int32 [qb_max] per-query-block tile counts
+  size_t seq_off;      // int32 [8][batch + 1] per-sequence scratch (two used)
+  size_t qb_off;       // int32 [5][qb_max] per-query-block scheduler arrays
   size_t units_off;    // WorkUnit [unit_max]
   size_t uorder_off;   // int32 [unit_max] units by cost, largest first
   size_t comb_off;     // CombineEntry [comb_max]
