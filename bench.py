@@ -20,6 +20,7 @@ this build), on a bounded row sample of the same workload per step.
 from __future__ import annotations
 
 import argparse
+import copy
 import json
 import math
 import os
@@ -325,6 +326,15 @@ class ExtendStep:
         return [self.q, self.prefix_indptr, self.prefix_indices, self.extend_start,
                 self.extend_lens, self.extend_indices, self.qo_indptr]
 
+    def twin(self):
+        """The same step over the same pool with its own input, output and
+        workspace buffers (double buffering of the end-to-end loop)."""
+        t = copy.copy(self)
+        for name in ("q", "prefix_indptr", "prefix_indices", "extend_start", "extend_lens",
+                     "extend_indices", "qo_indptr", "uptr", "uidx", "plen", "o", "lse", "ws"):
+            setattr(t, name, torch.empty_like(getattr(self, name)))
+        return t
+
     def __call__(self):
         s = self.wl.spec
         self.pkx.build_unified_kv_indices(self.prefix_indptr, self.prefix_indices,
@@ -359,6 +369,12 @@ class DecodeStep:
 
     def inputs(self):
         return [self.q, self.kvp, self.kvi]
+
+    def twin(self):
+        t = copy.copy(self)
+        for name in ("q", "kvp", "kvi", "o", "lse", "ws"):
+            setattr(t, name, torch.empty_like(getattr(self, name)))
+        return t
 
     def __call__(self):
         s = self.wl.spec
@@ -421,6 +437,73 @@ def measure_e2e(step: ExtendStep, steps, warmup, flush, dev):
         e2e_step()
     ms, _ = time_steps(e2e_step, steps, flush, dev)
     return sum(ms) / len(ms), h2d, d2h
+
+
+def measure_e2e_pipelined(step, steps, warmup, flush, dev):
+    """The end-to-end loop as a server runs it: step i's inputs are copied
+    host-to-device on one stream while step i-1 computes, and step i's o is
+    copied back on another stream while step i+1 computes (two device
+    buffer sets alternate).  Every step's own copies and the L2 flush before
+    its compute are inside the timed region; time per step = total / steps."""
+    pin = lambda t: t.cpu().pin_memory()
+    pair = (step, step.twin())
+    host_in = [pin(t) for t in step.inputs()]
+    host_o = [torch.empty(st.o.shape, dtype=st.o.dtype).pin_memory() for st in pair]
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(n):
+        ev = lambda: torch.cuda.Event()
+        h2d_done, comp_done, d2h_done = [ev() for _ in range(n)], [ev() for _ in range(n)], \
+            [ev() for _ in range(n)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)
+        for i in range(n):
+            st = pair[i & 1]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[i - 2])  # this buffer set's inputs are free
+                for h, d in zip(host_in, st.inputs()):
+                    d.copy_(h, non_blocking=True)
+                h2d_done[i].record(s_in)
+            comp.wait_event(h2d_done[i])
+            if i >= 2:
+                comp.wait_event(d2h_done[i - 2])  # this buffer set's o has been read
+            flush.zero_()
+            st()
+            comp_done[i].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[i])
+                host_o[i & 1].copy_(st.o, non_blocking=True)
+                d2h_done[i].record(s_out)
+        s_out.wait_event(d2h_done[n - 1])
+        t1.record(s_out)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1) / n
+
+    run(max(warmup, 2))
+    ms = run(steps)
+    # the copies really carried the data: the last o read back equals the device o
+    last = pair[(steps - 1) & 1]
+    assert torch.equal(host_o[(steps - 1) & 1], last.o.cpu()), "pipelined e2e lost data"
+    return ms
+
+
+def e2e_entry(pipelined, serial, unit, h2d, d2h):
+    """The end-to-end figure: the faster of the two host loops, named, with
+    the other one beside it."""
+    modes = {
+        "pipelined": "step i's H2D and D2H run on copy streams while the neighbouring steps "
+                     "compute (two device buffer sets); each step's copies and its L2 flush "
+                     "are inside the timed region",
+        "serial": "per step: H2D of the inputs, the step, D2H of o, in order on one stream "
+                  "(L2 flushed before each step, outside the events)",
+    }
+    best = "pipelined" if pipelined >= serial else "serial"
+    return {"value": max(pipelined, serial), "unit": unit, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "mode": f"{best}: {modes[best]}",
+            "pipelined_value": pipelined, "serial_value": serial}
 
 
 def measure_component(name, dev, flush, steps, hbm_peak, bf16_peak):
@@ -489,7 +572,9 @@ def run_ours(args, ws, rank, local):
     value = flops * ws / (ms_max * 1e-3) / 1e12
     achieved = flops / (attn_avg * 1e-3) / 1e12
 
-    e2e_ms, h2d, d2h = measure_e2e(step, args.steps, 2, flush, dev)
+    e2e_serial_ms, h2d, d2h = measure_e2e(step, args.steps, 2, flush, dev)
+    e2e_serial_ms = max_over_ranks(e2e_serial_ms, ws, dev)
+    e2e_ms = measure_e2e_pipelined(step, args.steps, 2, flush, dev)
     e2e_ms = max_over_ranks(e2e_ms, ws, dev)
 
     components = {"attn_kernel_share_of_step": attn_avg / ms}
@@ -539,6 +624,7 @@ def run_ours(args, ws, rank, local):
                 "peak_source": f"hbm_gbs copy bandwidth, of {peak_src}",
                 "kernel": "attn_kernel (decode)", "algorithmic_bytes_per_launch": step.bytes}
         e2e_value = step.bytes * ws / (e2e_ms * 1e-3) / 1e9
+        e2e_serial = step.bytes * ws / (e2e_serial_ms * 1e-3) / 1e9
     else:
         metric, unit = "extend-attn TFLOP/s", "TFLOP/s"
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak,
@@ -548,6 +634,7 @@ def run_ours(args, ws, rank, local):
                 "algorithmic_flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": step.bytes}
         e2e_value = flops * ws / (e2e_ms * 1e-3) / 1e12
+        e2e_serial = flops * ws / (e2e_serial_ms * 1e-3) / 1e12
     line = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -555,8 +642,7 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic", "config": config_dict(wl),
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": unit,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": e2e_entry(e2e_value, e2e_serial, unit, h2d, d2h),
         "gpu_launches": step.launches * args.steps,
         "clocks": clock_info,
         "components": components,
