@@ -54,11 +54,11 @@ def _configure(lib):
     lib.oracle_extend_attention.restype = _i
     lib.oracle_extend_attention.argtypes = [
         _p, _p, _l, _l, _p, _l, _l, _p, _l, _l, _p, _l, _l,
-        _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _l, _p, _l, _p, _p]
+        _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _l, _p, _p, _p, _p, _l, _p, _p]
     lib.oracle_extend_attention_unified.restype = _i
     lib.oracle_extend_attention_unified.argtypes = [
         _p, _p, _l, _l, _p, _l, _l, _p, _p, _p, _p,
-        _i, _i, _i, _i, _i, _d, _d, _l, _p, _l, _p, _p]
+        _i, _i, _i, _i, _i, _d, _d, _l, _p, _p, _p, _p, _l, _p, _p]
     lib.oracle_decode_attention.restype = _i
     lib.oracle_decode_attention.argtypes = [
         _p, _p, _l, _l, _p, _l, _l, _p, _p,
@@ -141,13 +141,39 @@ def _rows_arg(rows):
     return r, r.numel()
 
 
+def _mask_args(custom_mask, mask_indptr, sinks, hq):
+    """(custom_mask uint8, mask_indptr int32, sinks float64) tensors or None;
+    a custom mask needs its offsets, sinks are one logit per query head."""
+    cm = mi = sk = None
+    if custom_mask is not None:
+        if mask_indptr is None:
+            raise ValueError("custom_mask needs mask_indptr")
+        cm = torch.as_tensor(custom_mask).to(torch.uint8).contiguous().cpu()
+        mi = _i32(mask_indptr)
+    if sinks is not None:
+        sk = torch.as_tensor(sinks).to(torch.float64).contiguous().cpu()
+        if sk.numel() != hq:
+            raise ValueError("sinks must hold one value per query head")
+    return cm, mi, sk
+
+
+def _opt(t):
+    return _ptr(t) if t is not None and t.numel() else None
+
+
 # ------------------------------------------------------------------ functions
 def extend_attention(q_extend, k_extend, v_extend, k_buffer, v_buffer,
                      qo_indptr, kv_indptr, kv_indices, sm_scale, logit_cap=0.0,
-                     sliding_window=-1, rows=None):
+                     sliding_window=-1, rows=None, custom_mask=None, mask_indptr=None,
+                     sinks=None):
     """Two-stage extend attention (sglang extend_attention.py,
     extend_attention_fwd): prefix K/V through kv_indptr/kv_indices into the
     pool, extend K/V contiguous at qo_indptr.
+
+    custom_mask (bytes, row i of sequence b at mask_indptr[b] + i * T_b over
+    its T_b keys) replaces the causal mask; sinks [Hq] add exp(sink - m) to
+    each row's softmax denominator (sglang extend_attention.py,
+    _fwd_kernel_unified).
 
     q_extend [N, Hq, Lq] bf16; k_extend [N, Hkv, Lq]; v_extend [N, Hkv, Lv];
     k_buffer [S, Hkv, Lq]; v_buffer [S, Hkv, Lv] (views with a contiguous last
@@ -166,6 +192,7 @@ def extend_attention(q_extend, k_extend, v_extend, k_buffer, v_buffer,
     kb, vb = _bf16_bits(k_buffer), _bf16_bits(v_buffer)
     qo, kvp, kvi = _i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices)
     batch = qo.numel() - 1
+    cm, mi, sk = _mask_args(custom_mask, mask_indptr, sinks, hq)
     rws, nr = _rows_arg(rows)
     count = nr if rws is not None else n * hq
     o = torch.empty(count, lv, dtype=torch.float64)
@@ -175,8 +202,8 @@ def extend_attention(q_extend, k_extend, v_extend, k_buffer, v_buffer,
         _ptr(kb), *_row_strides(kb), _ptr(vb), *_row_strides(vb),
         _ptr(qo), _ptr(kvp), _ptr(kvi) if kvi.numel() else None,
         batch, hq, hkv, lq, lv, float(sm_scale), float(logit_cap),
-        int(sliding_window), _ptr(rws) if rws is not None else None, nr,
-        _ptr(o), _ptr(lse))
+        int(sliding_window), _opt(cm), _opt(mi), _opt(sk),
+        _ptr(rws) if rws is not None else None, nr, _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_extend_attention: bad arguments")
     if rws is None:
@@ -186,7 +213,8 @@ def extend_attention(q_extend, k_extend, v_extend, k_buffer, v_buffer,
 
 def extend_attention_unified(q, k_buffer, v_buffer, qo_indptr, kv_indptr,
                              kv_indices, prefix_lens, sm_scale, logit_cap=0.0,
-                             sliding_window=-1, rows=None):
+                             sliding_window=-1, rows=None, custom_mask=None,
+                             mask_indptr=None, sinks=None):
     """Unified extend attention (sglang extend_attention.py,
     extend_attention_fwd_unified): all keys through the unified int64
     kv_indices; the first prefix_lens[b] keys of sequence b are its prefix.
@@ -201,6 +229,7 @@ def extend_attention_unified(q, k_buffer, v_buffer, qo_indptr, kv_indptr,
     kb, vb = _bf16_bits(k_buffer), _bf16_bits(v_buffer)
     qo, kvp, kvi, pl = _i32(qo_indptr), _i32(kv_indptr), _i64(kv_indices), _i32(prefix_lens)
     batch = qo.numel() - 1
+    cm, mi, sk = _mask_args(custom_mask, mask_indptr, sinks, hq)
     rws, nr = _rows_arg(rows)
     count = nr if rws is not None else n * hq
     o = torch.empty(count, lv, dtype=torch.float64)
@@ -209,8 +238,8 @@ def extend_attention_unified(q, k_buffer, v_buffer, qo_indptr, kv_indptr,
         _ptr(qb), _ptr(kb), *_row_strides(kb), _ptr(vb), *_row_strides(vb),
         _ptr(qo), _ptr(kvp), _ptr(kvi) if kvi.numel() else None, _ptr(pl),
         batch, hq, hkv, lq, lv, float(sm_scale), float(logit_cap),
-        int(sliding_window), _ptr(rws) if rws is not None else None, nr,
-        _ptr(o), _ptr(lse))
+        int(sliding_window), _opt(cm), _opt(mi), _opt(sk),
+        _ptr(rws) if rws is not None else None, nr, _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_extend_attention_unified: bad arguments")
     if rws is None:

@@ -33,6 +33,17 @@
  *
  * where a sequence's keys are its P prefix keys followed by its E extend keys,
  * and extend query i sits at position qpos = P + i.
+ *
+ * Optional, as in [EXT] _fwd_kernel_unified:
+ *   custom mask: a byte per (extend row i, key j) of sequence b at
+ *     custom_mask[mask_indptr[b] + i * T_b + j]; when given it replaces the
+ *     causal term, the window still applies ([EXT] "Apply custom mask",
+ *     "IS_CAUSAL and not USE_CUSTOM_MASK");
+ *   sink: a logit per query head that adds exp(sink - m) to the softmax
+ *     denominator and nothing to o ([EXT] "Handle sink tokens"):
+ *       l = sum_{vis} exp(s_j - m) + exp(sink - m), lse = m + log(l)
+ *     (m is any reference point; here the max over the visible s_j and
+ *     the sink).
  */
 #include <math.h>
 #include <stdint.h>
@@ -73,11 +84,14 @@ static void attend_one_query(const uint16_t *q, int lq, int lv, long n_keys,
                              const uint16_t *const *krow,
                              const uint16_t *const *vrow, long qpos,
                              long window, double sm_scale, double logit_cap,
+                             const uint8_t *mask_row, const double *sink,
                              double *s, double *o, double *lse)
 {
     double m = -INFINITY;
     for (long j = 0; j < n_keys; ++j) {
         int visible = (j <= qpos) && (window <= 0 || qpos - j <= window);
+        if (mask_row)
+            visible = (mask_row[j] != 0) && (window <= 0 || qpos - j <= window);
         if (!visible) {
             s[j] = -INFINITY;
             continue;
@@ -92,6 +106,8 @@ static void attend_one_query(const uint16_t *q, int lq, int lv, long n_keys,
         if (sj > m)
             m = sj;
     }
+    if (sink && *sink > m)
+        m = *sink;
     for (int d = 0; d < lv; ++d)
         o[d] = 0.0;
     if (m == -INFINITY) {
@@ -107,6 +123,8 @@ static void attend_one_query(const uint16_t *q, int lq, int lv, long n_keys,
         for (int d = 0; d < lv; ++d)
             o[d] += p * bf16_to_double(vrow[j][d]);
     }
+    if (sink)
+        l += exp(*sink - m);
     for (int d = 0; d < lv; ++d)
         o[d] /= l;
     *lse = m + log(l);
@@ -147,10 +165,11 @@ int oracle_extend_attention(
     long v_buf_ss, long v_buf_hs, const int32_t *qo_indptr,
     const int32_t *kv_indptr, const int32_t *kv_indices, int batch, int hq,
     int hkv, int lq, int lv, double sm_scale, double logit_cap,
-    long sliding_window, const int64_t *rows, long n_rows, double *o_out,
+    long sliding_window, const uint8_t *custom_mask, const int32_t *mask_indptr,
+    const double *sinks, const int64_t *rows, long n_rows, double *o_out,
     double *lse_out)
 {
-    if (batch < 0 || hkv <= 0 || hq % hkv != 0)
+    if (batch < 0 || hkv <= 0 || hq % hkv != 0 || (custom_mask && !mask_indptr))
         return -1;
     int group = hq / hkv; /* [EXT] kv_group_num: q heads per kv head */
     long n_tokens = batch > 0 ? qo_indptr[batch] : 0;
@@ -187,9 +206,12 @@ int oracle_extend_attention(
             vrow[p_len + e] = v_ext + te * v_ext_ts + (long)hk * v_ext_hs;
         }
         long i = t - qo_indptr[b];
+        const uint8_t *mask_row =
+            custom_mask ? custom_mask + mask_indptr[b] + i * n_keys : NULL;
         attend_one_query(q_extend + (t * hq + h) * (long)lq, lq, lv, n_keys,
                          krow, vrow, p_len + i, sliding_window, sm_scale,
-                         logit_cap, s, o_out + r * (long)lv, lse_out + r);
+                         logit_cap, mask_row, sinks ? sinks + h : NULL, s,
+                         o_out + r * (long)lv, lse_out + r);
         free(krow);
         free(vrow);
         free(s);
@@ -212,10 +234,11 @@ int oracle_extend_attention_unified(
     const int32_t *qo_indptr, const int32_t *kv_indptr,
     const int64_t *kv_indices, const int32_t *prefix_lens, int batch, int hq,
     int hkv, int lq, int lv, double sm_scale, double logit_cap,
-    long sliding_window, const int64_t *rows, long n_rows, double *o_out,
+    long sliding_window, const uint8_t *custom_mask, const int32_t *mask_indptr,
+    const double *sinks, const int64_t *rows, long n_rows, double *o_out,
     double *lse_out)
 {
-    if (batch < 0 || hkv <= 0 || hq % hkv != 0)
+    if (batch < 0 || hkv <= 0 || hq % hkv != 0 || (custom_mask && !mask_indptr))
         return -1;
     int group = hq / hkv;
     long n_tokens = batch > 0 ? qo_indptr[batch] : 0;
@@ -243,10 +266,12 @@ int oracle_extend_attention_unified(
             vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;
         }
         long i = t - qo_indptr[b];
+        const uint8_t *mask_row =
+            custom_mask ? custom_mask + mask_indptr[b] + i * n_keys : NULL;
         attend_one_query(q + (t * hq + h) * (long)lq, lq, lv, n_keys, krow,
                          vrow, (long)prefix_lens[b] + i, sliding_window,
-                         sm_scale, logit_cap, s, o_out + r * (long)lv,
-                         lse_out + r);
+                         sm_scale, logit_cap, mask_row, sinks ? sinks + h : NULL,
+                         s, o_out + r * (long)lv, lse_out + r);
         free(krow);
         free(vrow);
         free(s);
@@ -292,8 +317,8 @@ int oracle_decode_attention(const uint16_t *q, const uint16_t *k_buf,
             vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;
         }
         attend_one_query(q + r * (long)lq, lq, lv, n_keys, krow, vrow,
-                         n_keys - 1, sliding_window, sm_scale, logit_cap, s,
-                         o_out + r * (long)lv, lse_out + r);
+                         n_keys - 1, sliding_window, sm_scale, logit_cap, NULL,
+                         NULL, s, o_out + r * (long)lv, lse_out + r);
         free(krow);
         free(vrow);
         free(s);

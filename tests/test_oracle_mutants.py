@@ -43,6 +43,12 @@ MUTANTS = [
      "wb * bf16_to_double(v_a[r * dv + d]) +\n                                wa * bf16_to_double(v_b[r * dv + d]);", None),
     ("unified_extend_start_ignored", "extend_kv_indices[extend_start_loc[b] + e]", "extend_kv_indices[unified_kv_indptr[b] - prefix_kv_indptr[b] + e]", None),
     ("unified_indptr_drops_extend", "+ prefix_lens[b] + extend_seq_lens[b];", "+ prefix_lens[b];\n        unified_kv_indptr[b + 1] += extend_seq_lens[b] * (b > 0);", None),
+    ("mask_ignored", "        if (mask_row)\n            visible = (mask_row[j] != 0) && (window <= 0 || qpos - j <= window);\n", "", None),
+    ("mask_keeps_causal", "visible = (mask_row[j] != 0) && (window", "visible = (mask_row[j] != 0) && (j <= qpos) && (window", None),
+    ("mask_row_stride", "custom_mask + mask_indptr[b] + i * n_keys : NULL;", "custom_mask + mask_indptr[b] + i : NULL;", None),
+    ("sink_dropped", "    if (sink)\n        l += exp(*sink - m);\n", "", None),
+    ("sink_sign", "l += exp(*sink - m);", "l += exp(m - *sink);", None),
+    ("sink_in_values", "    if (sink)\n        l += exp(*sink - m);\n", "    if (sink) {\n        l += exp(*sink - m);\n        for (int d = 0; d < lv; ++d) o[d] += exp(*sink - m);\n    }\n", None),
 ]
 
 # The pins, cheapest first; a mutant is caught by the first one that fails.
@@ -62,6 +68,10 @@ BATTERY = [
     lambda: pins.test_two_stage_equals_unified(),
     lambda: pins.test_unified_indices_are_per_sequence_concatenation(0),
     lambda: pins.test_merge_of_two_key_halves_equals_attention_over_all(),
+    lambda: pins.test_custom_mask_matches_dense_formulation(0.0, -1, 1),
+    lambda: pins.test_causal_pattern_mask_equals_no_mask(),
+    lambda: pins.test_sinks_match_an_extra_zero_valued_key(-1),
+    lambda: pins.test_sink_with_one_visible_key_closed_form(),
 ]
 
 

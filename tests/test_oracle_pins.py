@@ -36,10 +36,14 @@ def _run_oracle(wl, cap=None, window=None, rows=None):
         s.sliding_window if window is None else window, rows=rows)
 
 
-def _dense_reference(wl, cap, window):
+def _dense_reference(wl, cap, window, masks=None, sinks=None):
     """Second formulation with library primitives: per sequence, the full
     [E, T] score matrix by matmul, tanh cap, a boolean mask from explicit
-    position tables, softmax and matmul.  Returns (o, lse) float64."""
+    position tables, softmax and matmul.  Returns (o, lse) float64.
+
+    masks: per sequence a bool [E, T] that replaces the causal table (the
+    window still applies).  sinks [Hq]: an extra key per row whose score is
+    the head's sink and whose value vector is zero."""
     s = wl.spec
     g = s.hq // s.hkv
     outs, lses = [], []
@@ -58,10 +62,14 @@ def _dense_reference(wl, cap, window):
             sc = cap * torch.tanh(sc / cap)
         qpos = torch.arange(E).view(E, 1) + wl.prefix_lens[b]
         kpos = torch.arange(T).view(1, T)
-        vis = kpos <= qpos
+        vis = kpos <= qpos if masks is None else masks[b].bool()
         if window > 0:
             vis = vis & (qpos - kpos <= window)
         sc = sc.masked_fill(~vis.unsqueeze(0), float("-inf"))
+        if sinks is not None:
+            extra = torch.as_tensor(sinks, dtype=torch.float64).view(-1, 1, 1).expand(-1, E, 1)
+            sc = torch.cat([sc, extra], dim=-1)                          # [Hq,E,T+1]
+            v = torch.cat([v, torch.zeros(1, v.shape[1], v.shape[2], dtype=v.dtype)])
         lse = torch.logsumexp(sc, dim=-1)                                # [Hq,E]
         o = torch.einsum("het,thd->ehd", torch.softmax(sc, dim=-1), v)
         outs.append(o)
@@ -477,3 +485,118 @@ def test_default_scale_is_inverse_sqrt_lq():
     o0, _ = oracle.extend_attention(*args, 0.0)
     o1, _ = oracle.extend_attention(*args, 1.0 / 8.0)
     assert torch.equal(o0, o1)
+
+
+# --------------------------------------------- custom mask and attention sinks
+def _random_masks(wl, seed, density=0.4):
+    """Per sequence a random bool [E, T] (each row also sees its own key),
+    and the flat uint8 layout with per-sequence offsets: row i of sequence b
+    at mask_indptr[b] + i * T_b."""
+    g = torch.Generator().manual_seed(seed)
+    masks, flat, indptr = [], [], [0]
+    for b in range(wl.batch):
+        E, P = wl.extend_lens[b], wl.prefix_lens[b]
+        T = P + E
+        m = torch.rand(E, T, generator=g) < density
+        m[torch.arange(E), P + torch.arange(E)] = True
+        masks.append(m)
+        flat.append(m.to(torch.uint8).reshape(-1))
+        indptr.append(indptr[-1] + E * T)
+    return masks, torch.cat(flat), torch.tensor(indptr, dtype=torch.int32)
+
+
+def _run_masked(wl, masks_flat=None, mask_indptr=None, sinks=None, cap=None, window=None):
+    k_ext, v_ext = wl.extend_kv()
+    kb, vb = wl.pool()
+    s = wl.spec
+    return oracle.extend_attention(
+        wl.q, k_ext, v_ext, kb, vb, wl.qo_indptr, wl.kv_indptr, wl.kv_indices,
+        wl.sm_scale, s.logit_cap if cap is None else cap,
+        s.sliding_window if window is None else window,
+        custom_mask=masks_flat, mask_indptr=mask_indptr, sinks=sinks)
+
+
+@pytest.mark.parametrize("cap,window,seed", [(0.0, -1, 1), (15.0, -1, 2), (0.0, 9, 3)])
+def test_custom_mask_matches_dense_formulation(cap, window, seed):
+    """A custom mask replaces the causal mask and keeps the window (sglang
+    extend_attention.py, _fwd_kernel_unified: "Apply custom mask", causal
+    only when not USE_CUSTOM_MASK): brute-force dense formulation."""
+    wl = W.draw(_spec(batch=3, hq=6, hkv=2, lq=64, lv=32, prefix=[0, 21, 7],
+                      extend=[11, 6, 30], seed=seed, std=2.0))
+    masks, flat, indptr = _random_masks(wl, seed)
+    o, lse = _run_masked(wl, flat, indptr, cap=cap, window=window)
+    ro, rl = _dense_reference(wl, cap, window, masks=masks)
+    torch.testing.assert_close(o, ro, rtol=0, atol=TOL)
+    torch.testing.assert_close(lse, rl, rtol=0, atol=TOL)
+
+
+def test_causal_pattern_mask_equals_no_mask():
+    """A mask that spells out the causal pattern gives the unmasked result."""
+    wl = W.draw(_spec(batch=2, hq=4, hkv=2, lq=64, lv=64, prefix=[5, 40], extend=[9, 17], seed=4))
+    flat, indptr = [], [0]
+    for b in range(wl.batch):
+        E, P = wl.extend_lens[b], wl.prefix_lens[b]
+        m = torch.arange(P + E).view(1, -1) <= (P + torch.arange(E)).view(-1, 1)
+        flat.append(m.to(torch.uint8).reshape(-1))
+        indptr.append(indptr[-1] + E * (P + E))
+    o, lse = _run_masked(wl, torch.cat(flat), torch.tensor(indptr, dtype=torch.int32))
+    ro, rl = _run_oracle(wl)
+    torch.testing.assert_close(o, ro, rtol=0, atol=TOL)
+    torch.testing.assert_close(lse, rl, rtol=0, atol=TOL)
+
+
+def test_all_ones_mask_is_non_causal_sdpa():
+    """An all-ones mask on a sequence without prefix is plain non-causal
+    attention: torch's scaled_dot_product_attention(is_causal=False)."""
+    wl = W.draw(_spec(batch=1, hq=4, hkv=2, lq=64, lv=64, prefix=[0], extend=[23], seed=12))
+    E = wl.extend_lens[0]
+    flat = torch.ones(E * E, dtype=torch.uint8)
+    o, _ = _run_masked(wl, flat, torch.tensor([0, E * E], dtype=torch.int32))
+    q = wl.q.double().transpose(0, 1)                                   # [Hq,E,D]
+    k = wl.k_rows[:E].double().repeat_interleave(2, dim=1).transpose(0, 1)
+    v = wl.v_rows[:E].double().repeat_interleave(2, dim=1).transpose(0, 1)
+    ref = F.scaled_dot_product_attention(q, k, v, is_causal=False, scale=wl.sm_scale)
+    torch.testing.assert_close(o, ref.transpose(0, 1), rtol=0, atol=TOL)
+
+
+@pytest.mark.parametrize("window", [-1, 7])
+def test_sinks_match_an_extra_zero_valued_key(window):
+    """A sink logit per head adds exp(sink - m) to the denominator only
+    (sglang extend_attention.py, "Handle sink tokens"): the same as one more
+    key per row whose score is the sink and whose value vector is zero."""
+    wl = W.draw(_spec(batch=3, hq=6, hkv=3, lq=64, lv=32, prefix=[0, 12, 50],
+                      extend=[8, 15, 4], seed=17, std=1.5))
+    sinks = torch.tensor([-1.0, 0.5, 2.0, 4.0, -3.0, 1.25], dtype=torch.float64)
+    o, lse = _run_masked(wl, sinks=sinks, window=window)
+    ro, rl = _dense_reference(wl, 0.0, window, sinks=sinks)
+    torch.testing.assert_close(o, ro, rtol=0, atol=TOL)
+    torch.testing.assert_close(lse, rl, rtol=0, atol=TOL)
+
+
+def test_sink_with_one_visible_key_closed_form():
+    """Window 0 leaves each row its own key only: o = v_self * e^s / (e^s +
+    e^sink), lse = log(e^s + e^sink)."""
+    wl = W.draw(_spec(batch=1, hq=2, hkv=1, lq=64, lv=64, prefix=[3], extend=[5], seed=6))
+    sinks = torch.tensor([0.7, -0.4], dtype=torch.float64)
+    # window 0 is "off"; a window of 1e-9 is not an integer: use the mask
+    E, P = 5, 3
+    m = torch.zeros(E, P + E, dtype=torch.bool)
+    m[torch.arange(E), P + torch.arange(E)] = True
+    o, lse = _run_masked(wl, m.to(torch.uint8).reshape(-1),
+                         torch.tensor([0, E * (P + E)], dtype=torch.int32), sinks=sinks)
+    for i in range(E):
+        for h in range(2):
+            k = wl.k_rows[P + i, 0].double()
+            v = wl.v_rows[P + i, 0].double()
+            sc = float(wl.sm_scale * (wl.q[i, h].double() * k).sum())
+            w = math.exp(sc) / (math.exp(sc) + math.exp(float(sinks[h])))
+            torch.testing.assert_close(o[i, h], v * w, rtol=0, atol=1e-12)
+            assert abs(float(lse[i, h]) - math.log(math.exp(sc) + math.exp(float(sinks[h])))) < 1e-12
+
+
+def test_very_negative_sinks_change_nothing():
+    wl = W.draw(_spec(batch=2, hq=4, hkv=2, lq=64, lv=64, prefix=[10, 0], extend=[6, 9], seed=9))
+    o, lse = _run_masked(wl, sinks=torch.full((4,), -1e4, dtype=torch.float64))
+    ro, rl = _run_oracle(wl)
+    torch.testing.assert_close(o, ro, rtol=0, atol=TOL)
+    torch.testing.assert_close(lse, rl, rtol=0, atol=TOL)
