@@ -103,6 +103,12 @@ void pkx_set_attention_events(void *before, void *after);
  *   logit_cap > 0; key j is visible iff j <= P_b + i and, if
  *   sliding_window > 0, (P_b + i) - j <= sliding_window;
  *   o = softmax over visible keys of s, applied to v;  lse = log sum exp s.
+ * With a custom mask (speculative tree verification, _fwd_kernel_unified
+ * "Apply custom mask"), key j is visible iff
+ * custom_mask[mask_indptr[b] + i * T_b + j] != 0 (T_b = P_b + E_b keys of
+ * the sequence) and the window holds: the mask replaces the causal term.
+ * With sinks (_fwd_kernel_unified "Handle sink tokens"), each row's softmax
+ * denominator gains exp(sinks[h] - m): o is scaled down, lse includes it.
  *
  *   q_extend   bf16 [num_q_tokens, hq, lq] contiguous
  *   k_extend   bf16 row (t, h) at k_extend + t*ke_st + h*ke_sh, lq elements
@@ -118,10 +124,16 @@ void pkx_set_attention_events(void *before, void *after);
  *   sm_scale   <= 0 selects 1/sqrt(lq)
  *   logit_cap  <= 0: no cap
  *   sliding_window <= 0: no window
+ *   custom_mask nullable uint8, one byte per (extend row, key) of every
+ *              sequence, sequence b's rows at mask_indptr[b]
+ *   mask_indptr int32 [batch+1] element offsets into custom_mask (needed
+ *              with a mask; NULL otherwise)
+ *   sinks      nullable fp32 [hq] sink logit per query head
  *   lse_out    nullable fp32 [num_q_tokens, hq] (natural log)
  *   workspace  >= pkx_extend_workspace_size(...) bytes
  * Supported (lq, lv): (64, 64), (128, 128), (576, 512); hq % hkv == 0 and
- * hq / hkv <= 128.
+ * hq / hkv <= 128.  custom_mask and sinks: (64, 64) and (128, 128) only
+ * (PKX_EUNSUPPORTED for the MLA shape).
  */
 int pkx_extend_attention_fwd(
     const void *q_extend, const void *k_extend, const void *v_extend,
@@ -131,6 +143,7 @@ int pkx_extend_attention_fwd(
     int lq, int lv, int64_t ke_st, int64_t ke_sh, int64_t ve_st,
     int64_t ve_sh, int64_t kb_ss, int64_t kb_sh, int64_t vb_ss, int64_t vb_sh,
     int64_t num_slots, float sm_scale, float logit_cap, int sliding_window,
+    const uint8_t *custom_mask, const int32_t *mask_indptr, const float *sinks,
     float *lse_out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -153,8 +166,9 @@ int pkx_extend_attention_fwd_unified(
     const int64_t *kv_indices, const int32_t *prefix_lens, int batch,
     int num_q_tokens, int hq, int hkv, int lq, int lv, int64_t kb_ss,
     int64_t kb_sh, int64_t vb_ss, int64_t vb_sh, int64_t num_slots,
-    float sm_scale, float logit_cap, int sliding_window, float *lse_out,
-    void *workspace, size_t workspace_bytes, void *stream);
+    float sm_scale, float logit_cap, int sliding_window,
+    const uint8_t *custom_mask, const int32_t *mask_indptr, const float *sinks,
+    float *lse_out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Decode attention.

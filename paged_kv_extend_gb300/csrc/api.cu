@@ -48,6 +48,18 @@ static int check_rows(const char *name, const void *p, int64_t s0, int64_t s1) {
   return PKX_OK;
 }
 
+// A custom mask needs its offsets; mask and sinks are built for the GQA
+// head dims only.
+static int check_mask_sinks(int lq, const uint8_t *custom_mask, const int32_t *mask_indptr,
+                            const float *sinks) {
+  if (custom_mask && (!mask_indptr || !aligned(mask_indptr, 4)))
+    return set_error(PKX_EINVAL, "custom_mask needs an aligned int32 mask_indptr");
+  if (sinks && !aligned(sinks, 4)) return set_error(PKX_EINVAL, "sinks misaligned");
+  if ((custom_mask || sinks) && lq == 576)
+    return set_error(PKX_EUNSUPPORTED, "custom_mask / sinks are not built for the MLA shape");
+  return PKX_OK;
+}
+
 static int check_scalars(float sm_scale, float logit_cap) {
   if (!std::isfinite(sm_scale) || !std::isfinite(logit_cap))
     return set_error(PKX_EINVAL, "sm_scale and logit_cap must be finite");
@@ -105,12 +117,14 @@ int pkx_extend_attention_fwd(const void *q_extend, const void *k_extend, const v
                              int hkv, int lq, int lv, int64_t ke_st, int64_t ke_sh,
                              int64_t ve_st, int64_t ve_sh, int64_t kb_ss, int64_t kb_sh,
                              int64_t vb_ss, int64_t vb_sh, int64_t num_slots, float sm_scale,
-                             float logit_cap, int sliding_window, float *lse_out,
+                             float logit_cap, int sliding_window, const uint8_t *custom_mask,
+                             const int32_t *mask_indptr, const float *sinks, float *lse_out,
                              void *workspace, size_t workspace_bytes, void *stream) {
   int rc;
   if (batch < 0 || num_q_tokens < 0) return set_error(PKX_EINVAL, "negative batch or token count");
   if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
   if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
+  if ((rc = check_mask_sinks(lq, custom_mask, mask_indptr, sinks))) return rc;
   if (batch == 0 || num_q_tokens == 0) return PKX_OK;
   if ((rc = check_rows("q_extend", q_extend, 8, 8))) return rc;
   if ((rc = check_rows("o_extend", o_extend, 8, 8))) return rc;
@@ -141,6 +155,7 @@ int pkx_extend_attention_fwd(const void *q_extend, const void *k_extend, const v
   a.kv_indices = kv_indices;
   a.batch = batch; a.num_q_tokens = num_q_tokens; a.hq = hq; a.hkv = hkv; a.lq = lq; a.lv = lv;
   a.sm_scale = sm_scale; a.logit_cap = logit_cap; a.window = sliding_window;
+  a.custom_mask = custom_mask; a.mask_indptr = mask_indptr; a.sinks = sinks;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   return launch_attention(a);
@@ -153,12 +168,15 @@ int pkx_extend_attention_fwd_unified(const void *q, void *o, const void *k_buffe
                                      int hq, int hkv, int lq, int lv, int64_t kb_ss,
                                      int64_t kb_sh, int64_t vb_ss, int64_t vb_sh,
                                      int64_t num_slots, float sm_scale, float logit_cap,
-                                     int sliding_window, float *lse_out, void *workspace,
-                                     size_t workspace_bytes, void *stream) {
+                                     int sliding_window, const uint8_t *custom_mask,
+                                     const int32_t *mask_indptr, const float *sinks,
+                                     float *lse_out, void *workspace, size_t workspace_bytes,
+                                     void *stream) {
   int rc;
   if (batch < 0 || num_q_tokens < 0) return set_error(PKX_EINVAL, "negative batch or token count");
   if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
   if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
+  if ((rc = check_mask_sinks(lq, custom_mask, mask_indptr, sinks))) return rc;
   if (batch == 0 || num_q_tokens == 0) return PKX_OK;
   if ((rc = check_rows("q", q, 8, 8))) return rc;
   if ((rc = check_rows("o", o, 8, 8))) return rc;
@@ -185,6 +203,7 @@ int pkx_extend_attention_fwd_unified(const void *q, void *o, const void *k_buffe
   a.kv_indices = kv_indices;
   a.batch = batch; a.num_q_tokens = num_q_tokens; a.hq = hq; a.hkv = hkv; a.lq = lq; a.lv = lv;
   a.sm_scale = sm_scale; a.logit_cap = logit_cap; a.window = sliding_window;
+  a.custom_mask = custom_mask; a.mask_indptr = mask_indptr; a.sinks = sinks;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   return launch_attention(a);

@@ -58,6 +58,7 @@ struct SchedParams {
   int batch, hkv, tok, window, num_q_tokens;
   int bn;        // keys per K/V tile
   int q_tile_tok;  // query tokens of one Q tile
+  int no_causal;   // a custom mask replaces the causal mask: blocks see every key
   int n_dsplit;  // units per (block, split): value-dim slices (1, or 4 for MLA)
   int unit_target, qb_max, unit_max, comb_max, slot_max;
   int32_t *seq;  // 8 arrays of batch+1 ints
@@ -119,7 +120,7 @@ __device__ __forceinline__ void qblock_range(const SchedParams &p, const SeqDims
   i0 = qb * p.tok;
   i1 = min(d.E, i0 + p.tok);
   const int qmin = d.P + i0, qmax = d.P + i1 - 1;
-  hi = min(qmax + 1, d.T);
+  hi = p.no_causal ? d.T : min(qmax + 1, d.T);
   lo = p.window > 0 ? max(0, qmin - p.window) : 0;
   if (hi < lo) hi = lo;
 }
@@ -379,6 +380,10 @@ struct KParams {
   float scale_log2;  // sm_scale * log2(e)           (no cap)
   float cap_pre;     // sm_scale / cap                (cap)
   float cap_log2;    // cap * log2(e)                 (cap)
+  const uint8_t *custom_mask;   // nullable: byte per (extend row, key); replaces causal
+  const int32_t *mask_indptr;   // [batch+1] offsets of each sequence's mask rows
+  const float *sinks;           // nullable [hq] sink logits (natural log)
+  const int32_t *prefix_lens;   // unified form: prefix length per sequence
   const WorkUnit *units;
   const int32_t *uorder;  // units by cost, largest first
   const WsHeader *hdr;
@@ -579,6 +584,16 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       const int qmin = w.qpos0 + tok0, qmax = w.qpos0 + tok0 + n_tok_i - 1;
       const int64_t orow_idx = (int64_t)(w.q_tok0 + t) * p.hq + w.kvh * G + g;
       const int64_t prow_idx = (int64_t)w.slot * p.rows_per_slot + tok0 * G + r;
+      // custom mask row of this query: byte per key of the sequence
+      const uint8_t *mrow = nullptr;
+      if (p.custom_mask && valid) {
+        const int qo0 = p.qo_indptr[w.b];
+        const int64_t n_keys = MODE == kTwoStage
+                                   ? (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]) +
+                                         (p.qo_indptr[w.b + 1] - qo0)
+                                   : (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]);
+        mrow = p.custom_mask + p.mask_indptr[w.b] + (int64_t)(w.q_tok0 + t - qo0) * n_keys;
+      }
       if (nt == 0) {
         if (valid) {
           if (w.slot < 0) {
@@ -631,9 +646,19 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             for (int i = 0; i < C::BN; ++i) x[i] = p.cap_log2 * tanh_approx(x[i] * p.cap_pre);
             sc = 1.0f;
           }
-          const bool need_mask = (ke - 1 > qmin) || (ke - kb < C::BN) ||
+          const bool need_mask = p.custom_mask || (ke - 1 > qmin) || (ke - kb < C::BN) ||
                                  (p.window > 0 && kb < qmax - p.window);
-          if (need_mask) {
+          if (p.custom_mask) {
+            // the custom mask replaces the causal term; the window stays
+#pragma unroll
+            for (int i = 0; i < C::BN; ++i) {
+              const int kpos = kb + i;
+              bool vis = mrow && kpos < ke && (p.window <= 0 || qpos - kpos <= p.window);
+              if (vis) vis = __ldg(mrow + kpos) != 0;
+              x[i] = vis ? x[i] * sc : -INFINITY;
+            }
+            sc = 1.0f;
+          } else if (need_mask) {
 #pragma unroll
             for (int i = 0; i < C::BN; ++i) {
               const int kpos = kb + i;
@@ -731,8 +756,18 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       ++o_cnt;
       tc_fence_after();
       if (warp_active) {
-        const float inv = l > 0.f ? 1.0f / l : 0.f;
-        const float lse_v = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        float inv = l > 0.f ? 1.0f / l : 0.f;
+        float lse_v = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (p.sinks && w.slot < 0) {
+          // the head's sink joins the denominator (a split row gets it in
+          // the combine): with M = max(m, sink), l' = l 2^(m-M) + 2^(sink-M)
+          const float s2 = __ldg(p.sinks + w.kvh * G + g) * 1.4426950408889634f;
+          const float M = fmaxf(m, s2);
+          const float a_m = m == -INFINITY ? 0.f : ex2_approx(m - M);
+          const float lt = l * a_m + ex2_approx(s2 - M);
+          inv = a_m / lt;
+          lse_v = (M + __log2f(lt)) * 0.69314718055994531f;
+        }
         uint32_t v[32];
 #pragma unroll
         for (int c = 0; c < C::HDV / 32; ++c) {
@@ -1090,8 +1125,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
 // (the merge_state formula applied n ways).
 __global__ void __launch_bounds__(256) combine_kernel(const WsHeader *hdr, const CombineEntry *ce,
                                                       const float *plse, const float *po,
-                                                      bf16 *o, float *lse, int hq, int group,
-                                                      int hdv, int rows_per_slot) {
+                                                      bf16 *o, float *lse, const float *sinks,
+                                                      int hq, int group, int hdv,
+                                                      int rows_per_slot) {
   const int n_comb = hdr->n_combine;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -1105,13 +1141,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const WsHeader *hdr, const
       mx = fmaxf(mx, plse[(int64_t)(E.slot0 + i) * rows_per_slot + r]);
     const int t = r / group, g = r - t * group;
     const int64_t orow = (int64_t)(E.q_tok0 + t) * hq + E.kvh * group + g;
-    if (mx == -INFINITY) {
+    // a sink (natural-log logit of the head) joins the denominator once
+    const float sink = sinks ? __ldg(sinks + E.kvh * group + g) : -INFINITY;
+    const float mx_p = mx;
+    mx = fmaxf(mx, sink);
+    if (mx_p == -INFINITY) {
       for (int c = lane * 8; c < hdv; c += 256)
         *reinterpret_cast<uint4 *>(o + orow * hdv + c) = make_uint4(0, 0, 0, 0);
-      if (lane == 0 && lse) lse[orow] = -INFINITY;
+      if (lane == 0 && lse) lse[orow] = sink;  // -inf without a sink
       continue;
     }
-    float wsum = 0.f;
+    float wsum = sinks ? exp2f((sink - mx) * 1.4426950408889634f) : 0.f;
     for (int i = 0; i < E.n_split; ++i)
       wsum += exp2f((plse[(int64_t)(E.slot0 + i) * rows_per_slot + r] - mx) * 1.4426950408889634f);
     const float inv = 1.0f / wsum;
@@ -1291,6 +1331,7 @@ int launch_attention(const AttnArgs &a) {
   sp.tok = (mla ? 1 : 2) * tok;
   sp.bn = mla ? MlaCfg<0>::BN : kBlockN;
   sp.q_tile_tok = tok > 0 ? tok : 1;
+  sp.no_causal = a.custom_mask != nullptr;
   sp.n_dsplit = mla ? MlaCfg<0>::LV / MlaCfg<0>::DVS : 1;
   sp.window = a.window;
   sp.num_q_tokens = nq;
@@ -1339,6 +1380,10 @@ int launch_attention(const AttnArgs &a) {
   kp.scale_log2 = sm_scale * log2e;
   kp.cap_pre = kp.use_cap ? sm_scale / a.logit_cap : 0.f;
   kp.cap_log2 = kp.use_cap ? a.logit_cap * log2e : 0.f;
+  kp.custom_mask = a.custom_mask;
+  kp.mask_indptr = a.mask_indptr;
+  kp.sinks = a.sinks;
+  kp.prefix_lens = a.prefix_lens;
   kp.units = sp.units;
   kp.uorder = sp.uorder;
   kp.next_unit = &hdr->next_unit;
@@ -1368,8 +1413,8 @@ int launch_attention(const AttnArgs &a) {
   }
   if (rc != PKX_OK) return rc;
   if (ev_after) cudaEventRecord(ev_after, a.stream);
-  combine_kernel<<<nsm * 2, 256, 0, a.stream>>>(hdr, sp.comb, kp.plse, kp.po, kp.o, a.lse, a.hq,
-                                               group, a.lv, L.rows_per_slot);
+  combine_kernel<<<nsm * 2, 256, 0, a.stream>>>(hdr, sp.comb, kp.plse, kp.po, kp.o, a.lse,
+                                               a.sinks, a.hq, group, a.lv, L.rows_per_slot);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(PKX_ECUDA, "attention launch: %s", cudaGetErrorString(e));
   return PKX_OK;

@@ -102,6 +102,9 @@ struct AttnArgs {
   int batch, num_q_tokens, hq, hkv, lq, lv;
   float sm_scale, logit_cap;
   int window;
+  const uint8_t *custom_mask;   // nullable: replaces the causal mask
+  const int32_t *mask_indptr;   // [batch+1] offsets into custom_mask
+  const float *sinks;           // nullable [hq] sink logits
   void *workspace;
   size_t workspace_bytes;
   cudaStream_t stream;

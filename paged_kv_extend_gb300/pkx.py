@@ -48,10 +48,11 @@ _SIGS = {
     "pkx_set_attention_events": (None, [_p, _p]),
     "pkx_extend_attention_fwd": (_i, [
         _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
-        _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _sz, _p]),
+        _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _p,
+        _p, _p, _sz, _p]),
     "pkx_extend_attention_fwd_unified": (_i, [
         _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
-        _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _sz, _p]),
+        _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _p, _p, _p, _sz, _p]),
     "pkx_decode_attention_fwd": (_i, [
         _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i,
         _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _sz, _p]),
@@ -110,6 +111,23 @@ def _i32(t: torch.Tensor, name: str):
     return t
 
 
+def _mask_sinks(custom_mask, mask_indptr, sinks):
+    """Check the optional custom mask (uint8, with int32 offsets) and sinks
+    (fp32, one per query head) and return their pointers."""
+    if custom_mask is not None:
+        if custom_mask.dtype not in (torch.uint8, torch.bool) or not custom_mask.is_cuda or \
+                not custom_mask.is_contiguous():
+            raise ValueError("custom_mask must be a contiguous CUDA uint8/bool tensor")
+        if mask_indptr is None:
+            raise ValueError("custom_mask needs mask_indptr")
+        _i32(mask_indptr, "mask_indptr")
+    if sinks is not None and (sinks.dtype != torch.float32 or not sinks.is_cuda or
+                              not sinks.is_contiguous()):
+        raise ValueError("sinks must be a contiguous CUDA float32 tensor")
+    return (_ptr(custom_mask), _ptr(mask_indptr) if custom_mask is not None else None,
+            _ptr(sinks))
+
+
 def version() -> str:
     return load_library().pkx_version().decode()
 
@@ -147,9 +165,11 @@ def _workspace(ws, nbytes, dev):
 
 def extend_attention_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffer,
                          qo_indptr, kv_indptr, kv_indices, sm_scale=None, logit_cap=0.0,
-                         sliding_window=-1, lse=None, workspace=None):
+                         sliding_window=-1, lse=None, workspace=None, custom_mask=None,
+                         mask_indptr=None, sinks=None):
     """Two-stage extend attention (pkx_extend_attention_fwd); writes o_extend
-    (and lse if given) in place.  Returns the workspace used."""
+    (and lse if given) in place.  Returns the workspace used.  custom_mask /
+    mask_indptr / sinks as in the C header."""
     lib = load_library()
     n, hq, lq = q_extend.shape
     hkv = k_buffer.shape[1]
@@ -169,14 +189,16 @@ def extend_attention_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buf
         _ptr(v_buffer), _ptr(qo_indptr), _ptr(kv_indptr),
         _ptr(kv_indices) if kv_indices.numel() else None, batch, n, hq, hkv, lq, lv,
         ke[0], ke[1], ve[0], ve[1], kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0],
-        float(sm_scale or 0.0), float(logit_cap or 0.0), int(sliding_window), _ptr(lse),
+        float(sm_scale or 0.0), float(logit_cap or 0.0), int(sliding_window),
+        *_mask_sinks(custom_mask, mask_indptr, sinks), _ptr(lse),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(q_extend.device)))
     return ws
 
 
 def extend_attention_fwd_unified(q, o, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices,
                                  prefix_lens, sm_scale=None, logit_cap=0.0, sliding_window=-1,
-                                 lse=None, workspace=None):
+                                 lse=None, workspace=None, custom_mask=None, mask_indptr=None,
+                                 sinks=None):
     """Unified extend attention (pkx_extend_attention_fwd_unified); int64
     kv_indices over every key.  Writes o (and lse) in place."""
     lib = load_library()
@@ -194,7 +216,8 @@ def extend_attention_fwd_unified(q, o, k_buffer, v_buffer, qo_indptr, kv_indptr,
         _ptr(q), _ptr(o), _ptr(k_buffer), _ptr(v_buffer), _ptr(qo_indptr), _ptr(kv_indptr),
         _ptr(kv_indices) if kv_indices.numel() else None, _ptr(prefix_lens), batch, n, hq, hkv,
         lq, lv, kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0], float(sm_scale or 0.0),
-        float(logit_cap or 0.0), int(sliding_window), _ptr(lse), _ptr(ws),
+        float(logit_cap or 0.0), int(sliding_window),
+        *_mask_sinks(custom_mask, mask_indptr, sinks), _ptr(lse), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(q.device)))
     return ws
 

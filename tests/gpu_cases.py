@@ -38,17 +38,17 @@ class DeviceWorkload:
         lse = torch.full((n, s.hq), float("nan"), dtype=torch.float32, device=DEV)
         return o, lse
 
-    def extend(self, cap=None, window=None):
+    def extend(self, cap=None, window=None, **mask_sinks):
         s = self.wl.spec
         o, lse = self.out()
         ws = pkx.extend_attention_fwd(
             self.q, self.k_extend, self.v_extend, o, self.k_buffer, self.v_buffer,
             self.qo_indptr, self.kv_indptr, self.kv_indices, self.wl.sm_scale,
             s.logit_cap if cap is None else cap,
-            s.sliding_window if window is None else window, lse=lse)
+            s.sliding_window if window is None else window, lse=lse, **_dev(mask_sinks))
         return o, lse, ws
 
-    def unified(self, cap=None, window=None, scale=None):
+    def unified(self, cap=None, window=None, scale=None, **mask_sinks):
         s = self.wl.spec
         uptr, uidx, plen = pkx.build_unified_kv_indices(
             self.kv_indptr, self.kv_indices, self.extend_start_loc, self.extend_seq_lens,
@@ -57,7 +57,7 @@ class DeviceWorkload:
         ws = pkx.extend_attention_fwd_unified(
             self.q, o, self.k_buffer, self.v_buffer, self.qo_indptr, uptr, uidx, plen,
             self.wl.sm_scale if scale is None else scale, s.logit_cap if cap is None else cap,
-            s.sliding_window if window is None else window, lse=lse)
+            s.sliding_window if window is None else window, lse=lse, **_dev(mask_sinks))
         return o, lse, ws
 
     def decode(self, cap=None, window=None):
@@ -70,7 +70,18 @@ class DeviceWorkload:
         return o, lse, ws
 
 
-def oracle_extend(wl: W.Workload, cap=None, window=None, rows=None, scale=None):
+def _dev(kw):
+    """custom_mask / mask_indptr / sinks moved to the GPU (sinks as fp32)."""
+    out = {}
+    for k, v in kw.items():
+        if v is None:
+            continue
+        v = v.to(DEV)
+        out[k] = v.float() if k == "sinks" else v
+    return out
+
+
+def oracle_extend(wl: W.Workload, cap=None, window=None, rows=None, scale=None, **mask_sinks):
     s = wl.spec
     k_ext, v_ext = wl.extend_kv()
     kb, vb = wl.pool()
@@ -78,7 +89,8 @@ def oracle_extend(wl: W.Workload, cap=None, window=None, rows=None, scale=None):
         wl.q, k_ext, v_ext, kb, vb, wl.qo_indptr, wl.kv_indptr, wl.kv_indices,
         wl.sm_scale if scale is None else scale,
         s.logit_cap if cap is None else cap, s.sliding_window if window is None else window,
-        rows=rows)
+        rows=rows, **{k: (v.double() if k == "sinks" else v) for k, v in mask_sinks.items()
+                      if v is not None})
 
 
 def oracle_decode(wl: W.Workload, cap=None, window=None):
@@ -112,3 +124,23 @@ def sample_rows(n_tokens, hq, count, seed):
     if total <= count:
         return torch.arange(total, dtype=torch.int64)
     return torch.randperm(total, generator=g)[:count].sort().values
+
+
+def random_masks(wl: W.Workload, seed, density=0.5):
+    """A custom mask for every sequence, flat uint8 with int32 offsets: row i
+    of sequence b (T_b keys) at mask_indptr[b] + i * T_b; prefix keys are
+    visible with probability 0.9, extend keys with ``density``, and every
+    row sees its own key."""
+    g = torch.Generator().manual_seed(seed)
+    flat, indptr = [], [0]
+    for b in range(wl.batch):
+        E, P = wl.extend_lens[b], wl.prefix_lens[b]
+        T = P + E
+        m = torch.rand(E, T, generator=g)
+        thr = torch.full((T,), density)
+        thr[:P] = 0.9
+        m = m < thr
+        m[torch.arange(E), P + torch.arange(E)] = True
+        flat.append(m.to(torch.uint8).reshape(-1))
+        indptr.append(indptr[-1] + E * T)
+    return torch.cat(flat), torch.tensor(indptr, dtype=torch.int32)

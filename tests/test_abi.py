@@ -50,12 +50,14 @@ def test_version(lib):
 def _extend(lib, **over):
     a = dict(q=None, k=None, v=None, o=None, kb=None, vb=None, qo=None, kvp=None, kvi=None,
              batch=1, n=4, hq=8, hkv=2, lq=128, lv=128, st=(1024, 128, 1024, 128, 1024, 128, 1024, 128),
-             slots=16, scale=0.0, cap=0.0, win=-1, lse=None, ws=None, wsb=0, stream=None)
+             slots=16, scale=0.0, cap=0.0, win=-1, mask=None, mask_indptr=None, sinks=None,
+             lse=None, ws=None, wsb=0, stream=None)
     a.update(over)
     return lib.pkx_extend_attention_fwd(
         a["q"], a["k"], a["v"], a["o"], a["kb"], a["vb"], a["qo"], a["kvp"], a["kvi"],
         a["batch"], a["n"], a["hq"], a["hkv"], a["lq"], a["lv"], *a["st"], a["slots"],
-        a["scale"], a["cap"], a["win"], a["lse"], a["ws"], a["wsb"], a["stream"])
+        a["scale"], a["cap"], a["win"], a["mask"], a["mask_indptr"], a["sinks"], a["lse"],
+        a["ws"], a["wsb"], a["stream"])
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -65,6 +67,10 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _extend(lib, hq=256, hkv=1) == pkx.PKX_EUNSUPPORTED
     assert _extend(lib, batch=-1) == pkx.PKX_EINVAL
     assert _extend(lib, scale=float("nan")) == pkx.PKX_EINVAL
+    # a custom mask needs its offsets; mask and sinks are not built for MLA
+    assert _extend(lib, mask=0x1000) == pkx.PKX_EINVAL
+    assert b"mask_indptr" in lib.pkx_last_error_string()
+    assert _extend(lib, lq=576, lv=512, hq=16, hkv=1, sinks=0x1000) == pkx.PKX_EUNSUPPORTED
     # null tensors
     assert _extend(lib) == pkx.PKX_EINVAL
     assert b"null" in lib.pkx_last_error_string()

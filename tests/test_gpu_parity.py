@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     from gpu_cases import (DEV, DeviceWorkload, assert_close, oracle_decode, oracle_extend,
-                           sample_rows)
+                           random_masks, sample_rows)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -184,6 +184,78 @@ def test_extend_scale_values(scale, cap, window):
     assert pkx.workspace_status(ws) == 0
     ro, rl = oracle_extend(wl, scale=scale)
     assert_close(o, lse, ro, rl, f"scale {scale}")
+
+
+# ------------------------------------------ custom mask and attention sinks
+MASK_SINK = [
+    # (lq, hq, hkv, prefix, extend, cap, window, mask, sinks)
+    (128, 32, 8, [0, 40, 300], [17, 64, 130], 0.0, -1, True, False),
+    (128, 32, 8, [900, 5], [70, 200], 0.0, -1, True, False),       # split key ranges
+    (128, 16, 4, [33, 260], [9, 40], 0.0, 100, True, False),        # mask and window
+    (128, 32, 8, [0, 40, 300], [17, 64, 130], 0.0, -1, False, True),
+    (128, 32, 8, [1400, 20], [33, 90], 25.0, -1, False, True),      # sinks, cap, split rows
+    (64, 12, 3, [500, 0, 77], [40, 129, 3], 0.0, -1, True, True),
+    (128, 28, 4, [700, 64], [100, 5], 0.0, 50, True, True),
+]
+
+
+@pytest.mark.parametrize("lq,hq,hkv,prefix,extend,cap,window,mask,sinks", MASK_SINK)
+def test_extend_custom_mask_and_sinks_vs_oracle(lq, hq, hkv, prefix, extend, cap, window,
+                                                mask, sinks):
+    """Custom mask (replaces the causal mask, keeps the window) and sinks
+    (extra denominator term per query head), two-stage and unified forms,
+    against the oracle."""
+    spec = W.small_spec(batch=len(prefix), hq=hq, hkv=hkv, lq=lq, lv=lq, prefix=prefix,
+                        extend=extend, logit_cap=cap, sliding_window=window,
+                        seed=sum(prefix) + 7 * sum(extend) + hq)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    kw = {}
+    if mask:
+        cm, mi = random_masks(wl, seed=sum(extend))
+        kw.update(custom_mask=cm, mask_indptr=mi)
+    if sinks:
+        g = torch.Generator().manual_seed(hq)
+        kw["sinks"] = (torch.randn(hq, generator=g) * 2.0).float()
+    ro, rl = oracle_extend(wl, **kw)
+    o, lse, ws = dw.extend(**kw)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    assert_close(o, lse, ro, rl, f"two-stage mask={mask} sinks={sinks}")
+    uo, ul, ws2 = dw.unified(**kw)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws2) == 0
+    assert_close(uo, ul, ro, rl, f"unified mask={mask} sinks={sinks}")
+
+
+def test_mask_rows_without_visible_keys_in_a_split_chunk():
+    """With a mask a row may see nothing in a split chunk (or nothing at
+    all): o = 0 there, lse = -inf, or the sink when one is given."""
+    spec = W.small_spec(batch=1, hq=8, hkv=2, lq=128, lv=128, prefix=[1500], extend=[40], seed=3)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    E, P = 40, 1500
+    m = torch.zeros(E, P + E, dtype=torch.bool)
+    m[:, :64] = True                  # only the first prefix keys ...
+    m[5] = False                      # ... and row 5 sees nothing
+    flat = m.to(torch.uint8).reshape(-1)
+    mi = torch.tensor([0, E * (P + E)], dtype=torch.int32)
+    for sinks in (None, torch.linspace(-2.0, 3.0, 8).float()):
+        kw = dict(custom_mask=flat, mask_indptr=mi, sinks=sinks)
+        ro, rl = oracle_extend(wl, **kw)
+        o, lse, ws = dw.unified(**kw)
+        torch.cuda.synchronize()
+        assert pkx.workspace_status(ws) == 0
+        assert_close(o, lse, ro, rl, f"empty rows sinks={sinks is not None}")
+
+
+def test_custom_mask_and_sinks_rejected_for_mla():
+    wl = W.draw(W.small_spec(batch=1, hq=16, hkv=1, lq=576, lv=512, prefix=[10], extend=[4],
+                             v_aliases_k=True, seed=2))
+    dw = DeviceWorkload(wl)
+    with pytest.raises(pkx.PkxError) as ei:
+        dw.unified(sinks=torch.zeros(16))
+    assert ei.value.code == pkx.PKX_EUNSUPPORTED
 
 
 def test_repeat_calls_are_bitwise_identical():
