@@ -65,8 +65,28 @@ def visible_pairs(spec: W.WorkloadSpec, prefix, extend, rows=None, qo_indptr=Non
     return int(allv[rows].sum())
 
 
+def mask_visible_per_token(wl: W.Workload) -> torch.Tensor:
+    """Visible keys per extend token under the workload's custom mask (the
+    mask replaces the causal term; the window still applies)."""
+    s = wl.spec
+    out = []
+    for b in range(wl.batch):
+        E, P = wl.extend_lens[b], wl.prefix_lens[b]
+        if E == 0:
+            continue
+        T = P + E
+        m = wl.custom_mask[int(wl.mask_indptr[b]): int(wl.mask_indptr[b]) + E * T].view(E, T).bool()
+        if s.sliding_window > 0:
+            qpos = torch.arange(P, P + E).view(E, 1)
+            m = m & (qpos - torch.arange(T).view(1, T) <= s.sliding_window)
+        out.append(m.sum(dim=1))
+    return torch.cat(out).to(torch.int64)
+
+
 def extend_flops(wl: W.Workload) -> float:
     s = wl.spec
+    if wl.custom_mask is not None:
+        return 2.0 * (s.lq + s.lv) * s.hq * int(mask_visible_per_token(wl).sum())
     return 2.0 * (s.lq + s.lv) * s.hq * visible_pairs(s, wl.prefix_lens, wl.extend_lens)
 
 
@@ -213,10 +233,15 @@ def oracle_rate(wl, rows, k_ext, v_ext, kb, vb):
     s = wl.spec
     t0 = time.perf_counter()
     oracle.extend_attention(wl.q, k_ext, v_ext, kb, vb, wl.qo_indptr, wl.kv_indptr,
-                            wl.kv_indices, wl.sm_scale, s.logit_cap, s.sliding_window, rows=rows)
+                            wl.kv_indices, wl.sm_scale, s.logit_cap, s.sliding_window, rows=rows,
+                            custom_mask=wl.custom_mask, mask_indptr=wl.mask_indptr,
+                            sinks=None if wl.sinks is None else wl.sinks.double())
     dt = time.perf_counter() - t0
     tok = rows // s.hq
-    pairs = visible_pairs(s, wl.prefix_lens, wl.extend_lens, rows=tok)
+    if wl.custom_mask is not None:
+        pairs = int(mask_visible_per_token(wl)[tok].sum())
+    else:
+        pairs = visible_pairs(s, wl.prefix_lens, wl.extend_lens, rows=tok)
     return dt, 2.0 * (s.lq + s.lv) * pairs
 
 
@@ -276,6 +301,10 @@ WORKLOAD_TEXT = {
     "tiny": "batch=2 Hq=4 Hkv=2 D=64 prefix={16,0} extend={8,5} pool=64 slots sm_scale=1/8",
     "decode_gqa": "decode: batch=64 Hq=32 Hkv=8 D=128 T=8193 pool=2^20 slots (permuted)",
     "decode_mla": "decode: batch=64 Hq=16 Hkv=1 Lq=576 Lv=512 (V aliases K) T=4096 pool=2^20 slots",
+    "spec_verify": "batch=64 Hq=32 Hkv=8 D=128 prefix~U[1024,4096] extend=64 draft-tree tokens "
+                   "under a custom mask (prefix + ancestors + self) pool=2^20 slots (permuted)",
+    "sinks_swa": "batch=16 Hq=64 Hkv=8 D=64 prefix~U[0,4096] extend~U[1,1024] sliding_window=128 "
+                 "sink logit per head ~N(0,1.5) pool=2^18 slots (permuted)",
 }
 
 
@@ -318,21 +347,29 @@ class ExtendStep:
         self.lse = torch.empty(n, s.hq, dtype=torch.float32, device=dev)
         nbytes = pkx.extend_workspace_size(wl.batch, n, s.hq, s.hkv, s.lq, s.lv)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.custom_mask = wl.custom_mask.to(dev) if wl.custom_mask is not None else None
+        self.mask_indptr = wl.mask_indptr.to(dev) if wl.mask_indptr is not None else None
+        self.sinks = wl.sinks.to(dev).float() if wl.sinks is not None else None
         self.launches = 4  # index build, scheduler, attention, combine
         self.flops = extend_flops(wl)
         self.bytes = extend_bytes(wl, unified=True)
 
     def inputs(self):
-        return [self.q, self.prefix_indptr, self.prefix_indices, self.extend_start,
-                self.extend_lens, self.extend_indices, self.qo_indptr]
+        ins = [self.q, self.prefix_indptr, self.prefix_indices, self.extend_start,
+               self.extend_lens, self.extend_indices, self.qo_indptr]
+        if self.custom_mask is not None:  # the draft tree changes every step
+            ins += [self.custom_mask, self.mask_indptr]
+        return ins
 
     def twin(self):
         """The same step over the same pool with its own input, output and
         workspace buffers (double buffering of the end-to-end loop)."""
         t = copy.copy(self)
         for name in ("q", "prefix_indptr", "prefix_indices", "extend_start", "extend_lens",
-                     "extend_indices", "qo_indptr", "uptr", "uidx", "plen", "o", "lse", "ws"):
-            setattr(t, name, torch.empty_like(getattr(self, name)))
+                     "extend_indices", "qo_indptr", "uptr", "uidx", "plen", "o", "lse", "ws",
+                     "custom_mask", "mask_indptr"):
+            if getattr(self, name) is not None:
+                setattr(t, name, torch.empty_like(getattr(self, name)))
         return t
 
     def __call__(self):
@@ -343,7 +380,8 @@ class ExtendStep:
                                           out=(self.uptr, self.uidx, self.plen))
         self.pkx.extend_attention_fwd_unified(
             self.q, self.o, self.kb, self.vb, self.qo_indptr, self.uptr, self.uidx, self.plen,
-            self.wl.sm_scale, s.logit_cap, s.sliding_window, lse=self.lse, workspace=self.ws)
+            self.wl.sm_scale, s.logit_cap, s.sliding_window, lse=self.lse, workspace=self.ws,
+            custom_mask=self.custom_mask, mask_indptr=self.mask_indptr, sinks=self.sinks)
 
 
 class DecodeStep:

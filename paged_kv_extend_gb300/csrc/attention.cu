@@ -491,7 +491,9 @@ __device__ __forceinline__ int ring_unit(uint64_t *u_full, uint64_t *u_empty,
   return u;
 }
 
-template <int HD, int MODE>
+// MASK: a custom mask replaces the causal mask (its own instantiation, so
+// the unmasked kernel carries none of the mask code).
+template <int HD, int MODE, bool MASK>
 __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     attn_kernel(const __grid_constant__ TMaps tm, const KParams p) {
   using C = Cfg<HD>;
@@ -586,7 +588,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       const int64_t prow_idx = (int64_t)w.slot * p.rows_per_slot + tok0 * G + r;
       // custom mask row of this query: byte per key of the sequence
       const uint8_t *mrow = nullptr;
-      if (p.custom_mask && valid) {
+      if (MASK && valid) {
         const int qo0 = p.qo_indptr[w.b];
         const int64_t n_keys = MODE == kTwoStage
                                    ? (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]) +
@@ -646,9 +648,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             for (int i = 0; i < C::BN; ++i) x[i] = p.cap_log2 * tanh_approx(x[i] * p.cap_pre);
             sc = 1.0f;
           }
-          const bool need_mask = p.custom_mask || (ke - 1 > qmin) || (ke - kb < C::BN) ||
+          const bool need_mask = MASK || (ke - 1 > qmin) || (ke - kb < C::BN) ||
                                  (p.window > 0 && kb < qmax - p.window);
-          if (p.custom_mask) {
+          if constexpr (MASK) {
             // the custom mask replaces the causal term; the window stays
 #pragma unroll
             for (int i = 0; i < C::BN; ++i) {
@@ -1256,18 +1258,18 @@ static int make_q_map(CUtensorMap *m, const void *q, int64_t n, int hq, int lq, 
   return PKX_OK;
 }
 
-template <int HD, int MODE>
+template <int HD, int MODE, bool MASK = false>
 static int launch_attn_kernel(const TMaps &tmaps, const KParams &kp, int grid, cudaStream_t s) {
   using C = Cfg<HD>;
   static bool configured = false;  // per instantiation; attribute is per device
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, MODE>,
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, MODE, MASK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
       return set_error(PKX_ECUDA, "cudaFuncSetAttribute(attn_kernel): %s", cudaGetErrorString(e));
     configured = true;
   }
-  attn_kernel<HD, MODE><<<grid, C::THREADS, C::SMEM, s>>>(tmaps, kp);
+  attn_kernel<HD, MODE, MASK><<<grid, C::THREADS, C::SMEM, s>>>(tmaps, kp);
   return PKX_OK;
 }
 
@@ -1396,13 +1398,22 @@ int launch_attention(const AttnArgs &a) {
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
   attention_events(&ev_before, &ev_after);
   if (ev_before) cudaEventRecord(ev_before, a.stream);
+  const bool masked = a.custom_mask != nullptr;
   if (a.lq == 128 && a.lv == 128) {
-    if (a.mode == kTwoStage) rc = launch_attn_kernel<128, kTwoStage>(tm, kp, grid, a.stream);
-    else if (a.mode == kUnified) rc = launch_attn_kernel<128, kUnified>(tm, kp, grid, a.stream);
+    if (a.mode == kTwoStage)
+      rc = masked ? launch_attn_kernel<128, kTwoStage, true>(tm, kp, grid, a.stream)
+                  : launch_attn_kernel<128, kTwoStage>(tm, kp, grid, a.stream);
+    else if (a.mode == kUnified)
+      rc = masked ? launch_attn_kernel<128, kUnified, true>(tm, kp, grid, a.stream)
+                  : launch_attn_kernel<128, kUnified>(tm, kp, grid, a.stream);
     else rc = launch_attn_kernel<128, kDecode>(tm, kp, grid, a.stream);
   } else if (a.lq == 64 && a.lv == 64) {
-    if (a.mode == kTwoStage) rc = launch_attn_kernel<64, kTwoStage>(tm, kp, grid, a.stream);
-    else if (a.mode == kUnified) rc = launch_attn_kernel<64, kUnified>(tm, kp, grid, a.stream);
+    if (a.mode == kTwoStage)
+      rc = masked ? launch_attn_kernel<64, kTwoStage, true>(tm, kp, grid, a.stream)
+                  : launch_attn_kernel<64, kTwoStage>(tm, kp, grid, a.stream);
+    else if (a.mode == kUnified)
+      rc = masked ? launch_attn_kernel<64, kUnified, true>(tm, kp, grid, a.stream)
+                  : launch_attn_kernel<64, kUnified>(tm, kp, grid, a.stream);
     else rc = launch_attn_kernel<64, kDecode>(tm, kp, grid, a.stream);
   } else if (mla) {
     if (a.mode == kTwoStage) rc = launch_mla_kernel<kTwoStage>(kp, grid, a.stream);

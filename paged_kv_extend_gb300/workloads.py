@@ -49,6 +49,9 @@ class WorkloadSpec:
     seed: int = 1000
     v_aliases_k: bool = False      # MLA: V = first lv dims of K
     decode: bool = False           # one query per sequence over all T_b keys
+    tree_mask: bool = False        # custom mask: each extend token is a draft-tree
+                                   # node that sees the prefix, its ancestors and itself
+    sinks: bool = False            # a sink logit per query head
 
     @property
     def group(self) -> int:
@@ -89,6 +92,18 @@ SPECS = {
         prefix=("const", 4095), extend=("const", 1), num_slots=1 << 20,
         sm_scale=1.0 / math.sqrt(192.0), std=0.5, seed=1006, v_aliases_k=True,
         decode=True),
+    # Speculative-decoding verification: a 64-node draft tree per sequence
+    # over its cached prefix, under a custom (tree) mask.
+    "spec_verify": WorkloadSpec(
+        "spec_verify", batch=64, hq=32, hkv=8, lq=128, lv=128,
+        prefix=("uniform", 1024, 4096), extend=("const", 64), num_slots=1 << 20,
+        seed=1007, tree_mask=True),
+    # A layer with attention sinks and a 128-token sliding window (64-dim
+    # heads, 64 query / 8 KV heads).
+    "sinks_swa": WorkloadSpec(
+        "sinks_swa", batch=16, hq=64, hkv=8, lq=64, lv=64,
+        prefix=("uniform", 0, 4096), extend=("uniform", 1, 1024), num_slots=1 << 18,
+        sliding_window=128, seed=1008, sinks=True),
 }
 
 
@@ -143,6 +158,9 @@ class Workload:
     extend_start_loc: torch.Tensor   # int32 [B]
     extend_seq_lens: torch.Tensor    # int32 [B]
     token_offsets: torch.Tensor      # int64 [B+1] start of sequence b in k_rows
+    custom_mask: Optional[torch.Tensor] = None  # uint8, row i of b at mask_indptr[b] + i*T_b
+    mask_indptr: Optional[torch.Tensor] = None  # int32 [B+1]
+    sinks: Optional[torch.Tensor] = None        # fp32 [Hq]
 
     @property
     def batch(self) -> int:
@@ -230,13 +248,33 @@ def draw(spec: WorkloadSpec, seed: Optional[int] = None) -> Workload:
         kv_indptr = _cumsum0(p)
         kv_indices = cat(pre_idx)
         qo_indptr = _cumsum0(e)
+    # drawn after everything else, so the other fields do not depend on them
+    custom_mask = mask_indptr = sinks = None
+    if spec.tree_mask and not spec.decode:
+        rows, mptr = [], [0]
+        for i in range(b):
+            E, P = e[i], p[i]
+            anc = torch.zeros(E, E, dtype=torch.bool)     # anc[n, a]: a is n or an ancestor
+            for n in range(E):
+                if n > 0:
+                    parent = int(torch.randint(0, n, (1,), generator=g))
+                    anc[n] = anc[parent]
+                anc[n, n] = True
+            m = torch.cat([torch.ones(E, P, dtype=torch.bool), anc], dim=1)
+            rows.append(m.to(torch.uint8).reshape(-1))
+            mptr.append(mptr[-1] + E * (P + E))
+        custom_mask = torch.cat(rows) if rows else torch.zeros(0, dtype=torch.uint8)
+        mask_indptr = torch.tensor(mptr, dtype=torch.int32)
+    if spec.sinks:
+        sinks = torch.randn(spec.hq, generator=g) * 1.5
     return Workload(
         spec=spec, prefix_lens=p, extend_lens=e, slots=perm, k_rows=k_rows,
         v_rows=v_rows, q=q, qo_indptr=qo_indptr, kv_indptr=kv_indptr,
         kv_indices=kv_indices.to(torch.int32), extend_kv_indices=cat(ext_idx).to(torch.int32),
         extend_start_loc=_cumsum0(e)[:-1].clone(),
         extend_seq_lens=torch.tensor(e, dtype=torch.int32),
-        token_offsets=torch.tensor(offs, dtype=torch.int64))
+        token_offsets=torch.tensor(offs, dtype=torch.int64),
+        custom_mask=custom_mask, mask_indptr=mask_indptr, sinks=sinks)
 
 
 def small_spec(name="rand", batch=3, hq=8, hkv=2, lq=128, lv=128, prefix=None,

@@ -367,6 +367,30 @@ def test_full_size_sampled_rows(name):
     del dw
 
 
+@pytest.mark.parametrize("name", ["spec_verify", "sinks_swa"])
+def test_full_size_mask_and_sinks_sampled_rows(name):
+    """The draft-tree verification workload (custom mask) and the sink +
+    sliding-window workload at full size, through the unified call the
+    benchmark times; the oracle computes a seeded sample of rows."""
+    wl = W.draw(W.SPECS[name])
+    dw = DeviceWorkload(wl)
+    kw = {}
+    if wl.custom_mask is not None:
+        kw.update(custom_mask=wl.custom_mask, mask_indptr=wl.mask_indptr)
+    if wl.sinks is not None:
+        kw["sinks"] = wl.sinks.float()
+    o, lse, ws = dw.unified(**kw)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    rows = sample_rows(wl.n_q_tokens, wl.spec.hq, 2048, seed=78)
+    ro, rl = oracle_extend(wl, rows=rows, **kw)
+    go = o.view(-1, o.shape[-1])[rows.to(DEV)]
+    gl = lse.view(-1)[rows.to(DEV)]
+    assert_close(go, gl, ro, rl, name)
+    assert torch.isfinite(o.float()).all()
+    del dw
+
+
 def test_full_size_decode():
     wl = W.draw(W.SPECS["decode_gqa"])
     dw = DeviceWorkload(wl)
