@@ -586,15 +586,16 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       const int qmin = w.qpos0 + tok0, qmax = w.qpos0 + tok0 + n_tok_i - 1;
       const int64_t orow_idx = (int64_t)(w.q_tok0 + t) * p.hq + w.kvh * G + g;
       const int64_t prow_idx = (int64_t)w.slot * p.rows_per_slot + tok0 * G + r;
-      // custom mask row of this query: byte per key of the sequence
-      const uint8_t *mrow = nullptr;
-      if (MASK && valid) {
+      // custom mask rows: a byte per key of the sequence for each extend
+      // token; mbase is the row of this Q tile's first token
+      const uint8_t *mbase = nullptr;
+      int64_t mstride = 0;
+      if (MASK) {
         const int qo0 = p.qo_indptr[w.b];
-        const int64_t n_keys = MODE == kTwoStage
-                                   ? (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]) +
-                                         (p.qo_indptr[w.b + 1] - qo0)
-                                   : (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]);
-        mrow = p.custom_mask + p.mask_indptr[w.b] + (int64_t)(w.q_tok0 + t - qo0) * n_keys;
+        mstride = MODE == kTwoStage ? (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]) +
+                                          (p.qo_indptr[w.b + 1] - qo0)
+                                    : (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]);
+        mbase = p.custom_mask + p.mask_indptr[w.b] + (int64_t)(w.q_tok0 + tok0 - qo0) * mstride;
       }
       if (nt == 0) {
         if (valid) {
@@ -616,6 +617,39 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       for (int j = 0; j < nt; ++j) {
         int kb, ke;
         tile_keys(w, j, kb, ke);
+        // Mask bits of this thread's row for keys kb + 32 q + bit (q < 4).
+        // The G heads of a token share its mask row, so the warp walks its
+        // rows' tokens: all lanes read 32 consecutive bytes of the token's
+        // row (one sector per load), a ballot turns them into a word, and
+        // the lanes of that token keep it.  Issued before the S wait.
+        uint32_t mb[4] = {0u, 0u, 0u, 0u};
+        if constexpr (MASK) {
+          if (warp_active) {
+            const int t_lo = (wq * 32) / G, t_hi = min((wq * 32 + 31) / G, n_tok_i - 1);
+            const int my_t = r / G;
+            // eight tokens at a time: all loads first, so their latencies overlap
+            for (int tc = t_lo; tc <= t_hi; tc += 8) {
+              uint8_t by[8][4];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const uint8_t *rowp = mbase + (int64_t)(tc + u) * mstride;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  const int kpos = kb + 32 * q4 + lane;
+                  by[u][q4] = (tc + u <= t_hi && kpos < ke) ? __ldg(rowp + kpos) : (uint8_t)0;
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  const uint32_t word = __ballot_sync(0xffffffffu, by[u][q4] != 0);
+                  if (my_t == tc + u) mb[q4] = word;
+                }
+              }
+            }
+          }
+        }
         if (!mbar_wait(&bars[B_S_FULL + wg], s_cnt & 1u, abort_flag)) {
           abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
           break;
@@ -651,15 +685,21 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           const bool need_mask = MASK || (ke - 1 > qmin) || (ke - kb < C::BN) ||
                                  (p.window > 0 && kb < qmax - p.window);
           if constexpr (MASK) {
-            // the custom mask replaces the causal term; the window stays
+            // the custom mask replaces the causal term; the window stays.
+            // A row that sees every key of the tile (all bits set, the
+            // window does not cut) keeps the plain path.
+            const bool every = (mb[0] & mb[1] & mb[2] & mb[3]) == 0xffffffffu &&
+                               (p.window <= 0 || qpos - kb <= p.window);
+            if (!every) {
 #pragma unroll
-            for (int i = 0; i < C::BN; ++i) {
-              const int kpos = kb + i;
-              bool vis = mrow && kpos < ke && (p.window <= 0 || qpos - kpos <= p.window);
-              if (vis) vis = __ldg(mrow + kpos) != 0;
-              x[i] = vis ? x[i] * sc : -INFINITY;
+              for (int i = 0; i < C::BN; ++i) {
+                const int kpos = kb + i;
+                const bool vis = ((mb[i >> 5] >> (i & 31)) & 1u) &&
+                                 (p.window <= 0 || qpos - kpos <= p.window);
+                x[i] = vis ? x[i] * sc : -INFINITY;
+              }
+              sc = 1.0f;
             }
-            sc = 1.0f;
           } else if (need_mask) {
 #pragma unroll
             for (int i = 0; i < C::BN; ++i) {
