@@ -132,8 +132,7 @@ void pkx_set_attention_events(void *before, void *after);
  *   lse_out    nullable fp32 [num_q_tokens, hq] (natural log)
  *   workspace  >= pkx_extend_workspace_size(...) bytes
  * Supported (lq, lv): (64, 64), (128, 128), (576, 512); hq % hkv == 0 and
- * hq / hkv <= 128.  custom_mask and sinks: (64, 64) and (128, 128) only
- * (PKX_EUNSUPPORTED for the MLA shape).
+ * hq / hkv <= 128.
  */
 int pkx_extend_attention_fwd(
     const void *q_extend, const void *k_extend, const void *v_extend,

@@ -48,15 +48,12 @@ static int check_rows(const char *name, const void *p, int64_t s0, int64_t s1) {
   return PKX_OK;
 }
 
-// A custom mask needs its offsets; mask and sinks are built for the GQA
-// head dims only.
-static int check_mask_sinks(int lq, const uint8_t *custom_mask, const int32_t *mask_indptr,
+// A custom mask needs its offsets.
+static int check_mask_sinks(const uint8_t *custom_mask, const int32_t *mask_indptr,
                             const float *sinks) {
   if (custom_mask && (!mask_indptr || !aligned(mask_indptr, 4)))
     return set_error(PKX_EINVAL, "custom_mask needs an aligned int32 mask_indptr");
   if (sinks && !aligned(sinks, 4)) return set_error(PKX_EINVAL, "sinks misaligned");
-  if ((custom_mask || sinks) && lq == 576)
-    return set_error(PKX_EUNSUPPORTED, "custom_mask / sinks are not built for the MLA shape");
   return PKX_OK;
 }
 
@@ -124,7 +121,7 @@ int pkx_extend_attention_fwd(const void *q_extend, const void *k_extend, const v
   if (batch < 0 || num_q_tokens < 0) return set_error(PKX_EINVAL, "negative batch or token count");
   if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
   if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
-  if ((rc = check_mask_sinks(lq, custom_mask, mask_indptr, sinks))) return rc;
+  if ((rc = check_mask_sinks(custom_mask, mask_indptr, sinks))) return rc;
   if (batch == 0 || num_q_tokens == 0) return PKX_OK;
   if ((rc = check_rows("q_extend", q_extend, 8, 8))) return rc;
   if ((rc = check_rows("o_extend", o_extend, 8, 8))) return rc;
@@ -176,7 +173,7 @@ int pkx_extend_attention_fwd_unified(const void *q, void *o, const void *k_buffe
   if (batch < 0 || num_q_tokens < 0) return set_error(PKX_EINVAL, "negative batch or token count");
   if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
   if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
-  if ((rc = check_mask_sinks(lq, custom_mask, mask_indptr, sinks))) return rc;
+  if ((rc = check_mask_sinks(custom_mask, mask_indptr, sinks))) return rc;
   if (batch == 0 || num_q_tokens == 0) return PKX_OK;
   if ((rc = check_rows("q", q, 8, 8))) return rc;
   if ((rc = check_rows("o", o, 8, 8))) return rc;

@@ -1313,18 +1313,18 @@ static int launch_attn_kernel(const TMaps &tmaps, const KParams &kp, int grid, c
   return PKX_OK;
 }
 
-template <int MODE>
+template <int MODE, bool MASK = false>
 static int launch_mla_kernel(const KParams &kp, int grid, cudaStream_t s) {
   using C = MlaCfg<MODE>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mla_kernel<MODE>,
+    cudaError_t e = cudaFuncSetAttribute(mla_kernel<MODE, MASK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
       return set_error(PKX_ECUDA, "cudaFuncSetAttribute(mla_kernel): %s", cudaGetErrorString(e));
     configured = true;
   }
-  mla_kernel<MODE><<<grid, C::THREADS, C::SMEM, s>>>(kp);
+  mla_kernel<MODE, MASK><<<grid, C::THREADS, C::SMEM, s>>>(kp);
   return PKX_OK;
 }
 
@@ -1456,8 +1456,12 @@ int launch_attention(const AttnArgs &a) {
                   : launch_attn_kernel<64, kUnified>(tm, kp, grid, a.stream);
     else rc = launch_attn_kernel<64, kDecode>(tm, kp, grid, a.stream);
   } else if (mla) {
-    if (a.mode == kTwoStage) rc = launch_mla_kernel<kTwoStage>(kp, grid, a.stream);
-    else if (a.mode == kUnified) rc = launch_mla_kernel<kUnified>(kp, grid, a.stream);
+    if (a.mode == kTwoStage)
+      rc = masked ? launch_mla_kernel<kTwoStage, true>(kp, grid, a.stream)
+                  : launch_mla_kernel<kTwoStage>(kp, grid, a.stream);
+    else if (a.mode == kUnified)
+      rc = masked ? launch_mla_kernel<kUnified, true>(kp, grid, a.stream)
+                  : launch_mla_kernel<kUnified>(kp, grid, a.stream);
     else rc = launch_mla_kernel<kDecode>(kp, grid, a.stream);
   } else {
     return set_error(PKX_EUNSUPPORTED, "head dims (%d, %d) not built", a.lq, a.lv);

@@ -57,7 +57,8 @@ enum {
   M_RING = 16
 };
 
-template <int MODE>
+// MASK: a custom mask replaces the causal mask (own instantiation).
+template <int MODE, bool MASK>
 __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KParams p) {
   using C = MlaCfg<MODE>;
   extern __shared__ uint8_t smem_raw[];
@@ -137,6 +138,17 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
       const int64_t orow_idx = (int64_t)(w.q_tok0 + t) * p.hq + w.kvh * G + g;
       const int64_t prow_idx = (int64_t)w.slot * p.rows_per_slot + r;
       const int dv0 = w.dq * C::DVS;
+      // custom mask rows: a byte per key of the sequence for each extend
+      // token; mbase is the row of the unit's first token
+      const uint8_t *mbase = nullptr;
+      int64_t mstride = 0;
+      if (MASK) {
+        const int qo0 = p.qo_indptr[w.b];
+        mstride = MODE == kTwoStage ? (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]) +
+                                          (p.qo_indptr[w.b + 1] - qo0)
+                                    : (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]);
+        mbase = p.custom_mask + p.mask_indptr[w.b] + (int64_t)(w.q_tok0 - qo0) * mstride;
+      }
       if (nt == 0) {
         if (valid) {
           if (w.slot < 0) {
@@ -179,6 +191,35 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
       for (int j = 0; j < nt; ++j) {
         int kb, ke;
         tile_keys<C::BN>(w, j, kb, ke);
+        // mask bits of this thread's row for keys kb + 32 q + bit (q < 2):
+        // the warp's rows cover 32 / G tokens; all lanes read 32 consecutive
+        // bytes of a token's row per load, a ballot packs them
+        uint32_t mb[2] = {0u, 0u};
+        if constexpr (MASK) {
+          if (warp_active) {
+            const int t_lo = (warp * 32) / G, t_hi = min((warp * 32 + 31) / G, w.n_tok - 1);
+            for (int tc = t_lo; tc <= t_hi; tc += 4) {
+              uint8_t by[4][2];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint8_t *rowp = mbase + (int64_t)(tc + u) * mstride;
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                  const int kpos = kb + 32 * q2 + lane;
+                  by[u][q2] = (tc + u <= t_hi && kpos < ke) ? __ldg(rowp + kpos) : (uint8_t)0;
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                  const uint32_t word = __ballot_sync(0xffffffffu, by[u][q2] != 0);
+                  if (t == tc + u) mb[q2] = word;
+                }
+              }
+            }
+          }
+        }
         if (!mbar_wait(&bars[M_S_FULL], s_cnt & 1u, abort_flag)) {
           abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
           break;
@@ -215,7 +256,22 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
           }
           const bool need_mask = (ke - 1 > w.qpos0) || (ke - kb < C::BN) ||
                                  (p.window > 0 && kb < qmax - p.window);
-          if (need_mask) {
+          if constexpr (MASK) {
+            // the custom mask replaces the causal term; the window stays; a
+            // row that sees every key of the tile keeps the plain path
+            const bool every = (mb[0] & mb[1]) == 0xffffffffu &&
+                               (p.window <= 0 || qpos - kb <= p.window);
+            if (!every) {
+#pragma unroll
+              for (int i = 0; i < C::BN; ++i) {
+                const int kpos = kb + i;
+                const bool vis = ((mb[i >> 5] >> (i & 31)) & 1u) &&
+                                 (p.window <= 0 || qpos - kpos <= p.window);
+                x[i] = vis ? x[i] * sc : -INFINITY;
+              }
+              sc = 1.0f;
+            }
+          } else if (need_mask) {
 #pragma unroll
             for (int i = 0; i < C::BN; ++i) {
               const int kpos = kb + i;
@@ -302,8 +358,17 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
       pv_base += nt;
       tc_fence_after();
       if (warp_active) {
-        const float inv = l > 0.f ? 1.0f / l : 0.f;
-        const float lse_v = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        float inv = l > 0.f ? 1.0f / l : 0.f;
+        float lse_v = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (p.sinks && w.slot < 0) {
+          // the head's sink joins the denominator (split rows: in the combine)
+          const float s2 = __ldg(p.sinks + w.kvh * G + g) * 1.4426950408889634f;
+          const float M = fmaxf(m, s2);
+          const float a_m = m == -INFINITY ? 0.f : ex2_approx(m - M);
+          const float lt = l * a_m + ex2_approx(s2 - M);
+          inv = a_m / lt;
+          lse_v = (M + __log2f(lt)) * 0.69314718055994531f;
+        }
         uint32_t v[32];
 #pragma unroll
         for (int c = 0; c < C::DVS / 32; ++c) {

@@ -67,10 +67,10 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _extend(lib, hq=256, hkv=1) == pkx.PKX_EUNSUPPORTED
     assert _extend(lib, batch=-1) == pkx.PKX_EINVAL
     assert _extend(lib, scale=float("nan")) == pkx.PKX_EINVAL
-    # a custom mask needs its offsets; mask and sinks are not built for MLA
+    # a custom mask needs its offsets; sinks must be aligned
     assert _extend(lib, mask=0x1000) == pkx.PKX_EINVAL
     assert b"mask_indptr" in lib.pkx_last_error_string()
-    assert _extend(lib, lq=576, lv=512, hq=16, hkv=1, sinks=0x1000) == pkx.PKX_EUNSUPPORTED
+    assert _extend(lib, sinks=0x1002) == pkx.PKX_EINVAL
     # null tensors
     assert _extend(lib) == pkx.PKX_EINVAL
     assert b"null" in lib.pkx_last_error_string()

@@ -249,13 +249,34 @@ def test_mask_rows_without_visible_keys_in_a_split_chunk():
         assert_close(o, lse, ro, rl, f"empty rows sinks={sinks is not None}")
 
 
-def test_custom_mask_and_sinks_rejected_for_mla():
-    wl = W.draw(W.small_spec(batch=1, hq=16, hkv=1, lq=576, lv=512, prefix=[10], extend=[4],
-                             v_aliases_k=True, seed=2))
+@pytest.mark.parametrize("prefix,extend,window,mask,sinks", [
+    ([0, 300], [40, 70], -1, True, False),
+    ([700, 20], [9, 130], -1, False, True),
+    ([150, 2], [60, 17], 40, True, True),
+])
+def test_mla_custom_mask_and_sinks_vs_oracle(prefix, extend, window, mask, sinks):
+    """The MLA head (576/512, V aliases K) with a custom mask and/or sinks,
+    two-stage and unified forms."""
+    spec = W.small_spec(batch=len(prefix), hq=16, hkv=1, lq=576, lv=512, prefix=prefix,
+                        extend=extend, sliding_window=window, std=0.5, v_aliases_k=True,
+                        sm_scale=1.0 / math.sqrt(192.0), seed=sum(prefix) + sum(extend))
+    wl = W.draw(spec)
     dw = DeviceWorkload(wl)
-    with pytest.raises(pkx.PkxError) as ei:
-        dw.unified(sinks=torch.zeros(16))
-    assert ei.value.code == pkx.PKX_EUNSUPPORTED
+    kw = {}
+    if mask:
+        cm, mi = random_masks(wl, seed=5)
+        kw.update(custom_mask=cm, mask_indptr=mi)
+    if sinks:
+        kw["sinks"] = torch.linspace(-1.0, 2.5, 16).float()
+    ro, rl = oracle_extend(wl, **kw)
+    o, lse, ws = dw.extend(**kw)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    assert_close(o, lse, ro, rl, f"mla two-stage mask={mask} sinks={sinks}")
+    uo, ul, ws2 = dw.unified(**kw)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws2) == 0
+    assert_close(uo, ul, ro, rl, f"mla unified mask={mask} sinks={sinks}")
 
 
 def test_repeat_calls_are_bitwise_identical():
