@@ -68,6 +68,11 @@ def _configure(lib):
     lib.oracle_build_unified_kv_indices.restype = None
     lib.oracle_build_unified_kv_indices.argtypes = [
         _p, _p, _p, _p, _p, _i, _p, _p, _p]
+    lib.oracle_create_kv_indices.restype = None
+    lib.oracle_create_kv_indices.argtypes = [_p, _l, _p, _p, _p, _i, _p, _p]
+    lib.oracle_set_kv_buffer.restype = None
+    lib.oracle_set_kv_buffer.argtypes = [
+        _p, _l, _l, _p, _l, _l, _p, _l, _i, _i, _i, _p, _l, _l, _p, _l, _l]
     return lib
 
 
@@ -306,3 +311,47 @@ def build_unified_kv_indices(prefix_kv_indptr, prefix_kv_indices,
         _ptr(eix) if eix.numel() else None, int(bs), _ptr(uptr),
         _ptr(uidx) if uidx.numel() else None, _ptr(plen))
     return uptr, uidx, plen
+
+
+def create_kv_indices(req_to_token, req_pool_indices, paged_kernel_lens,
+                      kv_start_idx=None, fill=-1):
+    """KV-index gather (sglang flashinfer_backend.py,
+    create_flashinfer_kv_indices_triton and its callers' indptr).
+    req_to_token int32 [R, C]; req_pool_indices, paged_kernel_lens,
+    kv_start_idx int64 [bs].  Returns (kv_indptr int32 [bs+1], kv_indices
+    int32 [sum(paged_kernel_lens)]); ``fill`` marks entries not written."""
+    lib = _load()
+    rt = req_to_token.detach().cpu().to(torch.int32).contiguous()
+    rpi, pkl = _i64(req_pool_indices), _i64(paged_kernel_lens)
+    kst = _i64(kv_start_idx) if kv_start_idx is not None else None
+    bs = rpi.numel()
+    total = int(pkl.to(torch.int32).sum()) if bs else 0
+    kvp = torch.empty(bs + 1, dtype=torch.int32)
+    kvi = torch.full((total,), fill, dtype=torch.int32)
+    lib.oracle_create_kv_indices(
+        _ptr(rt) if rt.numel() else None, rt.shape[1] if rt.dim() == 2 else 0,
+        _ptr(rpi) if bs else None, _ptr(pkl) if bs else None,
+        _ptr(kst) if kst is not None and bs else None, bs, _ptr(kvp),
+        _ptr(kvi) if total else None)
+    return kvp, kvi
+
+
+def set_kv_buffer(k_buffer, v_buffer, cache_loc, k, v):
+    """KV write into the pool (sglang flashinfer_backend.py, set_kv_buffer
+    before the paged pass).  Returns new (k_buffer, v_buffer) bf16 tensors
+    equal to the inputs with row cache_loc[t] of every KV head replaced by
+    k[t] / v[t]; ``v`` may be None (K-only pool: v_buffer returned as is)."""
+    lib = _load()
+    kb = _bf16_bits(k_buffer).clone().contiguous()
+    vb = _bf16_bits(v_buffer).clone().contiguous()
+    kk = _bf16_bits(k).contiguous()
+    vv = _bf16_bits(v).contiguous() if v is not None else None
+    loc = _i64(cache_loc)
+    n, hkv, lk = kk.shape
+    lv = vv.shape[2] if vv is not None else 0
+    lib.oracle_set_kv_buffer(
+        _ptr(kk), *_row_strides(kk), _ptr(vv) if vv is not None else None,
+        *(_row_strides(vv) if vv is not None else (0, 0)),
+        _ptr(loc) if n else None, n, hkv, lk, lv,
+        _ptr(kb), *_row_strides(kb), _ptr(vb), *_row_strides(vb))
+    return kb.view(torch.bfloat16), vb.view(torch.bfloat16)

@@ -1,7 +1,8 @@
 /*
  * oracle.c -- plain, slow, float64 CPU restatement of extend attention over a
- * page-size-1 KV pool, decode attention, merge_state and the unified
- * KV-index build.
+ * page-size-1 KV pool, decode attention, merge_state, the unified KV-index
+ * build, the KV-index gather from the request-to-token table and the KV
+ * write into the pool.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
  * call this file.  It exists so that tests, the smoke check and the CPU
@@ -16,7 +17,7 @@
  *          _copy_unified_indices_kernel, build_unified_kv_indices.
  *   [FI]   sglang flashinfer_backend.py: forward_extend (ragged + paged +
  *          merge_state split), forward_decode, the sliding-window index
- *          updaters.
+ *          updaters, create_flashinfer_kv_indices_triton, set_kv_buffer.
  *   [CPU]  sglang cpu_graph_runner.py: the MLA K/V layout (V is the first
  *          kv_lora_rank dims of K) in the qkv_proj_with_rope fake.
  *
@@ -393,5 +394,63 @@ void oracle_build_unified_kv_indices(
         for (long e = 0; e < extend_seq_lens[b]; ++e)
             unified_kv_indices[dst + prefix_lens[b] + e] =
                 extend_kv_indices[extend_start_loc[b] + e];
+    }
+}
+
+/*
+ * KV-index gather from the request-to-token table ([FI]
+ * create_flashinfer_kv_indices_triton, with the indptr its callers build in
+ * the decode and prefill index updaters):
+ *   kv_indptr[0]   = 0
+ *   kv_indptr[b+1] = kv_indptr[b] + paged_kernel_lens[b]
+ *   kv_indices[kv_indptr[b] + j]
+ *       = req_to_token[req_pool_indices[b] * stride + kv_start[b] + j]
+ *   for j < paged_kernel_lens[b], with kv_start[b] = kv_start_idx[b], or 0
+ *   when kv_start_idx is NULL.  Lengths and starts are taken as 32-bit, as the
+ *   gather does.  Entries past kv_indptr[bs] are not written.
+ */
+void oracle_create_kv_indices(
+    const int32_t *req_to_token, long stride, const int64_t *req_pool_indices,
+    const int64_t *paged_kernel_lens, const int64_t *kv_start_idx, int bs,
+    int32_t *kv_indptr, int32_t *kv_indices)
+{
+    kv_indptr[0] = 0;
+    for (int b = 0; b < bs; ++b)
+        kv_indptr[b + 1] = kv_indptr[b] + (int32_t)paged_kernel_lens[b];
+    for (int b = 0; b < bs; ++b) {
+        long row = (long)req_pool_indices[b] * stride;
+        long start = kv_start_idx ? (long)(int32_t)kv_start_idx[b] : 0;
+        for (long j = 0; j < (long)(int32_t)paged_kernel_lens[b]; ++j)
+            kv_indices[kv_indptr[b] + j] = req_to_token[row + start + j];
+    }
+}
+
+/*
+ * KV write into the pool ([FI] forward_extend / forward_decode,
+ * token_to_kv_pool.set_kv_buffer(layer, cache_loc, k, v, ...)): token t's
+ * rows go to pool slot cache_loc[t], every KV head:
+ *   k_buf[cache_loc[t], h, :lk] = k[t, h, :lk]
+ *   v_buf[cache_loc[t], h, :lv] = v[t, h, :lv]     (skipped when v is NULL:
+ *                                                    the MLA pool holds K only)
+ * The pool is bf16 like the inputs, so the write is a copy of the bit
+ * patterns.  Slots not named in cache_loc keep their contents.
+ */
+void oracle_set_kv_buffer(
+    const uint16_t *k, long k_ts, long k_hs, const uint16_t *v, long v_ts,
+    long v_hs, const int64_t *cache_loc, long n_tokens, int hkv, int lk,
+    int lv, uint16_t *k_buf, long k_buf_ss, long k_buf_hs, uint16_t *v_buf,
+    long v_buf_ss, long v_buf_hs)
+{
+    for (long t = 0; t < n_tokens; ++t) {
+        long slot = (long)cache_loc[t];
+        for (int h = 0; h < hkv; ++h) {
+            for (int d = 0; d < lk; ++d)
+                k_buf[slot * k_buf_ss + (long)h * k_buf_hs + d] =
+                    k[t * k_ts + (long)h * k_hs + d];
+            if (v)
+                for (int d = 0; d < lv; ++d)
+                    v_buf[slot * v_buf_ss + (long)h * v_buf_hs + d] =
+                        v[t * v_ts + (long)h * v_hs + d];
+        }
     }
 }

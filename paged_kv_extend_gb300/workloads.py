@@ -191,6 +191,26 @@ class Workload:
             return k, k[..., : self.spec.lv]
         return k, self.v_rows.index_select(0, rows).to(device)
 
+    def req_to_token(self, rows: Optional[int] = None, cols: Optional[int] = None,
+                     seed: int = 0):
+        """A request-to-token table holding this batch: sequence b sits in a
+        random row req_pool_indices[b] (row 0 stays reserved and all zero),
+        its T_b slots in columns [0, T_b) in key order; every other entry is a
+        random slot.  Returns (req_to_token int32 [rows, cols],
+        req_pool_indices int64 [B], seq_lens int64 [B])."""
+        g = torch.Generator().manual_seed(seed)
+        t = [p + e for p, e in zip(self.prefix_lens, self.extend_lens)]
+        rows = rows if rows is not None else 2 * self.batch + 1
+        cols = cols if cols is not None else max(t + [1]) + 7
+        table = torch.randint(0, max(self.spec.num_slots, 1), (rows, cols),
+                              generator=g, dtype=torch.int32)
+        table[0] = 0
+        rpi = (torch.randperm(rows - 1, generator=g)[: self.batch] + 1).to(torch.int64)
+        for b in range(self.batch):
+            o = int(self.token_offsets[b])
+            table[int(rpi[b]), : t[b]] = self.slots[o: o + t[b]]
+        return table, rpi, torch.tensor(t, dtype=torch.int64)
+
     def pool(self, device="cpu"):
         """(k_buffer [S, Hkv, Lq], v_buffer [S, Hkv, Lv]) on device, zero
         except at the workload's slots.  For MLA, v_buffer is a view of the

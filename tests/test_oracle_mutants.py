@@ -48,6 +48,15 @@ MUTANTS = [
     ("mask_row_stride", "custom_mask + mask_indptr[b] + i * n_keys : NULL;", "custom_mask + mask_indptr[b] + i : NULL;", None),
     ("sink_dropped", "    if (sink)\n        l += exp(*sink - m);\n", "", None),
     ("sink_sign", "l += exp(*sink - m);", "l += exp(m - *sink);", None),
+    ("kvidx_start_ignored", "long start = kv_start_idx ? (long)(int32_t)kv_start_idx[b] : 0;", "long start = 0;", None),
+    ("kvidx_row_is_batch_index", "long row = (long)req_pool_indices[b] * stride;", "long row = (long)b * stride;", None),
+    ("kvidx_len_minus_start", "for (long j = 0; j < (long)(int32_t)paged_kernel_lens[b]; ++j)",
+     "for (long j = 0; j < (long)(int32_t)paged_kernel_lens[b] - start; ++j)", None),
+    ("kvidx_segment_reversed", "kv_indices[kv_indptr[b] + j] = req_to_token[row + start + j];",
+     "kv_indices[kv_indptr[b + 1] - 1 - j] = req_to_token[row + start + j];", None),
+    ("setkv_slot_is_token", "long slot = (long)cache_loc[t];", "long slot = t;", None),
+    ("setkv_heads_reversed", "k[t * k_ts + (long)h * k_hs + d];", "k[t * k_ts + (long)(hkv - 1 - h) * k_hs + d];", None),
+    ("setkv_v_from_k", "v[t * v_ts + (long)h * v_hs + d];", "k[t * k_ts + (long)h * k_hs + d];", None),
     ("sink_in_values", "    if (sink)\n        l += exp(*sink - m);\n", "    if (sink) {\n        l += exp(*sink - m);\n        for (int d = 0; d < lv; ++d) o[d] += exp(*sink - m);\n    }\n", None),
 ]
 
@@ -72,6 +81,10 @@ BATTERY = [
     lambda: pins.test_causal_pattern_mask_equals_no_mask(),
     lambda: pins.test_sinks_match_an_extra_zero_valued_key(-1),
     lambda: pins.test_sink_with_one_visible_key_closed_form(),
+    lambda: pins.test_kv_indices_hand_fixture(),
+    lambda: pins.test_set_kv_buffer_hand_fixture(),
+    lambda: pins.test_kv_indices_are_row_slices(0),
+    lambda: pins.test_set_kv_buffer_matches_index_copy(3, 128, 96, False),
 ]
 
 

@@ -600,3 +600,154 @@ def test_very_negative_sinks_change_nothing():
     ro, rl = _run_oracle(wl)
     torch.testing.assert_close(o, ro, rtol=0, atol=TOL)
     torch.testing.assert_close(lse, rl, rtol=0, atol=TOL)
+
+
+# ------------------------------- KV-index gather and KV write into the pool
+def _gather(table, rpi, lens, start=None):
+    t = lambda x: torch.tensor(x, dtype=torch.int64) if x is not None else None
+    return oracle.create_kv_indices(torch.tensor(table, dtype=torch.int32),
+                                    t(rpi), t(lens), t(start))
+
+
+def test_kv_indices_hand_fixture():
+    """Hand-derived worked example (tests/golden/kv_indices_hand.json),
+    with and without kv_start_idx."""
+    with open(os.path.join(GOLDEN, "kv_indices_hand.json")) as f:
+        fx = json.load(f)
+    for name, c in fx["cases"].items():
+        kvp, kvi = _gather(fx["req_to_token"], c["req_pool_indices"],
+                           c["paged_kernel_lens"], c["kv_start_idx"])
+        assert kvp.tolist() == c["expected_kv_indptr"], name
+        assert kvi.tolist() == c["expected_kv_indices"], name
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_kv_indices_are_row_slices(seed):
+    """Random tables, rows and windows: kv_indices equals numpy
+    concatenation of the row slices [kv_start, kv_start + len), kv_indptr
+    equals numpy's running sum, bit for bit."""
+    rng = np.random.default_rng(seed)
+    rows, cols, bs = 9, 300, 6
+    table = rng.integers(0, 1 << 30, size=(rows, cols), dtype=np.int32)
+    rpi = rng.choice(rows, size=bs, replace=False)
+    lens = rng.integers(0, 120, size=bs)
+    lens[seed % bs] = 0
+    start = rng.integers(0, cols - 120, size=bs)
+    for st in (None, start):
+        kvp, kvi = oracle.create_kv_indices(torch.from_numpy(table), torch.from_numpy(rpi),
+                                            torch.from_numpy(lens),
+                                            torch.from_numpy(st) if st is not None else None)
+        s0 = st if st is not None else np.zeros(bs, dtype=np.int64)
+        want = np.concatenate([table[rpi[b], s0[b]:s0[b] + lens[b]] for b in range(bs)])
+        assert np.array_equal(kvi.numpy(), want)
+        assert np.array_equal(kvp.numpy(), np.concatenate([[0], np.cumsum(lens)]))
+
+
+def test_whole_sequence_gather_is_the_unified_index_list():
+    """With paged_kernel_lens = seq_lens and no start (the full-attention
+    prefill updater), the gather from a table holding each sequence's
+    prefix then extend slots is the unified index list of
+    build_unified_kv_indices."""
+    wl = W.draw(_spec(batch=4, hq=4, hkv=2, lq=64, lv=64, prefix=[9, 0, 31, 2],
+                      extend=[4, 7, 0, 1], seed=41))
+    table, rpi, seq = wl.req_to_token(seed=3)
+    kvp, kvi = oracle.create_kv_indices(table, rpi, seq)
+    uptr, uidx, _ = oracle.build_unified_kv_indices(
+        wl.kv_indptr, wl.kv_indices, wl.extend_start_loc, wl.extend_seq_lens,
+        wl.extend_kv_indices, wl.batch)
+    assert torch.equal(kvp, uptr)
+    assert torch.equal(kvi.to(torch.int64), uidx)
+
+
+@pytest.mark.parametrize("window", [1, 5, 40])
+def test_window_start_keeps_the_extend_window(window):
+    """The sliding-window prefill updater gathers only the last
+    min(T, W + E) slots (kv_start = T - that); extend attention with window W
+    over those keys equals extend attention with window W over all keys."""
+    wl = W.draw(_spec(batch=3, hq=4, hkv=2, lq=64, lv=64, prefix=[30, 0, 12],
+                      extend=[6, 9, 3], seed=42))
+    table, rpi, seq = wl.req_to_token(seed=4)
+    ext = torch.tensor(wl.extend_lens, dtype=torch.int64)
+    pre = seq - ext
+    paged = torch.minimum(seq, window + seq - pre)
+    kvp, kvi = oracle.create_kv_indices(table, rpi, paged, seq - paged)
+    kb, vb = wl.pool()
+    o, lse = oracle.extend_attention_unified(
+        wl.q, kb, vb, wl.qo_indptr, kvp, kvi, (paged - ext).to(torch.int32),
+        wl.sm_scale, 0.0, window)
+    fp, fi = oracle.create_kv_indices(table, rpi, seq)
+    o2, l2 = oracle.extend_attention_unified(
+        wl.q, kb, vb, wl.qo_indptr, fp, fi, pre.to(torch.int32), wl.sm_scale, 0.0, window)
+    torch.testing.assert_close(o, o2, rtol=0, atol=TOL)
+    torch.testing.assert_close(lse, l2, rtol=0, atol=TOL)
+
+
+def test_window_start_keeps_the_decode_window():
+    """The sliding-window decode updater gathers the last min(T, W + 1)
+    slots; plain decode over them equals windowed decode over all slots."""
+    wl = W.draw(W.WorkloadSpec("dec", batch=3, hq=4, hkv=2, lq=64, lv=64,
+                               prefix=[25, 2, 0], extend=[1, 1, 1], num_slots=96, seed=43,
+                               decode=True))
+    table, rpi, seq = wl.req_to_token(seed=5)
+    kb, vb = wl.pool()
+    Wn = 7
+    paged = torch.clamp(seq, max=Wn + 1)
+    kvp, kvi = oracle.create_kv_indices(table, rpi, paged, seq - paged)
+    o, lse = oracle.decode_attention(wl.q, kb, vb, kvp, kvi, wl.sm_scale)
+    fp, fi = oracle.create_kv_indices(table, rpi, seq)
+    o2, l2 = oracle.decode_attention(wl.q, kb, vb, fp, fi, wl.sm_scale, sliding_window=Wn)
+    torch.testing.assert_close(o, o2, rtol=0, atol=TOL)
+    torch.testing.assert_close(lse, l2, rtol=0, atol=TOL)
+
+
+def test_set_kv_buffer_hand_fixture():
+    """Hand-derived worked example (tests/golden/set_kv_buffer_hand.json)."""
+    with open(os.path.join(GOLDEN, "set_kv_buffer_hand.json")) as f:
+        fx = json.load(f)
+    bf = lambda x: torch.tensor(x, dtype=torch.bfloat16)
+    kb = torch.full((fx["num_slots"], 2, 2), fx["fill"], dtype=torch.bfloat16)
+    vb = kb.clone()
+    k2, v2 = oracle.set_kv_buffer(kb, vb, torch.tensor(fx["cache_loc"]), bf(fx["k"]), bf(fx["v"]))
+    assert torch.equal(k2, bf(fx["expected_k_buffer"]))
+    assert torch.equal(v2, bf(fx["expected_v_buffer"]))
+
+
+@pytest.mark.parametrize("hkv,lk,lv,k_only", [(2, 64, 64, False), (3, 128, 96, False),
+                                              (1, 576, 512, True)])
+def test_set_kv_buffer_matches_index_copy(hkv, lk, lv, k_only):
+    """Random pools, distinct random slots and strided inputs (every head
+    row taken from a wider tensor): the write equals torch index_copy_ of the
+    token rows into the pool, and no other slot changes."""
+    g = torch.Generator().manual_seed(44 + lk)
+    slots, n = 50, 17
+    kb = torch.randn(slots, hkv, lk, generator=g).to(torch.bfloat16)
+    vb = torch.randn(slots, hkv, lv, generator=g).to(torch.bfloat16)
+    loc = torch.randperm(slots, generator=g)[:n]
+    k = torch.randn(n, hkv + 1, lk + 8, generator=g).to(torch.bfloat16)[:, 1:, 8:]
+    v = torch.randn(n, hkv, 2 * lv, generator=g).to(torch.bfloat16)[:, :, :lv]
+    k2, v2 = oracle.set_kv_buffer(kb, vb, loc, k, None if k_only else v)
+    assert torch.equal(k2, kb.clone().index_copy_(0, loc, k.contiguous()))
+    assert torch.equal(v2, vb if k_only else vb.clone().index_copy_(0, loc, v.contiguous()))
+
+
+def test_written_pool_gives_the_two_stage_result():
+    """Extend slots holding stale data, then set_kv_buffer of k_extend and
+    v_extend at out_cache_loc (the extend slots): unified attention over the
+    written pool equals the two-stage form, which reads the extend K/V
+    directly (forward_extend writes the pool before the paged pass)."""
+    wl = W.draw(_spec(batch=3, hq=8, hkv=2, lq=128, lv=128, prefix=[11, 0, 40],
+                      extend=[5, 13, 2], seed=45))
+    o, lse = _run_oracle(wl)
+    kb, vb = wl.pool()
+    loc = wl.extend_kv_indices.to(torch.int64)
+    g = torch.Generator().manual_seed(9)
+    kb[loc] = torch.randn(kb[loc].shape, generator=g).to(torch.bfloat16)
+    vb[loc] = torch.randn(vb[loc].shape, generator=g).to(torch.bfloat16)
+    k_ext, v_ext = wl.extend_kv()
+    kb2, vb2 = oracle.set_kv_buffer(kb, vb, loc, k_ext, v_ext)
+    uptr, uidx, plen = oracle.build_unified_kv_indices(
+        wl.kv_indptr, wl.kv_indices, wl.extend_start_loc, wl.extend_seq_lens,
+        wl.extend_kv_indices, wl.batch)
+    uo, ul = oracle.extend_attention_unified(wl.q, kb2, vb2, wl.qo_indptr, uptr, uidx, plen,
+                                             wl.sm_scale, 0.0, -1)
+    assert torch.equal(o, uo) and torch.equal(lse, ul)
