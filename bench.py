@@ -9,7 +9,8 @@ slots, bf16 N(0,1), sm_scale 1/sqrt(128)):
   2. extend_attention_fwd_unified (device scheduler, paged gather, QK^T,
      mask, online softmax, PV, split-KV combine)
 Inputs are resident in HBM when the timed region starts; L2 is flushed
-(a 512 MiB buffer is written) before every timed step, outside the timing.
+(a 512 MiB buffer is written, then read back so that L2 holds clean lines)
+before every timed step, outside the timing.
 
 value = algorithmic FLOPs of all ranks / max over ranks of the device time
 (TFLOP/s); FLOPs = 2 (Lq + Lv) per visible (query head, key) pair.
@@ -315,7 +316,7 @@ def config_dict(wl):
     return {"workload": f"{s.name}: {WORKLOAD_TEXT.get(s.name, '')}",
             "batch": s.batch, "q_tokens": wl.n_q_tokens,
             "kv_tokens": int(sum(wl.prefix_lens) + sum(wl.extend_lens)),
-            "seed": s.seed, "l2": "flushed before every timed step (512 MiB write)",
+            "seed": s.seed, "l2": "flushed before every timed step (512 MiB write, then read back so the evicted lines are clean)",
             "step": step}
 
 
@@ -426,6 +427,14 @@ def make_step(name, dev):
     return (DecodeStep if wl.spec.decode else ExtendStep)(wl, dev)
 
 
+def flush_l2(flush):
+    """Evict L2: write the 512 MiB buffer (about four times L2), then read it
+    back, so that the lines left in L2 are clean ones of this buffer and the
+    timed kernel pays for no write-back of the flush's own dirty lines."""
+    flush.zero_()
+    flush.view(torch.int64).sum()
+
+
 def time_steps(step, steps, flush, dev, attn_events=False, pkx=None):
     """Per-step device time (ms) with CUDA events on the current stream, L2
     flushed before each step outside the events; optionally the attention
@@ -438,7 +447,7 @@ def time_steps(step, steps, flush, dev, attn_events=False, pkx=None):
         e.record()
     torch.cuda.synchronize(dev)
     for k in range(steps):
-        flush.zero_()
+        flush_l2(flush)
         if attn_events:
             pkx.set_attention_events(ab[k], ae[k])
         starts[k].record()
@@ -568,6 +577,67 @@ def measure_component(name, dev, flush, steps, hbm_peak, bf16_peak):
     return out
 
 
+def time_launches(fn, steps, flush, dev):
+    """Mean device time (ms) of ``fn`` with CUDA events on the current
+    stream, L2 flushed before each launch outside the events."""
+    for _ in range(3):
+        fn()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for k in range(steps):
+        flush_l2(flush)
+        starts[k].record()
+        fn()
+        ends[k].record()
+    torch.cuda.synchronize(dev)
+    return sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / steps
+
+
+def measure_kv_ops(dev, flush, steps, hbm_peak):
+    """The steps on either side of the attention call, each on its own:
+    the KV write of a batch's extend tokens into the pool (set_kv_buffer)
+    and the KV-index gather from the request-to-token table, for the
+    default extend batch and for the long-prefix batch.  HBM GB/s of
+    algorithmic bytes (every byte read or written once) and the fraction of
+    the measured copy bandwidth."""
+    from paged_kv_extend_gb300 import pkx
+    out = {}
+    for name in ("llama3_8b", "long_prefix"):
+        wl = W.draw(W.SPECS[name])
+        s = wl.spec
+        kb, vb = wl.pool(dev)
+        k_ext, v_ext = wl.extend_kv(dev)
+        loc = wl.extend_kv_indices.to(dev, torch.int64)
+        n = loc.numel()
+        ms = time_launches(lambda: pkx.set_kv_buffer(kb, vb, loc, k_ext, v_ext), steps, flush, dev)
+        nbytes = 2.0 * n * s.hkv * (s.lq + s.lv) * 2 + 8.0 * n
+        out[f"set_kv_buffer/{name}"] = {
+            "what": f"{n} extend tokens x {s.hkv} KV heads x (K {s.lq} + V {s.lv}) bf16 into "
+                    f"a {s.num_slots}-slot pool at random slots",
+            "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+            "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+            "algorithmic_bytes": nbytes}
+        del kb, vb, k_ext, v_ext
+        table, rpi, seq = wl.req_to_token(seed=1)
+        table, rpi, seq = table.to(dev), rpi.to(dev), seq.to(dev)
+        total = int(sum(p + e for p, e in zip(wl.prefix_lens, wl.extend_lens)))
+        kvp = torch.empty(wl.batch + 1, dtype=torch.int32, device=dev)
+        kvi = torch.empty(total, dtype=torch.int32, device=dev)
+        ms = time_launches(lambda: pkx.create_kv_indices(table, rpi, seq, None, kv_indptr=kvp,
+                                                         kv_indices=kvi), steps, flush, dev)
+        nbytes = 8.0 * total + 16.0 * wl.batch + 4.0 * (wl.batch + 1)
+        out[f"create_kv_indices/{name}"] = {
+            "what": f"{wl.batch} sequences, {total} indices gathered from a "
+                    f"{tuple(table.shape)} request-to-token table",
+            "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+            "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+            "algorithmic_bytes": nbytes}
+        del table, rpi, seq, kvp, kvi
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, ws, rank, local):
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the CUDA library has no CPU path)")
@@ -625,6 +695,7 @@ def run_ours(args, ws, rank, local):
                 continue
             components[name] = measure_component(name, dev, flush, max(5, min(args.steps, 20)),
                                                  hbm_peak, bf16_peak)
+        components.update(measure_kv_ops(dev, flush, max(5, min(args.steps, 50)), hbm_peak))
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not wl.spec.decode:

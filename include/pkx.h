@@ -1,6 +1,7 @@
 /*
  * pkx.h -- C ABI of libpkx: extend attention over a page-size-1 KV pool and
- * its companions (decode attention, unified KV-index build, merge_state),
+ * its companions (decode attention, unified KV-index build, merge_state, the
+ * KV write into the pool and the KV-index gather from the request table),
  * as hand-written CUDA kernels for sm_103a (GB300).
  *
  * Conventions for every call below
@@ -250,6 +251,64 @@ int pkx_build_unified_kv_indices(
     const int32_t *extend_start_loc, const int32_t *extend_seq_lens,
     const int32_t *extend_kv_indices, int batch, int32_t *unified_kv_indptr,
     int64_t *unified_kv_indices, int32_t *prefix_lens, void *stream);
+
+/*
+ * KV write into the pool.
+ * Source: sglang flashinfer_backend.py, forward_extend and forward_decode:
+ * before the paged pass, token_to_kv_pool.set_kv_buffer(layer, cache_loc, k,
+ * v, ...) stores each new token's K and V rows at its pool slot.  For
+ * t < n_tokens and every KV head h:
+ *   k_buffer[cache_loc[t], h, :lk] = k[t, h, :lk]
+ *   v_buffer[cache_loc[t], h, :lv] = v[t, h, :lv]
+ *   k         bf16 [n_tokens, hkv, lk], strides (k_ts, k_hs)
+ *   v         bf16 [n_tokens, hkv, lv], strides (v_ts, v_hs), or NULL for a
+ *             K-only pool (the MLA pool, whose V is the first lv dims of K):
+ *             then v_buffer and its strides are ignored
+ *   cache_loc int64 [n_tokens] pool slots (the batch's out_cache_loc)
+ *   k_buffer / v_buffer  bf16 pools [num_slots, hkv, lk] / [.., lv] (written)
+ * The pool has the inputs' dtype, so the write is an exact copy (the fp8
+ * scales of the pages' call do not apply to a bf16 pool).  lk and lv are any
+ * positive multiples of 8.  Slots outside [0, num_slots) are skipped, so a
+ * bad slot never writes out of the pool.  Two tokens with the same slot leave
+ * either one's row there.  Slots not in cache_loc keep their contents.
+ */
+int pkx_set_kv_buffer(
+    const void *k, int64_t k_ts, int64_t k_hs, const void *v, int64_t v_ts,
+    int64_t v_hs, const int64_t *cache_loc, int64_t n_tokens, int hkv, int lk,
+    int lv, void *k_buffer, int64_t kb_ss, int64_t kb_hs, void *v_buffer,
+    int64_t vb_ss, int64_t vb_hs, int64_t num_slots, void *stream);
+
+/*
+ * KV-index gather from the request-to-token table.
+ * Source: sglang flashinfer_backend.py, create_flashinfer_kv_indices_triton
+ * and the decode / prefill index updaters that build its kv_indptr.  For
+ * b < batch, with kv_start[b] = kv_start_idx[b] (0 when kv_start_idx is
+ * NULL):
+ *   kv_indptr[0]   = 0
+ *   kv_indptr[b+1] = kv_indptr[b] + paged_kernel_lens[b]
+ *   kv_indices[kv_indptr[b] + j]
+ *       = req_to_token[req_pool_indices[b] * req_to_token_stride
+ *                      + kv_start[b] + j]             (j < paged_kernel_lens[b])
+ *   req_to_token       int32 [req_to_token_rows, req_to_token_stride]
+ *   req_pool_indices,
+ *   paged_kernel_lens,
+ *   kv_start_idx       int64 [batch] (kv_start_idx nullable); lengths and
+ *                      starts are taken as 32-bit, as the pages' gather does
+ *   kv_indptr          int32 [batch+1] (written: this call does the running
+ *                      sum the pages' callers do before the gather)
+ *   kv_indices         int32 [kv_indices_capacity] (written up to
+ *                      min(kv_indptr[batch], capacity); the rest untouched)
+ * The window updaters pass paged_kernel_lens = the kept tail and
+ * kv_start_idx = seq_lens - paged_kernel_lens.  An entry whose source lies
+ * outside the table is written as -1 instead of being read.  batch <= 12000
+ * (PKX_EUNSUPPORTED above).
+ */
+int pkx_create_kv_indices(
+    const int32_t *req_to_token, int64_t req_to_token_rows,
+    int64_t req_to_token_stride, const int64_t *req_pool_indices,
+    const int64_t *paged_kernel_lens, const int64_t *kv_start_idx, int batch,
+    int32_t *kv_indptr, int32_t *kv_indices, int64_t kv_indices_capacity,
+    void *stream);
 
 #ifdef __cplusplus
 }

@@ -277,4 +277,55 @@ int pkx_build_unified_kv_indices(const int32_t *prefix_kv_indptr,
                               unified_kv_indices, prefix_lens, static_cast<cudaStream_t>(stream));
 }
 
+int pkx_set_kv_buffer(const void *k, int64_t k_ts, int64_t k_hs, const void *v, int64_t v_ts,
+                      int64_t v_hs, const int64_t *cache_loc, int64_t n_tokens, int hkv, int lk,
+                      int lv, void *k_buffer, int64_t kb_ss, int64_t kb_hs, void *v_buffer,
+                      int64_t vb_ss, int64_t vb_hs, int64_t num_slots, void *stream) {
+  if (n_tokens < 0 || hkv <= 0 || lk <= 0 || lk % 8 || (v && (lv <= 0 || lv % 8)))
+    return set_error(PKX_EINVAL,
+                     "set_kv_buffer: n_tokens >= 0, hkv > 0, lk (and lv) positive multiples of 8");
+  if (num_slots < 0) return set_error(PKX_EINVAL, "set_kv_buffer: negative num_slots");
+  if (n_tokens == 0) return PKX_OK;
+  if (!cache_loc || !aligned(cache_loc, 8))
+    return set_error(PKX_EINVAL, "set_kv_buffer: cache_loc null or misaligned");
+  int rc;
+  if ((rc = check_rows("k", k, k_ts, k_hs)) != PKX_OK) return rc;
+  if ((rc = check_rows("k_buffer", k_buffer, kb_ss, kb_hs)) != PKX_OK) return rc;
+  if (v) {
+    if ((rc = check_rows("v", v, v_ts, v_hs)) != PKX_OK) return rc;
+    if ((rc = check_rows("v_buffer", v_buffer, vb_ss, vb_hs)) != PKX_OK) return rc;
+  }
+  return launch_set_kv_buffer(k, k_ts, k_hs, v, v_ts, v_hs, cache_loc, n_tokens, hkv, lk, lv,
+                              k_buffer, kb_ss, kb_hs, v_buffer, vb_ss, vb_hs, num_slots,
+                              static_cast<cudaStream_t>(stream));
+}
+
+int pkx_create_kv_indices(const int32_t *req_to_token, int64_t req_to_token_rows,
+                          int64_t req_to_token_stride, const int64_t *req_pool_indices,
+                          const int64_t *paged_kernel_lens, const int64_t *kv_start_idx,
+                          int batch, int32_t *kv_indptr, int32_t *kv_indices,
+                          int64_t kv_indices_capacity, void *stream) {
+  if (batch < 0 || batch > kGatherMaxBatch)
+    return set_error(PKX_EUNSUPPORTED, "create_kv_indices: batch %d outside [0, %d]", batch,
+                     kGatherMaxBatch);
+  if (req_to_token_rows < 0 || req_to_token_stride < 0 || kv_indices_capacity < 0)
+    return set_error(PKX_EINVAL, "create_kv_indices: negative table size or capacity");
+  if (!kv_indptr || !aligned(kv_indptr, 4))
+    return set_error(PKX_EINVAL, "create_kv_indices: kv_indptr null or misaligned");
+  if (batch > 0) {
+    if (!req_pool_indices || !paged_kernel_lens || !aligned(req_pool_indices, 8) ||
+        !aligned(paged_kernel_lens, 8) || (kv_start_idx && !aligned(kv_start_idx, 8)))
+      return set_error(PKX_EINVAL, "create_kv_indices: null or misaligned per-sequence array");
+    if (kv_indices_capacity > 0 && (!kv_indices || !aligned(kv_indices, 4)))
+      return set_error(PKX_EINVAL, "create_kv_indices: kv_indices null or misaligned");
+    if (req_to_token_rows > 0 && req_to_token_stride > 0 &&
+        (!req_to_token || !aligned(req_to_token, 4)))
+      return set_error(PKX_EINVAL, "create_kv_indices: req_to_token null or misaligned");
+  }
+  return launch_create_kv_indices(req_to_token, req_to_token_rows, req_to_token_stride,
+                                  req_pool_indices, paged_kernel_lens, kv_start_idx, batch,
+                                  kv_indptr, kv_indices, kv_indices_capacity,
+                                  static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

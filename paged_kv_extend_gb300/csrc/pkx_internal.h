@@ -117,5 +117,16 @@ int launch_build_unified(const int32_t *prefix_kv_indptr, const int32_t *prefix_
                          const int32_t *extend_start_loc, const int32_t *extend_seq_lens,
                          const int32_t *extend_kv_indices, int batch, int32_t *unified_kv_indptr,
                          int64_t *unified_kv_indices, int32_t *prefix_lens, cudaStream_t s);
+int launch_set_kv_buffer(const void *k, int64_t k_ts, int64_t k_hs, const void *v, int64_t v_ts,
+                         int64_t v_hs, const int64_t *cache_loc, int64_t n_tokens, int hkv, int lk,
+                         int lv, void *k_buffer, int64_t kb_ss, int64_t kb_hs, void *v_buffer,
+                         int64_t vb_ss, int64_t vb_hs, int64_t num_slots, cudaStream_t s);
+// Largest batch the index gather takes (its running sum lives in 48 KB of
+// shared memory).
+constexpr int kGatherMaxBatch = 12000;
+int launch_create_kv_indices(const int32_t *req_to_token, int64_t rows, int64_t stride,
+                             const int64_t *req_pool_indices, const int64_t *paged_kernel_lens,
+                             const int64_t *kv_start_idx, int batch, int32_t *kv_indptr,
+                             int32_t *kv_indices, int64_t capacity, cudaStream_t s);
 
 }  // namespace pkx

@@ -61,6 +61,11 @@ _SIGS = {
         _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p]),
     "pkx_merge_state": (_i, [_p, _p, _p, _p, _p, _p, _i64, _i, _i, _p]),
     "pkx_build_unified_kv_indices": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _p, _p]),
+    "pkx_set_kv_buffer": (_i, [
+        _p, _i64, _i64, _p, _i64, _i64, _p, _i64, _i, _i, _i,
+        _p, _i64, _i64, _p, _i64, _i64, _i64, _p]),
+    "pkx_create_kv_indices": (_i, [
+        _p, _i64, _i64, _p, _p, _p, _i, _p, _p, _i64, _p]),
 }
 
 
@@ -304,3 +309,73 @@ def build_unified_kv_indices(prefix_kv_indptr, prefix_kv_indices, extend_start_l
         _ptr(extend_kv_indices) if extend_kv_indices.numel() else None, int(bs), _ptr(uptr),
         _ptr(uidx) if uidx.numel() else None, _ptr(plen), _stream(dev)))
     return uptr, uidx, plen
+
+
+def _i64_vec(t: torch.Tensor, name: str):
+    if t.dtype != torch.int64 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA int64 tensor")
+    return t
+
+
+def set_kv_buffer(k_buffer, v_buffer, cache_loc, k, v=None):
+    """KV write into the pool (pkx_set_kv_buffer): row cache_loc[t] of every
+    KV head of k_buffer / v_buffer becomes k[t] / v[t], in place.  ``v`` None
+    writes K only (a K-only MLA pool).  cache_loc int64 [n]."""
+    lib = load_library()
+    _i64_vec(cache_loc, "cache_loc")
+    n, hkv, lk = k.shape
+    if cache_loc.numel() != n:
+        raise ValueError("cache_loc must hold one slot per token")
+    ks, kbs = _rows(k, "k"), _rows(k_buffer, "k_buffer")
+    if k_buffer.shape[1] != hkv or k_buffer.shape[2] != lk:
+        raise ValueError("k_buffer must be [slots, hkv, lk] like k")
+    lv, vs, vbs = 0, (0, 0), (0, 0)
+    if v is not None:
+        vs, vbs = _rows(v, "v"), _rows(v_buffer, "v_buffer")
+        lv = v.shape[2]
+        if v.shape[:2] != (n, hkv) or v_buffer.shape[1:] != (hkv, lv):
+            raise ValueError("v / v_buffer shapes do not match k")
+        if v_buffer.shape[0] != k_buffer.shape[0]:
+            raise ValueError("k_buffer and v_buffer must have the same number of slots")
+    _check(lib.pkx_set_kv_buffer(
+        _ptr(k), ks[0], ks[1], _ptr(v), vs[0], vs[1], _ptr(cache_loc) if n else None, n, hkv,
+        lk, lv, _ptr(k_buffer), kbs[0], kbs[1], _ptr(v_buffer) if v is not None else None,
+        vbs[0], vbs[1], k_buffer.shape[0], _stream(k.device)))
+    return k_buffer, v_buffer
+
+
+def create_kv_indices(req_to_token, req_pool_indices, paged_kernel_lens, kv_start_idx=None,
+                      kv_indptr=None, kv_indices=None, capacity=None):
+    """KV-index gather from the request-to-token table
+    (pkx_create_kv_indices).  req_to_token int32 [rows, cols];
+    req_pool_indices, paged_kernel_lens, kv_start_idx int64 [bs].  Returns
+    (kv_indptr int32 [bs+1], kv_indices int32).  Without ``kv_indices`` the
+    output is allocated with ``capacity`` entries, which the caller must
+    give (the host knows the sum of paged_kernel_lens; reading it back here
+    would synchronise)."""
+    lib = load_library()
+    if req_to_token.dtype != torch.int32 or not req_to_token.is_cuda or \
+            req_to_token.dim() != 2 or not req_to_token.is_contiguous():
+        raise ValueError("req_to_token must be a contiguous CUDA int32 [rows, cols] tensor")
+    _i64_vec(req_pool_indices, "req_pool_indices")
+    _i64_vec(paged_kernel_lens, "paged_kernel_lens")
+    if kv_start_idx is not None:
+        _i64_vec(kv_start_idx, "kv_start_idx")
+    bs = req_pool_indices.numel()
+    dev = req_to_token.device
+    if kv_indptr is None:
+        kv_indptr = torch.empty(bs + 1, dtype=torch.int32, device=dev)
+    if kv_indices is None:
+        if capacity is None:
+            raise ValueError("give kv_indices or capacity (the sum of paged_kernel_lens)")
+        kv_indices = torch.empty(int(capacity), dtype=torch.int32, device=dev)
+    _i32(kv_indptr, "kv_indptr")
+    _i32(kv_indices, "kv_indices")
+    _check(lib.pkx_create_kv_indices(
+        _ptr(req_to_token) if req_to_token.numel() else None, req_to_token.shape[0],
+        req_to_token.stride(0), _ptr(req_pool_indices) if bs else None,
+        _ptr(paged_kernel_lens) if bs else None,
+        _ptr(kv_start_idx) if kv_start_idx is not None and bs else None, int(bs),
+        _ptr(kv_indptr), _ptr(kv_indices) if kv_indices.numel() else None,
+        kv_indices.numel(), _stream(dev)))
+    return kv_indptr, kv_indices

@@ -31,6 +31,7 @@ def test_header_declares_the_boundary():
     for must in ["pkx_extend_attention_fwd", "pkx_extend_attention_fwd_unified",
                  "pkx_decode_attention_fwd", "pkx_merge_state",
                  "pkx_build_unified_kv_indices", "pkx_extend_workspace_size",
+                 "pkx_set_kv_buffer", "pkx_create_kv_indices",
                  "pkx_decode_workspace_size", "pkx_workspace_status",
                  "pkx_last_error_string", "pkx_version"]:
         assert must in names
@@ -91,6 +92,38 @@ def test_merge_and_index_validation(lib):
     assert lib.pkx_build_unified_kv_indices(None, None, None, None, None, 3, None, None, None,
                                             None) == pkx.PKX_EINVAL
     assert lib.pkx_workspace_status(None, None) == pkx.PKX_EINVAL
+
+
+def test_kv_write_and_gather_validation(lib):
+    """pkx_set_kv_buffer / pkx_create_kv_indices reject bad arguments on the
+    host (and an empty call is a no-op that needs no device)."""
+    A = 0x10000  # an aligned stand-in pointer; never dereferenced on these paths
+    kv = lambda **o: lib.pkx_set_kv_buffer(
+        o.get("k", A), o.get("kts", 256), 128, o.get("v", A), 256, 128, o.get("loc", A),
+        o.get("n", 4), 2, o.get("lk", 128), o.get("lv", 128), o.get("kb", A), 256, 128, A,
+        256, 128, 64, None)
+    assert kv(n=0) == pkx.PKX_OK
+    assert kv(lk=100) == pkx.PKX_EINVAL          # not a multiple of 8
+    assert kv(lv=0) == pkx.PKX_EINVAL
+    assert kv(loc=None) == pkx.PKX_EINVAL
+    assert kv(loc=A + 4) == pkx.PKX_EINVAL       # int64 misaligned
+    assert kv(k=A + 2) == pkx.PKX_EINVAL         # bf16 rows must be 16-byte aligned
+    assert kv(kts=260) == pkx.PKX_EINVAL         # stride not a multiple of 8
+    assert kv(kb=None) == pkx.PKX_EINVAL
+    assert kv(v=None, lv=0, n=0) == pkx.PKX_OK   # K-only pool
+    g = lambda **o: lib.pkx_create_kv_indices(
+        o.get("rt", A), 4, 8, o.get("rpi", A), o.get("lens", A), o.get("start", None),
+        o.get("bs", 2), o.get("ptr", A), o.get("idx", A), o.get("cap", 16), None)
+    assert g(bs=-1) == pkx.PKX_EUNSUPPORTED
+    assert g(bs=12001) == pkx.PKX_EUNSUPPORTED
+    assert g(ptr=None) == pkx.PKX_EINVAL
+    assert g(ptr=A + 2) == pkx.PKX_EINVAL
+    assert g(rpi=None) == pkx.PKX_EINVAL
+    assert g(lens=A + 4) == pkx.PKX_EINVAL
+    assert g(start=A + 4) == pkx.PKX_EINVAL
+    assert g(idx=None) == pkx.PKX_EINVAL
+    assert g(rt=None) == pkx.PKX_EINVAL
+    assert g(cap=-1) == pkx.PKX_EINVAL
 
 
 def test_workspace_size_grows_with_problem(lib):

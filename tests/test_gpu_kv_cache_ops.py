@@ -1,0 +1,231 @@
+"""GPU parity of the KV write into the pool (pkx_set_kv_buffer) and the
+KV-index gather from the request-to-token table (pkx_create_kv_indices),
+called through the C ABI, against the oracle.  Both are integer / byte work:
+the bar is bit-exact.
+"""
+import json
+import os
+
+import pytest
+import torch
+
+import oracle
+from paged_kv_extend_gb300 import pkx
+from paged_kv_extend_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from gpu_cases import DEV, assert_close, oracle_decode
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkx.load_library()
+
+
+def _i64(x):
+    return torch.as_tensor(x, dtype=torch.int64).to(DEV) if x is not None else None
+
+
+def _gather_gpu(table, rpi, lens, start=None, capacity=None, fill=-7):
+    table = torch.as_tensor(table, dtype=torch.int32).to(DEV)
+    bs = len(rpi)
+    total = int(torch.as_tensor(lens).sum()) if bs else 0
+    cap = total if capacity is None else capacity
+    kvp = torch.full((bs + 1,), fill, dtype=torch.int32, device=DEV)
+    kvi = torch.full((cap + 5,), fill, dtype=torch.int32, device=DEV)
+    pkx.create_kv_indices(table, _i64(rpi), _i64(lens), _i64(start), kv_indptr=kvp,
+                          kv_indices=kvi[:cap])
+    torch.cuda.synchronize()
+    return kvp.cpu(), kvi.cpu()
+
+
+# ------------------------------------------------------------ index gather
+def test_gather_hand_fixture_bit_exact():
+    fx = json.load(open(os.path.join(GOLDEN, "kv_indices_hand.json")))
+    for name, c in fx["cases"].items():
+        kvp, kvi = _gather_gpu(fx["req_to_token"], c["req_pool_indices"],
+                               c["paged_kernel_lens"], c["kv_start_idx"])
+        n = c["expected_kv_indptr"][-1]
+        assert kvp.tolist() == c["expected_kv_indptr"], name
+        assert kvi[:n].tolist() == c["expected_kv_indices"], name
+        assert torch.all(kvi[n:] == -7), name
+
+
+@pytest.mark.parametrize("seed,bs,rows,cols,maxlen,with_start", [
+    (0, 1, 2, 64, 64, False), (1, 7, 16, 600, 512, True), (2, 64, 80, 3000, 2900, False),
+    (3, 300, 512, 5000, 4000, True), (4, 4096, 4100, 700, 600, True),
+    (5, 12000, 12300, 40, 40, False)])
+def test_gather_bit_exact_vs_oracle(seed, bs, rows, cols, maxlen, with_start):
+    """Random tables, empty and one-entry sequences, lengths that straddle the
+    CTA shares, and the largest batch the call takes."""
+    g = torch.Generator().manual_seed(seed)
+    table = torch.randint(0, 1 << 30, (rows, cols), generator=g, dtype=torch.int32)
+    rpi = torch.randperm(rows, generator=g)[:bs]
+    lens = torch.randint(0, maxlen + 1, (bs,), generator=g)
+    lens[: min(bs, 3)] = torch.tensor([0, 1, maxlen])[: min(bs, 3)]
+    start = torch.randint(0, cols - maxlen + 1, (bs,), generator=g) if with_start else None
+    want_p, want_i = oracle.create_kv_indices(table, rpi, lens, start)
+    kvp, kvi = _gather_gpu(table, rpi, lens, start)
+    n = int(want_p[-1])
+    assert torch.equal(kvp, want_p)
+    assert torch.equal(kvi[:n], want_i)
+    assert torch.all(kvi[n:] == -7)
+
+
+def test_gather_full_size_long_sequences():
+    """Sequences of up to 128K tokens (the long-prefix shape) in one call:
+    every entry bit-exact against the oracle."""
+    g = torch.Generator().manual_seed(11)
+    bs, cols = 16, 131072
+    table = torch.randint(0, 1 << 22, (bs + 1, cols), generator=g, dtype=torch.int32)
+    rpi = torch.arange(1, bs + 1)
+    lens = torch.randint(60000, cols + 1, (bs,), generator=g)
+    want_p, want_i = oracle.create_kv_indices(table, rpi, lens)
+    kvp, kvi = _gather_gpu(table, rpi, lens)
+    assert torch.equal(kvp, want_p)
+    assert torch.equal(kvi[: int(want_p[-1])], want_i)
+
+
+def test_gather_respects_capacity_and_table_bounds():
+    """Entries past the output capacity are not written; an entry whose
+    source lies outside the table reads as -1 (nothing outside the table is
+    dereferenced)."""
+    table = torch.arange(40, dtype=torch.int32).view(4, 10)
+    kvp, kvi = _gather_gpu(table, [1, 2], [6, 6], capacity=8)
+    assert kvp.tolist() == [0, 6, 12]
+    assert kvi[:8].tolist() == [10, 11, 12, 13, 14, 15, 20, 21]
+    assert torch.all(kvi[8:] == -7)
+    # row 7 does not exist; columns 8.. of row 3 run off the end of the row
+    kvp, kvi = _gather_gpu(table, [7, 3], [2, 4], start=[0, 8])
+    assert kvp.tolist() == [0, 2, 6]
+    assert kvi[:6].tolist() == [-1, -1, 38, 39, -1, -1]
+
+
+def test_gather_empty_batch():
+    kvp = torch.full((1,), -7, dtype=torch.int32, device=DEV)
+    kvi = torch.empty(0, dtype=torch.int32, device=DEV)
+    e = torch.empty(0, dtype=torch.int64, device=DEV)
+    pkx.create_kv_indices(torch.zeros(2, 4, dtype=torch.int32, device=DEV), e, e, None,
+                          kv_indptr=kvp, kv_indices=kvi)
+    torch.cuda.synchronize()
+    assert kvp.tolist() == [0]
+
+
+# ------------------------------------------------------------ KV write
+def _pools(slots, hkv, lk, lv, seed):
+    g = torch.Generator().manual_seed(seed)
+    kb = torch.randn(slots, hkv, lk, generator=g).to(torch.bfloat16)
+    vb = torch.randn(slots, hkv, lv, generator=g).to(torch.bfloat16)
+    return kb, vb, g
+
+
+@pytest.mark.parametrize("n,hkv,lk,lv,slots,strided", [
+    (1, 1, 64, 64, 8, False), (37, 8, 128, 128, 500, False), (300, 2, 64, 64, 4096, True),
+    (1000, 4, 128, 96, 3000, True), (129, 3, 8, 16, 400, False)])
+def test_kv_write_bit_exact_vs_oracle(n, hkv, lk, lv, slots, strided):
+    kb, vb, g = _pools(slots, hkv, lk, lv, n)
+    loc = torch.randperm(slots, generator=g)[:n]
+    if strided:  # every head row taken out of a wider tensor
+        k = torch.randn(n, hkv + 1, lk + 16, generator=g).to(torch.bfloat16)[:, 1:, 16:]
+        v = torch.randn(n, hkv, 2 * lv, generator=g).to(torch.bfloat16)[:, :, :lv]
+    else:
+        k = torch.randn(n, hkv, lk, generator=g).to(torch.bfloat16)
+        v = torch.randn(n, hkv, lv, generator=g).to(torch.bfloat16)
+    want_k, want_v = oracle.set_kv_buffer(kb, vb, loc, k, v)
+    dkb, dvb = kb.to(DEV), vb.to(DEV)
+    pkx.set_kv_buffer(dkb, dvb, loc.to(DEV), k.to(DEV), v.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(dkb.cpu().view(torch.int16), want_k.view(torch.int16))
+    assert torch.equal(dvb.cpu().view(torch.int16), want_v.view(torch.int16))
+
+
+def test_kv_write_k_only_mla_pool():
+    """MLA: the pool row is the 576-dim latent; V is its first 512 dims, so
+    only K is written."""
+    slots, n = 2000, 321
+    kb, _, g = _pools(slots, 1, 576, 8, 5)
+    loc = torch.randperm(slots, generator=g)[:n]
+    k = torch.randn(n, 1, 576, generator=g).to(torch.bfloat16)
+    want_k, _ = oracle.set_kv_buffer(kb, kb[..., :512], loc, k, None)
+    dkb = kb.to(DEV)
+    pkx.set_kv_buffer(dkb, dkb[..., :512], loc.to(DEV), k.to(DEV), None)
+    torch.cuda.synchronize()
+    assert torch.equal(dkb.cpu().view(torch.int16), want_k.view(torch.int16))
+
+
+def test_kv_write_skips_slots_outside_the_pool():
+    slots = 64
+    kb, vb, g = _pools(slots, 2, 64, 64, 6)
+    loc = torch.tensor([3, -1, 64, 10, 1 << 40])
+    k = torch.randn(5, 2, 64, generator=g).to(torch.bfloat16)
+    v = torch.randn(5, 2, 64, generator=g).to(torch.bfloat16)
+    dkb, dvb = kb.to(DEV), vb.to(DEV)
+    pkx.set_kv_buffer(dkb, dvb, loc.to(DEV), k.to(DEV), v.to(DEV))
+    torch.cuda.synchronize()
+    keep = torch.tensor([0, 3])
+    want_k, want_v = oracle.set_kv_buffer(kb, vb, loc[keep], k[keep], v[keep])
+    assert torch.equal(dkb.cpu().view(torch.int16), want_k.view(torch.int16))
+    assert torch.equal(dvb.cpu().view(torch.int16), want_v.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["llama3_8b", "mla"])
+def test_kv_write_full_size(name):
+    """The extend tokens of a full-size workload written into a pool whose
+    extend slots hold stale rows: every written row equals its input row
+    (any size), and the pool's other rows are untouched."""
+    wl = W.draw(W.SPECS[name])
+    s = wl.spec
+    kb, vb = wl.pool(DEV)
+    loc = wl.extend_kv_indices.to(DEV, torch.int64)
+    k_ext, v_ext = wl.extend_kv(DEV)
+    kb.index_fill_(0, loc, 0.5)
+    before = kb.clone()
+    if s.v_aliases_k:
+        pkx.set_kv_buffer(kb, vb, loc, k_ext, None)
+    else:
+        vb.index_fill_(0, loc, 0.5)
+        pkx.set_kv_buffer(kb, vb, loc, k_ext, v_ext)
+        assert torch.equal(vb.index_select(0, loc).view(torch.int16), v_ext.view(torch.int16))
+    torch.cuda.synchronize()
+    assert torch.equal(kb.index_select(0, loc).view(torch.int16), k_ext.view(torch.int16))
+    other = torch.ones(s.num_slots, dtype=torch.bool, device=DEV)
+    other[loc] = False
+    assert torch.equal(kb[other].view(torch.int16), before[other].view(torch.int16))
+
+
+# ------------------------------------------ gather + write + attention chain
+def test_window_decode_through_gather_matches_windowed_oracle():
+    """The sliding-window decode updater's chain on the GPU: the new token's
+    K/V written at its slot, the last W+1 slots gathered from the
+    request-to-token table, plain decode over them; against windowed decode
+    of the oracle over all slots."""
+    wl = W.draw(W.WorkloadSpec("dec", batch=24, hq=16, hkv=4, lq=128, lv=128,
+                               prefix=("uniform", 1, 3000), extend=("const", 1), num_slots=200000,
+                               seed=12, decode=True))
+    table, rpi, seq = wl.req_to_token(seed=8)
+    Wn = 255
+    kb, vb = wl.pool()
+    last = (wl.token_offsets[1:] - 1)              # each sequence's new token
+    loc = wl.slots[last].to(torch.int64)
+    stale_k, stale_v = kb.clone(), vb.clone()
+    stale_k[loc] = 0
+    stale_v[loc] = 0
+    dkb, dvb = stale_k.to(DEV), stale_v.to(DEV)
+    pkx.set_kv_buffer(dkb, dvb, loc.to(DEV), wl.k_rows[last].to(DEV), wl.v_rows[last].to(DEV))
+    paged = torch.clamp(seq, max=Wn + 1)
+    kvp, kvi = pkx.create_kv_indices(table.to(DEV), rpi.to(DEV), paged.to(DEV),
+                                     (seq - paged).to(DEV), capacity=int(paged.sum()))
+    s = wl.spec
+    o = torch.empty(s.batch, s.hq, s.lv, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(s.batch, s.hq, dtype=torch.float32, device=DEV)
+    pkx.decode_attention_fwd(wl.q.to(DEV), o, dkb, dvb, kvp, kvi, wl.sm_scale, lse=lse)
+    torch.cuda.synchronize()
+    want_o, want_l = oracle.decode_attention(wl.q, kb, vb, wl.kv_indptr, wl.kv_indices,
+                                             wl.sm_scale, sliding_window=Wn)
+    assert_close(o.cpu(), lse.cpu(), want_o, want_l)
