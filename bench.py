@@ -638,6 +638,44 @@ def measure_kv_ops(dev, flush, steps, hbm_peak):
     return out
 
 
+def measure_split(dev, flush, steps, bf16_peak, name="llama3_8b"):
+    """The two-stage extend call against the ragged + paged + merge_state
+    split the pages take for 4096 or more extend tokens, on the same batch
+    (same algorithmic FLOPs; device time of the whole call)."""
+    from paged_kv_extend_gb300 import pkx
+    wl = W.draw(W.SPECS[name])
+    s = wl.spec
+    kb, vb = wl.pool(dev)
+    k_ext, v_ext = wl.extend_kv(dev)
+    q, qo = wl.q.to(dev), wl.qo_indptr.to(dev)
+    kvp, kvi = wl.kv_indptr.to(dev), wl.kv_indices.to(dev)
+    n = wl.n_q_tokens
+    o = torch.empty(n, s.hq, s.lv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(n, s.hq, dtype=torch.float32, device=dev)
+    ws2 = torch.empty(pkx.extend_workspace_size(wl.batch, n, s.hq, s.hkv, s.lq, s.lv),
+                      dtype=torch.uint8, device=dev)
+    wsr = torch.empty(pkx.ragged_paged_workspace_size(wl.batch, n, s.hq, s.hkv, s.lq, s.lv),
+                      dtype=torch.uint8, device=dev)
+    args = (q, k_ext, v_ext, o, kb, vb, qo, kvp, kvi, wl.sm_scale, s.logit_cap, s.sliding_window)
+    flops = extend_flops(wl)
+    out = {}
+    for label, fn, w in (("two_stage", pkx.extend_attention_fwd, ws2),
+                         ("ragged_paged", pkx.extend_attention_fwd_ragged_paged, wsr)):
+        ms = time_launches(lambda: fn(*args, lse=lse, workspace=w), steps, flush, dev)
+        if pkx.workspace_status(w) != 0:
+            raise SystemExit(f"{label}: device status {pkx.workspace_status(w)}")
+        out[f"{label}/{name}"] = {
+            "what": ("one extend call (scheduler, attention, combine)" if label == "two_stage"
+                     else "ragged pass over the extend keys + paged pass over the prefix "
+                          "keys + merge_state"),
+            "ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
+            "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / bf16_peak,
+            "algorithmic_flops": flops}
+    del kb, vb, k_ext, v_ext, ws2, wsr
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, ws, rank, local):
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the CUDA library has no CPU path)")
@@ -687,15 +725,24 @@ def run_ours(args, ws, rank, local):
 
     components = {"attn_kernel_share_of_step": attn_avg / ms}
     if not args.no_components:
-        names = ["decode_gqa", "mla"]
+        names = (args.components.split(",") if args.components
+                 else ["decode_gqa", "mla", "kv_ops", "split"])
         if args.all_workloads:
-            names = ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla"]
+            names = ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla", "kv_ops",
+                     "split"]
         for name in names:
             if name == args.workload:
                 continue
+            if name == "split":
+                components.update(measure_split(dev, flush, max(5, min(args.steps, 20)),
+                                                bf16_peak))
+                continue
+            if name == "kv_ops":
+                components.update(measure_kv_ops(dev, flush, max(5, min(args.steps, 50)),
+                                                 hbm_peak))
+                continue
             components[name] = measure_component(name, dev, flush, max(5, min(args.steps, 20)),
                                                  hbm_peak, bf16_peak)
-        components.update(measure_kv_ops(dev, flush, max(5, min(args.steps, 50)), hbm_peak))
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not wl.spec.decode:
@@ -769,6 +816,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-components", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--components", default="",
+                    help="comma-separated components to measure besides the step (workload "
+                         "names, kv_ops, split; default decode_gqa,mla,kv_ops,split)")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(W.SPECS),
                     help="workload of the timed step (default: the Llama-3-8B-shaped layer)")
     ap.add_argument("--all-workloads", action="store_true",

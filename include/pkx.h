@@ -147,6 +147,36 @@ int pkx_extend_attention_fwd(
     float *lse_out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Extend attention, ragged + paged split.
+ * Source: sglang flashinfer_backend.py, forward_extend with use_ragged (taken
+ * there for 4096 or more extend tokens): a causal pass over the extend keys
+ * alone (the ragged pass, k_extend / v_extend), a pass over the prefix keys
+ * alone in which every prefix key is visible to every extend query (the
+ * paged pass, the pool through kv_indptr / kv_indices), and merge_state of
+ * the two (o, lse) pairs.  The result is the two-stage form's up to bf16
+ * rounding of the two partial outputs (each pass writes bf16, as the pages'
+ * wrappers do); a sequence without prefix takes the ragged result alone
+ * (the paged pass gives it lse = -inf, weight 0).
+ * Arguments as pkx_extend_attention_fwd, without custom_mask / mask_indptr /
+ * sinks (the pages' ragged path has neither), and
+ *   workspace  >= pkx_ragged_paged_workspace_size(...) bytes: the passes'
+ *              scratch, the paged pass's output and both passes' lse.
+ * Runs three kernels' worth of launches in order on `stream`; o_extend holds
+ * the ragged pass's output in between.
+ */
+size_t pkx_ragged_paged_workspace_size(int batch, int num_q_tokens, int hq,
+                                       int hkv, int lq, int lv);
+int pkx_extend_attention_fwd_ragged_paged(
+    const void *q_extend, const void *k_extend, const void *v_extend,
+    void *o_extend, const void *k_buffer, const void *v_buffer,
+    const int32_t *qo_indptr, const int32_t *kv_indptr,
+    const int32_t *kv_indices, int batch, int num_q_tokens, int hq, int hkv,
+    int lq, int lv, int64_t ke_st, int64_t ke_sh, int64_t ve_st,
+    int64_t ve_sh, int64_t kb_ss, int64_t kb_sh, int64_t vb_ss, int64_t vb_sh,
+    int64_t num_slots, float sm_scale, float logit_cap, int sliding_window,
+    float *lse_out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Extend attention, unified form.
  * Source: sglang extend_attention.py, extend_attention_fwd_unified and
  * _fwd_kernel_unified: prefix and extend keys alike are pool slots

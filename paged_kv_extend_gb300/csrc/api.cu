@@ -107,22 +107,29 @@ int pkx_workspace_status(const void *workspace, void *stream) {
   return PKX_OK;
 }
 
-int pkx_extend_attention_fwd(const void *q_extend, const void *k_extend, const void *v_extend,
-                             void *o_extend, const void *k_buffer, const void *v_buffer,
-                             const int32_t *qo_indptr, const int32_t *kv_indptr,
-                             const int32_t *kv_indices, int batch, int num_q_tokens, int hq,
-                             int hkv, int lq, int lv, int64_t ke_st, int64_t ke_sh,
-                             int64_t ve_st, int64_t ve_sh, int64_t kb_ss, int64_t kb_sh,
-                             int64_t vb_ss, int64_t vb_sh, int64_t num_slots, float sm_scale,
-                             float logit_cap, int sliding_window, const uint8_t *custom_mask,
-                             const int32_t *mask_indptr, const float *sinks, float *lse_out,
-                             void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+// Validation and argument packing shared by the two-stage entry points.
+static int two_stage_args(AttnArgs &a, const void *q_extend, const void *k_extend,
+                          const void *v_extend, void *o_extend, const void *k_buffer,
+                          const void *v_buffer, const int32_t *qo_indptr,
+                          const int32_t *kv_indptr, const int32_t *kv_indices, int batch,
+                          int num_q_tokens, int hq, int hkv, int lq, int lv, int64_t ke_st,
+                          int64_t ke_sh, int64_t ve_st, int64_t ve_sh, int64_t kb_ss,
+                          int64_t kb_sh, int64_t vb_ss, int64_t vb_sh, int64_t num_slots,
+                          float sm_scale, float logit_cap, int sliding_window,
+                          const uint8_t *custom_mask, const int32_t *mask_indptr,
+                          const float *sinks, float *lse_out, bool *nothing_to_do) {
   int rc;
+  *nothing_to_do = false;
   if (batch < 0 || num_q_tokens < 0) return set_error(PKX_EINVAL, "negative batch or token count");
   if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
   if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
   if ((rc = check_mask_sinks(custom_mask, mask_indptr, sinks))) return rc;
-  if (batch == 0 || num_q_tokens == 0) return PKX_OK;
+  if (batch == 0 || num_q_tokens == 0) {
+    *nothing_to_do = true;
+    return PKX_OK;
+  }
   if ((rc = check_rows("q_extend", q_extend, 8, 8))) return rc;
   if ((rc = check_rows("o_extend", o_extend, 8, 8))) return rc;
   if ((rc = check_rows("k_extend", k_extend, ke_st, ke_sh))) return rc;
@@ -134,7 +141,6 @@ int pkx_extend_attention_fwd(const void *q_extend, const void *k_extend, const v
   if (kv_indices && !aligned(kv_indices, 4)) return set_error(PKX_EINVAL, "kv_indices misaligned");
   if (lse_out && !aligned(lse_out, 4)) return set_error(PKX_EINVAL, "lse_out misaligned");
   if (num_slots <= 0) return set_error(PKX_EINVAL, "num_slots must be positive");
-  AttnArgs a{};
   a.mode = kTwoStage;
   a.q = q_extend;
   a.o = o_extend;
@@ -153,9 +159,107 @@ int pkx_extend_attention_fwd(const void *q_extend, const void *k_extend, const v
   a.batch = batch; a.num_q_tokens = num_q_tokens; a.hq = hq; a.hkv = hkv; a.lq = lq; a.lv = lv;
   a.sm_scale = sm_scale; a.logit_cap = logit_cap; a.window = sliding_window;
   a.custom_mask = custom_mask; a.mask_indptr = mask_indptr; a.sinks = sinks;
+  return PKX_OK;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace of the ragged + paged split: one attention pass's scratch (the
+// passes run one after the other on the stream and share it), the paged
+// pass's bf16 output and both passes' lse.
+struct SplitLayout {
+  size_t attn, o_paged, lse_paged, lse_ragged, total;
+};
+
+static SplitLayout split_layout(int batch, int num_q_tokens, int hq, int hkv, int lq, int lv) {
+  SplitLayout L;
+  L.attn = 0;
+  const size_t attn = align256(ws_layout(batch, num_q_tokens, hkv, hq / hkv, lv,
+                                         num_sms_current_device(), false,
+                                         lq == 576 && lv == 512).total);
+  const size_t rows = (size_t)num_q_tokens * hq;
+  L.o_paged = attn;
+  L.lse_paged = L.o_paged + align256(rows * lv * 2);
+  L.lse_ragged = L.lse_paged + align256(rows * 4);
+  L.total = L.lse_ragged + align256(rows * 4);
+  return L;
+}
+
+extern "C" {
+
+int pkx_extend_attention_fwd(const void *q_extend, const void *k_extend, const void *v_extend,
+                             void *o_extend, const void *k_buffer, const void *v_buffer,
+                             const int32_t *qo_indptr, const int32_t *kv_indptr,
+                             const int32_t *kv_indices, int batch, int num_q_tokens, int hq,
+                             int hkv, int lq, int lv, int64_t ke_st, int64_t ke_sh,
+                             int64_t ve_st, int64_t ve_sh, int64_t kb_ss, int64_t kb_sh,
+                             int64_t vb_ss, int64_t vb_sh, int64_t num_slots, float sm_scale,
+                             float logit_cap, int sliding_window, const uint8_t *custom_mask,
+                             const int32_t *mask_indptr, const float *sinks, float *lse_out,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+  AttnArgs a{};
+  bool done;
+  int rc = two_stage_args(a, q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffer,
+                          qo_indptr, kv_indptr, kv_indices, batch, num_q_tokens, hq, hkv, lq, lv,
+                          ke_st, ke_sh, ve_st, ve_sh, kb_ss, kb_sh, vb_ss, vb_sh, num_slots,
+                          sm_scale, logit_cap, sliding_window, custom_mask, mask_indptr, sinks,
+                          lse_out, &done);
+  if (rc != PKX_OK || done) return rc;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   return launch_attention(a);
+}
+
+size_t pkx_ragged_paged_workspace_size(int batch, int num_q_tokens, int hq, int hkv, int lq,
+                                       int lv) {
+  if (batch < 0 || num_q_tokens < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM ||
+      lv <= 0)
+    return 0;
+  return split_layout(batch, num_q_tokens, hq, hkv, lq, lv).total;
+}
+
+int pkx_extend_attention_fwd_ragged_paged(
+    const void *q_extend, const void *k_extend, const void *v_extend, void *o_extend,
+    const void *k_buffer, const void *v_buffer, const int32_t *qo_indptr,
+    const int32_t *kv_indptr, const int32_t *kv_indices, int batch, int num_q_tokens, int hq,
+    int hkv, int lq, int lv, int64_t ke_st, int64_t ke_sh, int64_t ve_st, int64_t ve_sh,
+    int64_t kb_ss, int64_t kb_sh, int64_t vb_ss, int64_t vb_sh, int64_t num_slots,
+    float sm_scale, float logit_cap, int sliding_window, float *lse_out, void *workspace,
+    size_t workspace_bytes, void *stream) {
+  AttnArgs a{};
+  bool done;
+  int rc = two_stage_args(a, q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffer,
+                          qo_indptr, kv_indptr, kv_indices, batch, num_q_tokens, hq, hkv, lq, lv,
+                          ke_st, ke_sh, ve_st, ve_sh, kb_ss, kb_sh, vb_ss, vb_sh, num_slots,
+                          sm_scale, logit_cap, sliding_window, nullptr, nullptr, nullptr,
+                          lse_out, &done);
+  if (rc != PKX_OK || done) return rc;
+  const SplitLayout L = split_layout(batch, num_q_tokens, hq, hkv, lq, lv);
+  if (!workspace || workspace_bytes < L.total)
+    return set_error(PKX_EWORKSPACE, "workspace of %zu bytes given, %zu needed", workspace_bytes,
+                     L.total);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return set_error(PKX_EINVAL, "workspace must be 256-byte aligned");
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  void *o_paged = ws + L.o_paged;
+  float *lse_paged = reinterpret_cast<float *>(ws + L.lse_paged);
+  float *lse_ragged = reinterpret_cast<float *>(ws + L.lse_ragged);
+  a.workspace = ws + L.attn;
+  a.workspace_bytes = L.o_paged - L.attn;
+  a.stream = static_cast<cudaStream_t>(stream);
+  // ragged pass: extend keys only, causal, straight into o_extend
+  a.key_set = kExtendKeys;
+  a.lse = lse_ragged;
+  if ((rc = launch_attention(a)) != PKX_OK) return rc;
+  // paged pass: prefix keys only, all visible, into the workspace
+  a.key_set = kPrefixKeys;
+  a.keep_status = 1;
+  a.o = o_paged;
+  a.lse = lse_paged;
+  if ((rc = launch_attention(a)) != PKX_OK) return rc;
+  // merge the two states in place
+  return launch_merge_state(o_extend, lse_ragged, o_paged, lse_paged, o_extend, lse_out,
+                            num_q_tokens, hq, lv, a.stream);
 }
 
 int pkx_extend_attention_fwd_unified(const void *q, void *o, const void *k_buffer,

@@ -59,6 +59,8 @@ struct SchedParams {
   int bn;        // keys per K/V tile
   int q_tile_tok;  // query tokens of one Q tile
   int no_causal;   // a custom mask replaces the causal mask: blocks see every key
+  int key_set;     // two-stage form only: kAllKeys, kPrefixKeys or kExtendKeys
+  int keep_status; // leave the status word as an earlier pass left it
   int n_dsplit;  // units per (block, split): value-dim slices (1, or 4 for MLA)
   int unit_target, qb_max, unit_max, comb_max, slot_max;
   int32_t *seq;  // 8 arrays of batch+1 ints
@@ -99,6 +101,11 @@ __device__ SeqDims seq_dims(const SchedParams &p, int b) {
   if (p.mode == kTwoStage) {
     d.P = p.kv_indptr[b + 1] - p.kv_indptr[b];
     d.T = d.P + d.E;
+    // One half of the ragged + paged split: the prefix keys alone (every
+    // one visible to every extend query), or the extend keys alone with
+    // causal positions counted from the first extend token.
+    if (p.key_set == kPrefixKeys) d.T = d.P;
+    else if (p.key_set == kExtendKeys) { d.P = 0; d.T = d.E; }
   } else {
     d.T = p.kv_indptr[b + 1] - p.kv_indptr[b];
     d.P = p.prefix_lens[b];
@@ -205,7 +212,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   int32_t *qboff = p.seq + 1 * (B + 1); // [B]  first query block of sequence
 
   if (tid == 0) {
-    p.hdr->status = 0;
+    if (!p.keep_status) p.hdr->status = 0;
     p.hdr->next_unit = 0;
   }
   __syncthreads();
@@ -1374,6 +1381,8 @@ int launch_attention(const AttnArgs &a) {
   sp.bn = mla ? MlaCfg<0>::BN : kBlockN;
   sp.q_tile_tok = tok > 0 ? tok : 1;
   sp.no_causal = a.custom_mask != nullptr;
+  sp.key_set = a.mode == kTwoStage ? a.key_set : kAllKeys;
+  sp.keep_status = a.keep_status;
   sp.n_dsplit = mla ? MlaCfg<0>::LV / MlaCfg<0>::DVS : 1;
   sp.window = a.window;
   sp.num_q_tokens = nq;

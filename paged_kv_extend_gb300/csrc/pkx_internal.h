@@ -20,6 +20,14 @@ enum KeyMode : int {
   kDecode = 2,    // every key via int32 kv_indices, query at position T-1
 };
 
+// Which keys a two-stage pass attends to (the ragged + paged split runs the
+// extend keys and the prefix keys as two passes and merges them).
+enum KeySet : int {
+  kAllKeys = 0,
+  kPrefixKeys = 1,  // prefix only: every prefix key visible to every extend query
+  kExtendKeys = 2,  // extend only: causal over the extend keys
+};
+
 // Rows of one query tile (tcgen05 M) and keys of one KV tile.
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
@@ -105,6 +113,8 @@ struct AttnArgs {
   const uint8_t *custom_mask;   // nullable: replaces the causal mask
   const int32_t *mask_indptr;   // [batch+1] offsets into custom_mask
   const float *sinks;           // nullable [hq] sink logits
+  int key_set = kAllKeys;       // two-stage form: which keys this pass sees
+  int keep_status = 0;          // a later pass of one call keeps the status word
   void *workspace;
   size_t workspace_bytes;
   cudaStream_t stream;

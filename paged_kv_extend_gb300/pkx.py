@@ -50,6 +50,10 @@ _SIGS = {
         _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
         _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _p,
         _p, _p, _sz, _p]),
+    "pkx_ragged_paged_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "pkx_extend_attention_fwd_ragged_paged": (_i, [
+        _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
+        _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _sz, _p]),
     "pkx_extend_attention_fwd_unified": (_i, [
         _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
         _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _p, _p, _p, _sz, _p]),
@@ -196,6 +200,44 @@ def extend_attention_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buf
         ke[0], ke[1], ve[0], ve[1], kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0],
         float(sm_scale or 0.0), float(logit_cap or 0.0), int(sliding_window),
         *_mask_sinks(custom_mask, mask_indptr, sinks), _ptr(lse),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(q_extend.device)))
+    return ws
+
+
+def ragged_paged_workspace_size(batch, num_q_tokens, hq, hkv, lq, lv) -> int:
+    return int(load_library().pkx_ragged_paged_workspace_size(batch, num_q_tokens, hq, hkv,
+                                                               lq, lv))
+
+
+def extend_attention_fwd_ragged_paged(q_extend, k_extend, v_extend, o_extend, k_buffer,
+                                      v_buffer, qo_indptr, kv_indptr, kv_indices, sm_scale=None,
+                                      logit_cap=0.0, sliding_window=-1, lse=None,
+                                      workspace=None):
+    """Extend attention as a ragged pass over the extend keys, a paged pass
+    over the prefix keys and merge_state of the two
+    (pkx_extend_attention_fwd_ragged_paged); arguments as
+    extend_attention_fwd without mask and sinks.  Returns the workspace."""
+    lib = load_library()
+    n, hq, lq = q_extend.shape
+    hkv = k_buffer.shape[1]
+    lv = v_buffer.shape[2]
+    batch = qo_indptr.numel() - 1
+    ke = _rows(k_extend, "k_extend")
+    ve = _rows(v_extend, "v_extend")
+    kb = _rows(k_buffer, "k_buffer")
+    vb = _rows(v_buffer, "v_buffer")
+    for t, nm in ((q_extend, "q_extend"), (o_extend, "o_extend")):
+        if not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{nm} must be contiguous bf16")
+    _i32(qo_indptr, "qo_indptr"), _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
+    ws = _workspace(workspace, ragged_paged_workspace_size(batch, n, hq, hkv, lq, lv),
+                    q_extend.device)
+    _check(lib.pkx_extend_attention_fwd_ragged_paged(
+        _ptr(q_extend), _ptr(k_extend), _ptr(v_extend), _ptr(o_extend), _ptr(k_buffer),
+        _ptr(v_buffer), _ptr(qo_indptr), _ptr(kv_indptr),
+        _ptr(kv_indices) if kv_indices.numel() else None, batch, n, hq, hkv, lq, lv,
+        ke[0], ke[1], ve[0], ve[1], kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0],
+        float(sm_scale or 0.0), float(logit_cap or 0.0), int(sliding_window), _ptr(lse),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(q_extend.device)))
     return ws
 

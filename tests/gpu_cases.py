@@ -48,6 +48,16 @@ class DeviceWorkload:
             s.sliding_window if window is None else window, lse=lse, **_dev(mask_sinks))
         return o, lse, ws
 
+    def ragged_paged(self, cap=None, window=None):
+        s = self.wl.spec
+        o, lse = self.out()
+        ws = pkx.extend_attention_fwd_ragged_paged(
+            self.q, self.k_extend, self.v_extend, o, self.k_buffer, self.v_buffer,
+            self.qo_indptr, self.kv_indptr, self.kv_indices, self.wl.sm_scale,
+            s.logit_cap if cap is None else cap,
+            s.sliding_window if window is None else window, lse=lse)
+        return o, lse, ws
+
     def unified(self, cap=None, window=None, scale=None, **mask_sinks):
         s = self.wl.spec
         uptr, uidx, plen = pkx.build_unified_kv_indices(

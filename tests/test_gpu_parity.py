@@ -168,6 +168,52 @@ def test_extend_small_vs_oracle(lq, hq, hkv, prefix, extend, cap, window):
     assert_close(uo, ul, ro, rl, "unified")
 
 
+@pytest.mark.parametrize("lq,hq,hkv,prefix,extend,cap,window", SMALL)
+def test_ragged_paged_split_vs_oracle(lq, hq, hkv, prefix, extend, cap, window):
+    """The ragged + paged + merge_state split gives the two-stage result
+    (the oracle's) within the same bar, including sequences without prefix
+    (their paged pass is empty) and windows that cut into the prefix."""
+    spec = W.small_spec(batch=len(prefix), hq=hq, hkv=hkv, lq=lq, lv=lq, prefix=prefix,
+                        extend=extend, logit_cap=cap, sliding_window=window,
+                        seed=sum(prefix) + 3 * sum(extend) + hq)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.ragged_paged()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_extend(wl)
+    assert_close(o, lse, ro, rl, f"ragged+paged {lq} {hq}/{hkv}")
+
+
+def test_ragged_paged_split_mla():
+    spec = W.small_spec(batch=3, hq=16, hkv=1, lq=576, lv=512, prefix=[300, 0, 129],
+                        extend=[64, 130, 1], sm_scale=1.0 / math.sqrt(192.0), std=0.5,
+                        v_aliases_k=True, seed=91)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.ragged_paged()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_extend(wl)
+    assert_close(o, lse, ro, rl, "ragged+paged mla")
+
+
+def test_ragged_paged_split_full_size_sampled_rows():
+    """The Llama-3-8B-shaped batch (8353 extend tokens, past the pages' 4096
+    threshold for the split) through the split path, sampled rows."""
+    wl = W.draw(W.SPECS["llama3_8b"])
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.ragged_paged()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    rows = sample_rows(wl.n_q_tokens, wl.spec.hq, 3072, seed=78)
+    ro, rl = oracle_extend(wl, rows=rows)
+    go = o.view(-1, o.shape[-1])[rows.to(DEV)]
+    gl = lse.view(-1)[rows.to(DEV)]
+    assert_close(go, gl, ro, rl, "ragged+paged llama3_8b")
+    assert torch.isfinite(o.float()).all()
+
+
 @pytest.mark.parametrize("scale,cap,window", [
     (-0.09, 0.0, -1),   # negative scale: the row max is scale * min(q.k)
     (0.0, 0.0, -1),     # uniform weights over the visible keys
