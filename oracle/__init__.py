@@ -53,15 +53,15 @@ def _configure(lib):
     lib.oracle_num_threads.restype = _i
     lib.oracle_extend_attention.restype = _i
     lib.oracle_extend_attention.argtypes = [
-        _p, _p, _l, _l, _p, _l, _l, _p, _l, _l, _p, _l, _l,
+        _p, _p, _l, _l, _p, _l, _l, _p, _l, _l, _p, _l, _l, _i, _d, _d,
         _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _l, _p, _p, _p, _p, _l, _p, _p]
     lib.oracle_extend_attention_unified.restype = _i
     lib.oracle_extend_attention_unified.argtypes = [
-        _p, _p, _l, _l, _p, _l, _l, _p, _p, _p, _p,
+        _p, _p, _l, _l, _p, _l, _l, _i, _d, _d, _p, _p, _p, _p,
         _i, _i, _i, _i, _i, _d, _d, _l, _p, _p, _p, _p, _l, _p, _p]
     lib.oracle_decode_attention.restype = _i
     lib.oracle_decode_attention.argtypes = [
-        _p, _p, _l, _l, _p, _l, _l, _p, _p,
+        _p, _p, _l, _l, _p, _l, _l, _i, _d, _d, _p, _p,
         _i, _i, _i, _i, _i, _d, _d, _l, _p, _p]
     lib.oracle_merge_state.restype = None
     lib.oracle_merge_state.argtypes = [_p, _p, _p, _p, _l, _i, _i, _p, _p]
@@ -70,6 +70,14 @@ def _configure(lib):
         _p, _p, _p, _p, _p, _i, _p, _p, _p]
     lib.oracle_create_kv_indices.restype = None
     lib.oracle_create_kv_indices.argtypes = [_p, _l, _p, _p, _p, _i, _p, _p]
+    lib.oracle_fp8_value.restype = _d
+    lib.oracle_fp8_value.argtypes = [ctypes.c_uint8, _i]
+    lib.oracle_fp8_code.restype = ctypes.c_uint8
+    lib.oracle_fp8_code.argtypes = [ctypes.c_float, _i]
+    lib.oracle_set_kv_buffer_fp8.restype = None
+    lib.oracle_set_kv_buffer_fp8.argtypes = [
+        _p, _l, _l, _p, _l, _l, _p, _l, _i, _i, _i, ctypes.c_float, ctypes.c_float, _i,
+        _p, _l, _l, _p, _l, _l]
     lib.oracle_set_kv_buffer.restype = None
     lib.oracle_set_kv_buffer.argtypes = [
         _p, _l, _l, _p, _l, _l, _p, _l, _i, _i, _i, _p, _l, _l, _p, _l, _l]
@@ -162,6 +170,29 @@ def _mask_args(custom_mask, mask_indptr, sinks, hq):
     return cm, mi, sk
 
 
+# pool element formats (oracle.c KV_BF16 / KV_E4M3 / KV_E5M2)
+KV_BF16, KV_E4M3, KV_E5M2 = 0, 1, 2
+_FP8 = {KV_E4M3: torch.float8_e4m3fn, KV_E5M2: torch.float8_e5m2}
+
+
+def _pool(t: torch.Tensor):
+    """(element view for the C side, format) of a bf16 or fp8 pool tensor."""
+    if t.dtype == torch.bfloat16:
+        return _bf16_bits(t), KV_BF16
+    for fmt, dt in _FP8.items():
+        if t.dtype == dt:
+            return t.detach().cpu().view(torch.uint8), fmt
+    raise ValueError(f"pool dtype {t.dtype} is neither bf16 nor fp8")
+
+
+def _pools(k_buffer, v_buffer):
+    kb, fk = _pool(k_buffer)
+    vb, fv = _pool(v_buffer)
+    if fk != fv:
+        raise ValueError("k_buffer and v_buffer must share one format")
+    return kb, vb, fk
+
+
 def _opt(t):
     return _ptr(t) if t is not None and t.numel() else None
 
@@ -170,7 +201,7 @@ def _opt(t):
 def extend_attention(q_extend, k_extend, v_extend, k_buffer, v_buffer,
                      qo_indptr, kv_indptr, kv_indices, sm_scale, logit_cap=0.0,
                      sliding_window=-1, rows=None, custom_mask=None, mask_indptr=None,
-                     sinks=None):
+                     sinks=None, k_scale=1.0, v_scale=1.0):
     """Two-stage extend attention (sglang extend_attention.py,
     extend_attention_fwd): prefix K/V through kv_indptr/kv_indices into the
     pool, extend K/V contiguous at qo_indptr.
@@ -182,7 +213,10 @@ def extend_attention(q_extend, k_extend, v_extend, k_buffer, v_buffer,
 
     q_extend [N, Hq, Lq] bf16; k_extend [N, Hkv, Lq]; v_extend [N, Hkv, Lv];
     k_buffer [S, Hkv, Lq]; v_buffer [S, Hkv, Lv] (views with a contiguous last
-    dim; v may alias k).  sm_scale <= 0 means 1/sqrt(Lq).
+    dim; v may alias k).  sm_scale <= 0 means 1/sqrt(Lq).  The pool may be
+    fp8 (torch.float8_e4m3fn / float8_e5m2): its keys then read code *
+    k_scale and its values code * v_scale (sglang flashinfer_backend.py,
+    forward with k_scale / v_scale).
     Returns (o [N, Hq, Lv] float64, lse [N, Hq] float64), or for ``rows`` (a
     list of token*Hq + head) o [R, Lv] and lse [R].
     """
@@ -194,7 +228,7 @@ def extend_attention(q_extend, k_extend, v_extend, k_buffer, v_buffer,
         sm_scale = 1.0 / (lq ** 0.5)
     q = _bf16_bits(q_extend).contiguous()
     ke, ve = _bf16_bits(k_extend), _bf16_bits(v_extend)
-    kb, vb = _bf16_bits(k_buffer), _bf16_bits(v_buffer)
+    kb, vb, fmt = _pools(k_buffer, v_buffer)
     qo, kvp, kvi = _i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices)
     batch = qo.numel() - 1
     cm, mi, sk = _mask_args(custom_mask, mask_indptr, sinks, hq)
@@ -205,6 +239,7 @@ def extend_attention(q_extend, k_extend, v_extend, k_buffer, v_buffer,
     rc = lib.oracle_extend_attention(
         _ptr(q), _ptr(ke), *_row_strides(ke), _ptr(ve), *_row_strides(ve),
         _ptr(kb), *_row_strides(kb), _ptr(vb), *_row_strides(vb),
+        fmt, float(k_scale), float(v_scale),
         _ptr(qo), _ptr(kvp), _ptr(kvi) if kvi.numel() else None,
         batch, hq, hkv, lq, lv, float(sm_scale), float(logit_cap),
         int(sliding_window), _opt(cm), _opt(mi), _opt(sk),
@@ -219,7 +254,7 @@ def extend_attention(q_extend, k_extend, v_extend, k_buffer, v_buffer,
 def extend_attention_unified(q, k_buffer, v_buffer, qo_indptr, kv_indptr,
                              kv_indices, prefix_lens, sm_scale, logit_cap=0.0,
                              sliding_window=-1, rows=None, custom_mask=None,
-                             mask_indptr=None, sinks=None):
+                             mask_indptr=None, sinks=None, k_scale=1.0, v_scale=1.0):
     """Unified extend attention (sglang extend_attention.py,
     extend_attention_fwd_unified): all keys through the unified int64
     kv_indices; the first prefix_lens[b] keys of sequence b are its prefix.
@@ -231,7 +266,7 @@ def extend_attention_unified(q, k_buffer, v_buffer, qo_indptr, kv_indptr,
     if sm_scale is None or sm_scale <= 0:
         sm_scale = 1.0 / (lq ** 0.5)
     qb = _bf16_bits(q).contiguous()
-    kb, vb = _bf16_bits(k_buffer), _bf16_bits(v_buffer)
+    kb, vb, fmt = _pools(k_buffer, v_buffer)
     qo, kvp, kvi, pl = _i32(qo_indptr), _i32(kv_indptr), _i64(kv_indices), _i32(prefix_lens)
     batch = qo.numel() - 1
     cm, mi, sk = _mask_args(custom_mask, mask_indptr, sinks, hq)
@@ -241,6 +276,7 @@ def extend_attention_unified(q, k_buffer, v_buffer, qo_indptr, kv_indptr,
     lse = torch.empty(count, dtype=torch.float64)
     rc = lib.oracle_extend_attention_unified(
         _ptr(qb), _ptr(kb), *_row_strides(kb), _ptr(vb), *_row_strides(vb),
+        fmt, float(k_scale), float(v_scale),
         _ptr(qo), _ptr(kvp), _ptr(kvi) if kvi.numel() else None, _ptr(pl),
         batch, hq, hkv, lq, lv, float(sm_scale), float(logit_cap),
         int(sliding_window), _opt(cm), _opt(mi), _opt(sk),
@@ -253,7 +289,7 @@ def extend_attention_unified(q, k_buffer, v_buffer, qo_indptr, kv_indptr,
 
 
 def decode_attention(q, k_buffer, v_buffer, kv_indptr, kv_indices, sm_scale,
-                     logit_cap=0.0, sliding_window=-1):
+                     logit_cap=0.0, sliding_window=-1, k_scale=1.0, v_scale=1.0):
     """Decode attention (sglang flashinfer_backend.py, forward_decode): one
     query per sequence over all of its pooled keys.
     q [B, Hq, Lq] bf16 -> (o [B, Hq, Lv] float64, lse [B, Hq] float64)."""
@@ -264,13 +300,14 @@ def decode_attention(q, k_buffer, v_buffer, kv_indptr, kv_indices, sm_scale,
     if sm_scale is None or sm_scale <= 0:
         sm_scale = 1.0 / (lq ** 0.5)
     qb = _bf16_bits(q).contiguous()
-    kb, vb = _bf16_bits(k_buffer), _bf16_bits(v_buffer)
+    kb, vb, fmt = _pools(k_buffer, v_buffer)
     kvp, kvi = _i32(kv_indptr), _i32(kv_indices)
     o = torch.empty(b, hq, lv, dtype=torch.float64)
     lse = torch.empty(b, hq, dtype=torch.float64)
     rc = lib.oracle_decode_attention(
         _ptr(qb), _ptr(kb), *_row_strides(kb), _ptr(vb), *_row_strides(vb),
-        _ptr(kvp), _ptr(kvi) if kvi.numel() else None, b, hq, hkv, lq, lv,
+        fmt, float(k_scale), float(v_scale), _ptr(kvp),
+        _ptr(kvi) if kvi.numel() else None, b, hq, hkv, lq, lv,
         float(sm_scale), float(logit_cap), int(sliding_window), _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_decode_attention: bad arguments")
@@ -355,3 +392,37 @@ def set_kv_buffer(k_buffer, v_buffer, cache_loc, k, v):
         _ptr(loc) if n else None, n, hkv, lk, lv,
         _ptr(kb), *_row_strides(kb), _ptr(vb), *_row_strides(vb))
     return kb.view(torch.bfloat16), vb.view(torch.bfloat16)
+
+
+def fp8_value(code: int, fmt: int) -> float:
+    """The value of one fp8 code (fmt KV_E4M3 or KV_E5M2)."""
+    return float(_load().oracle_fp8_value(int(code) & 0xFF, int(fmt)))
+
+
+def fp8_code(x: float, fmt: int) -> int:
+    """The fp8 code of an fp32 value: nearest, ties to even, saturating."""
+    return int(_load().oracle_fp8_code(float(x), int(fmt)))
+
+
+def set_kv_buffer_fp8(k_buffer, v_buffer, cache_loc, k, v, k_scale, v_scale):
+    """KV write into an fp8 pool (sglang flashinfer_backend.py,
+    set_kv_buffer(layer, cache_loc, k, v, k_scale, v_scale) with an fp8 KV
+    cache): every element of k[t] / v[t] divided by its scale in fp32 and
+    stored as its nearest fp8 code at slot cache_loc[t].  Pools are
+    torch.float8_e4m3fn or float8_e5m2; returns new (k_buffer, v_buffer)."""
+    lib = _load()
+    kb0, vb0, fmt = _pools(k_buffer, v_buffer)
+    if fmt == KV_BF16:
+        raise ValueError("set_kv_buffer_fp8 needs an fp8 pool")
+    kb, vb = kb0.clone().contiguous(), vb0.clone().contiguous()
+    kk = _bf16_bits(k).contiguous()
+    vv = _bf16_bits(v).contiguous() if v is not None else None
+    loc = _i64(cache_loc)
+    n, hkv, lk = kk.shape
+    lv = vv.shape[2] if vv is not None else 0
+    lib.oracle_set_kv_buffer_fp8(
+        _ptr(kk), *_row_strides(kk), _ptr(vv) if vv is not None else None,
+        *(_row_strides(vv) if vv is not None else (0, 0)), _ptr(loc) if n else None, n, hkv,
+        lk, lv, float(k_scale), float(v_scale), fmt, _ptr(kb), *_row_strides(kb), _ptr(vb),
+        *_row_strides(vb))
+    return kb.view(_FP8[fmt]), vb.view(_FP8[fmt])

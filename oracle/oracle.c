@@ -2,7 +2,8 @@
  * oracle.c -- plain, slow, float64 CPU restatement of extend attention over a
  * page-size-1 KV pool, decode attention, merge_state, the unified KV-index
  * build, the KV-index gather from the request-to-token table and the KV
- * write into the pool.
+ * write into the pool, for bf16 pools and for fp8 (e4m3 / e5m2) pools with
+ * per-tensor k_scale / v_scale.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
  * call this file.  It exists so that tests, the smoke check and the CPU
@@ -63,6 +64,96 @@ static double bf16_to_double(uint16_t bits)
     return (double)f;
 }
 
+/*
+ * fp8 codes of the pool ([FI] kv_cache_dtype float8_e4m3fn / float8_e5m2,
+ * with k_scale / v_scale): the value of a code, from the formats'
+ * definitions.
+ *   e4m3fn: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is
+ *           subnormal (m/8 * 2^-6); S.1111.111 is NaN; no infinities.
+ *   e5m2:   sign, 5 exponent bits (bias 15), 2 mantissa bits; exponent 0 is
+ *           subnormal (m/4 * 2^-14); exponent 31 is inf (m = 0) or NaN.
+ */
+enum { KV_BF16 = 0, KV_E4M3 = 1, KV_E5M2 = 2 };
+
+double oracle_fp8_value(uint8_t code, int fmt)
+{
+    int sign = code >> 7;
+    int e, m;
+    double v;
+    if (fmt == KV_E4M3) {
+        e = (code >> 3) & 15;
+        m = code & 7;
+        if (e == 15 && m == 7)
+            return NAN;
+        v = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    } else {
+        e = (code >> 2) & 31;
+        m = code & 3;
+        if (e == 31)
+            return m == 0 ? (sign ? -INFINITY : INFINITY) : NAN;
+        v = e == 0 ? ldexp(m / 4.0, -14) : ldexp(1.0 + m / 4.0, e - 15);
+    }
+    return sign ? -v : v;
+}
+
+/*
+ * The code of an fp32 value: the nearest finite code, ties to the code
+ * with an even mantissa (round to nearest even), values past the largest
+ * finite magnitude saturate to it (448 for e4m3, 57344 for e5m2).  The sign
+ * is kept, so a negative value that rounds to zero gives -0.  Written as a
+ * search over the 128 non-negative codes.
+ */
+uint8_t oracle_fp8_code(float x, int fmt)
+{
+    int neg = signbit(x) != 0;
+    double a = fabs((double)x);
+    int best = 0;
+    double best_d = INFINITY;
+    /* past the largest finite code: that code (the distances below would
+     * lose their precision there) */
+    int top = fmt == KV_E4M3 ? 0x7e : 0x7b;
+    if (a >= oracle_fp8_value((uint8_t)top, fmt))
+        return (uint8_t)(top | (neg ? 0x80 : 0));
+    for (int c = 0; c < 128; ++c) {
+        double v = oracle_fp8_value((uint8_t)c, fmt);
+        if (isnan(v) || isinf(v))
+            continue;
+        double d = fabs(v - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(best | (neg ? 0x80 : 0));
+}
+
+/* One key or value row: bf16 elements, or fp8 codes times the row's scale. */
+typedef struct {
+    const void *p;
+    int fmt;
+    double scale;
+} kv_row;
+
+static double row_elem(kv_row r, int d)
+{
+    if (r.fmt == KV_BF16)
+        return bf16_to_double(((const uint16_t *)r.p)[d]);
+    return oracle_fp8_value(((const uint8_t *)r.p)[d], r.fmt) * r.scale;
+}
+
+/* Row (slot, h) of a pool whose element size follows its format. */
+static kv_row pool_row(const void *buf, int fmt, double scale, long slot,
+                       long ss, long hs, int hk)
+{
+    kv_row r;
+    long off = slot * ss + (long)hk * hs;
+    r.p = fmt == KV_BF16 ? (const void *)((const uint16_t *)buf + off)
+                         : (const void *)((const uint8_t *)buf + off);
+    r.fmt = fmt;
+    r.scale = scale;
+    return r;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP
@@ -82,8 +173,7 @@ int oracle_num_threads(void)
  * lse = -inf.
  */
 static void attend_one_query(const uint16_t *q, int lq, int lv, long n_keys,
-                             const uint16_t *const *krow,
-                             const uint16_t *const *vrow, long qpos,
+                             const kv_row *krow, const kv_row *vrow, long qpos,
                              long window, double sm_scale, double logit_cap,
                              const uint8_t *mask_row, const double *sink,
                              double *s, double *o, double *lse)
@@ -99,7 +189,7 @@ static void attend_one_query(const uint16_t *q, int lq, int lv, long n_keys,
         }
         double dot = 0.0;
         for (int d = 0; d < lq; ++d)
-            dot += bf16_to_double(q[d]) * bf16_to_double(krow[j][d]);
+            dot += bf16_to_double(q[d]) * row_elem(krow[j], d);
         double sj = sm_scale * dot;
         if (logit_cap > 0.0)
             sj = logit_cap * tanh(sj / logit_cap);
@@ -122,7 +212,7 @@ static void attend_one_query(const uint16_t *q, int lq, int lv, long n_keys,
         double p = exp(s[j] - m);
         l += p;
         for (int d = 0; d < lv; ++d)
-            o[d] += p * bf16_to_double(vrow[j][d]);
+            o[d] += p * row_elem(vrow[j], d);
     }
     if (sink)
         l += exp(*sink - m);
@@ -153,6 +243,9 @@ static int sequence_of_token(const int32_t *qo_indptr, int batch, long t)
  *   v_extend row (t, h) at v_ext + t*v_ext_ts + h*v_ext_hs  (lv elements)
  *   k_buffer row (slot, h) at k_buf + slot*k_buf_ss + h*k_buf_hs
  *   v_buffer row (slot, h) at v_buf + slot*v_buf_ss + h*v_buf_hs
+ * kv_fmt: the pool's element format (KV_BF16, or fp8 KV_E4M3 / KV_E5M2 whose
+ *   keys read code * k_scale and values code * v_scale; [FI] forward with
+ *   k_scale / v_scale); k_extend / v_extend are always bf16.
  * rows: NULL -> every (token, head) and o_out is [n_tokens, hq, lv],
  *       lse_out [n_tokens, hq];
  *       else rows[r] = token*hq + head for r < n_rows, and o_out is
@@ -162,8 +255,9 @@ static int sequence_of_token(const int32_t *qo_indptr, int batch, long t)
 int oracle_extend_attention(
     const uint16_t *q_extend, const uint16_t *k_ext, long k_ext_ts,
     long k_ext_hs, const uint16_t *v_ext, long v_ext_ts, long v_ext_hs,
-    const uint16_t *k_buf, long k_buf_ss, long k_buf_hs, const uint16_t *v_buf,
-    long v_buf_ss, long v_buf_hs, const int32_t *qo_indptr,
+    const void *k_buf, long k_buf_ss, long k_buf_hs, const void *v_buf,
+    long v_buf_ss, long v_buf_hs, int kv_fmt, double k_scale, double v_scale,
+    const int32_t *qo_indptr,
     const int32_t *kv_indptr, const int32_t *kv_indices, int batch, int hq,
     int hkv, int lq, int lv, double sm_scale, double logit_cap,
     long sliding_window, const uint8_t *custom_mask, const int32_t *mask_indptr,
@@ -191,20 +285,20 @@ int oracle_extend_attention(
         long p_len = kv_indptr[b + 1] - kv_indptr[b];
         long e_len = qo_indptr[b + 1] - qo_indptr[b];
         long n_keys = p_len + e_len;
-        const uint16_t **krow = malloc(sizeof(*krow) * (size_t)(n_keys + 1));
-        const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)(n_keys + 1));
+        kv_row *krow = malloc(sizeof(*krow) * (size_t)(n_keys + 1));
+        kv_row *vrow = malloc(sizeof(*vrow) * (size_t)(n_keys + 1));
         double *s = malloc(sizeof(double) * (size_t)(n_keys + 1));
         /* Key j of sequence b: prefix keys through the page table, then the
          * sequence's own extend tokens. */
         for (long j = 0; j < p_len; ++j) {
             long slot = kv_indices[kv_indptr[b] + j];
-            krow[j] = k_buf + slot * k_buf_ss + (long)hk * k_buf_hs;
-            vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;
+            krow[j] = pool_row(k_buf, kv_fmt, k_scale, slot, k_buf_ss, k_buf_hs, hk);
+            vrow[j] = pool_row(v_buf, kv_fmt, v_scale, slot, v_buf_ss, v_buf_hs, hk);
         }
         for (long e = 0; e < e_len; ++e) {
             long te = qo_indptr[b] + e;
-            krow[p_len + e] = k_ext + te * k_ext_ts + (long)hk * k_ext_hs;
-            vrow[p_len + e] = v_ext + te * v_ext_ts + (long)hk * v_ext_hs;
+            krow[p_len + e] = pool_row(k_ext, KV_BF16, 1.0, te, k_ext_ts, k_ext_hs, hk);
+            vrow[p_len + e] = pool_row(v_ext, KV_BF16, 1.0, te, v_ext_ts, v_ext_hs, hk);
         }
         long i = t - qo_indptr[b];
         const uint8_t *mask_row =
@@ -230,10 +324,10 @@ int oracle_extend_attention(
  * oracle_extend_attention.
  */
 int oracle_extend_attention_unified(
-    const uint16_t *q, const uint16_t *k_buf, long k_buf_ss, long k_buf_hs,
-    const uint16_t *v_buf, long v_buf_ss, long v_buf_hs,
-    const int32_t *qo_indptr, const int32_t *kv_indptr,
-    const int64_t *kv_indices, const int32_t *prefix_lens, int batch, int hq,
+    const uint16_t *q, const void *k_buf, long k_buf_ss, long k_buf_hs,
+    const void *v_buf, long v_buf_ss, long v_buf_hs, int kv_fmt,
+    double k_scale, double v_scale, const int32_t *qo_indptr,
+    const int32_t *kv_indptr, const int64_t *kv_indices, const int32_t *prefix_lens, int batch, int hq,
     int hkv, int lq, int lv, double sm_scale, double logit_cap,
     long sliding_window, const uint8_t *custom_mask, const int32_t *mask_indptr,
     const double *sinks, const int64_t *rows, long n_rows, double *o_out,
@@ -258,13 +352,13 @@ int oracle_extend_attention_unified(
         }
         int hk = h / group;
         long n_keys = kv_indptr[b + 1] - kv_indptr[b];
-        const uint16_t **krow = malloc(sizeof(*krow) * (size_t)(n_keys + 1));
-        const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)(n_keys + 1));
+        kv_row *krow = malloc(sizeof(*krow) * (size_t)(n_keys + 1));
+        kv_row *vrow = malloc(sizeof(*vrow) * (size_t)(n_keys + 1));
         double *s = malloc(sizeof(double) * (size_t)(n_keys + 1));
         for (long j = 0; j < n_keys; ++j) {
             long slot = (long)kv_indices[kv_indptr[b] + j];
-            krow[j] = k_buf + slot * k_buf_ss + (long)hk * k_buf_hs;
-            vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;
+            krow[j] = pool_row(k_buf, kv_fmt, k_scale, slot, k_buf_ss, k_buf_hs, hk);
+            vrow[j] = pool_row(v_buf, kv_fmt, v_scale, slot, v_buf_ss, v_buf_hs, hk);
         }
         long i = t - qo_indptr[b];
         const uint8_t *mask_row =
@@ -289,9 +383,10 @@ int oracle_extend_attention_unified(
  * q [batch, hq, lq] contiguous; o_out [batch, hq, lv]; lse_out [batch, hq].
  * A sequence with T_b = 0 gets o = 0, lse = -inf.
  */
-int oracle_decode_attention(const uint16_t *q, const uint16_t *k_buf,
-                            long k_buf_ss, long k_buf_hs, const uint16_t *v_buf,
-                            long v_buf_ss, long v_buf_hs,
+int oracle_decode_attention(const uint16_t *q, const void *k_buf,
+                            long k_buf_ss, long k_buf_hs, const void *v_buf,
+                            long v_buf_ss, long v_buf_hs, int kv_fmt,
+                            double k_scale, double v_scale,
                             const int32_t *kv_indptr, const int32_t *kv_indices,
                             int batch, int hq, int hkv, int lq, int lv,
                             double sm_scale, double logit_cap,
@@ -309,13 +404,13 @@ int oracle_decode_attention(const uint16_t *q, const uint16_t *k_buf,
         int h = (int)(r % hq);
         int hk = h / group;
         long n_keys = kv_indptr[b + 1] - kv_indptr[b];
-        const uint16_t **krow = malloc(sizeof(*krow) * (size_t)(n_keys + 1));
-        const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)(n_keys + 1));
+        kv_row *krow = malloc(sizeof(*krow) * (size_t)(n_keys + 1));
+        kv_row *vrow = malloc(sizeof(*vrow) * (size_t)(n_keys + 1));
         double *s = malloc(sizeof(double) * (size_t)(n_keys + 1));
         for (long j = 0; j < n_keys; ++j) {
             long slot = kv_indices[kv_indptr[b] + j];
-            krow[j] = k_buf + slot * k_buf_ss + (long)hk * k_buf_hs;
-            vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;
+            krow[j] = pool_row(k_buf, kv_fmt, k_scale, slot, k_buf_ss, k_buf_hs, hk);
+            vrow[j] = pool_row(v_buf, kv_fmt, v_scale, slot, v_buf_ss, v_buf_hs, hk);
         }
         attend_one_query(q + r * (long)lq, lq, lv, n_keys, krow, vrow,
                          n_keys - 1, sliding_window, sm_scale, logit_cap, NULL,
@@ -451,6 +546,39 @@ void oracle_set_kv_buffer(
                 for (int d = 0; d < lv; ++d)
                     v_buf[slot * v_buf_ss + (long)h * v_buf_hs + d] =
                         v[t * v_ts + (long)h * v_hs + d];
+        }
+    }
+}
+
+/*
+ * KV write into an fp8 pool ([FI] set_kv_buffer(layer, cache_loc, k, v,
+ * k_scale, v_scale) with kv_cache_dtype fp8): each element is divided by its
+ * scale in fp32 and stored as the nearest fp8 code (oracle_fp8_code):
+ *   k_buf[cache_loc[t], h, d] = code((float)k[t, h, d] / (float)k_scale)
+ *   v_buf[cache_loc[t], h, d] = code((float)v[t, h, d] / (float)v_scale)
+ * v may be NULL (K-only pool).  Slots not in cache_loc keep their codes.
+ */
+void oracle_set_kv_buffer_fp8(
+    const uint16_t *k, long k_ts, long k_hs, const uint16_t *v, long v_ts,
+    long v_hs, const int64_t *cache_loc, long n_tokens, int hkv, int lk,
+    int lv, float k_scale, float v_scale, int fmt, uint8_t *k_buf,
+    long k_buf_ss, long k_buf_hs, uint8_t *v_buf, long v_buf_ss,
+    long v_buf_hs)
+{
+    for (long t = 0; t < n_tokens; ++t) {
+        long slot = (long)cache_loc[t];
+        for (int h = 0; h < hkv; ++h) {
+            for (int d = 0; d < lk; ++d) {
+                float x = (float)bf16_to_double(k[t * k_ts + (long)h * k_hs + d]);
+                k_buf[slot * k_buf_ss + (long)h * k_buf_hs + d] =
+                    oracle_fp8_code(x / k_scale, fmt);
+            }
+            if (v)
+                for (int d = 0; d < lv; ++d) {
+                    float x = (float)bf16_to_double(v[t * v_ts + (long)h * v_hs + d]);
+                    v_buf[slot * v_buf_ss + (long)h * v_buf_hs + d] =
+                        oracle_fp8_code(x / v_scale, fmt);
+                }
         }
     }
 }

@@ -29,13 +29,13 @@ MUTANTS = [
      "double sj = dot;\n        if (logit_cap > 0.0)\n            sj = logit_cap * tanh(sj / logit_cap);\n        sj *= sm_scale;", None),
     ("lse_drops_max", "*lse = m + log(l);", "*lse = log(l);", None),
     ("no_normalise", "o[d] /= l;", "o[d] /= 1.0;", None),
-    ("v_is_k", "bf16_to_double(vrow[j][d])", "bf16_to_double(krow[j][d])", None),
+    ("v_is_k", "o[d] += p * row_elem(vrow[j], d);", "o[d] += p * row_elem(krow[j], d);", None),
     ("gqa_modulo", "int hk = h / group;", "int hk = h % hkv;", None),
     ("extend_qpos_no_prefix", "p_len + i, sliding_window", "i, sliding_window", None),
     ("unified_qpos_no_prefix", "(long)prefix_lens[b] + i", "(long)i", None),
     ("extend_rows_reversed", "long te = qo_indptr[b] + e;", "long te = qo_indptr[b] + (e_len - 1 - e);", None),
-    ("prefix_reversed", "long slot = kv_indices[kv_indptr[b] + j];\n            krow[j] = k_buf + slot * k_buf_ss + (long)hk * k_buf_hs;\n            vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;\n        }\n        for (long e = 0",
-     "long slot = kv_indices[kv_indptr[b] + (p_len - 1 - j)];\n            krow[j] = k_buf + slot * k_buf_ss + (long)hk * k_buf_hs;\n            vrow[j] = v_buf + slot * v_buf_ss + (long)hk * v_buf_hs;\n        }\n        for (long e = 0", None),
+    ("prefix_reversed", "long slot = kv_indices[kv_indptr[b] + j];\n            krow[j] = pool_row(k_buf, kv_fmt, k_scale, slot, k_buf_ss, k_buf_hs, hk);\n            vrow[j] = pool_row(v_buf, kv_fmt, v_scale, slot, v_buf_ss, v_buf_hs, hk);\n        }\n        for (long e = 0",
+     "long slot = kv_indices[kv_indptr[b] + (p_len - 1 - j)];\n            krow[j] = pool_row(k_buf, kv_fmt, k_scale, slot, k_buf_ss, k_buf_hs, hk);\n            vrow[j] = pool_row(v_buf, kv_fmt, v_scale, slot, v_buf_ss, v_buf_hs, hk);\n        }\n        for (long e = 0", None),
     ("decode_qpos", "n_keys - 1, sliding_window", "n_keys - 2, sliding_window", None),
     ("merge_weight_uses_max", "double wa = exp(sa - s), wb = exp(sb - s);", "double wa = exp(sa - m), wb = exp(sb - m);", None),
     ("merge_lse_drops_max", "double s = m + log(exp(sa - m) + exp(sb - m));", "double s = log(exp(sa - m) + exp(sb - m));", None),
@@ -57,6 +57,13 @@ MUTANTS = [
     ("setkv_slot_is_token", "long slot = (long)cache_loc[t];", "long slot = t;", None),
     ("setkv_heads_reversed", "k[t * k_ts + (long)h * k_hs + d];", "k[t * k_ts + (long)(hkv - 1 - h) * k_hs + d];", None),
     ("setkv_v_from_k", "v[t * v_ts + (long)h * v_hs + d];", "k[t * k_ts + (long)h * k_hs + d];", None),
+    ("fp8_e4m3_bias", "ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)", None),
+    ("fp8_e4m3_subnormal", "ldexp(m / 8.0, -6)", "ldexp(m / 8.0, -7)", None),
+    ("fp8_e5m2_bias", "ldexp(1.0 + m / 4.0, e - 15)", "ldexp(1.0 + m / 4.0, e - 16)", None),
+    ("fp8_ties_to_odd", "(d == best_d && (c & 1) == 0)", "(d == best_d && (c & 1) == 1)", None),
+    ("fp8_scale_dropped", "r.fmt) * r.scale;", "r.fmt);", None),
+    ("fp8_kv_scales_swapped", "pool_row(k_buf, kv_fmt, k_scale,", "pool_row(k_buf, kv_fmt, v_scale,", None),
+    ("fp8_write_no_divide", "oracle_fp8_code(x / k_scale, fmt)", "oracle_fp8_code(x, fmt)", None),
     ("sink_in_values", "    if (sink)\n        l += exp(*sink - m);\n", "    if (sink) {\n        l += exp(*sink - m);\n        for (int d = 0; d < lv; ++d) o[d] += exp(*sink - m);\n    }\n", None),
 ]
 
@@ -85,6 +92,11 @@ BATTERY = [
     lambda: pins.test_set_kv_buffer_hand_fixture(),
     lambda: pins.test_kv_indices_are_row_slices(0),
     lambda: pins.test_set_kv_buffer_matches_index_copy(3, 128, 96, False),
+    lambda: pins.test_fp8_code_values_match_torch(*pins.FP8[0]),
+    lambda: pins.test_fp8_code_values_match_torch(*pins.FP8[1]),
+    lambda: pins.test_fp8_rounding_matches_torch_in_range(*pins.FP8[0]),
+    lambda: pins.test_fp8_write_matches_torch_quantization(),
+    lambda: pins.test_fp8_pool_attention_equals_bf16_pool_of_its_values(pins.oracle.KV_E4M3),
 ]
 
 

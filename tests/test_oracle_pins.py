@@ -751,3 +751,111 @@ def test_written_pool_gives_the_two_stage_result():
     uo, ul = oracle.extend_attention_unified(wl.q, kb2, vb2, wl.qo_indptr, uptr, uidx, plen,
                                              wl.sm_scale, 0.0, -1)
     assert torch.equal(o, uo) and torch.equal(lse, ul)
+
+
+# ------------------------------------------------------------- fp8 KV pool
+FP8 = [(oracle.KV_E4M3, torch.float8_e4m3fn, 448.0), (oracle.KV_E5M2, torch.float8_e5m2, 57344.0)]
+
+
+@pytest.mark.parametrize("fmt,dt,_max", FP8)
+def test_fp8_code_values_match_torch(fmt, dt, _max):
+    """Every one of the 256 codes decodes to torch's own float8 value (NaN
+    where torch has NaN, +-inf for e5m2's infinities)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    want = codes.view(dt).to(torch.float64)
+    got = torch.tensor([oracle.fp8_value(c, fmt) for c in range(256)], dtype=torch.float64)
+    assert torch.equal(torch.isnan(got), torch.isnan(want))
+    ok = ~torch.isnan(want)
+    assert torch.equal(got[ok], want[ok])
+
+
+@pytest.mark.parametrize("fmt,dt,vmax", FP8)
+def test_fp8_rounding_matches_torch_in_range(fmt, dt, vmax):
+    """In range, the code of an fp32 value is torch's round-to-nearest-even
+    conversion: random values over many binades, every midpoint between two
+    neighbouring codes (the ties), the subnormal range and signed zeros."""
+    g = torch.Generator().manual_seed(61)
+    vals = [torch.randn(4000, generator=g) * s for s in (1e-4, 1e-2, 0.3, 3.0, 60.0)]
+    finite = [oracle.fp8_value(c, fmt) for c in range(128)]
+    finite = sorted(v for v in finite if math.isfinite(v))
+    mids = [(a + b) / 2 for a, b in zip(finite, finite[1:])]
+    vals.append(torch.tensor(mids + [-m for m in mids] + [0.0, -0.0, vmax, -vmax]))
+    x = torch.cat(vals).to(torch.float32)
+    x = x[x.abs() <= vmax]
+    want = x.to(dt).view(torch.uint8).to(torch.int64)
+    got = torch.tensor([oracle.fp8_code(float(v), fmt) for v in x], dtype=torch.int64)
+    assert torch.equal(got, want)
+
+
+@pytest.mark.parametrize("fmt,dt,vmax", FP8)
+def test_fp8_saturates_past_the_largest_code(fmt, dt, vmax):
+    top = [c for c in range(128) if oracle.fp8_value(c, fmt) == vmax][0]
+    for x in (vmax * 1.01, vmax * 4, 1e30, float("inf")):
+        assert oracle.fp8_code(x, fmt) == top
+        assert oracle.fp8_code(-x, fmt) == top | 0x80
+
+
+def _fp8_pool_pair(wl, fmt, k_scale, v_scale):
+    """The workload's pool quantized into fp8 through the oracle's KV write,
+    and the same pool dequantized into bf16 (exact: a code times a power of
+    two fits in bf16)."""
+    kb, vb = wl.pool()
+    dt = dict((f, d) for f, d, _ in FP8)[fmt]
+    z8k = torch.zeros(kb.shape, dtype=torch.uint8).view(dt)
+    z8v = torch.zeros(vb.shape, dtype=torch.uint8).view(dt)
+    loc = wl.slots.to(torch.int64)
+    k8, v8 = oracle.set_kv_buffer_fp8(z8k, z8v, loc, wl.k_rows, wl.v_rows, k_scale, v_scale)
+    kdq = (k8.to(torch.float64) * k_scale).to(torch.bfloat16)
+    vdq = (v8.to(torch.float64) * v_scale).to(torch.bfloat16)
+    assert torch.equal(kdq.double(), k8.to(torch.float64) * k_scale)  # exact
+    return k8, v8, kdq, vdq
+
+
+@pytest.mark.parametrize("fmt", [oracle.KV_E4M3, oracle.KV_E5M2])
+def test_fp8_pool_attention_equals_bf16_pool_of_its_values(fmt):
+    """With power-of-two scales every dequantized element is a bf16 value;
+    two-stage, unified and decode attention over the fp8 pool (k_scale,
+    v_scale) equal the same attention over that bf16 pool, bit for bit."""
+    ks, vs = 0.25, 4.0
+    wl = W.draw(_spec(batch=3, hq=8, hkv=2, lq=64, lv=64, prefix=[20, 0, 45],
+                      extend=[6, 9, 3], seed=62))
+    k8, v8, kdq, vdq = _fp8_pool_pair(wl, fmt, ks, vs)
+    k_ext, v_ext = wl.extend_kv()
+    s = wl.spec
+    args = (wl.qo_indptr, wl.kv_indptr, wl.kv_indices, wl.sm_scale, 10.0, 30)
+    o8, l8 = oracle.extend_attention(wl.q, k_ext, v_ext, k8, v8, *args, k_scale=ks, v_scale=vs)
+    ob, lb = oracle.extend_attention(wl.q, k_ext, v_ext, kdq, vdq, *args)
+    assert torch.equal(o8, ob) and torch.equal(l8, lb)
+    uptr, uidx, plen = oracle.build_unified_kv_indices(
+        wl.kv_indptr, wl.kv_indices, wl.extend_start_loc, wl.extend_seq_lens,
+        wl.extend_kv_indices, wl.batch)
+    o8, l8 = oracle.extend_attention_unified(wl.q, k8, v8, wl.qo_indptr, uptr, uidx, plen,
+                                             wl.sm_scale, 0.0, -1, k_scale=ks, v_scale=vs)
+    ob, lb = oracle.extend_attention_unified(wl.q, kdq, vdq, wl.qo_indptr, uptr, uidx, plen,
+                                             wl.sm_scale, 0.0, -1)
+    assert torch.equal(o8, ob) and torch.equal(l8, lb)
+    q1 = wl.q[:3]
+    o8, l8 = oracle.decode_attention(q1, k8, v8, uptr, uidx.to(torch.int32), wl.sm_scale,
+                                     k_scale=ks, v_scale=vs)
+    ob, lb = oracle.decode_attention(q1, kdq, vdq, uptr, uidx.to(torch.int32), wl.sm_scale)
+    assert torch.equal(o8, ob) and torch.equal(l8, lb)
+
+
+def test_fp8_write_matches_torch_quantization():
+    """The fp8 KV write equals torch: (k.float() / scale).to(float8) at the
+    slots (values kept in range), other slots unchanged."""
+    g = torch.Generator().manual_seed(63)
+    n, hkv, d, slots = 13, 2, 64, 40
+    k = (torch.randn(n, hkv, d, generator=g) * 3).to(torch.bfloat16)
+    v = (torch.randn(n, hkv, d, generator=g) * 3).to(torch.bfloat16)
+    loc = torch.randperm(slots, generator=g)[:n]
+    for fmt, dt, _ in FP8:
+        kb = torch.randint(0, 120, (slots, hkv, d), generator=g, dtype=torch.uint8).view(dt)
+        vb = torch.randint(0, 120, (slots, hkv, d), generator=g, dtype=torch.uint8).view(dt)
+        k2, v2 = oracle.set_kv_buffer_fp8(kb, vb, loc, k, v, 0.5, 2.0)
+        wk = kb.view(torch.uint8).clone()
+        wk[loc] = (k.float() / 0.5).to(dt).view(torch.uint8)
+        wv = vb.view(torch.uint8).clone()
+        wv[loc] = (v.float() / 2.0).to(dt).view(torch.uint8)
+        assert torch.equal(k2.view(torch.uint8), wk)
+        assert torch.equal(v2.view(torch.uint8), wv)
