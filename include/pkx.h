@@ -54,6 +54,22 @@ extern "C" {
 #define PKX_EDEVICE 5       /* device-side index check failed (status word)  */
 #define PKX_EWORKSPACE 6    /* workspace null or smaller than required       */
 
+/*
+ * Element format of the KV pool (kv_dtype arguments).
+ * Source: sglang flashinfer_backend.py: the KV cache dtype may be bf16 or
+ * float8_e4m3fn / float8_e5m2, and the attention call takes the layer's
+ * k_scale and v_scale.  In an fp8 pool a key element reads code * k_scale
+ * and a value element code * v_scale (k_scale, v_scale positive host
+ * floats; ignored for bf16).  An fp8 pool's strides are in bytes (its
+ * elements are one byte); the 16-byte alignment rule for rows still
+ * applies.  Built for Lq = Lv = 64 or 128 without a custom mask; other fp8
+ * calls return PKX_EUNSUPPORTED.  The extend rows of the two-stage form
+ * (k_extend / v_extend) stay bf16.
+ */
+#define PKX_KV_BF16 0
+#define PKX_KV_FP8_E4M3 1
+#define PKX_KV_FP8_E5M2 2
+
 /* Reason for the last failing call on this thread ("" if none). */
 const char *pkx_last_error_string(void);
 
@@ -130,6 +146,7 @@ void pkx_set_attention_events(void *before, void *after);
  *   mask_indptr int32 [batch+1] element offsets into custom_mask (needed
  *              with a mask; NULL otherwise)
  *   sinks      nullable fp32 [hq] sink logit per query head
+ *   kv_dtype, k_scale, v_scale  the pool's format and scales (PKX_KV_*)
  *   lse_out    nullable fp32 [num_q_tokens, hq] (natural log)
  *   workspace  >= pkx_extend_workspace_size(...) bytes
  * Supported (lq, lv): (64, 64), (128, 128), (576, 512); hq % hkv == 0 and
@@ -144,7 +161,8 @@ int pkx_extend_attention_fwd(
     int64_t ve_sh, int64_t kb_ss, int64_t kb_sh, int64_t vb_ss, int64_t vb_sh,
     int64_t num_slots, float sm_scale, float logit_cap, int sliding_window,
     const uint8_t *custom_mask, const int32_t *mask_indptr, const float *sinks,
-    float *lse_out, void *workspace, size_t workspace_bytes, void *stream);
+    int kv_dtype, float k_scale, float v_scale, float *lse_out,
+    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Extend attention, ragged + paged split.
@@ -174,7 +192,8 @@ int pkx_extend_attention_fwd_ragged_paged(
     int lq, int lv, int64_t ke_st, int64_t ke_sh, int64_t ve_st,
     int64_t ve_sh, int64_t kb_ss, int64_t kb_sh, int64_t vb_ss, int64_t vb_sh,
     int64_t num_slots, float sm_scale, float logit_cap, int sliding_window,
-    float *lse_out, void *workspace, size_t workspace_bytes, void *stream);
+    int kv_dtype, float k_scale, float v_scale, float *lse_out,
+    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Extend attention, unified form.
@@ -198,7 +217,8 @@ int pkx_extend_attention_fwd_unified(
     int64_t kb_sh, int64_t vb_ss, int64_t vb_sh, int64_t num_slots,
     float sm_scale, float logit_cap, int sliding_window,
     const uint8_t *custom_mask, const int32_t *mask_indptr, const float *sinks,
-    float *lse_out, void *workspace, size_t workspace_bytes, void *stream);
+    int kv_dtype, float k_scale, float v_scale, float *lse_out,
+    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Decode attention.
@@ -217,8 +237,8 @@ int pkx_decode_attention_fwd(
     const int32_t *kv_indptr, const int32_t *kv_indices, int batch, int hq,
     int hkv, int lq, int lv, int64_t kb_ss, int64_t kb_sh, int64_t vb_ss,
     int64_t vb_sh, int64_t num_slots, float sm_scale, float logit_cap,
-    int sliding_window, float *lse_out, void *workspace,
-    size_t workspace_bytes, void *stream);
+    int sliding_window, int kv_dtype, float k_scale, float v_scale,
+    float *lse_out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Decode attention without a workspace argument, for callers that cannot
@@ -227,7 +247,7 @@ int pkx_decode_attention_fwd(
  * that must not call cudaMalloc (which synchronises the device).  The pages
  * have no counterpart to this call; it is this library's own addition.
  * Same arguments and results as pkx_decode_attention_fwd minus
- * workspace/workspace_bytes.  Its scratch is a fixed 96 MiB device array
+ * workspace/workspace_bytes and the pool format (a bf16 pool).  Its scratch is a fixed 96 MiB device array
  * inside the library that every GPU loading the library holds until exit.
  * The first call on each device looks up that array's address (make it
  * before any stream capture).  Calls share the array: calls that overlap on
@@ -307,6 +327,26 @@ int pkx_set_kv_buffer(
     int64_t v_hs, const int64_t *cache_loc, int64_t n_tokens, int hkv, int lk,
     int lv, void *k_buffer, int64_t kb_ss, int64_t kb_hs, void *v_buffer,
     int64_t vb_ss, int64_t vb_hs, int64_t num_slots, void *stream);
+
+/*
+ * KV write into an fp8 pool.
+ * Source: sglang flashinfer_backend.py, set_kv_buffer(layer, cache_loc, k,
+ * v, k_scale, v_scale) with an fp8 KV cache.  For t < n_tokens, every KV
+ * head h and element d:
+ *   k_buffer[cache_loc[t], h, d] = fp8(k[t, h, d] / k_scale)
+ *   v_buffer[cache_loc[t], h, d] = fp8(v[t, h, d] / v_scale)
+ * where the quotient is an IEEE fp32 division and fp8() rounds to the
+ * nearest code, ties to even, and saturates at the largest finite code
+ * (448 for e4m3, 57344 for e5m2).  kv_dtype PKX_KV_FP8_E4M3 or
+ * PKX_KV_FP8_E5M2; pools of one-byte codes, strides in bytes (multiples of
+ * 8); other arguments and rules as pkx_set_kv_buffer.
+ */
+int pkx_set_kv_buffer_fp8(
+    const void *k, int64_t k_ts, int64_t k_hs, const void *v, int64_t v_ts,
+    int64_t v_hs, const int64_t *cache_loc, int64_t n_tokens, int hkv, int lk,
+    int lv, float k_scale, float v_scale, int kv_dtype, void *k_buffer,
+    int64_t kb_ss, int64_t kb_hs, void *v_buffer, int64_t vb_ss,
+    int64_t vb_hs, int64_t num_slots, void *stream);
 
 /*
  * KV-index gather from the request-to-token table.

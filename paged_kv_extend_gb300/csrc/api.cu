@@ -57,6 +57,21 @@ static int check_mask_sinks(const uint8_t *custom_mask, const int32_t *mask_indp
   return PKX_OK;
 }
 
+// The pool's element format and its scales (an fp8 pool: Lq = Lv = 64 or
+// 128, no custom mask).
+static int check_kv_format(int kv_dtype, float k_scale, float v_scale, int lq, int lv,
+                           const uint8_t *custom_mask) {
+  if (kv_dtype == kKvBf16) return PKX_OK;
+  if (kv_dtype != kKvFp8E4M3 && kv_dtype != kKvFp8E5M2)
+    return set_error(PKX_EINVAL, "kv_dtype %d is not a PKX_KV_* value", kv_dtype);
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return set_error(PKX_EINVAL, "k_scale and v_scale must be positive and finite");
+  if (!((lq == 64 && lv == 64) || (lq == 128 && lv == 128)) || custom_mask)
+    return set_error(PKX_EUNSUPPORTED,
+                     "an fp8 pool is built for Lq = Lv = 64 or 128 without a custom mask");
+  return PKX_OK;
+}
+
 static int check_scalars(float sm_scale, float logit_cap) {
   if (!std::isfinite(sm_scale) || !std::isfinite(logit_cap))
     return set_error(PKX_EINVAL, "sm_scale and logit_cap must be finite");
@@ -119,13 +134,15 @@ static int two_stage_args(AttnArgs &a, const void *q_extend, const void *k_exten
                           int64_t kb_sh, int64_t vb_ss, int64_t vb_sh, int64_t num_slots,
                           float sm_scale, float logit_cap, int sliding_window,
                           const uint8_t *custom_mask, const int32_t *mask_indptr,
-                          const float *sinks, float *lse_out, bool *nothing_to_do) {
+                          const float *sinks, int kv_dtype, float k_scale, float v_scale,
+                          float *lse_out, bool *nothing_to_do) {
   int rc;
   *nothing_to_do = false;
   if (batch < 0 || num_q_tokens < 0) return set_error(PKX_EINVAL, "negative batch or token count");
   if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
   if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
   if ((rc = check_mask_sinks(custom_mask, mask_indptr, sinks))) return rc;
+  if ((rc = check_kv_format(kv_dtype, k_scale, v_scale, lq, lv, custom_mask))) return rc;
   if (batch == 0 || num_q_tokens == 0) {
     *nothing_to_do = true;
     return PKX_OK;
@@ -159,6 +176,7 @@ static int two_stage_args(AttnArgs &a, const void *q_extend, const void *k_exten
   a.batch = batch; a.num_q_tokens = num_q_tokens; a.hq = hq; a.hkv = hkv; a.lq = lq; a.lv = lv;
   a.sm_scale = sm_scale; a.logit_cap = logit_cap; a.window = sliding_window;
   a.custom_mask = custom_mask; a.mask_indptr = mask_indptr; a.sinks = sinks;
+  a.kv_fmt = kv_dtype; a.k_scale = k_scale; a.v_scale = v_scale;
   return PKX_OK;
 }
 
@@ -195,15 +213,16 @@ int pkx_extend_attention_fwd(const void *q_extend, const void *k_extend, const v
                              int64_t ve_st, int64_t ve_sh, int64_t kb_ss, int64_t kb_sh,
                              int64_t vb_ss, int64_t vb_sh, int64_t num_slots, float sm_scale,
                              float logit_cap, int sliding_window, const uint8_t *custom_mask,
-                             const int32_t *mask_indptr, const float *sinks, float *lse_out,
-                             void *workspace, size_t workspace_bytes, void *stream) {
+                             const int32_t *mask_indptr, const float *sinks, int kv_dtype,
+                             float k_scale, float v_scale, float *lse_out, void *workspace,
+                             size_t workspace_bytes, void *stream) {
   AttnArgs a{};
   bool done;
   int rc = two_stage_args(a, q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffer,
                           qo_indptr, kv_indptr, kv_indices, batch, num_q_tokens, hq, hkv, lq, lv,
                           ke_st, ke_sh, ve_st, ve_sh, kb_ss, kb_sh, vb_ss, vb_sh, num_slots,
                           sm_scale, logit_cap, sliding_window, custom_mask, mask_indptr, sinks,
-                          lse_out, &done);
+                          kv_dtype, k_scale, v_scale, lse_out, &done);
   if (rc != PKX_OK || done) return rc;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
@@ -224,15 +243,15 @@ int pkx_extend_attention_fwd_ragged_paged(
     const int32_t *kv_indptr, const int32_t *kv_indices, int batch, int num_q_tokens, int hq,
     int hkv, int lq, int lv, int64_t ke_st, int64_t ke_sh, int64_t ve_st, int64_t ve_sh,
     int64_t kb_ss, int64_t kb_sh, int64_t vb_ss, int64_t vb_sh, int64_t num_slots,
-    float sm_scale, float logit_cap, int sliding_window, float *lse_out, void *workspace,
-    size_t workspace_bytes, void *stream) {
+    float sm_scale, float logit_cap, int sliding_window, int kv_dtype, float k_scale,
+    float v_scale, float *lse_out, void *workspace, size_t workspace_bytes, void *stream) {
   AttnArgs a{};
   bool done;
   int rc = two_stage_args(a, q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffer,
                           qo_indptr, kv_indptr, kv_indices, batch, num_q_tokens, hq, hkv, lq, lv,
                           ke_st, ke_sh, ve_st, ve_sh, kb_ss, kb_sh, vb_ss, vb_sh, num_slots,
                           sm_scale, logit_cap, sliding_window, nullptr, nullptr, nullptr,
-                          lse_out, &done);
+                          kv_dtype, k_scale, v_scale, lse_out, &done);
   if (rc != PKX_OK || done) return rc;
   const SplitLayout L = split_layout(batch, num_q_tokens, hq, hkv, lq, lv);
   if (!workspace || workspace_bytes < L.total)
@@ -271,13 +290,14 @@ int pkx_extend_attention_fwd_unified(const void *q, void *o, const void *k_buffe
                                      int64_t num_slots, float sm_scale, float logit_cap,
                                      int sliding_window, const uint8_t *custom_mask,
                                      const int32_t *mask_indptr, const float *sinks,
-                                     float *lse_out, void *workspace, size_t workspace_bytes,
-                                     void *stream) {
+                                     int kv_dtype, float k_scale, float v_scale, float *lse_out,
+                                     void *workspace, size_t workspace_bytes, void *stream) {
   int rc;
   if (batch < 0 || num_q_tokens < 0) return set_error(PKX_EINVAL, "negative batch or token count");
   if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
   if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
   if ((rc = check_mask_sinks(custom_mask, mask_indptr, sinks))) return rc;
+  if ((rc = check_kv_format(kv_dtype, k_scale, v_scale, lq, lv, custom_mask))) return rc;
   if (batch == 0 || num_q_tokens == 0) return PKX_OK;
   if ((rc = check_rows("q", q, 8, 8))) return rc;
   if ((rc = check_rows("o", o, 8, 8))) return rc;
@@ -305,6 +325,7 @@ int pkx_extend_attention_fwd_unified(const void *q, void *o, const void *k_buffe
   a.batch = batch; a.num_q_tokens = num_q_tokens; a.hq = hq; a.hkv = hkv; a.lq = lq; a.lv = lv;
   a.sm_scale = sm_scale; a.logit_cap = logit_cap; a.window = sliding_window;
   a.custom_mask = custom_mask; a.mask_indptr = mask_indptr; a.sinks = sinks;
+  a.kv_fmt = kv_dtype; a.k_scale = k_scale; a.v_scale = v_scale;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   return launch_attention(a);
@@ -314,12 +335,14 @@ int pkx_decode_attention_fwd(const void *q, void *o, const void *k_buffer, const
                              const int32_t *kv_indptr, const int32_t *kv_indices, int batch,
                              int hq, int hkv, int lq, int lv, int64_t kb_ss, int64_t kb_sh,
                              int64_t vb_ss, int64_t vb_sh, int64_t num_slots, float sm_scale,
-                             float logit_cap, int sliding_window, float *lse_out,
-                             void *workspace, size_t workspace_bytes, void *stream) {
+                             float logit_cap, int sliding_window, int kv_dtype, float k_scale,
+                             float v_scale, float *lse_out, void *workspace,
+                             size_t workspace_bytes, void *stream) {
   int rc;
   if (batch < 0) return set_error(PKX_EINVAL, "negative batch");
   if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
   if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
+  if ((rc = check_kv_format(kv_dtype, k_scale, v_scale, lq, lv, nullptr))) return rc;
   if (batch == 0) return PKX_OK;
   if ((rc = check_rows("q", q, 8, 8))) return rc;
   if ((rc = check_rows("o", o, 8, 8))) return rc;
@@ -345,6 +368,7 @@ int pkx_decode_attention_fwd(const void *q, void *o, const void *k_buffer, const
   a.kv_indices = kv_indices;
   a.batch = batch; a.num_q_tokens = batch; a.hq = hq; a.hkv = hkv; a.lq = lq; a.lv = lv;
   a.sm_scale = sm_scale; a.logit_cap = logit_cap; a.window = sliding_window;
+  a.kv_fmt = kv_dtype; a.k_scale = k_scale; a.v_scale = v_scale;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   return launch_attention(a);
@@ -402,6 +426,34 @@ int pkx_set_kv_buffer(const void *k, int64_t k_ts, int64_t k_hs, const void *v, 
   return launch_set_kv_buffer(k, k_ts, k_hs, v, v_ts, v_hs, cache_loc, n_tokens, hkv, lk, lv,
                               k_buffer, kb_ss, kb_hs, v_buffer, vb_ss, vb_hs, num_slots,
                               static_cast<cudaStream_t>(stream));
+}
+
+int pkx_set_kv_buffer_fp8(const void *k, int64_t k_ts, int64_t k_hs, const void *v,
+                          int64_t v_ts, int64_t v_hs, const int64_t *cache_loc, int64_t n_tokens,
+                          int hkv, int lk, int lv, float k_scale, float v_scale, int kv_dtype,
+                          void *k_buffer, int64_t kb_ss, int64_t kb_hs, void *v_buffer,
+                          int64_t vb_ss, int64_t vb_hs, int64_t num_slots, void *stream) {
+  if (kv_dtype != kKvFp8E4M3 && kv_dtype != kKvFp8E5M2)
+    return set_error(PKX_EINVAL, "set_kv_buffer_fp8: kv_dtype must be an fp8 PKX_KV_* value");
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return set_error(PKX_EINVAL, "set_kv_buffer_fp8: scales must be positive and finite");
+  if (n_tokens < 0 || hkv <= 0 || lk <= 0 || lk % 8 || (v && (lv <= 0 || lv % 8)))
+    return set_error(PKX_EINVAL,
+                     "set_kv_buffer_fp8: n_tokens >= 0, hkv > 0, lk (and lv) multiples of 8");
+  if (num_slots < 0) return set_error(PKX_EINVAL, "set_kv_buffer_fp8: negative num_slots");
+  if (n_tokens == 0) return PKX_OK;
+  if (!cache_loc || !aligned(cache_loc, 8))
+    return set_error(PKX_EINVAL, "set_kv_buffer_fp8: cache_loc null or misaligned");
+  int rc;
+  if ((rc = check_rows("k", k, k_ts, k_hs)) != PKX_OK) return rc;
+  if ((rc = check_rows("k_buffer", k_buffer, kb_ss, kb_hs)) != PKX_OK) return rc;
+  if (v) {
+    if ((rc = check_rows("v", v, v_ts, v_hs)) != PKX_OK) return rc;
+    if ((rc = check_rows("v_buffer", v_buffer, vb_ss, vb_hs)) != PKX_OK) return rc;
+  }
+  return launch_set_kv_buffer_fp8(k, k_ts, k_hs, v, v_ts, v_hs, cache_loc, n_tokens, hkv, lk, lv,
+                                  k_scale, v_scale, kv_dtype, k_buffer, kb_ss, kb_hs, v_buffer,
+                                  vb_ss, vb_hs, num_slots, static_cast<cudaStream_t>(stream));
 }
 
 int pkx_create_kv_indices(const int32_t *req_to_token, int64_t req_to_token_rows,

@@ -41,6 +41,8 @@
 #include <cstring>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -390,6 +392,11 @@ struct KParams {
   const uint8_t *custom_mask;   // nullable: byte per (extend row, key); replaces causal
   const int32_t *mask_indptr;   // [batch+1] offsets of each sequence's mask rows
   const float *sinks;           // nullable [hq] sink logits (natural log)
+  // fp8 pool: a key reads code * k_scale, a value code * v_scale.  The codes
+  // go to shared memory as exact bf16; k_scale is folded into the logit
+  // scale of pool tiles, v_scale into their P through the exponent
+  // (2^(s - m + log2 v_scale)), and the tile's row sum is divided back
+  float scale_log2_k, cap_pre_k, log2_v_scale, inv_v_scale;
   const int32_t *prefix_lens;   // unified form: prefix length per sequence
   const WorkUnit *units;
   const int32_t *uorder;  // units by cost, largest first
@@ -500,7 +507,27 @@ __device__ __forceinline__ int ring_unit(uint64_t *u_full, uint64_t *u_empty,
 
 // MASK: a custom mask replaces the causal mask (its own instantiation, so
 // the unmasked kernel carries none of the mask code).
-template <int HD, int MODE, bool MASK>
+// Eight fp8 codes (e4m3 for FMT 1, e5m2 for FMT 2) as eight bf16 of the same
+// values (exact: every code is a bf16 value), in element order (the code in
+// the lowest byte first).
+template <int FMT>
+__device__ __forceinline__ uint4 fp8x8_to_bf16x8(uint2 raw) {
+  constexpr __nv_fp8_interpretation_t kind = FMT == 1 ? __NV_E4M3 : __NV_E5M2;
+  const uint32_t w[2] = {raw.x, raw.y};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h(__nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(w[i >> 1] >> (16 * (i & 1))), kind));
+    const float2 f = __half22float2(h);
+    out[i] = pack_bf16(f.x, f.y);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// FMT: the pool's element format (0 bf16; 1 fp8 e4m3, 2 fp8 e5m2 with
+// k_scale / v_scale).  Extend rows of the two-stage form are always bf16.
+template <int HD, int MODE, bool MASK, int FMT = 0>
 __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     attn_kernel(const __grid_constant__ TMaps tm, const KParams p) {
   using C = Cfg<HD>;
@@ -683,10 +710,14 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           // Logits in the log2 domain are sc * x.  The plain path keeps the
           // raw dot products and folds sc into the exponent's FMA; a capped
           // or masked tile is first mapped into the log2 domain (sc = 1).
-          float sc = p.scale_log2;
+          // A tile of an fp8 pool holds the codes: its logits take k_scale
+          // in the scale, its P takes v_scale.
+          const bool pool8 = FMT != 0 && !(MODE == kTwoStage && kb >= w.k_split);
+          float sc = pool8 ? p.scale_log2_k : p.scale_log2;
           if (p.use_cap) {
+            const float pre = pool8 ? p.cap_pre_k : p.cap_pre;
 #pragma unroll
-            for (int i = 0; i < C::BN; ++i) x[i] = p.cap_log2 * tanh_approx(x[i] * p.cap_pre);
+            for (int i = 0; i < C::BN; ++i) x[i] = p.cap_log2 * tanh_approx(x[i] * pre);
             sc = 1.0f;
           }
           const bool need_mask = MASK || (ke - 1 > qmin) || (ke - kb < C::BN) ||
@@ -754,7 +785,14 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           }
           const float mref = m == -INFINITY ? 0.f : m;
           // p = 2^(sc * x - m): one FMA into each exp2
-          const float nm = -mref;
+          float nm = -mref;
+          float lscale = 1.0f;
+          if constexpr (FMT != 0) {
+            if (pool8) {
+              nm += p.log2_v_scale;
+              lscale = p.inv_v_scale;
+            }
+          }
           float l0 = 0.f, l1 = 0.f;
           uint32_t pk[C::BN / 2];
 #pragma unroll
@@ -765,7 +803,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             l1 += e1;
             pk[i / 2] = pack_bf16(e0, e1);
           }
-          l += l0 + l1;
+          if constexpr (FMT != 0) l += (l0 + l1) * lscale;
+          else l += l0 + l1;
           // P (bf16 pairs) over the first 64 columns of this tile's S.
           {
             uint32_t a[32], b[32];
@@ -1090,65 +1129,194 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     };
     uint32_t kc = 0, vc = 0, ic = 0;
     bool ok = true;
+    if constexpr (FMT == 0) {
+      for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+        const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ok);
+        if (u < 0) break;
+        const WorkUnit w = p.units[p.uorder[u]];
+        const int nt = w.n_tiles;
+        if (nt == 0) continue;
+        const bf16 *kp = p.k_pool + (int64_t)w.kvh * p.kb_sh + ch * 8;
+        const bf16 *vp = p.v_pool + (int64_t)w.kvh * p.vb_sh + ch * 8;
+        const bf16 *kx = p.k_ext + (int64_t)w.kvh * p.ke_sh + ch * 8;
+        const bf16 *vx = p.v_ext + (int64_t)w.kvh * p.ve_sh + ch * 8;
+        for (int j = 0; j < nt; ++j) {
+          int kb, ke;
+          tile_keys(w, j, kb, ke);
+          const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
+          // this thread's rows from the index ring
+          const int is = ic % C::NI;
+          if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          int rows[NKEYS];
+          {
+            const int4 *ring =
+                reinterpret_cast<const int4 *>(smem + C::OFF_I + is * C::I_BYTES) + key0 * (NKEYS / 4);
+  #pragma unroll
+            for (int q = 0; q < NKEYS / 4; ++q) {
+              const int4 v = ring[q];
+              rows[4 * q] = v.x;
+              rows[4 * q + 1] = v.y;
+              rows[4 * q + 2] = v.z;
+              rows[4 * q + 3] = v.w;
+            }
+          }
+          __syncwarp();  // the warp is done with the ring slot
+          if (lane == 0) mbar_arrive(&i_empty[is]);
+          ++ic;
+          // K tile
+          const int ks = kc % C::NK;
+          if (kc >= (uint32_t)C::NK &&
+              !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          copy_rows(sbase + C::OFF_K + ks * C::K_BYTES, from_ext ? kx : kp,
+                    from_ext ? p.ke_st : p.kb_ss, rows);
+          cp_async_arrive_noinc(&k_full[ks]);
+          ++kc;
+          // V tile
+          const int vs = vc % C::NV;
+          if (vc >= (uint32_t)C::NV &&
+              !mbar_wait(&v_empty[vs], ((vc / C::NV) - 1) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          copy_rows(sbase + C::OFF_V + vs * C::V_BYTES, from_ext ? vx : vp,
+                    from_ext ? p.ve_st : p.vb_ss, rows);
+          cp_async_arrive_noinc(&v_full[vs]);
+          ++vc;
+        }
+      }
+    } else {
+    // fp8 pool.  A pool tile's codes are copied 8 bytes per (thread, key)
+    // into the first half of the 16-byte chunk the same thread later
+    // writes, and converted there in place to bf16 once they have landed, so no thread overwrites another's codes.  The copies
+    // of tile j+1 go out before tile j is converted, in the order
+    // K(j+1), convert K(j), V(j+1), convert V(j): V(j+1) reuses the stage of
+    // V(j-1), which the tensor core frees only after K(j) is full.  Extend
+    // tiles (bf16 rows of the two-stage form) take the plain copy.  One
+    // cp.async group is committed per issued tile.
+    auto issue_raw = [&](uint32_t stage, const uint8_t *base, int64_t stride, const int *rows) {
+      static_for<0, NKEYS>([&](auto i_c) {
+        constexpr int i = decltype(i_c)::value;
+        const int r = rows[i];
+        const uint8_t *src = base + (int64_t)max(r, 0) * stride;
+        cp_async_8_at<i * KPP * 128>(stage + dthr, src, r >= 0 ? 8u : 0u);
+      });
+    };
+    auto convert = [&](uint32_t stage) {
+      static_for<0, NKEYS>([&](auto i_c) {
+        constexpr int i = decltype(i_c)::value;
+        const uint32_t a = stage + dthr + i * KPP * 128;
+        st_shared_u4(a, fp8x8_to_bf16x8<FMT>(ld_shared_u2(a)));
+      });
+      fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+    };
     for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
       const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ok);
       if (u < 0) break;
       const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
       if (nt == 0) continue;
-      const bf16 *kp = p.k_pool + (int64_t)w.kvh * p.kb_sh + ch * 8;
-      const bf16 *vp = p.v_pool + (int64_t)w.kvh * p.vb_sh + ch * 8;
+      const uint8_t *kp8 =
+          reinterpret_cast<const uint8_t *>(p.k_pool) + (int64_t)w.kvh * p.kb_sh + ch * 8;
+      const uint8_t *vp8 =
+          reinterpret_cast<const uint8_t *>(p.v_pool) + (int64_t)w.kvh * p.vb_sh + ch * 8;
       const bf16 *kx = p.k_ext + (int64_t)w.kvh * p.ke_sh + ch * 8;
       const bf16 *vx = p.v_ext + (int64_t)w.kvh * p.ve_sh + ch * 8;
-      for (int j = 0; j < nt; ++j) {
+      int rows[NKEYS];
+      auto tile_from_ext = [&](int j) {
         int kb, ke;
         tile_keys(w, j, kb, ke);
-        const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
-        // this thread's rows from the index ring
+        return MODE == kTwoStage && kb >= w.k_split;
+      };
+      auto fetch = [&]() -> bool {
         const int is = ic % C::NI;
-        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        int rows[NKEYS];
-        {
-          const int4 *ring =
-              reinterpret_cast<const int4 *>(smem + C::OFF_I + is * C::I_BYTES) + key0 * (NKEYS / 4);
+        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag)) return false;
+        const int4 *ring =
+            reinterpret_cast<const int4 *>(smem + C::OFF_I + is * C::I_BYTES) + key0 * (NKEYS / 4);
 #pragma unroll
-          for (int q = 0; q < NKEYS / 4; ++q) {
-            const int4 v = ring[q];
-            rows[4 * q] = v.x;
-            rows[4 * q + 1] = v.y;
-            rows[4 * q + 2] = v.z;
-            rows[4 * q + 3] = v.w;
-          }
+        for (int q = 0; q < NKEYS / 4; ++q) {
+          const int4 v = ring[q];
+          rows[4 * q] = v.x;
+          rows[4 * q + 1] = v.y;
+          rows[4 * q + 2] = v.z;
+          rows[4 * q + 3] = v.w;
         }
         __syncwarp();  // the warp is done with the ring slot
         if (lane == 0) mbar_arrive(&i_empty[is]);
         ++ic;
-        // K tile
+        return true;
+      };
+      auto issue_k = [&](bool from_ext) -> bool {
         const int ks = kc % C::NK;
         if (kc >= (uint32_t)C::NK &&
-            !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag)) {
-          ok = false;
-          break;
+            !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag))
+          return false;
+        const uint32_t stage = sbase + C::OFF_K + ks * C::K_BYTES;
+        if (from_ext) {
+          copy_rows(stage, kx, p.ke_st, rows);
+          cp_async_arrive_noinc(&k_full[ks]);
+        } else {
+          issue_raw(stage, kp8, p.kb_ss, rows);
         }
-        copy_rows(sbase + C::OFF_K + ks * C::K_BYTES, from_ext ? kx : kp,
-                  from_ext ? p.ke_st : p.kb_ss, rows);
-        cp_async_arrive_noinc(&k_full[ks]);
+        cp_async_commit();
         ++kc;
-        // V tile
+        return true;
+      };
+      auto issue_v = [&](bool from_ext) -> bool {
         const int vs = vc % C::NV;
         if (vc >= (uint32_t)C::NV &&
-            !mbar_wait(&v_empty[vs], ((vc / C::NV) - 1) & 1u, abort_flag)) {
+            !mbar_wait(&v_empty[vs], ((vc / C::NV) - 1) & 1u, abort_flag))
+          return false;
+        const uint32_t stage = sbase + C::OFF_V + vs * C::V_BYTES;
+        if (from_ext) {
+          copy_rows(stage, vx, p.ve_st, rows);
+          cp_async_arrive_noinc(&v_full[vs]);
+        } else {
+          issue_raw(stage, vp8, p.vb_ss, rows);
+        }
+        cp_async_commit();
+        ++vc;
+        return true;
+      };
+      bool ext_j = tile_from_ext(0);
+      if (!fetch() || !issue_k(ext_j) || !issue_v(ext_j)) {
+        ok = false;
+        break;
+      }
+      for (int j = 0; j < nt; ++j) {
+        const int ks_j = (kc - 1) % C::NK, vs_j = (vc - 1) % C::NV;
+        const bool more = j + 1 < nt;
+        const bool ext_n = more && tile_from_ext(j + 1);
+        if (more && (!fetch() || !issue_k(ext_n))) {
           ok = false;
           break;
         }
-        copy_rows(sbase + C::OFF_V + vs * C::V_BYTES, from_ext ? vx : vp,
-                  from_ext ? p.ve_st : p.vb_ss, rows);
-        cp_async_arrive_noinc(&v_full[vs]);
-        ++vc;
+        if (!ext_j) {
+          // groups issued after K(j): V(j), and K(j+1) if there is one
+          if (more) cp_async_wait_group<2>();
+          else cp_async_wait_group<1>();
+          convert(sbase + C::OFF_K + ks_j * C::K_BYTES);
+          mbar_arrive(&k_full[ks_j]);
+        }
+        if (more && !issue_v(ext_n)) {
+          ok = false;
+          break;
+        }
+        if (!ext_j) {
+          // groups issued after V(j): K(j+1) and V(j+1) if there are
+          if (more) cp_async_wait_group<2>();
+          else cp_async_wait_group<0>();
+          convert(sbase + C::OFF_V + vs_j * C::V_BYTES);
+          mbar_arrive(&v_full[vs_j]);
+        }
+        ext_j = ext_n;
       }
+    }
     }
     if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
     cp_async_wait_all();
@@ -1305,19 +1473,28 @@ static int make_q_map(CUtensorMap *m, const void *q, int64_t n, int hq, int lq, 
   return PKX_OK;
 }
 
-template <int HD, int MODE, bool MASK = false>
+template <int HD, int MODE, bool MASK = false, int FMT = 0>
 static int launch_attn_kernel(const TMaps &tmaps, const KParams &kp, int grid, cudaStream_t s) {
   using C = Cfg<HD>;
   static bool configured = false;  // per instantiation; attribute is per device
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, MODE, MASK>,
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, MODE, MASK, FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
       return set_error(PKX_ECUDA, "cudaFuncSetAttribute(attn_kernel): %s", cudaGetErrorString(e));
     configured = true;
   }
-  attn_kernel<HD, MODE, MASK><<<grid, C::THREADS, C::SMEM, s>>>(tmaps, kp);
+  attn_kernel<HD, MODE, MASK, FMT><<<grid, C::THREADS, C::SMEM, s>>>(tmaps, kp);
   return PKX_OK;
+}
+
+// The three key modes of one head size over an fp8 pool (no custom mask).
+template <int HD, int FMT>
+static int launch_attn_fp8(int mode, const TMaps &tmaps, const KParams &kp, int grid,
+                           cudaStream_t s) {
+  if (mode == kTwoStage) return launch_attn_kernel<HD, kTwoStage, false, FMT>(tmaps, kp, grid, s);
+  if (mode == kUnified) return launch_attn_kernel<HD, kUnified, false, FMT>(tmaps, kp, grid, s);
+  return launch_attn_kernel<HD, kDecode, false, FMT>(tmaps, kp, grid, s);
 }
 
 template <int MODE, bool MASK = false>
@@ -1431,9 +1608,13 @@ int launch_attention(const AttnArgs &a) {
   kp.scale_log2 = sm_scale * log2e;
   kp.cap_pre = kp.use_cap ? sm_scale / a.logit_cap : 0.f;
   kp.cap_log2 = kp.use_cap ? a.logit_cap * log2e : 0.f;
+  kp.scale_log2_k = kp.scale_log2 * a.k_scale;
+  kp.cap_pre_k = kp.cap_pre * a.k_scale;
   kp.custom_mask = a.custom_mask;
   kp.mask_indptr = a.mask_indptr;
   kp.sinks = a.sinks;
+  kp.log2_v_scale = log2f(a.v_scale);
+  kp.inv_v_scale = 1.0f / a.v_scale;
   kp.prefix_lens = a.prefix_lens;
   kp.units = sp.units;
   kp.uorder = sp.uorder;
@@ -1448,7 +1629,18 @@ int launch_attention(const AttnArgs &a) {
   attention_events(&ev_before, &ev_after);
   if (ev_before) cudaEventRecord(ev_before, a.stream);
   const bool masked = a.custom_mask != nullptr;
-  if (a.lq == 128 && a.lv == 128) {
+  if (a.kv_fmt != kKvBf16) {
+    if (masked || mla || !((a.lq == 128 && a.lv == 128) || (a.lq == 64 && a.lv == 64)))
+      return set_error(PKX_EUNSUPPORTED, "an fp8 pool is built for Lq = Lv = 64 or 128 "
+                                         "without a custom mask");
+    const bool e4 = a.kv_fmt == kKvFp8E4M3;
+    if (a.lq == 128)
+      rc = e4 ? launch_attn_fp8<128, 1>(a.mode, tm, kp, grid, a.stream)
+              : launch_attn_fp8<128, 2>(a.mode, tm, kp, grid, a.stream);
+    else
+      rc = e4 ? launch_attn_fp8<64, 1>(a.mode, tm, kp, grid, a.stream)
+              : launch_attn_fp8<64, 2>(a.mode, tm, kp, grid, a.stream);
+  } else if (a.lq == 128 && a.lv == 128) {
     if (a.mode == kTwoStage)
       rc = masked ? launch_attn_kernel<128, kTwoStage, true>(tm, kp, grid, a.stream)
                   : launch_attn_kernel<128, kTwoStage>(tm, kp, grid, a.stream);

@@ -85,6 +85,6 @@ extern "C" int pkx_decode_attention_fwd_no_alloc(
   if (rc != PKX_OK) return rc;
   return pkx_decode_attention_fwd(q, o, k_buffer, v_buffer, kv_indptr, kv_indices, batch, hq, hkv,
                                   lq, lv, kb_ss, kb_sh, vb_ss, vb_sh, num_slots, sm_scale,
-                                  logit_cap, sliding_window, lse_out, scratch,
+                                  logit_cap, sliding_window, 0, 1.0f, 1.0f, lse_out, scratch,
                                   kNoAllocScratchBytes, stream);
 }

@@ -24,6 +24,8 @@
 // evenly over the CTAs, so one long sequence does not serialise on one CTA as
 // it would with a CTA per sequence.  A thread finds the sequence of its entry
 // by binary search in the shared running sum.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "pkx_internal.h"
@@ -125,6 +127,112 @@ int launch_set_kv_buffer(const void *k, int64_t k_ts, int64_t k_hs, const void *
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess)
     return set_error(PKX_ECUDA, "set_kv_buffer launch: %s", cudaGetErrorString(e));
+  return PKX_OK;
+}
+
+// ------------------------------------------------------------ KV write, fp8 pool
+// The same flat list of 16-byte input chunks (8 bf16); each becomes 8 fp8
+// codes (an 8-byte store): element / scale in IEEE fp32, then the nearest
+// code, ties to even, saturating at the largest finite one.
+struct KvWriteFp8Args {
+  const uint4 *k, *v;
+  int64_t k_ts, k_hs, v_ts, v_hs;  // input strides in 16-byte chunks
+  const int64_t *cache_loc;
+  uint2 *k_buf, *v_buf;
+  int64_t kb_ss, kb_hs, vb_ss, vb_hs;  // pool strides in 8-byte chunks
+  int64_t num_slots;
+  uint32_t hkv, ck, cv;
+  uint64_t total;
+  float k_scale, v_scale;
+};
+
+template <int FMT>
+__device__ __forceinline__ uint2 bf16x8_to_fp8x8(uint4 in, float scale) {
+  constexpr __nv_fp8_interpretation_t kind = FMT == 1 ? __NV_E4M3 : __NV_E5M2;
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t out[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+    const float2 f = __bfloat1622float2(b);
+    const float2 q = make_float2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+    const uint32_t two = __nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, kind);
+    out[i >> 1] |= (two & 0xFFFFu) << (16 * (i & 1));
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kKvThreads) set_kv_buffer_fp8_kernel(const KvWriteFp8Args a) {
+  const uint32_t total = (uint32_t)a.total;  // < 2^31 (the launcher checks)
+  const uint32_t stride = gridDim.x * kKvThreads;
+  const uint32_t per_row = a.ck + a.cv;
+  for (uint32_t base = blockIdx.x * kKvThreads + threadIdx.x; base < total;
+       base += stride * kUnroll) {
+    uint4 val[kUnroll];
+    int64_t slot[kUnroll];
+    uint32_t hh[kUnroll], cc[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t i = base + u * stride;
+      slot[u] = -1;
+      if (i < total) {
+        const uint32_t row = i / per_row;
+        cc[u] = i - row * per_row;
+        const uint32_t t = row / a.hkv;
+        hh[u] = row - t * a.hkv;
+        slot[u] = __ldg(a.cache_loc + t);
+        val[u] = __ldg(cc[u] < a.ck
+                           ? a.k + (int64_t)t * a.k_ts + (int64_t)hh[u] * a.k_hs + cc[u]
+                           : a.v + (int64_t)t * a.v_ts + (int64_t)hh[u] * a.v_hs + (cc[u] - a.ck));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (slot[u] < 0 || slot[u] >= a.num_slots) continue;  // outside the pool: skipped
+      if (cc[u] < a.ck)
+        a.k_buf[slot[u] * a.kb_ss + (int64_t)hh[u] * a.kb_hs + cc[u]] =
+            bf16x8_to_fp8x8<FMT>(val[u], a.k_scale);
+      else
+        a.v_buf[slot[u] * a.vb_ss + (int64_t)hh[u] * a.vb_hs + (cc[u] - a.ck)] =
+            bf16x8_to_fp8x8<FMT>(val[u], a.v_scale);
+    }
+  }
+}
+
+int launch_set_kv_buffer_fp8(const void *k, int64_t k_ts, int64_t k_hs, const void *v,
+                             int64_t v_ts, int64_t v_hs, const int64_t *cache_loc,
+                             int64_t n_tokens, int hkv, int lk, int lv, float k_scale,
+                             float v_scale, int fmt, void *k_buffer, int64_t kb_ss,
+                             int64_t kb_hs, void *v_buffer, int64_t vb_ss, int64_t vb_hs,
+                             int64_t num_slots, cudaStream_t st) {
+  KvWriteFp8Args a;
+  a.k = static_cast<const uint4 *>(k);
+  a.v = static_cast<const uint4 *>(v);
+  a.k_ts = k_ts / 8; a.k_hs = k_hs / 8; a.v_ts = v_ts / 8; a.v_hs = v_hs / 8;
+  a.cache_loc = cache_loc;
+  a.k_buf = static_cast<uint2 *>(k_buffer);
+  a.v_buf = static_cast<uint2 *>(v_buffer);
+  a.kb_ss = kb_ss / 8; a.kb_hs = kb_hs / 8; a.vb_ss = vb_ss / 8; a.vb_hs = vb_hs / 8;
+  a.num_slots = num_slots;
+  a.hkv = (uint32_t)hkv;
+  a.ck = (uint32_t)(lk / 8);
+  a.cv = v ? (uint32_t)(lv / 8) : 0u;
+  a.total = (uint64_t)n_tokens * a.hkv * (a.ck + a.cv);
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  if (a.total == 0) return PKX_OK;
+  if (a.total >= (1ull << 31))
+    return set_error(PKX_EUNSUPPORTED, "set_kv_buffer_fp8: 2^31 or more chunks in one call");
+  const int nsm = num_sms_current_device();
+  const uint64_t need = (a.total + kKvThreads * kUnroll - 1) / (kKvThreads * kUnroll);
+  const uint64_t cap = (uint64_t)nsm * 4;
+  const unsigned grid = (unsigned)(need < cap ? need : cap);
+  if (fmt == kKvFp8E4M3) set_kv_buffer_fp8_kernel<1><<<grid, kKvThreads, 0, st>>>(a);
+  else set_kv_buffer_fp8_kernel<2><<<grid, kKvThreads, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return set_error(PKX_ECUDA, "set_kv_buffer_fp8 launch: %s", cudaGetErrorString(e));
   return PKX_OK;
 }
 

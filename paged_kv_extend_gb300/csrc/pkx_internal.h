@@ -20,6 +20,9 @@ enum KeyMode : int {
   kDecode = 2,    // every key via int32 kv_indices, query at position T-1
 };
 
+// Element format of the KV pool (the values of include/pkx.h's PKX_KV_*).
+enum KvFormat : int { kKvBf16 = 0, kKvFp8E4M3 = 1, kKvFp8E5M2 = 2 };
+
 // Which keys a two-stage pass attends to (the ragged + paged split runs the
 // extend keys and the prefix keys as two passes and merges them).
 enum KeySet : int {
@@ -113,6 +116,8 @@ struct AttnArgs {
   const uint8_t *custom_mask;   // nullable: replaces the causal mask
   const int32_t *mask_indptr;   // [batch+1] offsets into custom_mask
   const float *sinks;           // nullable [hq] sink logits
+  int kv_fmt = 0;               // pool format: kKvBf16, kKvFp8E4M3, kKvFp8E5M2
+  float k_scale = 1.f, v_scale = 1.f;  // fp8 pool: key = code * k_scale, value = code * v_scale
   int key_set = kAllKeys;       // two-stage form: which keys this pass sees
   int keep_status = 0;          // a later pass of one call keeps the status word
   void *workspace;
@@ -131,6 +136,12 @@ int launch_set_kv_buffer(const void *k, int64_t k_ts, int64_t k_hs, const void *
                          int64_t v_hs, const int64_t *cache_loc, int64_t n_tokens, int hkv, int lk,
                          int lv, void *k_buffer, int64_t kb_ss, int64_t kb_hs, void *v_buffer,
                          int64_t vb_ss, int64_t vb_hs, int64_t num_slots, cudaStream_t s);
+int launch_set_kv_buffer_fp8(const void *k, int64_t k_ts, int64_t k_hs, const void *v,
+                             int64_t v_ts, int64_t v_hs, const int64_t *cache_loc,
+                             int64_t n_tokens, int hkv, int lk, int lv, float k_scale,
+                             float v_scale, int fmt, void *k_buffer, int64_t kb_ss,
+                             int64_t kb_hs, void *v_buffer, int64_t vb_ss, int64_t vb_hs,
+                             int64_t num_slots, cudaStream_t s);
 // Largest batch the index gather takes (its running sum lives in 48 KB of
 // shared memory).
 constexpr int kGatherMaxBatch = 12000;

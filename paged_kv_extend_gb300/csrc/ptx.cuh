@@ -131,6 +131,24 @@ __device__ __forceinline__ void cp_async_16_at(uint32_t dst, const void *src, ui
                "r"(src_bytes), "n"(DOFF), "n"(SOFF)
                : "memory");
 }
+// 8-byte global -> shared copy (8-byte copies exist only in the L1-allocating
+// form); src_bytes = 0 fills the 8 bytes with zeros.
+template <uint32_t DOFF>
+__device__ __forceinline__ void cp_async_8_at(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0+%3], [%1], 8, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "n"(DOFF)
+               : "memory");
+}
+__device__ __forceinline__ uint2 ld_shared_u2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
 // Arrive on `bar` (counted as one of its expected arrivals) once every
 // cp.async this thread has issued so far has landed.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {

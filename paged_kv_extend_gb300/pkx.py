@@ -49,17 +49,18 @@ _SIGS = {
     "pkx_extend_attention_fwd": (_i, [
         _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
         _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _p,
-        _p, _p, _sz, _p]),
+        _i, _f, _f, _p, _p, _sz, _p]),
     "pkx_ragged_paged_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "pkx_extend_attention_fwd_ragged_paged": (_i, [
         _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
-        _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _sz, _p]),
+        _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _i, _f, _f,
+        _p, _p, _sz, _p]),
     "pkx_extend_attention_fwd_unified": (_i, [
         _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
-        _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _p, _p, _p, _sz, _p]),
+        _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _p, _i, _f, _f, _p, _p, _sz, _p]),
     "pkx_decode_attention_fwd": (_i, [
         _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i,
-        _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _sz, _p]),
+        _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _i, _f, _f, _p, _p, _sz, _p]),
     "pkx_decode_attention_fwd_no_alloc": (_i, [
         _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i,
         _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p]),
@@ -67,6 +68,9 @@ _SIGS = {
     "pkx_build_unified_kv_indices": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _p, _p]),
     "pkx_set_kv_buffer": (_i, [
         _p, _i64, _i64, _p, _i64, _i64, _p, _i64, _i, _i, _i,
+        _p, _i64, _i64, _p, _i64, _i64, _i64, _p]),
+    "pkx_set_kv_buffer_fp8": (_i, [
+        _p, _i64, _i64, _p, _i64, _i64, _p, _i64, _i, _i, _i, _f, _f, _i,
         _p, _i64, _i64, _p, _i64, _i64, _i64, _p]),
     "pkx_create_kv_indices": (_i, [
         _p, _i64, _i64, _p, _p, _p, _i, _p, _p, _i64, _p]),
@@ -112,6 +116,26 @@ def _rows(t: torch.Tensor, name: str):
     if t.dtype != torch.bfloat16 or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA bf16 tensor")
     return t.stride(0), t.stride(1)
+
+
+# pool element formats (include/pkx.h PKX_KV_*)
+PKX_KV_BF16, PKX_KV_FP8_E4M3, PKX_KV_FP8_E5M2 = 0, 1, 2
+_KV_CODES = {torch.bfloat16: PKX_KV_BF16, torch.float8_e4m3fn: PKX_KV_FP8_E4M3,
+             torch.float8_e5m2: PKX_KV_FP8_E5M2}
+
+
+def _pool_rows(k_buffer: torch.Tensor, v_buffer: torch.Tensor):
+    """Strides of a bf16 or fp8 pool pair and its PKX_KV_* format."""
+    codes = [_KV_CODES.get(t.dtype) for t in (k_buffer, v_buffer)]
+    if codes[0] is None or codes[0] != codes[1]:
+        raise ValueError("k_buffer and v_buffer must both be bf16, float8_e4m3fn or float8_e5m2")
+    out = []
+    for t, nm in ((k_buffer, "k_buffer"), (v_buffer, "v_buffer")):
+        if t.dim() != 3 or t.stride(2) != 1 or not t.is_cuda:
+            raise ValueError(f"{nm} must be a CUDA [slots, heads, dim] tensor with a "
+                             "contiguous last dim")
+        out.append((t.stride(0), t.stride(1)))
+    return out[0], out[1], codes[0]
 
 
 def _i32(t: torch.Tensor, name: str):
@@ -175,10 +199,11 @@ def _workspace(ws, nbytes, dev):
 def extend_attention_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffer,
                          qo_indptr, kv_indptr, kv_indices, sm_scale=None, logit_cap=0.0,
                          sliding_window=-1, lse=None, workspace=None, custom_mask=None,
-                         mask_indptr=None, sinks=None):
+                         mask_indptr=None, sinks=None, k_scale=1.0, v_scale=1.0):
     """Two-stage extend attention (pkx_extend_attention_fwd); writes o_extend
     (and lse if given) in place.  Returns the workspace used.  custom_mask /
-    mask_indptr / sinks as in the C header."""
+    mask_indptr / sinks as in the C header.  The pool may be fp8
+    (torch.float8_e4m3fn / float8_e5m2) with k_scale / v_scale."""
     lib = load_library()
     n, hq, lq = q_extend.shape
     hkv = k_buffer.shape[1]
@@ -186,8 +211,7 @@ def extend_attention_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buf
     batch = qo_indptr.numel() - 1
     ke = _rows(k_extend, "k_extend")
     ve = _rows(v_extend, "v_extend")
-    kb = _rows(k_buffer, "k_buffer")
-    vb = _rows(v_buffer, "v_buffer")
+    kb, vb, kv_dtype = _pool_rows(k_buffer, v_buffer)
     for t, nm in ((q_extend, "q_extend"), (o_extend, "o_extend")):
         if not t.is_contiguous() or t.dtype != torch.bfloat16:
             raise ValueError(f"{nm} must be contiguous bf16")
@@ -199,8 +223,8 @@ def extend_attention_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buf
         _ptr(kv_indices) if kv_indices.numel() else None, batch, n, hq, hkv, lq, lv,
         ke[0], ke[1], ve[0], ve[1], kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0],
         float(sm_scale or 0.0), float(logit_cap or 0.0), int(sliding_window),
-        *_mask_sinks(custom_mask, mask_indptr, sinks), _ptr(lse),
-        _ptr(ws), ws.numel() * ws.element_size(), _stream(q_extend.device)))
+        *_mask_sinks(custom_mask, mask_indptr, sinks), kv_dtype, float(k_scale), float(v_scale),
+        _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(q_extend.device)))
     return ws
 
 
@@ -212,7 +236,7 @@ def ragged_paged_workspace_size(batch, num_q_tokens, hq, hkv, lq, lv) -> int:
 def extend_attention_fwd_ragged_paged(q_extend, k_extend, v_extend, o_extend, k_buffer,
                                       v_buffer, qo_indptr, kv_indptr, kv_indices, sm_scale=None,
                                       logit_cap=0.0, sliding_window=-1, lse=None,
-                                      workspace=None):
+                                      workspace=None, k_scale=1.0, v_scale=1.0):
     """Extend attention as a ragged pass over the extend keys, a paged pass
     over the prefix keys and merge_state of the two
     (pkx_extend_attention_fwd_ragged_paged); arguments as
@@ -224,8 +248,7 @@ def extend_attention_fwd_ragged_paged(q_extend, k_extend, v_extend, o_extend, k_
     batch = qo_indptr.numel() - 1
     ke = _rows(k_extend, "k_extend")
     ve = _rows(v_extend, "v_extend")
-    kb = _rows(k_buffer, "k_buffer")
-    vb = _rows(v_buffer, "v_buffer")
+    kb, vb, kv_dtype = _pool_rows(k_buffer, v_buffer)
     for t, nm in ((q_extend, "q_extend"), (o_extend, "o_extend")):
         if not t.is_contiguous() or t.dtype != torch.bfloat16:
             raise ValueError(f"{nm} must be contiguous bf16")
@@ -237,15 +260,16 @@ def extend_attention_fwd_ragged_paged(q_extend, k_extend, v_extend, o_extend, k_
         _ptr(v_buffer), _ptr(qo_indptr), _ptr(kv_indptr),
         _ptr(kv_indices) if kv_indices.numel() else None, batch, n, hq, hkv, lq, lv,
         ke[0], ke[1], ve[0], ve[1], kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0],
-        float(sm_scale or 0.0), float(logit_cap or 0.0), int(sliding_window), _ptr(lse),
-        _ptr(ws), ws.numel() * ws.element_size(), _stream(q_extend.device)))
+        float(sm_scale or 0.0), float(logit_cap or 0.0), int(sliding_window), kv_dtype,
+        float(k_scale), float(v_scale), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(q_extend.device)))
     return ws
 
 
 def extend_attention_fwd_unified(q, o, k_buffer, v_buffer, qo_indptr, kv_indptr, kv_indices,
                                  prefix_lens, sm_scale=None, logit_cap=0.0, sliding_window=-1,
                                  lse=None, workspace=None, custom_mask=None, mask_indptr=None,
-                                 sinks=None):
+                                 sinks=None, k_scale=1.0, v_scale=1.0):
     """Unified extend attention (pkx_extend_attention_fwd_unified); int64
     kv_indices over every key.  Writes o (and lse) in place."""
     lib = load_library()
@@ -253,8 +277,7 @@ def extend_attention_fwd_unified(q, o, k_buffer, v_buffer, qo_indptr, kv_indptr,
     hkv = k_buffer.shape[1]
     lv = v_buffer.shape[2]
     batch = qo_indptr.numel() - 1
-    kb = _rows(k_buffer, "k_buffer")
-    vb = _rows(v_buffer, "v_buffer")
+    kb, vb, kv_dtype = _pool_rows(k_buffer, v_buffer)
     if kv_indices.dtype != torch.int64 or not kv_indices.is_contiguous():
         raise ValueError("kv_indices must be contiguous int64")
     _i32(qo_indptr, "qo_indptr"), _i32(kv_indptr, "kv_indptr"), _i32(prefix_lens, "prefix_lens")
@@ -264,27 +287,29 @@ def extend_attention_fwd_unified(q, o, k_buffer, v_buffer, qo_indptr, kv_indptr,
         _ptr(kv_indices) if kv_indices.numel() else None, _ptr(prefix_lens), batch, n, hq, hkv,
         lq, lv, kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0], float(sm_scale or 0.0),
         float(logit_cap or 0.0), int(sliding_window),
-        *_mask_sinks(custom_mask, mask_indptr, sinks), _ptr(lse), _ptr(ws),
-        ws.numel() * ws.element_size(), _stream(q.device)))
+        *_mask_sinks(custom_mask, mask_indptr, sinks), kv_dtype, float(k_scale),
+        float(v_scale), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(q.device)))
     return ws
 
 
 def decode_attention_fwd(q, o, k_buffer, v_buffer, kv_indptr, kv_indices, sm_scale=None,
-                         logit_cap=0.0, sliding_window=-1, lse=None, workspace=None):
+                         logit_cap=0.0, sliding_window=-1, lse=None, workspace=None,
+                         k_scale=1.0, v_scale=1.0):
     """Decode attention (pkx_decode_attention_fwd): q [B, Hq, Lq] -> o."""
     lib = load_library()
     b, hq, lq = q.shape
     hkv = k_buffer.shape[1]
     lv = v_buffer.shape[2]
-    kb = _rows(k_buffer, "k_buffer")
-    vb = _rows(v_buffer, "v_buffer")
+    kb, vb, kv_dtype = _pool_rows(k_buffer, v_buffer)
     _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
     ws = _workspace(workspace, decode_workspace_size(b, hq, hkv, lq, lv), q.device)
     _check(lib.pkx_decode_attention_fwd(
         _ptr(q), _ptr(o), _ptr(k_buffer), _ptr(v_buffer), _ptr(kv_indptr),
         _ptr(kv_indices) if kv_indices.numel() else None, b, hq, hkv, lq, lv,
         kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0], float(sm_scale or 0.0),
-        float(logit_cap or 0.0), int(sliding_window), _ptr(lse), _ptr(ws),
+        float(logit_cap or 0.0), int(sliding_window), kv_dtype, float(k_scale),
+        float(v_scale), _ptr(lse), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(q.device)))
     return ws
 
@@ -421,3 +446,29 @@ def create_kv_indices(req_to_token, req_pool_indices, paged_kernel_lens, kv_star
         _ptr(kv_indptr), _ptr(kv_indices) if kv_indices.numel() else None,
         kv_indices.numel(), _stream(dev)))
     return kv_indptr, kv_indices
+
+
+def set_kv_buffer_fp8(k_buffer, v_buffer, cache_loc, k, v, k_scale, v_scale):
+    """KV write into an fp8 pool (pkx_set_kv_buffer_fp8): k[t] / k_scale and
+    v[t] / v_scale as fp8 codes at slot cache_loc[t], in place.  Pools are
+    torch.float8_e4m3fn or float8_e5m2 [slots, hkv, d]; ``v`` None writes K
+    only."""
+    lib = load_library()
+    _i64_vec(cache_loc, "cache_loc")
+    n, hkv, lk = k.shape
+    if cache_loc.numel() != n:
+        raise ValueError("cache_loc must hold one slot per token")
+    kb, vb, fmt = _pool_rows(k_buffer, v_buffer)
+    if fmt == PKX_KV_BF16:
+        raise ValueError("set_kv_buffer_fp8 needs fp8 pools")
+    ks = _rows(k, "k")
+    lv, vs = 0, (0, 0)
+    if v is not None:
+        vs = _rows(v, "v")
+        lv = v.shape[2]
+    _check(lib.pkx_set_kv_buffer_fp8(
+        _ptr(k), ks[0], ks[1], _ptr(v), vs[0], vs[1], _ptr(cache_loc) if n else None, n, hkv,
+        lk, lv, float(k_scale), float(v_scale), fmt, _ptr(k_buffer), kb[0], kb[1],
+        _ptr(v_buffer) if v is not None else None, vb[0], vb[1], k_buffer.shape[0],
+        _stream(k.device)))
+    return k_buffer, v_buffer

@@ -191,6 +191,19 @@ class Workload:
             return k, k[..., : self.spec.lv]
         return k, self.v_rows.index_select(0, rows).to(device)
 
+    def pool_fp8(self, dtype, k_scale: float, v_scale: float, device="cpu"):
+        """The pool in an fp8 format (torch.float8_e4m3fn or float8_e5m2):
+        every token row divided by its scale and converted by torch, zero
+        elsewhere.  (k_buffer, v_buffer) as one-byte tensors of that dtype."""
+        s = self.spec
+        slots = self.slots.to(torch.int64)
+        k = torch.zeros(s.num_slots, s.hkv, s.lq, dtype=torch.uint8)
+        v = torch.zeros(s.num_slots, s.hkv, s.lv, dtype=torch.uint8)
+        if slots.numel():
+            k[slots] = (self.k_rows.float() / k_scale).to(dtype).view(torch.uint8)
+            v[slots] = (self.v_rows.float() / v_scale).to(dtype).view(torch.uint8)
+        return k.view(dtype).to(device), v.view(dtype).to(device)
+
     def req_to_token(self, rows: Optional[int] = None, cols: Optional[int] = None,
                      seed: int = 0):
         """A request-to-token table holding this batch: sequence b sits in a

@@ -31,7 +31,8 @@ def test_header_declares_the_boundary():
     for must in ["pkx_extend_attention_fwd", "pkx_extend_attention_fwd_unified",
                  "pkx_decode_attention_fwd", "pkx_merge_state",
                  "pkx_build_unified_kv_indices", "pkx_extend_workspace_size",
-                 "pkx_set_kv_buffer", "pkx_create_kv_indices",
+                 "pkx_set_kv_buffer", "pkx_create_kv_indices", "pkx_set_kv_buffer_fp8",
+                 "pkx_extend_attention_fwd_ragged_paged",
                  "pkx_decode_workspace_size", "pkx_workspace_status",
                  "pkx_last_error_string", "pkx_version"]:
         assert must in names
@@ -52,13 +53,13 @@ def _extend(lib, **over):
     a = dict(q=None, k=None, v=None, o=None, kb=None, vb=None, qo=None, kvp=None, kvi=None,
              batch=1, n=4, hq=8, hkv=2, lq=128, lv=128, st=(1024, 128, 1024, 128, 1024, 128, 1024, 128),
              slots=16, scale=0.0, cap=0.0, win=-1, mask=None, mask_indptr=None, sinks=None,
-             lse=None, ws=None, wsb=0, stream=None)
+             kvd=0, ksc=1.0, vsc=1.0, lse=None, ws=None, wsb=0, stream=None)
     a.update(over)
     return lib.pkx_extend_attention_fwd(
         a["q"], a["k"], a["v"], a["o"], a["kb"], a["vb"], a["qo"], a["kvp"], a["kvi"],
         a["batch"], a["n"], a["hq"], a["hkv"], a["lq"], a["lv"], *a["st"], a["slots"],
-        a["scale"], a["cap"], a["win"], a["mask"], a["mask_indptr"], a["sinks"], a["lse"],
-        a["ws"], a["wsb"], a["stream"])
+        a["scale"], a["cap"], a["win"], a["mask"], a["mask_indptr"], a["sinks"], a["kvd"],
+        a["ksc"], a["vsc"], a["lse"], a["ws"], a["wsb"], a["stream"])
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -80,6 +81,12 @@ def test_host_validation_rejects_bad_arguments(lib):
     # stride not a multiple of 8 elements
     assert _extend(lib, q=0x1000, o=0x1000, k=0x1000, v=0x1000, kb=0x1000, vb=0x1000,
                    st=(1024, 127, 1024, 128, 1024, 128, 1024, 128)) == pkx.PKX_EINVAL
+    # pool format: an unknown format, bad scales, fp8 where it is not built
+    assert _extend(lib, kvd=3) == pkx.PKX_EINVAL
+    assert _extend(lib, kvd=1, ksc=0.0) == pkx.PKX_EINVAL
+    assert _extend(lib, kvd=2, vsc=float("inf")) == pkx.PKX_EINVAL
+    assert _extend(lib, kvd=1, lq=576, lv=512, hq=16, hkv=1) == pkx.PKX_EUNSUPPORTED
+    assert _extend(lib, kvd=1, mask=0x1000, mask_indptr=0x1000) == pkx.PKX_EUNSUPPORTED
     # empty problem: nothing to do, succeeds without touching a device
     assert _extend(lib, batch=0) == pkx.PKX_OK
     assert _extend(lib, n=0) == pkx.PKX_OK
@@ -92,6 +99,19 @@ def test_merge_and_index_validation(lib):
     assert lib.pkx_build_unified_kv_indices(None, None, None, None, None, 3, None, None, None,
                                             None) == pkx.PKX_EINVAL
     assert lib.pkx_workspace_status(None, None) == pkx.PKX_EINVAL
+
+
+def test_fp8_write_validation(lib):
+    A = 0x10000
+    w = lambda **o: lib.pkx_set_kv_buffer_fp8(
+        A, 256, 128, A, 256, 128, A, o.get("n", 4), 2, 128, 128, o.get("ks", 1.0),
+        o.get("vs", 1.0), o.get("fmt", 1), A, 256, 128, A, 256, 128, 64, None)
+    assert w(fmt=0) == pkx.PKX_EINVAL        # bf16 is not an fp8 format
+    assert w(fmt=3) == pkx.PKX_EINVAL
+    assert w(ks=-1.0) == pkx.PKX_EINVAL
+    assert w(vs=float("nan")) == pkx.PKX_EINVAL
+    assert w(n=0) == pkx.PKX_OK
+    assert w(n=0, fmt=2) == pkx.PKX_OK
 
 
 def test_kv_write_and_gather_validation(lib):
