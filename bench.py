@@ -91,11 +91,11 @@ def extend_flops(wl: W.Workload) -> float:
     return 2.0 * (s.lq + s.lv) * s.hq * visible_pairs(s, wl.prefix_lens, wl.extend_lens)
 
 
-def extend_bytes(wl: W.Workload, unified: bool) -> float:
+def extend_bytes(wl: W.Workload, unified: bool, kv_elem_bytes: int = 2) -> float:
     """Algorithmic bytes: every visible K/V row once per (sequence, KV head),
     4 B per prefix index (8 B per unified index), Q read, O write, lse."""
     s = wl.spec
-    kv_row = (s.lq if s.v_aliases_k else s.lq + s.lv) * 2
+    kv_row = (s.lq if s.v_aliases_k else s.lq + s.lv) * kv_elem_bytes
     keys = 0
     for p, e in zip(wl.prefix_lens, wl.extend_lens):
         if e == 0:
@@ -108,9 +108,9 @@ def extend_bytes(wl: W.Workload, unified: bool) -> float:
     return keys * s.hkv * kv_row + idx + qo
 
 
-def decode_bytes(wl: W.Workload) -> float:
+def decode_bytes(wl: W.Workload, kv_elem_bytes: int = 2) -> float:
     s = wl.spec
-    kv_row = (s.lq if s.v_aliases_k else s.lq + s.lv) * 2
+    kv_row = (s.lq if s.v_aliases_k else s.lq + s.lv) * kv_elem_bytes
     keys = 0
     for p in wl.prefix_lens:
         T = p + 1
@@ -325,13 +325,15 @@ class ExtendStep:
     """Device-resident inputs and the one-step call sequence (unified
     index build + unified extend attention)."""
 
-    def __init__(self, wl: W.Workload, dev):
+    def __init__(self, wl: W.Workload, dev, fp8=None):
         from paged_kv_extend_gb300 import pkx
         self.pkx = pkx
         s = wl.spec
         self.wl = wl
         self.dev = dev
-        self.kb, self.vb = wl.pool(dev)
+        self.kv_scales = {"k_scale": FP8_SCALE, "v_scale": FP8_SCALE} if fp8 is not None else {}
+        self.kb, self.vb = (wl.pool(dev) if fp8 is None
+                            else wl.pool_fp8(fp8, FP8_SCALE, FP8_SCALE, dev))
         self.q = wl.q.to(dev)
         self.prefix_indptr = wl.kv_indptr.to(dev)
         self.prefix_indices = wl.kv_indices.to(dev)
@@ -353,7 +355,7 @@ class ExtendStep:
         self.sinks = wl.sinks.to(dev).float() if wl.sinks is not None else None
         self.launches = 4  # index build, scheduler, attention, combine
         self.flops = extend_flops(wl)
-        self.bytes = extend_bytes(wl, unified=True)
+        self.bytes = extend_bytes(wl, unified=True, kv_elem_bytes=1 if fp8 is not None else 2)
 
     def inputs(self):
         ins = [self.q, self.prefix_indptr, self.prefix_indices, self.extend_start,
@@ -382,18 +384,21 @@ class ExtendStep:
         self.pkx.extend_attention_fwd_unified(
             self.q, self.o, self.kb, self.vb, self.qo_indptr, self.uptr, self.uidx, self.plen,
             self.wl.sm_scale, s.logit_cap, s.sliding_window, lse=self.lse, workspace=self.ws,
-            custom_mask=self.custom_mask, mask_indptr=self.mask_indptr, sinks=self.sinks)
+            custom_mask=self.custom_mask, mask_indptr=self.mask_indptr, sinks=self.sinks,
+            **self.kv_scales)
 
 
 class DecodeStep:
     """One decode step over a decode workload (one query per sequence)."""
 
-    def __init__(self, wl: W.Workload, dev):
+    def __init__(self, wl: W.Workload, dev, fp8=None):
         from paged_kv_extend_gb300 import pkx
         self.pkx = pkx
         s = wl.spec
         self.wl = wl
-        self.kb, self.vb = wl.pool(dev)
+        self.kv_scales = {"k_scale": FP8_SCALE, "v_scale": FP8_SCALE} if fp8 is not None else {}
+        self.kb, self.vb = (wl.pool(dev) if fp8 is None
+                            else wl.pool_fp8(fp8, FP8_SCALE, FP8_SCALE, dev))
         self.q = wl.q.to(dev)
         self.kvp, self.kvi = wl.kv_indptr.to(dev), wl.kv_indices.to(dev)
         self.o = torch.empty(s.batch, s.hq, s.lv, dtype=torch.bfloat16, device=dev)
@@ -404,7 +409,7 @@ class DecodeStep:
         self.flops = 2.0 * (s.lq + s.lv) * s.hq * sum(
             min(p + 1, s.sliding_window + 1) if s.sliding_window > 0 else p + 1
             for p in wl.prefix_lens)
-        self.bytes = decode_bytes(wl)
+        self.bytes = decode_bytes(wl, kv_elem_bytes=1 if fp8 is not None else 2)
 
     def inputs(self):
         return [self.q, self.kvp, self.kvi]
@@ -419,12 +424,16 @@ class DecodeStep:
         s = self.wl.spec
         self.pkx.decode_attention_fwd(self.q, self.o, self.kb, self.vb, self.kvp, self.kvi,
                                       self.wl.sm_scale, s.logit_cap, s.sliding_window,
-                                      lse=self.lse, workspace=self.ws)
+                                      lse=self.lse, workspace=self.ws, **self.kv_scales)
 
 
-def make_step(name, dev):
+# k_scale = v_scale of the fp8-pool measurements (N(0, 1) rows stay in range)
+FP8_SCALE = 0.5
+
+
+def make_step(name, dev, fp8=None):
     wl = W.draw(W.SPECS[name])
-    return (DecodeStep if wl.spec.decode else ExtendStep)(wl, dev)
+    return (DecodeStep if wl.spec.decode else ExtendStep)(wl, dev, fp8=fp8)
 
 
 def flush_l2(flush):
@@ -553,17 +562,19 @@ def e2e_entry(pipelined, serial, unit, h2d, d2h):
             "pipelined_value": pipelined, "serial_value": serial}
 
 
-def measure_component(name, dev, flush, steps, hbm_peak, bf16_peak):
+def measure_component(name, dev, flush, steps, hbm_peak, bf16_peak, fp8=None):
     """One workload's step, device-timed, with the attention kernel's own
-    time; TFLOP/s and GB/s of algorithmic work and the roofline fractions."""
+    time; TFLOP/s and GB/s of algorithmic work and the roofline fractions.
+    fp8: the pool in that torch float8 dtype (k_scale = v_scale = 0.5)."""
     from paged_kv_extend_gb300 import pkx
-    step = make_step(name, dev)
+    step = make_step(name, dev, fp8=fp8)
     for _ in range(3):
         step()
     ms, attn = time_steps(step, steps, flush, dev, attn_events=True, pkx=pkx)
     status = pkx.workspace_status(step.ws)
     m, a = sum(ms) / len(ms), sum(attn) / len(attn)
-    out = {"workload": f"{name}: {WORKLOAD_TEXT.get(name, '')}", "ms": m, "attn_kernel_ms": a,
+    pool = "" if fp8 is None else f" [pool {str(fp8).replace('torch.', '')}, scales {FP8_SCALE}]"
+    out = {"workload": f"{name}: {WORKLOAD_TEXT.get(name, '')}{pool}", "ms": m, "attn_kernel_ms": a,
            "TFLOP/s": step.flops / (m * 1e-3) / 1e12,
            "attn_kernel_TFLOP/s": step.flops / (a * 1e-3) / 1e12,
            "GB/s": step.bytes / (m * 1e-3) / 1e9,
@@ -726,12 +737,17 @@ def run_ours(args, ws, rank, local):
     components = {"attn_kernel_share_of_step": attn_avg / ms}
     if not args.no_components:
         names = (args.components.split(",") if args.components
-                 else ["decode_gqa", "mla", "kv_ops", "split"])
+                 else ["decode_gqa", "mla", "kv_ops", "split", "decode_gqa_fp8"])
         if args.all_workloads:
             names = ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla", "kv_ops",
-                     "split"]
+                     "split", "decode_gqa_fp8", "long_prefix_fp8", "llama3_8b_fp8"]
         for name in names:
             if name == args.workload:
+                continue
+            if name.endswith("_fp8"):
+                components[name] = measure_component(name[:-4], dev, flush,
+                                                     max(5, min(args.steps, 20)), hbm_peak,
+                                                     bf16_peak, fp8=torch.float8_e4m3fn)
                 continue
             if name == "split":
                 components.update(measure_split(dev, flush, max(5, min(args.steps, 20)),
@@ -818,7 +834,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--components", default="",
                     help="comma-separated components to measure besides the step (workload "
-                         "names, kv_ops, split; default decode_gqa,mla,kv_ops,split)")
+                         "names, a workload name + _fp8 for an e4m3 pool, kv_ops, split; "
+                         "default decode_gqa,mla,kv_ops,split,decode_gqa_fp8)")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(W.SPECS),
                     help="workload of the timed step (default: the Llama-3-8B-shaped layer)")
     ap.add_argument("--all-workloads", action="store_true",
