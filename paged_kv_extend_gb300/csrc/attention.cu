@@ -63,6 +63,7 @@ struct SchedParams {
   int no_causal;   // a custom mask replaces the causal mask: blocks see every key
   int key_set;     // two-stage form only: kAllKeys, kPrefixKeys or kExtendKeys
   int keep_status; // leave the status word as an earlier pass left it
+  int two_streams; // decode units run two key streams, each with its own partial slot
   int n_dsplit;  // units per (block, split): value-dim slices (1, or 4 for MLA)
   int unit_target, qb_max, unit_max, comb_max, slot_max;
   int32_t *seq;  // 8 arrays of batch+1 ints
@@ -275,12 +276,16 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   auto splits = [&](int nt) { return nt > 0 ? (nt + C - 1) / C : 1; };
   const int chunk = (total_qb + 1023) / 1024;
   const int qb_beg = min(total_qb, tid * chunk), qb_end = min(total_qb, qb_beg + chunk);
+  // two key streams: every unit has two partial slots and every block a
+  // combine entry
+  const int spu = p.two_streams ? 2 : 1;
+  auto combined = [&](int S) { return S > 1 || p.two_streams; };
   int lu = 0, ls = 0, lc = 0;
   for (int qb = qb_beg; qb < qb_end; ++qb) {
     const int S = splits(qbt[qb]);
     lu += S * nd;
-    if (S > 1) {
-      ls += S;
+    if (combined(S)) {
+      ls += S * spu;
       lc += 1;
     }
   }
@@ -294,8 +299,8 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     qco[qb] = c0;
     const int S = splits(qbt[qb]);
     u0 += S * nd;
-    if (S > 1) {
-      s0 += S;
+    if (combined(S)) {
+      s0 += S * spu;
       c0 += 1;
     }
   }
@@ -325,13 +330,13 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     const int tps = nt > 0 ? (nt + S - 1) / S : 0;
     int uo = kvh * tu + quo[qb];
     const int so = kvh * ts + qso[qb];
-    if (S > 1) {
+    if (combined(S)) {
       CombineEntry e;
       e.q_tok0 = d.qbase + i0;
       e.n_tok = i1 - i0;
       e.kvh = kvh;
       e.slot0 = so;
-      e.n_split = S;
+      e.n_split = S * spu;
       e.pad[0] = e.pad[1] = e.pad[2] = 0;
       p.comb[kvh * tcm + qco[qb]] = e;
     }
@@ -347,7 +352,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
         w.k_split = split_at;
         w.n_tiles = range_tiles(w.k_begin, w.k_end, split_at, p.bn);
         w.b = b;
-        w.slot = S > 1 ? so + sp : -1;
+        w.slot = combined(S) ? so + sp * spu : -1;
         w.dq = dq;
         w.pad = 0;
         p.units[uo++] = w;
@@ -608,9 +613,11 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         break;
       }
       const WorkUnit w = p.units[p.uorder[u]];
-      const int nt = w.n_tiles;
-      const int tok0 = wg * TOK;  // first token of this Q tile in the block
-      if (wg == 1 && w.n_tok <= TOK) continue;
+      // decode: warpgroup wg takes the unit's tiles wg, wg + 2, ... of the
+      // one query tile (two key streams, merged by the combine)
+      const int nt = MODE == kDecode ? (w.n_tiles + 1 - wg) / 2 : w.n_tiles;
+      const int tok0 = MODE == kDecode ? 0 : wg * TOK;  // first token of this Q tile
+      if (MODE != kDecode && wg == 1 && w.n_tok <= TOK) continue;
       const int n_tok_i = min(TOK, w.n_tok - tok0);
       const int rows_valid = n_tok_i * G;
       const bool valid = r < rows_valid;
@@ -619,7 +626,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       const int qpos = w.qpos0 + t;
       const int qmin = w.qpos0 + tok0, qmax = w.qpos0 + tok0 + n_tok_i - 1;
       const int64_t orow_idx = (int64_t)(w.q_tok0 + t) * p.hq + w.kvh * G + g;
-      const int64_t prow_idx = (int64_t)w.slot * p.rows_per_slot + tok0 * G + r;
+      const int64_t prow_idx =
+          (int64_t)(w.slot + (MODE == kDecode ? wg : 0)) * p.rows_per_slot + tok0 * G + r;
       // custom mask rows: a byte per key of the sequence for each extend
       // token; mbase is the row of this Q tile's first token
       const uint8_t *mbase = nullptr;
@@ -650,7 +658,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j) {
         int kb, ke;
-        tile_keys(w, j, kb, ke);
+        tile_keys(w, MODE == kDecode ? 2 * j + wg : j, kb, ke);
         // Mask bits of this thread's row for keys kb + 32 q + bit (q < 4).
         // The G heads of a token share its mask row, so the warp walks its
         // rows' tokens: all lanes read 32 consecutive bytes of the token's
@@ -917,6 +925,18 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         });
         tc_commit(&bars[B_S_FULL + qt]);
       };
+      // S of query tile 0 into S/P buffer `buf` (the decode streams)
+      auto issue_s_q0 = [&](int buf, uint32_t sK) {
+        const uint32_t a_lo = K_LO | (sQ0 >> 4), b_lo = K_LO | (sK >> 4);
+        const uint32_t d = tmem + buf * C::BN;
+        static_for<0, HD / 16>([&](auto kk_c) {
+          constexpr int kk = decltype(kk_c)::value;
+          constexpr uint32_t ao = ((kk / 4) * (C::BM * 128) + (kk % 4) * 32) / 16;
+          constexpr uint32_t bo = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) / 16;
+          tc_mma_ss_step<ao, bo>(d, a_lo, b_lo, K_HI, C::IDESC_QK, kk > 0 ? 1u : 0u);
+        });
+        tc_commit(&bars[B_S_FULL + buf]);
+      };
       auto issue_pv = [&](int qt, uint32_t sV, bool acc_first) {
         const uint32_t b_lo = V_LO | (sV >> 4);
         const uint32_t d = tmem + 2 * C::BN + qt * C::HDV, a = tmem + qt * C::BN;
@@ -936,6 +956,58 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         if (!mbar_wait(&bars[B_Q_FULL], q_cnt & 1u, abort_flag)) { ok = false; break; }
         ++q_cnt;
         tc_fence_after();
+        if constexpr (MODE == kDecode) {
+          // Two key streams over the one query tile: even tiles into S/P
+          // buffer 0 (softmax warpgroup 0, O 0), odd tiles into buffer 1
+          // (warpgroup 1, O 1).  S(j) waits only for PV(j-2), which reads
+          // the P it overwrites, so one stream's softmax runs while the
+          // other's products do.
+          for (int j = 0; j < nt && ok; ++j) {
+            const int b = j & 1;
+            if (j >= 2) {
+              const int vs = vc % C::NV;
+              uint32_t &pc = b ? p_cnt1 : p_cnt0;
+              if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag) ||
+                  !mbar_wait(&bars[B_P_FULL + b], pc & 1u, abort_flag)) {
+                ok = false;
+                break;
+              }
+              ++pc;
+              fence_proxy_async_smem();
+              tc_fence_after();
+              issue_pv(b, sbase + C::OFF_V + vs * C::V_BYTES, j >= 4);
+              tc_commit(&v_empty[vs]);
+              ++vc;
+            }
+            const int ks = kc % C::NK;
+            if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag)) { ok = false; break; }
+            fence_proxy_async_smem();
+            tc_fence_after();
+            issue_s_q0(b, sbase + C::OFF_K + ks * C::K_BYTES);
+            tc_commit(&k_empty[ks]);
+            ++kc;
+            if (j == nt - 1) tc_commit(&bars[B_Q_EMPTY]);
+          }
+          // the last PV of each stream, in tile order
+          for (int j = nt >= 2 ? nt - 2 : 0; j < nt && ok; ++j) {
+            const int b = j & 1;
+            const int vs = vc % C::NV;
+            uint32_t &pc = b ? p_cnt1 : p_cnt0;
+            if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag) ||
+                !mbar_wait(&bars[B_P_FULL + b], pc & 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            ++pc;
+            fence_proxy_async_smem();
+            tc_fence_after();
+            issue_pv(b, sbase + C::OFF_V + vs * C::V_BYTES, j >= 2);
+            tc_commit(&bars[B_O_DONE + b]);
+            tc_commit(&v_empty[vs]);
+            ++vc;
+          }
+          continue;
+        }
         // tile 0: S of both Q tiles
         {
           const int ks = kc % C::NK;
@@ -1422,6 +1494,12 @@ WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int 
   L.unit_max = (L.unit_target + hkv * L.qb_max) * (mla ? 4 : 1);
   L.slot_max = 2 * L.unit_target;
   L.comb_max = L.unit_target;
+  if (decode && !mla) {
+    // two key streams per unit: two partial slots per unit, a combine entry
+    // per (query block, KV head)
+    L.slot_max = 2 * L.unit_max;
+    L.comb_max = L.unit_target + hkv * L.qb_max;
+  }
   L.rows_per_slot = rows_per_slot(decode, group, mla);
   size_t off = align256(sizeof(WsHeader));
   L.seq_off = off;
@@ -1560,6 +1638,7 @@ int launch_attention(const AttnArgs &a) {
   sp.no_causal = a.custom_mask != nullptr;
   sp.key_set = a.mode == kTwoStage ? a.key_set : kAllKeys;
   sp.keep_status = a.keep_status;
+  sp.two_streams = decode && !mla;
   sp.n_dsplit = mla ? MlaCfg<0>::LV / MlaCfg<0>::DVS : 1;
   sp.window = a.window;
   sp.num_q_tokens = nq;
