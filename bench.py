@@ -792,7 +792,7 @@ def run_ours(args, ws, rank, local):
         value = step.bytes * ws / (ms_max * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": step.bytes / (attn_avg * 1e-3) / 1e9,
                 "peak": hbm_peak, "unit": "GB/s",
-                "frac": step.bytes / (attn_avg * 1e-3) / 1e9 / hbm_peak, "traffic": None,
+                "frac": step.bytes / (attn_avg * 1e-3) / 1e9 / hbm_peak, "traffic": traffic,
                 "peak_source": f"hbm_gbs copy bandwidth, of {peak_src}",
                 "kernel": "attn_kernel (decode)", "algorithmic_bytes_per_launch": step.bytes}
         e2e_value = step.bytes * ws / (e2e_ms * 1e-3) / 1e9
