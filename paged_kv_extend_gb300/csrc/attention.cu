@@ -401,7 +401,7 @@ struct KParams {
   // go to shared memory as exact bf16; k_scale is folded into the logit
   // scale of pool tiles, v_scale into their P through the exponent
   // (2^(s - m + log2 v_scale)), and the tile's row sum is divided back
-  float scale_log2_k, cap_pre_k, log2_v_scale, inv_v_scale;
+  float scale_log2_k, cap_pre_k, log2_v_scale, inv_v_scale, v_scale;
   const int32_t *prefix_lens;   // unified form: prefix length per sequence
   const WorkUnit *units;
   const int32_t *uorder;  // units by cost, largest first
@@ -460,6 +460,7 @@ enum {
   B_FINAL = 8,
   B_U_FULL = 9,    // + unit ring slot (kUnitRing)
   B_U_EMPTY = 12,  // + unit ring slot
+  B_Q_CONV = 15,   // decode over fp8: the query rows converted to f16
   B_RING = 16,  // K full[NK], K empty[NK], V full[NV], V empty[NV],
                 // I full[NI], I empty[NI]
 };
@@ -530,12 +531,58 @@ __device__ __forceinline__ uint4 fp8x8_to_bf16x8(uint2 raw) {
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// Eight fp8 codes as eight f16 of the same values (exact), element order
+// kept: an e5m2 code is the top byte of its f16; e4m3 goes through the
+// converter.
+template <int FMT>
+__device__ __forceinline__ uint4 fp8x8_to_f16x8(uint2 raw) {
+  uint32_t out[4];
+  if constexpr (FMT == 2) {
+    out[0] = __byte_perm(raw.x, 0u, 0x1404);
+    out[1] = __byte_perm(raw.x, 0u, 0x3424);
+    out[2] = __byte_perm(raw.y, 0u, 0x1404);
+    out[3] = __byte_perm(raw.y, 0u, 0x3424);
+  } else {
+    const uint32_t w[2] = {raw.x, raw.y};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+          static_cast<__nv_fp8x2_storage_t>(w[i >> 1] >> (16 * (i & 1))), __NV_E4M3);
+      out[i] = (uint32_t)h.x | ((uint32_t)h.y << 16);
+    }
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// Eight bf16 times 2^-8 as eight f16 (round to nearest): the power of two
+// keeps any bf16 of magnitude below 2^24 inside the f16 range; the logit
+// scale takes the 2^8 back.
+constexpr float kQF16Down = 0x1p-8f, kQF16Up = 256.0f;
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16) * kQF16Down;
+    const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * kQF16Down;
+    const __half2 h = __floats2half2_rn(lo, hi);
+    out[i] = *reinterpret_cast<const uint32_t *>(&h);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 // FMT: the pool's element format (0 bf16; 1 fp8 e4m3, 2 fp8 e5m2 with
 // k_scale / v_scale).  Extend rows of the two-stage form are always bf16.
 template <int HD, int MODE, bool MASK, int FMT = 0>
 __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     attn_kernel(const __grid_constant__ TMaps tm, const KParams p) {
   using C = Cfg<HD>;
+  // Decode over an fp8 pool runs its products in f16: a code becomes f16 in
+  // one step (exact), the unit's query rows are converted once (times 2^-8),
+  // P is written as f16 and v_scale is applied to the output.
+  constexpr bool F16 = FMT != 0 && MODE == kDecode;
+  constexpr uint32_t IDQK = F16 ? idesc_f16_f32(C::BM, C::BN, 0) : C::IDESC_QK;
+  constexpr uint32_t IDPV = F16 ? idesc_f16_f32(C::BM, C::HDV, 1) : C::IDESC_PV;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -558,6 +605,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
 
   if (tid == 0) {
     mbar_init(&bars[B_Q_FULL], 1);
+    mbar_init(&bars[B_Q_CONV], C::COPY_THREADS);
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[B_S_FULL + i], 1);
@@ -721,9 +769,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           // A tile of an fp8 pool holds the codes: its logits take k_scale
           // in the scale, its P takes v_scale.
           const bool pool8 = FMT != 0 && !(MODE == kTwoStage && kb >= w.k_split);
-          float sc = pool8 ? p.scale_log2_k : p.scale_log2;
+          float sc = pool8 ? p.scale_log2_k * (F16 ? kQF16Up : 1.0f) : p.scale_log2;
           if (p.use_cap) {
-            const float pre = pool8 ? p.cap_pre_k : p.cap_pre;
+            const float pre = pool8 ? p.cap_pre_k * (F16 ? kQF16Up : 1.0f) : p.cap_pre;
 #pragma unroll
             for (int i = 0; i < C::BN; ++i) x[i] = p.cap_log2 * tanh_approx(x[i] * pre);
             sc = 1.0f;
@@ -795,7 +843,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           // p = 2^(sc * x - m): one FMA into each exp2
           float nm = -mref;
           float lscale = 1.0f;
-          if constexpr (FMT != 0) {
+          if constexpr (FMT != 0 && !F16) {
             if (pool8) {
               nm += p.log2_v_scale;
               lscale = p.inv_v_scale;
@@ -809,7 +857,12 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             const float e1 = ex2_approx(fmaf(x[i + 1], sc, nm));
             l0 += e0;
             l1 += e1;
-            pk[i / 2] = pack_bf16(e0, e1);
+            if constexpr (F16) {
+              const __half2 h = __floats2half2_rn(e0, e1);
+              pk[i / 2] = *reinterpret_cast<const uint32_t *>(&h);
+            } else {
+              pk[i / 2] = pack_bf16(e0, e1);
+            }
           }
           if constexpr (FMT != 0) l += (l0 + l1) * lscale;
           else l += l0 + l1;
@@ -864,6 +917,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           inv = a_m / lt;
           lse_v = (M + __log2f(lt)) * 0.69314718055994531f;
         }
+        if constexpr (F16) inv *= p.v_scale;  // V was read as its codes
         uint32_t v[32];
 #pragma unroll
         for (int c = 0; c < C::HDV / 32; ++c) {
@@ -933,7 +987,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           constexpr int kk = decltype(kk_c)::value;
           constexpr uint32_t ao = ((kk / 4) * (C::BM * 128) + (kk % 4) * 32) / 16;
           constexpr uint32_t bo = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) / 16;
-          tc_mma_ss_step<ao, bo>(d, a_lo, b_lo, K_HI, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          tc_mma_ss_step<ao, bo>(d, a_lo, b_lo, K_HI, IDQK, kk > 0 ? 1u : 0u);
         });
         tc_commit(&bars[B_S_FULL + buf]);
       };
@@ -943,7 +997,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         const uint32_t acc0 = acc_first ? 1u : 0u;
         static_for<0, C::BN / 16>([&](auto kk_c) {
           constexpr int kk = decltype(kk_c)::value;
-          tc_mma_ts_step<kk * 8, kk * 128>(d, a, b_lo, V_HI, C::IDESC_PV, kk > 0 ? 1u : acc0);
+          tc_mma_ts_step<kk * 8, kk * 128>(d, a, b_lo, V_HI, IDPV, kk > 0 ? 1u : acc0);
         });
       };
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
@@ -953,7 +1007,10 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         const int nt = w.n_tiles;
         if (nt == 0) continue;
         const bool q1 = w.n_tok > TOK;
-        if (!mbar_wait(&bars[B_Q_FULL], q_cnt & 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&bars[F16 ? B_Q_CONV : B_Q_FULL], q_cnt & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
         ++q_cnt;
         tc_fence_after();
         if constexpr (MODE == kDecode) {
@@ -1199,7 +1256,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         cp_async_16_at<i * KPP * 128, 0>(stage + dthr, src, bytes);
       });
     };
-    uint32_t kc = 0, vc = 0, ic = 0;
+    uint32_t kc = 0, vc = 0, ic = 0, qc = 0;
     bool ok = true;
     if constexpr (FMT == 0) {
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
@@ -1283,7 +1340,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       static_for<0, NKEYS>([&](auto i_c) {
         constexpr int i = decltype(i_c)::value;
         const uint32_t a = stage + dthr + i * KPP * 128;
-        st_shared_u4(a, fp8x8_to_bf16x8<FMT>(ld_shared_u2(a)));
+        if constexpr (F16) st_shared_u4(a, fp8x8_to_f16x8<FMT>(ld_shared_u2(a)));
+        else st_shared_u4(a, fp8x8_to_bf16x8<FMT>(ld_shared_u2(a)));
       });
       fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
     };
@@ -1359,6 +1417,26 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       if (!fetch() || !issue_k(ext_j) || !issue_v(ext_j)) {
         ok = false;
         break;
+      }
+      if constexpr (F16) {
+        // the unit's query rows (tokens x G heads of query tile 0) to f16 in
+        // place once their load has landed, 16 bytes at a time (the swizzle
+        // only permutes whole chunks within a row)
+        if (!mbar_wait(&bars[B_Q_FULL], qc & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ++qc;
+        const int n_chunks = w.n_tok * G * (HD / 8);
+        for (int c = ct; c < n_chunks; c += C::COPY_THREADS) {
+          const int row = c / (HD / 8), k = c % (HD / 8);
+          const uint32_t off = C::OFF_Q + (uint32_t)(k >> 3) * (C::BM * 128) +
+                               (uint32_t)row * 128u + (uint32_t)(k & 7) * 16u;
+          const uint4 v = *reinterpret_cast<const uint4 *>(smem + off);
+          st_shared_u4(sbase + off, bf16x8_to_f16x8_scaled(v));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[B_Q_CONV]);
       }
       for (int j = 0; j < nt; ++j) {
         const int ks_j = (kc - 1) % C::NK, vs_j = (vc - 1) % C::NV;
@@ -1693,6 +1771,7 @@ int launch_attention(const AttnArgs &a) {
   kp.mask_indptr = a.mask_indptr;
   kp.sinks = a.sinks;
   kp.log2_v_scale = log2f(a.v_scale);
+  kp.v_scale = a.v_scale;
   kp.inv_v_scale = 1.0f / a.v_scale;
   kp.prefix_lens = a.prefix_lens;
   kp.units = sp.units;

@@ -328,6 +328,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_maj
          | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int b_mn_major) {
+  return (1u << 4)                      // D format: f32 (A and B format 0: f16)
+         | ((uint32_t)b_mn_major << 16) // B major-ness
+         | ((uint32_t)(N >> 3) << 17)   // N / 8
+         | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a
 // 128-byte-swizzled block whose rows are 128 bytes apart.
 __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk) {
