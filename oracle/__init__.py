@@ -78,6 +78,8 @@ def _configure(lib):
     lib.oracle_set_kv_buffer_fp8.argtypes = [
         _p, _l, _l, _p, _l, _l, _p, _l, _i, _i, _i, ctypes.c_float, ctypes.c_float, _i,
         _p, _l, _l, _p, _l, _l]
+    lib.oracle_expand_paged_kv_indices.restype = None
+    lib.oracle_expand_paged_kv_indices.argtypes = [_p, _p, _p, _i, _i, _p, _p]
     lib.oracle_set_kv_buffer.restype = None
     lib.oracle_set_kv_buffer.argtypes = [
         _p, _l, _l, _p, _l, _l, _p, _l, _i, _i, _i, _p, _l, _l, _p, _l, _l]
@@ -426,3 +428,23 @@ def set_kv_buffer_fp8(k_buffer, v_buffer, cache_loc, k, v, k_scale, v_scale):
         lk, lv, float(k_scale), float(v_scale), fmt, _ptr(kb), *_row_strides(kb), _ptr(vb),
         *_row_strides(vb))
     return kb.view(_FP8[fmt]), vb.view(_FP8[fmt])
+
+
+def expand_paged_kv_indices(kv_indptr, kv_indices, kv_last_page_len, page_size, fill=-1):
+    """Paged KV indices (sglang flashinfer_backend.py, the wrappers' paged
+    format: indptr over pages, page indices, last_page_len, page_size) to
+    per-token pool slots.  Returns (token_indptr int32 [bs+1], token_indices
+    int32 [sum T_b]); ``fill`` marks entries not written."""
+    lib = _load()
+    kvp, kvi, lpl = _i32(kv_indptr), _i32(kv_indices), _i32(kv_last_page_len)
+    bs = kvp.numel() - 1
+    pages = (kvp[1:] - kvp[:-1]).to(torch.int64)
+    t = torch.where(pages > 0, (pages - 1) * int(page_size) + lpl.to(torch.int64),
+                    torch.zeros_like(pages))
+    total = int(t.sum()) if bs else 0
+    tptr = torch.empty(bs + 1, dtype=torch.int32)
+    tidx = torch.full((total,), fill, dtype=torch.int32)
+    lib.oracle_expand_paged_kv_indices(
+        _ptr(kvp), _ptr(kvi) if kvi.numel() else None, _ptr(lpl) if bs else None,
+        int(page_size), bs, _ptr(tptr), _ptr(tidx) if total else None)
+    return tptr, tidx

@@ -3,7 +3,8 @@
  * page-size-1 KV pool, decode attention, merge_state, the unified KV-index
  * build, the KV-index gather from the request-to-token table and the KV
  * write into the pool, for bf16 pools and for fp8 (e4m3 / e5m2) pools with
- * per-tensor k_scale / v_scale.
+ * per-tensor k_scale / v_scale, and the expansion of paged KV indices (page
+ * size > 1) into per-token pool slots.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
  * call this file.  It exists so that tests, the smoke check and the CPU
@@ -580,5 +581,39 @@ void oracle_set_kv_buffer_fp8(
                         oracle_fp8_code(x / v_scale, fmt);
                 }
         }
+    }
+}
+
+/*
+ * Paged KV indices to per-token pool slots ([FI] the paged KV format of the
+ * wrappers' plan: indptr over pages, indices of pages, last_page_len, and
+ * page_size; the pool viewed as [pages, page_size, ...], so key j of
+ * sequence b sits in page kv_indices[kv_indptr[b] + j / page_size] at
+ * offset j % page_size):
+ *   pages_b            = kv_indptr[b+1] - kv_indptr[b]
+ *   T_b                = pages_b > 0 ? (pages_b - 1) * page_size
+ *                                      + kv_last_page_len[b] : 0
+ *   token_indptr[b+1]  = token_indptr[b] + T_b          (token_indptr[0] = 0)
+ *   token_indices[token_indptr[b] + j]
+ *       = kv_indices[kv_indptr[b] + j / page_size] * page_size
+ *         + j % page_size                                  (j < T_b)
+ */
+void oracle_expand_paged_kv_indices(
+    const int32_t *kv_indptr, const int32_t *kv_indices,
+    const int32_t *kv_last_page_len, int page_size, int bs,
+    int32_t *token_indptr, int32_t *token_indices)
+{
+    token_indptr[0] = 0;
+    for (int b = 0; b < bs; ++b) {
+        long pages = kv_indptr[b + 1] - kv_indptr[b];
+        long t = pages > 0 ? (pages - 1) * page_size + kv_last_page_len[b] : 0;
+        token_indptr[b + 1] = token_indptr[b] + (int32_t)t;
+    }
+    for (int b = 0; b < bs; ++b) {
+        long t = token_indptr[b + 1] - token_indptr[b];
+        for (long j = 0; j < t; ++j)
+            token_indices[token_indptr[b] + j] =
+                kv_indices[kv_indptr[b] + j / page_size] * page_size +
+                (int32_t)(j % page_size);
     }
 }

@@ -64,6 +64,10 @@ MUTANTS = [
     ("fp8_scale_dropped", "r.fmt) * r.scale;", "r.fmt);", None),
     ("fp8_kv_scales_swapped", "pool_row(k_buf, kv_fmt, k_scale,", "pool_row(k_buf, kv_fmt, v_scale,", None),
     ("fp8_write_no_divide", "oracle_fp8_code(x / k_scale, fmt)", "oracle_fp8_code(x, fmt)", None),
+    ("paged_offset_dropped", "kv_indices[kv_indptr[b] + j / page_size] * page_size +\n                (int32_t)(j % page_size);",
+     "kv_indices[kv_indptr[b] + j / page_size] * page_size;", None),
+    ("paged_last_page_len_ignored", "(pages - 1) * page_size + kv_last_page_len[b] : 0;", "(pages - 1) * page_size + 1 : 0;", None),
+    ("paged_page_not_scaled", "kv_indices[kv_indptr[b] + j / page_size] * page_size +", "kv_indices[kv_indptr[b] + j / page_size] +", None),
     ("sink_in_values", "    if (sink)\n        l += exp(*sink - m);\n", "    if (sink) {\n        l += exp(*sink - m);\n        for (int d = 0; d < lv; ++d) o[d] += exp(*sink - m);\n    }\n", None),
 ]
 
@@ -97,6 +101,8 @@ BATTERY = [
     lambda: pins.test_fp8_rounding_matches_torch_in_range(*pins.FP8[0]),
     lambda: pins.test_fp8_write_matches_torch_quantization(),
     lambda: pins.test_fp8_pool_attention_equals_bf16_pool_of_its_values(pins.oracle.KV_E4M3),
+    lambda: pins.test_paged_indices_hand_fixture(),
+    lambda: pins.test_paged_indices_are_page_blocks(16),
 ]
 
 

@@ -859,3 +859,84 @@ def test_fp8_write_matches_torch_quantization():
         wv[loc] = (v.float() / 2.0).to(dt).view(torch.uint8)
         assert torch.equal(k2.view(torch.uint8), wk)
         assert torch.equal(v2.view(torch.uint8), wv)
+
+
+# ------------------------------------------------------ paged KV (page size > 1)
+def test_paged_indices_hand_fixture():
+    """Hand-derived worked example (tests/golden/paged_indices_hand.json)."""
+    with open(os.path.join(GOLDEN, "paged_indices_hand.json")) as f:
+        fx = json.load(f)
+    t = lambda k: torch.tensor(fx[k], dtype=torch.int32)
+    tptr, tidx = oracle.expand_paged_kv_indices(t("kv_indptr"), t("kv_indices"),
+                                                t("kv_last_page_len"), fx["page_size"])
+    assert tptr.tolist() == fx["expected_token_indptr"]
+    assert tidx.tolist() == fx["expected_token_indices"]
+
+
+def test_page_size_one_is_the_identity():
+    """Page size 1 with last_page_len 1 (the pages' own configuration) maps
+    every index to itself."""
+    g = torch.Generator().manual_seed(71)
+    idx = torch.randint(0, 1 << 20, (500,), generator=g, dtype=torch.int32)
+    ptr = torch.tensor([0, 0, 120, 121, 500], dtype=torch.int32)
+    tptr, tidx = oracle.expand_paged_kv_indices(ptr, idx, torch.ones(4, dtype=torch.int32), 1)
+    assert torch.equal(tptr, ptr) and torch.equal(tidx, idx)
+
+
+@pytest.mark.parametrize("ps", [2, 16, 64])
+def test_paged_indices_are_page_blocks(ps):
+    """Random page tables: the slots equal numpy's arange blocks of each page
+    (ps consecutive slots per page, the last page cut at last_page_len)."""
+    rng = np.random.default_rng(ps)
+    bs = 9
+    pages = rng.integers(0, 6, size=bs)
+    pages[0] = 0
+    last = rng.integers(1, ps + 1, size=bs)
+    ptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    idx = rng.permutation(1000)[: ptr[-1]].astype(np.int32)
+    tptr, tidx = oracle.expand_paged_kv_indices(torch.from_numpy(ptr), torch.from_numpy(idx),
+                                                torch.from_numpy(last.astype(np.int32)), ps)
+    want = []
+    for b in range(bs):
+        for k in range(pages[b]):
+            n = ps if k < pages[b] - 1 else last[b]
+            want.append(idx[ptr[b] + k] * ps + np.arange(n))
+    want = np.concatenate(want) if want else np.zeros(0, np.int32)
+    assert np.array_equal(tidx.numpy(), want)
+    t = np.where(pages > 0, (pages - 1) * ps + last, 0)
+    assert np.array_equal(tptr.numpy(), np.concatenate([[0], np.cumsum(t)]))
+
+
+def test_decode_over_a_paged_pool_equals_decode_over_its_tokens():
+    """A pool laid out in pages of 16 (every sequence's tokens in its own
+    pages, in order, pages shuffled over the pool): decode through the
+    expanded page table equals decode through the tokens' own slots."""
+    ps = 16
+    wl = W.draw(W.WorkloadSpec("dec", batch=4, hq=8, hkv=2, lq=64, lv=64,
+                               prefix=[40, 15, 0, 70], extend=[1, 1, 1, 1], num_slots=1024,
+                               seed=72, decode=True))
+    g = torch.Generator().manual_seed(73)
+    t = [p + 1 for p in wl.prefix_lens]
+    n_pages = [(x + ps - 1) // ps for x in t]
+    page_ids = torch.randperm(1024 // ps, generator=g)[: sum(n_pages)].to(torch.int32)
+    kb_tok, vb_tok = wl.pool()
+    kb = torch.zeros_like(kb_tok)
+    vb = torch.zeros_like(vb_tok)
+    ptr, slots, p0 = [0], [], 0
+    for b in range(wl.batch):
+        o = int(wl.token_offsets[b])
+        for j in range(t[b]):
+            s = int(page_ids[p0 + j // ps]) * ps + j % ps
+            slots.append(s)
+            kb[s] = wl.k_rows[o + j]
+            vb[s] = wl.v_rows[o + j]
+        p0 += n_pages[b]
+        ptr.append(p0)
+    last = torch.tensor([x - (n - 1) * ps for x, n in zip(t, n_pages)], dtype=torch.int32)
+    tptr, tidx = oracle.expand_paged_kv_indices(torch.tensor(ptr, dtype=torch.int32), page_ids,
+                                                last, ps)
+    assert tidx.tolist() == slots
+    o1, l1 = oracle.decode_attention(wl.q, kb, vb, tptr, tidx, wl.sm_scale)
+    o2, l2 = oracle.decode_attention(wl.q, kb_tok, vb_tok, wl.kv_indptr, wl.kv_indices,
+                                     wl.sm_scale)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
