@@ -646,6 +646,26 @@ def measure_kv_ops(dev, flush, steps, hbm_peak):
             "algorithmic_bytes": nbytes}
         del table, rpi, seq, kvp, kvi
         torch.cuda.empty_cache()
+    # a page table of 16-slot pages for the decode batch (64 x 8193 keys)
+    ps = 16
+    wl = W.draw(W.SPECS["decode_gqa"])
+    t = [p + 1 for p in wl.prefix_lens]
+    n_pages = [(x + ps - 1) // ps for x in t]
+    g = torch.Generator().manual_seed(5)
+    page_ids = torch.randperm(wl.spec.num_slots // ps, generator=g)[: sum(n_pages)]
+    ptr = torch.tensor([0] + list(torch.tensor(n_pages).cumsum(0)), dtype=torch.int32, device=dev)
+    ids = page_ids.to(device=dev, dtype=torch.int32)
+    last = torch.tensor([x - (n - 1) * ps for x, n in zip(t, n_pages)], dtype=torch.int32,
+                        device=dev)
+    tptr = torch.empty(wl.batch + 1, dtype=torch.int32, device=dev)
+    tidx = torch.empty(sum(t), dtype=torch.int32, device=dev)
+    ms = time_launches(lambda: pkx.expand_paged_kv_indices(ptr, ids, last, ps, token_indptr=tptr,
+                                                           token_indices=tidx), steps, flush, dev)
+    nbytes = 4.0 * sum(t) + 4.0 * sum(n_pages) + 8.0 * wl.batch + 4.0 * (wl.batch + 1)
+    out["expand_paged_kv_indices/decode_gqa"] = {
+        "what": f"{wl.batch} sequences, {sum(n_pages)} pages of {ps} -> {sum(t)} token slots",
+        "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+        "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": nbytes}
     return out
 
 

@@ -380,6 +380,32 @@ int pkx_create_kv_indices(
     int32_t *kv_indptr, int32_t *kv_indices, int64_t kv_indices_capacity,
     void *stream);
 
+/*
+ * Paged KV indices (page size > 1) to per-token pool slots.
+ * Source: sglang flashinfer_backend.py, the paged KV format the wrappers'
+ * plan takes: indptr over pages, page indices, last_page_len (entries in
+ * each sequence's last page) and page_size, the pool viewed as
+ * [pages, page_size, heads, dim].  For b < batch:
+ *   pages_b          = kv_indptr[b+1] - kv_indptr[b]
+ *   T_b              = pages_b > 0 ? (pages_b - 1) * page_size
+ *                                    + kv_last_page_len[b] : 0
+ *   token_indptr     = [0, running sum of T_b]                   (written)
+ *   token_indices[token_indptr[b] + j]
+ *       = kv_indices[kv_indptr[b] + j / page_size] * page_size
+ *         + j % page_size                                          (written)
+ * The result is the page-size-1 index list every attention call above
+ * takes (for the pool viewed as [pages * page_size, heads, dim]).  All
+ * arrays int32; token_indices holds token_indices_capacity entries, and
+ * none past it is written.  A key whose page would lie past its sequence's
+ * pages (kv_last_page_len[b] > page_size) is written as -1, which the
+ * attention calls report instead of reading.  batch <= 12000.
+ */
+int pkx_expand_paged_kv_indices(
+    const int32_t *kv_indptr, const int32_t *kv_indices,
+    const int32_t *kv_last_page_len, int page_size, int batch,
+    int32_t *token_indptr, int32_t *token_indices,
+    int64_t token_indices_capacity, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -456,6 +456,30 @@ int pkx_set_kv_buffer_fp8(const void *k, int64_t k_ts, int64_t k_hs, const void 
                                   vb_ss, vb_hs, num_slots, static_cast<cudaStream_t>(stream));
 }
 
+int pkx_expand_paged_kv_indices(const int32_t *kv_indptr, const int32_t *kv_indices,
+                                const int32_t *kv_last_page_len, int page_size, int batch,
+                                int32_t *token_indptr, int32_t *token_indices,
+                                int64_t token_indices_capacity, void *stream) {
+  if (batch < 0 || batch > kGatherMaxBatch)
+    return set_error(PKX_EUNSUPPORTED, "expand_paged_kv_indices: batch %d outside [0, %d]",
+                     batch, kGatherMaxBatch);
+  if (page_size <= 0) return set_error(PKX_EINVAL, "expand_paged_kv_indices: page_size <= 0");
+  if (token_indices_capacity < 0)
+    return set_error(PKX_EINVAL, "expand_paged_kv_indices: negative capacity");
+  if (!token_indptr || !aligned(token_indptr, 4))
+    return set_error(PKX_EINVAL, "expand_paged_kv_indices: token_indptr null or misaligned");
+  if (batch > 0) {
+    if (!kv_indptr || !kv_last_page_len || !aligned(kv_indptr, 4) ||
+        !aligned(kv_last_page_len, 4) || (kv_indices && !aligned(kv_indices, 4)))
+      return set_error(PKX_EINVAL, "expand_paged_kv_indices: null or misaligned input");
+    if (token_indices_capacity > 0 && (!token_indices || !aligned(token_indices, 4)))
+      return set_error(PKX_EINVAL, "expand_paged_kv_indices: token_indices null or misaligned");
+  }
+  return launch_expand_paged(kv_indptr, kv_indices, kv_last_page_len, page_size, batch,
+                             token_indptr, token_indices, token_indices_capacity,
+                             static_cast<cudaStream_t>(stream));
+}
+
 int pkx_create_kv_indices(const int32_t *req_to_token, int64_t req_to_token_rows,
                           int64_t req_to_token_stride, const int64_t *req_pool_indices,
                           const int64_t *paged_kernel_lens, const int64_t *kv_start_idx,

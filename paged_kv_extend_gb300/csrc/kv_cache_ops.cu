@@ -318,6 +318,113 @@ __global__ void __launch_bounds__(kGatherThreads) create_kv_indices_kernel(
   }
 }
 
+// ------------------------------------------------------------ page tables
+// Paged KV indices (indptr over pages, page ids, entries in each sequence's
+// last page, page size) to per-token pool slots, the layout every attention
+// call here takes: key j of sequence b is slot
+// kv_indices[kv_indptr[b] + j / page_size] * page_size + j % page_size.
+// Same shape as the gather above: every CTA scans the key counts, CTA 0
+// writes token_indptr, the token range is split evenly over the CTAs.
+__global__ void __launch_bounds__(kGatherThreads) expand_paged_kernel(
+    const int32_t *__restrict__ kv_indptr, const int32_t *__restrict__ kv_indices,
+    const int32_t *__restrict__ last_page_len, int page_size, int batch, int32_t *token_indptr,
+    int32_t *token_indices, int64_t capacity) {
+  extern __shared__ int32_t s_ptr[];  // [batch + 1] running sum of key counts
+  __shared__ int32_t s_warp[kGatherThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto keys_of = [&](int b) -> int32_t {
+    const int32_t pages = kv_indptr[b + 1] - kv_indptr[b];
+    return pages > 0 ? (pages - 1) * page_size + last_page_len[b] : 0;
+  };
+  const int per = (batch + kGatherThreads - 1) / kGatherThreads;
+  const int b0 = tid * per < batch ? tid * per : batch;
+  const int b1 = b0 + per < batch ? b0 + per : batch;
+  int32_t run = 0;
+  for (int b = b0; b < b1; ++b) run += keys_of(b);
+  int32_t incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = lane < kGatherThreads / 32 ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kGatherThreads / 32) s_warp[lane] = w;
+  }
+  __syncthreads();
+  int32_t acc = incl - run + (warp > 0 ? s_warp[warp - 1] : 0);
+  for (int b = b0; b < b1; ++b) {
+    s_ptr[b] = acc;
+    acc += keys_of(b);
+  }
+  if (tid == kGatherThreads - 1) s_ptr[batch] = s_warp[kGatherThreads / 32 - 1];
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int b = tid; b <= batch; b += kGatherThreads) token_indptr[b] = s_ptr[b];
+
+  int64_t total = s_ptr[batch];
+  if (total > capacity) total = capacity;
+  if (total < 0) total = 0;
+  const int64_t share = (total + gridDim.x - 1) / gridDim.x;
+  const int64_t f0 = (int64_t)blockIdx.x * share;
+  const int64_t f1 = f0 + share < total ? f0 + share : total;
+  for (int64_t base = f0 + tid; base < f1; base += (int64_t)kGatherThreads * kGatherPerThread) {
+    int32_t val[kGatherPerThread];
+#pragma unroll
+    for (int u = 0; u < kGatherPerThread; ++u) {
+      const int64_t f = base + (int64_t)u * kGatherThreads;
+      val[u] = -1;
+      if (f < f1) {
+        int lo = 0, hi = batch - 1;  // last b with s_ptr[b] <= f
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_ptr[mid] <= f) lo = mid; else hi = mid - 1;
+        }
+        const int64_t j = f - s_ptr[lo];
+        const int64_t pg = kv_indptr[lo] + j / page_size;
+        if (pg >= kv_indptr[lo] && pg < kv_indptr[lo + 1])  // a page of this sequence
+          val[u] = __ldg(kv_indices + pg) * page_size + (int32_t)(j % page_size);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kGatherPerThread; ++u) {
+      const int64_t f = base + (int64_t)u * kGatherThreads;
+      if (f < f1) token_indices[f] = val[u];
+    }
+  }
+}
+
+int launch_expand_paged(const int32_t *kv_indptr, const int32_t *kv_indices,
+                        const int32_t *last_page_len, int page_size, int batch,
+                        int32_t *token_indptr, int32_t *token_indices, int64_t capacity,
+                        cudaStream_t st) {
+  if (batch == 0) {
+    cudaError_t e = cudaMemsetAsync(token_indptr, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return set_error(PKX_ECUDA, "memset: %s", cudaGetErrorString(e));
+    return PKX_OK;
+  }
+  const int nsm = num_sms_current_device();
+  const int64_t per_cta = batch * 2 > 1024 ? (int64_t)batch * 2 : 1024;
+  int64_t grid = (capacity + per_cta - 1) / per_cta;
+  if (grid < 1) grid = 1;
+  if (grid > (int64_t)nsm * 4) grid = (int64_t)nsm * 4;
+  const size_t smem = sizeof(int32_t) * (size_t)(batch + 1);
+  expand_paged_kernel<<<(unsigned)grid, kGatherThreads, smem, st>>>(
+      kv_indptr, kv_indices, last_page_len, page_size, batch, token_indptr, token_indices,
+      capacity);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return set_error(PKX_ECUDA, "expand_paged_kv_indices launch: %s", cudaGetErrorString(e));
+  return PKX_OK;
+}
+
 int launch_create_kv_indices(const int32_t *req_to_token, int64_t rows, int64_t stride,
                              const int64_t *req_pool_indices, const int64_t *paged_kernel_lens,
                              const int64_t *kv_start_idx, int batch, int32_t *kv_indptr,

@@ -145,6 +145,10 @@ int launch_set_kv_buffer_fp8(const void *k, int64_t k_ts, int64_t k_hs, const vo
 // Largest batch the index gather takes (its running sum lives in 48 KB of
 // shared memory).
 constexpr int kGatherMaxBatch = 12000;
+int launch_expand_paged(const int32_t *kv_indptr, const int32_t *kv_indices,
+                        const int32_t *last_page_len, int page_size, int batch,
+                        int32_t *token_indptr, int32_t *token_indices, int64_t capacity,
+                        cudaStream_t s);
 int launch_create_kv_indices(const int32_t *req_to_token, int64_t rows, int64_t stride,
                              const int64_t *req_pool_indices, const int64_t *paged_kernel_lens,
                              const int64_t *kv_start_idx, int batch, int32_t *kv_indptr,

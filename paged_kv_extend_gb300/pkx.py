@@ -72,6 +72,7 @@ _SIGS = {
     "pkx_set_kv_buffer_fp8": (_i, [
         _p, _i64, _i64, _p, _i64, _i64, _p, _i64, _i, _i, _i, _f, _f, _i,
         _p, _i64, _i64, _p, _i64, _i64, _i64, _p]),
+    "pkx_expand_paged_kv_indices": (_i, [_p, _p, _p, _i, _i, _p, _p, _i64, _p]),
     "pkx_create_kv_indices": (_i, [
         _p, _i64, _i64, _p, _p, _p, _i, _p, _p, _i64, _p]),
 }
@@ -472,3 +473,31 @@ def set_kv_buffer_fp8(k_buffer, v_buffer, cache_loc, k, v, k_scale, v_scale):
         _ptr(v_buffer) if v is not None else None, vb[0], vb[1], k_buffer.shape[0],
         _stream(k.device)))
     return k_buffer, v_buffer
+
+
+def expand_paged_kv_indices(kv_indptr, kv_indices, kv_last_page_len, page_size,
+                            token_indptr=None, token_indices=None, capacity=None):
+    """Paged KV indices (page size > 1) to per-token pool slots
+    (pkx_expand_paged_kv_indices).  All int32 CUDA tensors.  Returns
+    (token_indptr [bs+1], token_indices); without ``token_indices`` the output
+    is allocated with ``capacity`` entries (the host-known key count)."""
+    lib = load_library()
+    for t, nm in ((kv_indptr, "kv_indptr"), (kv_indices, "kv_indices"),
+                  (kv_last_page_len, "kv_last_page_len")):
+        _i32(t, nm)
+    bs = kv_indptr.numel() - 1
+    dev = kv_indptr.device
+    if token_indptr is None:
+        token_indptr = torch.empty(bs + 1, dtype=torch.int32, device=dev)
+    if token_indices is None:
+        if capacity is None:
+            raise ValueError("give token_indices or capacity (the total key count)")
+        token_indices = torch.empty(int(capacity), dtype=torch.int32, device=dev)
+    _i32(token_indptr, "token_indptr")
+    _i32(token_indices, "token_indices")
+    _check(lib.pkx_expand_paged_kv_indices(
+        _ptr(kv_indptr), _ptr(kv_indices) if kv_indices.numel() else None,
+        _ptr(kv_last_page_len), int(page_size), int(bs), _ptr(token_indptr),
+        _ptr(token_indices) if token_indices.numel() else None, token_indices.numel(),
+        _stream(dev)))
+    return token_indptr, token_indices

@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
                  "pkx_decode_attention_fwd", "pkx_merge_state",
                  "pkx_build_unified_kv_indices", "pkx_extend_workspace_size",
                  "pkx_set_kv_buffer", "pkx_create_kv_indices", "pkx_set_kv_buffer_fp8",
-                 "pkx_extend_attention_fwd_ragged_paged",
+                 "pkx_extend_attention_fwd_ragged_paged", "pkx_expand_paged_kv_indices",
                  "pkx_decode_workspace_size", "pkx_workspace_status",
                  "pkx_last_error_string", "pkx_version"]:
         assert must in names
@@ -112,6 +112,19 @@ def test_fp8_write_validation(lib):
     assert w(vs=float("nan")) == pkx.PKX_EINVAL
     assert w(n=0) == pkx.PKX_OK
     assert w(n=0, fmt=2) == pkx.PKX_OK
+
+
+def test_paged_expansion_validation(lib):
+    A = 0x10000
+    e = lambda **o: lib.pkx_expand_paged_kv_indices(
+        o.get("ptr", A), A, o.get("last", A), o.get("ps", 16), o.get("bs", 2), o.get("out", A),
+        A, o.get("cap", 64), None)
+    assert e(ps=0) == pkx.PKX_EINVAL
+    assert e(bs=12001) == pkx.PKX_EUNSUPPORTED
+    assert e(out=None) == pkx.PKX_EINVAL
+    assert e(last=A + 2) == pkx.PKX_EINVAL
+    assert e(ptr=None) == pkx.PKX_EINVAL
+    assert e(cap=-1) == pkx.PKX_EINVAL
 
 
 def test_kv_write_and_gather_validation(lib):

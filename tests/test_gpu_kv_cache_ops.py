@@ -229,3 +229,91 @@ def test_window_decode_through_gather_matches_windowed_oracle():
     want_o, want_l = oracle.decode_attention(wl.q, kb, vb, wl.kv_indptr, wl.kv_indices,
                                              wl.sm_scale, sliding_window=Wn)
     assert_close(o.cpu(), lse.cpu(), want_o, want_l)
+
+
+# ------------------------------------------------------ page tables (page size > 1)
+def _expand_gpu(ptr, idx, last, ps, capacity=None, fill=-7):
+    ptr = torch.as_tensor(ptr, dtype=torch.int32)
+    idx = torch.as_tensor(idx, dtype=torch.int32)
+    last = torch.as_tensor(last, dtype=torch.int32)
+    want_p, want_i = oracle.expand_paged_kv_indices(ptr, idx, last, ps)
+    cap = want_i.numel() if capacity is None else capacity
+    tptr = torch.full((ptr.numel(),), fill, dtype=torch.int32, device=DEV)
+    tidx = torch.full((cap + 5,), fill, dtype=torch.int32, device=DEV)
+    pkx.expand_paged_kv_indices(ptr.to(DEV), idx.to(DEV), last.to(DEV), ps,
+                                token_indptr=tptr, token_indices=tidx[:cap])
+    torch.cuda.synchronize()
+    return tptr.cpu(), tidx.cpu(), want_p, want_i
+
+
+def test_paged_expansion_hand_fixture():
+    fx = json.load(open(os.path.join(GOLDEN, "paged_indices_hand.json")))
+    tptr, tidx, _, _ = _expand_gpu(fx["kv_indptr"], fx["kv_indices"], fx["kv_last_page_len"],
+                                   fx["page_size"])
+    n = fx["expected_token_indptr"][-1]
+    assert tptr.tolist() == fx["expected_token_indptr"]
+    assert tidx[:n].tolist() == fx["expected_token_indices"]
+    assert torch.all(tidx[n:] == -7)
+
+
+@pytest.mark.parametrize("seed,bs,ps,max_pages", [
+    (0, 1, 16, 3), (1, 64, 16, 300), (2, 300, 64, 40), (3, 4096, 8, 20), (4, 12000, 32, 2),
+    (5, 16, 128, 1100)])
+def test_paged_expansion_bit_exact_vs_oracle(seed, bs, ps, max_pages):
+    g = torch.Generator().manual_seed(seed)
+    pages = torch.randint(0, max_pages + 1, (bs,), generator=g)
+    pages[0] = 0
+    ptr = torch.cat([torch.zeros(1, dtype=torch.int64), pages.cumsum(0)])
+    idx = torch.randint(0, 1 << 24, (int(ptr[-1]),), generator=g, dtype=torch.int32)
+    last = torch.randint(1, ps + 1, (bs,), generator=g)
+    tptr, tidx, want_p, want_i = _expand_gpu(ptr, idx, last, ps)
+    assert torch.equal(tptr, want_p)
+    assert torch.equal(tidx[: want_i.numel()], want_i)
+
+
+def test_paged_expansion_bounds():
+    """A last page longer than the page size reads no page past the
+    sequence's own (those keys come out as -1); no entry past the capacity
+    is written."""
+    tptr, tidx, _, _ = _expand_gpu([0, 1, 2], [3, 5], [6, 2], 4, capacity=7)
+    assert tptr.tolist() == [0, 6, 8]
+    assert tidx[:7].tolist() == [12, 13, 14, 15, -1, -1, 20]
+    assert torch.all(tidx[7:] == -7)
+
+
+def test_decode_through_a_page_table():
+    """Decode over a pool laid out in pages of 16: the page table expanded on
+    the GPU, then decode; against the oracle's decode over the tokens' own
+    slots."""
+    ps = 16
+    wl = W.draw(W.WorkloadSpec("dec", batch=12, hq=32, hkv=8, lq=128, lv=128,
+                               prefix=("uniform", 0, 2000), extend=("const", 1),
+                               num_slots=1 << 16, seed=74, decode=True))
+    g = torch.Generator().manual_seed(75)
+    t = [p + 1 for p in wl.prefix_lens]
+    n_pages = [(x + ps - 1) // ps for x in t]
+    page_ids = torch.randperm((1 << 16) // ps, generator=g)[: sum(n_pages)].to(torch.int32)
+    kb = torch.zeros(1 << 16, 8, 128, dtype=torch.bfloat16)
+    vb = torch.zeros_like(kb)
+    ptr, p0 = [0], 0
+    for b in range(wl.batch):
+        o = int(wl.token_offsets[b])
+        slots = page_ids[p0 + torch.arange(t[b]) // ps].long() * ps + torch.arange(t[b]) % ps
+        kb[slots] = wl.k_rows[o:o + t[b]]
+        vb[slots] = wl.v_rows[o:o + t[b]]
+        p0 += n_pages[b]
+        ptr.append(p0)
+    last = torch.tensor([x - (n - 1) * ps for x, n in zip(t, n_pages)], dtype=torch.int32)
+    kvp, kvi = pkx.expand_paged_kv_indices(torch.tensor(ptr, dtype=torch.int32).to(DEV),
+                                           page_ids.to(DEV), last.to(DEV), ps, capacity=sum(t))
+    s = wl.spec
+    o = torch.empty(s.batch, s.hq, s.lv, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(s.batch, s.hq, dtype=torch.float32, device=DEV)
+    ws = pkx.decode_attention_fwd(wl.q.to(DEV), o, kb.to(DEV), vb.to(DEV), kvp, kvi,
+                                  wl.sm_scale, lse=lse)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ko, vo = wl.pool()
+    want_o, want_l = oracle.decode_attention(wl.q, ko, vo, wl.kv_indptr, wl.kv_indices,
+                                             wl.sm_scale)
+    assert_close(o.cpu(), lse.cpu(), want_o, want_l)
