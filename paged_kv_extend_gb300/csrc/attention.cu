@@ -63,7 +63,9 @@ struct SchedParams {
   int no_causal;   // a custom mask replaces the causal mask: blocks see every key
   int key_set;     // two-stage form only: kAllKeys, kPrefixKeys or kExtendKeys
   int keep_status; // leave the status word as an earlier pass left it
-  int two_streams; // decode units run two key streams, each with its own partial slot
+  int two_streams; // GQA kernel: decode units run two key streams, each with its own
+                   // partial slot; split extend units of one query tile run two
+                   // streams into the two halves of their slot
   int n_dsplit;  // units per (block, split): value-dim slices (1, or 4 for MLA)
   int unit_target, qb_max, unit_max, comb_max, slot_max;
   int32_t *seq;  // 8 arrays of batch+1 ints
@@ -278,8 +280,9 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   const int qb_beg = min(total_qb, tid * chunk), qb_end = min(total_qb, qb_beg + chunk);
   // two key streams: every unit has two partial slots and every block a
   // combine entry
-  const int spu = p.two_streams ? 2 : 1;
-  auto combined = [&](int S) { return S > 1 || p.two_streams; };
+  const bool dec2 = p.two_streams && p.mode == kDecode;
+  const int spu = dec2 ? 2 : 1;
+  auto combined = [&](int S) { return S > 1 || dec2; };
   int lu = 0, ls = 0, lc = 0;
   for (int qb = qb_beg; qb < qb_end; ++qb) {
     const int S = splits(qbt[qb]);
@@ -337,7 +340,10 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
       e.kvh = kvh;
       e.slot0 = so;
       e.n_split = S * spu;
-      e.pad[0] = e.pad[1] = e.pad[2] = 0;
+      // a split extend block of one query tile: its units' second stream
+      // fills the second half of each slot
+      e.pad[0] = p.two_streams && p.mode != kDecode && S > 1 && i1 - i0 <= p.q_tile_tok ? 2 : 1;
+      e.pad[1] = e.pad[2] = 0;
       p.comb[kvh * tcm + qco[qb]] = e;
     }
     for (int sp = 0; sp < S; ++sp) {
@@ -663,9 +669,15 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       const WorkUnit w = p.units[p.uorder[u]];
       // decode: warpgroup wg takes the unit's tiles wg, wg + 2, ... of the
       // one query tile (two key streams, merged by the combine)
-      const int nt = MODE == kDecode ? (w.n_tiles + 1 - wg) / 2 : w.n_tiles;
-      const int tok0 = MODE == kDecode ? 0 : wg * TOK;  // first token of this Q tile
-      if (MODE != kDecode && wg == 1 && w.n_tok <= TOK) continue;
+      // Two key streams (decode units; split units of one query tile):
+      // warpgroup wg takes the unit's tiles wg, wg + 2, ... of the one query
+      // tile and writes its own partial, which the combine merges.
+      const bool two = MODE == kDecode || (w.slot >= 0 && w.n_tok <= TOK);
+      // this warpgroup's tiles: j0, j0 + jstep, ... below the unit's n_tiles
+      const int j0 = two ? wg : 0, jstep = two ? 2 : 1;
+      const int nt = w.n_tiles - j0;  // > 0 when the warpgroup has a tile
+      const int tok0 = two ? 0 : wg * TOK;  // first token of this warpgroup's Q rows
+      if (!two && wg == 1 && w.n_tok <= TOK) continue;
       const int n_tok_i = min(TOK, w.n_tok - tok0);
       const int rows_valid = n_tok_i * G;
       const bool valid = r < rows_valid;
@@ -675,7 +687,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       const int qmin = w.qpos0 + tok0, qmax = w.qpos0 + tok0 + n_tok_i - 1;
       const int64_t orow_idx = (int64_t)(w.q_tok0 + t) * p.hq + w.kvh * G + g;
       const int64_t prow_idx =
-          (int64_t)(w.slot + (MODE == kDecode ? wg : 0)) * p.rows_per_slot + tok0 * G + r;
+          MODE == kDecode ? (int64_t)(w.slot + wg) * p.rows_per_slot + r
+                          : (int64_t)w.slot * p.rows_per_slot + wg * TOK * G + r;
       // custom mask rows: a byte per key of the sequence for each extend
       // token; mbase is the row of this Q tile's first token
       const uint8_t *mbase = nullptr;
@@ -687,7 +700,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
                                     : (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]);
         mbase = p.custom_mask + p.mask_indptr[w.b] + (int64_t)(w.q_tok0 + tok0 - qo0) * mstride;
       }
-      if (nt == 0) {
+      if (nt <= 0) {
         if (valid) {
           if (w.slot < 0) {
             bf16 *orow = p.o + orow_idx * C::HDV;
@@ -704,9 +717,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         continue;
       }
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < nt; ++j) {
+      for (int j = j0; j < w.n_tiles; j += jstep) {
         int kb, ke;
-        tile_keys(w, MODE == kDecode ? 2 * j + wg : j, kb, ke);
+        tile_keys(w, j, kb, ke);
         // Mask bits of this thread's row for keys kb + 32 q + bit (q < 4).
         // The G heads of a token share its mask row, so the warp walks its
         // rows' tokens: all lanes read 32 consecutive bytes of the token's
@@ -834,7 +847,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           // quiescent here.)
           const bool grow = m_new > m + 8.0f;
           const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
-          const bool o_needs = grow && j > 0 && l > 0.f;
+          const bool o_needs = grow && j > j0 && l > 0.f;
           if (grow) {
             l *= alpha;
             m = m_new;
@@ -1013,7 +1026,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         }
         ++q_cnt;
         tc_fence_after();
-        if constexpr (MODE == kDecode) {
+        if (MODE == kDecode || (w.slot >= 0 && !q1)) {
           // Two key streams over the one query tile: even tiles into S/P
           // buffer 0 (softmax warpgroup 0, O 0), odd tiles into buffer 1
           // (warpgroup 1, O 1).  S(j) waits only for PV(j-2), which reads
@@ -1503,9 +1516,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const WsHeader *hdr, const
     const int e = (int)(idx / rows_per_slot), r = (int)(idx % rows_per_slot);
     const CombineEntry E = ce[e];
     if (r >= E.n_tok * group) continue;
+    // partial i: slot slot0 + i / halves, half i % halves (halves = 2 when
+    // the block's two key streams share each slot)
+    const int halves = E.pad[0] == 2 ? 2 : 1, n_part = E.n_split * halves;
+    auto prow = [&](int i) {
+      return (int64_t)(E.slot0 + i / halves) * rows_per_slot + (i % halves) * (rows_per_slot / 2) +
+             r;
+    };
     float mx = -INFINITY;
-    for (int i = 0; i < E.n_split; ++i)
-      mx = fmaxf(mx, plse[(int64_t)(E.slot0 + i) * rows_per_slot + r]);
+    for (int i = 0; i < n_part; ++i) mx = fmaxf(mx, plse[prow(i)]);
     const int t = r / group, g = r - t * group;
     const int64_t orow = (int64_t)(E.q_tok0 + t) * hq + E.kvh * group + g;
     // a sink (natural-log logit of the head) joins the denominator once
@@ -1519,13 +1538,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const WsHeader *hdr, const
       continue;
     }
     float wsum = sinks ? exp2f((sink - mx) * 1.4426950408889634f) : 0.f;
-    for (int i = 0; i < E.n_split; ++i)
-      wsum += exp2f((plse[(int64_t)(E.slot0 + i) * rows_per_slot + r] - mx) * 1.4426950408889634f);
+    for (int i = 0; i < n_part; ++i) wsum += exp2f((plse[prow(i)] - mx) * 1.4426950408889634f);
     const float inv = 1.0f / wsum;
     for (int c = lane * 8; c < hdv; c += 256) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int i = 0; i < E.n_split; ++i) {
-        const int64_t sr = (int64_t)(E.slot0 + i) * rows_per_slot + r;
+      for (int i = 0; i < n_part; ++i) {
+        const int64_t sr = prow(i);
         const float wi = exp2f((plse[sr] - mx) * 1.4426950408889634f) * inv;
         const float *src = po + sr * hdv + c;
         const float4 a = *reinterpret_cast<const float4 *>(src);
@@ -1716,7 +1734,7 @@ int launch_attention(const AttnArgs &a) {
   sp.no_causal = a.custom_mask != nullptr;
   sp.key_set = a.mode == kTwoStage ? a.key_set : kAllKeys;
   sp.keep_status = a.keep_status;
-  sp.two_streams = decode && !mla;
+  sp.two_streams = !mla;
   sp.n_dsplit = mla ? MlaCfg<0>::LV / MlaCfg<0>::DVS : 1;
   sp.window = a.window;
   sp.num_q_tokens = nq;
