@@ -1,40 +1,51 @@
 // attention.cu -- extend and decode attention over a page-size-1 KV pool for
 // sm_103a: a device-side work scheduler, a warp-specialised tcgen05/TMEM
-// attention kernel fed by TMA gathers, and the split-KV combine.
+// attention kernel whose K/V rows are gathered by cp.async copy warps, and
+// the split-KV combine.
 //
 // Method (sglang extend_attention.py, _fwd_kernel_unified and
 // extend_attention_fwd; flashinfer_backend.py, forward_decode):
 //   for each query row and each visible key j:  s_j = sm_scale * <q, k_j>,
-//   optionally s_j = cap * tanh(s_j / cap); visible iff j <= qpos and, with a
-//   window W > 0, qpos - j <= W; o = sum_j softmax(s)_j v_j; lse = log sum
-//   exp s.  The online softmax keeps a running max and sum per row and
-//   rescales the accumulator when the max moves.
+//   optionally s_j = cap * tanh(s_j / cap); visible iff j <= qpos (or, with a
+//   custom mask, iff its mask byte is set) and, with a window W > 0,
+//   qpos - j <= W; o = sum_j softmax(s)_j v_j (a sink logit per head joins
+//   the denominator); lse = log sum exp s.  The online softmax keeps a
+//   running max and sum per row and rescales the accumulator when the max
+//   moves.
 //
 // GB300 design (differs from the pages' Triton kernel, which launches one
 // program per (sequence, q head, 128-row block) and re-reads K/V per q head):
 //  * a Q tile = 128 rows = (tokens x the Hq/Hkv query heads of one KV head),
 //    and a CTA runs two Q tiles of consecutive tokens against each K/V tile:
 //    K/V of a KV head are gathered once for 2 x 128 query rows;
-//  * K and V rows are gathered from the pool by six warps with 16-byte
+//  * K and V rows are gathered from the pool by four warps with 16-byte
 //    cp.async copies placed straight into the 128-byte-swizzled layout the
 //    MMA descriptors read (random 256-byte rows need many copying threads
 //    to reach HBM bandwidth; a TMA gather4 moves only four 128-byte rows
 //    per instruction and stalls on its issue rate); each copying thread
 //    arrives on the stage barrier when its own copies land.  An index warp
-//    resolves every tile's slot indices into a small smem ring ahead of the
-//    copy warps and loads the Q tiles (3-D TMA boxes).  setmaxnreg moves
-//    registers from these warps to the softmax warpgroups;
+//    claims work units, resolves every tile's slot indices into a small smem
+//    ring ahead of the copy warps and loads the Q tiles (3-D TMA boxes).
+//    setmaxnreg moves registers from these warps to the softmax warpgroups;
 //  * QK^T and PV are tcgen05.mma (M=128, bf16 in, fp32 accumulate in TMEM).
 //    TMEM holds S and O of both Q tiles (4 x 128 columns).  The softmax
 //    warpgroup of a tile writes P (bf16) back over its S columns and PV
 //    reads A = P straight from TMEM.  While one warpgroup runs its softmax,
 //    the tensor core runs the other tile's PV and QK^T;
+//  * a unit with one Q tile (every decode unit; split extend units of at
+//    most 128/G tokens) runs two key streams instead: the two warpgroups
+//    take alternate K/V tiles with their own S/P and O, and the combine
+//    merges the two partials;
+//  * an fp8 pool (e4m3 / e5m2 codes with k_scale, v_scale) is staged as
+//    codes and converted in place to exact bf16 (f16 for decode) by the
+//    copy warps; the scales go into the logit scale and P (or the output);
 //  * the KV loop stops at the causal diagonal and starts at the window edge
 //    (the Triton kernel walks every tile and masks);
 //  * a device-built work list (no host sync, graph-safe) splits long key
 //    ranges across CTAs (split-KV); a combine kernel merges the partial
 //    (o, lse) pairs with the merge_state formula;
-//  * a persistent grid of one CTA per SM walks the work list.
+//  * a persistent grid of one CTA per SM claims the work units in cost
+//    order.
 #include <algorithm>
 #include <climits>
 #include <cstdio>
