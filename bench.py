@@ -446,27 +446,33 @@ def flush_l2(flush):
 
 def time_steps(step, steps, flush, dev, attn_events=False, pkx=None):
     """Per-step device time (ms) with CUDA events on the current stream, L2
-    flushed before each step outside the events; optionally the attention
-    kernel's own time."""
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ab = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ae = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    for e in ab + ae:
-        e.record()
-    torch.cuda.synchronize(dev)
-    for k in range(steps):
-        flush_l2(flush)
-        if attn_events:
-            pkx.set_attention_events(ab[k], ae[k])
-        starts[k].record()
-        step()
-        ends[k].record()
-    if attn_events:
-        pkx.set_attention_events(None, None)
-    torch.cuda.synchronize(dev)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    attn_ms = [s.elapsed_time(e) for s, e in zip(ab, ae)] if attn_events else None
+    flushed before each step outside the events.  With ``attn_events`` a
+    second loop of the same steps times the attention kernel alone (events
+    recorded around it inside the library); the step times come from the
+    first, uninstrumented loop, since an event between two kernels keeps the
+    second from starting early."""
+    def loop(instrumented):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ab = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ae = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for e in ab + ae:
+            e.record()
+        torch.cuda.synchronize(dev)
+        for k in range(steps):
+            flush_l2(flush)
+            if instrumented:
+                pkx.set_attention_events(ab[k], ae[k])
+            starts[k].record()
+            step()
+            ends[k].record()
+        if instrumented:
+            pkx.set_attention_events(None, None)
+        torch.cuda.synchronize(dev)
+        return ([s.elapsed_time(e) for s, e in zip(starts, ends)],
+                [s.elapsed_time(e) for s, e in zip(ab, ae)])
+    step_ms, _ = loop(False)
+    attn_ms = loop(True)[1] if attn_events else None
     return step_ms, attn_ms
 
 

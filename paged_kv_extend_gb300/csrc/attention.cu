@@ -227,6 +227,8 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   int32_t *nqb = p.seq;                 // [B]  query blocks per sequence
   int32_t *qboff = p.seq + 1 * (B + 1); // [B]  first query block of sequence
 
+  grid_dep_wait();    // inputs written by the previous kernel on the stream
+  grid_dep_launch();  // the attention grid may start its prologue now
   if (tid == 0) {
     if (!p.keep_status) p.hdr->status = 0;
     p.hdr->next_unit = 0;
@@ -656,6 +658,10 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the prologue above reads no global memory; the work list, indices and
+  // Q come from the kernels before this one on the stream
+  grid_dep_wait();
+  grid_dep_launch();  // the combine may be scheduled (it waits for this grid)
   const uint32_t tmem = s_tmem;
   const int n_units = p.hdr->n_units;
   const int G = p.group, TOK = p.tok;
@@ -1519,6 +1525,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const WsHeader *hdr, const
                                                       bf16 *o, float *lse, const float *sinks,
                                                       int hq, int group, int hdv,
                                                       int rows_per_slot) {
+  grid_dep_wait();  // the attention kernel's partials
   const int n_comb = hdr->n_combine;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -1543,31 +1550,26 @@ __global__ void __launch_bounds__(256) combine_kernel(const WsHeader *hdr, const
     const float mx_p = mx;
     mx = fmaxf(mx, sink);
     if (mx_p == -INFINITY) {
-      for (int c = lane * 8; c < hdv; c += 256)
-        *reinterpret_cast<uint4 *>(o + orow * hdv + c) = make_uint4(0, 0, 0, 0);
+      for (int c = lane * 4; c < hdv; c += 128)
+        *reinterpret_cast<uint2 *>(o + orow * hdv + c) = make_uint2(0, 0);
       if (lane == 0 && lse) lse[orow] = sink;  // -inf without a sink
       continue;
     }
     float wsum = sinks ? exp2f((sink - mx) * 1.4426950408889634f) : 0.f;
     for (int i = 0; i < n_part; ++i) wsum += exp2f((plse[prow(i)] - mx) * 1.4426950408889634f);
     const float inv = 1.0f / wsum;
-    for (int c = lane * 8; c < hdv; c += 256) {
-      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    // every lane takes 4 consecutive value dims (a 128-dim row is one pass
+    // of the warp)
+    for (int c = lane * 4; c < hdv; c += 128) {
+      float acc[4] = {0, 0, 0, 0};
       for (int i = 0; i < n_part; ++i) {
         const int64_t sr = prow(i);
         const float wi = exp2f((plse[sr] - mx) * 1.4426950408889634f) * inv;
-        const float *src = po + sr * hdv + c;
-        const float4 a = *reinterpret_cast<const float4 *>(src);
-        const float4 b = *reinterpret_cast<const float4 *>(src + 4);
+        const float4 a = *reinterpret_cast<const float4 *>(po + sr * hdv + c);
         acc[0] += wi * a.x; acc[1] += wi * a.y; acc[2] += wi * a.z; acc[3] += wi * a.w;
-        acc[4] += wi * b.x; acc[5] += wi * b.y; acc[6] += wi * b.z; acc[7] += wi * b.w;
       }
-      uint4 pk;
-      pk.x = pack_bf16(acc[0], acc[1]);
-      pk.y = pack_bf16(acc[2], acc[3]);
-      pk.z = pack_bf16(acc[4], acc[5]);
-      pk.w = pack_bf16(acc[6], acc[7]);
-      *reinterpret_cast<uint4 *>(o + orow * hdv + c) = pk;
+      *reinterpret_cast<uint2 *>(o + orow * hdv + c) =
+          make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
     }
     if (lane == 0 && lse) lse[orow] = mx + logf(wsum);
   }
@@ -1669,7 +1671,10 @@ static int launch_attn_kernel(const TMaps &tmaps, const KParams &kp, int grid, c
       return set_error(PKX_ECUDA, "cudaFuncSetAttribute(attn_kernel): %s", cudaGetErrorString(e));
     configured = true;
   }
-  attn_kernel<HD, MODE, MASK, FMT><<<grid, C::THREADS, C::SMEM, s>>>(tmaps, kp);
+  cudaError_t e = launch_pdl(attn_kernel<HD, MODE, MASK, FMT>, dim3(grid), dim3(C::THREADS),
+                             C::SMEM, s, tmaps, kp);
+  if (e != cudaSuccess)
+    return set_error(PKX_ECUDA, "attn_kernel launch: %s", cudaGetErrorString(e));
   return PKX_OK;
 }
 
@@ -1693,7 +1698,10 @@ static int launch_mla_kernel(const KParams &kp, int grid, cudaStream_t s) {
       return set_error(PKX_ECUDA, "cudaFuncSetAttribute(mla_kernel): %s", cudaGetErrorString(e));
     configured = true;
   }
-  mla_kernel<MODE, MASK><<<grid, C::THREADS, C::SMEM, s>>>(kp);
+  cudaError_t e = launch_pdl(mla_kernel<MODE, MASK>, dim3(grid), dim3(C::THREADS), C::SMEM, s,
+                             kp);
+  if (e != cudaSuccess)
+    return set_error(PKX_ECUDA, "mla_kernel launch: %s", cudaGetErrorString(e));
   return PKX_OK;
 }
 
@@ -1760,7 +1768,11 @@ int launch_attention(const AttnArgs &a) {
   sp.uorder = reinterpret_cast<int32_t *>(ws + L.uorder_off);
   sp.comb = reinterpret_cast<CombineEntry *>(ws + L.comb_off);
   sp.hdr = hdr;
-  sched_kernel<<<1, 1024, 0, a.stream>>>(sp);
+  {
+    cudaError_t e = launch_pdl(sched_kernel, dim3(1), dim3(1024), 0, a.stream, sp);
+    if (e != cudaSuccess)
+      return set_error(PKX_ECUDA, "sched_kernel launch: %s", cudaGetErrorString(e));
+  }
 
   KParams kp;
   kp.q = static_cast<const bf16 *>(a.q);
@@ -1856,9 +1868,15 @@ int launch_attention(const AttnArgs &a) {
   }
   if (rc != PKX_OK) return rc;
   if (ev_after) cudaEventRecord(ev_after, a.stream);
-  combine_kernel<<<nsm * 2, 256, 0, a.stream>>>(hdr, sp.comb, kp.plse, kp.po, kp.o, a.lse,
-                                               a.sinks, a.hq, group, a.lv, L.rows_per_slot);
-  cudaError_t e = cudaGetLastError();
+  // one warp per combined row: enough CTAs for a full wave of warps (the
+  // rows' partial reads are latency-bound), eight per SM at most
+  const size_t comb_rows = (size_t)L.comb_max * L.rows_per_slot;
+  const int comb_grid = (int)std::min<size_t>((comb_rows + 7) / 8, (size_t)nsm * 8);
+  cudaError_t e = launch_pdl(combine_kernel, dim3(comb_grid > 0 ? comb_grid : 1), dim3(256), 0,
+                             a.stream,
+                             (const WsHeader *)hdr, (const CombineEntry *)sp.comb,
+                             (const float *)kp.plse, (const float *)kp.po, kp.o, a.lse, a.sinks,
+                             a.hq, group, a.lv, L.rows_per_slot);
   if (e != cudaSuccess) return set_error(PKX_ECUDA, "attention launch: %s", cudaGetErrorString(e));
   return PKX_OK;
 }

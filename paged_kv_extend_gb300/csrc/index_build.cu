@@ -8,13 +8,36 @@
 // (the prefix part of the running sum is prefix_kv_indptr[b] -
 // prefix_kv_indptr[0]; the extend part is a block reduction over
 // extend_seq_lens[0..b)), writes its indptr entry and prefix length, then
-// copies its two slices with coalesced 4-byte loads and 8-byte stores.  No
-// separate scan launch and no host sync.
+// copies its two slices with coalesced 4-byte loads and 8-byte stores, eight
+// loads in flight per thread.  No separate scan launch and no host sync.
 #include <cuda_runtime.h>
 
 #include "pkx_internal.h"
+#include "ptx.cuh"
 
 namespace pkx {
+
+// dst[j] = src[j] for j < n by the block's 256 threads, eight independent
+// loads in flight per thread before their stores (a long prefix is
+// thousands of entries; one load-then-store per step would serialise on
+// the memory latency).
+__device__ __forceinline__ void copy_widen(const int32_t *__restrict__ src, int64_t *dst, int n,
+                                           int tid) {
+  constexpr int U = 8;
+  for (int base = tid; base < n; base += 256 * U) {
+    int32_t v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = base + u * 256;
+      v[u] = j < n ? __ldg(src + j) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = base + u * 256;
+      if (j < n) dst[j] = v[u];
+    }
+  }
+}
 
 __global__ void __launch_bounds__(256) build_unified_kernel(
     const int32_t *__restrict__ prefix_kv_indptr, const int32_t *__restrict__ prefix_kv_indices,
@@ -22,6 +45,7 @@ __global__ void __launch_bounds__(256) build_unified_kernel(
     const int32_t *__restrict__ extend_kv_indices, int batch, int32_t *unified_kv_indptr,
     int64_t *unified_kv_indices, int32_t *prefix_lens) {
   __shared__ long long red[256];
+  grid_dep_launch();  // the scheduler may start (it waits for this grid's writes)
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   long long ext_before = 0;
@@ -42,11 +66,8 @@ __global__ void __launch_bounds__(256) build_unified_kernel(
     if (b == 0) unified_kv_indptr[0] = 0;
   }
   int64_t *dst = unified_kv_indices + start;
-  const int32_t *src_p = prefix_kv_indices + p0;
-  for (int j = tid; j < plen; j += 256) dst[j] = src_p[j];
-  const int32_t *src_e = extend_kv_indices + extend_start_loc[b];
-  int64_t *dst_e = dst + plen;
-  for (int j = tid; j < elen; j += 256) dst_e[j] = src_e[j];
+  copy_widen(prefix_kv_indices + p0, dst, plen, tid);
+  copy_widen(extend_kv_indices + extend_start_loc[b], dst + plen, elen, tid);
 }
 
 int launch_build_unified(const int32_t *prefix_kv_indptr, const int32_t *prefix_kv_indices,

@@ -109,6 +109,10 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the prologue above reads no global memory; the work list, indices and
+  // Q come from the kernels before this one on the stream
+  grid_dep_wait();
+  grid_dep_launch();
   const uint32_t tmem = s_tmem;
   const int n_units = p.hdr->n_units;
   const int G = p.group;

@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <utility>
 
 #include "../../include/pkx.h"
 
@@ -90,6 +91,25 @@ struct WsLayout {
 };
 
 int num_sms_current_device();
+
+// Launch `kernel` with programmatic stream serialization: it may start while
+// the previous kernel on the stream runs, and waits for it in-kernel
+// (grid_dep_wait) before reading its results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 // Events set by pkx_set_attention_events for this thread (may be null).
 void attention_events(cudaEvent_t *before, cudaEvent_t *after);
 int tokens_per_block(int group);

@@ -117,6 +117,20 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
+// ------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start before
+// the previous kernel on the stream has finished; it calls grid_dep_wait()
+// before its first read of anything that kernel wrote (the wait returns once
+// that grid has completed and its writes are visible; without the launch
+// attribute it returns at once).  grid_dep_launch() lets the next such
+// kernel start early.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy; src_bytes = 0 fills the 16 bytes with zeros.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
