@@ -87,6 +87,12 @@ const char *pkx_version(void);
 size_t pkx_extend_workspace_size(int batch, int num_q_tokens, int hq, int hkv,
                                  int lq, int lv);
 size_t pkx_decode_workspace_size(int batch, int hq, int hkv, int lq, int lv);
+/*
+ * The smallest workspace decode attention accepts.  With at least
+ * pkx_decode_workspace_size bytes every decode unit runs two key streams (the
+ * faster schedule); with less, but at least this many, one stream.
+ */
+size_t pkx_decode_workspace_min_size(int batch, int hq, int hkv, int lq, int lv);
 
 /*
  * Device status word of the last attention call that used `workspace`:

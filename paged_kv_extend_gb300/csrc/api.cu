@@ -102,6 +102,13 @@ size_t pkx_extend_workspace_size(int batch, int num_q_tokens, int hq, int hkv, i
       .total;
 }
 
+size_t pkx_decode_workspace_min_size(int batch, int hq, int hkv, int lq, int lv) {
+  if (batch < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM || lv <= 0) return 0;
+  return ws_layout(batch, batch, hkv, hq / hkv, lv, num_sms_current_device(), true,
+                   lq == 576 && lv == 512, false)
+      .total;
+}
+
 size_t pkx_decode_workspace_size(int batch, int hq, int hkv, int lq, int lv) {
   if (batch < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM || lv <= 0) return 0;
   return ws_layout(batch, batch, hkv, hq / hkv, lv, num_sms_current_device(), true,

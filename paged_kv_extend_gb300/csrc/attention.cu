@@ -421,6 +421,7 @@ struct KParams {
   // scale of pool tiles, v_scale into their P through the exponent
   // (2^(s - m + log2 v_scale)), and the tile's row sum is divided back
   float scale_log2_k, cap_pre_k, log2_v_scale, inv_v_scale, v_scale;
+  int dec_two;  // decode units run two key streams (else one)
   const int32_t *prefix_lens;   // unified form: prefix length per sequence
   const WorkUnit *units;
   const int32_t *uorder;  // units by cost, largest first
@@ -689,7 +690,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       // Two key streams (decode units; split units of one query tile):
       // warpgroup wg takes the unit's tiles wg, wg + 2, ... of the one query
       // tile and writes its own partial, which the combine merges.
-      const bool two = MODE == kDecode || (w.slot >= 0 && w.n_tok <= TOK);
+      const bool two = MODE == kDecode ? p.dec_two != 0 : (w.slot >= 0 && w.n_tok <= TOK);
       // this warpgroup's tiles: j0, j0 + jstep, ... below the unit's n_tiles
       const int j0 = two ? wg : 0, jstep = two ? 2 : 1;
       const int nt = w.n_tiles - j0;  // > 0 when the warpgroup has a tile
@@ -1043,7 +1044,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         }
         ++q_cnt;
         tc_fence_after();
-        if (MODE == kDecode || (w.slot >= 0 && !q1)) {
+        if (MODE == kDecode ? p.dec_two != 0 : (w.slot >= 0 && !q1)) {
           // Two key streams over the one query tile: even tiles into S/P
           // buffer 0 (softmax warpgroup 0, O 0), odd tiles into buffer 1
           // (warpgroup 1, O 1).  S(j) waits only for PV(j-2), which reads
@@ -1594,7 +1595,7 @@ int rows_per_slot(bool decode, int group, bool mla) {
 }
 
 WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int num_sms,
-                   bool decode, bool mla) {
+                   bool decode, bool mla, bool two_streams) {
   WsLayout L{};
   // tokens of a query block: two Q tiles (GQA kernel) or one (MLA kernel)
   const int tok = (mla ? 1 : 2) * tokens_per_block(group);
@@ -1603,7 +1604,7 @@ WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int 
   L.unit_max = (L.unit_target + hkv * L.qb_max) * (mla ? 4 : 1);
   L.slot_max = 2 * L.unit_target;
   L.comb_max = L.unit_target;
-  if (decode && !mla) {
+  if (decode && !mla && two_streams) {
     // two key streams per unit: two partial slots per unit, a combine entry
     // per (query block, KV head)
     L.slot_max = 2 * L.unit_max;
@@ -1713,6 +1714,16 @@ int launch_attention(const AttnArgs &a) {
   const bool mla = a.lq == 576 && a.lv == 512;
   const int nq = decode ? a.batch : a.num_q_tokens;
   WsLayout L = ws_layout(a.batch, nq, a.hkv, group, a.lv, nsm, decode, mla);
+  // Decode runs two key streams when the workspace holds their partial
+  // slots (pkx_decode_workspace_size asks for that), else one stream.
+  bool dec_two = decode && !mla;
+  if (dec_two && a.workspace_bytes < L.total) {
+    const WsLayout L1 = ws_layout(a.batch, nq, a.hkv, group, a.lv, nsm, decode, mla, false);
+    if (a.workspace_bytes >= L1.total) {
+      L = L1;
+      dec_two = false;
+    }
+  }
   if (mla) {
     // V must be the first 512 dims of each K row (the MLA layout).
     const bool pool_alias = a.v_buf == a.k_buf && a.vb_ss == a.kb_ss && a.vb_sh == a.kb_sh;
@@ -1753,7 +1764,7 @@ int launch_attention(const AttnArgs &a) {
   sp.no_causal = a.custom_mask != nullptr;
   sp.key_set = a.mode == kTwoStage ? a.key_set : kAllKeys;
   sp.keep_status = a.keep_status;
-  sp.two_streams = !mla;
+  sp.two_streams = !mla && (!decode || dec_two);
   sp.n_dsplit = mla ? MlaCfg<0>::LV / MlaCfg<0>::DVS : 1;
   sp.window = a.window;
   sp.num_q_tokens = nq;
@@ -1811,6 +1822,7 @@ int launch_attention(const AttnArgs &a) {
   kp.custom_mask = a.custom_mask;
   kp.mask_indptr = a.mask_indptr;
   kp.sinks = a.sinks;
+  kp.dec_two = dec_two ? 1 : 0;
   kp.log2_v_scale = log2f(a.v_scale);
   kp.v_scale = a.v_scale;
   kp.inv_v_scale = 1.0f / a.v_scale;

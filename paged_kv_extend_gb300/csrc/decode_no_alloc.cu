@@ -74,7 +74,9 @@ extern "C" int pkx_decode_attention_fwd_no_alloc(
     float sm_scale, float logit_cap, int sliding_window, float *lse_out, void *stream) {
   if (batch < 0) return set_error(PKX_EINVAL, "negative batch");
   if (batch == 0) return PKX_OK;
-  const size_t need = pkx_decode_workspace_size(batch, hq, hkv, lq, lv);
+  // the smallest workspace decode takes (one key stream per unit); the
+  // call runs two streams when the scratch also holds their slots
+  const size_t need = pkx_decode_workspace_min_size(batch, hq, hkv, lq, lv);
   if (need == 0) return set_error(PKX_EINVAL, "bad head configuration (hq=%d, hkv=%d)", hq, hkv);
   if (need > kNoAllocScratchBytes)
     return set_error(PKX_EWORKSPACE,

@@ -114,8 +114,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 void attention_events(cudaEvent_t *before, cudaEvent_t *after);
 int tokens_per_block(int group);
 int rows_per_slot(bool decode, int group, bool mla);
+// two_streams: the decode layout with two partial slots per unit (the GQA
+// kernel's two key streams); without it decode units run one stream.
 WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int num_sms,
-                   bool decode, bool mla);
+                   bool decode, bool mla, bool two_streams = true);
 
 // Arguments of one attention launch (any key mode).
 struct AttnArgs {

@@ -44,6 +44,7 @@ _SIGS = {
     "pkx_version": (ctypes.c_char_p, []),
     "pkx_extend_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "pkx_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "pkx_decode_workspace_min_size": (_sz, [_i, _i, _i, _i, _i]),
     "pkx_workspace_status": (_i, [_p, _p]),
     "pkx_set_attention_events": (None, [_p, _p]),
     "pkx_extend_attention_fwd": (_i, [
@@ -172,6 +173,11 @@ def extend_workspace_size(batch, num_q_tokens, hq, hkv, lq, lv) -> int:
 
 def decode_workspace_size(batch, hq, hkv, lq, lv) -> int:
     return int(load_library().pkx_decode_workspace_size(batch, hq, hkv, lq, lv))
+
+
+def decode_workspace_min_size(batch, hq, hkv, lq, lv) -> int:
+    """The smallest decode workspace (one key stream per unit)."""
+    return int(load_library().pkx_decode_workspace_min_size(batch, hq, hkv, lq, lv))
 
 
 def workspace_status(workspace: torch.Tensor) -> int:

@@ -57,7 +57,7 @@ def test_no_alloc_rejects_problem_beyond_scratch():
     dev = torch.device("cuda:0")
     h, d = 128, 128
     batch = 1000
-    while pkx.decode_workspace_size(batch, h, h, d, d) <= (96 << 20):
+    while pkx.decode_workspace_min_size(batch, h, h, d, d) <= (96 << 20):
         batch *= 2
         assert batch <= (1 << 17)
     q = torch.zeros(batch, h, d, dtype=torch.bfloat16, device=dev)
@@ -69,3 +69,34 @@ def test_no_alloc_rejects_problem_beyond_scratch():
         pkx.decode_attention_fwd_no_alloc(q, o, kb, kb, kvp, kvi)
     assert e.value.code == pkx.PKX_EWORKSPACE
     assert "scratch" in str(e.value)
+
+
+def test_no_alloc_falls_back_to_one_key_stream():
+    """A batch whose two-stream scratch exceeds the built-in array but whose
+    one-stream scratch fits runs with one key stream per unit, and matches
+    the workspace call (two streams)."""
+    dev = torch.device("cuda:0")
+    hq, hkv, d, t = 32, 8, 128, 40
+    batch = 256
+    while pkx.decode_workspace_size(batch, hq, hkv, d, d) <= (96 << 20):
+        batch *= 2
+    assert pkx.decode_workspace_min_size(batch, hq, hkv, d, d) <= (96 << 20)
+    g = torch.Generator().manual_seed(5)
+    slots = batch * t
+    kb = torch.randn(slots, hkv, d, generator=g).to(torch.bfloat16).to(dev)
+    vb = torch.randn(slots, hkv, d, generator=g).to(torch.bfloat16).to(dev)
+    q = torch.randn(batch, hq, d, generator=g).to(torch.bfloat16).to(dev)
+    lens = torch.randint(1, t + 1, (batch,), generator=g)
+    kvp = torch.cat([torch.zeros(1, dtype=torch.int64), lens.cumsum(0)]).to(torch.int32).to(dev)
+    kvi = torch.randperm(slots, generator=g)[: int(lens.sum())].to(torch.int32).to(dev)
+    o_ref = torch.empty(batch, hq, d, dtype=torch.bfloat16, device=dev)
+    l_ref = torch.empty(batch, hq, dtype=torch.float32, device=dev)
+    pkx.decode_attention_fwd(q, o_ref, kb, vb, kvp, kvi, lse=l_ref)
+    o = torch.full_like(o_ref, float("nan"))
+    lse = torch.full_like(l_ref, float("nan"))
+    pkx.decode_attention_fwd_no_alloc(q, o, kb, vb, kvp, kvi, lse=lse)
+    torch.cuda.synchronize()
+    err = (o.float() - o_ref.float()).abs()
+    assert torch.isfinite(o.float()).all()
+    assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS
+    assert (lse - l_ref).abs().max().item() <= LSE_ABS
