@@ -236,7 +236,10 @@ int pkx_extend_attention_fwd_unified(
  * o = 0 and lse = -inf.
  *   q  bf16 [batch, hq, lq] contiguous;  o  bf16 [batch, hq, lv] contiguous
  *   kv_indptr int32 [batch+1]; kv_indices int32 [kv_indptr[batch]]
- *   workspace >= pkx_decode_workspace_size(...) bytes
+ *   kv_dtype, k_scale, v_scale  the pool's format and scales (PKX_KV_*)
+ *   workspace >= pkx_decode_workspace_size(...) bytes for the two-key-stream
+ *             schedule; at least pkx_decode_workspace_min_size(...) bytes
+ *             runs one stream per unit (same results)
  */
 int pkx_decode_attention_fwd(
     const void *q, void *o, const void *k_buffer, const void *v_buffer,
