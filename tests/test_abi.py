@@ -166,3 +166,24 @@ def test_workspace_size_grows_with_problem(lib):
     assert pkx.extend_workspace_size(16, 90000, 32, 8, 128, 128) > a
     assert pkx.extend_workspace_size(16, 9000, 30, 8, 128, 128) == 0  # hq % hkv != 0
     assert pkx.decode_workspace_size(64, 32, 8, 128, 128) > 0
+
+
+def test_workspace_size_relations(lib):
+    """Host-side sizing the calls rely on: the one-stream decode layout never
+    exceeds the two-stream one (the call falls back to it), the ragged +
+    paged split holds at least one extend pass's scratch, and sizes grow
+    with the problem."""
+    for hq, hkv, d in [(32, 8, 128), (16, 16, 64), (28, 4, 128), (64, 8, 64), (16, 1, 576)]:
+        lv = 512 if d == 576 else d
+        prev = 0
+        for b in (1, 7, 64, 1000, 4096):
+            full = pkx.decode_workspace_size(b, hq, hkv, d, lv)
+            small = pkx.decode_workspace_min_size(b, hq, hkv, d, lv)
+            assert 0 < small <= full
+            assert full >= prev
+            prev = full
+        for b, n in ((1, 1), (16, 8353), (256, 100000)):
+            ext = pkx.extend_workspace_size(b, n, hq, hkv, d, lv)
+            split = pkx.ragged_paged_workspace_size(b, n, hq, hkv, d, lv)
+            assert 0 < ext < split
+    assert pkx.decode_workspace_min_size(4, 30, 8, 128, 128) == 0  # hq % hkv != 0
