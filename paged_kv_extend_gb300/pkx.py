@@ -278,7 +278,8 @@ def extend_attention_fwd_unified(q, o, k_buffer, v_buffer, qo_indptr, kv_indptr,
                                  lse=None, workspace=None, custom_mask=None, mask_indptr=None,
                                  sinks=None, k_scale=1.0, v_scale=1.0):
     """Unified extend attention (pkx_extend_attention_fwd_unified); int64
-    kv_indices over every key.  Writes o (and lse) in place."""
+    kv_indices over every key.  Writes o (and lse) in place.  The pool may be
+    fp8 (torch.float8_e4m3fn / float8_e5m2) with k_scale / v_scale."""
     lib = load_library()
     n, hq, lq = q.shape
     hkv = k_buffer.shape[1]
@@ -303,7 +304,11 @@ def extend_attention_fwd_unified(q, o, k_buffer, v_buffer, qo_indptr, kv_indptr,
 def decode_attention_fwd(q, o, k_buffer, v_buffer, kv_indptr, kv_indices, sm_scale=None,
                          logit_cap=0.0, sliding_window=-1, lse=None, workspace=None,
                          k_scale=1.0, v_scale=1.0):
-    """Decode attention (pkx_decode_attention_fwd): q [B, Hq, Lq] -> o."""
+    """Decode attention (pkx_decode_attention_fwd): q [B, Hq, Lq] -> o.  The
+    pool may be fp8 (torch.float8_e4m3fn / float8_e5m2) with k_scale /
+    v_scale.  A given ``workspace`` of at least decode_workspace_min_size
+    bytes is accepted (two key streams per unit from decode_workspace_size
+    bytes up, one below)."""
     lib = load_library()
     b, hq, lq = q.shape
     hkv = k_buffer.shape[1]
