@@ -187,3 +187,25 @@ def test_workspace_size_relations(lib):
             split = pkx.ragged_paged_workspace_size(b, n, hq, hkv, d, lv)
             assert 0 < ext < split
     assert pkx.decode_workspace_min_size(4, 30, 8, 128, 128) == 0  # hq % hkv != 0
+
+
+def test_plain_c_consumer(lib, tmp_path):
+    """pkx.h compiles as strict C99 and C++11, and a C program linked against
+    libpkx.so gets the version, workspace sizes and host-side rejections
+    without Python in between."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None or shutil.which("g++") is None:
+        pytest.skip("no host C compiler")
+    libdir = os.path.dirname(pkx.LIB_PATH)
+    exe = str(tmp_path / "c_consumer")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "c_consumer.c"),
+                    "-L", libdir, "-lpkx", "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.startswith("ok ") and "sm_103a" in r.stdout
+    cxx = tmp_path / "header.cpp"
+    cxx.write_text('#include "pkx.h"\nint main() { return pkx_version() == nullptr; }\n')
+    subprocess.run(["g++", "-std=c++11", "-Wall", "-Werror", "-pedantic", "-fsyntax-only",
+                    "-I", os.path.join(ROOT, "include"), str(cxx)], check=True)
