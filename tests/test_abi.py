@@ -66,6 +66,10 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _extend(lib, hq=6, hkv=4) == pkx.PKX_EINVAL
     assert b"multiple" in lib.pkx_last_error_string()
     assert _extend(lib, lq=96, lv=96) == pkx.PKX_EUNSUPPORTED
+    # the other split head dims are not built: a clean refusal, not a launch
+    assert _extend(lib, lq=192, lv=128) == pkx.PKX_EUNSUPPORTED
+    assert b"lq=192" in lib.pkx_last_error_string()
+    assert _extend(lib, lq=288, lv=256, hq=16, hkv=1) == pkx.PKX_EUNSUPPORTED
     assert _extend(lib, hq=256, hkv=1) == pkx.PKX_EUNSUPPORTED
     assert _extend(lib, batch=-1) == pkx.PKX_EINVAL
     assert _extend(lib, scale=float("nan")) == pkx.PKX_EINVAL

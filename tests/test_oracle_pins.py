@@ -78,7 +78,8 @@ def _dense_reference(wl, cap, window, masks=None, sinks=None):
 
 
 # ------------------------------------------------------------ prefix = 0 case
-@pytest.mark.parametrize("lq,lv,hq,hkv", [(64, 64, 4, 2), (128, 128, 8, 2), (96, 80, 6, 3)])
+@pytest.mark.parametrize("lq,lv,hq,hkv", [(64, 64, 4, 2), (128, 128, 8, 2), (96, 80, 6, 3),
+                                          (192, 128, 4, 1), (288, 256, 2, 1)])
 def test_no_prefix_is_torch_causal_sdpa(lq, lv, hq, hkv):
     """With no cached prefix, extend attention is plain causal attention
     (flashinfer_backend.py, forward_extend: the ragged result alone when no
@@ -135,6 +136,19 @@ def test_mla_shape_matches_dense_formulation():
                       sm_scale=1 / math.sqrt(192)))
     o, lse = _run_oracle(wl)
     ro, rl = _dense_reference(wl, 0.0, -1)
+    torch.testing.assert_close(o, ro, rtol=0, atol=TOL)
+    torch.testing.assert_close(lse, rl, rtol=0, atol=TOL)
+
+
+@pytest.mark.parametrize("lq,lv,seed", [(192, 128, 31), (288, 256, 32)])
+def test_split_head_dims_match_dense_formulation(lq, lv, seed):
+    """The other split head dims (extend_attention.py, the Lq = 192 = 128 +
+    64 and Lq = 288 = 256 + 32 cases): the score is the full Lq-dim dot
+    product and V has its own Lv dims; prefix, GQA and cap as elsewhere."""
+    wl = W.draw(_spec(batch=3, hq=4, hkv=2, lq=lq, lv=lv, prefix=[0, 9, 17],
+                      extend=[5, 3, 1], seed=seed, std=0.7))
+    o, lse = _run_oracle(wl, cap=20.0, window=-1)
+    ro, rl = _dense_reference(wl, 20.0, -1)
     torch.testing.assert_close(o, ro, rtol=0, atol=TOL)
     torch.testing.assert_close(lse, rl, rtol=0, atol=TOL)
 
