@@ -10,7 +10,8 @@
  *    are preallocated by the caller and written in place.  A call never
  *    allocates device memory and never synchronises the host with the
  *    device; everything is enqueued on `stream` (a cudaStream_t; NULL is
- *    the legacy default stream).
+ *    the legacy default stream).  Kernels run on the calling thread's
+ *    current CUDA device: `stream` and every pointer must belong to it.
  *  - bf16 means IEEE bfloat16 (16 bits).  Shapes are written outermost
  *    first; the last dimension is always contiguous.  Strides are in
  *    ELEMENTS.
