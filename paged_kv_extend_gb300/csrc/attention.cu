@@ -1006,7 +1006,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           constexpr int kk = decltype(kk_c)::value;
           constexpr uint32_t ao = ((kk / 4) * (C::BM * 128) + (kk % 4) * 32) / 16;
           constexpr uint32_t bo = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) / 16;
-          tc_mma_ss_step<ao, bo>(d, a_lo, b_lo, K_HI, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          tc_mma_ss_step<ao, bo>(d, a_lo, b_lo, K_HI, IDQK, kk > 0 ? 1u : 0u);
         });
         tc_commit(&bars[B_S_FULL + qt]);
       };

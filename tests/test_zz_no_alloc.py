@@ -100,3 +100,35 @@ def test_no_alloc_falls_back_to_one_key_stream():
     assert torch.isfinite(o.float()).all()
     assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS
     assert (lse - l_ref).abs().max().item() <= LSE_ABS
+
+
+@pytest.mark.parametrize("dt", [torch.float8_e4m3fn, torch.float8_e5m2])
+def test_fp8_decode_with_one_stream_workspace(dt):
+    """Decode over an fp8 pool given only decode_workspace_min_size bytes: one
+    key stream per unit, whose products run in f16 like the two-stream path
+    (the codes' values, the query times 2^-8), against the oracle."""
+    import oracle
+    dev = torch.device("cuda:0")
+    lens = [1, 130, 2049, 700]
+    hq, hkv, d, ks, vs = 16, 2, 128, 0.1, 0.04
+    spec = W.WorkloadSpec("dec", batch=len(lens), hq=hq, hkv=hkv, lq=d, lv=d,
+                          prefix=[t - 1 for t in lens], extend=[1] * len(lens),
+                          num_slots=2 * sum(lens) + 16, logit_cap=30.0, seed=71, decode=True)
+    wl = W.draw(spec)
+    kb, vb = wl.pool_fp8(dt, ks, vs)
+    ro, rl = oracle.decode_attention(wl.q, kb, vb, wl.kv_indptr, wl.kv_indices, wl.sm_scale,
+                                     30.0, -1, k_scale=ks, v_scale=vs)
+    n_min = pkx.decode_workspace_min_size(wl.batch, hq, hkv, d, d)
+    assert n_min < pkx.decode_workspace_size(wl.batch, hq, hkv, d, d)
+    ws = torch.empty(n_min, dtype=torch.uint8, device=dev)
+    o = torch.full((wl.batch, hq, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((wl.batch, hq), float("nan"), dtype=torch.float32, device=dev)
+    pkx.decode_attention_fwd(wl.q.to(dev), o, kb.to(dev), vb.to(dev), wl.kv_indptr.to(dev),
+                             wl.kv_indices.to(dev), wl.sm_scale, 30.0, lse=lse, workspace=ws,
+                             k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    err = (o.float().cpu() - ro.float()).abs()
+    assert torch.isfinite(o.float()).all()
+    assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS
+    assert (lse.cpu() - rl.float()).abs().max().item() <= LSE_ABS
