@@ -229,7 +229,8 @@ def extend_attention_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buf
             raise ValueError(f"{nm} must be contiguous bf16")
     _i32(qo_indptr, "qo_indptr"), _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
     ws = _workspace(workspace, extend_workspace_size(batch, n, hq, hkv, lq, lv), q_extend.device)
-    _check(_on(q_extend.device, lib.pkx_extend_attention_fwd,
+    _check(_on(
+        q_extend.device, lib.pkx_extend_attention_fwd,
         _ptr(q_extend), _ptr(k_extend), _ptr(v_extend), _ptr(o_extend), _ptr(k_buffer),
         _ptr(v_buffer), _ptr(qo_indptr), _ptr(kv_indptr),
         _ptr(kv_indices) if kv_indices.numel() else None, batch, n, hq, hkv, lq, lv,
@@ -267,7 +268,8 @@ def extend_attention_fwd_ragged_paged(q_extend, k_extend, v_extend, o_extend, k_
     _i32(qo_indptr, "qo_indptr"), _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
     ws = _workspace(workspace, ragged_paged_workspace_size(batch, n, hq, hkv, lq, lv),
                     q_extend.device)
-    _check(_on(q_extend.device, lib.pkx_extend_attention_fwd_ragged_paged,
+    _check(_on(
+        q_extend.device, lib.pkx_extend_attention_fwd_ragged_paged,
         _ptr(q_extend), _ptr(k_extend), _ptr(v_extend), _ptr(o_extend), _ptr(k_buffer),
         _ptr(v_buffer), _ptr(qo_indptr), _ptr(kv_indptr),
         _ptr(kv_indices) if kv_indices.numel() else None, batch, n, hq, hkv, lq, lv,
@@ -294,7 +296,8 @@ def extend_attention_fwd_unified(q, o, k_buffer, v_buffer, qo_indptr, kv_indptr,
         raise ValueError("kv_indices must be contiguous int64")
     _i32(qo_indptr, "qo_indptr"), _i32(kv_indptr, "kv_indptr"), _i32(prefix_lens, "prefix_lens")
     ws = _workspace(workspace, extend_workspace_size(batch, n, hq, hkv, lq, lv), q.device)
-    _check(_on(q.device, lib.pkx_extend_attention_fwd_unified,
+    _check(_on(
+        q.device, lib.pkx_extend_attention_fwd_unified,
         _ptr(q), _ptr(o), _ptr(k_buffer), _ptr(v_buffer), _ptr(qo_indptr), _ptr(kv_indptr),
         _ptr(kv_indices) if kv_indices.numel() else None, _ptr(prefix_lens), batch, n, hq, hkv,
         lq, lv, kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0], float(sm_scale or 0.0),
@@ -319,7 +322,8 @@ def decode_attention_fwd(q, o, k_buffer, v_buffer, kv_indptr, kv_indices, sm_sca
     kb, vb, kv_dtype = _pool_rows(k_buffer, v_buffer)
     _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
     ws = _workspace(workspace, decode_workspace_size(b, hq, hkv, lq, lv), q.device)
-    _check(_on(q.device, lib.pkx_decode_attention_fwd,
+    _check(_on(
+        q.device, lib.pkx_decode_attention_fwd,
         _ptr(q), _ptr(o), _ptr(k_buffer), _ptr(v_buffer), _ptr(kv_indptr),
         _ptr(kv_indices) if kv_indices.numel() else None, b, hq, hkv, lq, lv,
         kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0], float(sm_scale or 0.0),
@@ -341,7 +345,8 @@ def decode_attention_fwd_no_alloc(q, o, k_buffer, v_buffer, kv_indptr, kv_indice
     kb = _rows(k_buffer, "k_buffer")
     vb = _rows(v_buffer, "v_buffer")
     _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
-    _check(_on(q.device, lib.pkx_decode_attention_fwd_no_alloc,
+    _check(_on(
+        q.device, lib.pkx_decode_attention_fwd_no_alloc,
         _ptr(q), _ptr(o), _ptr(k_buffer), _ptr(v_buffer), _ptr(kv_indptr),
         _ptr(kv_indices) if kv_indices.numel() else None, b, hq, hkv, lq, lv,
         kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0], float(sm_scale or 0.0),
@@ -385,7 +390,8 @@ def build_unified_kv_indices(prefix_kv_indptr, prefix_kv_indices, extend_start_l
         plen = torch.empty(bs, dtype=torch.int32, device=dev)
     else:
         uptr, uidx, plen = out
-    _check(_on(dev, lib.pkx_build_unified_kv_indices,
+    _check(_on(
+        dev, lib.pkx_build_unified_kv_indices,
         _ptr(prefix_kv_indptr), _ptr(prefix_kv_indices) if prefix_kv_indices.numel() else None,
         _ptr(extend_start_loc), _ptr(extend_seq_lens),
         _ptr(extend_kv_indices) if extend_kv_indices.numel() else None, int(bs), _ptr(uptr),
@@ -419,7 +425,8 @@ def set_kv_buffer(k_buffer, v_buffer, cache_loc, k, v=None):
             raise ValueError("v / v_buffer shapes do not match k")
         if v_buffer.shape[0] != k_buffer.shape[0]:
             raise ValueError("k_buffer and v_buffer must have the same number of slots")
-    _check(_on(k.device, lib.pkx_set_kv_buffer,
+    _check(_on(
+        k.device, lib.pkx_set_kv_buffer,
         _ptr(k), ks[0], ks[1], _ptr(v), vs[0], vs[1], _ptr(cache_loc) if n else None, n, hkv,
         lk, lv, _ptr(k_buffer), kbs[0], kbs[1], _ptr(v_buffer) if v is not None else None,
         vbs[0], vbs[1], k_buffer.shape[0]))
@@ -453,7 +460,8 @@ def create_kv_indices(req_to_token, req_pool_indices, paged_kernel_lens, kv_star
         kv_indices = torch.empty(int(capacity), dtype=torch.int32, device=dev)
     _i32(kv_indptr, "kv_indptr")
     _i32(kv_indices, "kv_indices")
-    _check(_on(dev, lib.pkx_create_kv_indices,
+    _check(_on(
+        dev, lib.pkx_create_kv_indices,
         _ptr(req_to_token) if req_to_token.numel() else None, req_to_token.shape[0],
         req_to_token.stride(0), _ptr(req_pool_indices) if bs else None,
         _ptr(paged_kernel_lens) if bs else None,
@@ -481,7 +489,8 @@ def set_kv_buffer_fp8(k_buffer, v_buffer, cache_loc, k, v, k_scale, v_scale):
     if v is not None:
         vs = _rows(v, "v")
         lv = v.shape[2]
-    _check(_on(k.device, lib.pkx_set_kv_buffer_fp8,
+    _check(_on(
+        k.device, lib.pkx_set_kv_buffer_fp8,
         _ptr(k), ks[0], ks[1], _ptr(v), vs[0], vs[1], _ptr(cache_loc) if n else None, n, hkv,
         lk, lv, float(k_scale), float(v_scale), fmt, _ptr(k_buffer), kb[0], kb[1],
         _ptr(v_buffer) if v is not None else None, vb[0], vb[1], k_buffer.shape[0]))
@@ -508,7 +517,8 @@ def expand_paged_kv_indices(kv_indptr, kv_indices, kv_last_page_len, page_size,
         token_indices = torch.empty(int(capacity), dtype=torch.int32, device=dev)
     _i32(token_indptr, "token_indptr")
     _i32(token_indices, "token_indices")
-    _check(_on(dev, lib.pkx_expand_paged_kv_indices,
+    _check(_on(
+        dev, lib.pkx_expand_paged_kv_indices,
         _ptr(kv_indptr), _ptr(kv_indices) if kv_indices.numel() else None,
         _ptr(kv_last_page_len), int(page_size), int(bs), _ptr(token_indptr),
         _ptr(token_indices) if token_indices.numel() else None, token_indices.numel()))
