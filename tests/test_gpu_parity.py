@@ -109,17 +109,27 @@ def test_merge_state_vs_oracle(n, h, dv):
     assert (s.double().cpu()[fin] - rs[fin]).abs().max().item() <= 1e-5 if fin.any() else True
 
 
-def test_merge_state_in_place():
-    g = torch.Generator().manual_seed(5)
-    va = torch.randn(64, 4, 128, generator=g).to(torch.bfloat16)
-    vb = torch.randn(64, 4, 128, generator=g).to(torch.bfloat16)
-    sa, sb = torch.randn(64, 4, generator=g), torch.randn(64, 4, generator=g)
+@pytest.mark.parametrize("dv,alias", [(128, "vs"), (512, "vs"), (96, "vs"), (512, "s"),
+                                      (96, "v")])
+def test_merge_state_in_place(dv, alias):
+    """v_out = v_a and / or s_out = s_a.  A 512-dim row spans two warps and a
+    96-dim row can span two blocks, so the merged s must not be written
+    before every thread of its row has read the inputs."""
+    g = torch.Generator().manual_seed(5 + dv)
+    n = 300
+    va = torch.randn(n, 4, dv, generator=g).to(torch.bfloat16)
+    vb = torch.randn(n, 4, dv, generator=g).to(torch.bfloat16)
+    sa, sb = torch.randn(n, 4, generator=g) * 4, torch.randn(n, 4, generator=g) * 4
+    sa.view(-1)[::13] = float("-inf")
     rv, rs = oracle.merge_state(va, sa, vb, sb)
     a, s_a = va.to(DEV), sa.to(DEV)
-    pkx.merge_state(a, s_a, vb.to(DEV), sb.to(DEV), v_out=a, s_out=s_a)
+    v_out = a if "v" in alias else torch.empty_like(a)
+    s_out = s_a if "s" in alias else torch.empty_like(s_a)
+    pkx.merge_state(a, s_a, vb.to(DEV), sb.to(DEV), v_out=v_out, s_out=s_out)
     torch.cuda.synchronize()
-    assert (a.double().cpu() - rv).abs().max().item() <= 2e-2
-    assert (s_a.double().cpu() - rs).abs().max().item() <= 1e-5
+    err = (v_out.double().cpu() - rv).abs()
+    assert err.max().item() <= 2e-2 and err.mean().item() <= 2e-3
+    assert (s_out.double().cpu() - rs).abs().max().item() <= 1e-5
 
 
 # ------------------------------------------------------------ extend attention
