@@ -1,0 +1,293 @@
+"""A CPU model of the mbarrier protocol inside attn_kernel (csrc/attention.cu),
+run over random unit mixes and random interleavings.  No GPU: each warp role
+is a Python generator of the barrier operations it performs, in its order.
+
+Roles and barriers (as in the kernel):
+- index warp: claims units into the 3-slot unit ring (U_FULL / U_EMPTY),
+  loads each unit's Q (Q_FULL) once the previous unit's products released it
+  (Q_EMPTY), and hands each K/V tile's row indices to the copy warps through
+  the index ring (I_FULL / I_EMPTY);
+- copy warps: fill the K and V stage rings (K_FULL / V_FULL) once the tensor
+  core has released the stage (K_EMPTY / V_EMPTY);
+- MMA thread: S(j) into buffer b (S_FULL(b)), PV after the buffer's P
+  (P_FULL(b)), commits that arrive when its earlier products complete (the
+  model completes them after random delays), O_DONE(b) after a unit's last PV;
+- softmax warpgroups 0 / 1: wait S_FULL(wg), store P (P_FULL(wg)), wait
+  O_DONE(wg) for the epilogue.
+Unit kinds: two query tiles ("dual"), one query tile ("one"), and one query
+tile split with two key streams, tile j into buffer j & 1 ("two").
+
+Checks: every role finishes (no deadlock); every parity wait passes with its
+barrier exactly one phase past what the waiter has consumed, so a parity wait
+never aliases a phase two ahead; and every product reads a K or V stage whose
+fill for that use has completed.  Planted mistakes must be caught.
+"""
+import random
+
+import pytest
+
+NK, NV, NI, RING = 3, 2, 3, 3
+
+
+class _Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.arrivals, self.phase = name, count, 0, 0
+
+    def arrive(self):
+        self.arrivals += 1
+        assert self.arrivals <= self.count, self.name
+        if self.arrivals == self.count:
+            self.arrivals = 0
+            self.phase += 1
+
+
+class _Model:
+    def __init__(self, units, seed, mistake=None):
+        self.rng = random.Random(seed)
+        self.units = units
+        self.mistake = mistake
+        self.ring = [None] * RING
+        self.pending = []  # barriers of the MMA thread's commits, in issue order
+        self.bars = {}
+        for name, count in [("Q_FULL", 1), ("Q_EMPTY", 1)]:
+            self.bars[name] = _Bar(name, count)
+        for b in range(2):
+            for name in ("S", "P", "O"):
+                self.bars[f"{name}{b}"] = _Bar(f"{name}{b}", 1)
+        for s in range(RING):
+            self.bars[f"UF{s}"] = _Bar(f"UF{s}", 1)
+            self.bars[f"UE{s}"] = _Bar(f"UE{s}", 4)  # two warpgroups, MMA, copy
+        for pre, n in (("K", NK), ("V", NV), ("I", NI)):
+            for s in range(n):
+                self.bars[f"{pre}F{s}"] = _Bar(f"{pre}F{s}", 1)
+                self.bars[f"{pre}E{s}"] = _Bar(f"{pre}E{s}", 1)
+
+    def run(self, max_steps=500000):
+        roles = {"index": self._index(), "copy": self._copy(), "wg0": self._softmax(0),
+                 "wg1": self._softmax(1), "mma": self._mma()}
+        cur = {k: next(g) for k, g in roles.items()}
+        done = set()
+        for _ in range(max_steps):
+            if self.pending and self.rng.random() < 0.3:
+                self.bars[self.pending.pop(0)].arrive()  # the oldest product completes
+            ready = [k for k, op in cur.items() if k not in done and
+                     (op[0] != "wait" or (self.bars[op[1]].phase & 1) != op[2])]
+            if not ready:
+                if self.pending:
+                    continue
+                live = [k for k in cur if k not in done]
+                if not live:
+                    return
+                raise AssertionError("deadlock: " + ", ".join(f"{k} {cur[k]}" for k in live))
+            k = self.rng.choice(ready)
+            op = cur[k]
+            if op[0] == "wait":
+                assert self.bars[op[1]].phase == op[3] + 1, f"{k}: {op[1]} aliased"
+            elif op[0] == "use":
+                assert self.bars[op[1]].phase == op[2] + 1, f"{k}: read {op[1]} before its fill"
+            elif op[0] == "arrive":
+                self.bars[op[1]].arrive()
+            elif op[0] == "commit":
+                self.pending.append(op[1])
+            try:
+                cur[k] = next(roles[k])
+            except StopIteration:
+                done.add(k)
+        raise AssertionError("step limit")
+
+    @staticmethod
+    def _wait(bar, consumed):
+        return ("wait", bar, consumed & 1, consumed)
+
+    def _units(self):
+        full = [0] * RING
+        uc = 0
+        while True:
+            s = uc % RING
+            yield self._wait(f"UF{s}", full[s])
+            full[s] += 1
+            u = self.ring[s]
+            yield ("arrive", f"UE{s}")
+            yield ("unit", u)
+            if u is None:
+                return
+            uc += 1
+
+    def _index(self):
+        q_cnt = ic = 0
+        for uc, u in enumerate(self.units + [None]):
+            s = uc % RING
+            if uc >= RING:
+                yield self._wait(f"UE{s}", uc // RING - 1)
+            self.ring[s] = u
+            yield ("arrive", f"UF{s}")
+            if u is None:
+                return
+            if u["nt"] == 0:
+                continue
+            if q_cnt > 0:
+                yield self._wait("Q_EMPTY", q_cnt - 1)
+            yield ("arrive", "Q_FULL")
+            q_cnt += 1
+            for _ in range(u["nt"]):
+                si = ic % NI
+                if ic >= NI:
+                    yield self._wait(f"IE{si}", ic // NI - 1)
+                yield ("arrive", f"IF{si}")
+                ic += 1
+
+    def _copy(self):
+        kc = vc = ic = 0
+        for op in self._units():
+            if op[0] != "unit":
+                yield op
+                continue
+            if op[1] is None:
+                return
+            for _ in range(op[1]["nt"]):
+                si = ic % NI
+                yield self._wait(f"IF{si}", ic // NI)
+                yield ("arrive", f"IE{si}")
+                ic += 1
+                ks, vs = kc % NK, vc % NV
+                if kc >= NK:
+                    yield self._wait(f"KE{ks}", kc // NK - 1)
+                yield ("arrive", f"KF{ks}")
+                kc += 1
+                if vc >= NV and self.mistake != "V refilled before release":
+                    yield self._wait(f"VE{vs}", vc // NV - 1)
+                yield ("arrive", f"VF{vs}")
+                vc += 1
+
+    def _softmax(self, wg):
+        s_cnt = o_cnt = 0
+        for op in self._units():
+            if op[0] != "unit":
+                yield op
+                continue
+            u = op[1]
+            if u is None:
+                return
+            two = u["kind"] == "two"
+            if not two and wg == 1 and u["kind"] == "one":
+                continue  # one query tile: warpgroup 1 has no rows
+            j0, step = (wg, 2) if two else (0, 1)
+            if u["nt"] - j0 <= 0:
+                continue  # no tile of this stream: zero partial, no barrier
+            for _ in range(j0, u["nt"], step):
+                yield self._wait(f"S{wg}", s_cnt)
+                s_cnt += 1
+                yield ("arrive", f"P{wg}")
+            yield self._wait(f"O{wg}", o_cnt)
+            o_cnt += 1
+
+    def _mma(self):
+        q_cnt = kc = vc = 0
+        p = [0, 0]
+        shared_p = self.mistake == "shared P counter"
+
+        def wait_p(b):
+            i = 0 if shared_p else b
+            op = self._wait(f"P{b}", p[i])
+            p[i] += 1
+            return op
+
+        for op in self._units():
+            if op[0] != "unit":
+                yield op
+                continue
+            u = op[1]
+            if u is None:
+                return
+            nt = u["nt"]
+            if nt == 0:
+                continue
+            yield self._wait("Q_FULL", q_cnt)
+            q_cnt += 1
+            if u["kind"] == "two":
+                # S(j) into buffer j & 1 waits only for PV(j - 2)
+                for j in range(nt):
+                    b = j & 1
+                    if j >= 2:
+                        vs = vc % NV
+                        yield self._wait(f"VF{vs}", vc // NV)
+                        yield wait_p(b)
+                        yield ("use", f"VF{vs}", vc // NV)
+                        yield ("commit", f"VE{vs}")
+                        vc += 1
+                    ks = kc % NK
+                    yield self._wait(f"KF{ks}", kc // NK)
+                    yield ("use", f"KF{ks}", kc // NK)
+                    yield ("commit", f"S{b}")
+                    yield ("commit", f"KE{ks}")
+                    kc += 1
+                    if j == nt - 1 and self.mistake != "no Q release":
+                        yield ("commit", "Q_EMPTY")
+                for j in range(max(nt - 2, 0), nt):
+                    vs = vc % NV
+                    yield self._wait(f"VF{vs}", vc // NV)
+                    yield wait_p(j & 1)
+                    yield ("use", f"VF{vs}", vc // NV)
+                    yield ("commit", f"O{j & 1}")
+                    yield ("commit", f"VE{vs}")
+                    vc += 1
+                continue
+            q1 = u["kind"] == "dual"
+            ks = kc % NK
+            yield self._wait(f"KF{ks}", kc // NK)
+            yield ("commit", "S0")
+            if q1:
+                yield ("commit", "S1")
+            yield ("commit", f"KE{ks}")
+            kc += 1
+            if nt == 1:
+                yield ("commit", "Q_EMPTY")
+            for j in range(1, nt):
+                ks, vs = kc % NK, vc % NV
+                yield self._wait(f"KF{ks}", kc // NK)
+                yield self._wait(f"VF{vs}", vc // NV)
+                yield wait_p(0)
+                yield ("use", f"KF{ks}", kc // NK)
+                yield ("use", f"VF{vs}", vc // NV)
+                yield ("commit", "S0")
+                if q1:
+                    yield wait_p(1)
+                    yield ("commit", "S1")
+                yield ("commit", f"VE{vs}")
+                vc += 1
+                yield ("commit", f"KE{ks}")
+                kc += 1
+                if j == nt - 1:
+                    yield ("commit", "Q_EMPTY")
+            vs = vc % NV
+            yield self._wait(f"VF{vs}", vc // NV)
+            yield wait_p(0)
+            yield ("use", f"VF{vs}", vc // NV)
+            yield ("commit", "O0")
+            if q1:
+                yield wait_p(1)
+                yield ("commit", "O1")
+            yield ("commit", f"VE{vs}")
+            vc += 1
+
+
+def _random_units(rng, n):
+    return [{"kind": rng.choice(["dual", "one", "two"]),
+             "nt": rng.choice([0, 1, 1, 2, 3, 4, 5, 7])} for _ in range(n)]
+
+
+def _trials(n, mistake=None):
+    rng = random.Random(1)
+    for t in range(n):
+        _Model(_random_units(rng, rng.randint(1, 12)), seed=t, mistake=mistake).run()
+
+
+def test_protocol_has_no_deadlock_and_no_parity_aliasing():
+    _trials(150)
+
+
+@pytest.mark.parametrize("mistake", ["shared P counter", "no Q release",
+                                     "V refilled before release"])
+def test_model_catches_planted_mistakes(mistake):
+    with pytest.raises(AssertionError):
+        _trials(150, mistake)
