@@ -20,7 +20,8 @@ tile split with two key streams, tile j into buffer j & 1 ("two").
 Checks: every role finishes (no deadlock); every parity wait passes with its
 barrier exactly one phase past what the waiter has consumed, so a parity wait
 never aliases a phase two ahead; and every product reads a K or V stage whose
-fill for that use has completed.  Planted mistakes must be caught.
+fill for that use has completed.  Planted mistakes must be caught.  The same
+model runs the MLA kernel's protocol (csrc/mla_kernel.cuh) at the end.
 """
 import random
 
@@ -62,9 +63,12 @@ class _Model:
                 self.bars[f"{pre}F{s}"] = _Bar(f"{pre}F{s}", 1)
                 self.bars[f"{pre}E{s}"] = _Bar(f"{pre}E{s}", 1)
 
+    def _roles(self):
+        return {"index": self._index(), "copy": self._copy(), "wg0": self._softmax(0),
+                "wg1": self._softmax(1), "mma": self._mma()}
+
     def run(self, max_steps=500000):
-        roles = {"index": self._index(), "copy": self._copy(), "wg0": self._softmax(0),
-                 "wg1": self._softmax(1), "mma": self._mma()}
+        roles = self._roles()
         cur = {k: next(g) for k, g in roles.items()}
         done = set()
         for _ in range(max_steps):
@@ -291,3 +295,148 @@ def test_protocol_has_no_deadlock_and_no_parity_aliasing():
 def test_model_catches_planted_mistakes(mistake):
     with pytest.raises(AssertionError):
         _trials(150, mistake)
+
+
+# ------------------------------------------------------------------ MLA kernel
+class _MlaModel:
+    """The mbarrier protocol of mla_kernel (csrc/mla_kernel.cuh): one K ring
+    (the tile is also V), S released early (S_FREE) so that QK^T of tile j+1
+    runs during the softmax of tile j, P and O reused after each PV (PV_DONE),
+    whose phases the softmax counts across units (pv_base)."""
+    NK, NI = 3, 4
+
+    def __init__(self, units, seed, mistake=None):
+        self.rng = random.Random(seed)
+        self.units, self.mistake = units, mistake
+        self.ring = [None] * RING
+        self.pending = []
+        self.bars = {n: _Bar(n, 1) for n in ("Q_FULL", "S_FULL", "P_FULL", "O_DONE", "S_FREE",
+                                              "PV_DONE")}
+        for s in range(RING):
+            self.bars[f"UF{s}"] = _Bar(f"UF{s}", 1)
+            self.bars[f"UE{s}"] = _Bar(f"UE{s}", 3)  # softmax, MMA, copy
+        for pre, n in (("K", self.NK), ("I", self.NI)):
+            for s in range(n):
+                self.bars[f"{pre}F{s}"] = _Bar(f"{pre}F{s}", 1)
+                self.bars[f"{pre}E{s}"] = _Bar(f"{pre}E{s}", 1)
+
+    run = _Model.run
+    _wait = staticmethod(_Model._wait)
+    _units = _Model._units
+
+    def _roles(self):
+        return {"index": self._index(), "copy": self._copy(), "softmax": self._softmax(),
+                "mma": self._mma()}
+
+    def _index(self):
+        ic = 0
+        for uc, u in enumerate(self.units + [None]):
+            s = uc % RING
+            if uc >= RING:
+                yield self._wait(f"UE{s}", uc // RING - 1)
+            self.ring[s] = u
+            yield ("arrive", f"UF{s}")
+            if u is None:
+                return
+            for _ in range(u["nt"]):
+                si = ic % self.NI
+                if ic >= self.NI:
+                    yield self._wait(f"IE{si}", ic // self.NI - 1)
+                yield ("arrive", f"IF{si}")
+                ic += 1
+
+    def _copy(self):
+        kc = ic = 0
+        for op in self._units():
+            if op[0] != "unit":
+                yield op
+                continue
+            if op[1] is None:
+                return
+            for _ in range(op[1]["nt"]):
+                si = ic % self.NI
+                yield self._wait(f"IF{si}", ic // self.NI)
+                yield ("arrive", f"IE{si}")
+                ic += 1
+                ks = kc % self.NK
+                if kc >= self.NK:
+                    yield self._wait(f"KE{ks}", kc // self.NK - 1)
+                yield ("arrive", f"KF{ks}")
+                kc += 1
+
+    def _softmax(self):
+        s_cnt = o_cnt = pv_base = 0
+        for op in self._units():
+            if op[0] != "unit":
+                yield op
+                continue
+            u = op[1]
+            if u is None:
+                return
+            nt = u["nt"]
+            if nt == 0:
+                continue
+            yield ("arrive", "Q_FULL")  # the unit's Q rows written into TMEM
+            for j in range(nt):
+                yield self._wait("S_FULL", s_cnt)
+                s_cnt += 1
+                yield ("arrive", "S_FREE")
+                if j > 0 and self.mistake != "P written before the previous PV":
+                    yield self._wait("PV_DONE", pv_base + j - 1)
+                yield ("arrive", "P_FULL")
+            yield self._wait("O_DONE", o_cnt)
+            o_cnt += 1
+            if self.mistake != "PV count not carried across units":
+                pv_base += nt
+
+    def _mma(self):
+        q_cnt = kc = s_free = p_cnt = 0
+        for op in self._units():
+            if op[0] != "unit":
+                yield op
+                continue
+            u = op[1]
+            if u is None:
+                return
+            nt = u["nt"]
+            if nt == 0:
+                continue
+            yield self._wait("Q_FULL", q_cnt)
+            q_cnt += 1
+            k0 = kc
+            yield self._wait(f"KF{k0 % self.NK}", k0 // self.NK)
+            yield ("use", f"KF{k0 % self.NK}", k0 // self.NK)
+            yield ("commit", "S_FULL")
+            for j in range(nt):
+                yield self._wait("S_FREE", s_free)
+                s_free += 1
+                if j + 1 < nt:
+                    kn = k0 + j + 1
+                    yield self._wait(f"KF{kn % self.NK}", kn // self.NK)
+                    yield ("use", f"KF{kn % self.NK}", kn // self.NK)
+                    yield ("commit", "S_FULL")
+                yield self._wait("P_FULL", p_cnt)
+                p_cnt += 1
+                yield ("use", f"KF{(k0 + j) % self.NK}", (k0 + j) // self.NK)  # V = the K tile
+                yield ("commit", "PV_DONE")
+                yield ("commit", f"KE{(k0 + j) % self.NK}")
+            kc = k0 + nt
+            yield ("commit", "O_DONE")
+
+
+def _mla_trials(n, mistake=None):
+    rng = random.Random(2)
+    for t in range(n):
+        units = [{"nt": rng.choice([0, 1, 1, 2, 3, 5, 8])} for _ in range(rng.randint(1, 10))]
+        _MlaModel(units, seed=t, mistake=mistake).run()
+
+
+def test_mla_protocol_has_no_deadlock_and_no_parity_aliasing():
+    _mla_trials(150)
+
+
+@pytest.mark.parametrize("mistake", ["P written before the previous PV",
+                                     "PV count not carried across units"])
+def test_mla_model_catches_planted_mistakes(mistake):
+    with pytest.raises(AssertionError):
+        _mla_trials(150, mistake)
