@@ -43,14 +43,16 @@ class _Bar:
 
 
 class _Model:
-    def __init__(self, units, seed, mistake=None):
+    def __init__(self, units, seed, mistake=None, fp8=False, f16_decode=False):
         self.rng = random.Random(seed)
         self.units = units
         self.mistake = mistake
+        self.fp8 = fp8 or f16_decode  # an fp8 pool: codes converted in shared memory
+        self.f16 = f16_decode  # decode over an fp8 pool: the copy warps also convert Q
         self.ring = [None] * RING
         self.pending = []  # barriers of the MMA thread's commits, in issue order
         self.bars = {}
-        for name, count in [("Q_FULL", 1), ("Q_EMPTY", 1)]:
+        for name, count in [("Q_FULL", 1), ("Q_EMPTY", 1), ("Q_CONV", 1)]:
             self.bars[name] = _Bar(name, count)
         for b in range(2):
             for name in ("S", "P", "O"):
@@ -141,6 +143,9 @@ class _Model:
                 ic += 1
 
     def _copy(self):
+        if self.fp8:
+            yield from self._copy_fp8()
+            return
         kc = vc = ic = 0
         for op in self._units():
             if op[0] != "unit":
@@ -161,6 +166,53 @@ class _Model:
                 if vc >= NV and self.mistake != "V refilled before release":
                     yield self._wait(f"VE{vs}", vc // NV - 1)
                 yield ("arrive", f"VF{vs}")
+                vc += 1
+
+    def _copy_fp8(self):
+        """The fp8-pool order: a tile's codes are issued, and converted (then
+        the stage's full barrier) only after the next tile's codes are issued:
+        K(0), V(0), the query rows' conversion, then per tile K(j+1),
+        convert K(j), V(j+1), convert V(j)."""
+        kc = vc = ic = qc = 0
+
+        def fetch():
+            nonlocal ic
+            si = ic % NI
+            yield self._wait(f"IF{si}", ic // NI)
+            yield ("arrive", f"IE{si}")
+            ic += 1
+
+        def issue(pre, cnt, n):  # wait until the stage is free again
+            if cnt >= n:
+                yield self._wait(f"{pre}E{cnt % n}", cnt // n - 1)
+
+        for op in self._units():
+            if op[0] != "unit":
+                yield op
+                continue
+            u = op[1]
+            if u is None:
+                return
+            nt = u["nt"]
+            if nt == 0:
+                continue
+            yield from fetch()
+            yield from issue("K", kc, NK)
+            yield from issue("V", vc, NV)
+            if self.f16:
+                yield self._wait("Q_FULL", qc)
+                qc += 1
+                yield ("arrive", "Q_CONV")
+            for j in range(nt):
+                more = j + 1 < nt
+                if more:
+                    yield from fetch()
+                    yield from issue("K", kc + 1, NK)
+                yield ("arrive", f"KF{kc % NK}")
+                kc += 1
+                if more:
+                    yield from issue("V", vc + 1, NV)
+                yield ("arrive", f"VF{vc % NV}")
                 vc += 1
 
     def _softmax(self, wg):
@@ -206,7 +258,7 @@ class _Model:
             nt = u["nt"]
             if nt == 0:
                 continue
-            yield self._wait("Q_FULL", q_cnt)
+            yield self._wait("Q_CONV" if self.f16 else "Q_FULL", q_cnt)
             q_cnt += 1
             if u["kind"] == "two":
                 # S(j) into buffer j & 1 waits only for PV(j - 2)
@@ -284,6 +336,19 @@ def _trials(n, mistake=None):
     rng = random.Random(1)
     for t in range(n):
         _Model(_random_units(rng, rng.randint(1, 12)), seed=t, mistake=mistake).run()
+
+
+def test_fp8_protocols_have_no_deadlock_and_no_parity_aliasing():
+    """An fp8 pool: extend units of every kind with the fp8 copy order, and
+    decode units (two key streams, or one stream when the workspace holds one
+    partial slot per unit) whose query rows the copy warps convert to f16."""
+    rng = random.Random(3)
+    for t in range(150):
+        _Model(_random_units(rng, rng.randint(1, 12)), seed=t, fp8=True).run()
+    for t in range(150):
+        kind = rng.choice(["two", "one"])
+        units = [{"kind": kind, "nt": rng.choice([0, 1, 2, 3, 6])} for _ in range(rng.randint(1, 10))]
+        _Model(units, seed=t, f16_decode=True).run()
 
 
 def test_protocol_has_no_deadlock_and_no_parity_aliasing():
