@@ -26,6 +26,10 @@
  *    dereferenced: the kernel reads a zero row instead and records
  *    PKX_EDEVICE in the workspace's status word, which
  *    pkx_workspace_status() reads back.
+ *  - Array extents are the caller's: an array described by an indptr (for
+ *    example kv_indices[kv_indptr[b] .. kv_indptr[b+1])) must hold every
+ *    entry the indptr names, as a C array argument must; its length is not
+ *    checked.  Such an array may be NULL only when the indptr names no entry.
  *  - Every wait inside a kernel is bounded (about two seconds); a wait that
  *    runs out records PKX_ETIMEOUT in the same status word and the kernel
  *    returns instead of hanging.
