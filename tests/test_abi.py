@@ -213,3 +213,13 @@ def test_plain_c_consumer(lib, tmp_path):
     cxx.write_text('#include "pkx.h"\nint main() { return pkx_version() == nullptr; }\n')
     subprocess.run(["g++", "-std=c++11", "-Wall", "-Werror", "-pedantic", "-fsyntax-only",
                     "-I", os.path.join(ROOT, "include"), str(cxx)], check=True)
+
+
+def test_header_constants_match_the_binding():
+    """Every status code and pool-format value pkx.h defines has the same
+    value in the Python binding."""
+    text = open(HEADER).read()
+    defs = dict(re.findall(r"#define (PKX_\w+) (\d+)", text))
+    assert {"PKX_OK", "PKX_EINVAL", "PKX_EWORKSPACE", "PKX_KV_BF16", "PKX_KV_FP8_E5M2"} <= set(defs)
+    for name, value in defs.items():
+        assert getattr(pkx, name) == int(value), name
