@@ -223,3 +223,49 @@ def test_header_constants_match_the_binding():
     assert {"PKX_OK", "PKX_EINVAL", "PKX_EWORKSPACE", "PKX_KV_BF16", "PKX_KV_FP8_E5M2"} <= set(defs)
     for name, value in defs.items():
         assert getattr(pkx, name) == int(value), name
+
+
+def _prototypes():
+    """name -> list of parameter C types, from pkx.h (comments removed)."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b(pkx_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = " ".join(m.group(2).split())
+        if params in ("", "void"):
+            protos[m.group(1)] = []
+            continue
+        types = []
+        for p in params.split(","):
+            p = p.strip()
+            # drop the parameter name: the last identifier, unless it is all there is
+            ptype = re.sub(r"\b\w+$", "", p).strip() if re.search(r"[\s*]\w+$", p) else p
+            types.append(ptype)
+        protos[m.group(1)] = types
+    return protos
+
+
+def test_binding_signatures_match_the_header():
+    """The ctypes argument list of every entry point matches its C prototype:
+    the same count, and per position a pointer, a 32-bit int, a 64-bit int,
+    a size_t or a float."""
+    import ctypes
+
+    def kind_c(t):
+        if "*" in t:
+            return "ptr"
+        t = t.replace("const", "").strip()
+        return {"int": "i32", "int64_t": "i64", "size_t": "size", "float": "f32"}[t]
+
+    def kind_py(a):
+        if a in (ctypes.c_void_p, ctypes.c_char_p):
+            return "ptr"
+        if a is ctypes.c_size_t:
+            return "size"
+        return {ctypes.c_int: "i32", ctypes.c_int64: "i64", ctypes.c_float: "f32"}[a]
+
+    protos = _prototypes()
+    assert set(protos) == set(pkx._SIGS)
+    for name, (_, args) in pkx._SIGS.items():
+        c_kinds = [kind_c(t) for t in protos[name]]
+        py_kinds = [kind_py(a) for a in args]
+        assert c_kinds == py_kinds, (name, c_kinds, py_kinds)
