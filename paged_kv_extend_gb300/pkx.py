@@ -105,7 +105,15 @@ def _check(rc: int):
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else t.data_ptr()
+    """Device address of ``t`` for a C entry point (every tensor argument of
+    the library is a device pointer: a host tensor would reach a kernel as a
+    host address, so it is refused here)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device} "
+                         f"(shape {tuple(t.shape)}, {t.dtype})")
+    return t.data_ptr()
 
 
 def _on(dev: torch.device, fn, *args):

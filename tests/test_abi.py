@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from paged_kv_extend_gb300 import build as pkx_build
 from paged_kv_extend_gb300 import pkx
@@ -269,3 +270,15 @@ def test_binding_signatures_match_the_header():
         c_kinds = [kind_c(t) for t in protos[name]]
         py_kinds = [kind_py(a) for a in args]
         assert c_kinds == py_kinds, (name, c_kinds, py_kinds)
+
+
+def test_binding_refuses_host_tensors():
+    """A host tensor among the arguments never reaches the library (it would
+    arrive in a kernel as a host address): the binding raises first."""
+    v = torch.zeros(4, 2, 16, dtype=torch.bfloat16)
+    s = torch.zeros(4, 2, dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA"):
+        pkx.merge_state(v, s, v, s)
+    with pytest.raises(ValueError, match="CUDA"):
+        pkx._ptr(s)
+    assert pkx._ptr(None) is None
