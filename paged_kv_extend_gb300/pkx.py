@@ -208,6 +208,28 @@ def set_attention_events(before=None, after=None):
         None if after is None else after.cuda_event)
 
 
+def _check_attn(q, o, lse, k_buffer, v_buffer, n_q, hq, lq, lv):
+    """Host-side shape checks of an attention call (the C entry points take
+    raw pointers, so an undersized output would be written out of bounds)."""
+    for t, nm in ((q, "q"), (o, "o")):
+        if t.dim() != 3 or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{nm} must be a contiguous bf16 [tokens, heads, dim] tensor")
+    if tuple(o.shape) != (n_q, hq, lv):
+        raise ValueError(f"o has shape {tuple(o.shape)}, expected {(n_q, hq, lv)}")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or
+                            tuple(lse.shape) != (n_q, hq)):
+        raise ValueError(f"lse must be a contiguous float32 [{n_q}, {hq}] tensor")
+    if (k_buffer.dim() != 3 or v_buffer.dim() != 3 or k_buffer.shape[0] != v_buffer.shape[0]
+            or k_buffer.shape[1] != v_buffer.shape[1] or k_buffer.shape[2] != lq):
+        raise ValueError("k_buffer [slots, Hkv, Lq] and v_buffer [slots, Hkv, Lv] disagree "
+                         f"with each other or with q's Lq={lq}")
+
+
+def _check_len(t, n, name):
+    if t.numel() != n:
+        raise ValueError(f"{name} has {t.numel()} entries, expected {n}")
+
+
 def _workspace(ws, nbytes, dev):
     """The caller's workspace (its size is checked by the library), or a new
     one of the size the library asks for."""
@@ -229,6 +251,11 @@ def extend_attention_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buf
     hkv = k_buffer.shape[1]
     lv = v_buffer.shape[2]
     batch = qo_indptr.numel() - 1
+    _check_attn(q_extend, o_extend, lse, k_buffer, v_buffer, n, hq, lq, lv)
+    _check_len(kv_indptr, batch + 1, "kv_indptr")
+    if tuple(k_extend.shape) != (n, hkv, lq) or tuple(v_extend.shape) != (n, hkv, lv):
+        raise ValueError("k_extend / v_extend must be [tokens, Hkv, Lq] / [tokens, Hkv, Lv] "
+                         "with q's token count")
     ke = _rows(k_extend, "k_extend")
     ve = _rows(v_extend, "v_extend")
     kb, vb, kv_dtype = _pool_rows(k_buffer, v_buffer)
@@ -267,6 +294,11 @@ def extend_attention_fwd_ragged_paged(q_extend, k_extend, v_extend, o_extend, k_
     hkv = k_buffer.shape[1]
     lv = v_buffer.shape[2]
     batch = qo_indptr.numel() - 1
+    _check_attn(q_extend, o_extend, lse, k_buffer, v_buffer, n, hq, lq, lv)
+    _check_len(kv_indptr, batch + 1, "kv_indptr")
+    if tuple(k_extend.shape) != (n, hkv, lq) or tuple(v_extend.shape) != (n, hkv, lv):
+        raise ValueError("k_extend / v_extend must be [tokens, Hkv, Lq] / [tokens, Hkv, Lv] "
+                         "with q's token count")
     ke = _rows(k_extend, "k_extend")
     ve = _rows(v_extend, "v_extend")
     kb, vb, kv_dtype = _pool_rows(k_buffer, v_buffer)
@@ -299,6 +331,9 @@ def extend_attention_fwd_unified(q, o, k_buffer, v_buffer, qo_indptr, kv_indptr,
     hkv = k_buffer.shape[1]
     lv = v_buffer.shape[2]
     batch = qo_indptr.numel() - 1
+    _check_attn(q, o, lse, k_buffer, v_buffer, n, hq, lq, lv)
+    _check_len(kv_indptr, batch + 1, "kv_indptr")
+    _check_len(prefix_lens, batch, "prefix_lens")
     kb, vb, kv_dtype = _pool_rows(k_buffer, v_buffer)
     if kv_indices.dtype != torch.int64 or not kv_indices.is_contiguous():
         raise ValueError("kv_indices must be contiguous int64")
@@ -327,6 +362,8 @@ def decode_attention_fwd(q, o, k_buffer, v_buffer, kv_indptr, kv_indices, sm_sca
     b, hq, lq = q.shape
     hkv = k_buffer.shape[1]
     lv = v_buffer.shape[2]
+    _check_attn(q, o, lse, k_buffer, v_buffer, b, hq, lq, lv)
+    _check_len(kv_indptr, b + 1, "kv_indptr")
     kb, vb, kv_dtype = _pool_rows(k_buffer, v_buffer)
     _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
     ws = _workspace(workspace, decode_workspace_size(b, hq, hkv, lq, lv), q.device)
@@ -350,6 +387,8 @@ def decode_attention_fwd_no_alloc(q, o, k_buffer, v_buffer, kv_indptr, kv_indice
     b, hq, lq = q.shape
     hkv = k_buffer.shape[1]
     lv = v_buffer.shape[2]
+    _check_attn(q, o, lse, k_buffer, v_buffer, b, hq, lq, lv)
+    _check_len(kv_indptr, b + 1, "kv_indptr")
     kb = _rows(k_buffer, "k_buffer")
     vb = _rows(v_buffer, "v_buffer")
     _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
@@ -370,11 +409,11 @@ def merge_state(v_a, s_a, v_b, s_b, v_out=None, s_out=None):
     if s_out is None:
         s_out = torch.empty_like(s_a)
     for t in (v_a, v_b, v_out):
-        if t.dtype != torch.bfloat16 or not t.is_contiguous():
-            raise ValueError("v tensors must be contiguous bf16")
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != v_a.shape:
+            raise ValueError("v tensors must be contiguous bf16 of v_a's shape")
     for t in (s_a, s_b, s_out):
-        if t.dtype != torch.float32 or not t.is_contiguous():
-            raise ValueError("s tensors must be contiguous fp32")
+        if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != (n, h):
+            raise ValueError(f"s tensors must be contiguous fp32 [{n}, {h}]")
     _check(_on(v_a.device, lib.pkx_merge_state, _ptr(v_a), _ptr(s_a), _ptr(v_b), _ptr(s_b),
                _ptr(v_out), _ptr(s_out), n, h, dv))
     return v_out, s_out

@@ -282,3 +282,32 @@ def test_binding_refuses_host_tensors():
     with pytest.raises(ValueError, match="CUDA"):
         pkx._ptr(s)
     assert pkx._ptr(None) is None
+
+
+def test_binding_checks_shapes_before_the_call():
+    """An output smaller than the problem, or index arrays of the wrong
+    length, are refused in the binding (the C entry points take raw
+    pointers and would write out of bounds).  Host tensors are enough here:
+    the shape checks come before any pointer is taken."""
+    bf = torch.bfloat16
+    q = torch.zeros(5, 8, 128, dtype=bf)
+    kb = torch.zeros(64, 2, 128, dtype=bf)
+    kvp = torch.zeros(3, dtype=torch.int32)
+    kvi = torch.zeros(0, dtype=torch.int32)
+    with pytest.raises(ValueError, match="o has shape"):
+        pkx.decode_attention_fwd(q, torch.zeros(5, 8, 64, dtype=bf), kb, kb, kvp, kvi)
+    with pytest.raises(ValueError, match="lse"):
+        pkx.decode_attention_fwd(q, torch.zeros_like(q), kb, kb, kvp, kvi,
+                                 lse=torch.zeros(5, 4))
+    with pytest.raises(ValueError, match="kv_indptr has 3 entries, expected 6"):
+        pkx.decode_attention_fwd(q, torch.zeros_like(q), kb, kb, kvp, kvi)
+    with pytest.raises(ValueError, match="disagree"):
+        pkx.decode_attention_fwd(q, torch.zeros_like(q), kb, torch.zeros(32, 2, 128, dtype=bf),
+                                 torch.zeros(6, dtype=torch.int32), kvi)
+    with pytest.raises(ValueError, match="k_extend"):
+        pkx.extend_attention_fwd(q, torch.zeros(4, 2, 128, dtype=bf), torch.zeros(5, 2, 128, dtype=bf),
+                                 torch.zeros_like(q), kb, kb, torch.zeros(2, dtype=torch.int32),
+                                 torch.zeros(2, dtype=torch.int32), kvi)
+    v = torch.zeros(4, 2, 16, dtype=bf)
+    with pytest.raises(ValueError, match="v_a's shape"):
+        pkx.merge_state(v, torch.zeros(4, 2), torch.zeros(4, 2, 8, dtype=bf), torch.zeros(4, 2))
