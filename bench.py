@@ -138,6 +138,21 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    @staticmethod
+    def smi_id(gpu_index: int) -> str:
+        """nvidia-smi's name for CUDA device ``gpu_index``: its UUID when
+        nvidia-smi lists it (nvidia-smi ignores CUDA_VISIBLE_DEVICES, so the
+        CUDA index can name another GPU), else the index itself."""
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(gpu_index).uuid)
+            listed = subprocess.run(["nvidia-smi", "--query-gpu=uuid", "--format=csv,noheader"],
+                                    capture_output=True, text=True, timeout=20).stdout.split()
+            if uuid in listed:
+                return uuid
+        except Exception:
+            pass
+        return str(gpu_index)
+
     def __init__(self, gpu_index: int):
         self.samples = []
         self.window = None
@@ -145,7 +160,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "20", "-i", str(gpu_index)],
+                 "-lms", "20", "-i", self.smi_id(gpu_index)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
