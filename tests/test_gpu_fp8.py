@@ -153,6 +153,41 @@ def test_full_size_decode_over_fp8_pool():
     assert_close(o, lse, ro, rl, "decode_gqa fp8")
 
 
+@pytest.mark.parametrize("name", ["llama3_8b", "long_prefix"])
+def test_full_size_unified_extend_over_fp8_pool(name):
+    """The benchmarked unified step over an e4m3 pool (k_scale = v_scale =
+    0.5, as bench.py's fp8 components): GPU-built unified indices, then the
+    unified call; a seeded sample of 3072 rows against the oracle reading the
+    same codes through its own unified indices."""
+    wl = W.draw(W.SPECS[name])
+    s = wl.spec
+    ks = vs = 0.5
+    kb, vb = wl.pool_fp8(torch.float8_e4m3fn, ks, vs)
+    uptr, uidx, plen = pkx.build_unified_kv_indices(
+        wl.kv_indptr.to(DEV), wl.kv_indices.to(DEV), wl.extend_start_loc.to(DEV),
+        wl.extend_seq_lens.to(DEV), wl.extend_kv_indices.to(DEV), wl.batch)
+    rptr, ridx, rplen = oracle.build_unified_kv_indices(
+        wl.kv_indptr, wl.kv_indices, wl.extend_start_loc, wl.extend_seq_lens,
+        wl.extend_kv_indices, wl.batch)
+    n = wl.n_q_tokens
+    o = torch.full((n, s.hq, s.lv), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((n, s.hq), float("nan"), dtype=torch.float32, device=DEV)
+    ws = pkx.extend_attention_fwd_unified(wl.q.to(DEV), o, kb.to(DEV), vb.to(DEV),
+                                          wl.qo_indptr.to(DEV), uptr, uidx, plen, wl.sm_scale,
+                                          s.logit_cap, s.sliding_window, lse=lse, k_scale=ks,
+                                          v_scale=vs)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    rows = sample_rows(n, s.hq, 3072, seed=80)
+    ro, rl = oracle.extend_attention_unified(wl.q, kb, vb, wl.qo_indptr, rptr, ridx, rplen,
+                                             wl.sm_scale, s.logit_cap, s.sliding_window,
+                                             rows=rows, k_scale=ks, v_scale=vs)
+    go = o.view(-1, s.lv)[rows.to(DEV)]
+    gl = lse.view(-1)[rows.to(DEV)]
+    assert_close(go, gl, ro, rl, f"{name} unified fp8")
+    assert torch.isfinite(o.float()).all()
+
+
 def test_fp8_write_then_decode_chain():
     """The decode step's own chain on the GPU: the new tokens' K/V written
     into an e5m2 pool by the fp8 KV write, then decode; against the oracle's

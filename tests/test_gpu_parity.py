@@ -427,8 +427,9 @@ def test_workspace_too_small_is_rejected():
 # ------------------------------------------------- full-size sampled parity
 @pytest.mark.parametrize("name", ["llama3_8b", "long_prefix", "heavy_tail"])
 def test_full_size_sampled_rows(name):
-    """The full-size workloads, in the launch configuration the benchmark
-    times; the oracle computes a seeded sample of (token, head) rows."""
+    """The full-size workloads through the two-stage call (prefix from the
+    pool, extend rows from k_extend / v_extend); the oracle computes a
+    seeded sample of (token, head) rows."""
     wl = W.draw(W.SPECS[name])
     dw = DeviceWorkload(wl)
     o, lse, ws = dw.extend()
@@ -440,6 +441,47 @@ def test_full_size_sampled_rows(name):
     go = o.view(-1, o.shape[-1])[rows.to(DEV)]
     gl = lse.view(-1)[rows.to(DEV)]
     assert_close(go, gl, ro, rl, name)
+    assert torch.isfinite(o.float()).all()
+    del dw
+
+
+def _unified_oracle_indices(wl):
+    return oracle.build_unified_kv_indices(wl.kv_indptr, wl.kv_indices, wl.extend_start_loc,
+                                           wl.extend_seq_lens, wl.extend_kv_indices, wl.batch)
+
+
+@pytest.mark.parametrize("name", ["llama3_8b", "heavy_tail", "long_prefix", "mla"])
+def test_full_size_unified_sampled_rows(name):
+    """The benchmarked step itself: build_unified_kv_indices on the GPU, then
+    extend_attention_fwd_unified over every key of the pool, at full size
+    and in the launch configuration bench.py times.  The GPU-built indices
+    are compared bit for bit with the oracle's; the oracle's unified
+    attention (over its own indices) computes a seeded sample of 3072
+    (token, head) rows."""
+    wl = W.draw(W.SPECS[name])
+    dw = DeviceWorkload(wl)
+    uptr, uidx, plen = pkx.build_unified_kv_indices(
+        dw.kv_indptr, dw.kv_indices, dw.extend_start_loc, dw.extend_seq_lens,
+        dw.extend_kv_indices, wl.batch)
+    rptr, ridx, rplen = _unified_oracle_indices(wl)
+    n_u = int(rptr[-1])
+    assert torch.equal(uptr.cpu(), rptr) and torch.equal(plen.cpu(), rplen)
+    assert torch.equal(uidx.cpu()[:n_u], ridx[:n_u])
+    s = wl.spec
+    o, lse = dw.out()
+    ws = pkx.extend_attention_fwd_unified(dw.q, o, dw.k_buffer, dw.v_buffer, dw.qo_indptr, uptr,
+                                          uidx, plen, wl.sm_scale, s.logit_cap, s.sliding_window,
+                                          lse=lse)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    rows = sample_rows(wl.n_q_tokens, s.hq, 3072, seed=79)
+    kb, vb = wl.pool()
+    ro, rl = oracle.extend_attention_unified(wl.q, kb, vb, wl.qo_indptr, rptr, ridx, rplen,
+                                             wl.sm_scale, s.logit_cap, s.sliding_window,
+                                             rows=rows)
+    go = o.view(-1, o.shape[-1])[rows.to(DEV)]
+    gl = lse.view(-1)[rows.to(DEV)]
+    assert_close(go, gl, ro, rl, f"{name} unified")
     assert torch.isfinite(o.float()).all()
     del dw
 
