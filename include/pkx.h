@@ -118,6 +118,27 @@ int pkx_workspace_status(const void *workspace, void *stream);
 void pkx_set_attention_events(void *before, void *after);
 
 /*
+ * Time limit of every bounded wait inside the attention kernels launched
+ * later on this thread, in nanoseconds (0 restores the default of two
+ * seconds).  A wait that runs out records PKX_ETIMEOUT in the status word,
+ * raises the CTA's abort flag, lets the tensor core and its own copies
+ * finish, frees its tensor memory and returns; the call's outputs are then
+ * undefined but the context stays usable.  This serves the library's own
+ * failure handling (no device wait may hang); the pages have no
+ * counterpart.
+ */
+void pkx_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test hook for the timeout path above: when `on` is non-zero, the softmax
+ * warps of every attention kernel launched later on this thread first wait
+ * on a barrier no thread arrives at, so that their bounded wait runs out and
+ * the call reports PKX_ETIMEOUT.  Pass 0 to stop.  Not for production use;
+ * the pages have no counterpart.
+ */
+void pkx_set_stall_injection(int on);
+
+/*
  * Extend attention, two-stage form.
  * Source: sglang extend_attention.py (diff 0.5.3rc2 -> 0.5.4.post1),
  * extend_attention_fwd and its _fwd_kernel (prefix K/V read from the pool
@@ -261,13 +282,18 @@ int pkx_decode_attention_fwd(
  * that must not call cudaMalloc (which synchronises the device).  The pages
  * have no counterpart to this call; it is this library's own addition.
  * Same arguments and results as pkx_decode_attention_fwd minus
- * workspace/workspace_bytes and the pool format (a bf16 pool).  Its scratch is a fixed 96 MiB device array
- * inside the library that every GPU loading the library holds until exit.
- * The first call on each device looks up that array's address (make it
- * before any stream capture).  Calls share the array: calls that overlap on
- * the GPU race and must be serialised.  A problem whose scratch
- * (pkx_decode_workspace_size) exceeds 96 MiB returns PKX_EWORKSPACE before
- * anything is enqueued.  Nothing is allocated.
+ * workspace/workspace_bytes and the pool format (a bf16 pool).  Its scratch
+ * is a fixed 96 MiB device array inside the library that every GPU loading
+ * the library holds until exit.  The first call on each device looks up
+ * that array's address (make it before any stream capture); the address
+ * stays cached for the process, so after cudaDeviceReset this call must not
+ * be used again.  Calls share the array: calls that overlap on the GPU race
+ * and must be serialised.  A problem whose smallest decode scratch
+ * (pkx_decode_workspace_min_size) exceeds 96 MiB returns PKX_EWORKSPACE
+ * before anything is enqueued; when pkx_decode_workspace_size also fits,
+ * the call runs the two-key-stream schedule, otherwise one stream per unit
+ * (same results).  Nothing is allocated.  Device-side errors go to the
+ * array's status word, read by pkx_decode_no_alloc_status.
  */
 int pkx_decode_attention_fwd_no_alloc(
     const void *q, void *o, const void *k_buffer, const void *v_buffer,
@@ -275,6 +301,16 @@ int pkx_decode_attention_fwd_no_alloc(
     int hkv, int lq, int lv, int64_t kb_ss, int64_t kb_sh, int64_t vb_ss,
     int64_t vb_sh, int64_t num_slots, float sm_scale, float logit_cap,
     int sliding_window, float *lse_out, void *stream);
+
+/*
+ * Device status word of the last pkx_decode_attention_fwd_no_alloc call on
+ * the current device, as pkx_workspace_status reads a workspace's: copies it
+ * to the host (synchronising `stream`) and returns PKX_OK, PKX_EDEVICE or
+ * PKX_ETIMEOUT; PKX_ECUDA if the copy fails.  PKX_OK when no such call has
+ * run on the device.  Like the entry point it serves, it has no counterpart
+ * on the pages.
+ */
+int pkx_decode_no_alloc_status(void *stream);
 
 /*
  * merge_state.

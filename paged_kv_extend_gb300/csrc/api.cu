@@ -13,10 +13,17 @@ namespace pkx {
 
 static thread_local char g_err[512] = "";
 static thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+static thread_local uint64_t g_wait_ns = 0;
+static thread_local int g_stall = 0;
 
 void attention_events(cudaEvent_t *before, cudaEvent_t *after) {
   *before = g_ev_before;
   *after = g_ev_after;
+}
+
+void wait_settings(uint64_t *wait_ns, int *stall) {
+  *wait_ns = g_wait_ns ? g_wait_ns : 2000000000ull;
+  *stall = g_stall;
 }
 
 int set_error(int code, const char *fmt, ...) {
@@ -92,6 +99,10 @@ void pkx_set_attention_events(void *before, void *after) {
   g_ev_before = static_cast<cudaEvent_t>(before);
   g_ev_after = static_cast<cudaEvent_t>(after);
 }
+
+void pkx_set_wait_limit_ns(uint64_t ns) { g_wait_ns = ns; }
+
+void pkx_set_stall_injection(int on) { g_stall = on ? 1 : 0; }
 
 size_t pkx_extend_workspace_size(int batch, int num_q_tokens, int hq, int hkv, int lq, int lv) {
   if (batch < 0 || num_q_tokens < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM ||

@@ -429,6 +429,9 @@ struct KParams {
   int32_t *next_unit;     // claim counter over uorder (zeroed by the scheduler)
   int32_t *status;
   float *plse, *po;
+  uint64_t wait_ns;       // time limit of every bounded wait
+  int stall;              // test hook: the softmax warps first wait on a barrier
+                          // no thread arrives at, so that the limit runs out
 };
 
 // TMA descriptor of q (3-D: dim, head, token).
@@ -451,7 +454,7 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NK * K_BYTES;
   static constexpr int OFF_I = OFF_V + NV * V_BYTES;
   static constexpr int OFF_BAR = OFF_I + NI * I_BYTES;
-  static constexpr int N_BARS = 16 + 2 * NK + 2 * NV + 2 * NI;
+  static constexpr int N_BARS = 17 + 2 * NK + 2 * NV + 2 * NI;
   static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 1024;  // + alignment slack
   static constexpr int TMEM_COLS = 512;  // S0 | S1 | O0 | O1, 128 columns each
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
@@ -481,7 +484,8 @@ enum {
   B_U_FULL = 9,    // + unit ring slot (kUnitRing)
   B_U_EMPTY = 12,  // + unit ring slot
   B_Q_CONV = 15,   // decode over fp8: the query rows converted to f16
-  B_RING = 16,  // K full[NK], K empty[NK], V full[NV], V empty[NV],
+  B_NEVER = 16,    // no thread ever arrives (the stall hook waits on it)
+  B_RING = 17,  // K full[NK], K empty[NK], V full[NV], V empty[NV],
                 // I full[NI], I empty[NI]
 };
 
@@ -515,9 +519,10 @@ constexpr int kUnitRing = 3;
 // read: by every lane of a warp (lane 0 arrives) or by a lone thread.
 __device__ __forceinline__ int ring_unit(uint64_t *u_full, uint64_t *u_empty,
                                          const volatile int *ring, uint32_t uc,
-                                         volatile int *abort_flag, bool whole_warp, bool &ok) {
+                                         volatile int *abort_flag, bool whole_warp, bool &ok,
+                                         uint64_t limit_ns) {
   const int slot = uc % kUnitRing;
-  if (!mbar_wait(&u_full[slot], (uc / kUnitRing) & 1u, abort_flag)) {
+  if (!mbar_wait(&u_full[slot], (uc / kUnitRing) & 1u, abort_flag, limit_ns)) {
     ok = false;
     return -1;
   }
@@ -633,6 +638,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       mbar_init(&bars[B_O_DONE + i], 1);
     }
     mbar_init(&bars[B_FINAL], 1);
+    mbar_init(&bars[B_NEVER], 1);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(&bars[B_U_FULL + i], 1);
       mbar_init(&bars[B_U_EMPTY + i], 8 + 1 + C::COPY_THREADS / 32);
@@ -678,8 +684,12 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     const uint32_t o_col = 2 * C::BN + wg * C::HDV;
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ring_ok = true;
+    // test hook: a wait that cannot succeed, so that the time limit runs out
+    // and the abort path (flag, drain, TMEM release, return) runs
+    if (p.stall && !mbar_wait(&bars[B_NEVER], 0, abort_flag, p.wait_ns))
+      abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
     for (uint32_t uc = 0; !*abort_flag; ++uc) {
-      const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ring_ok);
+      const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ring_ok, p.wait_ns);
       if (u < 0) {
         if (!ring_ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
         break;
@@ -771,7 +781,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             }
           }
         }
-        if (!mbar_wait(&bars[B_S_FULL + wg], s_cnt & 1u, abort_flag)) {
+        if (!mbar_wait(&bars[B_S_FULL + wg], s_cnt & 1u, abort_flag, p.wait_ns)) {
           abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
           break;
         }
@@ -929,7 +939,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       }
       if (*abort_flag) break;
       // epilogue: wait for the last PV of this tile, normalise, store
-      if (!mbar_wait(&bars[B_O_DONE + wg], o_cnt & 1u, abort_flag)) {
+      if (!mbar_wait(&bars[B_O_DONE + wg], o_cnt & 1u, abort_flag, p.wait_ns)) {
         abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
         break;
       }
@@ -1032,13 +1042,13 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         });
       };
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-        const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, false, ok);
+        const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, false, ok, p.wait_ns);
         if (u < 0) break;
         const WorkUnit w = p.units[p.uorder[u]];
         const int nt = w.n_tiles;
         if (nt == 0) continue;
         const bool q1 = w.n_tok > TOK;
-        if (!mbar_wait(&bars[F16 ? B_Q_CONV : B_Q_FULL], q_cnt & 1u, abort_flag)) {
+        if (!mbar_wait(&bars[F16 ? B_Q_CONV : B_Q_FULL], q_cnt & 1u, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -1055,8 +1065,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             if (j >= 2) {
               const int vs = vc % C::NV;
               uint32_t &pc = b ? p_cnt1 : p_cnt0;
-              if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag) ||
-                  !mbar_wait(&bars[B_P_FULL + b], pc & 1u, abort_flag)) {
+              if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag, p.wait_ns) ||
+                  !mbar_wait(&bars[B_P_FULL + b], pc & 1u, abort_flag, p.wait_ns)) {
                 ok = false;
                 break;
               }
@@ -1068,7 +1078,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
               ++vc;
             }
             const int ks = kc % C::NK;
-            if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
             fence_proxy_async_smem();
             tc_fence_after();
             issue_s_q0(b, sbase + C::OFF_K + ks * C::K_BYTES);
@@ -1081,8 +1091,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             const int b = j & 1;
             const int vs = vc % C::NV;
             uint32_t &pc = b ? p_cnt1 : p_cnt0;
-            if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag) ||
-                !mbar_wait(&bars[B_P_FULL + b], pc & 1u, abort_flag)) {
+            if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag, p.wait_ns) ||
+                !mbar_wait(&bars[B_P_FULL + b], pc & 1u, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -1099,7 +1109,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         // tile 0: S of both Q tiles
         {
           const int ks = kc % C::NK;
-          if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.mma reads
           tc_fence_after();
           const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
@@ -1111,9 +1121,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         }
         for (int j = 1; j < nt && ok; ++j) {
           const int ks = kc % C::NK, vs = vc % C::NV;
-          if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(&bars[B_P_FULL + 0], p_cnt0 & 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&bars[B_P_FULL + 0], p_cnt0 & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           ++p_cnt0;
           fence_proxy_async_smem();
           tc_fence_after();
@@ -1122,7 +1132,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           issue_pv(0, sV, j > 1);
           issue_s(0, sK);
           if (q1) {
-            if (!mbar_wait(&bars[B_P_FULL + 1], p_cnt1 & 1u, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(&bars[B_P_FULL + 1], p_cnt1 & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
             ++p_cnt1;
             tc_fence_after();
             issue_pv(1, sV, j > 1);
@@ -1138,8 +1148,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         // last PV of both Q tiles
         {
           const int vs = vc % C::NV;
-          if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(&bars[B_P_FULL + 0], p_cnt0 & 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&bars[B_P_FULL + 0], p_cnt0 & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           ++p_cnt0;
           fence_proxy_async_smem();
           tc_fence_after();
@@ -1147,7 +1157,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           issue_pv(0, sV, nt > 1);
           tc_commit(&bars[B_O_DONE + 0]);
           if (q1) {
-            if (!mbar_wait(&bars[B_P_FULL + 1], p_cnt1 & 1u, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(&bars[B_P_FULL + 1], p_cnt1 & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
             ++p_cnt1;
             tc_fence_after();
             issue_pv(1, sV, nt > 1);
@@ -1184,7 +1194,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       {
         const int slot = uc % kUnitRing;
         if (uc >= (uint32_t)kUnitRing &&
-            !mbar_wait(&bars[B_U_EMPTY + slot], ((uc / kUnitRing) - 1) & 1u, abort_flag)) {
+            !mbar_wait(&bars[B_U_EMPTY + slot], ((uc / kUnitRing) - 1) & 1u, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -1199,7 +1209,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       if (nt == 0) continue;
       const bool q1 = w.n_tok > TOK;
       if (lane == 0) {
-        if (q_cnt > 0 && !mbar_wait(&bars[B_Q_EMPTY], (q_cnt - 1) & 1u, abort_flag)) ok = false;
+        if (q_cnt > 0 && !mbar_wait(&bars[B_Q_EMPTY], (q_cnt - 1) & 1u, abort_flag, p.wait_ns)) ok = false;
         if (ok) {
           const int nq = q1 ? 2 : 1;
           mbar_arrive_expect_tx(&bars[B_Q_FULL], q_box_bytes * (HD / 64) * nq);
@@ -1242,7 +1252,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         if (bad) record_status(p.status, PKX_EDEVICE);
         const int is = ic % C::NI;
         if (ic >= (uint32_t)C::NI &&
-            !mbar_wait(&i_empty[is], ((ic / C::NI) - 1) & 1u, abort_flag)) {
+            !mbar_wait(&i_empty[is], ((ic / C::NI) - 1) & 1u, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -1261,6 +1271,11 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       }
     }
     if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+    // the last Q load this warp issued lands before the CTA may exit (after
+    // an abort nobody else may have waited for it)
+    if (lane == 0 && q_cnt > 0 && !mbar_wait_drain(&bars[B_Q_FULL], (q_cnt - 1) & 1u))
+      record_status(p.status, PKX_ETIMEOUT);
+    __syncwarp();
   } else if (warp < C::COPY_WARP0 + C::COPY_THREADS / 32) {
     // ------------------------------------------------ K/V copies (4 warps)
     // Thread ct copies 16-byte chunk ch = ct % CPR of keys key0 + KPP * i
@@ -1291,7 +1306,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     bool ok = true;
     if constexpr (FMT == 0) {
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-        const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ok);
+        const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ok, p.wait_ns);
         if (u < 0) break;
         const WorkUnit w = p.units[p.uorder[u]];
         const int nt = w.n_tiles;
@@ -1306,7 +1321,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
           // this thread's rows from the index ring
           const int is = ic % C::NI;
-          if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag)) {
+          if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -1329,7 +1344,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           // K tile
           const int ks = kc % C::NK;
           if (kc >= (uint32_t)C::NK &&
-              !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag)) {
+              !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -1340,7 +1355,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           // V tile
           const int vs = vc % C::NV;
           if (vc >= (uint32_t)C::NV &&
-              !mbar_wait(&v_empty[vs], ((vc / C::NV) - 1) & 1u, abort_flag)) {
+              !mbar_wait(&v_empty[vs], ((vc / C::NV) - 1) & 1u, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -1377,7 +1392,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
     };
     for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-      const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ok);
+      const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ok, p.wait_ns);
       if (u < 0) break;
       const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
@@ -1396,7 +1411,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       };
       auto fetch = [&]() -> bool {
         const int is = ic % C::NI;
-        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag)) return false;
+        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag, p.wait_ns)) return false;
         const int4 *ring =
             reinterpret_cast<const int4 *>(smem + C::OFF_I + is * C::I_BYTES) + key0 * (NKEYS / 4);
 #pragma unroll
@@ -1415,7 +1430,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       auto issue_k = [&](bool from_ext) -> bool {
         const int ks = kc % C::NK;
         if (kc >= (uint32_t)C::NK &&
-            !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag))
+            !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag, p.wait_ns))
           return false;
         const uint32_t stage = sbase + C::OFF_K + ks * C::K_BYTES;
         if (from_ext) {
@@ -1431,7 +1446,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       auto issue_v = [&](bool from_ext) -> bool {
         const int vs = vc % C::NV;
         if (vc >= (uint32_t)C::NV &&
-            !mbar_wait(&v_empty[vs], ((vc / C::NV) - 1) & 1u, abort_flag))
+            !mbar_wait(&v_empty[vs], ((vc / C::NV) - 1) & 1u, abort_flag, p.wait_ns))
           return false;
         const uint32_t stage = sbase + C::OFF_V + vs * C::V_BYTES;
         if (from_ext) {
@@ -1453,7 +1468,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         // the unit's query rows (tokens x G heads of query tile 0) to f16 in
         // place once their load has landed, 16 bytes at a time (the swizzle
         // only permutes whole chunks within a row)
-        if (!mbar_wait(&bars[B_Q_FULL], qc & 1u, abort_flag)) {
+        if (!mbar_wait(&bars[B_Q_FULL], qc & 1u, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -1834,6 +1849,7 @@ int launch_attention(const AttnArgs &a) {
   kp.status = &hdr->status;
   kp.plse = reinterpret_cast<float *>(ws + L.plse_off);
   kp.po = reinterpret_cast<float *>(ws + L.po_off);
+  wait_settings(&kp.wait_ns, &kp.stall);
 
   const int grid = nsm;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;

@@ -26,6 +26,13 @@
 //  * Problems whose scratch would not fit are rejected before anything is
 //    enqueued, with PKX_EWORKSPACE and a message giving both sizes.
 //  * No cudaMalloc, cudaFree or other allocating routine is called.
+//  * Device-side errors (an index outside the pool, a bounded wait that ran
+//    out) land in the status word at the start of the array, as they do in
+//    a caller's workspace; pkx_decode_no_alloc_status reads it back.
+//  * The cached address belongs to the device's primary context.  After
+//    cudaDeviceReset (or anything else that destroys and re-creates that
+//    context) it is stale, and this entry point must not be called again in
+//    the process.
 #include <cstdint>
 #include <mutex>
 
@@ -89,4 +96,23 @@ extern "C" int pkx_decode_attention_fwd_no_alloc(
                                   lq, lv, kb_ss, kb_sh, vb_ss, vb_sh, num_slots, sm_scale,
                                   logit_cap, sliding_window, 0, 1.0f, 1.0f, lse_out, scratch,
                                   kNoAllocScratchBytes, stream);
+}
+
+// The built-in scratch starts with the same header as a caller's workspace,
+// so its status word is read the way pkx_workspace_status reads one.  On a
+// device where no allocation-free call has run yet there is nothing to
+// report.
+extern "C" int pkx_decode_no_alloc_status(void *stream) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(PKX_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return set_error(PKX_EUNSUPPORTED, "device index %d beyond %d", dev, kMaxDevices);
+  void *scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    scratch = g_scratch_ptr[dev];
+  }
+  if (!scratch) return PKX_OK;
+  return pkx_workspace_status(scratch, stream);
 }

@@ -52,6 +52,7 @@ enum {
   M_FINAL = 4,
   M_S_FREE = 5,   // S read into registers: the next QK^T may overwrite it
   M_PV_DONE = 6,  // one phase per PV: P and O are free again
+  M_NEVER = 7,    // no thread ever arrives (the stall hook waits on it)
   M_U_FULL = 8,   // + unit ring slot
   M_U_EMPTY = 11, // + unit ring slot
   M_RING = 16
@@ -87,6 +88,7 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     mbar_init(&bars[M_FINAL], 1);
     mbar_init(&bars[M_S_FREE], 4);  // one arrival per softmax warp
     mbar_init(&bars[M_PV_DONE], 1);
+    mbar_init(&bars[M_NEVER], 1);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(&bars[M_U_FULL + i], 1);
       mbar_init(&bars[M_U_EMPTY + i], 4 + 1 + C::COPY_THREADS / 32);
@@ -124,9 +126,12 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     uint32_t s_cnt = 0, o_cnt = 0;
     uint32_t pv_base = 0;  // PVs of earlier units (M_PV_DONE phases)
     bool ring_ok = true;
+    // test hook: a wait that cannot succeed (see attn_kernel)
+    if (p.stall && !mbar_wait(&bars[M_NEVER], 0, abort_flag, p.wait_ns))
+      abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
     for (uint32_t uc = 0; !*abort_flag; ++uc) {
       const int u = ring_unit(&bars[M_U_FULL], &bars[M_U_EMPTY], s_unit, uc, abort_flag, true,
-                              ring_ok);
+                              ring_ok, p.wait_ns);
       if (u < 0) {
         if (!ring_ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
         break;
@@ -224,7 +229,7 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
             }
           }
         }
-        if (!mbar_wait(&bars[M_S_FULL], s_cnt & 1u, abort_flag)) {
+        if (!mbar_wait(&bars[M_S_FULL], s_cnt & 1u, abort_flag, p.wait_ns)) {
           abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
           break;
         }
@@ -328,7 +333,7 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
         // Every warp waits, also one without rows: S of the next tile can
         // land before this tile's P, and a warp that ran ahead would arrive
         // on P_FULL twice in one phase.
-        if (j > 0 && !mbar_wait(&bars[M_PV_DONE], (pv_base + j - 1) & 1u, abort_flag)) {
+        if (j > 0 && !mbar_wait(&bars[M_PV_DONE], (pv_base + j - 1) & 1u, abort_flag, p.wait_ns)) {
           abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
         }
         tc_fence_after();
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
         if (lane == 0) mbar_arrive(&bars[M_P_FULL]);
       }
       if (*abort_flag) break;
-      if (!mbar_wait(&bars[M_O_DONE], o_cnt & 1u, abort_flag)) {
+      if (!mbar_wait(&bars[M_O_DONE], o_cnt & 1u, abort_flag, p.wait_ns)) {
         abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
         break;
       }
@@ -443,32 +448,32 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
       auto k_tile = [&](uint32_t kpos) { return sbase + C::OFF_K + (kpos % C::NK) * C::K_BYTES; };
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
         const int u = ring_unit(&bars[M_U_FULL], &bars[M_U_EMPTY], s_unit, uc, abort_flag, false,
-                                ok);
+                                ok, p.wait_ns);
         if (u < 0) break;
         const WorkUnit w = p.units[p.uorder[u]];
         const int nt = w.n_tiles;
         if (nt == 0) continue;
-        if (!mbar_wait(&bars[M_Q_FULL], q_cnt & 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&bars[M_Q_FULL], q_cnt & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
         ++q_cnt;
         tc_fence_after();
         const uint32_t k0 = kc;  // ring position of this unit's first K tile
-        if (!mbar_wait(&k_full[k0 % C::NK], (k0 / C::NK) & 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&k_full[k0 % C::NK], (k0 / C::NK) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
         fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.mma reads
         tc_fence_after();
         issue_s(k_tile(k0));
         const uint32_t dv_off = (w.dq * (C::DVS / 64)) * (C::BN * 128);
         for (int j = 0; j < nt; ++j) {
-          if (!mbar_wait(&bars[M_S_FREE], f_cnt & 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&bars[M_S_FREE], f_cnt & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           ++f_cnt;
           tc_fence_after();
           if (j + 1 < nt) {
             const uint32_t kn = k0 + j + 1;
-            if (!mbar_wait(&k_full[kn % C::NK], (kn / C::NK) & 1u, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(&k_full[kn % C::NK], (kn / C::NK) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
             fence_proxy_async_smem();
             tc_fence_after();
             issue_s(k_tile(kn));
           }
-          if (!mbar_wait(&bars[M_P_FULL], p_cnt & 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&bars[M_P_FULL], p_cnt & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           ++p_cnt;
           tc_fence_after();
           issue_pv(k_tile(k0 + j) + dv_off, j > 0);
@@ -497,7 +502,7 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
       {
         const int slot = uc % kUnitRing;
         if (uc >= (uint32_t)kUnitRing &&
-            !mbar_wait(&bars[M_U_EMPTY + slot], ((uc / kUnitRing) - 1) & 1u, abort_flag)) {
+            !mbar_wait(&bars[M_U_EMPTY + slot], ((uc / kUnitRing) - 1) & 1u, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -540,7 +545,7 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
         if (bad) record_status(p.status, PKX_EDEVICE);
         const int is = ic % C::NI;
         if (ic >= (uint32_t)C::NI &&
-            !mbar_wait(&i_empty[is], ((ic / C::NI) - 1) & 1u, abort_flag)) {
+            !mbar_wait(&i_empty[is], ((ic / C::NI) - 1) & 1u, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -576,7 +581,7 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     uint32_t kc = 0, ic = 0;
     bool ok = true;
     for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-      const int u = ring_unit(&bars[M_U_FULL], &bars[M_U_EMPTY], s_unit, uc, abort_flag, true, ok);
+      const int u = ring_unit(&bars[M_U_FULL], &bars[M_U_EMPTY], s_unit, uc, abort_flag, true, ok, p.wait_ns);
       if (u < 0) break;
       const WorkUnit w = p.units[p.uorder[u]];
       const int nt = w.n_tiles;
@@ -588,7 +593,7 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
         tile_keys<C::BN>(w, j, kb, ke);
         const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
         const int is = ic % C::NI;
-        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag)) {
+        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -596,7 +601,7 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
         ++ic;
         const int ks = kc % C::NK;
         if (kc >= (uint32_t)C::NK &&
-            !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag)) {
+            !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }

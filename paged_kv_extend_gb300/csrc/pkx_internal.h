@@ -112,6 +112,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 // Events set by pkx_set_attention_events for this thread (may be null).
 void attention_events(cudaEvent_t *before, cudaEvent_t *after);
+// Wait limit (ns) and stall hook set by pkx_set_wait_limit_ns /
+// pkx_set_stall_injection for this thread.
+void wait_settings(uint64_t *wait_ns, int *stall);
 int tokens_per_block(int group);
 int rows_per_slot(bool decode, int group, bool mla);
 // two_streams: the decode layout with two partial slots per unit (the GQA

@@ -43,26 +43,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Time limit of every device-side wait.  A wait that runs out returns false;
-// the caller records a timeout and winds the kernel down.
+// Default time limit of a device-side wait (the host may set another one
+// per launch).  A wait that runs out returns false; the caller records a
+// timeout and winds the kernel down.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Wait until the barrier's phase with the given parity has completed, or the
-// abort flag is raised, or the time limit passes.  Returns true on success.
+// abort flag is raised, or limit_ns nanoseconds pass.  Returns true on
+// success.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int *abort_flag) {
+                                          volatile int *abort_flag, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
 }
 
-// Bounded wait that ignores any abort flag (used to drain in-flight work).
+// Bounded wait that ignores any abort flag (used to drain in-flight work:
+// the products and copies it waits for were issued from valid operands and
+// finish by themselves, so it keeps the default limit).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
@@ -91,18 +95,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 }
 
 // ---------------------------------------------------------------- TMA
-// Four rows (row0..row3) x one box width of a 2-D tensor map starting at
-// column x, written as four consecutive box rows at dst; completion counted
-// in bytes on `bar`.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int x, int row0,
-                                            int row1, int row2, int row3, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(row0), "r"(row1), "r"(row2), "r"(row3), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // One box of a 3-D tensor map at coordinates (c0, c1, c2).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, uint64_t *bar) {

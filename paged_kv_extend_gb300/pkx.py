@@ -47,6 +47,8 @@ _SIGS = {
     "pkx_decode_workspace_min_size": (_sz, [_i, _i, _i, _i, _i]),
     "pkx_workspace_status": (_i, [_p, _p]),
     "pkx_set_attention_events": (None, [_p, _p]),
+    "pkx_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "pkx_set_stall_injection": (None, [_i]),
     "pkx_extend_attention_fwd": (_i, [
         _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
         _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _p,
@@ -65,6 +67,7 @@ _SIGS = {
     "pkx_decode_attention_fwd_no_alloc": (_i, [
         _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i,
         _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p]),
+    "pkx_decode_no_alloc_status": (_i, [_p]),
     "pkx_merge_state": (_i, [_p, _p, _p, _p, _p, _p, _i64, _i, _i, _p]),
     "pkx_build_unified_kv_indices": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _p, _p]),
     "pkx_set_kv_buffer": (_i, [
@@ -206,6 +209,19 @@ def set_attention_events(before=None, after=None):
     load_library().pkx_set_attention_events(
         None if before is None else before.cuda_event,
         None if after is None else after.cuda_event)
+
+
+def set_wait_limit_ns(ns: int = 0):
+    """Time limit (ns) of the bounded device waits of attention kernels
+    launched later on this thread; 0 restores the default (two seconds)."""
+    load_library().pkx_set_wait_limit_ns(int(ns))
+
+
+def set_stall_injection(on: bool):
+    """Test hook: while on, attention kernels launched on this thread stall
+    their softmax warps on a barrier nothing arrives at, so the bounded wait
+    runs out and the call reports PKX_ETIMEOUT."""
+    load_library().pkx_set_stall_injection(1 if on else 0)
 
 
 def _check_attn(q, o, lse, k_buffer, v_buffer, n_q, hq, lq, lv):
@@ -400,6 +416,15 @@ def decode_attention_fwd_no_alloc(q, o, k_buffer, v_buffer, kv_indptr, kv_indice
         float(logit_cap or 0.0), int(sliding_window), _ptr(lse)))
 
 
+def decode_no_alloc_status(device=None) -> int:
+    """Status word of the last allocation-free decode call on ``device``
+    (default: the current one), read back like workspace_status (synchronises
+    that device's current stream).  Returns the code; does not raise."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    return int(_on(dev, load_library().pkx_decode_no_alloc_status))
+
+
 def merge_state(v_a, s_a, v_b, s_b, v_out=None, s_out=None):
     """merge_state (pkx_merge_state).  Returns (v_out, s_out)."""
     lib = load_library()
@@ -430,13 +455,28 @@ def build_unified_kv_indices(prefix_kv_indptr, prefix_kv_indices, extend_start_l
                   (extend_start_loc, "extend_start_loc"), (extend_seq_lens, "extend_seq_lens"),
                   (extend_kv_indices, "extend_kv_indices")):
         _i32(t, nm)
+    _check_len(prefix_kv_indptr, bs + 1, "prefix_kv_indptr")
+    _check_len(extend_start_loc, bs, "extend_start_loc")
+    _check_len(extend_seq_lens, bs, "extend_seq_lens")
+    n_idx = prefix_kv_indices.numel() + extend_kv_indices.numel()
     if out is None:
         uptr = torch.empty(bs + 1, dtype=torch.int32, device=dev)
-        uidx = torch.empty(prefix_kv_indices.numel() + extend_kv_indices.numel(),
-                           dtype=torch.int64, device=dev)
+        uidx = torch.empty(n_idx, dtype=torch.int64, device=dev)
         plen = torch.empty(bs, dtype=torch.int32, device=dev)
     else:
         uptr, uidx, plen = out
+        _i32(uptr, "unified_kv_indptr"), _i32(plen, "prefix_lens")
+        _check_len(uptr, bs + 1, "unified_kv_indptr")
+        _check_len(plen, bs, "prefix_lens")
+        if uidx.dtype != torch.int64 or not uidx.is_contiguous() or uidx.device != dev:
+            raise ValueError("unified_kv_indices must be a contiguous int64 tensor on "
+                             f"{dev}")
+        if uidx.numel() < n_idx:
+            raise ValueError(f"unified_kv_indices holds {uidx.numel()} entries, fewer than the "
+                             f"{n_idx} prefix + extend indices")
+    for t, nm in ((uptr, "unified_kv_indptr"), (plen, "prefix_lens")):
+        if t.device != dev:
+            raise ValueError(f"{nm} must be on {dev}")
     _check(_on(
         dev, lib.pkx_build_unified_kv_indices,
         _ptr(prefix_kv_indptr), _ptr(prefix_kv_indices) if prefix_kv_indices.numel() else None,

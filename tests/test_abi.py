@@ -255,7 +255,9 @@ def test_binding_signatures_match_the_header():
         if "*" in t:
             return "ptr"
         t = t.replace("const", "").strip()
-        return {"int": "i32", "int64_t": "i64", "size_t": "size", "float": "f32"}[t]
+        # uint64_t and size_t are both 64-bit unsigned here (ctypes has one type)
+        return {"int": "i32", "int64_t": "i64", "size_t": "size", "uint64_t": "size",
+                "float": "f32"}[t]
 
     def kind_py(a):
         if a in (ctypes.c_void_p, ctypes.c_char_p):

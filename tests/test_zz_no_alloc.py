@@ -33,22 +33,54 @@ def _decode_inputs(dev):
     return wl, kb, vb, wl.q.to(dev), wl.kv_indptr.to(dev), wl.kv_indices.to(dev)
 
 
+def _assert_close(o, lse, ref_o, ref_lse):
+    o, lse = o.double().cpu(), lse.double().cpu()
+    ref_o, ref_lse = ref_o.double().cpu(), ref_lse.double().cpu()
+    err = (o - ref_o).abs()
+    assert torch.isfinite(o).all()
+    assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS
+    assert (lse - ref_lse).abs().max().item() <= LSE_ABS
+
+
 def test_no_alloc_decode_matches_workspace_decode_twice():
+    """Two calls in a row (sharing and reusing the scratch) against the
+    workspace call and against the float64 oracle; the status word of the
+    built-in scratch reads clean after each."""
+    import oracle
     dev = torch.device("cuda:0")
     wl, kb, vb, q, kvp, kvi = _decode_inputs(dev)
     s = wl.spec
     o_ref = torch.empty(s.batch, s.hq, s.lv, dtype=torch.bfloat16, device=dev)
     l_ref = torch.empty(s.batch, s.hq, dtype=torch.float32, device=dev)
     pkx.decode_attention_fwd(q, o_ref, kb, vb, kvp, kvi, wl.sm_scale, s.logit_cap, lse=l_ref)
-    for _ in range(2):  # two calls in a row share (and reuse) the scratch
+    ckb, cvb = wl.pool()
+    ro, rl = oracle.decode_attention(wl.q, ckb, cvb, wl.kv_indptr, wl.kv_indices, wl.sm_scale,
+                                     s.logit_cap)
+    for _ in range(2):
         o = torch.full_like(o_ref, float("nan"))
         lse = torch.full_like(l_ref, float("nan"))
         pkx.decode_attention_fwd_no_alloc(q, o, kb, vb, kvp, kvi, wl.sm_scale, s.logit_cap, lse=lse)
         torch.cuda.synchronize()
-        err = (o.float() - o_ref.float()).abs()
-        assert torch.isfinite(o.float()).all()
-        assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS
-        assert (lse - l_ref).abs().max().item() <= LSE_ABS
+        assert pkx.decode_no_alloc_status() == pkx.PKX_OK
+        _assert_close(o, lse, o_ref, l_ref)
+        _assert_close(o, lse, ro, rl)
+
+
+def test_no_alloc_reports_device_status():
+    """An index outside the pool is not read; the call records PKX_EDEVICE in
+    the built-in scratch's status word, which decode_no_alloc_status reads
+    back, and the next good call clears it."""
+    dev = torch.device("cuda:0")
+    wl, kb, vb, q, kvp, kvi = _decode_inputs(dev)
+    s = wl.spec
+    bad = kvi.clone()
+    bad[5] = kb.shape[0] + 77
+    o = torch.empty(s.batch, s.hq, s.lv, dtype=torch.bfloat16, device=dev)
+    pkx.decode_attention_fwd_no_alloc(q, o, kb, vb, kvp, bad, wl.sm_scale, s.logit_cap)
+    assert pkx.decode_no_alloc_status() == pkx.PKX_EDEVICE
+    assert torch.isfinite(o.float()).all()
+    pkx.decode_attention_fwd_no_alloc(q, o, kb, vb, kvp, kvi, wl.sm_scale, s.logit_cap)
+    assert pkx.decode_no_alloc_status() == pkx.PKX_OK
 
 
 def test_no_alloc_rejects_problem_beyond_scratch():
