@@ -369,6 +369,7 @@ class ExtendStep:
         self.mask_indptr = wl.mask_indptr.to(dev) if wl.mask_indptr is not None else None
         self.sinks = wl.sinks.to(dev).float() if wl.sinks is not None else None
         self.launches = 4  # index build, scheduler, attention, combine
+        self.tokens = wl.n_q_tokens  # query (extend) tokens of one step
         self.flops = extend_flops(wl)
         self.bytes = extend_bytes(wl, unified=True, kv_elem_bytes=1 if fp8 is not None else 2)
 
@@ -421,6 +422,7 @@ class DecodeStep:
         self.ws = torch.empty(pkx.decode_workspace_size(s.batch, s.hq, s.hkv, s.lq, s.lv),
                               dtype=torch.uint8, device=dev)
         self.launches = 3  # scheduler, attention, combine
+        self.tokens = s.batch  # one new token per sequence
         self.flops = 2.0 * (s.lq + s.lv) * s.hq * sum(
             min(p + 1, s.sliding_window + 1) if s.sliding_window > 0 else p + 1
             for p in wl.prefix_lens)
@@ -596,6 +598,7 @@ def measure_component(name, dev, flush, steps, hbm_peak, bf16_peak, fp8=None):
     m, a = sum(ms) / len(ms), sum(attn) / len(attn)
     pool = "" if fp8 is None else f" [pool {str(fp8).replace('torch.', '')}, scales {FP8_SCALE}]"
     out = {"workload": f"{name}: {WORKLOAD_TEXT.get(name, '')}{pool}", "ms": m, "attn_kernel_ms": a,
+           "tokens/s": step.tokens / (m * 1e-3),
            "TFLOP/s": step.flops / (m * 1e-3) / 1e12,
            "attn_kernel_TFLOP/s": step.flops / (a * 1e-3) / 1e12,
            "GB/s": step.bytes / (m * 1e-3) / 1e9,
@@ -778,7 +781,8 @@ def run_ours(args, ws, rank, local):
     components = {"attn_kernel_share_of_step": attn_avg / ms}
     if not args.no_components:
         names = (args.components.split(",") if args.components
-                 else ["decode_gqa", "mla", "kv_ops", "split", "decode_gqa_fp8"])
+                 else ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla",
+                       "kv_ops", "split", "decode_gqa_fp8", "llama3_8b_fp8"])
         if args.all_workloads:
             names = ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla", "kv_ops",
                      "split", "decode_gqa_fp8", "long_prefix_fp8", "llama3_8b_fp8"]
@@ -859,6 +863,7 @@ def run_ours(args, ws, rank, local):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e_entry(e2e_value, e2e_serial, unit, h2d, d2h),
+        "tokens_per_s": step.tokens * ws / (ms_max * 1e-3),
         "gpu_launches": step.launches * args.steps,
         "clocks": clock_info,
         "components": components,
