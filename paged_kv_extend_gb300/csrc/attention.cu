@@ -999,8 +999,13 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
   } else {
   regs_decrease<C::REGS_OTHER>();
   if (warp == 8) {
-    // ------------------------------------------------ MMA issue (one thread)
-    if (lane == 0) {
+    // ------------------------------------------------ MMA issue (one warp)
+    // All 32 lanes run the loop (and its waits), so the descriptors and
+    // counters stay warp-uniform; one elected lane issues each tcgen05
+    // operation.  The same loop run by lane 0 alone issued about 25 %
+    // slower.
+    {
+      const bool leader = elect_one();
       uint32_t q_cnt = 0, kc = 0, vc = 0, p_cnt0 = 0, p_cnt1 = 0;
       const uint32_t sQ0 = sbase + C::OFF_Q, sQ1 = sQ0 + C::Q_BYTES;
       bool ok = true;
@@ -1016,9 +1021,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           constexpr int kk = decltype(kk_c)::value;
           constexpr uint32_t ao = ((kk / 4) * (C::BM * 128) + (kk % 4) * 32) / 16;
           constexpr uint32_t bo = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) / 16;
-          tc_mma_ss_step<ao, bo>(d, a_lo, b_lo, K_HI, IDQK, kk > 0 ? 1u : 0u);
+          if (leader) tc_mma_ss_step<ao, bo>(d, a_lo, b_lo, K_HI, IDQK, kk > 0 ? 1u : 0u);
         });
-        tc_commit(&bars[B_S_FULL + qt]);
+        if (leader) tc_commit(&bars[B_S_FULL + qt]);
       };
       // S of query tile 0 into S/P buffer `buf` (the decode streams)
       auto issue_s_q0 = [&](int buf, uint32_t sK) {
@@ -1028,9 +1033,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           constexpr int kk = decltype(kk_c)::value;
           constexpr uint32_t ao = ((kk / 4) * (C::BM * 128) + (kk % 4) * 32) / 16;
           constexpr uint32_t bo = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) / 16;
-          tc_mma_ss_step<ao, bo>(d, a_lo, b_lo, K_HI, IDQK, kk > 0 ? 1u : 0u);
+          if (leader) tc_mma_ss_step<ao, bo>(d, a_lo, b_lo, K_HI, IDQK, kk > 0 ? 1u : 0u);
         });
-        tc_commit(&bars[B_S_FULL + buf]);
+        if (leader) tc_commit(&bars[B_S_FULL + buf]);
       };
       auto issue_pv = [&](int qt, uint32_t sV, bool acc_first) {
         const uint32_t b_lo = V_LO | (sV >> 4);
@@ -1038,11 +1043,11 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         const uint32_t acc0 = acc_first ? 1u : 0u;
         static_for<0, C::BN / 16>([&](auto kk_c) {
           constexpr int kk = decltype(kk_c)::value;
-          tc_mma_ts_step<kk * 8, kk * 128>(d, a, b_lo, V_HI, IDPV, kk > 0 ? 1u : acc0);
+          if (leader) tc_mma_ts_step<kk * 8, kk * 128>(d, a, b_lo, V_HI, IDPV, kk > 0 ? 1u : acc0);
         });
       };
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-        const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, false, ok, p.wait_ns);
+        const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ok, p.wait_ns);
         if (u < 0) break;
         const WorkUnit w = p.units[p.uorder[u]];
         const int nt = w.n_tiles;
@@ -1074,7 +1079,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
               fence_proxy_async_smem();
               tc_fence_after();
               issue_pv(b, sbase + C::OFF_V + vs * C::V_BYTES, j >= 4);
-              tc_commit(&v_empty[vs]);
+              if (leader) tc_commit(&v_empty[vs]);
               ++vc;
             }
             const int ks = kc % C::NK;
@@ -1082,9 +1087,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             fence_proxy_async_smem();
             tc_fence_after();
             issue_s_q0(b, sbase + C::OFF_K + ks * C::K_BYTES);
-            tc_commit(&k_empty[ks]);
+            if (leader) tc_commit(&k_empty[ks]);
             ++kc;
-            if (j == nt - 1) tc_commit(&bars[B_Q_EMPTY]);
+            if (j == nt - 1 && leader) tc_commit(&bars[B_Q_EMPTY]);
           }
           // the last PV of each stream, in tile order
           for (int j = nt >= 2 ? nt - 2 : 0; j < nt && ok; ++j) {
@@ -1100,8 +1105,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             fence_proxy_async_smem();
             tc_fence_after();
             issue_pv(b, sbase + C::OFF_V + vs * C::V_BYTES, j >= 2);
-            tc_commit(&bars[B_O_DONE + b]);
-            tc_commit(&v_empty[vs]);
+            if (leader) tc_commit(&bars[B_O_DONE + b]);
+            if (leader) tc_commit(&v_empty[vs]);
             ++vc;
           }
           continue;
@@ -1115,9 +1120,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
           issue_s(0, sK);
           if (q1) issue_s(1, sK);
-          tc_commit(&k_empty[ks]);
+          if (leader) tc_commit(&k_empty[ks]);
           ++kc;
-          if (nt == 1) tc_commit(&bars[B_Q_EMPTY]);
+          if (nt == 1 && leader) tc_commit(&bars[B_Q_EMPTY]);
         }
         for (int j = 1; j < nt && ok; ++j) {
           const int ks = kc % C::NK, vs = vc % C::NV;
@@ -1138,11 +1143,11 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             issue_pv(1, sV, j > 1);
             issue_s(1, sK);
           }
-          tc_commit(&v_empty[vs]);
+          if (leader) tc_commit(&v_empty[vs]);
           ++vc;
-          tc_commit(&k_empty[ks]);
+          if (leader) tc_commit(&k_empty[ks]);
           ++kc;
-          if (j == nt - 1) tc_commit(&bars[B_Q_EMPTY]);
+          if (j == nt - 1 && leader) tc_commit(&bars[B_Q_EMPTY]);
         }
         if (!ok) break;
         // last PV of both Q tiles
@@ -1155,21 +1160,21 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           tc_fence_after();
           const uint32_t sV = sbase + C::OFF_V + vs * C::V_BYTES;
           issue_pv(0, sV, nt > 1);
-          tc_commit(&bars[B_O_DONE + 0]);
+          if (leader) tc_commit(&bars[B_O_DONE + 0]);
           if (q1) {
             if (!mbar_wait(&bars[B_P_FULL + 1], p_cnt1 & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
             ++p_cnt1;
             tc_fence_after();
             issue_pv(1, sV, nt > 1);
-            tc_commit(&bars[B_O_DONE + 1]);
+            if (leader) tc_commit(&bars[B_O_DONE + 1]);
           }
-          tc_commit(&v_empty[vs]);
+          if (leader) tc_commit(&v_empty[vs]);
           ++vc;
         }
       }
       if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
       // drain: every MMA issued above must finish before TMEM is freed
-      tc_commit(&bars[B_FINAL]);
+      if (leader) tc_commit(&bars[B_FINAL]);
       if (!mbar_wait_drain(&bars[B_FINAL], 0)) record_status(p.status, PKX_ETIMEOUT);
     }
   } else if (warp == 9) {

@@ -419,8 +419,10 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
     // ------------------------------------------------ MMA issue (one thread)
     // Per K tile j: S(j+1) = Q K(j+1)^T as soon as the softmax has read S(j),
     // then O += P(j) V(j) once P(j) is written.  Descriptors are formed once
-    // per tile and stepped by constants.
-    if (lane == 0) {
+    // per tile and stepped by constants.  The whole warp runs the loop (the
+    // values stay warp-uniform); one elected lane issues.
+    {
+      const bool leader = elect_one();
       uint32_t q_cnt = 0, kc = 0, p_cnt = 0, f_cnt = 0;
       bool ok = true;
       constexpr uint32_t K_LO = sw128_desc_lo(0), K_HI = sw128_desc_hi(1024);
@@ -430,24 +432,24 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
         static_for<0, C::LQ / 16>([&](auto kk_c) {
           constexpr int kk = decltype(kk_c)::value;
           constexpr uint32_t bo = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) / 16;
-          tc_mma_ts_step<kk * 8, bo>(tmem + C::S_COL, tmem + C::Q_COL, b_lo, K_HI, C::IDESC_QK,
+          if (leader) tc_mma_ts_step<kk * 8, bo>(tmem + C::S_COL, tmem + C::Q_COL, b_lo, K_HI, C::IDESC_QK,
                                      kk > 0 ? 1u : 0u);
         });
-        tc_commit(&bars[M_S_FULL]);
+        if (leader) tc_commit(&bars[M_S_FULL]);
       };
       auto issue_pv = [&](uint32_t sV, bool acc_first) {
         const uint32_t b_lo = V_LO | (sV >> 4);
         const uint32_t acc0 = acc_first ? 1u : 0u;
         static_for<0, C::BN / 16>([&](auto kk_c) {
           constexpr int kk = decltype(kk_c)::value;
-          tc_mma_ts_step<kk * 8, kk * 128>(tmem + C::O_COL, tmem + C::P_COL, b_lo, V_HI,
+          if (leader) tc_mma_ts_step<kk * 8, kk * 128>(tmem + C::O_COL, tmem + C::P_COL, b_lo, V_HI,
                                            C::IDESC_PV, kk > 0 ? 1u : acc0);
         });
-        tc_commit(&bars[M_PV_DONE]);
+        if (leader) tc_commit(&bars[M_PV_DONE]);
       };
       auto k_tile = [&](uint32_t kpos) { return sbase + C::OFF_K + (kpos % C::NK) * C::K_BYTES; };
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-        const int u = ring_unit(&bars[M_U_FULL], &bars[M_U_EMPTY], s_unit, uc, abort_flag, false,
+        const int u = ring_unit(&bars[M_U_FULL], &bars[M_U_EMPTY], s_unit, uc, abort_flag, true,
                                 ok, p.wait_ns);
         if (u < 0) break;
         const WorkUnit w = p.units[p.uorder[u]];
@@ -477,14 +479,14 @@ __global__ void __launch_bounds__(MlaCfg<MODE>::THREADS, 1) mla_kernel(const KPa
           ++p_cnt;
           tc_fence_after();
           issue_pv(k_tile(k0 + j) + dv_off, j > 0);
-          tc_commit(&k_empty[(k0 + j) % C::NK]);
+          if (leader) tc_commit(&k_empty[(k0 + j) % C::NK]);
         }
         if (!ok) break;
         kc = k0 + nt;
-        tc_commit(&bars[M_O_DONE]);
+        if (leader) tc_commit(&bars[M_O_DONE]);
       }
       if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
-      tc_commit(&bars[M_FINAL]);
+      if (leader) tc_commit(&bars[M_FINAL]);
       if (!mbar_wait_drain(&bars[M_FINAL], 0)) record_status(p.status, PKX_ETIMEOUT);
     }
   } else if (warp == 5) {

@@ -216,6 +216,17 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// True in exactly one lane of the (converged) warp.  The MMA warps run their
+// issue loops with all 32 lanes, so the descriptors and addresses stay
+// warp-uniform, and only the elected lane issues each tcgen05 operation.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Arrive (once) on an mbarrier when every tcgen05 op this thread issued so far
 // has completed.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
