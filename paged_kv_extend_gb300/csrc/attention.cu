@@ -81,6 +81,7 @@ struct SchedParams {
   int unit_target, qb_max, unit_max, comb_max, slot_max;
   int32_t *seq;  // 8 arrays of batch+1 ints
   int32_t *qbt;  // [5][qb_max]: tiles, sequence, unit / slot / combine offsets per block
+  int seq_in_smem, blk_in_smem;  // those arrays in dynamic shared memory instead
   WorkUnit *units;
   int32_t *uorder;  // units by cost, largest first
   CombineEntry *comb;
@@ -157,25 +158,60 @@ __device__ __forceinline__ int range_tiles(int kb, int ke, int split, int bn) {
   return n_pre + n_ext;
 }
 
-// Exclusive scan of in[0..n) into out[0..n) by the whole 1024-thread block;
-// returns the total.  in and out may alias.
+// Exclusive scan of one value per thread over the 1024-thread block (warp
+// shuffles, then one warp over the 32 warp totals: three block barriers);
+// the total goes to *total.  sh must hold 32 ints.
+__device__ int block_scan_value(int v, int *sh, int &total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int t = sh[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    sh[lane] = t;
+  }
+  __syncthreads();
+  const int excl = (wid ? sh[wid - 1] : 0) + x - v;
+  total = sh[31];
+  __syncthreads();  // sh may be reused by the caller
+  return excl;
+}
+
+// Maximum of one value per thread over the 1024-thread block.
+__device__ int block_max(int v, int *sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) sh[wid] = v;
+  __syncthreads();
+  int m = sh[lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __syncthreads();  // sh may be reused by the caller
+  return m;
+}
+
+// Exclusive scan of in[0..n) into out[0..n) by the whole 1024-thread block
+// (each thread a contiguous chunk); returns the total.  in and out may
+// alias.
 __device__ int block_exclusive_scan(const int32_t *in, int32_t *out, int n, int *sh) {
   const int tid = threadIdx.x;
   const int ch = (n + 1023) / 1024;
   const int beg = min(n, tid * ch), end = min(n, beg + ch);
   int local = 0;
   for (int i = beg; i < end; ++i) local += in[i];
-  __syncthreads();
-  sh[tid] = local;
-  __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {
-    int v = tid >= off ? sh[tid - off] : 0;
-    __syncthreads();
-    sh[tid] += v;
-    __syncthreads();
-  }
-  int run = sh[tid] - local;
-  const int total = sh[1023];
+  int total;
+  int run = block_scan_value(local, sh, total);
   for (int i = beg; i < end; ++i) {
     int v = in[i];
     out[i] = run;
@@ -185,30 +221,14 @@ __device__ int block_exclusive_scan(const int32_t *in, int32_t *out, int n, int 
   return total;
 }
 
-// Exclusive scan of one value per thread over the 1024-thread block; the
-// total goes to *total.
-__device__ int block_scan_value(int v, int *sh, int &total) {
-  const int tid = threadIdx.x;
-  __syncthreads();
-  sh[tid] = v;
-  __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {
-    const int x = tid >= off ? sh[tid - off] : 0;
-    __syncthreads();
-    sh[tid] += x;
-    __syncthreads();
-  }
-  const int incl = sh[tid];
-  total = sh[1023];
-  __syncthreads();
-  return incl - v;
-}
-
-// Per-block tile counts live in shared memory when they fit (they are read
-// back many times while the units are emitted).
-constexpr int kSchedSmemBlocks = 8192;
-// Buckets of the counting sort of units by cost.
+// Buckets of the counting sorts (claim order, sequence ranks).
 constexpr int kCostBuckets = 2048;
+// Dynamic shared memory the scheduler may take: the histogram always, and
+// the per-sequence and per-block arrays when they fit (else they live in
+// the workspace, which is slower but has no size limit).
+constexpr int kSchedSmemMax = 200 * 1024;
+// Per-sequence and per-block arrays of the scheduler.
+constexpr int kSchedSeqArrays = 5, kSchedBlockArrays = 5;
 
 // Relative cost of a unit: its K/V tiles times its Q tiles, plus one for the
 // per-unit prologue and epilogue (clamped to the sort's bucket range).
@@ -217,15 +237,36 @@ __device__ __forceinline__ int unit_cost(const WorkUnit &w, int q_tile_tok) {
   return min(w.n_tiles * max(nq, 1) + 1, kCostBuckets - 1);
 }
 
+// Device-side work list.  Only the first phase reads global memory (the
+// indptrs); the per-sequence and per-block values then live in shared memory
+// (or, for very large batches, in the workspace), so the later phases are
+// throughput-bound rather than chains of dependent global loads.
+//   1. per sequence: P, E, T, first query row and query blocks; a scan gives
+//      each sequence's first block;
+//   2. per query block (of one KV head): its K/V tiles; their total sets the
+//      split-KV chunk C;
+//   3. per block: units (splits x value slices), partial slots and combine
+//      entries, and their offsets (scans);
+//   4-6. combine entries; every unit written and counted by its claim key
+//      (its cost, largest first), then placed in the claim order.
+// Largest first balances the CTAs, which claim units at run time.  (Orders
+// that keep a sequence's units together cut DRAM re-reads of K/V but cost
+// more in balance than they save: the kernel is not bound by DRAM.)
 __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
-  __shared__ int sh[1024];
+  extern __shared__ int sdyn[];
+  __shared__ int sh[32];
   __shared__ int s_c;
-  __shared__ int s_qbt[kSchedSmemBlocks];
-  __shared__ int s_hist[kCostBuckets];
   const int tid = threadIdx.x;
   const int B = p.batch;
-  int32_t *nqb = p.seq;                 // [B]  query blocks per sequence
-  int32_t *qboff = p.seq + 1 * (B + 1); // [B]  first query block of sequence
+  const int S1 = B + 1;
+  int *hist = sdyn;
+  int *seqa = p.seq_in_smem ? sdyn + kCostBuckets : p.seq;
+  int *sP = seqa, *sE = seqa + S1, *sT = seqa + 2 * S1, *sQ0 = seqa + 3 * S1;
+  int *sOff = seqa + 4 * S1;   // first query block of each sequence; [B] = total
+  int *blk = p.blk_in_smem ? sdyn + kCostBuckets + (p.seq_in_smem ? kSchedSeqArrays * S1 : 0)
+                           : p.qbt;
+  int *bNt = blk, *bSeq = blk + p.qb_max, *bUo = blk + 2 * p.qb_max;
+  int *bSo = blk + 3 * p.qb_max, *bCo = blk + 4 * p.qb_max;
 
   grid_dep_wait();    // inputs written by the previous kernel on the stream
   grid_dep_launch();  // the attention grid may start its prologue now
@@ -233,12 +274,19 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     if (!p.keep_status) p.hdr->status = 0;
     p.hdr->next_unit = 0;
   }
-  __syncthreads();
 
-  // 1. query blocks per sequence and their offsets
-  for (int b = tid; b < B; b += 1024) nqb[b] = seq_dims(p, b).nqb;
+  // 1. per sequence
+  for (int b = tid; b < B; b += 1024) {
+    const SeqDims d = seq_dims(p, b);
+    sP[b] = d.P;
+    sE[b] = d.E;
+    sT[b] = d.T;
+    sQ0[b] = d.qbase;
+    sOff[b] = d.nqb;
+  }
   __syncthreads();
-  const int total_qb = block_exclusive_scan(nqb, qboff, B, sh);
+  const int total_qb = block_exclusive_scan(sOff, sOff, B, sh);
+  if (tid == 0) sOff[B] = total_qb;
   if (total_qb > p.qb_max) {  // cannot happen for consistent indptrs
     if (tid == 0) {
       record_status(&p.hdr->status, PKX_EDEVICE);
@@ -247,58 +295,63 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     }
     return;
   }
-
-  int32_t *qbt = total_qb <= kSchedSmemBlocks ? s_qbt : p.qbt;
-  int32_t *qbs = p.qbt + p.qb_max;      // [total_qb] sequence of the block
-  int32_t *quo = p.qbt + 2 * p.qb_max;  // first unit of the block (one KV head)
-  int32_t *qso = p.qbt + 3 * p.qb_max;  // first partial slot
-  int32_t *qco = p.qbt + 4 * p.qb_max;  // combine entry
-
-  // 2. KV tiles per query block; total tiles
-  long long my_tiles = 0;
-  for (int b = tid; b < B; b += 1024) {
-    SeqDims d = seq_dims(p, b);
-    for (int qb = 0; qb < d.nqb; ++qb) {
-      int lo, hi, i0, i1;
-      qblock_range(p, d, qb, lo, hi, i0, i1);
-      const int nt = (hi - lo + p.bn - 1) / p.bn;
-      qbt[qboff[b] + qb] = nt;
-      qbs[qboff[b] + qb] = b;
-      my_tiles += nt;
+  __syncthreads();
+  auto dims = [&](int b) {
+    SeqDims d;
+    d.P = sP[b];
+    d.E = sE[b];
+    d.T = sT[b];
+    d.qbase = sQ0[b];
+    d.nqb = sOff[b + 1] - sOff[b];
+    return d;
+  };
+  // the sequence of query block qb: the last b with sOff[b] <= qb
+  auto seq_of = [&](int qb) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sOff[mid] <= qb) lo = mid;
+      else hi = mid - 1;
     }
+    return lo;
+  };
+
+  // 2. K/V tiles per query block; total tiles -> chunk size C
+  int my_tiles = 0;
+  for (int qb = tid; qb < total_qb; qb += 1024) {
+    const int b = seq_of(qb);
+    const SeqDims d = dims(b);
+    int lo, hi, i0, i1;
+    qblock_range(p, d, qb - sOff[b], lo, hi, i0, i1);
+    const int nt = (hi - lo + p.bn - 1) / p.bn;
+    bNt[qb] = nt;
+    bSeq[qb] = b;
+    my_tiles = min(my_tiles + nt, 0x1fffff);
   }
-  __syncthreads();
-  sh[tid] = (int)min(my_tiles, (long long)0x3fffffff);
-  __syncthreads();
-  for (int off = 512; off > 0; off >>= 1) {
-    if (tid < off) sh[tid] = min(sh[tid] + sh[tid + off], 0x3fffffff);
-    __syncthreads();
-  }
-  const long long total_tiles = (long long)sh[0] * p.hkv * p.n_dsplit;
-  __syncthreads();
+  int tiles_all;
+  block_scan_value(my_tiles, sh, tiles_all);
   if (tid == 0) {
-    long long c = (total_tiles + p.unit_target - 1) / p.unit_target;
+    const long long total_tiles = (long long)tiles_all * p.hkv * p.n_dsplit;
+    const long long c = (total_tiles + p.unit_target - 1) / p.unit_target;
     s_c = (int)max((long long)kMinSplitTiles, c);
     p.hdr->split_tiles = s_c;
   }
   __syncthreads();
   const int C = s_c;
 
-  // 3. per query block (of one KV head): units (splits x value slices),
-  //    partial slots and combine entries, and their offsets (each thread
-  //    scans a contiguous chunk of blocks)
+  // 3. per query block: units, slots, combine entries; their offsets
   const int nd = p.n_dsplit;
   auto splits = [&](int nt) { return nt > 0 ? (nt + C - 1) / C : 1; };
-  const int chunk = (total_qb + 1023) / 1024;
-  const int qb_beg = min(total_qb, tid * chunk), qb_end = min(total_qb, qb_beg + chunk);
-  // two key streams: every unit has two partial slots and every block a
-  // combine entry
+  // two key streams: every decode unit has two partial slots and every
+  // block a combine entry
   const bool dec2 = p.two_streams && p.mode == kDecode;
   const int spu = dec2 ? 2 : 1;
   auto combined = [&](int S) { return S > 1 || dec2; };
+  const int chunk = (total_qb + 1023) / 1024;
+  const int qb_beg = min(total_qb, tid * chunk), qb_end = min(total_qb, qb_beg + chunk);
   int lu = 0, ls = 0, lc = 0;
   for (int qb = qb_beg; qb < qb_end; ++qb) {
-    const int S = splits(qbt[qb]);
+    const int nt = bNt[qb], S = splits(nt);
     lu += S * nd;
     if (combined(S)) {
       ls += S * spu;
@@ -310,10 +363,10 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   int s0 = block_scan_value(ls, sh, ts);
   int c0 = block_scan_value(lc, sh, tcm);
   for (int qb = qb_beg; qb < qb_end; ++qb) {
-    quo[qb] = u0;
-    qso[qb] = s0;
-    qco[qb] = c0;
-    const int S = splits(qbt[qb]);
+    bUo[qb] = u0;
+    bSo[qb] = s0;
+    bCo[qb] = c0;
+    const int S = splits(bNt[qb]);
     u0 += S * nd;
     if (combined(S)) {
       s0 += S * spu;
@@ -331,66 +384,98 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     return;
   }
   const int n_units = (int)n_units_l, n_comb = (int)n_comb_l;
-  __syncthreads();
 
-  // 4. emit, one (KV head, query block) pair at a time per thread
-  for (int idx = tid; idx < p.hkv * total_qb; idx += 1024) {
+  // 4. claim keys: the unit's cost, largest first
+  for (int i = tid; i < kCostBuckets; i += 1024) hist[i] = 0;
+  __syncthreads();
+  auto claim_key = [&](const WorkUnit &w) { return kCostBuckets - 1 - unit_cost(w, p.q_tile_tok); };
+
+  // 5. combine entries, one (KV head, query block) pair per thread
+  const int n_pairs = p.hkv * total_qb;
+  for (int idx = tid; idx < n_pairs; idx += 1024) {
     const int kvh = idx / total_qb, qb = idx - kvh * total_qb;
-    const int b = qbs[qb];
-    SeqDims d = seq_dims(p, b);
+    const int S = splits(bNt[qb]);
+    if (!combined(S)) continue;
+    const int b = bSeq[qb];
+    const SeqDims d = dims(b);
+    int lo, hi, i0, i1;
+    qblock_range(p, d, qb - sOff[b], lo, hi, i0, i1);
+    CombineEntry e;
+    e.q_tok0 = d.qbase + i0;
+    e.n_tok = i1 - i0;
+    e.kvh = kvh;
+    e.slot0 = kvh * ts + bSo[qb];
+    e.n_split = S * spu;
+    // a split extend block of one query tile: its units' second stream
+    // fills the second half of each slot
+    e.pad[0] = p.two_streams && p.mode != kDecode && S > 1 && i1 - i0 <= p.q_tile_tok ? 2 : 1;
+    e.pad[1] = e.pad[2] = 0;
+    p.comb[kvh * tcm + bCo[qb]] = e;
+  }
+  // Unit u: KV head u / tu; within the head, query block qb is the last
+  // block with bUo[qb] <= rest, and the unit is its (split, value slice)
+  // number rest - bUo[qb].
+  auto unit_at = [&](int u) {
+    const int kvh = u / tu, rest = u - kvh * tu;
+    int lo_b = 0, hi_b = total_qb - 1;
+    while (lo_b < hi_b) {
+      const int mid = (lo_b + hi_b + 1) >> 1;
+      if (bUo[mid] <= rest) lo_b = mid;
+      else hi_b = mid - 1;
+    }
+    const int qb = lo_b, k = rest - bUo[qb];
+    const int sp = k / nd, dq = k - sp * nd;
+    const int b = bSeq[qb];
+    const SeqDims d = dims(b);
     const int split_at = p.mode == kTwoStage ? d.P : INT_MAX;
     int lo, hi, i0, i1;
-    qblock_range(p, d, qb - qboff[b], lo, hi, i0, i1);
-    const int nt = qbt[qb];
-    const int S = splits(nt);
+    qblock_range(p, d, qb - sOff[b], lo, hi, i0, i1);
+    const int nt = bNt[qb], S = splits(nt);
     const int tps = nt > 0 ? (nt + S - 1) / S : 0;
-    int uo = kvh * tu + quo[qb];
-    const int so = kvh * ts + qso[qb];
-    if (combined(S)) {
-      CombineEntry e;
-      e.q_tok0 = d.qbase + i0;
-      e.n_tok = i1 - i0;
-      e.kvh = kvh;
-      e.slot0 = so;
-      e.n_split = S * spu;
-      // a split extend block of one query tile: its units' second stream
-      // fills the second half of each slot
-      e.pad[0] = p.two_streams && p.mode != kDecode && S > 1 && i1 - i0 <= p.q_tile_tok ? 2 : 1;
-      e.pad[1] = e.pad[2] = 0;
-      p.comb[kvh * tcm + qco[qb]] = e;
-    }
-    for (int sp = 0; sp < S; ++sp) {
-      for (int dq = 0; dq < nd; ++dq) {
-        WorkUnit w;
-        w.q_tok0 = d.qbase + i0;
-        w.n_tok = i1 - i0;
-        w.qpos0 = d.P + i0;
-        w.kvh = kvh;
-        w.k_begin = min(hi, lo + sp * tps * p.bn);
-        w.k_end = min(hi, lo + (sp + 1) * tps * p.bn);
-        w.k_split = split_at;
-        w.n_tiles = range_tiles(w.k_begin, w.k_end, split_at, p.bn);
-        w.b = b;
-        w.slot = combined(S) ? so + sp * spu : -1;
-        w.dq = dq;
-        w.pad = 0;
-        p.units[uo++] = w;
+    WorkUnit w;
+    w.q_tok0 = d.qbase + i0;
+    w.n_tok = i1 - i0;
+    w.qpos0 = d.P + i0;
+    w.kvh = kvh;
+    w.k_begin = min(hi, lo + sp * tps * p.bn);
+    w.k_end = min(hi, lo + (sp + 1) * tps * p.bn);
+    w.k_split = split_at;
+    w.n_tiles = range_tiles(w.k_begin, w.k_end, split_at, p.bn);
+    w.b = b;
+    w.slot = combined(S) ? kvh * ts + bSo[qb] + sp * spu : -1;
+    w.dq = dq;
+    w.pad = 0;
+    return w;
+  };
+
+  // 6. units, consecutive threads on consecutive units (their records go
+  //    out as 16-byte stores); pass 0 writes them and counts their claim
+  //    keys, pass 1 places them in the claim order.  Lanes of a warp whose
+  //    units share a key make one atomic for the group (units of one
+  //    sequence and cost class share a key, so per-unit atomics serialise).
+  const int lane = tid & 31;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int base = tid - lane; base < n_units; base += 1024) {
+      const int u = base + lane;
+      const bool act = u < n_units;
+      WorkUnit w;
+      int key = -1;
+      if (act) {
+        w = unit_at(u);
+        key = claim_key(w);
+      }
+      const unsigned grp = __match_any_sync(0xffffffffu, key);
+      const int leader = __ffs(grp) - 1;
+      int first = 0;
+      if (act && lane == leader) first = atomicAdd(&hist[key], __popc(grp));
+      first = __shfl_sync(0xffffffffu, first, leader);
+      if (act) {
+        if (pass == 0) p.units[u] = w;
+        else p.uorder[first + __popc(grp & ((1u << lane) - 1u))] = u;
       }
     }
-  }
-
-  // 6. order the units by cost, largest first (counting sort; the order
-  //    within a cost is arbitrary).  The attention kernels hand them to
-  //    CTAs in serpentine order, which balances the work per CTA.
-  for (int i = tid; i < kCostBuckets; i += 1024) s_hist[i] = 0;
-  __syncthreads();
-  for (int u = tid; u < n_units; u += 1024)
-    atomicAdd(&s_hist[kCostBuckets - 1 - unit_cost(p.units[u], p.q_tile_tok)], 1);
-  __syncthreads();
-  block_exclusive_scan(s_hist, s_hist, kCostBuckets, sh);
-  for (int u = tid; u < n_units; u += 1024) {
-    const int pos = atomicAdd(&s_hist[kCostBuckets - 1 - unit_cost(p.units[u], p.q_tile_tok)], 1);
-    p.uorder[pos] = u;
+    __syncthreads();
+    if (pass == 0) block_exclusive_scan(hist, hist, kCostBuckets, sh);
   }
   if (tid == 0) {
     p.hdr->n_units = n_units;
@@ -1608,6 +1693,8 @@ int tokens_per_block(int group) { return group >= 1 && group <= kBlockM ? kBlock
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+constexpr int kMaxDevicesCfg = 64;
+
 // Rows of one split-KV partial slot: both Q tiles of an extend block, or the
 // group's rows of a decode query.
 int rows_per_slot(bool decode, int group, bool mla) {
@@ -1650,6 +1737,18 @@ WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int 
   return L;
 }
 
+// Whether a kernel's dynamic shared-memory limit has been raised on the
+// current device (the attribute is per device; one flag array per kernel).
+static bool needs_config(bool (&done)[kMaxDevicesCfg]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesCfg) return true;
+  return !done[dev];
+}
+static void mark_configured(bool (&done)[kMaxDevicesCfg]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevicesCfg) done[dev] = true;
+}
+
 // cuTensorMapEncodeTiled from the driver, looked up once.
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1684,13 +1783,13 @@ static int make_q_map(CUtensorMap *m, const void *q, int64_t n, int hq, int lq, 
 template <int HD, int MODE, bool MASK = false, int FMT = 0>
 static int launch_attn_kernel(const TMaps &tmaps, const KParams &kp, int grid, cudaStream_t s) {
   using C = Cfg<HD>;
-  static bool configured = false;  // per instantiation; attribute is per device
-  if (!configured) {
+  static bool configured[kMaxDevicesCfg] = {};  // per instantiation and device
+  if (needs_config(configured)) {
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, MODE, MASK, FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
       return set_error(PKX_ECUDA, "cudaFuncSetAttribute(attn_kernel): %s", cudaGetErrorString(e));
-    configured = true;
+    mark_configured(configured);
   }
   cudaError_t e = launch_pdl(attn_kernel<HD, MODE, MASK, FMT>, dim3(grid), dim3(C::THREADS),
                              C::SMEM, s, tmaps, kp);
@@ -1711,13 +1810,13 @@ static int launch_attn_fp8(int mode, const TMaps &tmaps, const KParams &kp, int 
 template <int MODE, bool MASK = false>
 static int launch_mla_kernel(const KParams &kp, int grid, cudaStream_t s) {
   using C = MlaCfg<MODE>;
-  static bool configured = false;
-  if (!configured) {
+  static bool configured[kMaxDevicesCfg] = {};
+  if (needs_config(configured)) {
     cudaError_t e = cudaFuncSetAttribute(mla_kernel<MODE, MASK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
       return set_error(PKX_ECUDA, "cudaFuncSetAttribute(mla_kernel): %s", cudaGetErrorString(e));
-    configured = true;
+    mark_configured(configured);
   }
   cudaError_t e = launch_pdl(mla_kernel<MODE, MASK>, dim3(grid), dim3(C::THREADS), C::SMEM, s,
                              kp);
@@ -1799,8 +1898,25 @@ int launch_attention(const AttnArgs &a) {
   sp.uorder = reinterpret_cast<int32_t *>(ws + L.uorder_off);
   sp.comb = reinterpret_cast<CombineEntry *>(ws + L.comb_off);
   sp.hdr = hdr;
+  size_t sched_smem = kCostBuckets * sizeof(int);
   {
-    cudaError_t e = launch_pdl(sched_kernel, dim3(1), dim3(1024), 0, a.stream, sp);
+    const size_t seq_b = (size_t)kSchedSeqArrays * (a.batch + 1) * sizeof(int);
+    const size_t blk_b = (size_t)kSchedBlockArrays * L.qb_max * sizeof(int);
+    sp.seq_in_smem = sched_smem + seq_b <= (size_t)kSchedSmemMax;
+    if (sp.seq_in_smem) sched_smem += seq_b;
+    sp.blk_in_smem = sched_smem + blk_b <= (size_t)kSchedSmemMax;
+    if (sp.blk_in_smem) sched_smem += blk_b;
+    static bool configured[kMaxDevicesCfg] = {};
+    if (needs_config(configured)) {
+      cudaError_t e = cudaFuncSetAttribute(sched_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSchedSmemMax);
+      if (e != cudaSuccess)
+        return set_error(PKX_ECUDA, "cudaFuncSetAttribute(sched_kernel): %s", cudaGetErrorString(e));
+      mark_configured(configured);
+    }
+  }
+  {
+    cudaError_t e = launch_pdl(sched_kernel, dim3(1), dim3(1024), sched_smem, a.stream, sp);
     if (e != cudaSuccess)
       return set_error(PKX_ECUDA, "sched_kernel launch: %s", cudaGetErrorString(e));
   }

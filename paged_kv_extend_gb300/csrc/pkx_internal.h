@@ -41,7 +41,7 @@ constexpr int kMinSplitTiles = 4;
 // One unit of attention work: a block of query tokens of one sequence and one
 // KV head (up to two Q tiles; in a tile, row = token * group + head-in-group),
 // over the key range [k_begin, k_end).
-struct WorkUnit {
+struct __align__(16) WorkUnit {
   int32_t q_tok0;   // first query row in q/o (token index)
   int32_t n_tok;    // tokens in the block
   int32_t qpos0;    // position of the first query token in its sequence
@@ -58,7 +58,7 @@ struct WorkUnit {
 
 // A query block whose key range was split: its partials live in slots
 // [slot0, slot0 + n_split).
-struct CombineEntry {
+struct __align__(16) CombineEntry {
   int32_t q_tok0;
   int32_t n_tok;
   int32_t kvh;
@@ -79,7 +79,7 @@ struct WsHeader {
 
 // Byte offsets of the workspace regions for one problem.
 struct WsLayout {
-  size_t seq_off;      // int32 [8][batch + 1] per-sequence scratch (two used)
+  size_t seq_off;      // int32 [8][batch + 1] per-sequence scratch (five used)
   size_t qb_off;       // int32 [5][qb_max] per-query-block scheduler arrays
   size_t units_off;    // WorkUnit [unit_max]
   size_t uorder_off;   // int32 [unit_max] units by cost, largest first
