@@ -319,6 +319,10 @@ WORKLOAD_TEXT = {
     "decode_mla": "decode: batch=64 Hq=16 Hkv=1 Lq=576 Lv=512 (V aliases K) T=4096 pool=2^20 slots",
     "spec_verify": "batch=64 Hq=32 Hkv=8 D=128 prefix~U[1024,4096] extend=64 draft-tree tokens "
                    "under a custom mask (prefix + ancestors + self) pool=2^20 slots (permuted)",
+    "split_192": "batch=16 Hq=16 Hkv=16 Lq=192 (128+64 rope) Lv=128 prefix~U[0,4096] "
+                 "extend~U[1,1024] pool=2^18 slots (permuted) bf16 N(0,1) sm_scale=1/sqrt(192)",
+    "split_288": "batch=16 Hq=16 Hkv=4 Lq=288 (256+32 rope) Lv=256 prefix~U[0,4096] "
+                 "extend~U[1,1024] pool=2^18 slots (permuted) bf16 N(0,1) sm_scale=1/sqrt(288)",
     "sinks_swa": "batch=16 Hq=64 Hkv=8 D=64 prefix~U[0,4096] extend~U[1,1024] sliding_window=128 "
                  "sink logit per head ~N(0,1.5) pool=2^18 slots (permuted)",
 }
@@ -782,7 +786,8 @@ def run_ours(args, ws, rank, local):
     if not args.no_components:
         names = (args.components.split(",") if args.components
                  else ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla",
-                       "kv_ops", "split", "decode_gqa_fp8", "llama3_8b_fp8"])
+                       "split_192", "split_288", "kv_ops", "split", "decode_gqa_fp8",
+                       "llama3_8b_fp8"])
         if args.all_workloads:
             names = ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla", "kv_ops",
                      "split", "decode_gqa_fp8", "long_prefix_fp8", "llama3_8b_fp8"]

@@ -41,7 +41,8 @@ static int check_heads(int hq, int hkv, int lq, int lv) {
     return set_error(PKX_EINVAL, "hq=%d must be a positive multiple of hkv=%d", hq, hkv);
   if (hq / hkv > kBlockM)
     return set_error(PKX_EUNSUPPORTED, "group size hq/hkv=%d > %d not built", hq / hkv, kBlockM);
-  const bool ok = (lq == 64 && lv == 64) || (lq == 128 && lv == 128) || (lq == 576 && lv == 512);
+  const bool ok = (lq == 64 && lv == 64) || (lq == 128 && lv == 128) || (lq == 576 && lv == 512) ||
+                  split_head_dims(lq, lv);
   if (!ok) return set_error(PKX_EUNSUPPORTED, "head dims (lq=%d, lv=%d) not built", lq, lv);
   return PKX_OK;
 }
@@ -108,22 +109,19 @@ size_t pkx_extend_workspace_size(int batch, int num_q_tokens, int hq, int hkv, i
   if (batch < 0 || num_q_tokens < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM ||
       lv <= 0)
     return 0;
-  return ws_layout(batch, num_q_tokens, hkv, hq / hkv, lv, num_sms_current_device(), false,
-                   lq == 576 && lv == 512)
+  return ws_layout(batch, num_q_tokens, hkv, hq / hkv, lq, lv, num_sms_current_device(), false)
       .total;
 }
 
 size_t pkx_decode_workspace_min_size(int batch, int hq, int hkv, int lq, int lv) {
   if (batch < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM || lv <= 0) return 0;
-  return ws_layout(batch, batch, hkv, hq / hkv, lv, num_sms_current_device(), true,
-                   lq == 576 && lv == 512, false)
+  return ws_layout(batch, batch, hkv, hq / hkv, lq, lv, num_sms_current_device(), true, false)
       .total;
 }
 
 size_t pkx_decode_workspace_size(int batch, int hq, int hkv, int lq, int lv) {
   if (batch < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM || lv <= 0) return 0;
-  return ws_layout(batch, batch, hkv, hq / hkv, lv, num_sms_current_device(), true,
-                   lq == 576 && lv == 512)
+  return ws_layout(batch, batch, hkv, hq / hkv, lq, lv, num_sms_current_device(), true)
       .total;
 }
 
@@ -210,9 +208,8 @@ struct SplitLayout {
 static SplitLayout split_layout(int batch, int num_q_tokens, int hq, int hkv, int lq, int lv) {
   SplitLayout L;
   L.attn = 0;
-  const size_t attn = align256(ws_layout(batch, num_q_tokens, hkv, hq / hkv, lv,
-                                         num_sms_current_device(), false,
-                                         lq == 576 && lv == 512).total);
+  const size_t attn = align256(ws_layout(batch, num_q_tokens, hkv, hq / hkv, lq, lv,
+                                         num_sms_current_device(), false).total);
   const size_t rows = (size_t)num_q_tokens * hq;
   L.o_paged = attn;
   L.lse_paged = L.o_paged + align256(rows * lv * 2);

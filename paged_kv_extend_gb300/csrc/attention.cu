@@ -524,24 +524,39 @@ struct TMaps {
   CUtensorMap q;
 };
 
+// Head configuration HD: 64 and 128 are Lq = Lv = HD (two Q tiles per unit);
+// 192 and 288 are the split head dims Lq = 192 / Lv = 128 and Lq = 288 /
+// Lv = 256 (sglang extend_attention.py, _get_block_sizes_for_extend_attention:
+// 192 = 128 + 64 rope, 288 = 256 + 32 rope), run with one Q tile per unit and
+// one key stream: S (128 columns) and O (Lv columns) of the one tile fit TMEM,
+// and a K stage of 128 keys fits shared memory next to the larger Q tile.
 template <int HD>
 struct Cfg {
-  static constexpr int BM = kBlockM, BN = kBlockN, HDV = HD;
-  static constexpr int NK = HD == 128 ? 3 : 5;  // K ring stages
-  static constexpr int NV = HD == 128 ? 2 : 5;  // V ring stages
-  static constexpr int NI = HD == 128 ? 3 : 4;  // row-index ring stages
-  static constexpr int Q_BYTES = BM * HD * 2;   // one Q tile
-  static constexpr int K_BYTES = BN * HD * 2;
-  static constexpr int V_BYTES = BN * HDV * 2;
+  static constexpr bool SPLIT = HD == 192 || HD == 288;
+  static constexpr int BM = kBlockM, BN = kBlockN;
+  static constexpr int LQ = HD;
+  static constexpr int HDV = HD == 192 ? 128 : HD == 288 ? 256 : HD;
+  static constexpr int QA = (LQ + 63) / 64;  // 64-dim swizzle atoms of a Q / K row
+  static constexpr int VA = HDV / 64;        // ... of a V row
+  static constexpr int NQT = SPLIT ? 1 : 2;  // Q tiles per unit
+  static constexpr bool TWO_OK = !SPLIT;     // two key streams for one-tile units
+  static constexpr int NK = HD == 128 ? 3 : HD == 64 ? 5 : HD == 192 ? 2 : 1;  // K ring stages
+  static constexpr int NV = HD == 128 ? 2 : HD == 64 ? 5 : HD == 192 ? 2 : 1;  // V ring stages
+  static constexpr int NI = HD == 64 ? 4 : 3;     // row-index ring stages
+  static constexpr int Q_BYTES = BM * QA * 128;   // one Q tile (a 288-dim row fills 4.5 atoms)
+  static constexpr int K_BYTES = BN * QA * 128;
+  static constexpr int V_BYTES = BN * VA * 128;
   static constexpr int I_BYTES = BN * 4;        // int32 row of each key
-  static constexpr int OFF_Q = 0;  // two Q tiles
-  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_Q = 0;               // NQT Q tiles
+  static constexpr int OFF_K = OFF_Q + NQT * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NK * K_BYTES;
   static constexpr int OFF_I = OFF_V + NV * V_BYTES;
   static constexpr int OFF_BAR = OFF_I + NI * I_BYTES;
   static constexpr int N_BARS = 17 + 2 * NK + 2 * NV + 2 * NI;
   static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 1024;  // + alignment slack
-  static constexpr int TMEM_COLS = 512;  // S0 | S1 | O0 | O1, 128 columns each
+  // S0 | S1 | O0 | O1, 128 columns each (split dims: S0 | unused | O0 of Lv)
+  static constexpr int TMEM_COLS = 512;
+  static_assert(2 * BN + NQT * HDV <= TMEM_COLS, "TMEM budget");
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HDV, 1);
   // warps 0-7: two softmax warpgroups; 8: MMA; 9: row indices + Q;
@@ -549,6 +564,10 @@ struct Cfg {
   static constexpr int THREADS = 512;
   static constexpr int COPY_WARP0 = 10;
   static constexpr int COPY_THREADS = 128;
+  // keys per copy pass: whole rows per thread group for 64 / 128 dims; by
+  // swizzle atom (chunk t % 8 of every atom, keys t / 8 + 16 i) for the
+  // split dims, whose 24 or 36 chunks per row do not divide 128 threads
+  static constexpr int KPP = SPLIT ? 16 : COPY_THREADS / (HD / 8);
   // Registers: the kernel launches with REGS_LAUNCH per thread (checked at
   // build time); the softmax warpgroups take REGS_SOFTMAX, the other two
   // give back down to REGS_OTHER.  The split must add up exactly.
@@ -785,7 +804,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       // Two key streams (decode units; split units of one query tile):
       // warpgroup wg takes the unit's tiles wg, wg + 2, ... of the one query
       // tile and writes its own partial, which the combine merges.
-      const bool two = MODE == kDecode ? p.dec_two != 0 : (w.slot >= 0 && w.n_tok <= TOK);
+      const bool two = C::TWO_OK && (MODE == kDecode ? p.dec_two != 0 : (w.slot >= 0 && w.n_tok <= TOK));
       // this warpgroup's tiles: j0, j0 + jstep, ... below the unit's n_tiles
       const int j0 = two ? wg : 0, jstep = two ? 2 : 1;
       const int nt = w.n_tiles - j0;  // > 0 when the warpgroup has a tile
@@ -1102,7 +1121,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       auto issue_s = [&](int qt, uint32_t sK) {
         const uint32_t a_lo = K_LO | ((qt ? sQ1 : sQ0) >> 4), b_lo = K_LO | (sK >> 4);
         const uint32_t d = tmem + qt * C::BN;
-        static_for<0, HD / 16>([&](auto kk_c) {
+        static_for<0, C::LQ / 16>([&](auto kk_c) {
           constexpr int kk = decltype(kk_c)::value;
           constexpr uint32_t ao = ((kk / 4) * (C::BM * 128) + (kk % 4) * 32) / 16;
           constexpr uint32_t bo = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) / 16;
@@ -1114,7 +1133,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       auto issue_s_q0 = [&](int buf, uint32_t sK) {
         const uint32_t a_lo = K_LO | (sQ0 >> 4), b_lo = K_LO | (sK >> 4);
         const uint32_t d = tmem + buf * C::BN;
-        static_for<0, HD / 16>([&](auto kk_c) {
+        static_for<0, C::LQ / 16>([&](auto kk_c) {
           constexpr int kk = decltype(kk_c)::value;
           constexpr uint32_t ao = ((kk / 4) * (C::BM * 128) + (kk % 4) * 32) / 16;
           constexpr uint32_t bo = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) / 16;
@@ -1144,7 +1163,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         }
         ++q_cnt;
         tc_fence_after();
-        if (MODE == kDecode ? p.dec_two != 0 : (w.slot >= 0 && !q1)) {
+        if (C::TWO_OK && (MODE == kDecode ? p.dec_two != 0 : (w.slot >= 0 && !q1))) {
           // Two key streams over the one query tile: even tiles into S/P
           // buffer 0 (softmax warpgroup 0, O 0), odd tiles into buffer 1
           // (warpgroup 1, O 1).  S(j) waits only for PV(j-2), which reads
@@ -1302,9 +1321,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         if (q_cnt > 0 && !mbar_wait(&bars[B_Q_EMPTY], (q_cnt - 1) & 1u, abort_flag, p.wait_ns)) ok = false;
         if (ok) {
           const int nq = q1 ? 2 : 1;
-          mbar_arrive_expect_tx(&bars[B_Q_FULL], q_box_bytes * (HD / 64) * nq);
+          mbar_arrive_expect_tx(&bars[B_Q_FULL], q_box_bytes * C::QA * nq);
           for (int qt = 0; qt < nq; ++qt)
-            for (int h = 0; h < HD / 64; ++h)
+            for (int h = 0; h < C::QA; ++h)
               tma_load_3d(sbase + C::OFF_Q + qt * C::Q_BYTES + h * (C::BM * 128), &tm.q, h * 64,
                           w.kvh * G, w.q_tok0 + qt * TOK, &bars[B_Q_FULL]);
         }
@@ -1348,7 +1367,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         }
         {
           // ring[key % KPP][key / KPP]: each copy thread's rows contiguous
-          constexpr int KPP = C::COPY_THREADS / (HD / 8), NK_T = C::BN / KPP;
+          constexpr int KPP = C::KPP, NK_T = C::BN / KPP;
           int *ring = reinterpret_cast<int *>(smem + C::OFF_I + is * C::I_BYTES);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -1375,23 +1394,40 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     // destination base.  The index warp stores each thread's rows
     // contiguously (ring[key0][i]).  A thread arrives (noinc) on the stage
     // barrier when its own copies have landed.
+    // Split head dims: thread ct copies chunk ct % 8 of every 64-dim atom of
+    // keys ct / 8 + 16 i (KPP = 16), so the swizzle term is again fixed per
+    // thread; a warp instruction reads four rows' 128-byte segments.
     const int ct = tid - C::COPY_WARP0 * 32;
-    constexpr int CPR = HD / 8;                 // chunks of a row
-    constexpr int KPP = C::COPY_THREADS / CPR;  // keys per pass
-    constexpr int NKEYS = C::BN / KPP;          // keys per thread
+    constexpr int CPR = C::SPLIT ? 8 : C::LQ / 8;  // chunk lanes of a key
+    constexpr int KPP = C::KPP;                    // keys per pass
+    constexpr int NKEYS = C::BN / KPP;             // keys per thread
+    static_assert(KPP * CPR == C::COPY_THREADS, "copy geometry");
     static_assert(KPP % 8 == 0 && C::BN % KPP == 0, "constant swizzle per thread");
     const int ch = ct % CPR, key0 = ct / CPR;
     const uint32_t dthr = (uint32_t)(ch >> 3) * (C::BN * 128) + (uint32_t)key0 * 128u +
                           ((uint32_t)((ch & 7) ^ (key0 & 7)) << 4);
-    auto copy_rows = [&](uint32_t stage, const bf16 *base, int64_t stride, const int *rows) {
+    // the thread's chunks of its NKEYS rows (of L elements) into a stage
+    auto copy_rows = [&](uint32_t stage, const bf16 *base, int64_t stride, const int *rows,
+                         auto l_c) {
+      constexpr int L = decltype(l_c)::value;
       static_for<0, NKEYS>([&](auto i_c) {
         constexpr int i = decltype(i_c)::value;
         const int r = rows[i];
         const uint32_t bytes = r >= 0 ? 16u : 0u;
         const bf16 *src = base + (int64_t)max(r, 0) * stride;
-        cp_async_16_at<i * KPP * 128, 0>(stage + dthr, src, bytes);
+        if constexpr (!C::SPLIT) {
+          cp_async_16_at<i * KPP * 128, 0>(stage + dthr, src, bytes);
+        } else {
+          static_for<0, (L + 63) / 64>([&](auto a_c) {
+            constexpr int a = decltype(a_c)::value;
+            if (a * 8 + ch < L / 8)  // the last atom of a 288-dim row holds 4 chunks
+              cp_async_16_at<a * C::BN * 128 + i * KPP * 128, a * 128>(stage + dthr, src, bytes);
+          });
+        }
       });
     };
+    constexpr std::integral_constant<int, C::LQ> K_LEN{};
+    constexpr std::integral_constant<int, C::HDV> V_LEN{};
     uint32_t kc = 0, vc = 0, ic = 0, qc = 0;
     bool ok = true;
     if constexpr (FMT == 0) {
@@ -1439,7 +1475,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             break;
           }
           copy_rows(sbase + C::OFF_K + ks * C::K_BYTES, from_ext ? kx : kp,
-                    from_ext ? p.ke_st : p.kb_ss, rows);
+                    from_ext ? p.ke_st : p.kb_ss, rows, K_LEN);
           cp_async_arrive_noinc(&k_full[ks]);
           ++kc;
           // V tile
@@ -1450,7 +1486,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
             break;
           }
           copy_rows(sbase + C::OFF_V + vs * C::V_BYTES, from_ext ? vx : vp,
-                    from_ext ? p.ve_st : p.vb_ss, rows);
+                    from_ext ? p.ve_st : p.vb_ss, rows, V_LEN);
           cp_async_arrive_noinc(&v_full[vs]);
           ++vc;
         }
@@ -1524,7 +1560,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           return false;
         const uint32_t stage = sbase + C::OFF_K + ks * C::K_BYTES;
         if (from_ext) {
-          copy_rows(stage, kx, p.ke_st, rows);
+          copy_rows(stage, kx, p.ke_st, rows, K_LEN);
           cp_async_arrive_noinc(&k_full[ks]);
         } else {
           issue_raw(stage, kp8, p.kb_ss, rows);
@@ -1540,7 +1576,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           return false;
         const uint32_t stage = sbase + C::OFF_V + vs * C::V_BYTES;
         if (from_ext) {
-          copy_rows(stage, vx, p.ve_st, rows);
+          copy_rows(stage, vx, p.ve_st, rows, V_LEN);
           cp_async_arrive_noinc(&v_full[vs]);
         } else {
           issue_raw(stage, vp8, p.vb_ss, rows);
@@ -1697,27 +1733,36 @@ constexpr int kMaxDevicesCfg = 64;
 
 // Rows of one split-KV partial slot: both Q tiles of an extend block, or the
 // group's rows of a decode query.
-int rows_per_slot(bool decode, int group, bool mla) {
-  return decode ? group : (mla ? 1 : 2) * tokens_per_block(group) * group;
+bool split_head_dims(int lq, int lv) { return (lq == 192 && lv == 128) || (lq == 288 && lv == 256); }
+
+int q_tiles_per_unit(int lq, int lv) {
+  return (lq == 576 && lv == 512) || split_head_dims(lq, lv) ? 1 : 2;
 }
 
-WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int num_sms,
-                   bool decode, bool mla, bool two_streams) {
+int rows_per_slot(bool decode, int group, int nqt) {
+  return decode ? group : nqt * tokens_per_block(group) * group;
+}
+
+WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lq, int lv, int num_sms,
+                   bool decode, bool two_streams) {
   WsLayout L{};
-  // tokens of a query block: two Q tiles (GQA kernel) or one (MLA kernel)
-  const int tok = (mla ? 1 : 2) * tokens_per_block(group);
+  const bool mla = lq == 576 && lv == 512;
+  // tokens of a query block: two Q tiles (GQA kernel, Lq = Lv <= 128) or one
+  // (MLA kernel, split head dims)
+  const int nqt = q_tiles_per_unit(lq, lv);
+  const int tok = nqt * tokens_per_block(group);
   L.unit_target = 4 * (num_sms > 0 ? num_sms : 160);
   L.qb_max = (tok > 0 ? (num_q_tokens + tok - 1) / tok : 0) + batch + 1;
   L.unit_max = (L.unit_target + hkv * L.qb_max) * (mla ? 4 : 1);
   L.slot_max = 2 * L.unit_target;
   L.comb_max = L.unit_target;
-  if (decode && !mla && two_streams) {
+  if (decode && !mla && !split_head_dims(lq, lv) && two_streams) {
     // two key streams per unit: two partial slots per unit, a combine entry
     // per (query block, KV head)
     L.slot_max = 2 * L.unit_max;
     L.comb_max = L.unit_target + hkv * L.qb_max;
   }
-  L.rows_per_slot = rows_per_slot(decode, group, mla);
+  L.rows_per_slot = rows_per_slot(decode, group, nqt);
   size_t off = align256(sizeof(WsHeader));
   L.seq_off = off;
   off = align256(off + sizeof(int32_t) * 8 * (size_t)(batch + 1));
@@ -1832,12 +1877,14 @@ int launch_attention(const AttnArgs &a) {
   const bool decode = a.mode == kDecode;
   const bool mla = a.lq == 576 && a.lv == 512;
   const int nq = decode ? a.batch : a.num_q_tokens;
-  WsLayout L = ws_layout(a.batch, nq, a.hkv, group, a.lv, nsm, decode, mla);
+  const bool split = split_head_dims(a.lq, a.lv);
+  WsLayout L = ws_layout(a.batch, nq, a.hkv, group, a.lq, a.lv, nsm, decode);
   // Decode runs two key streams when the workspace holds their partial
-  // slots (pkx_decode_workspace_size asks for that), else one stream.
-  bool dec_two = decode && !mla;
+  // slots (pkx_decode_workspace_size asks for that), else one stream.  The
+  // MLA kernel and the split head dims run one stream.
+  bool dec_two = decode && !mla && !split;
   if (dec_two && a.workspace_bytes < L.total) {
-    const WsLayout L1 = ws_layout(a.batch, nq, a.hkv, group, a.lv, nsm, decode, mla, false);
+    const WsLayout L1 = ws_layout(a.batch, nq, a.hkv, group, a.lq, a.lv, nsm, decode, false);
     if (a.workspace_bytes >= L1.total) {
       L = L1;
       dec_two = false;
@@ -1877,13 +1924,13 @@ int launch_attention(const AttnArgs &a) {
   sp.prefix_lens = a.prefix_lens;
   sp.batch = a.batch;
   sp.hkv = a.hkv;
-  sp.tok = (mla ? 1 : 2) * tok;
+  sp.tok = q_tiles_per_unit(a.lq, a.lv) * tok;
   sp.bn = mla ? MlaCfg<0>::BN : kBlockN;
   sp.q_tile_tok = tok > 0 ? tok : 1;
   sp.no_causal = a.custom_mask != nullptr;
   sp.key_set = a.mode == kTwoStage ? a.key_set : kAllKeys;
   sp.keep_status = a.keep_status;
-  sp.two_streams = !mla && (!decode || dec_two);
+  sp.two_streams = !mla && !split && (!decode || dec_two);
   sp.n_dsplit = mla ? MlaCfg<0>::LV / MlaCfg<0>::DVS : 1;
   sp.window = a.window;
   sp.num_q_tokens = nq;
@@ -2004,6 +2051,19 @@ int launch_attention(const AttnArgs &a) {
       rc = masked ? launch_attn_kernel<64, kUnified, true>(tm, kp, grid, a.stream)
                   : launch_attn_kernel<64, kUnified>(tm, kp, grid, a.stream);
     else rc = launch_attn_kernel<64, kDecode>(tm, kp, grid, a.stream);
+  } else if (split) {
+    if (masked)
+      return set_error(PKX_EUNSUPPORTED, "a custom mask is not built for head dims (%d, %d)",
+                       a.lq, a.lv);
+    if (a.lq == 192) {
+      if (a.mode == kTwoStage) rc = launch_attn_kernel<192, kTwoStage>(tm, kp, grid, a.stream);
+      else if (a.mode == kUnified) rc = launch_attn_kernel<192, kUnified>(tm, kp, grid, a.stream);
+      else rc = launch_attn_kernel<192, kDecode>(tm, kp, grid, a.stream);
+    } else {
+      if (a.mode == kTwoStage) rc = launch_attn_kernel<288, kTwoStage>(tm, kp, grid, a.stream);
+      else if (a.mode == kUnified) rc = launch_attn_kernel<288, kUnified>(tm, kp, grid, a.stream);
+      else rc = launch_attn_kernel<288, kDecode>(tm, kp, grid, a.stream);
+    }
   } else if (mla) {
     if (a.mode == kTwoStage)
       rc = masked ? launch_mla_kernel<kTwoStage, true>(kp, grid, a.stream)

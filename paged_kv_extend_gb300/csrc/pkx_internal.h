@@ -116,11 +116,15 @@ void attention_events(cudaEvent_t *before, cudaEvent_t *after);
 // pkx_set_stall_injection for this thread.
 void wait_settings(uint64_t *wait_ns, int *stall);
 int tokens_per_block(int group);
-int rows_per_slot(bool decode, int group, bool mla);
+// The split head dims Lq / Lv = 192 / 128 and 288 / 256.
+bool split_head_dims(int lq, int lv);
+// Q tiles (of 128 rows) per work unit: 2 for Lq = Lv <= 128, else 1.
+int q_tiles_per_unit(int lq, int lv);
+int rows_per_slot(bool decode, int group, int nqt);
 // two_streams: the decode layout with two partial slots per unit (the GQA
 // kernel's two key streams); without it decode units run one stream.
-WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lv, int num_sms,
-                   bool decode, bool mla, bool two_streams = true);
+WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lq, int lv, int num_sms,
+                   bool decode, bool two_streams = true);
 
 // Arguments of one attention launch (any key mode).
 struct AttnArgs {

@@ -104,6 +104,18 @@ SPECS = {
         "sinks_swa", batch=16, hq=64, hkv=8, lq=64, lv=64,
         prefix=("uniform", 0, 4096), extend=("uniform", 1, 1024), num_slots=1 << 18,
         sliding_window=128, seed=1008, sinks=True),
+    # The split head dims of the pages' launcher (Lq = 192 = 128 + 64 rope with
+    # Lv = 128, and Lq = 288 = 256 + 32 rope with Lv = 256) on the
+    # Llama-shaped length mix; 16 query heads each, one KV head per query head
+    # for 192 / 128 (an MHA latent-free layout) and groups of four for 288.
+    "split_192": WorkloadSpec(
+        "split_192", batch=16, hq=16, hkv=16, lq=192, lv=128,
+        prefix=("uniform", 0, 4096), extend=("uniform", 1, 1024), num_slots=1 << 18,
+        sm_scale=1.0 / math.sqrt(192.0), seed=1009),
+    "split_288": WorkloadSpec(
+        "split_288", batch=16, hq=16, hkv=4, lq=288, lv=256,
+        prefix=("uniform", 0, 4096), extend=("uniform", 1, 1024), num_slots=1 << 18,
+        sm_scale=1.0 / math.sqrt(288.0), seed=1010),
 }
 
 

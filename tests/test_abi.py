@@ -67,10 +67,14 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _extend(lib, hq=6, hkv=4) == pkx.PKX_EINVAL
     assert b"multiple" in lib.pkx_last_error_string()
     assert _extend(lib, lq=96, lv=96) == pkx.PKX_EUNSUPPORTED
-    # the other split head dims are not built: a clean refusal, not a launch
-    assert _extend(lib, lq=192, lv=128) == pkx.PKX_EUNSUPPORTED
+    # the split head dims pass the head check (the null q is what is refused)
+    assert _extend(lib, lq=192, lv=128) == pkx.PKX_EINVAL
+    assert b"q_extend" in lib.pkx_last_error_string()
+    assert _extend(lib, lq=288, lv=256, hq=16, hkv=1) == pkx.PKX_EINVAL
+    assert _extend(lib, lq=192, lv=256) == pkx.PKX_EUNSUPPORTED
     assert b"lq=192" in lib.pkx_last_error_string()
-    assert _extend(lib, lq=288, lv=256, hq=16, hkv=1) == pkx.PKX_EUNSUPPORTED
+    # an fp8 pool is built for Lq = Lv = 64 / 128 only
+    assert _extend(lib, lq=192, lv=128, kvd=1) == pkx.PKX_EUNSUPPORTED
     assert _extend(lib, hq=256, hkv=1) == pkx.PKX_EUNSUPPORTED
     assert _extend(lib, batch=-1) == pkx.PKX_EINVAL
     assert _extend(lib, scale=float("nan")) == pkx.PKX_EINVAL

@@ -43,7 +43,9 @@ class _Bar:
 
 
 class _Model:
-    def __init__(self, units, seed, mistake=None, fp8=False, f16_decode=False):
+    def __init__(self, units, seed, mistake=None, fp8=False, f16_decode=False,
+                 stages=(NK, NV, NI)):
+        self.NK, self.NV, self.NI = stages  # K, V and row-index ring depths
         self.rng = random.Random(seed)
         self.units = units
         self.mistake = mistake
@@ -60,7 +62,7 @@ class _Model:
         for s in range(RING):
             self.bars[f"UF{s}"] = _Bar(f"UF{s}", 1)
             self.bars[f"UE{s}"] = _Bar(f"UE{s}", 4)  # two warpgroups, MMA, copy
-        for pre, n in (("K", NK), ("V", NV), ("I", NI)):
+        for pre, n in (("K", self.NK), ("V", self.NV), ("I", self.NI)):
             for s in range(n):
                 self.bars[f"{pre}F{s}"] = _Bar(f"{pre}F{s}", 1)
                 self.bars[f"{pre}E{s}"] = _Bar(f"{pre}E{s}", 1)
@@ -136,9 +138,9 @@ class _Model:
             yield ("arrive", "Q_FULL")
             q_cnt += 1
             for _ in range(u["nt"]):
-                si = ic % NI
-                if ic >= NI:
-                    yield self._wait(f"IE{si}", ic // NI - 1)
+                si = ic % self.NI
+                if ic >= self.NI:
+                    yield self._wait(f"IE{si}", ic // self.NI - 1)
                 yield ("arrive", f"IF{si}")
                 ic += 1
 
@@ -154,17 +156,17 @@ class _Model:
             if op[1] is None:
                 return
             for _ in range(op[1]["nt"]):
-                si = ic % NI
-                yield self._wait(f"IF{si}", ic // NI)
+                si = ic % self.NI
+                yield self._wait(f"IF{si}", ic // self.NI)
                 yield ("arrive", f"IE{si}")
                 ic += 1
-                ks, vs = kc % NK, vc % NV
-                if kc >= NK:
-                    yield self._wait(f"KE{ks}", kc // NK - 1)
+                ks, vs = kc % self.NK, vc % self.NV
+                if kc >= self.NK:
+                    yield self._wait(f"KE{ks}", kc // self.NK - 1)
                 yield ("arrive", f"KF{ks}")
                 kc += 1
-                if vc >= NV and self.mistake != "V refilled before release":
-                    yield self._wait(f"VE{vs}", vc // NV - 1)
+                if vc >= self.NV and self.mistake != "V refilled before release":
+                    yield self._wait(f"VE{vs}", vc // self.NV - 1)
                 yield ("arrive", f"VF{vs}")
                 vc += 1
 
@@ -177,8 +179,8 @@ class _Model:
 
         def fetch():
             nonlocal ic
-            si = ic % NI
-            yield self._wait(f"IF{si}", ic // NI)
+            si = ic % self.NI
+            yield self._wait(f"IF{si}", ic // self.NI)
             yield ("arrive", f"IE{si}")
             ic += 1
 
@@ -197,8 +199,8 @@ class _Model:
             if nt == 0:
                 continue
             yield from fetch()
-            yield from issue("K", kc, NK)
-            yield from issue("V", vc, NV)
+            yield from issue("K", kc, self.NK)
+            yield from issue("V", vc, self.NV)
             if self.f16:
                 yield self._wait("Q_FULL", qc)
                 qc += 1
@@ -207,12 +209,12 @@ class _Model:
                 more = j + 1 < nt
                 if more:
                     yield from fetch()
-                    yield from issue("K", kc + 1, NK)
-                yield ("arrive", f"KF{kc % NK}")
+                    yield from issue("K", kc + 1, self.NK)
+                yield ("arrive", f"KF{kc % self.NK}")
                 kc += 1
                 if more:
-                    yield from issue("V", vc + 1, NV)
-                yield ("arrive", f"VF{vc % NV}")
+                    yield from issue("V", vc + 1, self.NV)
+                yield ("arrive", f"VF{vc % self.NV}")
                 vc += 1
 
     def _softmax(self, wg):
@@ -265,32 +267,32 @@ class _Model:
                 for j in range(nt):
                     b = j & 1
                     if j >= 2:
-                        vs = vc % NV
-                        yield self._wait(f"VF{vs}", vc // NV)
+                        vs = vc % self.NV
+                        yield self._wait(f"VF{vs}", vc // self.NV)
                         yield wait_p(b)
-                        yield ("use", f"VF{vs}", vc // NV)
+                        yield ("use", f"VF{vs}", vc // self.NV)
                         yield ("commit", f"VE{vs}")
                         vc += 1
-                    ks = kc % NK
-                    yield self._wait(f"KF{ks}", kc // NK)
-                    yield ("use", f"KF{ks}", kc // NK)
+                    ks = kc % self.NK
+                    yield self._wait(f"KF{ks}", kc // self.NK)
+                    yield ("use", f"KF{ks}", kc // self.NK)
                     yield ("commit", f"S{b}")
                     yield ("commit", f"KE{ks}")
                     kc += 1
                     if j == nt - 1 and self.mistake != "no Q release":
                         yield ("commit", "Q_EMPTY")
                 for j in range(max(nt - 2, 0), nt):
-                    vs = vc % NV
-                    yield self._wait(f"VF{vs}", vc // NV)
+                    vs = vc % self.NV
+                    yield self._wait(f"VF{vs}", vc // self.NV)
                     yield wait_p(j & 1)
-                    yield ("use", f"VF{vs}", vc // NV)
+                    yield ("use", f"VF{vs}", vc // self.NV)
                     yield ("commit", f"O{j & 1}")
                     yield ("commit", f"VE{vs}")
                     vc += 1
                 continue
             q1 = u["kind"] == "dual"
-            ks = kc % NK
-            yield self._wait(f"KF{ks}", kc // NK)
+            ks = kc % self.NK
+            yield self._wait(f"KF{ks}", kc // self.NK)
             yield ("commit", "S0")
             if q1:
                 yield ("commit", "S1")
@@ -299,12 +301,12 @@ class _Model:
             if nt == 1:
                 yield ("commit", "Q_EMPTY")
             for j in range(1, nt):
-                ks, vs = kc % NK, vc % NV
-                yield self._wait(f"KF{ks}", kc // NK)
-                yield self._wait(f"VF{vs}", vc // NV)
+                ks, vs = kc % self.NK, vc % self.NV
+                yield self._wait(f"KF{ks}", kc // self.NK)
+                yield self._wait(f"VF{vs}", vc // self.NV)
                 yield wait_p(0)
-                yield ("use", f"KF{ks}", kc // NK)
-                yield ("use", f"VF{vs}", vc // NV)
+                yield ("use", f"KF{ks}", kc // self.NK)
+                yield ("use", f"VF{vs}", vc // self.NV)
                 yield ("commit", "S0")
                 if q1:
                     yield wait_p(1)
@@ -315,10 +317,10 @@ class _Model:
                 kc += 1
                 if j == nt - 1:
                     yield ("commit", "Q_EMPTY")
-            vs = vc % NV
-            yield self._wait(f"VF{vs}", vc // NV)
+            vs = vc % self.NV
+            yield self._wait(f"VF{vs}", vc // self.NV)
             yield wait_p(0)
-            yield ("use", f"VF{vs}", vc // NV)
+            yield ("use", f"VF{vs}", vc // self.NV)
             yield ("commit", "O0")
             if q1:
                 yield wait_p(1)
@@ -353,6 +355,18 @@ def test_fp8_protocols_have_no_deadlock_and_no_parity_aliasing():
 
 def test_protocol_has_no_deadlock_and_no_parity_aliasing():
     _trials(150)
+
+
+@pytest.mark.parametrize("stages", [(2, 2, 3), (1, 1, 3)])
+def test_split_head_dim_protocol(stages):
+    """The split head dims (Lq / Lv = 192 / 128 with two K and two V stages,
+    288 / 256 with one of each): every unit has one query tile and one key
+    stream (warpgroup 1 idles), so only "one" units occur."""
+    rng = random.Random(7)
+    for t in range(200):
+        units = [{"kind": "one", "nt": rng.choice([0, 1, 2, 3, 5, 8])}
+                 for _ in range(rng.randint(1, 12))]
+        _Model(units, seed=t, stages=stages).run()
 
 
 @pytest.mark.parametrize("mistake", ["shared P counter", "no Q release",

@@ -601,3 +601,80 @@ def test_full_size_decode_mla():
     assert pkx.workspace_status(ws) == 0
     ro, rl = oracle_decode(wl)
     assert_close(o, lse, ro, rl, "decode_mla")
+
+
+# ---------------------------------------------------- split head dims
+SPLIT_SMALL = [
+    # (lq, lv, hq, hkv, prefix, extend, cap, window)
+    (192, 128, 16, 16, [0, 70, 300], [9, 1, 130], 0.0, -1),
+    (192, 128, 32, 8, [129, 5, 1000], [17, 300, 3], 20.0, -1),
+    (192, 128, 16, 2, [33, 0, 700], [64, 200, 1], 0.0, 50),
+    (288, 256, 16, 16, [0, 70, 300], [9, 1, 130], 0.0, -1),
+    (288, 256, 16, 4, [129, 5, 600], [17, 250, 3], 30.0, 100),
+    (288, 256, 8, 1, [0, 257], [300, 40], 0.0, -1),
+]
+
+
+@pytest.mark.parametrize("lq,lv,hq,hkv,prefix,extend,cap,window", SPLIT_SMALL)
+def test_split_head_dims_vs_oracle(lq, lv, hq, hkv, prefix, extend, cap, window):
+    """The split head dims of the pages' launcher (Lq = 192 = 128 + 64 and
+    Lq = 288 = 256 + 32, with Lv = 128 / 256): two-stage and unified extend
+    against the oracle over ragged batches with tails, GQA groups, cap and
+    window."""
+    spec = W.small_spec(batch=len(prefix), hq=hq, hkv=hkv, lq=lq, lv=lv, prefix=prefix,
+                        extend=extend, logit_cap=cap, sliding_window=window,
+                        seed=lq + sum(prefix) + 3 * sum(extend))
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    ro, rl = oracle_extend(wl)
+    o, lse, ws = dw.extend()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    assert_close(o, lse, ro, rl, f"{lq}/{lv} two-stage")
+    uo, ul, ws2 = dw.unified()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws2) == 0
+    assert_close(uo, ul, ro, rl, f"{lq}/{lv} unified")
+
+
+@pytest.mark.parametrize("lq,lv", [(192, 128), (288, 256)])
+def test_split_head_dims_decode_vs_oracle(lq, lv):
+    lens = [1, 64, 129, 1000, 3, 4097]
+    spec = W.WorkloadSpec("dec", batch=len(lens), hq=16, hkv=4, lq=lq, lv=lv,
+                          prefix=[x - 1 for x in lens], extend=[1] * len(lens),
+                          num_slots=16384, seed=lq + 11, decode=True)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.decode()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_decode(wl)
+    assert_close(o, lse, ro, rl, f"{lq}/{lv} decode")
+
+
+@pytest.mark.parametrize("name", ["split_192", "split_288"])
+def test_full_size_split_head_dims_sampled_rows(name):
+    """The split-head-dim workloads at full size through the unified call the
+    benchmark times (GPU-built indices); 2048 sampled rows against the
+    oracle."""
+    wl = W.draw(W.SPECS[name])
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.unified()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    rows = sample_rows(wl.n_q_tokens, wl.spec.hq, 2048, seed=81)
+    ro, rl = oracle_extend(wl, rows=rows)
+    go = o.view(-1, o.shape[-1])[rows.to(DEV)]
+    gl = lse.view(-1)[rows.to(DEV)]
+    assert_close(go, gl, ro, rl, name)
+    assert torch.isfinite(o.float()).all()
+
+
+def test_split_head_dims_refuse_mask_and_fp8():
+    spec = W.small_spec(batch=1, hq=8, hkv=2, lq=192, lv=128, prefix=[4], extend=[4], seed=3)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    mask, mptr = random_masks(wl, seed=1)
+    with pytest.raises(pkx.PkxError) as e:
+        dw.extend(custom_mask=mask, mask_indptr=mptr)
+    assert e.value.code == pkx.PKX_EUNSUPPORTED
