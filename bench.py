@@ -735,6 +735,51 @@ def measure_split(dev, flush, steps, bf16_peak, name="llama3_8b"):
     return out
 
 
+def measure_fused_write(dev, flush, steps, bf16_peak, name="llama3_8b"):
+    """The two-stage extend call with the KV write fused in (the new tokens'
+    K/V rows stored into the pool by the attention kernel's otherwise idle
+    warps) against the standalone KV write followed by the two-stage call,
+    on the same batch: device time of the whole sequence."""
+    from paged_kv_extend_gb300 import pkx
+    wl = W.draw(W.SPECS[name])
+    s = wl.spec
+    kb, vb = wl.pool(dev)
+    k_ext, v_ext = wl.extend_kv(dev)
+    q, qo = wl.q.to(dev), wl.qo_indptr.to(dev)
+    kvp, kvi = wl.kv_indptr.to(dev), wl.kv_indices.to(dev)
+    loc = wl.extend_kv_indices.to(dev, torch.int64)
+    n = wl.n_q_tokens
+    o = torch.empty(n, s.hq, s.lv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(n, s.hq, dtype=torch.float32, device=dev)
+    ws2 = torch.empty(pkx.extend_workspace_size(wl.batch, n, s.hq, s.hkv, s.lq, s.lv),
+                      dtype=torch.uint8, device=dev)
+    args = (q, k_ext, v_ext, o, kb, vb, qo, kvp, kvi, wl.sm_scale, s.logit_cap, s.sliding_window)
+    flops = extend_flops(wl)
+
+    def standalone():
+        pkx.set_kv_buffer(kb, vb, loc, k_ext, v_ext)
+        pkx.extend_attention_fwd(*args, lse=lse, workspace=ws2)
+
+    def fused():
+        pkx.extend_attention_fwd(*args, lse=lse, workspace=ws2, cache_loc=loc)
+
+    out = {}
+    for label, fn in (("write_then_extend", standalone), ("fused_write_extend", fused)):
+        ms = time_launches(fn, steps, flush, dev)
+        if pkx.workspace_status(ws2) != 0:
+            raise SystemExit(f"{label}: device status {pkx.workspace_status(ws2)}")
+        out[f"{label}/{name}"] = {
+            "what": ("set_kv_buffer of the extend rows, then the two-stage call"
+                     if label == "write_then_extend" else
+                     "the two-stage call with cache_loc (KV write inside the attention kernel)"),
+            "ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
+            "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / bf16_peak,
+            "algorithmic_flops": flops}
+    del kb, vb, k_ext, v_ext, ws2
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, ws, rank, local):
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the CUDA library has no CPU path)")
@@ -786,8 +831,8 @@ def run_ours(args, ws, rank, local):
     if not args.no_components:
         names = (args.components.split(",") if args.components
                  else ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla",
-                       "split_192", "split_288", "kv_ops", "split", "decode_gqa_fp8",
-                       "llama3_8b_fp8"])
+                       "split_192", "split_288", "kv_ops", "split", "fused_write",
+                       "decode_gqa_fp8", "llama3_8b_fp8"])
         if args.all_workloads:
             names = ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla", "kv_ops",
                      "split", "decode_gqa_fp8", "long_prefix_fp8", "llama3_8b_fp8"]
@@ -802,6 +847,10 @@ def run_ours(args, ws, rank, local):
             if name == "split":
                 components.update(measure_split(dev, flush, max(5, min(args.steps, 20)),
                                                 bf16_peak))
+                continue
+            if name == "fused_write":
+                components.update(measure_fused_write(dev, flush, max(5, min(args.steps, 20)),
+                                                      bf16_peak))
                 continue
             if name == "kv_ops":
                 components.update(measure_kv_ops(dev, flush, max(5, min(args.steps, 50)),

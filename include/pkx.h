@@ -181,8 +181,9 @@ void pkx_set_stall_injection(int on);
  *   kv_dtype, k_scale, v_scale  the pool's format and scales (PKX_KV_*)
  *   lse_out    nullable fp32 [num_q_tokens, hq] (natural log)
  *   workspace  >= pkx_extend_workspace_size(...) bytes
- * Supported (lq, lv): (64, 64), (128, 128), (576, 512); hq % hkv == 0 and
- * hq / hkv <= 128.
+ * Supported (lq, lv): (64, 64), (128, 128), (576, 512), and the split head
+ * dims (192, 128) and (288, 256) (no custom mask and no fp8 pool for those);
+ * hq % hkv == 0 and hq / hkv <= 128.
  */
 int pkx_extend_attention_fwd(
     const void *q_extend, const void *k_extend, const void *v_extend,
@@ -195,6 +196,38 @@ int pkx_extend_attention_fwd(
     const uint8_t *custom_mask, const int32_t *mask_indptr, const float *sinks,
     int kv_dtype, float k_scale, float v_scale, float *lse_out,
     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Extend attention, two-stage form, with the KV write fused in.
+ * Source: sglang flashinfer_backend.py, forward_extend: the new tokens' K
+ * and V rows are saved into the pool (token_to_kv_pool.set_kv_buffer(layer,
+ * cache_loc, k, v, ...)) before attention runs.  This call computes what
+ * pkx_set_kv_buffer (or pkx_set_kv_buffer_fp8 for an fp8 pool) followed by
+ * pkx_extend_attention_fwd computes:
+ *   k_buffer[cache_loc[t], h, :] = k_extend[t, h, :]  and likewise for v
+ * for every extend token t < num_q_tokens and KV head h, and the same o_extend
+ * and lse.  Arguments as pkx_extend_attention_fwd, with the pools writable and
+ *   cache_loc  int64 [num_q_tokens] pool slot of each extend token; the slots
+ *              are the new tokens' own, so none of them appears among the
+ *              prefix indices (kv_indices).  A slot outside the pool is
+ *              skipped.
+ * For a bf16 pool with Lq = Lv (64, 128) or the split head dims the attention
+ * kernel does the write itself (idle warps copy each unit's own tokens'
+ * rows, beside the attention); for the MLA pool (only K rows are written)
+ * and fp8 pools the standalone write kernel runs first on the stream.
+ */
+int pkx_extend_attention_fwd_kv_write(
+    const void *q_extend, const void *k_extend, const void *v_extend,
+    void *o_extend, void *k_buffer, void *v_buffer,
+    const int32_t *qo_indptr, const int32_t *kv_indptr,
+    const int32_t *kv_indices, int batch, int num_q_tokens, int hq, int hkv,
+    int lq, int lv, int64_t ke_st, int64_t ke_sh, int64_t ve_st,
+    int64_t ve_sh, int64_t kb_ss, int64_t kb_sh, int64_t vb_ss, int64_t vb_sh,
+    int64_t num_slots, float sm_scale, float logit_cap, int sliding_window,
+    const uint8_t *custom_mask, const int32_t *mask_indptr, const float *sinks,
+    int kv_dtype, float k_scale, float v_scale, float *lse_out,
+    const int64_t *cache_loc, void *workspace, size_t workspace_bytes,
+    void *stream);
 
 /*
  * Extend attention, ragged + paged split.

@@ -244,6 +244,46 @@ int pkx_extend_attention_fwd(const void *q_extend, const void *k_extend, const v
   return launch_attention(a);
 }
 
+int pkx_extend_attention_fwd_kv_write(
+    const void *q_extend, const void *k_extend, const void *v_extend, void *o_extend,
+    void *k_buffer, void *v_buffer, const int32_t *qo_indptr, const int32_t *kv_indptr,
+    const int32_t *kv_indices, int batch, int num_q_tokens, int hq, int hkv, int lq, int lv,
+    int64_t ke_st, int64_t ke_sh, int64_t ve_st, int64_t ve_sh, int64_t kb_ss, int64_t kb_sh,
+    int64_t vb_ss, int64_t vb_sh, int64_t num_slots, float sm_scale, float logit_cap,
+    int sliding_window, const uint8_t *custom_mask, const int32_t *mask_indptr,
+    const float *sinks, int kv_dtype, float k_scale, float v_scale, float *lse_out,
+    const int64_t *cache_loc, void *workspace, size_t workspace_bytes, void *stream) {
+  AttnArgs a{};
+  bool done;
+  int rc = two_stage_args(a, q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffer,
+                          qo_indptr, kv_indptr, kv_indices, batch, num_q_tokens, hq, hkv, lq, lv,
+                          ke_st, ke_sh, ve_st, ve_sh, kb_ss, kb_sh, vb_ss, vb_sh, num_slots,
+                          sm_scale, logit_cap, sliding_window, custom_mask, mask_indptr, sinks,
+                          kv_dtype, k_scale, v_scale, lse_out, &done);
+  if (rc != PKX_OK || done) return rc;
+  if (!cache_loc || !aligned(cache_loc, 8))
+    return set_error(PKX_EINVAL, "cache_loc null or misaligned");
+  a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  const bool mla = lq == 576 && lv == 512;
+  if (mla || kv_dtype != kKvBf16) {
+    // not fused for these pools: the standalone write first, as the pages
+    // order it (the MLA pool stores only the K row; V is its first 512 dims)
+    rc = kv_dtype != kKvBf16
+             ? pkx_set_kv_buffer_fp8(k_extend, ke_st, ke_sh, mla ? nullptr : v_extend, ve_st,
+                                     ve_sh, cache_loc, num_q_tokens, hkv, lq, lv, k_scale,
+                                     v_scale, kv_dtype, k_buffer, kb_ss, kb_sh, v_buffer, vb_ss,
+                                     vb_sh, num_slots, stream)
+             : pkx_set_kv_buffer(k_extend, ke_st, ke_sh, nullptr, ve_st, ve_sh, cache_loc,
+                                 num_q_tokens, hkv, lq, lv, k_buffer, kb_ss, kb_sh, v_buffer,
+                                 vb_ss, vb_sh, num_slots, stream);
+    if (rc != PKX_OK) return rc;
+    return launch_attention(a);
+  }
+  a.cache_loc = cache_loc;
+  return launch_attention(a);
+}
+
 size_t pkx_ragged_paged_workspace_size(int batch, int num_q_tokens, int hq, int hkv, int lq,
                                        int lv) {
   if (batch < 0 || num_q_tokens < 0 || hkv <= 0 || hq <= 0 || hq % hkv || hq / hkv > kBlockM ||

@@ -514,6 +514,10 @@ struct KParams {
   int32_t *next_unit;     // claim counter over uorder (zeroed by the scheduler)
   int32_t *status;
   float *plse, *po;
+  // two-stage form with the fused KV write: the pool slot of each extend
+  // token (nullable), and the pools as writable pointers
+  const int64_t *cache_loc;
+  bf16 *k_pool_w, *v_pool_w;
   uint64_t wait_ns;       // time limit of every bounded wait
   int stall;              // test hook: the softmax warps first wait on a barrier
                           // no thread arrives at, so that the limit runs out
@@ -731,6 +735,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  const bool kv_write = MODE == kTwoStage && p.cache_loc != nullptr;
 
   if (tid == 0) {
     mbar_init(&bars[B_Q_FULL], 1);
@@ -745,7 +750,9 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     mbar_init(&bars[B_NEVER], 1);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(&bars[B_U_FULL + i], 1);
-      mbar_init(&bars[B_U_EMPTY + i], 8 + 1 + C::COPY_THREADS / 32);
+      // softmax, MMA and copy warps (+ the two writer warps with the fused
+      // KV write)
+      mbar_init(&bars[B_U_EMPTY + i], 8 + 1 + C::COPY_THREADS / 32 + (kv_write ? 2 : 0));
     }
     for (int s = 0; s < C::NK; ++s) {
       mbar_init(&k_full[s], C::COPY_THREADS);
@@ -1642,6 +1649,56 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     }
     if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
     cp_async_wait_all();
+  } else if (kv_write) {
+    // ------------------------------------------ fused KV write (warps 14-15)
+    // The pages store the new tokens' K/V rows in the pool before attending
+    // (set_kv_buffer(layer, cache_loc, k, v)).  The two-stage form reads the
+    // extend keys from k_extend / v_extend, so the store can run beside the
+    // attention: each unit copies the rows of its own tokens whose key
+    // positions lie in its key range (split-KV units of one block cover
+    // disjoint ranges, so every (token, KV head) row is written once).  A
+    // slot outside the pool is skipped.
+    constexpr int CK = C::LQ / 8, CV = C::HDV / 8;  // 16-byte chunks of a K / V row
+    const int wt = tid - 14 * 32;                    // 0 .. 63
+    bool ok = true;
+    for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+      const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ok, p.wait_ns);
+      if (u < 0) break;
+      const WorkUnit w = p.units[p.uorder[u]];
+      const int t0 = max(w.k_begin, w.qpos0) - w.qpos0;
+      const int t1 = min(w.k_end, w.qpos0 + w.n_tok) - w.qpos0;
+      const int n = (t1 - t0) * (CK + CV);
+      const bf16 *kx = p.k_ext + (int64_t)w.kvh * p.ke_sh;
+      const bf16 *vx = p.v_ext + (int64_t)w.kvh * p.ve_sh;
+      bf16 *kp = p.k_pool_w + (int64_t)w.kvh * p.kb_sh;
+      bf16 *vp = p.v_pool_w + (int64_t)w.kvh * p.vb_sh;
+      // four chunks in flight per thread: loads first, then the stores
+      for (int c0 = wt; c0 < n; c0 += 4 * 64) {
+        uint4 v[4];
+        bf16 *dst[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = c0 + k * 64;
+          dst[k] = nullptr;
+          if (c < n) {
+            const int t = t0 + c / (CK + CV), ch = c % (CK + CV);
+            const int64_t row = w.q_tok0 + t;
+            const int64_t slot = __ldg(p.cache_loc + row);
+            if (slot >= 0 && slot < p.num_slots) {
+              const bool is_k = ch < CK;
+              const int e = (is_k ? ch : ch - CK) * 8;
+              v[k] = __ldg(reinterpret_cast<const uint4 *>(
+                  (is_k ? kx + row * p.ke_st : vx + row * p.ve_st) + e));
+              dst[k] = (is_k ? kp + slot * p.kb_ss : vp + slot * p.vb_ss) + e;
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (dst[k]) *reinterpret_cast<uint4 *>(dst[k]) = v[k];
+      }
+    }
+    if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
   }
   }
 
@@ -2018,6 +2075,9 @@ int launch_attention(const AttnArgs &a) {
   kp.plse = reinterpret_cast<float *>(ws + L.plse_off);
   kp.po = reinterpret_cast<float *>(ws + L.po_off);
   wait_settings(&kp.wait_ns, &kp.stall);
+  kp.cache_loc = a.cache_loc;
+  kp.k_pool_w = static_cast<bf16 *>(const_cast<void *>(a.k_buf));
+  kp.v_pool_w = static_cast<bf16 *>(const_cast<void *>(a.v_buf));
 
   const int grid = nsm;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;

@@ -149,6 +149,7 @@ struct AttnArgs {
   float k_scale = 1.f, v_scale = 1.f;  // fp8 pool: key = code * k_scale, value = code * v_scale
   int key_set = kAllKeys;       // two-stage form: which keys this pass sees
   int keep_status = 0;          // a later pass of one call keeps the status word
+  const int64_t *cache_loc = nullptr;  // two-stage: fused KV write of the extend rows
   void *workspace;
   size_t workspace_bytes;
   cudaStream_t stream;

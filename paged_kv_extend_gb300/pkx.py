@@ -53,6 +53,10 @@ _SIGS = {
         _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
         _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _p,
         _i, _f, _f, _p, _p, _sz, _p]),
+    "pkx_extend_attention_fwd_kv_write": (_i, [
+        _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
+        _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f, _f, _i, _p, _p, _p,
+        _i, _f, _f, _p, _p, _p, _sz, _p]),
     "pkx_ragged_paged_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "pkx_extend_attention_fwd_ragged_paged": (_i, [
         _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
@@ -257,11 +261,15 @@ def _workspace(ws, nbytes, dev):
 def extend_attention_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buffer,
                          qo_indptr, kv_indptr, kv_indices, sm_scale=None, logit_cap=0.0,
                          sliding_window=-1, lse=None, workspace=None, custom_mask=None,
-                         mask_indptr=None, sinks=None, k_scale=1.0, v_scale=1.0):
+                         mask_indptr=None, sinks=None, k_scale=1.0, v_scale=1.0,
+                         cache_loc=None):
     """Two-stage extend attention (pkx_extend_attention_fwd); writes o_extend
     (and lse if given) in place.  Returns the workspace used.  custom_mask /
     mask_indptr / sinks as in the C header.  The pool may be fp8
-    (torch.float8_e4m3fn / float8_e5m2) with k_scale / v_scale."""
+    (torch.float8_e4m3fn / float8_e5m2) with k_scale / v_scale.  With
+    ``cache_loc`` (int64 [tokens], each extend token's pool slot) the call
+    also stores k_extend / v_extend into the pool at those slots
+    (pkx_extend_attention_fwd_kv_write)."""
     lib = load_library()
     n, hq, lq = q_extend.shape
     hkv = k_buffer.shape[1]
@@ -280,15 +288,22 @@ def extend_attention_fwd(q_extend, k_extend, v_extend, o_extend, k_buffer, v_buf
             raise ValueError(f"{nm} must be contiguous bf16")
     _i32(qo_indptr, "qo_indptr"), _i32(kv_indptr, "kv_indptr"), _i32(kv_indices, "kv_indices")
     ws = _workspace(workspace, extend_workspace_size(batch, n, hq, hkv, lq, lv), q_extend.device)
-    _check(_on(
-        q_extend.device, lib.pkx_extend_attention_fwd,
+    args = [
         _ptr(q_extend), _ptr(k_extend), _ptr(v_extend), _ptr(o_extend), _ptr(k_buffer),
         _ptr(v_buffer), _ptr(qo_indptr), _ptr(kv_indptr),
         _ptr(kv_indices) if kv_indices.numel() else None, batch, n, hq, hkv, lq, lv,
         ke[0], ke[1], ve[0], ve[1], kb[0], kb[1], vb[0], vb[1], k_buffer.shape[0],
         float(sm_scale or 0.0), float(logit_cap or 0.0), int(sliding_window),
         *_mask_sinks(custom_mask, mask_indptr, sinks), kv_dtype, float(k_scale), float(v_scale),
-        _ptr(lse), _ptr(ws), ws.numel() * ws.element_size()))
+        _ptr(lse)]
+    if cache_loc is None:
+        _check(_on(q_extend.device, lib.pkx_extend_attention_fwd, *args, _ptr(ws),
+                   ws.numel() * ws.element_size()))
+    else:
+        _i64_vec(cache_loc, "cache_loc")
+        _check_len(cache_loc, n, "cache_loc")
+        _check(_on(q_extend.device, lib.pkx_extend_attention_fwd_kv_write, *args,
+                   _ptr(cache_loc) if n else None, _ptr(ws), ws.numel() * ws.element_size()))
     return ws
 
 

@@ -4,6 +4,7 @@ called through the C ABI, against the oracle.  Both are integer / byte work:
 the bar is bit-exact.
 """
 import json
+import math
 import os
 
 import pytest
@@ -317,3 +318,118 @@ def test_decode_through_a_page_table():
     want_o, want_l = oracle.decode_attention(wl.q, ko, vo, wl.kv_indptr, wl.kv_indices,
                                              wl.sm_scale)
     assert_close(o.cpu(), lse.cpu(), want_o, want_l)
+
+
+# ------------------------------------------------ KV write fused into extend
+FUSED = [
+    # (lq, lv, hq, hkv, prefix, extend) -- long prefixes make split-KV blocks
+    (128, 128, 32, 8, [0, 1500, 300, 9000], [200, 64, 1, 130]),
+    (64, 64, 12, 3, [999, 45, 0], [500, 2, 129]),
+    (192, 128, 16, 4, [700, 33], [150, 64]),
+    (288, 256, 16, 4, [129, 5], [70, 250]),
+]
+
+
+def _fused_case(wl, dev, fp8=None, scale=1.0):
+    """Pool with the extend slots overwritten by stale rows; the fused call;
+    returns (pool k, pool v, o, lse, ws) on the device and the oracle's
+    expected pools."""
+    k_ext, v_ext = wl.extend_kv()
+    loc = wl.extend_kv_indices.to(torch.int64)
+    if fp8 is None:
+        kb, vb = wl.pool()
+        kb = kb.clone()
+        vb = vb if wl.spec.v_aliases_k else vb.clone()
+        g = torch.Generator().manual_seed(3)
+        kb[loc] = torch.randn(kb[loc].shape, generator=g).to(torch.bfloat16)
+        if not wl.spec.v_aliases_k:
+            vb[loc] = torch.randn(vb[loc].shape, generator=g).to(torch.bfloat16)
+        else:
+            vb = kb[..., : wl.spec.lv]
+        want_k, want_v = oracle.set_kv_buffer(kb, vb, loc, k_ext,
+                                              None if wl.spec.v_aliases_k else v_ext)
+    else:
+        kb, vb = wl.pool_fp8(fp8, scale, scale)
+        kb.view(torch.uint8)[loc] = 0
+        vb.view(torch.uint8)[loc] = 0
+        want_k, want_v = oracle.set_kv_buffer_fp8(kb, vb, loc, k_ext, v_ext, scale, scale)
+    dkb = kb.to(dev)
+    dvb = dkb[..., : wl.spec.lv] if wl.spec.v_aliases_k else vb.to(dev)
+    n = wl.n_q_tokens
+    o = torch.full((n, wl.spec.hq, wl.spec.lv), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((n, wl.spec.hq), float("nan"), dtype=torch.float32, device=dev)
+    kw = {} if fp8 is None else {"k_scale": scale, "v_scale": scale}
+    dke = k_ext.to(dev)
+    dve = dke[..., : wl.spec.lv] if wl.spec.v_aliases_k else v_ext.to(dev)
+    ws = pkx.extend_attention_fwd(wl.q.to(dev), dke, dve, o, dkb, dvb,
+                                  wl.qo_indptr.to(dev), wl.kv_indptr.to(dev),
+                                  wl.kv_indices.to(dev), wl.sm_scale, wl.spec.logit_cap,
+                                  wl.spec.sliding_window, lse=lse, cache_loc=loc.to(dev), **kw)
+    torch.cuda.synchronize()
+    return dkb, dvb, o, lse, ws, want_k, want_v
+
+
+@pytest.mark.parametrize("lq,lv,hq,hkv,prefix,extend", FUSED)
+def test_fused_kv_write_bit_exact_and_attention(lq, lv, hq, hkv, prefix, extend):
+    """The two-stage call with cache_loc: the pool afterwards equals the
+    oracle's set_kv_buffer bit for bit (every new row written once, nothing
+    else touched), and o / lse match the oracle's two-stage attention."""
+    from gpu_cases import assert_close, oracle_extend
+    wl = W.draw(W.small_spec(batch=len(prefix), hq=hq, hkv=hkv, lq=lq, lv=lv, prefix=prefix,
+                             extend=extend, seed=lq + sum(extend)))
+    dkb, dvb, o, lse, ws, want_k, want_v = _fused_case(wl, DEV)
+    assert pkx.workspace_status(ws) == 0
+    assert torch.equal(dkb.cpu(), want_k)
+    assert torch.equal(dvb.cpu(), want_v)
+    ro, rl = oracle_extend(wl)
+    assert_close(o, lse, ro, rl, f"fused {lq}/{lv}")
+
+
+def test_fused_kv_write_mla_and_fp8_fall_back_to_the_standalone_write():
+    from gpu_cases import assert_close, oracle_extend
+    spec = W.small_spec(batch=2, hq=16, hkv=1, lq=576, lv=512, prefix=[300, 20], extend=[40, 70],
+                        std=0.5, v_aliases_k=True, sm_scale=1.0 / math.sqrt(192.0), seed=9)
+    wl = W.draw(spec)
+    dkb, dvb, o, lse, ws, want_k, _ = _fused_case(wl, DEV)
+    assert pkx.workspace_status(ws) == 0
+    assert torch.equal(dkb.cpu(), want_k)
+    ro, rl = oracle_extend(wl)
+    assert_close(o, lse, ro, rl, "fused mla")
+    wl = W.draw(W.small_spec(batch=2, hq=8, hkv=2, lq=128, lv=128, prefix=[300, 20],
+                             extend=[40, 70], seed=10))
+    dkb, dvb, o, lse, ws, want_k, want_v = _fused_case(wl, DEV, fp8=torch.float8_e4m3fn,
+                                                       scale=0.5)
+    assert pkx.workspace_status(ws) == 0
+    assert torch.equal(dkb.cpu().view(torch.uint8), want_k.view(torch.uint8))
+    assert torch.equal(dvb.cpu().view(torch.uint8), want_v.view(torch.uint8))
+    k_ext, v_ext = wl.extend_kv()
+    ro, rl = oracle.extend_attention(wl.q, k_ext, v_ext, want_k, want_v, wl.qo_indptr,
+                                     wl.kv_indptr, wl.kv_indices, wl.sm_scale, k_scale=0.5,
+                                     v_scale=0.5)
+    assert_close(o, lse, ro, rl, "fused fp8")
+
+
+def test_fused_kv_write_full_size():
+    """llama3_8b: the pool's extend slots are cleared, the fused call writes
+    them back; the pool equals the workload's full pool bit for bit, and 2048
+    sampled rows of o match the oracle."""
+    from gpu_cases import assert_close, oracle_extend, sample_rows
+    wl = W.draw(W.SPECS["llama3_8b"])
+    kb, vb = wl.pool(DEV)
+    full_k, full_v = kb.clone(), vb.clone()
+    loc = wl.extend_kv_indices.to(torch.int64).to(DEV)
+    kb[loc] = 0
+    vb[loc] = 0
+    k_ext, v_ext = wl.extend_kv(DEV)
+    n = wl.n_q_tokens
+    o = torch.empty(n, 32, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(n, 32, dtype=torch.float32, device=DEV)
+    ws = pkx.extend_attention_fwd(wl.q.to(DEV), k_ext, v_ext, o, kb, vb, wl.qo_indptr.to(DEV),
+                                  wl.kv_indptr.to(DEV), wl.kv_indices.to(DEV), wl.sm_scale,
+                                  lse=lse, cache_loc=loc)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    assert torch.equal(kb, full_k) and torch.equal(vb, full_v)
+    rows = sample_rows(n, 32, 2048, seed=82)
+    ro, rl = oracle_extend(wl, rows=rows)
+    assert_close(o.view(-1, 128)[rows.to(DEV)], lse.view(-1)[rows.to(DEV)], ro, rl, "fused full")
