@@ -904,7 +904,7 @@ def run_ours(args, ws, rank, local):
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak,
                 "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": traffic,
                 "peak_source": f"bf16_tflops burst, of {peak_src}",
-                "kernel": "mla_kernel<unified>" if wl.spec.lq == 576 else "attn_kernel<unified>",
+                "kernel": "mla_pair_kernel<unified>" if wl.spec.lq == 576 else "attn_kernel<unified>",
                 "algorithmic_flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": step.bytes}
         e2e_value = flops * ws / (e2e_ms * 1e-3) / 1e12

@@ -43,32 +43,38 @@ def needs_build() -> bool:
     return any(os.path.getmtime(f) > t for f in srcs + hdrs + [__file__])
 
 
+# Kernels that hand registers between warpgroups with setmaxnreg, and the
+# source file that states the launch register count the split assumes.
+SPLIT_KERNELS = (("attn_kernel", "attention.cu"), ("mla_pair_kernel", "mla_pair_kernel.cuh"))
+
+
 def check_attention_registers(ptxas_log: str) -> None:
-    """The attention kernel hands registers between warpgroups with
+    """The attention kernels hand registers between warpgroups with
     setmaxnreg; the split adds up only if every instantiation launches with
     exactly the register count the kernel source assumes (REGS_LAUNCH).
     Refuse to build otherwise: a wrong split would stall the kernel."""
-    src = open(os.path.join(CSRC, "attention.cu")).read()
-    m = re.search(r"REGS_LAUNCH = (\d+)", src)
-    if not m:
-        raise RuntimeError("attention.cu: REGS_LAUNCH not found")
-    want = int(m.group(1))
-    found = 0
-    current = None
-    for line in ptxas_log.splitlines():
-        fm = re.search(r"Compiling entry function '(\S+)'", line) or \
-            re.search(r"Function properties for (\S+)", line)
-        if fm:
-            current = fm.group(1)
-        rm = re.search(r"Used (\d+) registers", line)
-        if rm and current and "attn_kernel" in current:
-            found += 1
-            if int(rm.group(1)) != want:
-                raise RuntimeError(
-                    f"{current} uses {rm.group(1)} registers at launch, the register split "
-                    f"assumes {want}; not building")
-    if found == 0:
-        raise RuntimeError("no attn_kernel register report from ptxas; not building")
+    for kernel, fname in SPLIT_KERNELS:
+        src = open(os.path.join(CSRC, fname)).read()
+        m = re.search(r"REGS_LAUNCH = (\d+)", src)
+        if not m:
+            raise RuntimeError(f"{fname}: REGS_LAUNCH not found")
+        want = int(m.group(1))
+        found = 0
+        current = None
+        for line in ptxas_log.splitlines():
+            fm = re.search(r"Compiling entry function '(\S+)'", line) or \
+                re.search(r"Function properties for (\S+)", line)
+            if fm:
+                current = fm.group(1)
+            rm = re.search(r"Used (\d+) registers", line)
+            if rm and current and kernel in current:
+                found += 1
+                if int(rm.group(1)) != want:
+                    raise RuntimeError(
+                        f"{current} uses {rm.group(1)} registers at launch, the register "
+                        f"split assumes {want}; not building")
+        if found == 0:
+            raise RuntimeError(f"no {kernel} register report from ptxas; not building")
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

@@ -1126,7 +1126,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       constexpr uint32_t K_LO = sw128_desc_lo(0), K_HI = sw128_desc_hi(1024);
       constexpr uint32_t V_LO = sw128_desc_lo(C::BN * 128), V_HI = sw128_desc_hi(1024);
       auto issue_s = [&](int qt, uint32_t sK) {
-        const uint32_t a_lo = K_LO | ((qt ? sQ1 : sQ0) >> 4), b_lo = K_LO | (sK >> 4);
+        const uint32_t a_lo = K_LO | desc_addr(qt ? sQ1 : sQ0), b_lo = K_LO | desc_addr(sK);
         const uint32_t d = tmem + qt * C::BN;
         static_for<0, C::LQ / 16>([&](auto kk_c) {
           constexpr int kk = decltype(kk_c)::value;
@@ -1138,7 +1138,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       };
       // S of query tile 0 into S/P buffer `buf` (the decode streams)
       auto issue_s_q0 = [&](int buf, uint32_t sK) {
-        const uint32_t a_lo = K_LO | (sQ0 >> 4), b_lo = K_LO | (sK >> 4);
+        const uint32_t a_lo = K_LO | desc_addr(sQ0), b_lo = K_LO | desc_addr(sK);
         const uint32_t d = tmem + buf * C::BN;
         static_for<0, C::LQ / 16>([&](auto kk_c) {
           constexpr int kk = decltype(kk_c)::value;
@@ -1149,7 +1149,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         if (leader) tc_commit(&bars[B_S_FULL + buf]);
       };
       auto issue_pv = [&](int qt, uint32_t sV, bool acc_first) {
-        const uint32_t b_lo = V_LO | (sV >> 4);
+        const uint32_t b_lo = V_LO | desc_addr(sV);
         const uint32_t d = tmem + 2 * C::BN + qt * C::HDV, a = tmem + qt * C::BN;
         const uint32_t acc0 = acc_first ? 1u : 0u;
         static_for<0, C::BN / 16>([&](auto kk_c) {
@@ -1712,7 +1712,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
 }
 
 // ================================================================== MLA ====
-#include "mla_kernel.cuh"
+#include "mla_pair_kernel.cuh"
 
 // ============================================================== combine ====
 // Merge the split-KV partials of every split query block: with lse_i the
@@ -1909,21 +1909,59 @@ static int launch_attn_fp8(int mode, const TMaps &tmaps, const KParams &kp, int 
   return launch_attn_kernel<HD, kDecode, false, FMT>(tmaps, kp, grid, s);
 }
 
-template <int MODE, bool MASK = false>
-static int launch_mla_kernel(const KParams &kp, int grid, cudaStream_t s) {
-  using C = MlaCfg<MODE>;
+// Pair kernel launch: clusters of two CTAs, programmatic dependent launch.
+template <int MODE, bool MASK>
+static cudaError_t launch_pair(int pairs, cudaStream_t s, const KParams &kp, bool query_only,
+                               int *max_pairs) {
+  using C = MlaPairCfg;
   static bool configured[kMaxDevicesCfg] = {};
   if (needs_config(configured)) {
-    cudaError_t e = cudaFuncSetAttribute(mla_kernel<MODE, MASK>,
+    cudaError_t e = cudaFuncSetAttribute(mla_pair_kernel<MODE, MASK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess)
-      return set_error(PKX_ECUDA, "cudaFuncSetAttribute(mla_kernel): %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) return e;
     mark_configured(configured);
   }
-  cudaError_t e = launch_pdl(mla_kernel<MODE, MASK>, dim3(grid), dim3(C::THREADS), C::SMEM, s,
-                             kp);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = query_only ? 1 : 2;
+  if (query_only) return cudaOccupancyMaxActiveClusters(max_pairs, mla_pair_kernel<MODE, MASK>, &cfg);
+  return cudaLaunchKernelEx(&cfg, mla_pair_kernel<MODE, MASK>, kp);
+}
+
+// CTA pairs of the MLA kernel that run at once on the current device (an SM
+// group with an odd count of free SMs leaves one idle), queried once per
+// device; 0 on error.
+static int mla_pairs(int nsm) {
+  static int cached[kMaxDevicesCfg] = {};
+  int dev = 0;
+  const bool cache = cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevicesCfg;
+  if (cache && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (launch_pair<kUnified, false>(nsm / 2, nullptr, KParams{}, true, &n) != cudaSuccess) {
+    set_error(PKX_ECUDA, "cudaOccupancyMaxActiveClusters(mla_pair_kernel) failed");
+    return 0;
+  }
+  n = std::min(n, nsm / 2);
+  if (cache && n > 0) cached[dev] = n;
+  return n;
+}
+
+template <int MODE, bool MASK = false>
+static int launch_mla_pair(const KParams &kp, int pairs, cudaStream_t s) {
+  cudaError_t e = launch_pair<MODE, MASK>(pairs, s, kp, false, nullptr);
   if (e != cudaSuccess)
-    return set_error(PKX_ECUDA, "mla_kernel launch: %s", cudaGetErrorString(e));
+    return set_error(PKX_ECUDA, "mla_pair_kernel launch: %s", cudaGetErrorString(e));
   return PKX_OK;
 }
 
@@ -1956,6 +1994,12 @@ int launch_attention(const AttnArgs &a) {
       return set_error(PKX_EUNSUPPORTED,
                        "Lq=576/Lv=512 needs V to be the first 512 dims of each K row");
   }
+  // the MLA kernel runs on CTA pairs: units for four rounds of the pairs
+  int pairs = 0;
+  if (mla && a.kv_fmt == kKvBf16) {
+    pairs = mla_pairs(nsm);
+    if (pairs <= 0) return set_error(PKX_ECUDA, "no CTA pair of the MLA kernel fits the device");
+  }
   if (a.workspace == nullptr || a.workspace_bytes < L.total)
     return set_error(PKX_EWORKSPACE, "workspace of %zu bytes given, %zu needed",
                      a.workspace_bytes, L.total);
@@ -1982,16 +2026,16 @@ int launch_attention(const AttnArgs &a) {
   sp.batch = a.batch;
   sp.hkv = a.hkv;
   sp.tok = q_tiles_per_unit(a.lq, a.lv) * tok;
-  sp.bn = mla ? MlaCfg<0>::BN : kBlockN;
+  sp.bn = mla ? MlaPairCfg::BN : kBlockN;
   sp.q_tile_tok = tok > 0 ? tok : 1;
   sp.no_causal = a.custom_mask != nullptr;
   sp.key_set = a.mode == kTwoStage ? a.key_set : kAllKeys;
   sp.keep_status = a.keep_status;
   sp.two_streams = !mla && !split && (!decode || dec_two);
-  sp.n_dsplit = mla ? MlaCfg<0>::LV / MlaCfg<0>::DVS : 1;
+  sp.n_dsplit = 1;
   sp.window = a.window;
   sp.num_q_tokens = nq;
-  sp.unit_target = L.unit_target;
+  sp.unit_target = mla ? 4 * pairs : L.unit_target;
   sp.qb_max = L.qb_max;
   sp.unit_max = L.unit_max;
   sp.comb_max = L.comb_max;
@@ -2126,12 +2170,12 @@ int launch_attention(const AttnArgs &a) {
     }
   } else if (mla) {
     if (a.mode == kTwoStage)
-      rc = masked ? launch_mla_kernel<kTwoStage, true>(kp, grid, a.stream)
-                  : launch_mla_kernel<kTwoStage>(kp, grid, a.stream);
+      rc = masked ? launch_mla_pair<kTwoStage, true>(kp, pairs, a.stream)
+                  : launch_mla_pair<kTwoStage>(kp, pairs, a.stream);
     else if (a.mode == kUnified)
-      rc = masked ? launch_mla_kernel<kUnified, true>(kp, grid, a.stream)
-                  : launch_mla_kernel<kUnified>(kp, grid, a.stream);
-    else rc = launch_mla_kernel<kDecode>(kp, grid, a.stream);
+      rc = masked ? launch_mla_pair<kUnified, true>(kp, pairs, a.stream)
+                  : launch_mla_pair<kUnified>(kp, pairs, a.stream);
+    else rc = launch_mla_pair<kDecode>(kp, pairs, a.stream);
   } else {
     return set_error(PKX_EUNSUPPORTED, "head dims (%d, %d) not built", a.lq, a.lv);
   }

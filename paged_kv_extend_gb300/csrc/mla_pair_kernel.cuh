@@ -1,0 +1,680 @@
+// mla_pair_kernel.cuh -- extend / decode attention for the MLA head shape
+// (Lq = 576 = 512 latent + 64 rope dims, Lv = 512, one KV head, V = the first
+// 512 dims of each K row) on a pair of CTAs, included by attention.cu.
+//
+// The MLA layout (sglang cpu_graph_runner.py, qkv_proj_with_rope fake: V is a
+// narrow view of K; extend_attention.py, _get_block_sizes_for_extend_attention:
+// 576 = 512 + 64) makes the score one 576-dim dot product and lets the K tile
+// double as V.  A 128-row tile's O over all 512 value dims (512 TMEM columns)
+// does not fit one SM's TMEM next to Q and S, so the two CTAs of a cluster
+// split the dims instead of recomputing S per value slice:
+//   rank r holds value dims [256 r, 256 r + 256) and rope dims
+//   [512 + 32 r, 512 + 32 r + 32) of Q and K (288 dims each);
+//   each computes its partial S = Q_r K_r^T (64 keys per tile), sends it to
+//   the other, and adds the other's: fp32 addition commutes, so both hold the
+//   same S bit for bit, run the same softmax and get the same P;
+//   each then computes O for its own value dims, the first 256 of its K dims.
+// No product is recomputed: per (row, key) the pair does 2 x 576 + 2 x 512
+// FLOP, the algorithmic count.
+//
+//   TMEM (per CTA)  [0, 144) Q_r as bf16 pairs
+//                   [160, 192) P (bf16 pairs, 64 keys)
+//                   [192, 256) S, the partial of this rank (fp32)
+//                   [256, 512) O, 256 value dims (fp32)
+//   SMEM  four stages of a 64-key K tile (four 64-dim swizzle atoms of value
+//         dims and one atom whose first half holds the rope dims), the other
+//         rank's partial S of the current tile (16-byte chunk c of row r at
+//         c * 128 * 16 + r * 16), a ring of resolved row indices.
+//
+// The exchange runs one tile ahead of the softmax, so that its latency hides
+// behind the softmax of the previous tile, and QK^T runs two tiles ahead of
+// PV.  In the iteration of tile j each softmax thread
+//   adds its own partial of tile j (kept in registers) to the other rank's
+//   (received in shared memory; XFULL), then releases the receive buffer
+//   (XEMPTY of the other rank, one arrival per warp);
+//   reads S(j + 1) into registers and releases it (S_FREE; QK^T of tile
+//   j + 2 follows), waits until the other rank has read tile j from its
+//   receive buffer (XEMPTY here), and writes its row of S(j + 1) there with
+//   asynchronous remote stores whose bytes complete the other rank's XFULL;
+//   runs the softmax of tile j and writes P(j).
+// XFULL is armed (one arrival that expects the tile's bytes) by thread 0
+// once the previous tile's phase has completed; the bytes may land first.
+// Both CTAs of a pair take the same units (position pair + k * pairs of the
+// claim order), so their tile counters stay in step.
+// Warps: 0-3 softmax (one row per thread; they also write Q into TMEM), 4 MMA
+// issue, 5 row indices, 6-9 K-row copies (cp.async), 10-11 idle.
+
+struct MlaPairCfg {
+  static constexpr int BM = kBlockM, BN = 64;
+  static constexpr int LQ = 576, LV = 512;
+  static constexpr int DV = LV / 2;             // value dims per rank
+  static constexpr int DR = (LQ - LV) / 2;      // rope dims per rank
+  static constexpr int KSTEPS = (DV + DR) / 16;  // K-steps of QK^T: 18
+  static constexpr int NK = 4, NI = 4;
+  static constexpr int K_BYTES = BN * 5 * 128;  // four value atoms + the rope atom
+  static constexpr int X_BYTES = BM * BN * 4;   // a partial S
+  static constexpr int I_BYTES = BN * 4;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_X = NK * K_BYTES;     // received from the other rank
+  static constexpr int OFF_I = OFF_X + X_BYTES;
+  static constexpr int OFF_BAR = OFF_I + NI * I_BYTES;
+  static constexpr int N_BARS = 16 + 2 * NK + 2 * NI;
+  static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 1024;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int Q_COL = 0, P_COL = 160, S_COL = 192, O_COL = 256;
+  static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DV, 1);
+  static constexpr int THREADS = 384;
+  static constexpr int COPY_WARP0 = 6, COPY_THREADS = 128;
+  // Registers: the kernel launches with REGS_LAUNCH per thread (checked at
+  // build time); the softmax warpgroup takes REGS_SOFTMAX, the other two
+  // give back down to REGS_OTHER.  The split must add up exactly.
+  static constexpr int REGS_LAUNCH = 168, REGS_SOFTMAX = 232, REGS_OTHER = 136;
+  static_assert(128 * REGS_SOFTMAX + 256 * REGS_OTHER == THREADS * REGS_LAUNCH,
+                "register split");
+  static_assert(SMEM + 16 <= 232448, "shared memory budget (dynamic + static)");
+  static_assert(DR == 32 && KSTEPS == 18, "the rope dims fill half an atom");
+};
+
+enum {
+  X_Q_FULL = 0,
+  X_S_FULL = 1,   // the partial S landed
+  X_P_FULL = 2,   // P written
+  X_O_DONE = 3,   // last PV of a unit landed
+  X_FINAL = 4,
+  X_S_FREE = 5,   // S read into registers: the next QK^T may overwrite it
+  X_PV_DONE = 6,  // one phase per PV: P and O are free again
+  X_NEVER = 7,    // no thread ever arrives (the stall hook waits on it)
+  X_XFULL = 8,    // the other rank's partial landed (one arrival + its bytes)
+  X_XEMPTY = 9,   // the other rank has read what this CTA sent (4 remote arrivals)
+  X_RING = 16
+};
+
+// The i-th unit of this pair (claim order position pair + i * pairs), or -1.
+__device__ __forceinline__ int pair_unit(const KParams &p, int n_units, uint32_t i) {
+  const long long pos = (long long)(blockIdx.x >> 1) + (long long)i * (gridDim.x >> 1);
+  return pos < n_units ? p.uorder[pos] : -1;
+}
+
+template <int MODE, bool MASK>
+__global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const KParams p) {
+  using C = MlaPairCfg;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *k_full = bars + X_RING;
+  uint64_t *k_empty = k_full + C::NK;
+  uint64_t *i_full = k_empty + C::NK;
+  uint64_t *i_empty = i_full + C::NI;
+  volatile int *abort_flag = &s_abort;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
+  const int dv0 = (int)rank * C::DV;            // first value dim of this rank
+  const int dr0 = C::LV + (int)rank * C::DR;    // first rope dim of this rank
+
+  if (tid == 0) {
+    mbar_init(&bars[X_Q_FULL], 128);
+    mbar_init(&bars[X_S_FULL], 1);
+    mbar_init(&bars[X_P_FULL], 4);  // one arrival per softmax warp
+    mbar_init(&bars[X_O_DONE], 1);
+    mbar_init(&bars[X_FINAL], 1);
+    mbar_init(&bars[X_S_FREE], 4);
+    mbar_init(&bars[X_PV_DONE], 1);
+    mbar_init(&bars[X_NEVER], 1);
+    mbar_init(&bars[X_XFULL], 1);
+    mbar_init(&bars[X_XEMPTY], 4);
+    for (int s = 0; s < C::NK; ++s) {
+      mbar_init(&k_full[s], C::COPY_THREADS);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < C::NI; ++s) {
+      mbar_init(&i_full[s], 32);
+      mbar_init(&i_empty[s], C::COPY_THREADS);
+    }
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(&s_tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  // both CTAs' barriers exist before either arrives on the other's
+  cluster_sync();
+  tc_fence_after();
+  grid_dep_wait();
+  grid_dep_launch();
+  const uint32_t tmem = s_tmem;
+  const int n_units = p.hdr->n_units;
+  const int G = p.group;
+  if (warp < 4) regs_increase<C::REGS_SOFTMAX>();
+  else regs_decrease<C::REGS_OTHER>();
+
+  if (warp < 4) {
+    // ------------------------- Q -> TMEM, partial-S exchange, softmax, epilogue
+    const int r = tid;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    uint32_t s_cnt = 0, o_cnt = 0;
+    uint32_t n_sent = 0, n_recv = 0;  // tiles sent / combined so far
+    uint32_t pv_base = 0;  // PVs of earlier units (X_PV_DONE phases)
+    const uint32_t xempty_peer = cluster_addr(smem_u32(&bars[X_XEMPTY]), peer);
+    const uint32_t xfull_peer = cluster_addr(smem_u32(&bars[X_XFULL]), peer);
+    // this thread's row of the receive buffer (chunk c at c * BM * 16), here
+    // and in the other rank
+    const uint8_t *recv_row = smem + C::OFF_X + r * 16;
+    const uint32_t send_row = cluster_addr(sbase + C::OFF_X + r * 16, peer);
+    uint32_t own[C::BN];  // this rank's partial S of the next tile
+    // S of the next tile into registers, released for the next QK^T, and
+    // sent to the other rank once it has read the previous tile
+    auto send = [&]() -> bool {
+      if (!mbar_wait(&bars[X_S_FULL], s_cnt & 1u, abort_flag, p.wait_ns)) return false;
+      ++s_cnt;
+      tc_fence_after();
+      tmem_ld32(lane_base + C::S_COL, *reinterpret_cast<uint32_t (*)[32]>(own));
+      tmem_ld32(lane_base + C::S_COL + 32, *reinterpret_cast<uint32_t (*)[32]>(own + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[X_S_FREE]);
+      if (n_sent > 0 &&
+          !mbar_wait_cluster(&bars[X_XEMPTY], (n_sent - 1) & 1u, abort_flag, p.wait_ns))
+        return false;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_async_cluster_u4(send_row + c * (C::BM * 16),
+                            make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
+                            xfull_peer);
+      ++n_sent;
+      return true;
+    };
+    // both partials of the current tile added (own + other in both ranks:
+    // the same sum bit for bit), the receive buffer released
+    auto combine = [&](float (&x)[C::BN]) -> bool {
+      if (!mbar_wait_cluster(&bars[X_XFULL], n_recv & 1u, abort_flag, p.wait_ns)) return false;
+      ++n_recv;
+      // the phase of the next tile (its bytes cannot land before every warp
+      // here has released this one)
+      if (tid == 0) mbar_arrive_expect_tx(&bars[X_XFULL], C::X_BYTES);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 o4 = *reinterpret_cast<const uint4 *>(recv_row + c * (C::BM * 16));
+        x[4 * c + 0] = __uint_as_float(own[4 * c + 0]) + __uint_as_float(o4.x);
+        x[4 * c + 1] = __uint_as_float(own[4 * c + 1]) + __uint_as_float(o4.y);
+        x[4 * c + 2] = __uint_as_float(own[4 * c + 2]) + __uint_as_float(o4.z);
+        x[4 * c + 3] = __uint_as_float(own[4 * c + 3]) + __uint_as_float(o4.w);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(xempty_peer);
+      return true;
+    };
+    if (tid == 0) mbar_arrive_expect_tx(&bars[X_XFULL], C::X_BYTES);  // the first tile
+    if (p.stall && !mbar_wait(&bars[X_NEVER], 0, abort_flag, p.wait_ns))
+      abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+    for (uint32_t uc = 0; !*abort_flag; ++uc) {
+      const int u = pair_unit(p, n_units, uc);
+      if (u < 0) break;
+      const WorkUnit w = p.units[u];
+      const int nt = w.n_tiles;
+      const int rows_valid = w.n_tok * G;
+      const bool valid = r < rows_valid;
+      const bool warp_active = warp * 32 < rows_valid;
+      const int t = r / G, g = r - (r / G) * G;
+      const int qpos = w.qpos0 + t;
+      const int qmax = w.qpos0 + w.n_tok - 1;
+      const int64_t orow_idx = (int64_t)(w.q_tok0 + t) * p.hq + w.kvh * G + g;
+      const int64_t prow_idx = (int64_t)w.slot * p.rows_per_slot + r;
+      const uint8_t *mbase = nullptr;
+      int64_t mstride = 0;
+      if (MASK) {
+        const int qo0 = p.qo_indptr[w.b];
+        mstride = MODE == kTwoStage ? (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]) +
+                                          (p.qo_indptr[w.b + 1] - qo0)
+                                    : (int64_t)(p.kv_indptr[w.b + 1] - p.kv_indptr[w.b]);
+        mbase = p.custom_mask + p.mask_indptr[w.b] + (int64_t)(w.q_tok0 - qo0) * mstride;
+      }
+      if (nt == 0) {
+        if (valid) {
+          if (w.slot < 0) {
+            bf16 *orow = p.o + orow_idx * C::LV + dv0;
+            for (int c = 0; c < C::DV; c += 8)
+              *reinterpret_cast<uint4 *>(orow + c) = make_uint4(0, 0, 0, 0);
+            if (p.lse && rank == 0) p.lse[orow_idx] = -INFINITY;
+          } else {
+            float *prow = p.po + prow_idx * C::LV + dv0;
+            for (int c = 0; c < C::DV; c += 4)
+              *reinterpret_cast<float4 *>(prow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (rank == 0) p.plse[prow_idx] = -INFINITY;
+          }
+        }
+        continue;
+      }
+      // this rank's Q dims into TMEM as bf16 pairs: four value atoms in
+      // columns [0, 128), the rope dims in [128, 144) (zeros up to 160);
+      // rows past the block get zeros.  The previous unit's products have
+      // all completed (its epilogue waited for them).
+      {
+        const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + orow_idx * C::LQ);
+#pragma unroll 1
+        for (int c = 0; c < 5; ++c) {
+          uint32_t v[32];
+          const int q0 = c < 4 ? (dv0 + 64 * c) / 8 : dr0 / 8;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 x = valid && (c < 4 || i < C::DR / 8) ? __ldg(qrow + q0 + i)
+                                                              : make_uint4(0, 0, 0, 0);
+            v[4 * i + 0] = x.x;
+            v[4 * i + 1] = x.y;
+            v[4 * i + 2] = x.z;
+            v[4 * i + 3] = x.w;
+          }
+          tmem_st32(lane_base + C::Q_COL + c * 32, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars[X_Q_FULL]);
+      }
+      if (!send()) {  // the unit's first tile
+        abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+        break;
+      }
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nt; ++j) {
+        int kb, ke;
+        tile_keys<C::BN>(w, j, kb, ke);
+        uint32_t mb[2] = {0u, 0u};
+        if constexpr (MASK) {
+          if (warp_active) {
+            const int t_lo = (warp * 32) / G, t_hi = min((warp * 32 + 31) / G, w.n_tok - 1);
+            for (int tc = t_lo; tc <= t_hi; tc += 4) {
+              uint8_t by[4][2];
+#pragma unroll
+              for (int u2 = 0; u2 < 4; ++u2) {
+                const uint8_t *rowp = mbase + (int64_t)(tc + u2) * mstride;
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                  const int kpos = kb + 32 * q2 + lane;
+                  by[u2][q2] = (tc + u2 <= t_hi && kpos < ke) ? __ldg(rowp + kpos) : (uint8_t)0;
+                }
+              }
+#pragma unroll
+              for (int u2 = 0; u2 < 4; ++u2) {
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                  const uint32_t word = __ballot_sync(0xffffffffu, by[u2][q2] != 0);
+                  if (t == tc + u2) mb[q2] = word;
+                }
+              }
+            }
+          }
+        }
+        float x[C::BN];
+        if (!combine(x) || (j + 1 < nt && !send())) {
+          abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+          break;
+        }
+        float alpha = 1.0f;
+        bool o_needs = false;
+        uint32_t pk[32];
+        if (warp_active) {
+          float sc = p.scale_log2;
+          if (p.use_cap) {
+#pragma unroll
+            for (int i = 0; i < C::BN; ++i) x[i] = p.cap_log2 * tanh_approx(x[i] * p.cap_pre);
+            sc = 1.0f;
+          }
+          const bool need_mask = (ke - 1 > w.qpos0) || (ke - kb < C::BN) ||
+                                 (p.window > 0 && kb < qmax - p.window);
+          if constexpr (MASK) {
+            const bool every = (mb[0] & mb[1]) == 0xffffffffu &&
+                               (p.window <= 0 || qpos - kb <= p.window);
+            if (!every) {
+#pragma unroll
+              for (int i = 0; i < C::BN; ++i) {
+                const int kpos = kb + i;
+                const bool vis = ((mb[i >> 5] >> (i & 31)) & 1u) &&
+                                 (p.window <= 0 || qpos - kpos <= p.window);
+                x[i] = vis ? x[i] * sc : -INFINITY;
+              }
+              sc = 1.0f;
+            }
+          } else if (need_mask) {
+#pragma unroll
+            for (int i = 0; i < C::BN; ++i) {
+              const int kpos = kb + i;
+              const bool vis =
+                  kpos < ke && kpos <= qpos && (p.window <= 0 || qpos - kpos <= p.window);
+              x[i] = vis ? x[i] * sc : -INFINITY;
+            }
+            sc = 1.0f;
+          }
+          float mt;
+          if (sc >= 0.f) {
+            float mt0 = x[0], mt1 = x[1];
+#pragma unroll
+            for (int i = 2; i < C::BN; i += 2) {
+              mt0 = fmaxf(mt0, x[i]);
+              mt1 = fmaxf(mt1, x[i + 1]);
+            }
+            mt = fmaxf(mt0, mt1) * sc;
+          } else {
+            float mt0 = x[0], mt1 = x[1];
+#pragma unroll
+            for (int i = 2; i < C::BN; i += 2) {
+              mt0 = fminf(mt0, x[i]);
+              mt1 = fminf(mt1, x[i + 1]);
+            }
+            mt = fminf(mt0, mt1) * sc;
+          }
+          const float m_new = fmaxf(m, mt);
+          const bool grow = m_new > m + 8.0f;
+          alpha = grow ? ex2_approx(m - m_new) : 1.0f;
+          o_needs = grow && j > 0 && l > 0.f;
+          if (grow) {
+            l *= alpha;
+            m = m_new;
+          }
+          const float nm = m == -INFINITY ? 0.f : -m;
+          float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < C::BN; i += 2) {
+            const float e0 = ex2_approx(fmaf(x[i], sc, nm));
+            const float e1 = ex2_approx(fmaf(x[i + 1], sc, nm));
+            l0 += e0;
+            l1 += e1;
+            pk[i / 2] = pack_bf16(e0, e1);
+          }
+          l += l0 + l1;
+        }
+        // P's columns and O are free once the previous tile's PV has landed.
+        // Every warp waits, also one without rows, so that no warp arrives
+        // on P_FULL twice in one phase.
+        if (j > 0 && !mbar_wait(&bars[X_PV_DONE], (pv_base + j - 1) & 1u, abort_flag, p.wait_ns)) {
+          abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+        }
+        tc_fence_after();
+        if (warp_active) {
+          tmem_st32(lane_base + C::P_COL, pk);
+          if (__any_sync(0xffffffffu, o_needs)) {
+            const float a = o_needs ? alpha : 1.0f;
+            uint32_t v[32];
+#pragma unroll 1
+            for (int c = 0; c < C::DV / 32; ++c) {
+              const uint32_t ta = lane_base + C::O_COL + c * 32;
+              tmem_ld32(ta, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+              tmem_st32(ta, v);
+            }
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[X_P_FULL]);
+      }
+      if (*abort_flag) break;
+      if (!mbar_wait(&bars[X_O_DONE], o_cnt & 1u, abort_flag, p.wait_ns)) {
+        abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+        break;
+      }
+      ++o_cnt;
+      pv_base += nt;
+      tc_fence_after();
+      if (warp_active) {
+        float inv = l > 0.f ? 1.0f / l : 0.f;
+        float lse_v = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (p.sinks && w.slot < 0) {
+          const float s2 = __ldg(p.sinks + w.kvh * G + g) * 1.4426950408889634f;
+          const float M = fmaxf(m, s2);
+          const float a_m = m == -INFINITY ? 0.f : ex2_approx(m - M);
+          const float lt = l * a_m + ex2_approx(s2 - M);
+          inv = a_m / lt;
+          lse_v = (M + __log2f(lt)) * 0.69314718055994531f;
+        }
+        uint32_t v[32];
+#pragma unroll 1
+        for (int c = 0; c < C::DV / 32; ++c) {
+          tmem_ld32(lane_base + C::O_COL + c * 32, v);
+          tmem_wait_ld();
+          if (valid) {
+            if (w.slot < 0) {
+              bf16 *orow = p.o + orow_idx * C::LV + dv0 + c * 32;
+#pragma unroll
+              for (int i = 0; i < 32; i += 8) {
+                uint4 q4;
+                q4.x = pack_bf16(__uint_as_float(v[i + 0]) * inv, __uint_as_float(v[i + 1]) * inv);
+                q4.y = pack_bf16(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+                q4.z = pack_bf16(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv);
+                q4.w = pack_bf16(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
+                *reinterpret_cast<uint4 *>(orow + i) = q4;
+              }
+            } else {
+              float *prow = p.po + prow_idx * C::LV + dv0 + c * 32;
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4 *>(prow + i) =
+                    make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
+                                __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+            }
+          }
+        }
+        if (valid && rank == 0) {
+          if (w.slot < 0) {
+            if (p.lse) p.lse[orow_idx] = lse_v;
+          } else {
+            p.plse[prow_idx] = lse_v;
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------ MMA issue (one warp)
+    // QK^T runs two tiles ahead of PV: S(j + 2) = Q_r K_r(j + 2)^T as soon
+    // as the softmax has read S(j + 1) (it does so before it writes P(j)),
+    // then O += P(j) V_r(j) once P(j) is written.  The whole warp runs the
+    // loop; one elected lane issues.
+    const bool leader = elect_one();
+    uint32_t q_cnt = 0, kc = 0, p_cnt = 0, f_cnt = 0;
+    bool ok = true;
+    constexpr uint32_t K_LO = sw128_desc_lo(0), K_HI = sw128_desc_hi(1024);
+    constexpr uint32_t V_LO = sw128_desc_lo(C::BN * 128), V_HI = sw128_desc_hi(1024);
+    auto issue_s = [&](uint32_t sK) {
+      const uint32_t b_lo = K_LO | desc_addr(sK);
+      static_for<0, C::KSTEPS>([&](auto kk_c) {
+        constexpr int kk = decltype(kk_c)::value;
+        constexpr uint32_t bo = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) / 16;
+        if (leader)
+          tc_mma_ts_step<kk * 8, bo>(tmem + C::S_COL, tmem + C::Q_COL, b_lo, K_HI, C::IDESC_QK,
+                                     kk > 0 ? 1u : 0u);
+      });
+      if (leader) tc_commit(&bars[X_S_FULL]);
+    };
+    auto issue_pv = [&](uint32_t sV, bool acc_first) {
+      const uint32_t b_lo = V_LO | desc_addr(sV);
+      const uint32_t acc0 = acc_first ? 1u : 0u;
+      static_for<0, C::BN / 16>([&](auto kk_c) {
+        constexpr int kk = decltype(kk_c)::value;
+        if (leader)
+          tc_mma_ts_step<kk * 8, kk * 128>(tmem + C::O_COL, tmem + C::P_COL, b_lo, V_HI,
+                                           C::IDESC_PV, kk > 0 ? 1u : acc0);
+      });
+      if (leader) tc_commit(&bars[X_PV_DONE]);
+    };
+    auto k_tile = [&](uint32_t kpos) { return sbase + C::OFF_K + (kpos % C::NK) * C::K_BYTES; };
+    // QK^T of the tile at ring position kpos, once its K rows have landed
+    auto qk = [&](uint32_t kpos) -> bool {
+      if (!mbar_wait(&k_full[kpos % C::NK], (kpos / C::NK) & 1u, abort_flag, p.wait_ns))
+        return false;
+      fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.mma reads
+      tc_fence_after();
+      issue_s(k_tile(kpos));
+      return true;
+    };
+    auto s_free = [&]() -> bool {
+      if (!mbar_wait(&bars[X_S_FREE], f_cnt & 1u, abort_flag, p.wait_ns)) return false;
+      ++f_cnt;
+      tc_fence_after();
+      return true;
+    };
+    for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+      const int u = pair_unit(p, n_units, uc);
+      if (u < 0) break;
+      const WorkUnit w = p.units[u];
+      const int nt = w.n_tiles;
+      if (nt == 0) continue;
+      if (!mbar_wait(&bars[X_Q_FULL], q_cnt & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
+      ++q_cnt;
+      tc_fence_after();
+      const uint32_t k0 = kc;
+      // S(0); S(1) once S(0) is read
+      if (!qk(k0) || !s_free() || (nt > 1 && !qk(k0 + 1))) { ok = false; break; }
+      for (int j = 0; j < nt; ++j) {
+        // S(j + 1) read: S(j + 2) may overwrite it
+        if (j + 1 < nt && (!s_free() || (j + 2 < nt && !qk(k0 + j + 2)))) { ok = false; break; }
+        if (!mbar_wait(&bars[X_P_FULL], p_cnt & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
+        ++p_cnt;
+        tc_fence_after();
+        issue_pv(k_tile(k0 + j), j > 0);
+        if (leader) tc_commit(&k_empty[(k0 + j) % C::NK]);
+      }
+      if (!ok) break;
+      kc = k0 + nt;
+      if (leader) tc_commit(&bars[X_O_DONE]);
+    }
+    if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+    if (leader) tc_commit(&bars[X_FINAL]);
+    if (!mbar_wait_drain(&bars[X_FINAL], 0)) record_status(p.status, PKX_ETIMEOUT);
+  } else if (warp == 5) {
+    // ------------------------------------------------ row indices (one warp)
+    uint32_t ic = 0;
+    bool ok = true;
+    for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+      const int u = pair_unit(p, n_units, uc);
+      if (u < 0) break;
+      const WorkUnit w = p.units[u];
+      const int nt = w.n_tiles;
+      if (nt == 0) continue;
+      const int64_t kv_base = p.kv_indptr[w.b];
+      const int64_t ext_base = MODE == kTwoStage ? p.qo_indptr[w.b] : 0;
+      for (int j = 0; j < nt; ++j) {
+        int kb, ke;
+        tile_keys<C::BN>(w, j, kb, ke);
+        const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
+        int rows[2];
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int jpos = kb + 2 * lane + i;
+          int64_t row = -1;
+          if (jpos < ke) {
+            if (from_ext) {
+              row = ext_base + (jpos - w.k_split);
+            } else {
+              row = MODE == kUnified
+                        ? __ldg(static_cast<const int64_t *>(p.kv_indices) + kv_base + jpos)
+                        : (int64_t)__ldg(static_cast<const int32_t *>(p.kv_indices) + kv_base + jpos);
+              if (row < 0 || row >= p.num_slots) {
+                bad = true;
+                row = -1;
+              }
+            }
+          }
+          rows[i] = (int)row;
+        }
+        if (bad) record_status(p.status, PKX_EDEVICE);
+        const int is = ic % C::NI;
+        if (ic >= (uint32_t)C::NI &&
+            !mbar_wait(&i_empty[is], ((ic / C::NI) - 1) & 1u, abort_flag, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        *reinterpret_cast<int2 *>(smem + C::OFF_I + is * C::I_BYTES + lane * 8) =
+            make_int2(rows[0], rows[1]);
+        mbar_arrive(&i_full[is]);
+        ++ic;
+      }
+    }
+    if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+  } else if (warp < C::COPY_WARP0 + C::COPY_THREADS / 32) {
+    // ------------------------------------------------ K-row copies (4 warps)
+    // Thread ct copies chunk ct % 8 of each of this rank's four value atoms,
+    // and of its rope dims if ct % 8 < 4, for keys ct / 8 + 16 i (i < 4): the
+    // swizzle term (chunk ^ key % 8) is fixed per thread, and a warp
+    // instruction reads four rows' 128-byte segments.
+    const int ct = tid - C::COPY_WARP0 * 32;
+    const int ch = ct & 7, key0 = ct >> 3;
+    const uint32_t dthr = (uint32_t)key0 * 128u + ((uint32_t)(ch ^ (key0 & 7)) << 4);
+    uint32_t kc = 0, ic = 0;
+    bool ok = true;
+    for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+      const int u = pair_unit(p, n_units, uc);
+      if (u < 0) break;
+      const WorkUnit w = p.units[u];
+      const int nt = w.n_tiles;
+      if (nt == 0) continue;
+      const bf16 *kp = p.k_pool + (int64_t)w.kvh * p.kb_sh + dv0 + ch * 8;
+      const bf16 *kx = p.k_ext + (int64_t)w.kvh * p.ke_sh + dv0 + ch * 8;
+      for (int j = 0; j < nt; ++j) {
+        int kb, ke;
+        tile_keys<C::BN>(w, j, kb, ke);
+        const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
+        const int is = ic % C::NI;
+        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        const int *ring = reinterpret_cast<const int *>(smem + C::OFF_I + is * C::I_BYTES);
+        int rows[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rows[i] = ring[key0 + 16 * i];
+        mbar_arrive(&i_empty[is]);
+        ++ic;
+        const int ks = kc % C::NK;
+        if (kc >= (uint32_t)C::NK &&
+            !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        const bf16 *base = from_ext ? kx : kp;
+        const int64_t st = from_ext ? p.ke_st : p.kb_ss;
+        const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES + dthr;
+        static_for<0, 4>([&](auto i_c) {
+          constexpr int i = decltype(i_c)::value;
+          const int row = rows[i];
+          const bf16 *src = base + (int64_t)max(row, 0) * st;
+          const uint32_t bytes = row >= 0 ? 16u : 0u;
+          static_for<0, 4>([&](auto a_c) {
+            constexpr int a = decltype(a_c)::value;
+            cp_async_16_at<a * C::BN * 128 + i * 16 * 128, a * 128>(sK, src, bytes);
+          });
+          // the rope dims dr0 + 8 ch (value dims start at dv0 + 8 ch)
+          if (ch < C::DR / 8)
+            cp_async_16_at<4 * C::BN * 128 + i * 16 * 128, 0>(sK, src + (dr0 - dv0), bytes);
+        });
+        cp_async_arrive_noinc(&k_full[ks]);
+        ++kc;
+      }
+    }
+    if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+    cp_async_wait_all();
+  }
+
+  tc_fence_before();
+  // neither CTA leaves while the other may still store into its receive
+  // buffer or arrive on its barriers
+  cluster_sync();
+  if (warp == 4) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}

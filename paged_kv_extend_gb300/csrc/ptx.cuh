@@ -94,6 +94,67 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
+// ------------------------------------------------------ thread-block clusters
+// Rank of this CTA in its cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address of the same shared-memory location in CTA `rank` of the
+// cluster (for st.shared::cluster and remote mbarrier arrives).
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier of any CTA of the cluster; the thread's earlier
+// memory operations (its shared::cluster stores) are released at cluster
+// scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_bar_addr)
+               : "memory");
+}
+// try_wait that acquires at cluster scope (sees what the peer released).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort_flag, uint64_t limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+// Asynchronous 16-byte store into the shared memory of a CTA of the
+// cluster; its bytes complete the transaction count of that CTA's mbarrier
+// (the complete-tx has release semantics at cluster scope).
+__device__ __forceinline__ void st_async_cluster_u4(uint32_t addr, uint4 v, uint32_t bar_cluster) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar_cluster)
+      : "memory");
+}
+// Barrier of every thread of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 // One box of a 3-D tensor map at coordinates (c0, c1, c2).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -291,6 +352,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr, uint32_t lbo,
 // address field is bits 0-13 of the low word, so the descriptor of address a
 // is (lo | a >> 4, hi) and stepping it by b bytes adds b >> 4 to the low
 // word, with no carry while a + b stays inside shared memory (< 256 KB).
+// Start-address field of a descriptor's low word: bits [4, 18) of the shared
+// address.  The address of a CTA in a cluster can carry higher bits, which
+// must not reach the LBO field above it.
+__device__ __forceinline__ uint32_t desc_addr(uint32_t smem_addr) {
+  return (smem_addr & 0x3FFFFu) >> 4;
+}
 __host__ __device__ constexpr uint32_t sw128_desc_lo(uint32_t lbo) {
   return ((lbo >> 4) & 0x3FFFu) << 16;
 }

@@ -21,7 +21,7 @@ Checks: every role finishes (no deadlock); every parity wait passes with its
 barrier exactly one phase past what the waiter has consumed, so a parity wait
 never aliases a phase two ahead; and every product reads a K or V stage whose
 fill for that use has completed.  Planted mistakes must be caught.  The same
-model runs the MLA kernel's protocol (csrc/mla_kernel.cuh) at the end.
+model runs the MLA pair kernel's protocol (csrc/mla_pair_kernel.cuh) at the end.
 """
 import random
 
@@ -377,137 +377,208 @@ def test_model_catches_planted_mistakes(mistake):
 
 
 # ------------------------------------------------------------------ MLA kernel
-class _MlaModel:
-    """The mbarrier protocol of mla_kernel (csrc/mla_kernel.cuh): one K ring
-    (the tile is also V), S released early (S_FREE) so that QK^T of tile j+1
-    runs during the softmax of tile j, P and O reused after each PV (PV_DONE),
-    whose phases the softmax counts across units (pv_base)."""
-    NK, NI = 3, 4
+class _MlaPairModel:
+    """The mbarrier protocol of mla_pair_kernel (csrc/mla_pair_kernel.cuh):
+    two CTAs of a cluster take the same units in the same order (no unit
+    ring).  Per CTA: one K ring of four stages (the tile is also V); QK^T runs
+    two tiles ahead of PV, S is read and released early (S_FREE); P and O are
+    reused after each PV (PV_DONE), whose phases the softmax counts across
+    units (pv_base).
+
+    The partial S of each tile goes to the other CTA one tile ahead of its
+    softmax: the softmax reads S(t), releases it, waits until the other CTA
+    has read tile t - 1 from its receive buffer (XEMPTY, arrived from there)
+    and stores its partial there asynchronously; the bytes land later and
+    complete the other CTA's XFULL, which its thread 0 arms (one arrival) once
+    the previous phase has completed.  The softmax of tile t then adds the
+    received partial to its own and releases the buffer (XEMPTY of the other
+    CTA).  The model checks every buffer write and read against the buffer's
+    state."""
+    NK, NI = 4, 4
 
     def __init__(self, units, seed, mistake=None):
         self.rng = random.Random(seed)
         self.units, self.mistake = units, mistake
-        self.ring = [None] * RING
-        self.pending = []
-        self.bars = {n: _Bar(n, 1) for n in ("Q_FULL", "S_FULL", "P_FULL", "O_DONE", "S_FREE",
-                                              "PV_DONE")}
-        for s in range(RING):
-            self.bars[f"UF{s}"] = _Bar(f"UF{s}", 1)
-            self.bars[f"UE{s}"] = _Bar(f"UE{s}", 3)  # softmax, MMA, copy
-        for pre, n in (("K", self.NK), ("I", self.NI)):
-            for s in range(n):
-                self.bars[f"{pre}F{s}"] = _Bar(f"{pre}F{s}", 1)
-                self.bars[f"{pre}E{s}"] = _Bar(f"{pre}E{s}", 1)
+        self.pending = {0: [], 1: []}
+        self.xbuf = {0: None, 1: None}  # ("written" | "read", tile)
+        self.bars = {}
+        for c in (0, 1):
+            for n in ("Q_FULL", "S_FULL", "P_FULL", "O_DONE", "S_FREE", "PV_DONE", "XEMPTY"):
+                self.bars[f"{c}{n}"] = _Bar(f"{c}{n}", 1)
+            self.bars[f"{c}XFULL"] = _Bar(f"{c}XFULL", 2)  # the local arm + the stores' bytes
+            for pre, n in (("K", self.NK), ("I", self.NI)):
+                for s in range(n):
+                    self.bars[f"{c}{pre}F{s}"] = _Bar(f"{c}{pre}F{s}", 1)
+                    self.bars[f"{c}{pre}E{s}"] = _Bar(f"{c}{pre}E{s}", 1)
 
-    run = _Model.run
-    _wait = staticmethod(_Model._wait)
-    _units = _Model._units
+    @staticmethod
+    def _wait(bar, consumed):
+        return ("wait", bar, consumed & 1, consumed)
 
-    def _roles(self):
-        return {"index": self._index(), "copy": self._copy(), "softmax": self._softmax(),
-                "mma": self._mma()}
+    def run(self, max_steps=500000):
+        def ending(gen):  # every role ends with a no-op (a role may have no work)
+            yield from gen
+            yield ("end",)
 
-    def _index(self):
+        roles = {}
+        for c in (0, 1):
+            roles[f"{c}index"] = ending(self._index(c))
+            roles[f"{c}copy"] = ending(self._copy(c))
+            roles[f"{c}softmax"] = ending(self._softmax(c))
+            roles[f"{c}mma"] = ending(self._mma(c))
+        cur = {k: next(g) for k, g in roles.items()}
+        done = set()
+        for _ in range(max_steps):
+            for c in (0, 1):
+                if self.pending[c] and self.rng.random() < 0.3:
+                    ev = self.pending[c].pop(0)
+                    if isinstance(ev, tuple):  # stored bytes land in CTA ev[1]
+                        state = self.xbuf[ev[1]]
+                        assert state is None or state[0] == "read", "buffer overwritten"
+                        self.xbuf[ev[1]] = ("written", ev[2])
+                        self.bars[f"{ev[1]}XFULL"].arrive()
+                    else:
+                        self.bars[ev].arrive()
+            ready = [k for k, op in cur.items() if k not in done and
+                     (op[0] != "wait" or (self.bars[op[1]].phase & 1) != op[2])]
+            if not ready:
+                if self.pending[0] or self.pending[1]:
+                    continue
+                live = [k for k in cur if k not in done]
+                if not live:
+                    return
+                raise AssertionError("deadlock: " + ", ".join(f"{k} {cur[k]}" for k in live))
+            k = self.rng.choice(ready)
+            op = cur[k]
+            if op[0] == "wait":
+                assert self.bars[op[1]].phase == op[3] + 1, f"{k}: {op[1]} aliased"
+            elif op[0] == "use":
+                assert self.bars[op[1]].phase == op[2] + 1, f"{k}: read {op[1]} before its fill"
+            elif op[0] == "arrive":
+                self.bars[op[1]].arrive()
+            elif op[0] == "commit":
+                self.pending[int(op[1][0])].append(op[1])
+            elif op[0] == "send":  # asynchronous stores into the other CTA; they land later
+                self.pending[op[1]].append(("land", 1 - op[1], op[2]))
+            elif op[0] == "combine":  # the softmax reads the received partial of tile op[2]
+                assert self.xbuf[op[1]] == ("written", op[2]), f"{k}: partial read before it lands"
+                self.xbuf[op[1]] = ("read", op[2])
+            try:
+                cur[k] = next(roles[k])
+            except StopIteration:
+                done.add(k)
+        raise AssertionError("step limit")
+
+    def _index(self, c):
         ic = 0
-        for uc, u in enumerate(self.units + [None]):
-            s = uc % RING
-            if uc >= RING:
-                yield self._wait(f"UE{s}", uc // RING - 1)
-            self.ring[s] = u
-            yield ("arrive", f"UF{s}")
-            if u is None:
-                return
+        for u in self.units:
             for _ in range(u["nt"]):
                 si = ic % self.NI
                 if ic >= self.NI:
-                    yield self._wait(f"IE{si}", ic // self.NI - 1)
-                yield ("arrive", f"IF{si}")
+                    yield self._wait(f"{c}IE{si}", ic // self.NI - 1)
+                yield ("arrive", f"{c}IF{si}")
                 ic += 1
 
-    def _copy(self):
+    def _copy(self, c):
         kc = ic = 0
-        for op in self._units():
-            if op[0] != "unit":
-                yield op
-                continue
-            if op[1] is None:
-                return
-            for _ in range(op[1]["nt"]):
+        for u in self.units:
+            for _ in range(u["nt"]):
                 si = ic % self.NI
-                yield self._wait(f"IF{si}", ic // self.NI)
-                yield ("arrive", f"IE{si}")
+                yield self._wait(f"{c}IF{si}", ic // self.NI)
+                yield ("arrive", f"{c}IE{si}")
                 ic += 1
                 ks = kc % self.NK
                 if kc >= self.NK:
-                    yield self._wait(f"KE{ks}", kc // self.NK - 1)
-                yield ("arrive", f"KF{ks}")
+                    yield self._wait(f"{c}KE{ks}", kc // self.NK - 1)
+                yield ("arrive", f"{c}KF{ks}")
                 kc += 1
 
-    def _softmax(self):
-        s_cnt = o_cnt = pv_base = 0
-        for op in self._units():
-            if op[0] != "unit":
-                yield op
-                continue
-            u = op[1]
-            if u is None:
-                return
+    def _softmax(self, c):
+        s_cnt = o_cnt = pv_base = n_sent = n_recv = 0
+        peer = 1 - c
+
+        def send():
+            nonlocal s_cnt, n_sent
+            yield self._wait(f"{c}S_FULL", s_cnt)
+            s_cnt += 1
+            yield ("arrive", f"{c}S_FREE")
+            if n_sent > 0 and self.mistake != "no wait for the other CTA's read":
+                yield self._wait(f"{c}XEMPTY", n_sent - 1)
+            yield ("send", c, n_sent)
+            n_sent += 1
+
+        def combine():
+            nonlocal n_recv
+            early = self.mistake == "next phase armed before the wait"
+            if early:
+                yield ("arrive", f"{c}XFULL")
+            if self.mistake != "partial read before it lands":
+                yield self._wait(f"{c}XFULL", n_recv)
+            if not early:
+                yield ("arrive", f"{c}XFULL")  # arm the next tile's phase
+            yield ("combine", c, n_recv)
+            n_recv += 1
+            yield ("arrive", f"{peer}XEMPTY")
+
+        yield ("arrive", f"{c}XFULL")  # arm the first tile's phase
+        for u in self.units:
             nt = u["nt"]
             if nt == 0:
                 continue
-            yield ("arrive", "Q_FULL")  # the unit's Q rows written into TMEM
+            yield ("arrive", f"{c}Q_FULL")  # this CTA's Q dims written into TMEM
+            yield from send()
             for j in range(nt):
-                yield self._wait("S_FULL", s_cnt)
-                s_cnt += 1
-                yield ("arrive", "S_FREE")
+                yield from combine()
+                if j + 1 < nt:
+                    yield from send()
                 if j > 0 and self.mistake != "P written before the previous PV":
-                    yield self._wait("PV_DONE", pv_base + j - 1)
-                yield ("arrive", "P_FULL")
-            yield self._wait("O_DONE", o_cnt)
+                    yield self._wait(f"{c}PV_DONE", pv_base + j - 1)
+                yield ("arrive", f"{c}P_FULL")
+            yield self._wait(f"{c}O_DONE", o_cnt)
             o_cnt += 1
             if self.mistake != "PV count not carried across units":
                 pv_base += nt
 
-    def _mma(self):
+    def _mma(self, c):
         q_cnt = kc = s_free = p_cnt = 0
-        for op in self._units():
-            if op[0] != "unit":
-                yield op
-                continue
-            u = op[1]
-            if u is None:
-                return
+
+        def qk(kpos):
+            yield self._wait(f"{c}KF{kpos % self.NK}", kpos // self.NK)
+            yield ("use", f"{c}KF{kpos % self.NK}", kpos // self.NK)
+            yield ("commit", f"{c}S_FULL")
+
+        for u in self.units:
             nt = u["nt"]
             if nt == 0:
                 continue
-            yield self._wait("Q_FULL", q_cnt)
+            yield self._wait(f"{c}Q_FULL", q_cnt)
             q_cnt += 1
             k0 = kc
-            yield self._wait(f"KF{k0 % self.NK}", k0 // self.NK)
-            yield ("use", f"KF{k0 % self.NK}", k0 // self.NK)
-            yield ("commit", "S_FULL")
+            yield from qk(k0)
+            yield self._wait(f"{c}S_FREE", s_free)
+            s_free += 1
+            if nt > 1:
+                yield from qk(k0 + 1)
             for j in range(nt):
-                yield self._wait("S_FREE", s_free)
-                s_free += 1
                 if j + 1 < nt:
-                    kn = k0 + j + 1
-                    yield self._wait(f"KF{kn % self.NK}", kn // self.NK)
-                    yield ("use", f"KF{kn % self.NK}", kn // self.NK)
-                    yield ("commit", "S_FULL")
-                yield self._wait("P_FULL", p_cnt)
+                    yield self._wait(f"{c}S_FREE", s_free)
+                    s_free += 1
+                    if j + 2 < nt:
+                        yield from qk(k0 + j + 2)
+                yield self._wait(f"{c}P_FULL", p_cnt)
                 p_cnt += 1
-                yield ("use", f"KF{(k0 + j) % self.NK}", (k0 + j) // self.NK)  # V = the K tile
-                yield ("commit", "PV_DONE")
-                yield ("commit", f"KE{(k0 + j) % self.NK}")
+                yield ("use", f"{c}KF{(k0 + j) % self.NK}", (k0 + j) // self.NK)  # V = the K tile
+                yield ("commit", f"{c}PV_DONE")
+                yield ("commit", f"{c}KE{(k0 + j) % self.NK}")
             kc = k0 + nt
-            yield ("commit", "O_DONE")
+            yield ("commit", f"{c}O_DONE")
 
 
 def _mla_trials(n, mistake=None):
     rng = random.Random(2)
     for t in range(n):
         units = [{"nt": rng.choice([0, 1, 1, 2, 3, 5, 8])} for _ in range(rng.randint(1, 10))]
-        _MlaModel(units, seed=t, mistake=mistake).run()
+        _MlaPairModel(units, seed=t, mistake=mistake).run()
 
 
 def test_mla_protocol_has_no_deadlock_and_no_parity_aliasing():
@@ -515,7 +586,10 @@ def test_mla_protocol_has_no_deadlock_and_no_parity_aliasing():
 
 
 @pytest.mark.parametrize("mistake", ["P written before the previous PV",
-                                     "PV count not carried across units"])
+                                     "PV count not carried across units",
+                                     "partial read before it lands",
+                                     "no wait for the other CTA's read",
+                                     "next phase armed before the wait"])
 def test_mla_model_catches_planted_mistakes(mistake):
     with pytest.raises(AssertionError):
         _mla_trials(150, mistake)
