@@ -22,23 +22,28 @@
 //                   [192, 256) S, the partial of this rank (fp32)
 //                   [256, 512) O, 256 value dims (fp32)
 //   SMEM  four stages of a 64-key K tile (four 64-dim swizzle atoms of value
-//         dims and one atom whose first half holds the rope dims), the other
-//         rank's partial S of the current tile (16-byte chunk c of row r at
-//         c * 128 * 16 + r * 16), a ring of resolved row indices.
+//         dims and one atom whose first half holds the rope dims), two
+//         receive buffers of the other rank's partial S (tile t in buffer
+//         t & 1; 16-byte chunk c of row r at c * 128 * 16 + r * 16), a ring
+//         of resolved row indices.
 //
 // The exchange runs one tile ahead of the softmax, so that its latency hides
 // behind the softmax of the previous tile, and QK^T runs two tiles ahead of
 // PV.  In the iteration of tile j each softmax thread
 //   adds its own partial of tile j (kept in registers) to the other rank's
-//   (received in shared memory; XFULL), then releases the receive buffer
-//   (XEMPTY of the other rank, one arrival per warp);
+//   (received in shared memory; XFULL of the buffer);
 //   reads S(j + 1) into registers and releases it (S_FREE; QK^T of tile
-//   j + 2 follows), waits until the other rank has read tile j from its
-//   receive buffer (XEMPTY here), and writes its row of S(j + 1) there with
-//   asynchronous remote stores whose bytes complete the other rank's XFULL;
+//   j + 2 follows) and writes its row of S(j + 1) into the other rank's
+//   buffer (j + 1) & 1 with asynchronous remote stores whose bytes complete
+//   that buffer's XFULL there;
 //   runs the softmax of tile j and writes P(j).
-// XFULL is armed (one arrival that expects the tile's bytes) by thread 0
-// once the previous tile's phase has completed; the bytes may land first.
+// A buffer's XFULL is armed (one arrival that expects the tile's bytes) by
+// thread 0 once the buffer's previous phase has completed; the bytes may
+// land first.  No barrier frees a buffer: a thread sends tile t only after
+// tile t - 1 of all 128 threads of the other rank landed here, and each of
+// them read its row of tile t - 2 from the buffer before it sent tile t - 1
+// (the complete-tx of its stores releases at cluster scope, the wait here
+// acquires).
 // Both CTAs of a pair take the same units (position pair + k * pairs of the
 // claim order), so their tile counters stay in step.
 // Warps: 0-3 softmax (one row per thread; they also write Q into TMEM), 4 MMA
@@ -56,7 +61,7 @@ struct MlaPairCfg {
   static constexpr int I_BYTES = BN * 4;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_X = NK * K_BYTES;     // received from the other rank
-  static constexpr int OFF_I = OFF_X + X_BYTES;
+  static constexpr int OFF_I = OFF_X + 2 * X_BYTES;
   static constexpr int OFF_BAR = OFF_I + NI * I_BYTES;
   static constexpr int N_BARS = 16 + 2 * NK + 2 * NI;
   static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 1024;
@@ -85,8 +90,7 @@ enum {
   X_S_FREE = 5,   // S read into registers: the next QK^T may overwrite it
   X_PV_DONE = 6,  // one phase per PV: P and O are free again
   X_NEVER = 7,    // no thread ever arrives (the stall hook waits on it)
-  X_XFULL = 8,    // the other rank's partial landed (one arrival + its bytes)
-  X_XEMPTY = 9,   // the other rank has read what this CTA sent (4 remote arrivals)
+  X_XFULL = 8,    // + buffer: the other rank's partial landed (one arrival + its bytes)
   X_RING = 16
 };
 
@@ -128,8 +132,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     mbar_init(&bars[X_S_FREE], 4);
     mbar_init(&bars[X_PV_DONE], 1);
     mbar_init(&bars[X_NEVER], 1);
-    mbar_init(&bars[X_XFULL], 1);
-    mbar_init(&bars[X_XEMPTY], 4);
+    for (int b = 0; b < 2; ++b) mbar_init(&bars[X_XFULL + b], 1);
     for (int s = 0; s < C::NK; ++s) {
       mbar_init(&k_full[s], C::COPY_THREADS);
       mbar_init(&k_empty[s], 1);
@@ -164,15 +167,14 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     uint32_t s_cnt = 0, o_cnt = 0;
     uint32_t n_sent = 0, n_recv = 0;  // tiles sent / combined so far
     uint32_t pv_base = 0;  // PVs of earlier units (X_PV_DONE phases)
-    const uint32_t xempty_peer = cluster_addr(smem_u32(&bars[X_XEMPTY]), peer);
     const uint32_t xfull_peer = cluster_addr(smem_u32(&bars[X_XFULL]), peer);
-    // this thread's row of the receive buffer (chunk c at c * BM * 16), here
+    // this thread's row of receive buffer 0 (chunk c at c * BM * 16), here
     // and in the other rank
     const uint8_t *recv_row = smem + C::OFF_X + r * 16;
     const uint32_t send_row = cluster_addr(sbase + C::OFF_X + r * 16, peer);
     uint32_t own[C::BN];  // this rank's partial S of the next tile
     // S of the next tile into registers, released for the next QK^T, and
-    // sent to the other rank once it has read the previous tile
+    // sent to the other rank
     auto send = [&]() -> bool {
       if (!mbar_wait(&bars[X_S_FULL], s_cnt & 1u, abort_flag, p.wait_ns)) return false;
       ++s_cnt;
@@ -183,38 +185,40 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[X_S_FREE]);
-      if (n_sent > 0 &&
-          !mbar_wait_cluster(&bars[X_XEMPTY], (n_sent - 1) & 1u, abort_flag, p.wait_ns))
-        return false;
+      const uint32_t b = n_sent & 1u;
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        st_async_cluster_u4(send_row + c * (C::BM * 16),
+        st_async_cluster_u4(send_row + b * C::X_BYTES + c * (C::BM * 16),
                             make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
-                            xfull_peer);
+                            xfull_peer + b * 8u);
       ++n_sent;
       return true;
     };
     // both partials of the current tile added (own + other in both ranks:
-    // the same sum bit for bit), the receive buffer released
+    // the same sum bit for bit)
     auto combine = [&](float (&x)[C::BN]) -> bool {
-      if (!mbar_wait_cluster(&bars[X_XFULL], n_recv & 1u, abort_flag, p.wait_ns)) return false;
+      const uint32_t b = n_recv & 1u;
+      if (!mbar_wait_cluster(&bars[X_XFULL + b], (n_recv >> 1) & 1u, abort_flag, p.wait_ns))
+        return false;
       ++n_recv;
-      // the phase of the next tile (its bytes cannot land before every warp
-      // here has released this one)
-      if (tid == 0) mbar_arrive_expect_tx(&bars[X_XFULL], C::X_BYTES);
+      // the buffer's phase for tile n_recv + 1 (its bytes cannot land before
+      // every warp here has released this tile)
+      if (tid == 0) mbar_arrive_expect_tx(&bars[X_XFULL + b], C::X_BYTES);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        const uint4 o4 = *reinterpret_cast<const uint4 *>(recv_row + c * (C::BM * 16));
+        const uint4 o4 =
+            *reinterpret_cast<const uint4 *>(recv_row + b * C::X_BYTES + c * (C::BM * 16));
         x[4 * c + 0] = __uint_as_float(own[4 * c + 0]) + __uint_as_float(o4.x);
         x[4 * c + 1] = __uint_as_float(own[4 * c + 1]) + __uint_as_float(o4.y);
         x[4 * c + 2] = __uint_as_float(own[4 * c + 2]) + __uint_as_float(o4.z);
         x[4 * c + 3] = __uint_as_float(own[4 * c + 3]) + __uint_as_float(o4.w);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(xempty_peer);
       return true;
     };
-    if (tid == 0) mbar_arrive_expect_tx(&bars[X_XFULL], C::X_BYTES);  // the first tile
+    if (tid == 0) {  // the first two tiles
+      mbar_arrive_expect_tx(&bars[X_XFULL], C::X_BYTES);
+      mbar_arrive_expect_tx(&bars[X_XFULL + 1], C::X_BYTES);
+    }
     if (p.stall && !mbar_wait(&bars[X_NEVER], 0, abort_flag, p.wait_ns))
       abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
     for (uint32_t uc = 0; !*abort_flag; ++uc) {

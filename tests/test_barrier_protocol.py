@@ -386,26 +386,26 @@ class _MlaPairModel:
     units (pv_base).
 
     The partial S of each tile goes to the other CTA one tile ahead of its
-    softmax: the softmax reads S(t), releases it, waits until the other CTA
-    has read tile t - 1 from its receive buffer (XEMPTY, arrived from there)
+    softmax, into receive buffer t & 1: the softmax reads S(t), releases it
     and stores its partial there asynchronously; the bytes land later and
-    complete the other CTA's XFULL, which its thread 0 arms (one arrival) once
-    the previous phase has completed.  The softmax of tile t then adds the
-    received partial to its own and releases the buffer (XEMPTY of the other
-    CTA).  The model checks every buffer write and read against the buffer's
-    state."""
+    complete the other CTA's XFULL of the buffer, which its thread 0 arms
+    (one arrival) once the buffer's previous phase has completed.  The
+    softmax of tile t then adds the received partial to its own.  No barrier
+    frees a buffer; the model checks every buffer write and read against the
+    buffer's state, so a send that could overwrite an unread tile fails."""
     NK, NI = 4, 4
 
     def __init__(self, units, seed, mistake=None):
         self.rng = random.Random(seed)
         self.units, self.mistake = units, mistake
         self.pending = {0: [], 1: []}
-        self.xbuf = {0: None, 1: None}  # ("written" | "read", tile)
+        self.xbuf = {(c, b): None for c in (0, 1) for b in (0, 1)}  # ("written" | "read", tile)
         self.bars = {}
         for c in (0, 1):
-            for n in ("Q_FULL", "S_FULL", "P_FULL", "O_DONE", "S_FREE", "PV_DONE", "XEMPTY"):
+            for n in ("Q_FULL", "S_FULL", "P_FULL", "O_DONE", "S_FREE", "PV_DONE"):
                 self.bars[f"{c}{n}"] = _Bar(f"{c}{n}", 1)
-            self.bars[f"{c}XFULL"] = _Bar(f"{c}XFULL", 2)  # the local arm + the stores' bytes
+            for b in (0, 1):  # the local arm + the stores' bytes
+                self.bars[f"{c}XFULL{b}"] = _Bar(f"{c}XFULL{b}", 2)
             for pre, n in (("K", self.NK), ("I", self.NI)):
                 for s in range(n):
                     self.bars[f"{c}{pre}F{s}"] = _Bar(f"{c}{pre}F{s}", 1)
@@ -432,11 +432,12 @@ class _MlaPairModel:
             for c in (0, 1):
                 if self.pending[c] and self.rng.random() < 0.3:
                     ev = self.pending[c].pop(0)
-                    if isinstance(ev, tuple):  # stored bytes land in CTA ev[1]
-                        state = self.xbuf[ev[1]]
+                    if isinstance(ev, tuple):  # stored bytes land in CTA ev[1], buffer ev[2] & 1
+                        key = (ev[1], ev[2] & 1 if self.mistake != "one receive buffer" else 0)
+                        state = self.xbuf[key]
                         assert state is None or state[0] == "read", "buffer overwritten"
-                        self.xbuf[ev[1]] = ("written", ev[2])
-                        self.bars[f"{ev[1]}XFULL"].arrive()
+                        self.xbuf[key] = ("written", ev[2])
+                        self.bars[f"{ev[1]}XFULL{ev[2] & 1}"].arrive()
                     else:
                         self.bars[ev].arrive()
             ready = [k for k, op in cur.items() if k not in done and
@@ -461,8 +462,9 @@ class _MlaPairModel:
             elif op[0] == "send":  # asynchronous stores into the other CTA; they land later
                 self.pending[op[1]].append(("land", 1 - op[1], op[2]))
             elif op[0] == "combine":  # the softmax reads the received partial of tile op[2]
-                assert self.xbuf[op[1]] == ("written", op[2]), f"{k}: partial read before it lands"
-                self.xbuf[op[1]] = ("read", op[2])
+                key = (op[1], op[2] & 1 if self.mistake != "one receive buffer" else 0)
+                assert self.xbuf[key] == ("written", op[2]), f"{k}: partial read before it lands"
+                self.xbuf[key] = ("read", op[2])
             try:
                 cur[k] = next(roles[k])
             except StopIteration:
@@ -495,32 +497,30 @@ class _MlaPairModel:
 
     def _softmax(self, c):
         s_cnt = o_cnt = pv_base = n_sent = n_recv = 0
-        peer = 1 - c
 
         def send():
             nonlocal s_cnt, n_sent
             yield self._wait(f"{c}S_FULL", s_cnt)
             s_cnt += 1
             yield ("arrive", f"{c}S_FREE")
-            if n_sent > 0 and self.mistake != "no wait for the other CTA's read":
-                yield self._wait(f"{c}XEMPTY", n_sent - 1)
             yield ("send", c, n_sent)
             n_sent += 1
 
         def combine():
             nonlocal n_recv
+            b = n_recv & 1
             early = self.mistake == "next phase armed before the wait"
             if early:
-                yield ("arrive", f"{c}XFULL")
+                yield ("arrive", f"{c}XFULL{b}")
             if self.mistake != "partial read before it lands":
-                yield self._wait(f"{c}XFULL", n_recv)
+                yield self._wait(f"{c}XFULL{b}", n_recv >> 1)
             if not early:
-                yield ("arrive", f"{c}XFULL")  # arm the next tile's phase
+                yield ("arrive", f"{c}XFULL{b}")  # arm the buffer's phase for tile n_recv + 2
             yield ("combine", c, n_recv)
             n_recv += 1
-            yield ("arrive", f"{peer}XEMPTY")
 
-        yield ("arrive", f"{c}XFULL")  # arm the first tile's phase
+        yield ("arrive", f"{c}XFULL0")  # arm the first two tiles' phases
+        yield ("arrive", f"{c}XFULL1")
         for u in self.units:
             nt = u["nt"]
             if nt == 0:
@@ -588,8 +588,8 @@ def test_mla_protocol_has_no_deadlock_and_no_parity_aliasing():
 @pytest.mark.parametrize("mistake", ["P written before the previous PV",
                                      "PV count not carried across units",
                                      "partial read before it lands",
-                                     "no wait for the other CTA's read",
-                                     "next phase armed before the wait"])
+                                     "next phase armed before the wait",
+                                     "one receive buffer"])
 def test_mla_model_catches_planted_mistakes(mistake):
     with pytest.raises(AssertionError):
         _mla_trials(150, mistake)
