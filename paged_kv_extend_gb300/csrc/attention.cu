@@ -556,7 +556,12 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NK * K_BYTES;
   static constexpr int OFF_I = OFF_V + NV * V_BYTES;
   static constexpr int OFF_BAR = OFF_I + NI * I_BYTES;
-  static constexpr int N_BARS = 17 + 2 * NK + 2 * NV + 2 * NI;
+  // decode over an fp8 pool: the codes land in a ring of NRAW slots (the
+  // unused second Q tile and K stage 0) and are converted from there
+  static constexpr int NRAW = 4;
+  static constexpr int RAW_BYTES = BN * LQ;  // the fp8 codes of one K or V tile
+  static constexpr int OFF_RAW = OFF_Q + Q_BYTES;
+  static constexpr int N_BARS = 17 + 2 * NK + 2 * NV + 2 * NI + 2 * NRAW;
   static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 1024;  // + alignment slack
   // S0 | S1 | O0 | O1, 128 columns each (split dims: S0 | unused | O0 of Lv)
   static constexpr int TMEM_COLS = 512;
@@ -579,6 +584,8 @@ struct Cfg {
   static_assert(256 * REGS_SOFTMAX + 256 * REGS_OTHER == THREADS * REGS_LAUNCH,
                 "register split must match the launch allocation");
   static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(SPLIT || NRAW * RAW_BYTES == Q_BYTES + K_BYTES,
+                "the raw ring fills the second Q tile and K stage 0");
 };
 
 // barrier indices
@@ -594,7 +601,7 @@ enum {
   B_Q_CONV = 15,   // decode over fp8: the query rows converted to f16
   B_NEVER = 16,    // no thread ever arrives (the stall hook waits on it)
   B_RING = 17,  // K full[NK], K empty[NK], V full[NV], V empty[NV],
-                // I full[NI], I empty[NI]
+                // I full[NI], I empty[NI], raw full[NRAW], raw empty[NRAW]
 };
 
 // Key range [kb, ke) of tile j of a unit (tiles never straddle k_split).
@@ -716,6 +723,12 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
   constexpr bool F16 = FMT != 0 && MODE == kDecode;
   constexpr uint32_t IDQK = F16 ? idesc_f16_f32(C::BM, C::BN, 0) : C::IDESC_QK;
   constexpr uint32_t IDPV = F16 ? idesc_f16_f32(C::BM, C::HDV, 1) : C::IDESC_PV;
+  // K ring: decode over fp8 gives stage 0 to the raw-code ring
+  constexpr int NK_ = F16 ? C::NK - 1 : C::NK;
+  constexpr uint32_t K0 = C::OFF_K + (F16 ? C::K_BYTES : 0);
+  // decode over fp8: warps 10-11 copy the codes, warps 12-13 convert the K
+  // tiles and 14-15 the V tiles
+  constexpr int RAW_THREADS = 64, CONV_THREADS = 64;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -731,6 +744,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
   uint64_t *v_empty = v_full + C::NV;
   uint64_t *i_full = v_empty + C::NV;
   uint64_t *i_empty = i_full + C::NI;
+  uint64_t *raw_full = i_empty + C::NI;
+  uint64_t *raw_empty = raw_full + C::NRAW;
   volatile int *abort_flag = &s_abort;
 
   const int tid = threadIdx.x;
@@ -739,7 +754,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
 
   if (tid == 0) {
     mbar_init(&bars[B_Q_FULL], 1);
-    mbar_init(&bars[B_Q_CONV], C::COPY_THREADS);
+    mbar_init(&bars[B_Q_CONV], C::COPY_THREADS);  // decode over fp8: warps 12-15
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[B_S_FULL + i], 1);
@@ -752,19 +767,26 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       mbar_init(&bars[B_U_FULL + i], 1);
       // softmax, MMA and copy warps (+ the two writer warps with the fused
       // KV write)
-      mbar_init(&bars[B_U_EMPTY + i], 8 + 1 + C::COPY_THREADS / 32 + (kv_write ? 2 : 0));
+      mbar_init(&bars[B_U_EMPTY + i],
+                8 + 1 + C::COPY_THREADS / 32 + (kv_write || F16 ? 2 : 0));
     }
+    // stages are filled by the copy warps, or by the converting warps in
+    // decode over fp8
     for (int s = 0; s < C::NK; ++s) {
-      mbar_init(&k_full[s], C::COPY_THREADS);
+      mbar_init(&k_full[s], F16 ? CONV_THREADS : C::COPY_THREADS);
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < C::NV; ++s) {
-      mbar_init(&v_full[s], C::COPY_THREADS);
+      mbar_init(&v_full[s], F16 ? CONV_THREADS : C::COPY_THREADS);
       mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < C::NRAW; ++s) {
+      mbar_init(&raw_full[s], RAW_THREADS);
+      mbar_init(&raw_empty[s], CONV_THREADS);
     }
     for (int s = 0; s < C::NI; ++s) {
       mbar_init(&i_full[s], 32);
-      mbar_init(&i_empty[s], C::COPY_THREADS / 32);
+      mbar_init(&i_empty[s], (F16 ? RAW_THREADS : C::COPY_THREADS) / 32);
     }
     s_abort = 0;
     fence_barrier_init();
@@ -1193,11 +1215,11 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
               if (leader) tc_commit(&v_empty[vs]);
               ++vc;
             }
-            const int ks = kc % C::NK;
-            if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
+            const int ks = kc % NK_;
+            if (!mbar_wait(&k_full[ks], (kc / NK_) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
             fence_proxy_async_smem();
             tc_fence_after();
-            issue_s_q0(b, sbase + C::OFF_K + ks * C::K_BYTES);
+            issue_s_q0(b, sbase + K0 + ks * C::K_BYTES);
             if (leader) tc_commit(&k_empty[ks]);
             ++kc;
             if (j == nt - 1 && leader) tc_commit(&bars[B_Q_EMPTY]);
@@ -1224,11 +1246,11 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         }
         // tile 0: S of both Q tiles
         {
-          const int ks = kc % C::NK;
-          if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
+          const int ks = kc % NK_;
+          if (!mbar_wait(&k_full[ks], (kc / NK_) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.mma reads
           tc_fence_after();
-          const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
+          const uint32_t sK = sbase + K0 + ks * C::K_BYTES;
           issue_s(0, sK);
           if (q1) issue_s(1, sK);
           if (leader) tc_commit(&k_empty[ks]);
@@ -1236,14 +1258,14 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           if (nt == 1 && leader) tc_commit(&bars[B_Q_EMPTY]);
         }
         for (int j = 1; j < nt && ok; ++j) {
-          const int ks = kc % C::NK, vs = vc % C::NV;
-          if (!mbar_wait(&k_full[ks], (kc / C::NK) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
+          const int ks = kc % NK_, vs = vc % C::NV;
+          if (!mbar_wait(&k_full[ks], (kc / NK_) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           if (!mbar_wait(&v_full[vs], (vc / C::NV) & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           if (!mbar_wait(&bars[B_P_FULL + 0], p_cnt0 & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           ++p_cnt0;
           fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES;
+          const uint32_t sK = sbase + K0 + ks * C::K_BYTES;
           const uint32_t sV = sbase + C::OFF_V + vs * C::V_BYTES;
           issue_pv(0, sV, j > 1);
           issue_s(0, sK);
@@ -1392,6 +1414,173 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     if (lane == 0 && q_cnt > 0 && !mbar_wait_drain(&bars[B_Q_FULL], (q_cnt - 1) & 1u))
       record_status(p.status, PKX_ETIMEOUT);
     __syncwarp();
+  } else if (F16 && warp >= 12) {
+    // ------------------------------- fp8 codes -> f16 stages (warps 12-15)
+    // Decode over an fp8 pool: each raw slot (K(j) and V(j) alternate, in
+    // the order the copying warps issue them) is converted into the next
+    // stage of its ring once its codes have landed and the stage is free;
+    // warps 12-13 take the K slots and 14-15 the V slots, so that neither
+    // ring waits behind the other.  Chunk c of a slot holds the eight codes
+    // of key c / CPR, dims 8 (c % CPR) + [0, 8); thread cv of a group
+    // converts chunks cv + 64 m, so a warp reads 256 contiguous bytes and
+    // writes whole 128-byte rows of the swizzled stage.  Its chunk index
+    // (c % CPR) and the key's swizzle phase are the same for every m, so
+    // source and destination step by constants.  All four warps convert
+    // each unit's query rows to f16 (Q_CONV).
+    if constexpr (F16) {
+    constexpr int CPR = HD / 8;
+    constexpr int NCH = C::BN * CPR / CONV_THREADS;
+    constexpr int KSTEP = CONV_THREADS / CPR;  // keys between a thread's chunks
+    // swizzle phases (key % 8) a thread's keys cycle through
+    constexpr int NPH = KSTEP % 8 == 0 ? 1 : 8 / KSTEP;
+    static_assert(C::BN * CPR % CONV_THREADS == 0 && NCH % NPH == 0 &&
+                      (KSTEP % 8 == 0 || 8 % KSTEP == 0),
+                  "conversion geometry");
+    const int grp = warp >= 14;                // 0: K slots, 1: V slots
+    const int cq = tid - 12 * 32;              // 0 .. 127 for the query rows
+    const int cv = cq - grp * CONV_THREADS;    // 0 .. 63 within the group
+    const int ck = cv % CPR, key0 = cv / CPR;
+    const uint32_t sthr = (uint32_t)cv * 8u;
+    uint32_t dthr[NPH];  // chunk m = NPH mm + ph: key key0 + KSTEP m
+#pragma unroll
+    for (int ph = 0; ph < NPH; ++ph) {
+      const int key = key0 + KSTEP * ph;
+      dthr[ph] = (uint32_t)(ck >> 3) * (C::BN * 128) + (uint32_t)key * 128u +
+                 ((uint32_t)((ck & 7) ^ (key & 7)) << 4);
+    }
+    uint32_t rc = grp, kc = 0, vc = 0, qc = 0;  // rc: slot use (K even, V odd)
+    bool ok = true;
+    // the group's next slot into `stage` once both are ready
+    auto convert_slot = [&](uint64_t *st_empty, uint32_t n_used, int n_stages, uint32_t stage,
+                            uint64_t *st_full) -> bool {
+      const int s = rc % C::NRAW;
+      if (!mbar_wait(&raw_full[s], (rc / C::NRAW) & 1u, abort_flag, p.wait_ns)) return false;
+      if (n_used >= (uint32_t)n_stages &&
+          !mbar_wait(st_empty, ((n_used / n_stages) - 1) & 1u, abort_flag, p.wait_ns))
+        return false;
+      const uint32_t src = sbase + C::OFF_RAW + s * C::RAW_BYTES + sthr;
+#pragma unroll 2
+      for (int mm = 0; mm < NCH / NPH; ++mm) {
+#pragma unroll
+        for (int ph = 0; ph < NPH; ++ph)
+          st_shared_u4(stage + dthr[ph] + mm * (KSTEP * NPH * 128),
+                       fp8x8_to_f16x8<FMT>(
+                           ld_shared_u2(src + (mm * NPH + ph) * (CONV_THREADS * 8))));
+      }
+      fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+      mbar_arrive(st_full);
+      mbar_arrive(&raw_empty[s]);
+      rc += 2;
+      return true;
+    };
+    for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+      const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ok, p.wait_ns);
+      if (u < 0) break;
+      const WorkUnit w = p.units[p.uorder[u]];
+      const int nt = w.n_tiles;
+      if (nt == 0) continue;
+      // the unit's query rows (tokens x G heads of query tile 0) to f16 in
+      // place once their load has landed, 16 bytes at a time (the swizzle
+      // only permutes whole chunks within a row)
+      if (!mbar_wait(&bars[B_Q_FULL], qc & 1u, abort_flag, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      ++qc;
+      const int n_chunks = w.n_tok * G * (HD / 8);
+      for (int c = cq; c < n_chunks; c += 2 * CONV_THREADS) {
+        const int row = c / (HD / 8), k = c % (HD / 8);
+        const uint32_t off = C::OFF_Q + (uint32_t)(k >> 3) * (C::BM * 128) + (uint32_t)row * 128u +
+                             (uint32_t)(k & 7) * 16u;
+        const uint4 v = *reinterpret_cast<const uint4 *>(smem + off);
+        st_shared_u4(sbase + off, bf16x8_to_f16x8_scaled(v));
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[B_Q_CONV]);
+      for (int j = 0; j < nt; ++j) {
+        const int ks = kc % NK_, vs = vc % C::NV;
+        if (grp == 0 ? !convert_slot(&k_empty[ks], kc, NK_, sbase + K0 + ks * C::K_BYTES, &k_full[ks])
+                     : !convert_slot(&v_empty[vs], vc, C::NV, sbase + C::OFF_V + vs * C::V_BYTES,
+                                     &v_full[vs])) {
+          ok = false;
+          break;
+        }
+        if (grp == 0) ++kc;
+        else ++vc;
+      }
+    }
+    if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+    }
+  } else if (F16) {
+    // ------------------------------------ fp8 codes into raw slots (warps 10-11)
+    // Decode over an fp8 pool: the codes of each K and V tile go
+    // fire-and-forget into the next slot of the raw ring (row-major, 8 bytes
+    // per (key, chunk)) once the converting warps have read what it held;
+    // each thread arrives (noinc) on the slot's barrier when its own copies
+    // land.  Thread ct copies chunk ct % CPR of keys ct / CPR + KG i.
+    if constexpr (F16) {
+    constexpr int CPR = HD / 8, KG = RAW_THREADS / CPR, NKEYS = C::BN / KG;
+    constexpr int KPP = C::KPP, NK_T = C::BN / KPP;  // the index ring's layout
+    static_assert(KG * CPR == RAW_THREADS && C::BN % KG == 0, "copy geometry");
+    const int ct = tid - C::COPY_WARP0 * 32;
+    const int ch = ct % CPR, kg = ct / CPR;
+    const uint32_t rthr = (uint32_t)(kg * CPR + ch) * 8u;
+    uint32_t rc = 0, ic = 0;
+    bool ok = true;
+    for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+      const int u = ring_unit(&bars[B_U_FULL], &bars[B_U_EMPTY], s_unit, uc, abort_flag, true, ok, p.wait_ns);
+      if (u < 0) break;
+      const WorkUnit w = p.units[p.uorder[u]];
+      const int nt = w.n_tiles;
+      if (nt == 0) continue;
+      const uint8_t *kp8 =
+          reinterpret_cast<const uint8_t *>(p.k_pool) + (int64_t)w.kvh * p.kb_sh + ch * 8;
+      const uint8_t *vp8 =
+          reinterpret_cast<const uint8_t *>(p.v_pool) + (int64_t)w.kvh * p.vb_sh + ch * 8;
+      for (int j = 0; j < nt && ok; ++j) {
+        // this thread's rows (the index ring holds key's row at
+        // [key % KPP][key / KPP])
+        const int is = ic % C::NI;
+        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        int rows[NKEYS];
+        {
+          const int *ring = reinterpret_cast<const int *>(smem + C::OFF_I + is * C::I_BYTES);
+#pragma unroll
+          for (int i = 0; i < NKEYS; ++i) {
+            const int key = kg + KG * i;
+            rows[i] = ring[(key % KPP) * NK_T + key / KPP];
+          }
+        }
+        __syncwarp();  // the warp is done with the ring slot
+        if (lane == 0) mbar_arrive(&i_empty[is]);
+        ++ic;
+        for (int t = 0; t < 2; ++t) {  // K(j), then V(j)
+          const int s = rc % C::NRAW;
+          if (rc >= (uint32_t)C::NRAW &&
+              !mbar_wait(&raw_empty[s], ((rc / C::NRAW) - 1) & 1u, abort_flag, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          const uint8_t *base = t == 0 ? kp8 : vp8;
+          const int64_t stride = t == 0 ? p.kb_ss : p.vb_ss;
+          const uint32_t slot = sbase + C::OFF_RAW + s * C::RAW_BYTES + rthr;
+          static_for<0, NKEYS>([&](auto i_c) {
+            constexpr int i = decltype(i_c)::value;
+            const int r = rows[i];
+            const uint8_t *src = base + (int64_t)max(r, 0) * stride;
+            cp_async_8_at<i * KG * CPR * 8>(slot, src, r >= 0 ? 8u : 0u);
+          });
+          cp_async_arrive_noinc(&raw_full[s]);
+          ++rc;
+        }
+      }
+    }
+    if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+    cp_async_wait_all();
+    }
   } else if (warp < C::COPY_WARP0 + C::COPY_THREADS / 32) {
     // ------------------------------------------------ K/V copies (4 warps)
     // Thread ct copies 16-byte chunk ch = ct % CPR of keys key0 + KPP * i
@@ -1475,13 +1664,13 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           if (lane == 0) mbar_arrive(&i_empty[is]);
           ++ic;
           // K tile
-          const int ks = kc % C::NK;
-          if (kc >= (uint32_t)C::NK &&
-              !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag, p.wait_ns)) {
+          const int ks = kc % NK_;
+          if (kc >= (uint32_t)NK_ &&
+              !mbar_wait(&k_empty[ks], ((kc / NK_) - 1) & 1u, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
-          copy_rows(sbase + C::OFF_K + ks * C::K_BYTES, from_ext ? kx : kp,
+          copy_rows(sbase + K0 + ks * C::K_BYTES, from_ext ? kx : kp,
                     from_ext ? p.ke_st : p.kb_ss, rows, K_LEN);
           cp_async_arrive_noinc(&k_full[ks]);
           ++kc;
@@ -1499,7 +1688,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         }
       }
     } else {
-    // fp8 pool.  A pool tile's codes are copied 8 bytes per (thread, key)
+    // extend over an fp8 pool.  A pool tile's codes are copied 8 bytes per (thread, key)
     // into the first half of the 16-byte chunk the same thread later
     // writes, and converted there in place to bf16 once they have landed, so no thread overwrites another's codes.  The copies
     // of tile j+1 go out before tile j is converted, in the order
@@ -1519,8 +1708,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       static_for<0, NKEYS>([&](auto i_c) {
         constexpr int i = decltype(i_c)::value;
         const uint32_t a = stage + dthr + i * KPP * 128;
-        if constexpr (F16) st_shared_u4(a, fp8x8_to_f16x8<FMT>(ld_shared_u2(a)));
-        else st_shared_u4(a, fp8x8_to_bf16x8<FMT>(ld_shared_u2(a)));
+        st_shared_u4(a, fp8x8_to_bf16x8<FMT>(ld_shared_u2(a)));
       });
       fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
     };
@@ -1561,11 +1749,11 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         return true;
       };
       auto issue_k = [&](bool from_ext) -> bool {
-        const int ks = kc % C::NK;
-        if (kc >= (uint32_t)C::NK &&
-            !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag, p.wait_ns))
+        const int ks = kc % NK_;
+        if (kc >= (uint32_t)NK_ &&
+            !mbar_wait(&k_empty[ks], ((kc / NK_) - 1) & 1u, abort_flag, p.wait_ns))
           return false;
-        const uint32_t stage = sbase + C::OFF_K + ks * C::K_BYTES;
+        const uint32_t stage = sbase + K0 + ks * C::K_BYTES;
         if (from_ext) {
           copy_rows(stage, kx, p.ke_st, rows, K_LEN);
           cp_async_arrive_noinc(&k_full[ks]);
@@ -1597,28 +1785,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         ok = false;
         break;
       }
-      if constexpr (F16) {
-        // the unit's query rows (tokens x G heads of query tile 0) to f16 in
-        // place once their load has landed, 16 bytes at a time (the swizzle
-        // only permutes whole chunks within a row)
-        if (!mbar_wait(&bars[B_Q_FULL], qc & 1u, abort_flag, p.wait_ns)) {
-          ok = false;
-          break;
-        }
-        ++qc;
-        const int n_chunks = w.n_tok * G * (HD / 8);
-        for (int c = ct; c < n_chunks; c += C::COPY_THREADS) {
-          const int row = c / (HD / 8), k = c % (HD / 8);
-          const uint32_t off = C::OFF_Q + (uint32_t)(k >> 3) * (C::BM * 128) +
-                               (uint32_t)row * 128u + (uint32_t)(k & 7) * 16u;
-          const uint4 v = *reinterpret_cast<const uint4 *>(smem + off);
-          st_shared_u4(sbase + off, bf16x8_to_f16x8_scaled(v));
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[B_Q_CONV]);
-      }
       for (int j = 0; j < nt; ++j) {
-        const int ks_j = (kc - 1) % C::NK, vs_j = (vc - 1) % C::NV;
+        const int ks_j = (kc - 1) % NK_, vs_j = (vc - 1) % C::NV;
         const bool more = j + 1 < nt;
         const bool ext_n = more && tile_from_ext(j + 1);
         if (more && (!fetch() || !issue_k(ext_n))) {
@@ -1629,7 +1797,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           // groups issued after K(j): V(j), and K(j+1) if there is one
           if (more) cp_async_wait_group<2>();
           else cp_async_wait_group<1>();
-          convert(sbase + C::OFF_K + ks_j * C::K_BYTES);
+          convert(sbase + K0 + ks_j * C::K_BYTES);
           mbar_arrive(&k_full[ks_j]);
         }
         if (more && !issue_v(ext_n)) {

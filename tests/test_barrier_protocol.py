@@ -28,6 +28,7 @@ import random
 import pytest
 
 NK, NV, NI, RING = 3, 2, 3, 3
+NRAW = 4  # raw-code slots of decode over an fp8 pool
 
 
 class _Bar:
@@ -50,26 +51,36 @@ class _Model:
         self.units = units
         self.mistake = mistake
         self.fp8 = fp8 or f16_decode  # an fp8 pool: codes converted in shared memory
-        self.f16 = f16_decode  # decode over an fp8 pool: the copy warps also convert Q
+        # decode over an fp8 pool: the copy warps put the codes into a ring of
+        # raw slots (and convert Q); two converting warps fill the stages
+        self.f16 = f16_decode
+        self.raw = [None] * NRAW  # ("issued" | "landed" | "converted", slot use)
+        self.landing = []  # raw slots whose copies are in flight, in issue order
         self.ring = [None] * RING
         self.pending = []  # barriers of the MMA thread's commits, in issue order
         self.bars = {}
-        for name, count in [("Q_FULL", 1), ("Q_EMPTY", 1), ("Q_CONV", 1)]:
+        # the query rows of decode over fp8 are converted by both converting groups
+        for name, count in [("Q_FULL", 1), ("Q_EMPTY", 1), ("Q_CONV", 2 if f16_decode else 1)]:
             self.bars[name] = _Bar(name, count)
         for b in range(2):
             for name in ("S", "P", "O"):
                 self.bars[f"{name}{b}"] = _Bar(f"{name}{b}", 1)
         for s in range(RING):
             self.bars[f"UF{s}"] = _Bar(f"UF{s}", 1)
-            self.bars[f"UE{s}"] = _Bar(f"UE{s}", 4)  # two warpgroups, MMA, copy
-        for pre, n in (("K", self.NK), ("V", self.NV), ("I", self.NI)):
+            # two warpgroups, MMA, copy (+ the two converting groups)
+            self.bars[f"UE{s}"] = _Bar(f"UE{s}", 6 if self.f16 else 4)
+        for pre, n in (("K", self.NK), ("V", self.NV), ("I", self.NI), ("R", NRAW)):
             for s in range(n):
                 self.bars[f"{pre}F{s}"] = _Bar(f"{pre}F{s}", 1)
                 self.bars[f"{pre}E{s}"] = _Bar(f"{pre}E{s}", 1)
 
     def _roles(self):
-        return {"index": self._index(), "copy": self._copy(), "wg0": self._softmax(0),
-                "wg1": self._softmax(1), "mma": self._mma()}
+        roles = {"index": self._index(), "copy": self._copy(), "wg0": self._softmax(0),
+                 "wg1": self._softmax(1), "mma": self._mma()}
+        if self.f16:
+            roles["convert_k"] = self._convert("K")
+            roles["convert_v"] = self._convert("V")
+        return roles
 
     def run(self, max_steps=500000):
         roles = self._roles()
@@ -78,10 +89,15 @@ class _Model:
         for _ in range(max_steps):
             if self.pending and self.rng.random() < 0.3:
                 self.bars[self.pending.pop(0)].arrive()  # the oldest product completes
+            if self.landing and self.rng.random() < 0.3:  # the oldest raw slot's codes land
+                s, use = self.landing.pop(0)
+                assert self.raw[s] == ("issued", use)
+                self.raw[s] = ("landed", use)
+                self.bars[f"RF{s}"].arrive()
             ready = [k for k, op in cur.items() if k not in done and
                      (op[0] != "wait" or (self.bars[op[1]].phase & 1) != op[2])]
             if not ready:
-                if self.pending:
+                if self.pending or self.landing:
                     continue
                 live = [k for k in cur if k not in done]
                 if not live:
@@ -97,6 +113,14 @@ class _Model:
                 self.bars[op[1]].arrive()
             elif op[0] == "commit":
                 self.pending.append(op[1])
+            elif op[0] == "raw_issue":  # the copies of slot use op[2] into slot op[1]
+                assert self.raw[op[1]] in (None, ("converted", op[2] - NRAW)), \
+                    f"{k}: raw slot {op[1]} overwritten before its conversion"
+                self.raw[op[1]] = ("issued", op[2])
+                self.landing.append((op[1], op[2]))
+            elif op[0] == "raw_convert":
+                assert self.raw[op[1]] == ("landed", op[2]), f"{k}: raw slot converted before it landed"
+                self.raw[op[1]] = ("converted", op[2])
             try:
                 cur[k] = next(roles[k])
             except StopIteration:
@@ -145,6 +169,9 @@ class _Model:
                 ic += 1
 
     def _copy(self):
+        if self.f16:
+            yield from self._copy_raw()
+            return
         if self.fp8:
             yield from self._copy_fp8()
             return
@@ -169,6 +196,62 @@ class _Model:
                     yield self._wait(f"VE{vs}", vc // self.NV - 1)
                 yield ("arrive", f"VF{vs}")
                 vc += 1
+
+    def _copy_raw(self):
+        """Decode over an fp8 pool: per tile, the codes of K(j) and of V(j)
+        go into the next two raw slots once the converting warps have read
+        what those slots held."""
+        rc = ic = 0
+        for op in self._units():
+            if op[0] != "unit":
+                yield op
+                continue
+            u = op[1]
+            if u is None:
+                return
+            for j in range(u["nt"]):
+                si = ic % self.NI
+                yield self._wait(f"IF{si}", ic // self.NI)
+                yield ("arrive", f"IE{si}")
+                ic += 1
+                for _ in range(2):  # K(j), V(j)
+                    s = rc % NRAW
+                    if rc >= NRAW and self.mistake != "raw slot reused before its conversion":
+                        yield self._wait(f"RE{s}", rc // NRAW - 1)
+                    yield ("raw_issue", s, rc)
+                    rc += 1
+
+    def _convert(self, pre):
+        """A converting group (K or V slots): the unit's query rows (Q_CONV,
+        with the other group), then its raw slots in order (K(j) in use 2j,
+        V(j) in use 2j + 1), each into the next stage of its ring once the
+        codes have landed and the tensor core has released the stage."""
+        rc = 0 if pre == "K" else 1
+        cnt = qc = 0
+        n = self.NK if pre == "K" else self.NV
+        for op in self._units():
+            if op[0] != "unit":
+                yield op
+                continue
+            u = op[1]
+            if u is None:
+                return
+            if u["nt"] == 0:
+                continue
+            yield self._wait("Q_FULL", qc)
+            qc += 1
+            yield ("arrive", "Q_CONV")
+            for _ in range(u["nt"]):
+                s = rc % NRAW
+                if self.mistake != "raw slot converted before it landed":
+                    yield self._wait(f"RF{s}", rc // NRAW)
+                if cnt >= n:
+                    yield self._wait(f"{pre}E{cnt % n}", cnt // n - 1)
+                yield ("raw_convert", s, rc)
+                yield ("arrive", f"{pre}F{cnt % n}")
+                yield ("arrive", f"RE{s}")
+                rc += 2
+                cnt += 1
 
     def _copy_fp8(self):
         """The fp8-pool order: a tile's codes are issued, and converted (then
@@ -347,10 +430,22 @@ def test_fp8_protocols_have_no_deadlock_and_no_parity_aliasing():
     rng = random.Random(3)
     for t in range(150):
         _Model(_random_units(rng, rng.randint(1, 12)), seed=t, fp8=True).run()
-    for t in range(150):
+    for t in range(300):
+        # K stage 0 holds raw slots: 2 K stages for 128 dims, 4 for 64
+        stages = (2, 2, 3) if t % 2 else (4, 5, 4)
         kind = rng.choice(["two", "one"])
         units = [{"kind": kind, "nt": rng.choice([0, 1, 2, 3, 6])} for _ in range(rng.randint(1, 10))]
-        _Model(units, seed=t, f16_decode=True).run()
+        _Model(units, seed=t, f16_decode=True, stages=stages).run()
+
+
+@pytest.mark.parametrize("mistake", ["raw slot reused before its conversion",
+                                     "raw slot converted before it landed"])
+def test_fp8_decode_model_catches_planted_mistakes(mistake):
+    rng = random.Random(4)
+    with pytest.raises(AssertionError):
+        for t in range(150):
+            units = [{"kind": "two", "nt": rng.choice([1, 2, 3, 6])} for _ in range(rng.randint(1, 10))]
+            _Model(units, seed=t, f16_decode=True, stages=(2, 2, 3), mistake=mistake).run()
 
 
 def test_protocol_has_no_deadlock_and_no_parity_aliasing():
