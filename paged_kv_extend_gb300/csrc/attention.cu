@@ -444,15 +444,16 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     w.b = b;
     w.slot = combined(S) ? kvh * ts + bSo[qb] + sp * spu : -1;
     w.dq = dq;
-    w.pad = 0;
+    w.claim = 0;
     return w;
   };
 
   // 6. units, consecutive threads on consecutive units (their records go
-  //    out as 16-byte stores); pass 0 writes them and counts their claim
-  //    keys, pass 1 places them in the claim order.  Lanes of a warp whose
-  //    units share a key make one atomic for the group (units of one
-  //    sequence and cost class share a key, so per-unit atomics serialise).
+  //    out as 16-byte stores); pass 0 builds and writes them with their
+  //    claim keys and counts the keys, pass 1 reads the keys back and places
+  //    the units in the claim order.  Lanes of a warp whose units share a
+  //    key make one atomic for the group (units of one sequence and cost
+  //    class share a key, so per-unit atomics serialise).
   const int lane = tid & 31;
   for (int pass = 0; pass < 2; ++pass) {
     for (int base = tid - lane; base < n_units; base += 1024) {
@@ -461,8 +462,13 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
       WorkUnit w;
       int key = -1;
       if (act) {
-        w = unit_at(u);
-        key = claim_key(w);
+        if (pass == 0) {
+          w = unit_at(u);
+          key = claim_key(w);
+          w.claim = key;
+        } else {
+          key = p.units[u].claim;  // written in pass 0 (the block barrier between passes orders it)
+        }
       }
       const unsigned grp = __match_any_sync(0xffffffffu, key);
       const int leader = __ffs(grp) - 1;

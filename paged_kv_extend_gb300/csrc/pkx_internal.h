@@ -52,8 +52,8 @@ struct __align__(16) WorkUnit {
   int32_t n_tiles;  // K/V tiles (no tile straddles k_split)
   int32_t b;        // sequence
   int32_t slot;     // -1: write o/lse; else split-KV partial slot
-  int32_t dq;       // value-dim slice (MLA: 128 of the 512 value dims)
-  int32_t pad;
+  int32_t dq;       // value-dim slice (0: the kernels take all value dims)
+  int32_t claim;    // claim key (cost bucket, largest cost first), for the scheduler
 };
 
 // A query block whose key range was split: its partials live in slots
