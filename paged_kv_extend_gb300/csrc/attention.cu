@@ -2074,12 +2074,17 @@ static int launch_attn_kernel(const TMaps &tmaps, const KParams &kp, int grid, c
   return PKX_OK;
 }
 
-// The three key modes of one head size over an fp8 pool (no custom mask).
+// The three key modes of one head size over an fp8 pool (the two extend
+// forms with or without a custom mask).
 template <int HD, int FMT>
-static int launch_attn_fp8(int mode, const TMaps &tmaps, const KParams &kp, int grid,
-                           cudaStream_t s) {
-  if (mode == kTwoStage) return launch_attn_kernel<HD, kTwoStage, false, FMT>(tmaps, kp, grid, s);
-  if (mode == kUnified) return launch_attn_kernel<HD, kUnified, false, FMT>(tmaps, kp, grid, s);
+static int launch_attn_fp8(int mode, bool masked, const TMaps &tmaps, const KParams &kp,
+                           int grid, cudaStream_t s) {
+  if (mode == kTwoStage)
+    return masked ? launch_attn_kernel<HD, kTwoStage, true, FMT>(tmaps, kp, grid, s)
+                  : launch_attn_kernel<HD, kTwoStage, false, FMT>(tmaps, kp, grid, s);
+  if (mode == kUnified)
+    return masked ? launch_attn_kernel<HD, kUnified, true, FMT>(tmaps, kp, grid, s)
+                  : launch_attn_kernel<HD, kUnified, false, FMT>(tmaps, kp, grid, s);
   return launch_attn_kernel<HD, kDecode, false, FMT>(tmaps, kp, grid, s);
 }
 
@@ -2303,16 +2308,15 @@ int launch_attention(const AttnArgs &a) {
   if (ev_before) cudaEventRecord(ev_before, a.stream);
   const bool masked = a.custom_mask != nullptr;
   if (a.kv_fmt != kKvBf16) {
-    if (masked || mla || !((a.lq == 128 && a.lv == 128) || (a.lq == 64 && a.lv == 64)))
-      return set_error(PKX_EUNSUPPORTED, "an fp8 pool is built for Lq = Lv = 64 or 128 "
-                                         "without a custom mask");
+    if (mla || !((a.lq == 128 && a.lv == 128) || (a.lq == 64 && a.lv == 64)))
+      return set_error(PKX_EUNSUPPORTED, "an fp8 pool is built for Lq = Lv = 64 or 128");
     const bool e4 = a.kv_fmt == kKvFp8E4M3;
     if (a.lq == 128)
-      rc = e4 ? launch_attn_fp8<128, 1>(a.mode, tm, kp, grid, a.stream)
-              : launch_attn_fp8<128, 2>(a.mode, tm, kp, grid, a.stream);
+      rc = e4 ? launch_attn_fp8<128, 1>(a.mode, masked, tm, kp, grid, a.stream)
+              : launch_attn_fp8<128, 2>(a.mode, masked, tm, kp, grid, a.stream);
     else
-      rc = e4 ? launch_attn_fp8<64, 1>(a.mode, tm, kp, grid, a.stream)
-              : launch_attn_fp8<64, 2>(a.mode, tm, kp, grid, a.stream);
+      rc = e4 ? launch_attn_fp8<64, 1>(a.mode, masked, tm, kp, grid, a.stream)
+              : launch_attn_fp8<64, 2>(a.mode, masked, tm, kp, grid, a.stream);
   } else if (a.lq == 128 && a.lv == 128) {
     if (a.mode == kTwoStage)
       rc = masked ? launch_attn_kernel<128, kTwoStage, true>(tm, kp, grid, a.stream)

@@ -112,6 +112,60 @@ def test_extend_over_fp8_pool(dt, lq, hq, hkv, prefix, extend, cap, window, ks, 
     assert_close(o2, l2, uo, ul, f"unified fp8 {dt}")
 
 
+MASKED = [
+    # (lq, hq, hkv, prefix, extend, cap, window, k_scale, v_scale, sinks)
+    (128, 32, 8, [0, 40, 300], [17, 64, 130], 0.0, -1, 0.5, 0.25, False),
+    (128, 16, 4, [900, 5], [70, 200], 20.0, 100, 0.05, 0.02, True),   # split rows, cap, window
+    (64, 12, 3, [500, 0, 77], [40, 129, 3], 0.0, -1, 1.0, 2.0, True),
+]
+
+
+@pytest.mark.parametrize("dt", FMTS)
+@pytest.mark.parametrize("lq,hq,hkv,prefix,extend,cap,window,ks,vs,sinks", MASKED)
+def test_masked_extend_over_fp8_pool(dt, lq, hq, hkv, prefix, extend, cap, window, ks, vs, sinks):
+    """A custom mask (and sinks) over an fp8 pool, two-stage and unified,
+    against the oracle reading the same codes with the same mask."""
+    from gpu_cases import random_masks
+    wl, kb, vb = _extend_case(dt, lq, hq, hkv, prefix, extend, cap, window, ks, vs,
+                              seed=3 * sum(prefix) + sum(extend) + hq)
+    cm, mi = random_masks(wl, seed=sum(extend) + lq)
+    sk = (torch.randn(hq, generator=torch.Generator().manual_seed(hq)) * 2.0).float() \
+        if sinks else None
+    k_ext, v_ext = wl.extend_kv()
+    ro, rl = oracle.extend_attention(wl.q, k_ext, v_ext, kb, vb, wl.qo_indptr, wl.kv_indptr,
+                                     wl.kv_indices, wl.sm_scale, cap, window, custom_mask=cm,
+                                     mask_indptr=mi, sinks=sk, k_scale=ks, v_scale=vs)
+    dkb, dvb = kb.to(DEV), vb.to(DEV)
+    dsk = sk.to(DEV) if sk is not None else None
+    n = wl.n_q_tokens
+    o = torch.full((n, hq, lq), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((n, hq), float("nan"), dtype=torch.float32, device=DEV)
+    ws = pkx.extend_attention_fwd(wl.q.to(DEV), k_ext.to(DEV), v_ext.to(DEV), o, dkb, dvb,
+                                  wl.qo_indptr.to(DEV), wl.kv_indptr.to(DEV),
+                                  wl.kv_indices.to(DEV), wl.sm_scale, cap, window, lse=lse,
+                                  custom_mask=cm.to(DEV), mask_indptr=mi.to(DEV), sinks=dsk,
+                                  k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    assert_close(o, lse, ro, rl, f"two-stage masked fp8 {dt}")
+    uptr, uidx, plen = oracle.build_unified_kv_indices(
+        wl.kv_indptr, wl.kv_indices, wl.extend_start_loc, wl.extend_seq_lens,
+        wl.extend_kv_indices, wl.batch)
+    uo, ul = oracle.extend_attention_unified(wl.q, kb, vb, wl.qo_indptr, uptr, uidx, plen,
+                                             wl.sm_scale, cap, window, custom_mask=cm,
+                                             mask_indptr=mi, sinks=sk, k_scale=ks, v_scale=vs)
+    o2 = torch.full_like(o, float("nan"))
+    l2 = torch.full_like(lse, float("nan"))
+    ws2 = pkx.extend_attention_fwd_unified(wl.q.to(DEV), o2, dkb, dvb, wl.qo_indptr.to(DEV),
+                                           uptr.to(DEV), uidx.to(DEV), plen.to(DEV),
+                                           wl.sm_scale, cap, window, lse=l2,
+                                           custom_mask=cm.to(DEV), mask_indptr=mi.to(DEV),
+                                           sinks=dsk, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws2) == 0
+    assert_close(o2, l2, uo, ul, f"unified masked fp8 {dt}")
+
+
 @pytest.mark.parametrize("dt", FMTS)
 @pytest.mark.parametrize("lq,hq,hkv,lens,cap,window,ks,vs", [
     (128, 32, 8, [1, 17, 128, 129, 4000], 0.0, -1, 1.0, 1.0),
