@@ -832,10 +832,11 @@ def run_ours(args, ws, rank, local):
         names = (args.components.split(",") if args.components
                  else ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla",
                        "split_192", "split_288", "kv_ops", "split", "fused_write",
-                       "decode_gqa_fp8", "llama3_8b_fp8"])
+                       "decode_gqa_fp8", "llama3_8b_fp8", "mla_fp8", "decode_mla_fp8"])
         if args.all_workloads:
             names = ["long_prefix", "mla", "heavy_tail", "decode_gqa", "decode_mla", "kv_ops",
-                     "split", "decode_gqa_fp8", "long_prefix_fp8", "llama3_8b_fp8"]
+                     "split", "decode_gqa_fp8", "long_prefix_fp8", "llama3_8b_fp8", "mla_fp8",
+                     "decode_mla_fp8"]
         for name in names:
             if name == args.workload:
                 continue

@@ -67,9 +67,10 @@ extern "C" {
  * and a value element code * v_scale (k_scale, v_scale positive host
  * floats; ignored for bf16).  An fp8 pool's strides are in bytes (its
  * elements are one byte); the 16-byte alignment rule for rows still
- * applies.  Built for Lq = Lv = 64 or 128 (with or without a custom mask);
- * other fp8 calls return PKX_EUNSUPPORTED.  The extend rows of the two-stage
- * form (k_extend / v_extend) stay bf16.
+ * applies.  Built for Lq = Lv = 64 or 128 and for the MLA head Lq / Lv =
+ * 576 / 512 (v_buffer a view of k_buffer's codes), with or without a custom
+ * mask; other fp8 calls return PKX_EUNSUPPORTED.  The extend rows of the
+ * two-stage form (k_extend / v_extend) stay bf16.
  */
 #define PKX_KV_BF16 0
 #define PKX_KV_FP8_E4M3 1

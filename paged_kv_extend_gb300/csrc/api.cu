@@ -66,15 +66,16 @@ static int check_mask_sinks(const uint8_t *custom_mask, const int32_t *mask_indp
 }
 
 // The pool's element format and its scales (an fp8 pool: Lq = Lv = 64 or
-// 128, with or without a custom mask).
+// 128, or the MLA head 576 / 512; with or without a custom mask).
 static int check_kv_format(int kv_dtype, float k_scale, float v_scale, int lq, int lv) {
   if (kv_dtype == kKvBf16) return PKX_OK;
   if (kv_dtype != kKvFp8E4M3 && kv_dtype != kKvFp8E5M2)
     return set_error(PKX_EINVAL, "kv_dtype %d is not a PKX_KV_* value", kv_dtype);
   if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
     return set_error(PKX_EINVAL, "k_scale and v_scale must be positive and finite");
-  if (!((lq == 64 && lv == 64) || (lq == 128 && lv == 128)))
-    return set_error(PKX_EUNSUPPORTED, "an fp8 pool is built for Lq = Lv = 64 or 128");
+  if (!((lq == 64 && lv == 64) || (lq == 128 && lv == 128) || (lq == 576 && lv == 512)))
+    return set_error(PKX_EUNSUPPORTED,
+                     "an fp8 pool is built for Lq = Lv = 64 or 128 and for Lq / Lv = 576 / 512");
   return PKX_OK;
 }
 

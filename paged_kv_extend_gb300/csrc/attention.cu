@@ -2089,13 +2089,13 @@ static int launch_attn_fp8(int mode, bool masked, const TMaps &tmaps, const KPar
 }
 
 // Pair kernel launch: clusters of two CTAs, programmatic dependent launch.
-template <int MODE, bool MASK>
+template <int MODE, bool MASK, int FMT = 0>
 static cudaError_t launch_pair(int pairs, cudaStream_t s, const KParams &kp, bool query_only,
                                int *max_pairs) {
   using C = MlaPairCfg;
   static bool configured[kMaxDevicesCfg] = {};
   if (needs_config(configured)) {
-    cudaError_t e = cudaFuncSetAttribute(mla_pair_kernel<MODE, MASK>,
+    cudaError_t e = cudaFuncSetAttribute(mla_pair_kernel<MODE, MASK, FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     mark_configured(configured);
@@ -2114,8 +2114,8 @@ static cudaError_t launch_pair(int pairs, cudaStream_t s, const KParams &kp, boo
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = query_only ? 1 : 2;
-  if (query_only) return cudaOccupancyMaxActiveClusters(max_pairs, mla_pair_kernel<MODE, MASK>, &cfg);
-  return cudaLaunchKernelEx(&cfg, mla_pair_kernel<MODE, MASK>, kp);
+  if (query_only) return cudaOccupancyMaxActiveClusters(max_pairs, mla_pair_kernel<MODE, MASK, FMT>, &cfg);
+  return cudaLaunchKernelEx(&cfg, mla_pair_kernel<MODE, MASK, FMT>, kp);
 }
 
 // CTA pairs of the MLA kernel that run at once on the current device (an SM
@@ -2136,9 +2136,9 @@ static int mla_pairs(int nsm) {
   return n;
 }
 
-template <int MODE, bool MASK = false>
+template <int MODE, bool MASK = false, int FMT = 0>
 static int launch_mla_pair(const KParams &kp, int pairs, cudaStream_t s) {
-  cudaError_t e = launch_pair<MODE, MASK>(pairs, s, kp, false, nullptr);
+  cudaError_t e = launch_pair<MODE, MASK, FMT>(pairs, s, kp, false, nullptr);
   if (e != cudaSuccess)
     return set_error(PKX_ECUDA, "mla_pair_kernel launch: %s", cudaGetErrorString(e));
   return PKX_OK;
@@ -2175,7 +2175,7 @@ int launch_attention(const AttnArgs &a) {
   }
   // the MLA kernel runs on CTA pairs: units for four rounds of the pairs
   int pairs = 0;
-  if (mla && a.kv_fmt == kKvBf16) {
+  if (mla) {
     pairs = mla_pairs(nsm);
     if (pairs <= 0) return set_error(PKX_ECUDA, "no CTA pair of the MLA kernel fits the device");
   }
@@ -2307,9 +2307,26 @@ int launch_attention(const AttnArgs &a) {
   attention_events(&ev_before, &ev_after);
   if (ev_before) cudaEventRecord(ev_before, a.stream);
   const bool masked = a.custom_mask != nullptr;
-  if (a.kv_fmt != kKvBf16) {
-    if (mla || !((a.lq == 128 && a.lv == 128) || (a.lq == 64 && a.lv == 64)))
-      return set_error(PKX_EUNSUPPORTED, "an fp8 pool is built for Lq = Lv = 64 or 128");
+  if (a.kv_fmt != kKvBf16 && mla) {
+    // the MLA pair kernel over an fp8 pool
+    const bool e4 = a.kv_fmt == kKvFp8E4M3;
+    if (a.mode == kTwoStage)
+      rc = masked ? (e4 ? launch_mla_pair<kTwoStage, true, 1>(kp, pairs, a.stream)
+                        : launch_mla_pair<kTwoStage, true, 2>(kp, pairs, a.stream))
+                  : (e4 ? launch_mla_pair<kTwoStage, false, 1>(kp, pairs, a.stream)
+                        : launch_mla_pair<kTwoStage, false, 2>(kp, pairs, a.stream));
+    else if (a.mode == kUnified)
+      rc = masked ? (e4 ? launch_mla_pair<kUnified, true, 1>(kp, pairs, a.stream)
+                        : launch_mla_pair<kUnified, true, 2>(kp, pairs, a.stream))
+                  : (e4 ? launch_mla_pair<kUnified, false, 1>(kp, pairs, a.stream)
+                        : launch_mla_pair<kUnified, false, 2>(kp, pairs, a.stream));
+    else
+      rc = e4 ? launch_mla_pair<kDecode, false, 1>(kp, pairs, a.stream)
+              : launch_mla_pair<kDecode, false, 2>(kp, pairs, a.stream);
+  } else if (a.kv_fmt != kKvBf16) {
+    if (!((a.lq == 128 && a.lv == 128) || (a.lq == 64 && a.lv == 64)))
+      return set_error(PKX_EUNSUPPORTED,
+                       "an fp8 pool is built for Lq = Lv = 64 or 128 and for Lq / Lv = 576 / 512");
     const bool e4 = a.kv_fmt == kKvFp8E4M3;
     if (a.lq == 128)
       rc = e4 ? launch_attn_fp8<128, 1>(a.mode, masked, tm, kp, grid, a.stream)

@@ -100,7 +100,12 @@ __device__ __forceinline__ int pair_unit(const KParams &p, int n_units, uint32_t
   return pos < n_units ? p.uorder[pos] : -1;
 }
 
-template <int MODE, bool MASK>
+// FMT: the pool's element format (0 bf16; 1 fp8 e4m3, 2 fp8 e5m2 with
+// k_scale / v_scale: the copy warps stage a tile's codes and convert them in
+// place to bf16, exact, one tile behind their copies; k_scale joins the
+// logit scale of pool tiles and v_scale their P).  Extend rows of the
+// two-stage form are always bf16.
+template <int MODE, bool MASK, int FMT = 0>
 __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const KParams p) {
   using C = MlaPairCfg;
   extern __shared__ uint8_t smem_raw[];
@@ -327,10 +332,15 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
         bool o_needs = false;
         uint32_t pk[32];
         if (warp_active) {
-          float sc = p.scale_log2;
+          // a pool tile of an fp8 pool holds codes: k_scale joins the logit
+          // scale, v_scale its P (through the exponent; the row sum divides
+          // it back out)
+          const bool pool8 = FMT != 0 && !(MODE == kTwoStage && kb >= w.k_split);
+          float sc = pool8 ? p.scale_log2_k : p.scale_log2;
           if (p.use_cap) {
+            const float pre = pool8 ? p.cap_pre_k : p.cap_pre;
 #pragma unroll
-            for (int i = 0; i < C::BN; ++i) x[i] = p.cap_log2 * tanh_approx(x[i] * p.cap_pre);
+            for (int i = 0; i < C::BN; ++i) x[i] = p.cap_log2 * tanh_approx(x[i] * pre);
             sc = 1.0f;
           }
           const bool need_mask = (ke - 1 > w.qpos0) || (ke - kb < C::BN) ||
@@ -384,7 +394,8 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
             l *= alpha;
             m = m_new;
           }
-          const float nm = m == -INFINITY ? 0.f : -m;
+          float nm = m == -INFINITY ? 0.f : -m;
+          if (pool8) nm += p.log2_v_scale;
           float l0 = 0.f, l1 = 0.f;
 #pragma unroll
           for (int i = 0; i < C::BN; i += 2) {
@@ -394,7 +405,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
             l1 += e1;
             pk[i / 2] = pack_bf16(e0, e1);
           }
-          l += l0 + l1;
+          l += pool8 ? (l0 + l1) * p.inv_v_scale : l0 + l1;
         }
         // P's columns and O are free once the previous tile's PV has landed.
         // Every warp waits, also one without rows, so that no warp arrives
@@ -619,53 +630,173 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     const uint32_t dthr = (uint32_t)key0 * 128u + ((uint32_t)(ch ^ (key0 & 7)) << 4);
     uint32_t kc = 0, ic = 0;
     bool ok = true;
-    for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-      const int u = pair_unit(p, n_units, uc);
-      if (u < 0) break;
-      const WorkUnit w = p.units[u];
-      const int nt = w.n_tiles;
-      if (nt == 0) continue;
-      const bf16 *kp = p.k_pool + (int64_t)w.kvh * p.kb_sh + dv0 + ch * 8;
-      const bf16 *kx = p.k_ext + (int64_t)w.kvh * p.ke_sh + dv0 + ch * 8;
-      for (int j = 0; j < nt; ++j) {
-        int kb, ke;
-        tile_keys<C::BN>(w, j, kb, ke);
-        const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
-        const int is = ic % C::NI;
-        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag, p.wait_ns)) {
-          ok = false;
-          break;
+    if constexpr (FMT == 0) {
+      for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+        const int u = pair_unit(p, n_units, uc);
+        if (u < 0) break;
+        const WorkUnit w = p.units[u];
+        const int nt = w.n_tiles;
+        if (nt == 0) continue;
+        const bf16 *kp = p.k_pool + (int64_t)w.kvh * p.kb_sh + dv0 + ch * 8;
+        const bf16 *kx = p.k_ext + (int64_t)w.kvh * p.ke_sh + dv0 + ch * 8;
+        for (int j = 0; j < nt; ++j) {
+          int kb, ke;
+          tile_keys<C::BN>(w, j, kb, ke);
+          const bool from_ext = MODE == kTwoStage && kb >= w.k_split;
+          const int is = ic % C::NI;
+          if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          const int *ring = reinterpret_cast<const int *>(smem + C::OFF_I + is * C::I_BYTES);
+          int rows[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rows[i] = ring[key0 + 16 * i];
+          mbar_arrive(&i_empty[is]);
+          ++ic;
+          const int ks = kc % C::NK;
+          if (kc >= (uint32_t)C::NK &&
+              !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          const bf16 *base = from_ext ? kx : kp;
+          const int64_t st = from_ext ? p.ke_st : p.kb_ss;
+          const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES + dthr;
+          static_for<0, 4>([&](auto i_c) {
+            constexpr int i = decltype(i_c)::value;
+            const int row = rows[i];
+            const bf16 *src = base + (int64_t)max(row, 0) * st;
+            const uint32_t bytes = row >= 0 ? 16u : 0u;
+            static_for<0, 4>([&](auto a_c) {
+              constexpr int a = decltype(a_c)::value;
+              cp_async_16_at<a * C::BN * 128 + i * 16 * 128, a * 128>(sK, src, bytes);
+            });
+            // the rope dims dr0 + 8 ch (value dims start at dv0 + 8 ch)
+            if (ch < C::DR / 8)
+              cp_async_16_at<4 * C::BN * 128 + i * 16 * 128, 0>(sK, src + (dr0 - dv0), bytes);
+          });
+          cp_async_arrive_noinc(&k_full[ks]);
+          ++kc;
         }
+      }
+    } else {
+      // fp8 pool.  A pool tile's codes are copied 8 bytes per (thread, key,
+      // chunk) into the first half of the 16-byte chunk the same thread
+      // later writes, and converted there in place to bf16 once they have
+      // landed, so no thread overwrites another's codes.  Tile j is
+      // converted (and its stage marked full) after tile j + 1's copies are
+      // issued; extend tiles of the two-stage form are bf16 rows and take
+      // the plain copy.  One cp.async group per issued tile.
+      int rows[4];
+      auto fetch = [&]() -> bool {
+        const int is = ic % C::NI;
+        if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag, p.wait_ns)) return false;
         const int *ring = reinterpret_cast<const int *>(smem + C::OFF_I + is * C::I_BYTES);
-        int rows[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) rows[i] = ring[key0 + 16 * i];
         mbar_arrive(&i_empty[is]);
         ++ic;
-        const int ks = kc % C::NK;
-        if (kc >= (uint32_t)C::NK &&
-            !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag, p.wait_ns)) {
+        return true;
+      };
+      for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+        const int u = pair_unit(p, n_units, uc);
+        if (u < 0) break;
+        const WorkUnit w = p.units[u];
+        const int nt = w.n_tiles;
+        if (nt == 0) continue;
+        const uint8_t *kp8 =
+            reinterpret_cast<const uint8_t *>(p.k_pool) + (int64_t)w.kvh * p.kb_sh + dv0 + ch * 8;
+        const bf16 *kx = p.k_ext + (int64_t)w.kvh * p.ke_sh + dv0 + ch * 8;
+        auto tile_ext = [&](int j) {
+          int kb, ke;
+          tile_keys<C::BN>(w, j, kb, ke);
+          return MODE == kTwoStage && kb >= w.k_split;
+        };
+        // tile j's rows into the next stage; returns the stage, or -1
+        auto issue = [&](bool from_ext) -> int {
+          const int ks = kc % C::NK;
+          if (kc >= (uint32_t)C::NK &&
+              !mbar_wait(&k_empty[ks], ((kc / C::NK) - 1) & 1u, abort_flag, p.wait_ns))
+            return -1;
+          const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES + dthr;
+          if (from_ext) {
+            static_for<0, 4>([&](auto i_c) {
+              constexpr int i = decltype(i_c)::value;
+              const int row = rows[i];
+              const bf16 *src = kx + (int64_t)max(row, 0) * p.ke_st;
+              const uint32_t bytes = row >= 0 ? 16u : 0u;
+              static_for<0, 4>([&](auto a_c) {
+                constexpr int a = decltype(a_c)::value;
+                cp_async_16_at<a * C::BN * 128 + i * 16 * 128, a * 128>(sK, src, bytes);
+              });
+              if (ch < C::DR / 8)
+                cp_async_16_at<4 * C::BN * 128 + i * 16 * 128, 0>(sK, src + (dr0 - dv0), bytes);
+            });
+            cp_async_arrive_noinc(&k_full[ks]);
+          } else {
+            static_for<0, 4>([&](auto i_c) {
+              constexpr int i = decltype(i_c)::value;
+              const int row = rows[i];
+              const uint8_t *src = kp8 + (int64_t)max(row, 0) * p.kb_ss;
+              const uint32_t bytes = row >= 0 ? 8u : 0u;
+              static_for<0, 4>([&](auto a_c) {
+                constexpr int a = decltype(a_c)::value;
+                cp_async_8_at<a * C::BN * 128 + i * 16 * 128>(sK, src + a * 64, bytes);
+              });
+              if (ch < C::DR / 8)
+                cp_async_8_at<4 * C::BN * 128 + i * 16 * 128>(sK, src + (dr0 - dv0), bytes);
+            });
+          }
+          cp_async_commit();
+          ++kc;
+          return ks;
+        };
+        // the thread's codes of a stage to bf16, in place
+        auto convert = [&](int ks) {
+          const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES + dthr;
+          static_for<0, 4>([&](auto i_c) {
+            constexpr int i = decltype(i_c)::value;
+            static_for<0, 4>([&](auto a_c) {
+              constexpr int a = decltype(a_c)::value;
+              const uint32_t at = sK + a * C::BN * 128 + i * 16 * 128;
+              st_shared_u4(at, fp8x8_to_bf16x8<FMT>(ld_shared_u2(at)));
+            });
+            if (ch < C::DR / 8) {
+              const uint32_t at = sK + 4 * C::BN * 128 + i * 16 * 128;
+              st_shared_u4(at, fp8x8_to_bf16x8<FMT>(ld_shared_u2(at)));
+            }
+          });
+          fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+        };
+        bool ext_j = tile_ext(0);
+        int st_j = fetch() ? issue(ext_j) : -1;
+        if (st_j < 0) {
           ok = false;
           break;
         }
-        const bf16 *base = from_ext ? kx : kp;
-        const int64_t st = from_ext ? p.ke_st : p.kb_ss;
-        const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES + dthr;
-        static_for<0, 4>([&](auto i_c) {
-          constexpr int i = decltype(i_c)::value;
-          const int row = rows[i];
-          const bf16 *src = base + (int64_t)max(row, 0) * st;
-          const uint32_t bytes = row >= 0 ? 16u : 0u;
-          static_for<0, 4>([&](auto a_c) {
-            constexpr int a = decltype(a_c)::value;
-            cp_async_16_at<a * C::BN * 128 + i * 16 * 128, a * 128>(sK, src, bytes);
-          });
-          // the rope dims dr0 + 8 ch (value dims start at dv0 + 8 ch)
-          if (ch < C::DR / 8)
-            cp_async_16_at<4 * C::BN * 128 + i * 16 * 128, 0>(sK, src + (dr0 - dv0), bytes);
-        });
-        cp_async_arrive_noinc(&k_full[ks]);
-        ++kc;
+        for (int j = 0; j < nt; ++j) {
+          const bool more = j + 1 < nt;
+          bool ext_n = false;
+          int st_n = 0;
+          if (more) {
+            ext_n = tile_ext(j + 1);
+            st_n = fetch() ? issue(ext_n) : -1;
+            if (st_n < 0) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ext_j) {
+            // groups issued after tile j's: tile j + 1's, if there is one
+            if (more) cp_async_wait_group<1>();
+            else cp_async_wait_group<0>();
+            convert(st_j);
+            mbar_arrive(&k_full[st_j]);
+          }
+          ext_j = ext_n;
+          st_j = st_n;
+        }
       }
     }
     if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);

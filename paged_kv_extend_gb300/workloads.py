@@ -206,13 +206,20 @@ class Workload:
     def pool_fp8(self, dtype, k_scale: float, v_scale: float, device="cpu"):
         """The pool in an fp8 format (torch.float8_e4m3fn or float8_e5m2):
         every token row divided by its scale and converted by torch, zero
-        elsewhere.  (k_buffer, v_buffer) as one-byte tensors of that dtype."""
+        elsewhere.  (k_buffer, v_buffer) as one-byte tensors of that dtype; for
+        MLA, v_buffer is a view of k_buffer."""
         s = self.spec
         slots = self.slots.to(torch.int64)
         k = torch.zeros(s.num_slots, s.hkv, s.lq, dtype=torch.uint8)
-        v = torch.zeros(s.num_slots, s.hkv, s.lv, dtype=torch.uint8)
         if slots.numel():
             k[slots] = (self.k_rows.float() / k_scale).to(dtype).view(torch.uint8)
+        if s.v_aliases_k:
+            # MLA: v_buffer is a view of the first Lv codes of k_buffer (a
+            # value reads code * v_scale)
+            kd = k.view(dtype).to(device)
+            return kd, kd[..., : s.lv]
+        v = torch.zeros(s.num_slots, s.hkv, s.lv, dtype=torch.uint8)
+        if slots.numel():
             v[slots] = (self.v_rows.float() / v_scale).to(dtype).view(torch.uint8)
         return k.view(dtype).to(device), v.view(dtype).to(device)
 

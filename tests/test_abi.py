@@ -94,7 +94,11 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _extend(lib, kvd=3) == pkx.PKX_EINVAL
     assert _extend(lib, kvd=1, ksc=0.0) == pkx.PKX_EINVAL
     assert _extend(lib, kvd=2, vsc=float("inf")) == pkx.PKX_EINVAL
-    assert _extend(lib, kvd=1, lq=576, lv=512, hq=16, hkv=1) == pkx.PKX_EUNSUPPORTED
+    assert _extend(lib, kvd=1, lq=192, lv=128) == pkx.PKX_EUNSUPPORTED
+    # the MLA head over an fp8 pool is built: past the format check, the null
+    # tensors stop the call
+    assert _extend(lib, kvd=1, lq=576, lv=512, hq=16, hkv=1) == pkx.PKX_EINVAL
+    assert b"fp8" not in lib.pkx_last_error_string()
     # a custom mask over an fp8 pool is built: the call gets past the format
     # check and stops at the null tensors
     assert _extend(lib, kvd=1, mask=0x1000, mask_indptr=0x1000) == pkx.PKX_EINVAL

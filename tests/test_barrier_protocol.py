@@ -490,9 +490,12 @@ class _MlaPairModel:
     buffer's state, so a send that could overwrite an unread tile fails."""
     NK, NI = 4, 4
 
-    def __init__(self, units, seed, mistake=None):
+    def __init__(self, units, seed, mistake=None, fp8=False):
         self.rng = random.Random(seed)
         self.units, self.mistake = units, mistake
+        # an fp8 pool: the copy warps mark tile j full only after issuing
+        # tile j + 1 (they convert tile j's codes in place in between)
+        self.fp8 = fp8
         self.pending = {0: [], 1: []}
         self.xbuf = {(c, b): None for c in (0, 1) for b in (0, 1)}  # ("written" | "read", tile)
         self.bars = {}
@@ -578,17 +581,33 @@ class _MlaPairModel:
 
     def _copy(self, c):
         kc = ic = 0
+
+        def issue():
+            nonlocal kc, ic
+            si = ic % self.NI
+            yield self._wait(f"{c}IF{si}", ic // self.NI)
+            yield ("arrive", f"{c}IE{si}")
+            ic += 1
+            ks = kc % self.NK
+            if kc >= self.NK:
+                yield self._wait(f"{c}KE{ks}", kc // self.NK - 1)
+            kc += 1
+
         for u in self.units:
-            for _ in range(u["nt"]):
-                si = ic % self.NI
-                yield self._wait(f"{c}IF{si}", ic // self.NI)
-                yield ("arrive", f"{c}IE{si}")
-                ic += 1
-                ks = kc % self.NK
-                if kc >= self.NK:
-                    yield self._wait(f"{c}KE{ks}", kc // self.NK - 1)
-                yield ("arrive", f"{c}KF{ks}")
-                kc += 1
+            nt = u["nt"]
+            if not self.fp8:
+                for _ in range(nt):
+                    yield from issue()
+                    yield ("arrive", f"{c}KF{(kc - 1) % self.NK}")
+                continue
+            if nt == 0:
+                continue
+            yield from issue()
+            for j in range(nt):
+                st_j = (kc - 1) % self.NK
+                if j + 1 < nt:
+                    yield from issue()
+                yield ("arrive", f"{c}KF{st_j}")
 
     def _softmax(self, c):
         s_cnt = o_cnt = pv_base = n_sent = n_recv = 0
@@ -678,6 +697,14 @@ def _mla_trials(n, mistake=None):
 
 def test_mla_protocol_has_no_deadlock_and_no_parity_aliasing():
     _mla_trials(150)
+
+
+def test_mla_fp8_protocol_has_no_deadlock_and_no_parity_aliasing():
+    """An fp8 pool: tile j's stage becomes full after tile j + 1's copies."""
+    rng = random.Random(5)
+    for t in range(150):
+        units = [{"nt": rng.choice([0, 1, 1, 2, 3, 5, 8])} for _ in range(rng.randint(1, 10))]
+        _MlaPairModel(units, seed=t, fp8=True).run()
 
 
 @pytest.mark.parametrize("mistake", ["P written before the previous PV",

@@ -166,6 +166,90 @@ def test_masked_extend_over_fp8_pool(dt, lq, hq, hkv, prefix, extend, cap, windo
     assert_close(o2, l2, uo, ul, f"unified masked fp8 {dt}")
 
 
+MLA8 = [
+    # (prefix, extend, cap, window, k_scale, v_scale, mask, sinks)
+    ([0, 70, 300], [9, 1, 130], 0.0, -1, 0.25, 0.25, False, False),
+    ([129, 5], [17, 40], 20.0, 50, 0.5, 0.125, False, False),
+    ([60, 300], [33, 70], 0.0, -1, 0.25, 0.25, True, True),
+]
+
+
+@pytest.mark.parametrize("dt", FMTS)
+@pytest.mark.parametrize("prefix,extend,cap,window,ks,vs,mask,sinks", MLA8)
+def test_mla_extend_over_fp8_pool(dt, prefix, extend, cap, window, ks, vs, mask, sinks):
+    """The MLA head (576 / 512, v_buffer a view of k_buffer's codes) over an
+    fp8 pool on CTA pairs, two-stage and unified, against the oracle reading
+    the same codes (a key reads code * k_scale, a value code * v_scale)."""
+    from gpu_cases import random_masks
+    spec = W.small_spec(batch=len(prefix), hq=16, hkv=1, lq=576, lv=512, prefix=prefix,
+                        extend=extend, logit_cap=cap, sliding_window=window, std=0.5,
+                        v_aliases_k=True, sm_scale=1.0 / math.sqrt(192.0),
+                        seed=sum(prefix) + 3 * sum(extend))
+    wl = W.draw(spec)
+    kb, vb = wl.pool_fp8(dt, ks, vs)
+    kw = {}
+    if mask:
+        cm, mi = random_masks(wl, seed=sum(prefix))
+        kw.update(custom_mask=cm, mask_indptr=mi)
+    if sinks:
+        kw["sinks"] = (torch.randn(16, generator=torch.Generator().manual_seed(16)) * 2.0).float()
+    dkw = {k: v.to(DEV) for k, v in kw.items()}
+    k_ext, v_ext = wl.extend_kv()
+    ro, rl = oracle.extend_attention(wl.q, k_ext, v_ext, kb, vb, wl.qo_indptr, wl.kv_indptr,
+                                     wl.kv_indices, wl.sm_scale, cap, window, k_scale=ks,
+                                     v_scale=vs, **kw)
+    dkb = kb.to(DEV)
+    dvb = dkb[..., :512]
+    dke = k_ext.to(DEV)
+    n = wl.n_q_tokens
+    o = torch.full((n, 16, 512), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((n, 16), float("nan"), dtype=torch.float32, device=DEV)
+    ws = pkx.extend_attention_fwd(wl.q.to(DEV), dke, dke[..., :512], o, dkb, dvb,
+                                  wl.qo_indptr.to(DEV), wl.kv_indptr.to(DEV),
+                                  wl.kv_indices.to(DEV), wl.sm_scale, cap, window, lse=lse,
+                                  k_scale=ks, v_scale=vs, **dkw)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    assert_close(o, lse, ro, rl, f"mla two-stage fp8 {dt}")
+    uptr, uidx, plen = oracle.build_unified_kv_indices(
+        wl.kv_indptr, wl.kv_indices, wl.extend_start_loc, wl.extend_seq_lens,
+        wl.extend_kv_indices, wl.batch)
+    uo, ul = oracle.extend_attention_unified(wl.q, kb, vb, wl.qo_indptr, uptr, uidx, plen,
+                                             wl.sm_scale, cap, window, k_scale=ks, v_scale=vs,
+                                             **kw)
+    o2 = torch.full_like(o, float("nan"))
+    l2 = torch.full_like(lse, float("nan"))
+    ws2 = pkx.extend_attention_fwd_unified(wl.q.to(DEV), o2, dkb, dvb, wl.qo_indptr.to(DEV),
+                                           uptr.to(DEV), uidx.to(DEV), plen.to(DEV),
+                                           wl.sm_scale, cap, window, lse=l2, k_scale=ks,
+                                           v_scale=vs, **dkw)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws2) == 0
+    assert_close(o2, l2, uo, ul, f"mla unified fp8 {dt}")
+
+
+@pytest.mark.parametrize("dt", FMTS)
+def test_mla_decode_over_fp8_pool(dt):
+    lens = [1, 64, 65, 700, 4096]
+    spec = W.WorkloadSpec("dec_mla8", batch=len(lens), hq=16, hkv=1, lq=576, lv=512,
+                          prefix=[t - 1 for t in lens], extend=[1] * len(lens),
+                          num_slots=2 * sum(lens) + 16, sm_scale=1.0 / math.sqrt(192.0),
+                          std=0.5, seed=sum(lens), v_aliases_k=True, decode=True)
+    wl = W.draw(spec)
+    kb, vb = wl.pool_fp8(dt, 0.25, 0.25)
+    ro, rl = oracle.decode_attention(wl.q, kb, vb, wl.kv_indptr, wl.kv_indices, wl.sm_scale,
+                                     k_scale=0.25, v_scale=0.25)
+    dkb = kb.to(DEV)
+    o = torch.full((wl.batch, 16, 512), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((wl.batch, 16), float("nan"), dtype=torch.float32, device=DEV)
+    ws = pkx.decode_attention_fwd(wl.q.to(DEV), o, dkb, dkb[..., :512], wl.kv_indptr.to(DEV),
+                                  wl.kv_indices.to(DEV), wl.sm_scale, lse=lse, k_scale=0.25,
+                                  v_scale=0.25)
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    assert_close(o, lse, ro, rl, f"mla decode fp8 {dt}")
+
+
 @pytest.mark.parametrize("dt", FMTS)
 @pytest.mark.parametrize("lq,hq,hkv,lens,cap,window,ks,vs", [
     (128, 32, 8, [1, 17, 128, 129, 4000], 0.0, -1, 1.0, 1.0),
