@@ -40,10 +40,11 @@
 // A buffer's XFULL is armed (one arrival that expects the tile's bytes) by
 // thread 0 once the buffer's previous phase has completed; the bytes may
 // land first.  No barrier frees a buffer: a thread sends tile t only after
-// tile t - 1 of all 128 threads of the other rank landed here, and each of
-// them read its row of tile t - 2 from the buffer before it sent tile t - 1
-// (the complete-tx of its stores releases at cluster scope, the wait here
-// acquires).
+// tile t - 1 of all exchanging threads of the other rank landed here, and
+// each of them read its row of tile t - 2 from the buffer before it sent
+// tile t - 1 (the complete-tx of its stores releases at cluster scope, the
+// wait here acquires).  Extend exchanges all 128 rows; in decode, whose
+// units all hold G rows, only the warps with real rows exchange.
 // Both CTAs of a pair take the same units (position pair + k * pairs of the
 // claim order), so their tile counters stay in step.
 // Warps: 0-3 softmax (one row per thread; they also write Q into TMEM), 4 MMA
@@ -180,22 +181,32 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     uint32_t own[C::BN];  // this rank's partial S of the next tile
     // S of the next tile into registers, released for the next QK^T, and
     // sent to the other rank
+    // Warps that exchange: every decode unit holds G rows (one token), so
+    // only the warps with real rows send and receive, and a tile's phase
+    // expects their bytes; extend units exchange all 128 rows.
+    const int xw = MODE == kDecode ? min(4, (G + 31) / 32) : 4;
+    const bool xch = warp < xw;
+    const uint32_t xbytes = (uint32_t)xw * 32u * (C::BN * 4u);
     auto send = [&]() -> bool {
       if (!mbar_wait(&bars[X_S_FULL], s_cnt & 1u, abort_flag, p.wait_ns)) return false;
       ++s_cnt;
       tc_fence_after();
-      tmem_ld32(lane_base + C::S_COL, *reinterpret_cast<uint32_t (*)[32]>(own));
-      tmem_ld32(lane_base + C::S_COL + 32, *reinterpret_cast<uint32_t (*)[32]>(own + 32));
-      tmem_wait_ld();
+      if (xch) {
+        tmem_ld32(lane_base + C::S_COL, *reinterpret_cast<uint32_t (*)[32]>(own));
+        tmem_ld32(lane_base + C::S_COL + 32, *reinterpret_cast<uint32_t (*)[32]>(own + 32));
+        tmem_wait_ld();
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[X_S_FREE]);
       const uint32_t b = n_sent & 1u;
+      if (xch) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_async_cluster_u4(send_row + b * C::X_BYTES + c * (C::BM * 16),
-                            make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
-                            xfull_peer + b * 8u);
+        for (int c = 0; c < 16; ++c)
+          st_async_cluster_u4(send_row + b * C::X_BYTES + c * (C::BM * 16),
+                              make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
+                              xfull_peer + b * 8u);
+      }
       ++n_sent;
       return true;
     };
@@ -203,12 +214,14 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     // the same sum bit for bit)
     auto combine = [&](float (&x)[C::BN]) -> bool {
       const uint32_t b = n_recv & 1u;
-      if (!mbar_wait_cluster(&bars[X_XFULL + b], (n_recv >> 1) & 1u, abort_flag, p.wait_ns))
+      if (xch &&
+          !mbar_wait_cluster(&bars[X_XFULL + b], (n_recv >> 1) & 1u, abort_flag, p.wait_ns))
         return false;
       ++n_recv;
       // the buffer's phase for tile n_recv + 1 (its bytes cannot land before
-      // every warp here has released this tile)
-      if (tid == 0) mbar_arrive_expect_tx(&bars[X_XFULL + b], C::X_BYTES);
+      // every exchanging warp here has read this tile; warp 0 always exchanges)
+      if (tid == 0) mbar_arrive_expect_tx(&bars[X_XFULL + b], xbytes);
+      if (!xch) return true;  // no real rows: x is not used
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const uint4 o4 =
@@ -221,8 +234,8 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
       return true;
     };
     if (tid == 0) {  // the first two tiles
-      mbar_arrive_expect_tx(&bars[X_XFULL], C::X_BYTES);
-      mbar_arrive_expect_tx(&bars[X_XFULL + 1], C::X_BYTES);
+      mbar_arrive_expect_tx(&bars[X_XFULL], xbytes);
+      mbar_arrive_expect_tx(&bars[X_XFULL + 1], xbytes);
     }
     if (p.stall && !mbar_wait(&bars[X_NEVER], 0, abort_flag, p.wait_ns))
       abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
