@@ -431,14 +431,16 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     int lo, hi, i0, i1;
     qblock_range(p, d, qb - sOff[b], lo, hi, i0, i1);
     const int nt = bNt[qb], S = splits(nt);
-    const int tps = nt > 0 ? (nt + S - 1) / S : 0;
+    // split sp covers tiles [sp nt / S, (sp + 1) nt / S): sizes differ by
+    // one at most
+    const int t0 = (int)((long long)sp * nt / S), t1 = (int)((long long)(sp + 1) * nt / S);
     WorkUnit w;
     w.q_tok0 = d.qbase + i0;
     w.n_tok = i1 - i0;
     w.qpos0 = d.P + i0;
     w.kvh = kvh;
-    w.k_begin = min(hi, lo + sp * tps * p.bn);
-    w.k_end = min(hi, lo + (sp + 1) * tps * p.bn);
+    w.k_begin = min(hi, lo + t0 * p.bn);
+    w.k_end = min(hi, lo + t1 * p.bn);
     w.k_split = split_at;
     w.n_tiles = range_tiles(w.k_begin, w.k_end, split_at, p.bn);
     w.b = b;

@@ -45,10 +45,18 @@
 // tile t - 1 (the complete-tx of its stores releases at cluster scope, the
 // wait here acquires).  Extend exchanges all 128 rows; in decode, whose
 // units all hold G rows, only the warps with real rows exchange.
-// Both CTAs of a pair take the same units (position pair + k * pairs of the
-// claim order), so their tile counters stay in step.
+// Both CTAs of a pair take the same units in the same order, so their tile
+// counters stay in step: one thread of rank 0 claims them from the global
+// cost order (largest first) and writes each into slot uc % 4 of both ranks'
+// unit rings (a remote store, then a remote arrive that releases it on the
+// slot's U_FULL there); every consuming warp of both ranks releases the slot
+// on rank 0's U_EMPTY.  The claimer takes unit uc only once every warp has
+// taken unit uc - 2, so a pair holds at most three units and the rest stay
+// free for whichever pair finishes first.  The row-index warp, which runs
+// tiles ahead, prefetches each unit's query rows into L2.
 // Warps: 0-3 softmax (one row per thread; they also write Q into TMEM), 4 MMA
-// issue, 5 row indices, 6-9 K-row copies (cp.async), 10-11 idle.
+// issue, 5 row indices, 6-9 K-row copies (cp.async), 10 unit claims (one
+// thread of rank 0), 11 idle.
 
 struct MlaPairCfg {
   static constexpr int BM = kBlockM, BN = 64;
@@ -64,7 +72,10 @@ struct MlaPairCfg {
   static constexpr int OFF_X = NK * K_BYTES;     // received from the other rank
   static constexpr int OFF_I = OFF_X + 2 * X_BYTES;
   static constexpr int OFF_BAR = OFF_I + NI * I_BYTES;
-  static constexpr int N_BARS = 16 + 2 * NK + 2 * NI;
+  static constexpr int URING = 4;               // unit ring slots
+  static constexpr int CLAIM_AHEAD = 2;         // units claimed past the slowest warp's
+  static constexpr int UNIT_WARPS = 10;         // warps per CTA that take units
+  static constexpr int N_BARS = 18 + 2 * NK + 2 * NI;
   static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 1024;
   static constexpr int TMEM_COLS = 512;
   static constexpr int Q_COL = 0, P_COL = 160, S_COL = 192, O_COL = 256;
@@ -78,7 +89,7 @@ struct MlaPairCfg {
   static constexpr int REGS_LAUNCH = 168, REGS_SOFTMAX = 232, REGS_OTHER = 136;
   static_assert(128 * REGS_SOFTMAX + 256 * REGS_OTHER == THREADS * REGS_LAUNCH,
                 "register split");
-  static_assert(SMEM + 16 <= 232448, "shared memory budget (dynamic + static)");
+  static_assert(SMEM + 64 <= 232448, "shared memory budget (dynamic + static, padded)");
   static_assert(DR == 32 && KSTEPS == 18, "the rope dims fill half an atom");
 };
 
@@ -92,13 +103,28 @@ enum {
   X_PV_DONE = 6,  // one phase per PV: P and O are free again
   X_NEVER = 7,    // no thread ever arrives (the stall hook waits on it)
   X_XFULL = 8,    // + buffer: the other rank's partial landed (one arrival + its bytes)
-  X_RING = 16
+  X_U_FULL = 10,  // + slot: a unit written into the slot (the claimer's arrival)
+  X_U_EMPTY = 14, // + slot, rank 0 only: every consuming warp of both ranks read it
+  X_RING = 18
 };
 
-// The i-th unit of this pair (claim order position pair + i * pairs), or -1.
-__device__ __forceinline__ int pair_unit(const KParams &p, int n_units, uint32_t i) {
-  const long long pos = (long long)(blockIdx.x >> 1) + (long long)i * (gridDim.x >> 1);
-  return pos < n_units ? p.uorder[pos] : -1;
+// Unit uc of this pair from the claim ring, or -1 at the end.  Every lane of
+// the calling warp takes it; lane 0 then releases the slot on rank 0's
+// U_EMPTY (empty0: that barrier array's cluster address).  ok is cleared if
+// the wait gave up.
+__device__ __forceinline__ int pair_take(uint64_t *bars, const volatile int *ring,
+                                         uint32_t empty0, uint32_t uc, volatile int *abort_flag,
+                                         uint64_t limit_ns, bool &ok) {
+  const int slot = uc % MlaPairCfg::URING;
+  if (!mbar_wait_cluster(&bars[X_U_FULL + slot], (uc / MlaPairCfg::URING) & 1u, abort_flag,
+                         limit_ns)) {
+    ok = false;
+    return -1;
+  }
+  const int u = ring[slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(empty0 + (uint32_t)slot * 8u);
+  return u;
 }
 
 // FMT: the pool's element format (0 bf16; 1 fp8 e4m3, 2 fp8 e5m2 with
@@ -112,6 +138,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_unit[MlaPairCfg::URING];
 
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -139,6 +166,10 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     mbar_init(&bars[X_PV_DONE], 1);
     mbar_init(&bars[X_NEVER], 1);
     for (int b = 0; b < 2; ++b) mbar_init(&bars[X_XFULL + b], 1);
+    for (int s = 0; s < C::URING; ++s) {
+      mbar_init(&bars[X_U_FULL + s], 1);
+      mbar_init(&bars[X_U_EMPTY + s], 2 * C::UNIT_WARPS);
+    }
     for (int s = 0; s < C::NK; ++s) {
       mbar_init(&k_full[s], C::COPY_THREADS);
       mbar_init(&k_empty[s], 1);
@@ -163,6 +194,8 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
   const uint32_t tmem = s_tmem;
   const int n_units = p.hdr->n_units;
   const int G = p.group;
+  const volatile int *uring = s_unit;
+  const uint32_t empty0 = cluster_addr(smem_u32(&bars[X_U_EMPTY]), 0);
   if (warp < 4) regs_increase<C::REGS_SOFTMAX>();
   else regs_decrease<C::REGS_OTHER>();
 
@@ -237,10 +270,40 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
       mbar_arrive_expect_tx(&bars[X_XFULL], xbytes);
       mbar_arrive_expect_tx(&bars[X_XFULL + 1], xbytes);
     }
+    // this rank's Q dims of unit wq into TMEM as bf16 pairs: four value
+    // atoms in columns [0, 128), the rope dims in [128, 144) (zeros up to
+    // 160); rows past the block get zeros.  The previous unit's products
+    // have all completed (its epilogue waited for them).
+    auto write_q = [&](const WorkUnit &wq) {
+      const bool vq = r < wq.n_tok * G;
+      const int tq = r / G, gq = r - (r / G) * G;
+      const int64_t oq = (int64_t)(wq.q_tok0 + tq) * p.hq + wq.kvh * G + gq;
+      const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + oq * C::LQ);
+#pragma unroll 1
+      for (int c = 0; c < 5; ++c) {
+        uint32_t v[32];
+        const int q0 = c < 4 ? (dv0 + 64 * c) / 8 : dr0 / 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 x = vq && (c < 4 || i < C::DR / 8) ? __ldg(qrow + q0 + i)
+                                                         : make_uint4(0, 0, 0, 0);
+          v[4 * i + 0] = x.x;
+          v[4 * i + 1] = x.y;
+          v[4 * i + 2] = x.z;
+          v[4 * i + 3] = x.w;
+        }
+        tmem_st32(lane_base + C::Q_COL + c * 32, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[X_Q_FULL]);
+    };
     if (p.stall && !mbar_wait(&bars[X_NEVER], 0, abort_flag, p.wait_ns))
       abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
     for (uint32_t uc = 0; !*abort_flag; ++uc) {
-      const int u = pair_unit(p, n_units, uc);
+      bool took = true;
+      const int u = pair_take(bars, uring, empty0, uc, abort_flag, p.wait_ns, took);
+      if (!took) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
       if (u < 0) break;
       const WorkUnit w = p.units[u];
       const int nt = w.n_tiles;
@@ -277,31 +340,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
         }
         continue;
       }
-      // this rank's Q dims into TMEM as bf16 pairs: four value atoms in
-      // columns [0, 128), the rope dims in [128, 144) (zeros up to 160);
-      // rows past the block get zeros.  The previous unit's products have
-      // all completed (its epilogue waited for them).
-      {
-        const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + orow_idx * C::LQ);
-#pragma unroll 1
-        for (int c = 0; c < 5; ++c) {
-          uint32_t v[32];
-          const int q0 = c < 4 ? (dv0 + 64 * c) / 8 : dr0 / 8;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 x = valid && (c < 4 || i < C::DR / 8) ? __ldg(qrow + q0 + i)
-                                                              : make_uint4(0, 0, 0, 0);
-            v[4 * i + 0] = x.x;
-            v[4 * i + 1] = x.y;
-            v[4 * i + 2] = x.z;
-            v[4 * i + 3] = x.w;
-          }
-          tmem_st32(lane_base + C::Q_COL + c * 32, v);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars[X_Q_FULL]);
-      }
+      write_q(w);
       if (!send()) {  // the unit's first tile
         abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
         break;
@@ -554,7 +593,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
       return true;
     };
     for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-      const int u = pair_unit(p, n_units, uc);
+      const int u = pair_take(bars, uring, empty0, uc, abort_flag, p.wait_ns, ok);
       if (u < 0) break;
       const WorkUnit w = p.units[u];
       const int nt = w.n_tiles;
@@ -586,13 +625,18 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     uint32_t ic = 0;
     bool ok = true;
     for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-      const int u = pair_unit(p, n_units, uc);
+      const int u = pair_take(bars, uring, empty0, uc, abort_flag, p.wait_ns, ok);
       if (u < 0) break;
       const WorkUnit w = p.units[u];
       const int nt = w.n_tiles;
       if (nt == 0) continue;
       const int64_t kv_base = p.kv_indptr[w.b];
       const int64_t ext_base = MODE == kTwoStage ? p.qo_indptr[w.b] : 0;
+      // the unit's query rows (G consecutive rows per token) into L2: this
+      // warp runs tiles ahead of the softmax, which loads them into TMEM
+      for (int t = lane; t < w.n_tok; t += 32)
+        prefetch_l2_bulk(p.q + ((int64_t)(w.q_tok0 + t) * p.hq + w.kvh * G) * C::LQ,
+                         (uint32_t)(G * C::LQ * 2));
       for (int j = 0; j < nt; ++j) {
         int kb, ke;
         tile_keys<C::BN>(w, j, kb, ke);
@@ -645,7 +689,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     bool ok = true;
     if constexpr (FMT == 0) {
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-        const int u = pair_unit(p, n_units, uc);
+        const int u = pair_take(bars, uring, empty0, uc, abort_flag, p.wait_ns, ok);
         if (u < 0) break;
         const WorkUnit w = p.units[u];
         const int nt = w.n_tiles;
@@ -713,7 +757,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
         return true;
       };
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-        const int u = pair_unit(p, n_units, uc);
+        const int u = pair_take(bars, uring, empty0, uc, abort_flag, p.wait_ns, ok);
         if (u < 0) break;
         const WorkUnit w = p.units[u];
         const int nt = w.n_tiles;
@@ -814,6 +858,40 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     }
     if (!ok) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
     cp_async_wait_all();
+  } else if (warp == 10) {
+    // ------------------------------------- unit claims (one thread of rank 0)
+    // Claims the next unit of the cost order and writes it into the next
+    // slot of both ranks' rings once all consuming warps of both ranks have
+    // released the slot's previous unit; -1 (after the last unit, or after
+    // an abort) ends every consumer.
+    if (rank == 0 && lane == 0) {
+      const uint32_t ring_peer = cluster_addr(smem_u32(&s_unit[0]), 1);
+      const uint32_t full_peer = cluster_addr(smem_u32(&bars[X_U_FULL]), 1);
+      static_assert(C::CLAIM_AHEAD >= 1 && C::CLAIM_AHEAD <= C::URING, "claim lag");
+      for (uint32_t uc = 0;; ++uc) {
+        const int slot = uc % C::URING;
+        // every warp of both ranks took unit uc - CLAIM_AHEAD, and so the
+        // slot's previous unit uc - URING
+        if (uc >= (uint32_t)C::CLAIM_AHEAD) {
+          const uint32_t e = uc - C::CLAIM_AHEAD;
+          if (!mbar_wait_cluster(&bars[X_U_EMPTY + e % C::URING], (e / C::URING) & 1u, abort_flag,
+                                 p.wait_ns)) {
+            abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+            break;
+          }
+        }
+        int u = -1;
+        if (!*abort_flag) {
+          const int pos = atomicAdd(p.next_unit, 1);
+          if (pos < n_units) u = p.uorder[pos];
+        }
+        s_unit[slot] = u;
+        st_cluster_s32(ring_peer + (uint32_t)slot * 4u, u);
+        mbar_arrive(&bars[X_U_FULL + slot]);
+        mbar_arrive_cluster(full_peer + (uint32_t)slot * 8u);
+        if (u < 0) break;
+      }
+    }
   }
 
   tc_fence_before();

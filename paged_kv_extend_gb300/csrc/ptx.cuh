@@ -149,6 +149,11 @@ __device__ __forceinline__ void st_async_cluster_u4(uint32_t addr, uint4 v, uint
       ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar_cluster)
       : "memory");
 }
+// Plain 4-byte store into the shared memory of a CTA of the cluster (made
+// visible there by a later release, e.g. mbar_arrive_cluster).
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 // Barrier of every thread of every CTA of the cluster.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
@@ -164,6 +169,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Fetch [addr, addr + bytes) into L2 without waiting (addr 16-byte aligned,
+// bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void *addr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {

@@ -474,8 +474,14 @@ def test_model_catches_planted_mistakes(mistake):
 # ------------------------------------------------------------------ MLA kernel
 class _MlaPairModel:
     """The mbarrier protocol of mla_pair_kernel (csrc/mla_pair_kernel.cuh):
-    two CTAs of a cluster take the same units in the same order (no unit
-    ring).  Per CTA: one K ring of four stages (the tile is also V); QK^T runs
+    two CTAs of a cluster take the same units in the same order.  A claiming
+    thread of CTA 0 writes each unit into slot uc % 4 of both CTAs' unit
+    rings (U_FULL of each CTA); every role of both CTAs releases the slot on
+    CTA 0's U_EMPTY.  The claimer publishes unit uc once every role has taken
+    unit uc - 2, so a unit is never overwritten before all eight roles have
+    read it.  The softmax writes a unit's Q after the previous unit's
+    epilogue; the model tracks which unit's Q each CTA holds and the QK^T
+    products in flight that read it.  Per CTA: one K ring of four stages (the tile is also V); QK^T runs
     two tiles ahead of PV, S is read and released early (S_FREE); P and O are
     reused after each PV (PV_DONE), whose phases the softmax counts across
     units (pv_base).
@@ -488,11 +494,17 @@ class _MlaPairModel:
     softmax of tile t then adds the received partial to its own.  No barrier
     frees a buffer; the model checks every buffer write and read against the
     buffer's state, so a send that could overwrite an unread tile fails."""
-    NK, NI = 4, 4
+    NK, NI, R, AHEAD = 4, 4, 4, 2
+    ROLES = {"index", "copy", "softmax", "mma"}
 
-    def __init__(self, units, seed, mistake=None, fp8=False):
+    def __init__(self, units, seed, mistake=None, fp8=False, lead=1):
         self.rng = random.Random(seed)
         self.units, self.mistake = units, mistake
+        self.lead = lead  # CTA 0's roles are picked this many times as often
+        # unit ring slot (CTA, slot) -> (claim number, unit, roles that read it)
+        self.uring = {(c, s): None for c in (0, 1) for s in range(self.R)}
+        self.q_unit = {0: None, 1: None}   # whose Q the CTA's TMEM holds
+        self.q_readers = {0: 0, 1: 0}      # QK^T products in flight
         # an fp8 pool: the copy warps mark tile j full only after issuing
         # tile j + 1 (they convert tile j's codes in place in between)
         self.fp8 = fp8
@@ -508,6 +520,10 @@ class _MlaPairModel:
                 for s in range(n):
                     self.bars[f"{c}{pre}F{s}"] = _Bar(f"{c}{pre}F{s}", 1)
                     self.bars[f"{c}{pre}E{s}"] = _Bar(f"{c}{pre}E{s}", 1)
+            one_cta = mistake in ("rank 1 releases its own ring", "slot reused before both CTAs read it")
+            for s in range(self.R):
+                self.bars[f"{c}UF{s}"] = _Bar(f"{c}UF{s}", 1)
+                self.bars[f"{c}UE{s}"] = _Bar(f"{c}UE{s}", 4 if one_cta else 8)
 
     @staticmethod
     def _wait(bar, consumed):
@@ -518,7 +534,7 @@ class _MlaPairModel:
             yield from gen
             yield ("end",)
 
-        roles = {}
+        roles = {"0claim": ending(self._claim())}
         for c in (0, 1):
             roles[f"{c}index"] = ending(self._index(c))
             roles[f"{c}copy"] = ending(self._copy(c))
@@ -537,6 +553,8 @@ class _MlaPairModel:
                         self.xbuf[key] = ("written", ev[2])
                         self.bars[f"{ev[1]}XFULL{ev[2] & 1}"].arrive()
                     else:
+                        if ev.endswith("S_FULL"):  # the QK^T landed: its Q reads are done
+                            self.q_readers[int(ev[0])] -= 1
                         self.bars[ev].arrive()
             ready = [k for k, op in cur.items() if k not in done and
                      (op[0] != "wait" or (self.bars[op[1]].phase & 1) != op[2])]
@@ -547,7 +565,7 @@ class _MlaPairModel:
                 if not live:
                     return
                 raise AssertionError("deadlock: " + ", ".join(f"{k} {cur[k]}" for k in live))
-            k = self.rng.choice(ready)
+            k = self.rng.choices(ready, [self.lead if r[0] == "0" else 1 for r in ready])[0]
             op = cur[k]
             if op[0] == "wait":
                 assert self.bars[op[1]].phase == op[3] + 1, f"{k}: {op[1]} aliased"
@@ -559,6 +577,18 @@ class _MlaPairModel:
                 self.pending[int(op[1][0])].append(op[1])
             elif op[0] == "send":  # asynchronous stores into the other CTA; they land later
                 self.pending[op[1]].append(("land", 1 - op[1], op[2]))
+            elif op[0] == "writeq":  # the softmax writes unit op[2]'s Q into CTA op[1]'s TMEM
+                assert self.q_readers[op[1]] == 0, f"{k}: Q overwritten under a QK^T in flight"
+                self.q_unit[op[1]] = op[2]
+            elif op[0] == "qk":  # a QK^T of unit op[2] reads CTA op[1]'s Q
+                assert self.q_unit[op[1]] == op[2], f"{k}: QK^T of unit {op[2]} reads another unit's Q"
+                self.q_readers[op[1]] += 1
+            elif op[0] == "publish":  # the claimer writes unit use op[2] into slot op[1] of both CTAs
+                for c in (0, 1):
+                    prev = self.uring[(c, op[1])]
+                    assert prev is None or prev[2] == self.ROLES, \
+                        f"unit slot {op[1]} of CTA {c} overwritten before all its roles read it"
+                    self.uring[(c, op[1])] = (op[2], op[3], set())
             elif op[0] == "combine":  # the softmax reads the received partial of tile op[2]
                 key = (op[1], op[2] & 1 if self.mistake != "one receive buffer" else 0)
                 assert self.xbuf[key] == ("written", op[2]), f"{k}: partial read before it lands"
@@ -569,15 +599,40 @@ class _MlaPairModel:
                 done.add(k)
         raise AssertionError("step limit")
 
+    def _claim(self):
+        ahead = self.AHEAD
+        for uc, u in enumerate(self.units + [None]):
+            s = uc % self.R
+            if uc >= ahead:  # every role took unit uc - ahead (and so uc - R)
+                e = uc - ahead
+                yield self._wait(f"0UE{e % self.R}", e // self.R)
+            yield ("publish", s, uc, u)
+            yield ("arrive", "0UF" + str(s))  # local
+            yield ("arrive", "1UF" + str(s))  # remote, after the remote store
+            if u is None:
+                return
+
+    def _take(self, c, role, uc):
+        """Unit use uc from this CTA's ring: wait, read, release on CTA 0."""
+        s = uc % self.R
+        yield self._wait(f"{c}UF{s}", uc // self.R)
+        val = self.uring[(c, s)]
+        assert val is not None and val[0] == uc, f"{c}{role}: unit slot {s} does not hold use {uc}"
+        val[2].add(role)
+        own = self.mistake == "rank 1 releases its own ring"
+        yield ("arrive", f"{c if own else 0}UE{s}")
+
     def _index(self, c):
         ic = 0
-        for u in self.units:
+        for uc, u in enumerate(self.units):
+            yield from self._take(c, "index", uc)
             for _ in range(u["nt"]):
                 si = ic % self.NI
                 if ic >= self.NI:
                     yield self._wait(f"{c}IE{si}", ic // self.NI - 1)
                 yield ("arrive", f"{c}IF{si}")
                 ic += 1
+        yield from self._take(c, "index", len(self.units))
 
     def _copy(self, c):
         kc = ic = 0
@@ -593,7 +648,8 @@ class _MlaPairModel:
                 yield self._wait(f"{c}KE{ks}", kc // self.NK - 1)
             kc += 1
 
-        for u in self.units:
+        for uc, u in enumerate(self.units):
+            yield from self._take(c, "copy", uc)
             nt = u["nt"]
             if not self.fp8:
                 for _ in range(nt):
@@ -608,6 +664,7 @@ class _MlaPairModel:
                 if j + 1 < nt:
                     yield from issue()
                 yield ("arrive", f"{c}KF{st_j}")
+        yield from self._take(c, "copy", len(self.units))
 
     def _softmax(self, c):
         s_cnt = o_cnt = pv_base = n_sent = n_recv = 0
@@ -635,13 +692,29 @@ class _MlaPairModel:
 
         yield ("arrive", f"{c}XFULL0")  # arm the first two tiles' phases
         yield ("arrive", f"{c}XFULL1")
-        for u in self.units:
+        early = self.mistake == "next Q written before the last QK landed"
+        q_in = taken = False  # (planted mistake) the next unit taken and its Q written early
+        for uc, u in enumerate(self.units):
+            if not taken:
+                yield from self._take(c, "softmax", uc)
+            taken = False
             nt = u["nt"]
             if nt == 0:
+                q_in = False
                 continue
-            yield ("arrive", f"{c}Q_FULL")  # this CTA's Q dims written into TMEM
+            if not q_in:
+                yield ("writeq", c, uc)
+                yield ("arrive", f"{c}Q_FULL")  # this CTA's Q dims written into TMEM
+            q_in = False
             yield from send()
             for j in range(nt):
+                if early and j == 0:
+                    yield from self._take(c, "softmax", uc + 1)
+                    taken = True
+                    if uc + 1 < len(self.units) and self.units[uc + 1]["nt"] > 0:
+                        yield ("writeq", c, uc + 1)
+                        yield ("arrive", f"{c}Q_FULL")
+                        q_in = True
                 yield from combine()
                 if j + 1 < nt:
                     yield from send()
@@ -652,19 +725,25 @@ class _MlaPairModel:
             o_cnt += 1
             if self.mistake != "PV count not carried across units":
                 pv_base += nt
+        if not taken:
+            yield from self._take(c, "softmax", len(self.units))
 
     def _mma(self, c):
         q_cnt = kc = s_free = p_cnt = 0
+        cur = None
 
         def qk(kpos):
             yield self._wait(f"{c}KF{kpos % self.NK}", kpos // self.NK)
             yield ("use", f"{c}KF{kpos % self.NK}", kpos // self.NK)
+            yield ("qk", c, cur)
             yield ("commit", f"{c}S_FULL")
 
-        for u in self.units:
+        for uc, u in enumerate(self.units):
+            yield from self._take(c, "mma", uc)
             nt = u["nt"]
             if nt == 0:
                 continue
+            cur = uc
             yield self._wait(f"{c}Q_FULL", q_cnt)
             q_cnt += 1
             k0 = kc
@@ -686,13 +765,18 @@ class _MlaPairModel:
                 yield ("commit", f"{c}KE{(k0 + j) % self.NK}")
             kc = k0 + nt
             yield ("commit", f"{c}O_DONE")
+        yield from self._take(c, "mma", len(self.units))
 
 
 def _mla_trials(n, mistake=None):
     rng = random.Random(2)
     for t in range(n):
-        units = [{"nt": rng.choice([0, 1, 1, 2, 3, 5, 8])} for _ in range(rng.randint(1, 10))]
-        _MlaPairModel(units, seed=t, mistake=mistake).run()
+        # every third trial has runs of empty units, which the softmax of one
+        # CTA passes without an exchange (so it can run ahead of the other)
+        sizes = [0, 0, 0, 1, 2, 5] if t % 3 == 2 else [0, 1, 1, 2, 3, 5, 8]
+        units = [{"nt": rng.choice(sizes)} for _ in range(rng.randint(1, 12))]
+        # and in every other one CTA 0 runs ahead
+        _MlaPairModel(units, seed=t, mistake=mistake, lead=8 if t % 2 else 1).run()
 
 
 def test_mla_protocol_has_no_deadlock_and_no_parity_aliasing():
@@ -711,7 +795,10 @@ def test_mla_fp8_protocol_has_no_deadlock_and_no_parity_aliasing():
                                      "PV count not carried across units",
                                      "partial read before it lands",
                                      "next phase armed before the wait",
-                                     "one receive buffer"])
+                                     "one receive buffer",
+                                     "rank 1 releases its own ring",
+                                     "slot reused before both CTAs read it",
+                                     "next Q written before the last QK landed"])
 def test_mla_model_catches_planted_mistakes(mistake):
     with pytest.raises(AssertionError):
         _mla_trials(150, mistake)
