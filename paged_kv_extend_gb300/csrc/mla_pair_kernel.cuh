@@ -89,7 +89,7 @@ struct MlaPairCfg {
   static constexpr int REGS_LAUNCH = 168, REGS_SOFTMAX = 232, REGS_OTHER = 136;
   static_assert(128 * REGS_SOFTMAX + 256 * REGS_OTHER == THREADS * REGS_LAUNCH,
                 "register split");
-  static_assert(SMEM + 64 <= 232448, "shared memory budget (dynamic + static, padded)");
+  static_assert(SMEM + 256 <= 232448, "shared memory budget (dynamic + static, padded)");
   static_assert(DR == 32 && KSTEPS == 18, "the rope dims fill half an atom");
 };
 
@@ -108,23 +108,27 @@ enum {
   X_RING = 18
 };
 
-// Unit uc of this pair from the claim ring, or -1 at the end.  Every lane of
-// the calling warp takes it; lane 0 then releases the slot on rank 0's
-// U_EMPTY (empty0: that barrier array's cluster address).  ok is cleared if
+// The record of unit uc of this pair from the claim ring (copied there by
+// the claimer); n_tiles < 0 marks the end.  Every lane of the calling warp
+// takes it; lane 0 then releases the slot on rank 0's U_EMPTY (empty0: that
+// barrier array's cluster address).  ok is cleared (and the end returned) if
 // the wait gave up.
-__device__ __forceinline__ int pair_take(uint64_t *bars, const volatile int *ring,
-                                         uint32_t empty0, uint32_t uc, volatile int *abort_flag,
-                                         uint64_t limit_ns, bool &ok) {
+__device__ __forceinline__ WorkUnit pair_take(uint64_t *bars, const WorkUnit *recs,
+                                              uint32_t empty0, uint32_t uc,
+                                              volatile int *abort_flag, uint64_t limit_ns,
+                                              bool &ok) {
   const int slot = uc % MlaPairCfg::URING;
+  WorkUnit w;
   if (!mbar_wait_cluster(&bars[X_U_FULL + slot], (uc / MlaPairCfg::URING) & 1u, abort_flag,
                          limit_ns)) {
     ok = false;
-    return -1;
+    w.n_tiles = -1;
+    return w;
   }
-  const int u = ring[slot];
+  w = recs[slot];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(empty0 + (uint32_t)slot * 8u);
-  return u;
+  return w;
 }
 
 // FMT: the pool's element format (0 bf16; 1 fp8 e4m3, 2 fp8 e5m2 with
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_unit[MlaPairCfg::URING];
+  __shared__ WorkUnit s_rec[MlaPairCfg::URING];  // the claimed units' records
 
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -194,7 +198,6 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
   const uint32_t tmem = s_tmem;
   const int n_units = p.hdr->n_units;
   const int G = p.group;
-  const volatile int *uring = s_unit;
   const uint32_t empty0 = cluster_addr(smem_u32(&bars[X_U_EMPTY]), 0);
   if (warp < 4) regs_increase<C::REGS_SOFTMAX>();
   else regs_decrease<C::REGS_OTHER>();
@@ -302,10 +305,9 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
       abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
     for (uint32_t uc = 0; !*abort_flag; ++uc) {
       bool took = true;
-      const int u = pair_take(bars, uring, empty0, uc, abort_flag, p.wait_ns, took);
+      const WorkUnit w = pair_take(bars, s_rec, empty0, uc, abort_flag, p.wait_ns, took);
       if (!took) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
-      if (u < 0) break;
-      const WorkUnit w = p.units[u];
+      if (w.n_tiles < 0) break;
       const int nt = w.n_tiles;
       const int rows_valid = w.n_tok * G;
       const bool valid = r < rows_valid;
@@ -593,9 +595,8 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
       return true;
     };
     for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-      const int u = pair_take(bars, uring, empty0, uc, abort_flag, p.wait_ns, ok);
-      if (u < 0) break;
-      const WorkUnit w = p.units[u];
+      const WorkUnit w = pair_take(bars, s_rec, empty0, uc, abort_flag, p.wait_ns, ok);
+      if (w.n_tiles < 0) break;
       const int nt = w.n_tiles;
       if (nt == 0) continue;
       if (!mbar_wait(&bars[X_Q_FULL], q_cnt & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
@@ -625,9 +626,8 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     uint32_t ic = 0;
     bool ok = true;
     for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-      const int u = pair_take(bars, uring, empty0, uc, abort_flag, p.wait_ns, ok);
-      if (u < 0) break;
-      const WorkUnit w = p.units[u];
+      const WorkUnit w = pair_take(bars, s_rec, empty0, uc, abort_flag, p.wait_ns, ok);
+      if (w.n_tiles < 0) break;
       const int nt = w.n_tiles;
       if (nt == 0) continue;
       const int64_t kv_base = p.kv_indptr[w.b];
@@ -689,9 +689,8 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     bool ok = true;
     if constexpr (FMT == 0) {
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-        const int u = pair_take(bars, uring, empty0, uc, abort_flag, p.wait_ns, ok);
-        if (u < 0) break;
-        const WorkUnit w = p.units[u];
+        const WorkUnit w = pair_take(bars, s_rec, empty0, uc, abort_flag, p.wait_ns, ok);
+        if (w.n_tiles < 0) break;
         const int nt = w.n_tiles;
         if (nt == 0) continue;
         const bf16 *kp = p.k_pool + (int64_t)w.kvh * p.kb_sh + dv0 + ch * 8;
@@ -757,9 +756,8 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
         return true;
       };
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-        const int u = pair_take(bars, uring, empty0, uc, abort_flag, p.wait_ns, ok);
-        if (u < 0) break;
-        const WorkUnit w = p.units[u];
+        const WorkUnit w = pair_take(bars, s_rec, empty0, uc, abort_flag, p.wait_ns, ok);
+        if (w.n_tiles < 0) break;
         const int nt = w.n_tiles;
         if (nt == 0) continue;
         const uint8_t *kp8 =
@@ -865,7 +863,9 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     // released the slot's previous unit; -1 (after the last unit, or after
     // an abort) ends every consumer.
     if (rank == 0 && lane == 0) {
-      const uint32_t ring_peer = cluster_addr(smem_u32(&s_unit[0]), 1);
+      const uint32_t rec_peer = cluster_addr(smem_u32(&s_rec[0]), 1);
+      static_assert(sizeof(WorkUnit) % 16 == 0, "records move as 16-byte chunks");
+      constexpr int RCH = (int)(sizeof(WorkUnit) / 16);
       const uint32_t full_peer = cluster_addr(smem_u32(&bars[X_U_FULL]), 1);
       static_assert(C::CLAIM_AHEAD >= 1 && C::CLAIM_AHEAD <= C::URING, "claim lag");
       for (uint32_t uc = 0;; ++uc) {
@@ -885,8 +885,21 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
           const int pos = atomicAdd(p.next_unit, 1);
           if (pos < n_units) u = p.uorder[pos];
         }
-        s_unit[slot] = u;
-        st_cluster_s32(ring_peer + (uint32_t)slot * 4u, u);
+        // the record (or the end marker), here and in rank 1
+        WorkUnit rec;
+        if (u >= 0) {
+          rec = p.units[u];
+        } else {
+          rec = WorkUnit{};
+          rec.n_tiles = -1;
+        }
+        const uint4 *src = reinterpret_cast<const uint4 *>(&rec);
+        uint4 *dst = reinterpret_cast<uint4 *>(&s_rec[slot]);
+#pragma unroll
+        for (int i = 0; i < RCH; ++i) {
+          dst[i] = src[i];
+          st_cluster_u4(rec_peer + (uint32_t)(slot * (int)sizeof(WorkUnit) + 16 * i), src[i]);
+        }
         mbar_arrive(&bars[X_U_FULL + slot]);
         mbar_arrive_cluster(full_peer + (uint32_t)slot * 8u);
         if (u < 0) break;
