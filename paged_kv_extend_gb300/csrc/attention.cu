@@ -2091,13 +2091,13 @@ static int launch_attn_fp8(int mode, bool masked, const TMaps &tmaps, const KPar
 }
 
 // Pair kernel launch: clusters of two CTAs, programmatic dependent launch.
-template <int MODE, bool MASK, int FMT = 0>
+template <int MODE, bool MASK, int FMT = 0, bool SG = false>
 static cudaError_t launch_pair(int pairs, cudaStream_t s, const KParams &kp, bool query_only,
                                int *max_pairs) {
-  using C = MlaPairCfg;
+  using C = std::conditional_t<SG, MlaPairDecCfg, MlaPairCfg>;
   static bool configured[kMaxDevicesCfg] = {};
   if (needs_config(configured)) {
-    cudaError_t e = cudaFuncSetAttribute(mla_pair_kernel<MODE, MASK, FMT>,
+    cudaError_t e = cudaFuncSetAttribute(mla_pair_kernel<MODE, MASK, FMT, SG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     mark_configured(configured);
@@ -2116,8 +2116,9 @@ static cudaError_t launch_pair(int pairs, cudaStream_t s, const KParams &kp, boo
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = query_only ? 1 : 2;
-  if (query_only) return cudaOccupancyMaxActiveClusters(max_pairs, mla_pair_kernel<MODE, MASK, FMT>, &cfg);
-  return cudaLaunchKernelEx(&cfg, mla_pair_kernel<MODE, MASK, FMT>, kp);
+  if (query_only)
+    return cudaOccupancyMaxActiveClusters(max_pairs, mla_pair_kernel<MODE, MASK, FMT, SG>, &cfg);
+  return cudaLaunchKernelEx(&cfg, mla_pair_kernel<MODE, MASK, FMT, SG>, kp);
 }
 
 // CTA pairs of the MLA kernel that run at once on the current device (an SM
@@ -2140,7 +2141,14 @@ static int mla_pairs(int nsm) {
 
 template <int MODE, bool MASK = false, int FMT = 0>
 static int launch_mla_pair(const KParams &kp, int pairs, cudaStream_t s) {
-  cudaError_t e = launch_pair<MODE, MASK, FMT>(pairs, s, kp, false, nullptr);
+  cudaError_t e;
+  if constexpr (MODE == kDecode && !MASK) {
+    // decode of at most 32 rows per unit: the five-stage layout
+    e = kp.group <= MlaPairDecCfg::XR ? launch_pair<MODE, false, FMT, true>(pairs, s, kp, false, nullptr)
+                                      : launch_pair<MODE, false, FMT>(pairs, s, kp, false, nullptr);
+  } else {
+    e = launch_pair<MODE, MASK, FMT>(pairs, s, kp, false, nullptr);
+  }
   if (e != cudaSuccess)
     return set_error(PKX_ECUDA, "mla_pair_kernel launch: %s", cudaGetErrorString(e));
   return PKX_OK;

@@ -58,15 +58,18 @@
 // issue, 5 row indices, 6-9 K-row copies (cp.async), 10 unit claims (one
 // thread of rank 0), 11 idle.
 
-struct MlaPairCfg {
+// NK_: K stages; XR_: rows a receive buffer holds (the rows that exchange).
+template <int NK_, int XR_>
+struct MlaPairCfgT {
   static constexpr int BM = kBlockM, BN = 64;
   static constexpr int LQ = 576, LV = 512;
   static constexpr int DV = LV / 2;             // value dims per rank
   static constexpr int DR = (LQ - LV) / 2;      // rope dims per rank
   static constexpr int KSTEPS = (DV + DR) / 16;  // K-steps of QK^T: 18
-  static constexpr int NK = 4, NI = 4;
+  static constexpr int NK = NK_, NI = 4;
+  static constexpr int XR = XR_;
   static constexpr int K_BYTES = BN * 5 * 128;  // four value atoms + the rope atom
-  static constexpr int X_BYTES = BM * BN * 4;   // a partial S
+  static constexpr int X_BYTES = XR * BN * 4;   // a partial S
   static constexpr int I_BYTES = BN * 4;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_X = NK * K_BYTES;     // received from the other rank
@@ -91,7 +94,16 @@ struct MlaPairCfg {
                 "register split");
   static_assert(SMEM + 256 <= 232448, "shared memory budget (dynamic + static, padded)");
   static_assert(DR == 32 && KSTEPS == 18, "the rope dims fill half an atom");
+  static_assert(XR % 32 == 0 && XR <= BM, "whole warps exchange");
 };
+// Extend, and decode of more than 32 rows per unit: four K stages, every
+// row exchanged.
+using MlaPairCfg = MlaPairCfgT<4, kBlockM>;
+// Decode of at most 32 rows per unit (G <= 32): only warp 0 exchanges, so
+// the receive buffers shrink to 32 rows and a fifth K stage fits.  QK^T runs
+// two tiles ahead of PV and holds three stages, so the fifth doubles the
+// stages being copied.
+using MlaPairDecCfg = MlaPairCfgT<5, 32>;
 
 enum {
   X_Q_FULL = 0,
@@ -136,9 +148,12 @@ __device__ __forceinline__ WorkUnit pair_take(uint64_t *bars, const WorkUnit *re
 // place to bf16, exact, one tile behind their copies; k_scale joins the
 // logit scale of pool tiles and v_scale their P).  Extend rows of the
 // two-stage form are always bf16.
-template <int MODE, bool MASK, int FMT = 0>
+// SG: decode with at most 32 rows per unit (the launcher checks G <= 32),
+// laid out by MlaPairDecCfg.
+template <int MODE, bool MASK, int FMT = 0, bool SG = false>
 __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const KParams p) {
-  using C = MlaPairCfg;
+  static_assert(!SG || (MODE == kDecode && !MASK), "the small-group layout is for decode");
+  using C = std::conditional_t<SG, MlaPairDecCfg, MlaPairCfg>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -210,7 +225,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     uint32_t n_sent = 0, n_recv = 0;  // tiles sent / combined so far
     uint32_t pv_base = 0;  // PVs of earlier units (X_PV_DONE phases)
     const uint32_t xfull_peer = cluster_addr(smem_u32(&bars[X_XFULL]), peer);
-    // this thread's row of receive buffer 0 (chunk c at c * BM * 16), here
+    // this thread's row of receive buffer 0 (chunk c at c * XR * 16), here
     // and in the other rank
     const uint8_t *recv_row = smem + C::OFF_X + r * 16;
     const uint32_t send_row = cluster_addr(sbase + C::OFF_X + r * 16, peer);
@@ -219,8 +234,9 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     // sent to the other rank
     // Warps that exchange: every decode unit holds G rows (one token), so
     // only the warps with real rows send and receive, and a tile's phase
-    // expects their bytes; extend units exchange all 128 rows.
-    const int xw = MODE == kDecode ? min(4, (G + 31) / 32) : 4;
+    // expects their bytes; extend units exchange all 128 rows.  (The
+    // receive buffers hold C::XR rows: the decode layout takes G <= 32.)
+    const int xw = MODE == kDecode ? min(C::XR / 32, (G + 31) / 32) : C::XR / 32;
     const bool xch = warp < xw;
     const uint32_t xbytes = (uint32_t)xw * 32u * (C::BN * 4u);
     auto send = [&]() -> bool {
@@ -239,7 +255,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
       if (xch) {
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          st_async_cluster_u4(send_row + b * C::X_BYTES + c * (C::BM * 16),
+          st_async_cluster_u4(send_row + b * C::X_BYTES + c * (C::XR * 16),
                               make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
                               xfull_peer + b * 8u);
       }
@@ -261,7 +277,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const uint4 o4 =
-            *reinterpret_cast<const uint4 *>(recv_row + b * C::X_BYTES + c * (C::BM * 16));
+            *reinterpret_cast<const uint4 *>(recv_row + b * C::X_BYTES + c * (C::XR * 16));
         x[4 * c + 0] = __uint_as_float(own[4 * c + 0]) + __uint_as_float(o4.x);
         x[4 * c + 1] = __uint_as_float(own[4 * c + 1]) + __uint_as_float(o4.y);
         x[4 * c + 2] = __uint_as_float(own[4 * c + 2]) + __uint_as_float(o4.z);
@@ -342,7 +358,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
         }
         continue;
       }
-      write_q(w);
+      if constexpr (!SG) write_q(w);  // (small-group decode: the MMA warp writes Q)
       if (!send()) {  // the unit's first tile
         abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
         break;
@@ -599,9 +615,45 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
       if (w.n_tiles < 0) break;
       const int nt = w.n_tiles;
       if (nt == 0) continue;
-      if (!mbar_wait(&bars[X_Q_FULL], q_cnt & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
-      ++q_cnt;
-      tc_fence_after();
+      if constexpr (SG) {
+        // Decode of at most 32 rows: only TMEM lanes 0-31 matter, and this
+        // warp (lanes 0-31) writes the unit's Q itself.  Every QK^T of the
+        // previous unit has landed: this warp waited for its last P, which
+        // the softmax wrote after it saw the last S.  Lanes 32-127 keep
+        // whatever they hold; their rows are never read.
+        const bool vq = lane < w.n_tok * G;
+        const int64_t oq = (int64_t)(w.q_tok0 + lane / G) * p.hq + w.kvh * G + lane % G;
+        const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + oq * C::LQ);
+        static_for<0, 3>([&](auto h_c) {  // loads of 16, 16 and 4 chunks
+          constexpr int h = decltype(h_c)::value;
+          constexpr int c0 = 2 * h, nc = h < 2 ? 2 : 1;  // 32-column groups
+          uint32_t v[nc][32];
+#pragma unroll
+          for (int c = 0; c < nc; ++c) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int k = 8 * (c0 + c) + i;  // 16-byte chunk: 32 value, then 4 rope
+              const int q0 = k < C::DV / 8 ? dv0 / 8 + k : dr0 / 8 + (k - C::DV / 8);
+              const uint4 x = vq && k < (C::DV + C::DR) / 8 ? __ldg(qrow + q0)
+                                                            : make_uint4(0, 0, 0, 0);
+              v[c][4 * i + 0] = x.x;
+              v[c][4 * i + 1] = x.y;
+              v[c][4 * i + 2] = x.z;
+              v[c][4 * i + 3] = x.w;
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < nc; ++c) tmem_st32(tmem + C::Q_COL + (c0 + c) * 32, v[c]);
+        });
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        tc_fence_after();
+      } else {
+        if (!mbar_wait(&bars[X_Q_FULL], q_cnt & 1u, abort_flag, p.wait_ns)) { ok = false; break; }
+        ++q_cnt;
+        tc_fence_after();
+      }
       const uint32_t k0 = kc;
       // S(0); S(1) once S(0) is read
       if (!qk(k0) || !s_free() || (nt > 1 && !qk(k0 + 1))) { ok = false; break; }

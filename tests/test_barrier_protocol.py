@@ -480,8 +480,11 @@ class _MlaPairModel:
     CTA 0's U_EMPTY.  The claimer publishes unit uc once every role has taken
     unit uc - 2, so a unit is never overwritten before all eight roles have
     read it.  The softmax writes a unit's Q after the previous unit's
-    epilogue; the model tracks which unit's Q each CTA holds and the QK^T
-    products in flight that read it.  Per CTA: one K ring of four stages (the tile is also V); QK^T runs
+    epilogue (or, in decode of at most 32 rows, the MMA warp writes it as it
+    starts the unit: it has waited for the previous unit's last P, which the
+    softmax writes only after the last QK^T landed); the model tracks which
+    unit's Q each CTA holds and the QK^T products in flight that read it.
+    Per CTA: one K ring of four stages (the tile is also V); QK^T runs
     two tiles ahead of PV, S is read and released early (S_FREE); P and O are
     reused after each PV (PV_DONE), whose phases the softmax counts across
     units (pv_base).
@@ -497,7 +500,8 @@ class _MlaPairModel:
     NK, NI, R, AHEAD = 4, 4, 4, 2
     ROLES = {"index", "copy", "softmax", "mma"}
 
-    def __init__(self, units, seed, mistake=None, fp8=False, lead=1):
+    def __init__(self, units, seed, mistake=None, fp8=False, lead=1, mma_q=False):
+        self.mma_q = mma_q  # the MMA warp writes Q (decode of at most 32 rows)
         self.rng = random.Random(seed)
         self.units, self.mistake = units, mistake
         self.lead = lead  # CTA 0's roles are picked this many times as often
@@ -702,7 +706,7 @@ class _MlaPairModel:
             if nt == 0:
                 q_in = False
                 continue
-            if not q_in:
+            if not q_in and not self.mma_q:
                 yield ("writeq", c, uc)
                 yield ("arrive", f"{c}Q_FULL")  # this CTA's Q dims written into TMEM
             q_in = False
@@ -731,12 +735,21 @@ class _MlaPairModel:
     def _mma(self, c):
         q_cnt = kc = s_free = p_cnt = 0
         cur = None
+        early_q = False  # (planted mistake) the next unit's Q written after the last QK^T issue
+        nxt = {}
+        for i, u in enumerate(self.units):  # the next unit with tiles
+            nxt[i] = next((k for k in range(i + 1, len(self.units)) if self.units[k]["nt"] > 0), None)
 
         def qk(kpos):
+            nonlocal early_q
             yield self._wait(f"{c}KF{kpos % self.NK}", kpos // self.NK)
             yield ("use", f"{c}KF{kpos % self.NK}", kpos // self.NK)
             yield ("qk", c, cur)
             yield ("commit", f"{c}S_FULL")
+            if (self.mma_q and self.mistake == "next Q written after the last QK issue"
+                    and kpos == k_last and nxt[cur] is not None):
+                yield ("writeq", c, nxt[cur])
+                early_q = True
 
         for uc, u in enumerate(self.units):
             yield from self._take(c, "mma", uc)
@@ -744,9 +757,15 @@ class _MlaPairModel:
             if nt == 0:
                 continue
             cur = uc
-            yield self._wait(f"{c}Q_FULL", q_cnt)
+            if self.mma_q:
+                if not early_q:
+                    yield ("writeq", c, uc)
+                early_q = False
+            else:
+                yield self._wait(f"{c}Q_FULL", q_cnt)
             q_cnt += 1
             k0 = kc
+            k_last = k0 + nt - 1
             yield from qk(k0)
             yield self._wait(f"{c}S_FREE", s_free)
             s_free += 1
@@ -768,7 +787,7 @@ class _MlaPairModel:
         yield from self._take(c, "mma", len(self.units))
 
 
-def _mla_trials(n, mistake=None):
+def _mla_trials(n, mistake=None, mma_q=False):
     rng = random.Random(2)
     for t in range(n):
         # every third trial has runs of empty units, which the softmax of one
@@ -776,11 +795,21 @@ def _mla_trials(n, mistake=None):
         sizes = [0, 0, 0, 1, 2, 5] if t % 3 == 2 else [0, 1, 1, 2, 3, 5, 8]
         units = [{"nt": rng.choice(sizes)} for _ in range(rng.randint(1, 12))]
         # and in every other one CTA 0 runs ahead
-        _MlaPairModel(units, seed=t, mistake=mistake, lead=8 if t % 2 else 1).run()
+        _MlaPairModel(units, seed=t, mistake=mistake, lead=8 if t % 2 else 1, mma_q=mma_q).run()
 
 
 def test_mla_protocol_has_no_deadlock_and_no_parity_aliasing():
     _mla_trials(150)
+
+
+def test_mla_small_group_decode_protocol():
+    """Decode of at most 32 rows: the MMA warp writes each unit's Q itself."""
+    _mla_trials(150, mma_q=True)
+
+
+def test_mla_model_catches_q_written_under_products():
+    with pytest.raises(AssertionError):
+        _mla_trials(150, "next Q written after the last QK issue", mma_q=True)
 
 
 def test_mla_fp8_protocol_has_no_deadlock_and_no_parity_aliasing():
