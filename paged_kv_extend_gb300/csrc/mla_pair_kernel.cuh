@@ -49,14 +49,18 @@
 // counters stay in step: one thread of rank 0 claims them from the global
 // cost order (largest first) and writes each into slot uc % 4 of both ranks'
 // unit rings (a remote store, then a remote arrive that releases it on the
-// slot's U_FULL there); every consuming warp of both ranks releases the slot
-// on rank 0's U_EMPTY.  The claimer takes unit uc only once every warp has
-// taken unit uc - 2, so a pair holds at most three units and the rest stay
-// free for whichever pair finishes first.  The row-index warp, which runs
+// slot's U_FULL there); every consuming warp releases the slot on its own
+// CTA's U_EMPTY (a CTA-scope release, which does not wait for the warp's
+// earlier global stores to reach the cluster), and one thread of rank 1
+// forwards each completed phase of rank 1's U_EMPTY to rank 0's.  The
+// claimer takes unit uc only once every warp of both ranks has taken unit
+// uc - 2, so a pair holds at most three units and the rest stay free for
+// whichever pair finishes first.  The row-index warp, which runs
 // tiles ahead, prefetches each unit's query rows into L2.
 // Warps: 0-3 softmax (one row per thread; they also write Q into TMEM), 4 MMA
 // issue, 5 row indices, 6-9 K-row copies (cp.async), 10 unit claims (one
-// thread of rank 0), 11 idle.
+// thread of rank 0) and slot releases forwarded (one thread of rank 1), 11
+// idle.
 
 // NK_: K stages; XR_: rows a receive buffer holds (the rows that exchange).
 template <int NK_, int XR_>
@@ -116,17 +120,15 @@ enum {
   X_NEVER = 7,    // no thread ever arrives (the stall hook waits on it)
   X_XFULL = 8,    // + buffer: the other rank's partial landed (one arrival + its bytes)
   X_U_FULL = 10,  // + slot: a unit written into the slot (the claimer's arrival)
-  X_U_EMPTY = 14, // + slot, rank 0 only: every consuming warp of both ranks read it
+  X_U_EMPTY = 14, // + slot: every consuming warp of the CTA read it (rank 0: and rank 1's, forwarded)
   X_RING = 18
 };
 
 // The record of unit uc of this pair from the claim ring (copied there by
 // the claimer); n_tiles < 0 marks the end.  Every lane of the calling warp
-// takes it; lane 0 then releases the slot on rank 0's U_EMPTY (empty0: that
-// barrier array's cluster address).  ok is cleared (and the end returned) if
-// the wait gave up.
-__device__ __forceinline__ WorkUnit pair_take(uint64_t *bars, const WorkUnit *recs,
-                                              uint32_t empty0, uint32_t uc,
+// takes it; lane 0 then releases the slot on this CTA's U_EMPTY.  ok is
+// cleared (and the end returned) if the wait gave up.
+__device__ __forceinline__ WorkUnit pair_take(uint64_t *bars, const WorkUnit *recs, uint32_t uc,
                                               volatile int *abort_flag, uint64_t limit_ns,
                                               bool &ok) {
   const int slot = uc % MlaPairCfg::URING;
@@ -139,7 +141,7 @@ __device__ __forceinline__ WorkUnit pair_take(uint64_t *bars, const WorkUnit *re
   }
   w = recs[slot];
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(empty0 + (uint32_t)slot * 8u);
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&bars[X_U_EMPTY + slot]);
   return w;
 }
 
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     for (int b = 0; b < 2; ++b) mbar_init(&bars[X_XFULL + b], 1);
     for (int s = 0; s < C::URING; ++s) {
       mbar_init(&bars[X_U_FULL + s], 1);
-      mbar_init(&bars[X_U_EMPTY + s], 2 * C::UNIT_WARPS);
+      mbar_init(&bars[X_U_EMPTY + s], rank == 0 ? C::UNIT_WARPS + 1 : C::UNIT_WARPS);
     }
     for (int s = 0; s < C::NK; ++s) {
       mbar_init(&k_full[s], C::COPY_THREADS);
@@ -213,7 +215,6 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
   const uint32_t tmem = s_tmem;
   const int n_units = p.hdr->n_units;
   const int G = p.group;
-  const uint32_t empty0 = cluster_addr(smem_u32(&bars[X_U_EMPTY]), 0);
   if (warp < 4) regs_increase<C::REGS_SOFTMAX>();
   else regs_decrease<C::REGS_OTHER>();
 
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
       abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
     for (uint32_t uc = 0; !*abort_flag; ++uc) {
       bool took = true;
-      const WorkUnit w = pair_take(bars, s_rec, empty0, uc, abort_flag, p.wait_ns, took);
+      const WorkUnit w = pair_take(bars, s_rec, uc, abort_flag, p.wait_ns, took);
       if (!took) abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
       if (w.n_tiles < 0) break;
       const int nt = w.n_tiles;
@@ -611,7 +612,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
       return true;
     };
     for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-      const WorkUnit w = pair_take(bars, s_rec, empty0, uc, abort_flag, p.wait_ns, ok);
+      const WorkUnit w = pair_take(bars, s_rec, uc, abort_flag, p.wait_ns, ok);
       if (w.n_tiles < 0) break;
       const int nt = w.n_tiles;
       if (nt == 0) continue;
@@ -678,7 +679,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     uint32_t ic = 0;
     bool ok = true;
     for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-      const WorkUnit w = pair_take(bars, s_rec, empty0, uc, abort_flag, p.wait_ns, ok);
+      const WorkUnit w = pair_take(bars, s_rec, uc, abort_flag, p.wait_ns, ok);
       if (w.n_tiles < 0) break;
       const int nt = w.n_tiles;
       if (nt == 0) continue;
@@ -741,7 +742,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
     bool ok = true;
     if constexpr (FMT == 0) {
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-        const WorkUnit w = pair_take(bars, s_rec, empty0, uc, abort_flag, p.wait_ns, ok);
+        const WorkUnit w = pair_take(bars, s_rec, uc, abort_flag, p.wait_ns, ok);
         if (w.n_tiles < 0) break;
         const int nt = w.n_tiles;
         if (nt == 0) continue;
@@ -808,7 +809,7 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
         return true;
       };
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
-        const WorkUnit w = pair_take(bars, s_rec, empty0, uc, abort_flag, p.wait_ns, ok);
+        const WorkUnit w = pair_take(bars, s_rec, uc, abort_flag, p.wait_ns, ok);
         if (w.n_tiles < 0) break;
         const int nt = w.n_tiles;
         if (nt == 0) continue;
@@ -955,6 +956,22 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
         mbar_arrive(&bars[X_U_FULL + slot]);
         mbar_arrive_cluster(full_peer + (uint32_t)slot * 8u);
         if (u < 0) break;
+      }
+    } else if (rank == 1 && lane == 0) {
+      // Each completed phase of this CTA's U_EMPTY (every consuming warp
+      // read the slot) becomes one arrival on rank 0's, up to the end
+      // marker.  The record is intact until this arrival lets the claimer
+      // reuse the slot.
+      const uint32_t empty_peer = cluster_addr(smem_u32(&bars[X_U_EMPTY]), 0);
+      for (uint32_t uc = 0;; ++uc) {
+        const int slot = uc % C::URING;
+        if (!mbar_wait(&bars[X_U_EMPTY + slot], (uc / C::URING) & 1u, abort_flag, p.wait_ns)) {
+          abort_cta(abort_flag, p.status, PKX_ETIMEOUT);
+          break;
+        }
+        const bool end = s_rec[slot].n_tiles < 0;
+        mbar_arrive_cluster(empty_peer + (uint32_t)slot * 8u);
+        if (end) break;
       }
     }
   }

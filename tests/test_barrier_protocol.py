@@ -476,10 +476,11 @@ class _MlaPairModel:
     """The mbarrier protocol of mla_pair_kernel (csrc/mla_pair_kernel.cuh):
     two CTAs of a cluster take the same units in the same order.  A claiming
     thread of CTA 0 writes each unit into slot uc % 4 of both CTAs' unit
-    rings (U_FULL of each CTA); every role of both CTAs releases the slot on
-    CTA 0's U_EMPTY.  The claimer publishes unit uc once every role has taken
-    unit uc - 2, so a unit is never overwritten before all eight roles have
-    read it.  The softmax writes a unit's Q after the previous unit's
+    rings (U_FULL of each CTA); every role releases the slot on its own CTA's
+    U_EMPTY, and a forwarding thread of CTA 1 passes each completed phase of
+    CTA 1's U_EMPTY on to CTA 0's (one more arrival there).  The claimer
+    publishes unit uc once every role of both CTAs has taken unit uc - 2, so
+    a unit is never overwritten before all eight roles have read it.  The softmax writes a unit's Q after the previous unit's
     epilogue (or, in decode of at most 32 rows, the MMA warp writes it as it
     starts the unit: it has waited for the previous unit's last P, which the
     softmax writes only after the last QK^T landed); the model tracks which
@@ -524,10 +525,10 @@ class _MlaPairModel:
                 for s in range(n):
                     self.bars[f"{c}{pre}F{s}"] = _Bar(f"{c}{pre}F{s}", 1)
                     self.bars[f"{c}{pre}E{s}"] = _Bar(f"{c}{pre}E{s}", 1)
-            one_cta = mistake in ("rank 1 releases its own ring", "slot reused before both CTAs read it")
             for s in range(self.R):
                 self.bars[f"{c}UF{s}"] = _Bar(f"{c}UF{s}", 1)
-                self.bars[f"{c}UE{s}"] = _Bar(f"{c}UE{s}", 4 if one_cta else 8)
+                # CTA 0: its four roles and the forwarder; CTA 1: its four roles
+                self.bars[f"{c}UE{s}"] = _Bar(f"{c}UE{s}", 5 if c == 0 else 4)
 
     @staticmethod
     def _wait(bar, consumed):
@@ -538,7 +539,7 @@ class _MlaPairModel:
             yield from gen
             yield ("end",)
 
-        roles = {"0claim": ending(self._claim())}
+        roles = {"0claim": ending(self._claim()), "1forward": ending(self._forward())}
         for c in (0, 1):
             roles[f"{c}index"] = ending(self._index(c))
             roles[f"{c}copy"] = ending(self._copy(c))
@@ -616,15 +617,23 @@ class _MlaPairModel:
             if u is None:
                 return
 
+    def _forward(self):
+        """CTA 1's forwarder: each completed phase of CTA 1's U_EMPTY becomes
+        one arrival on CTA 0's, up to the end marker."""
+        for uc in range(len(self.units) + 1):
+            s = uc % self.R
+            if self.mistake != "forwarder arrives before CTA 1's roles read the slot":
+                yield self._wait(f"1UE{s}", uc // self.R)
+            yield ("arrive", f"0UE{s}")
+
     def _take(self, c, role, uc):
-        """Unit use uc from this CTA's ring: wait, read, release on CTA 0."""
+        """Unit use uc from this CTA's ring: wait, read, release locally."""
         s = uc % self.R
         yield self._wait(f"{c}UF{s}", uc // self.R)
         val = self.uring[(c, s)]
         assert val is not None and val[0] == uc, f"{c}{role}: unit slot {s} does not hold use {uc}"
         val[2].add(role)
-        own = self.mistake == "rank 1 releases its own ring"
-        yield ("arrive", f"{c if own else 0}UE{s}")
+        yield ("arrive", f"{c}UE{s}")
 
     def _index(self, c):
         ic = 0
@@ -825,8 +834,7 @@ def test_mla_fp8_protocol_has_no_deadlock_and_no_parity_aliasing():
                                      "partial read before it lands",
                                      "next phase armed before the wait",
                                      "one receive buffer",
-                                     "rank 1 releases its own ring",
-                                     "slot reused before both CTAs read it",
+                                     "forwarder arrives before CTA 1's roles read the slot",
                                      "next Q written before the last QK landed"])
 def test_mla_model_catches_planted_mistakes(mistake):
     with pytest.raises(AssertionError):
