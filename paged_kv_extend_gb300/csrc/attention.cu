@@ -79,8 +79,14 @@ struct SchedParams {
                    // streams into the two halves of their slot
   int n_dsplit;  // units per (block, split): value-dim slices (1, or 4 for MLA)
   int unit_target, qb_max, unit_max, comb_max, slot_max;
+  // Stream partition (parts > 0; one KV head): the blocks' key tiles laid
+  // end to end are cut into `parts` equal shares, a block is split where a
+  // share ends, each piece is claimed by its share's pair of CTAs, and
+  // part_first[k] is the first claim position of share k (k <= parts).
+  int parts;
+  int32_t *part_first;
   int32_t *seq;  // 8 arrays of batch+1 ints
-  int32_t *qbt;  // [5][qb_max]: tiles, sequence, unit / slot / combine offsets per block
+  int32_t *qbt;  // [6][qb_max]: tiles, sequence, unit / slot / combine offsets, tile offset per block
   int seq_in_smem, blk_in_smem;  // those arrays in dynamic shared memory instead
   WorkUnit *units;
   int32_t *uorder;  // units by cost, largest first
@@ -228,7 +234,7 @@ constexpr int kCostBuckets = 2048;
 // the workspace, which is slower but has no size limit).
 constexpr int kSchedSmemMax = 200 * 1024;
 // Per-sequence and per-block arrays of the scheduler.
-constexpr int kSchedSeqArrays = 5, kSchedBlockArrays = 5;
+constexpr int kSchedSeqArrays = 5, kSchedBlockArrays = 6;
 
 // Relative cost of a unit: its K/V tiles times its Q tiles, plus one for the
 // per-unit prologue and epilogue (clamped to the sort's bucket range).
@@ -255,7 +261,7 @@ __device__ __forceinline__ int unit_cost(const WorkUnit &w, int q_tile_tok) {
 __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   extern __shared__ int sdyn[];
   __shared__ int sh[32];
-  __shared__ int s_c;
+  __shared__ int s_c, s_share;
   const int tid = threadIdx.x;
   const int B = p.batch;
   const int S1 = B + 1;
@@ -267,6 +273,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
                            : p.qbt;
   int *bNt = blk, *bSeq = blk + p.qb_max, *bUo = blk + 2 * p.qb_max;
   int *bSo = blk + 3 * p.qb_max, *bCo = blk + 4 * p.qb_max;
+  int *bTo = blk + 5 * p.qb_max;  // stream partition: first tile of the block in the stream
 
   grid_dep_wait();    // inputs written by the previous kernel on the stream
   grid_dep_launch();  // the attention grid may start its prologue now
@@ -330,18 +337,29 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   }
   int tiles_all;
   block_scan_value(my_tiles, sh, tiles_all);
+  const bool stream = p.parts > 0;
+  if (stream) block_exclusive_scan(bNt, bTo, total_qb, sh);
   if (tid == 0) {
     const long long total_tiles = (long long)tiles_all * p.hkv * p.n_dsplit;
     const long long c = (total_tiles + p.unit_target - 1) / p.unit_target;
     s_c = (int)max((long long)kMinSplitTiles, c);
-    p.hdr->split_tiles = s_c;
+    s_share = stream ? max(1, (tiles_all + p.parts - 1) / p.parts) : 0;
+    p.hdr->split_tiles = stream ? s_share : s_c;
   }
   __syncthreads();
-  const int C = s_c;
+  const int C = s_c, share = s_share;
 
   // 3. per query block: units, slots, combine entries; their offsets
   const int nd = p.n_dsplit;
-  auto splits = [&](int nt) { return nt > 0 ? (nt + C - 1) / C : 1; };
+  // splits of block qb: chunks of C tiles, or (stream partition) one piece
+  // per share its tiles touch
+  auto splits = [&](int qb) {
+    const int nt = bNt[qb];
+    if (nt <= 0) return 1;
+    if (!stream) return (nt + C - 1) / C;
+    const int g0 = bTo[qb];
+    return (g0 + nt - 1) / share - g0 / share + 1;
+  };
   // two key streams: every decode unit has two partial slots and every
   // block a combine entry
   const bool dec2 = p.two_streams && p.mode == kDecode;
@@ -351,7 +369,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   const int qb_beg = min(total_qb, tid * chunk), qb_end = min(total_qb, qb_beg + chunk);
   int lu = 0, ls = 0, lc = 0;
   for (int qb = qb_beg; qb < qb_end; ++qb) {
-    const int nt = bNt[qb], S = splits(nt);
+    const int S = splits(qb);
     lu += S * nd;
     if (combined(S)) {
       ls += S * spu;
@@ -366,7 +384,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     bUo[qb] = u0;
     bSo[qb] = s0;
     bCo[qb] = c0;
-    const int S = splits(bNt[qb]);
+    const int S = splits(qb);
     u0 += S * nd;
     if (combined(S)) {
       s0 += S * spu;
@@ -394,7 +412,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   const int n_pairs = p.hkv * total_qb;
   for (int idx = tid; idx < n_pairs; idx += 1024) {
     const int kvh = idx / total_qb, qb = idx - kvh * total_qb;
-    const int S = splits(bNt[qb]);
+    const int S = splits(qb);
     if (!combined(S)) continue;
     const int b = bSeq[qb];
     const SeqDims d = dims(b);
@@ -430,10 +448,18 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     const int split_at = p.mode == kTwoStage ? d.P : INT_MAX;
     int lo, hi, i0, i1;
     qblock_range(p, d, qb - sOff[b], lo, hi, i0, i1);
-    const int nt = bNt[qb], S = splits(nt);
-    // split sp covers tiles [sp nt / S, (sp + 1) nt / S): sizes differ by
-    // one at most
-    const int t0 = (int)((long long)sp * nt / S), t1 = (int)((long long)(sp + 1) * nt / S);
+    const int nt = bNt[qb], S = splits(qb);
+    // split sp covers tiles [sp nt / S, (sp + 1) nt / S) (sizes differ by
+    // one at most), or (stream partition) the block's tiles inside share
+    // g0 / share + sp
+    int t0 = (int)((long long)sp * nt / S), t1 = (int)((long long)(sp + 1) * nt / S);
+    int part = 0;
+    if (stream) {
+      const int g0 = bTo[qb];
+      part = min(g0 / share + sp, p.parts - 1);
+      t0 = max(0, part * share - g0);
+      t1 = min(nt, (part + 1) * share - g0);
+    }
     WorkUnit w;
     w.q_tok0 = d.qbase + i0;
     w.n_tok = i1 - i0;
@@ -446,7 +472,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     w.b = b;
     w.slot = combined(S) ? kvh * ts + bSo[qb] + sp * spu : -1;
     w.dq = dq;
-    w.claim = 0;
+    w.claim = stream ? part : 0;
     return w;
   };
 
@@ -466,7 +492,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
       if (act) {
         if (pass == 0) {
           w = unit_at(u);
-          key = claim_key(w);
+          key = stream ? w.claim : claim_key(w);  // stream partition: the share, in order
           w.claim = key;
         } else {
           key = p.units[u].claim;  // written in pass 0 (the block barrier between passes orders it)
@@ -483,7 +509,12 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
       }
     }
     __syncthreads();
-    if (pass == 0) block_exclusive_scan(hist, hist, kCostBuckets, sh);
+    if (pass == 0) {
+      block_exclusive_scan(hist, hist, kCostBuckets, sh);
+      // each share's first claim position (keys are shares, all below parts)
+      if (stream)
+        for (int k = tid; k <= p.parts; k += 1024) p.part_first[k] = hist[k];
+    }
   }
   if (tid == 0) {
     p.hdr->n_units = n_units;
@@ -520,6 +551,7 @@ struct KParams {
   const int32_t *uorder;  // units by cost, largest first
   const WsHeader *hdr;
   int32_t *next_unit;     // claim counter over uorder (zeroed by the scheduler)
+  const int32_t *part_first;  // MLA pairs: each pair's claim positions (stream partition), or null
   int32_t *status;
   float *plse, *po;
   // two-stage form with the fused KV write: the pool slot of each extend
@@ -2000,7 +2032,9 @@ WsLayout ws_layout(int batch, int num_q_tokens, int hkv, int group, int lq, int 
   L.seq_off = off;
   off = align256(off + sizeof(int32_t) * 8 * (size_t)(batch + 1));
   L.qb_off = off;
-  off = align256(off + sizeof(int32_t) * 5 * (size_t)L.qb_max);
+  off = align256(off + sizeof(int32_t) * kSchedBlockArrays * (size_t)L.qb_max);
+  L.part_off = off;
+  off = align256(off + sizeof(int32_t) * (size_t)(kMaxStreamParts + 1));
   L.units_off = off;
   off = align256(off + sizeof(WorkUnit) * (size_t)L.unit_max);
   L.uorder_off = off;
@@ -2225,6 +2259,12 @@ int launch_attention(const AttnArgs &a) {
   sp.window = a.window;
   sp.num_q_tokens = nq;
   sp.unit_target = mla ? 4 * pairs : L.unit_target;
+  // MLA decode with one KV head: a stream partition, one share of the key
+  // tiles per CTA pair (equal shares, where run-time claims of equal units
+  // leave some pairs one unit more than others)
+  const bool stream = mla && decode && a.hkv == 1 && pairs <= kMaxStreamParts;
+  sp.parts = stream ? pairs : 0;
+  sp.part_first = reinterpret_cast<int32_t *>(ws + L.part_off);
   sp.qb_max = L.qb_max;
   sp.unit_max = L.unit_max;
   sp.comb_max = L.comb_max;
@@ -2303,6 +2343,7 @@ int launch_attention(const AttnArgs &a) {
   kp.units = sp.units;
   kp.uorder = sp.uorder;
   kp.next_unit = &hdr->next_unit;
+  kp.part_first = stream ? sp.part_first : nullptr;
   kp.hdr = hdr;
   kp.status = &hdr->status;
   kp.plse = reinterpret_cast<float *>(ws + L.plse_off);

@@ -55,8 +55,10 @@
 // forwards each completed phase of rank 1's U_EMPTY to rank 0's.  The
 // claimer takes unit uc only once every warp of both ranks has taken unit
 // uc - 2, so a pair holds at most three units and the rest stay free for
-// whichever pair finishes first.  The row-index warp, which runs
-// tiles ahead, prefetches each unit's query rows into L2.
+// whichever pair finishes first.  Under a stream partition (MLA decode with
+// one KV head) the pair walks its own share of the claim order instead.
+// The row-index warp, which runs tiles ahead, prefetches each unit's query
+// rows into L2.
 // Warps: 0-3 softmax (one row per thread; they also write Q into TMEM), 4 MMA
 // issue, 5 row indices, 6-9 K-row copies (cp.async), 10 unit claims (one
 // thread of rank 0) and slot releases forwarded (one thread of rank 1), 11
@@ -935,8 +937,14 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
         }
         int u = -1;
         if (!*abort_flag) {
-          const int pos = atomicAdd(p.next_unit, 1);
-          if (pos < n_units) u = p.uorder[pos];
+          if (p.part_first) {  // stream partition: this pair's share, in order
+            const int pair = (int)(blockIdx.x >> 1);
+            const int pos = p.part_first[pair] + (int)uc;
+            if (pos < p.part_first[pair + 1]) u = p.uorder[pos];
+          } else {
+            const int pos = atomicAdd(p.next_unit, 1);
+            if (pos < n_units) u = p.uorder[pos];
+          }
         }
         // the record (or the end marker), here and in rank 1
         WorkUnit rec;

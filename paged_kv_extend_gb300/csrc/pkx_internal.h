@@ -37,6 +37,8 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 // Smallest number of KV tiles a split-KV chunk holds.
 constexpr int kMinSplitTiles = 4;
+// Upper bound on the shares of a stream partition (CTA pairs of one launch).
+constexpr int kMaxStreamParts = 256;
 
 // One unit of attention work: a block of query tokens of one sequence and one
 // KV head (up to two Q tiles; in a tile, row = token * group + head-in-group),
@@ -80,7 +82,8 @@ struct WsHeader {
 // Byte offsets of the workspace regions for one problem.
 struct WsLayout {
   size_t seq_off;      // int32 [8][batch + 1] per-sequence scratch (five used)
-  size_t qb_off;       // int32 [5][qb_max] per-query-block scheduler arrays
+  size_t qb_off;       // int32 [6][qb_max] per-query-block scheduler arrays
+  size_t part_off;     // int32 [kMaxStreamParts + 1] first claim position of each share
   size_t units_off;    // WorkUnit [unit_max]
   size_t uorder_off;   // int32 [unit_max] units by cost, largest first
   size_t comb_off;     // CombineEntry [comb_max]

@@ -565,6 +565,50 @@ def test_mla_decode_small_vs_oracle():
     assert_close(o, lse, ro, rl, "mla decode")
 
 
+@pytest.mark.parametrize("hq,lens", [
+    # many short sequences around a long one: shares of the key tiles cut
+    # through several sequences and split the long one (G = 16)
+    (16, [1, 2, 3, 64, 65, 129, 4000, 1, 700, 5] * 3),
+    (8, [3000, 1, 1, 1, 300, 64, 2]),        # G = 8
+    (32, [5000, 1, 1, 1, 300]),              # G = 32: the largest small-group layout
+    (64, [70, 2000, 1, 129]),                # G = 64: the four-stage layout
+    (16, [150000]),                          # one sequence over every pair
+])
+def test_mla_decode_stream_partition_vs_oracle(hq, lens):
+    """MLA decode with one KV head splits the key tiles of all sequences laid
+    end to end into one equal share per CTA pair."""
+    spec = W.WorkloadSpec("dec", batch=len(lens), hq=hq, hkv=1, lq=576, lv=512,
+                          prefix=[x - 1 for x in lens], extend=[1] * len(lens),
+                          num_slots=sum(lens) + 4096, sm_scale=1.0 / math.sqrt(192.0), std=0.5,
+                          seed=sum(lens) % 1000 + hq, v_aliases_k=True, decode=True)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    o, lse, ws = dw.decode()
+    torch.cuda.synchronize()
+    assert pkx.workspace_status(ws) == 0
+    ro, rl = oracle_decode(wl)
+    assert_close(o, lse, ro, rl, "mla decode, stream partition")
+
+
+def test_mla_decode_padding_sequence_gives_zero():
+    """A padded MLA decode slot (T = 0) yields o = 0 and lse = -inf; its
+    neighbours' shares are unaffected."""
+    spec = W.WorkloadSpec("dec", batch=3, hq=16, hkv=1, lq=576, lv=512, prefix=[900, 0, 33],
+                          extend=[1, 1, 1], num_slots=2048, sm_scale=1.0 / math.sqrt(192.0),
+                          std=0.5, seed=4, v_aliases_k=True, decode=True)
+    wl = W.draw(spec)
+    dw = DeviceWorkload(wl)
+    kvp = torch.tensor([0, 901, 901, 935], dtype=torch.int32)
+    idx = torch.cat([wl.kv_indices[:901], wl.kv_indices[902:936]])
+    dw.kv_indptr, dw.kv_indices = kvp.to(DEV), idx.to(DEV)
+    o, lse, _ = dw.decode()
+    torch.cuda.synchronize()
+    kb, vb = wl.pool()
+    ro, rl = oracle.decode_attention(wl.q, kb, vb, kvp, idx, wl.sm_scale)
+    assert torch.all(o[1].cpu() == 0) and torch.all(torch.isneginf(lse[1].cpu()))
+    assert_close(o, lse, ro, rl, "mla decode padding")
+
+
 def test_mla_requires_v_alias():
     """Lq=576/Lv=512 with a V pool that is not a view of K is refused."""
     spec = W.small_spec(batch=1, hq=16, hkv=1, lq=576, lv=512, prefix=[4], extend=[4],
