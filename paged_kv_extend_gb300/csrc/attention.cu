@@ -1928,10 +1928,11 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
 //   lse = log sum_i exp(lse_i),  o = sum_i exp(lse_i - lse) o_i
 // (the merge_state formula applied n ways).
 __global__ void __launch_bounds__(256) combine_kernel(const WsHeader *hdr, const CombineEntry *ce,
-                                                      const float *plse, const float *po,
-                                                      bf16 *o, float *lse, const float *sinks,
-                                                      int hq, int group, int hdv,
-                                                      int rows_per_slot) {
+                                                      const float *__restrict__ plse,
+                                                      const float *__restrict__ po,
+                                                      bf16 *__restrict__ o, float *__restrict__ lse,
+                                                      const float *sinks, int hq, int group,
+                                                      int hdv, int rows_per_slot) {
   grid_dep_wait();  // the attention kernel's partials
   const int n_comb = hdr->n_combine;
   const int lane = threadIdx.x & 31;
@@ -1965,18 +1966,29 @@ __global__ void __launch_bounds__(256) combine_kernel(const WsHeader *hdr, const
     float wsum = sinks ? exp2f((sink - mx) * 1.4426950408889634f) : 0.f;
     for (int i = 0; i < n_part; ++i) wsum += exp2f((plse[prow(i)] - mx) * 1.4426950408889634f);
     const float inv = 1.0f / wsum;
-    // every lane takes 4 consecutive value dims (a 128-dim row is one pass
-    // of the warp)
-    for (int c = lane * 4; c < hdv; c += 128) {
-      float acc[4] = {0, 0, 0, 0};
-      for (int i = 0; i < n_part; ++i) {
-        const int64_t sr = prow(i);
-        const float wi = exp2f((plse[sr] - mx) * 1.4426950408889634f) * inv;
-        const float4 a = *reinterpret_cast<const float4 *>(po + sr * hdv + c);
-        acc[0] += wi * a.x; acc[1] += wi * a.y; acc[2] += wi * a.z; acc[3] += wi * a.w;
+    // every lane takes 4 consecutive value dims of each 128-dim pass (at
+    // most four passes: Lv <= 512); a partial's loads for all passes go out
+    // together, and the row is stored once every partial is added
+    constexpr int kPasses = 4;
+    float acc[kPasses][4] = {};
+    for (int i = 0; i < n_part; ++i) {
+      const int64_t sr = prow(i);
+      const float wi = exp2f((plse[sr] - mx) * 1.4426950408889634f) * inv;
+      const float *src = po + sr * hdv + lane * 4;
+#pragma unroll
+      for (int k = 0; k < kPasses; ++k) {
+        if (k * 128 + lane * 4 < hdv) {
+          const float4 a = *reinterpret_cast<const float4 *>(src + k * 128);
+          acc[k][0] += wi * a.x; acc[k][1] += wi * a.y; acc[k][2] += wi * a.z; acc[k][3] += wi * a.w;
+        }
       }
-      *reinterpret_cast<uint2 *>(o + orow * hdv + c) =
-          make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+    }
+#pragma unroll
+    for (int k = 0; k < kPasses; ++k) {
+      const int c = k * 128 + lane * 4;
+      if (c < hdv)
+        *reinterpret_cast<uint2 *>(o + orow * hdv + c) =
+            make_uint2(pack_bf16(acc[k][0], acc[k][1]), pack_bf16(acc[k][2], acc[k][3]));
     }
     if (lane == 0 && lse) lse[orow] = mx + logf(wsum);
   }
