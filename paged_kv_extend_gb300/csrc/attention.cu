@@ -2140,7 +2140,8 @@ static int launch_attn_fp8(int mode, bool masked, const TMaps &tmaps, const KPar
 template <int MODE, bool MASK, int FMT = 0, bool SG = false>
 static cudaError_t launch_pair(int pairs, cudaStream_t s, const KParams &kp, bool query_only,
                                int *max_pairs) {
-  using C = std::conditional_t<SG, MlaPairDecCfg, MlaPairCfg>;
+  using C = std::conditional_t<SG, std::conditional_t<FMT != 0, MlaPairDec8Cfg, MlaPairDecCfg>,
+                               MlaPairCfg>;
   static bool configured[kMaxDevicesCfg] = {};
   if (needs_config(configured)) {
     cudaError_t e = cudaFuncSetAttribute(mla_pair_kernel<MODE, MASK, FMT, SG>,

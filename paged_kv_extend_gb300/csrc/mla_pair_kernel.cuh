@@ -64,8 +64,10 @@
 // thread of rank 0) and slot releases forwarded (one thread of rank 1), 11
 // idle.
 
-// NK_: K stages; XR_: rows a receive buffer holds (the rows that exchange).
-template <int NK_, int XR_>
+// NK_: K stages; XR_: rows a receive buffer holds (the rows that exchange);
+// NRAW_: raw fp8 code slots per copy thread's ring (0: codes converted in
+// place in the stages).
+template <int NK_, int XR_, int NRAW_ = 0>
 struct MlaPairCfgT {
   static constexpr int BM = kBlockM, BN = 64;
   static constexpr int LQ = 576, LV = 512;
@@ -77,8 +79,13 @@ struct MlaPairCfgT {
   static constexpr int K_BYTES = BN * 5 * 128;  // four value atoms + the rope atom
   static constexpr int X_BYTES = XR * BN * 4;   // a partial S
   static constexpr int I_BYTES = BN * 4;
+  static constexpr int NRAW = NRAW_;
+  // a raw slot: the codes of a tile, four 64-byte value atoms per key
+  // (atom-major, key rows of 64 bytes) and then the 32-byte rope rows
+  static constexpr int RAW_BYTES = BN * (DV + DR);
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_X = NK * K_BYTES;     // received from the other rank
+  static constexpr int OFF_RAW = NK * K_BYTES;
+  static constexpr int OFF_X = OFF_RAW + NRAW * RAW_BYTES;  // received from the other rank
   static constexpr int OFF_I = OFF_X + 2 * X_BYTES;
   static constexpr int OFF_BAR = OFF_I + NI * I_BYTES;
   static constexpr int URING = 4;               // unit ring slots
@@ -110,6 +117,11 @@ using MlaPairCfg = MlaPairCfgT<4, kBlockM>;
 // two tiles ahead of PV and holds three stages, so the fifth doubles the
 // stages being copied.
 using MlaPairDecCfg = MlaPairCfgT<5, 32>;
+// The same over an fp8 pool: a copy thread stages its codes of a tile in
+// one of four private raw slots and converts them into one of three stages
+// three tiles later, so a stage is taken only from conversion to PV and the
+// copies' latency is covered by the raw ring.
+using MlaPairDec8Cfg = MlaPairCfgT<3, 32, 4>;
 
 enum {
   X_Q_FULL = 0,
@@ -157,7 +169,8 @@ __device__ __forceinline__ WorkUnit pair_take(uint64_t *bars, const WorkUnit *re
 template <int MODE, bool MASK, int FMT = 0, bool SG = false>
 __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const KParams p) {
   static_assert(!SG || (MODE == kDecode && !MASK), "the small-group layout is for decode");
-  using C = std::conditional_t<SG, MlaPairDecCfg, MlaPairCfg>;
+  using C = std::conditional_t<SG, std::conditional_t<FMT != 0, MlaPairDec8Cfg, MlaPairDecCfg>,
+                               MlaPairCfg>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -790,6 +803,87 @@ __global__ void __launch_bounds__(MlaPairCfg::THREADS, 1) mla_pair_kernel(const 
           cp_async_arrive_noinc(&k_full[ks]);
           ++kc;
         }
+      }
+    } else if constexpr (C::NRAW > 0) {
+      // fp8 pool, decode of at most 32 rows: tile t's codes go to this
+      // thread's raw slot t % NRAW (8 bytes per key, atom and chunk, at
+      // offsets fixed per thread), and tile t is converted into its stage
+      // once tile t + NRAW - 1 is issued: the stage is taken (k_empty) only
+      // then.  A unit's last tiles are converted before the next unit is
+      // taken: its claim may wait for this unit's products, which wait for
+      // these tiles.  One cp.async group per issued tile.
+      static_assert(MODE == kDecode, "the raw ring serves decode (no extend rows)");
+      const uint32_t rthr = (uint32_t)key0 * 64u + (uint32_t)ch * 8u;        // value atoms
+      const uint32_t rthr_r = (uint32_t)key0 * 32u + (uint32_t)ch * 8u;      // rope rows
+      constexpr uint32_t RAW_ROPE = 4u * C::BN * 64u;
+      uint32_t issued = 0, conv = 0;
+      int rows[4];
+      auto convert = [&](bool drain) -> bool {
+        const int ks = conv % C::NK;
+        if (conv >= (uint32_t)C::NK &&
+            !mbar_wait(&k_empty[ks], ((conv / C::NK) - 1) & 1u, abort_flag, p.wait_ns))
+          return false;
+        // tile conv's group: NRAW - 1 groups were issued after it, or fewer
+        // while draining
+        if (drain) cp_async_wait_group<0>();
+        else cp_async_wait_group<C::NRAW - 1>();
+        const uint32_t sR = sbase + C::OFF_RAW + (conv % C::NRAW) * C::RAW_BYTES;
+        const uint32_t sK = sbase + C::OFF_K + ks * C::K_BYTES + dthr;
+        static_for<0, 4>([&](auto i_c) {
+          constexpr int i = decltype(i_c)::value;
+          static_for<0, 4>([&](auto a_c) {
+            constexpr int a = decltype(a_c)::value;
+            st_shared_u4(sK + a * C::BN * 128 + i * 16 * 128,
+                         fp8x8_to_bf16x8<FMT>(ld_shared_u2(sR + rthr + a * (C::BN * 64) + i * (16 * 64))));
+          });
+          if (ch < C::DR / 8)
+            st_shared_u4(sK + 4 * C::BN * 128 + i * 16 * 128,
+                         fp8x8_to_bf16x8<FMT>(ld_shared_u2(sR + RAW_ROPE + rthr_r + i * (16 * 32))));
+        });
+        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+        mbar_arrive(&k_full[ks]);
+        ++conv;
+        return true;
+      };
+      for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
+        const WorkUnit w = pair_take(bars, s_rec, uc, abort_flag, p.wait_ns, ok);
+        if (w.n_tiles < 0) break;
+        const int nt = w.n_tiles;
+        if (nt == 0) continue;
+        const uint8_t *kp8 =
+            reinterpret_cast<const uint8_t *>(p.k_pool) + (int64_t)w.kvh * p.kb_sh + dv0 + ch * 8;
+        for (int j = 0; j < nt && ok; ++j) {
+          const int is = ic % C::NI;
+          if (!mbar_wait(&i_full[is], (ic / C::NI) & 1u, abort_flag, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          const int *ring = reinterpret_cast<const int *>(smem + C::OFF_I + is * C::I_BYTES);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rows[i] = ring[key0 + 16 * i];
+          mbar_arrive(&i_empty[is]);
+          ++ic;
+          // this thread converted tile issued - NRAW (the slot's last tile)
+          // before it got here, in program order
+          const uint32_t sR = sbase + C::OFF_RAW + (issued % C::NRAW) * C::RAW_BYTES;
+          static_for<0, 4>([&](auto i_c) {
+            constexpr int i = decltype(i_c)::value;
+            const int row = rows[i];
+            const uint8_t *src = kp8 + (int64_t)max(row, 0) * p.kb_ss;
+            const uint32_t bytes = row >= 0 ? 8u : 0u;
+            static_for<0, 4>([&](auto a_c) {
+              constexpr int a = decltype(a_c)::value;
+              cp_async_8_at<a * C::BN * 64 + i * 16 * 64>(sR + rthr, src + a * 64, bytes);
+            });
+            if (ch < C::DR / 8)
+              cp_async_8_at<RAW_ROPE + i * 16 * 32>(sR + rthr_r, src + (dr0 - dv0), bytes);
+          });
+          cp_async_commit();
+          ++issued;
+          if (issued - conv > (uint32_t)(C::NRAW - 1) && !convert(false)) ok = false;
+        }
+        while (ok && conv < issued)
+          if (!convert(true)) ok = false;
       }
     } else {
       // fp8 pool.  A pool tile's codes are copied 8 bytes per (thread, key,

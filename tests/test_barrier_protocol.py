@@ -501,8 +501,15 @@ class _MlaPairModel:
     NK, NI, R, AHEAD = 4, 4, 4, 2
     ROLES = {"index", "copy", "softmax", "mma"}
 
-    def __init__(self, units, seed, mistake=None, fp8=False, lead=1, mma_q=False):
+    def __init__(self, units, seed, mistake=None, fp8=False, lead=1, mma_q=False, raw=False):
         self.mma_q = mma_q  # the MMA warp writes Q (decode of at most 32 rows)
+        # decode over an fp8 pool, at most 32 rows: each copy thread stages
+        # its codes in a ring of NRAW private raw slots and converts a tile
+        # into one of three stages NRAW - 1 tiles later, across units
+        self.raw = raw
+        if raw:
+            self.NK, self.NRAW = 3, 4
+            self.rawslot = {(c, r): None for c in (0, 1) for r in range(self.NRAW)}
         self.rng = random.Random(seed)
         self.units, self.mistake = units, mistake
         self.lead = lead  # CTA 0's roles are picked this many times as often
@@ -588,6 +595,16 @@ class _MlaPairModel:
             elif op[0] == "qk":  # a QK^T of unit op[2] reads CTA op[1]'s Q
                 assert self.q_unit[op[1]] == op[2], f"{k}: QK^T of unit {op[2]} reads another unit's Q"
                 self.q_readers[op[1]] += 1
+            elif op[0] == "raw_put":  # codes of tile op[2] into raw slot op[2] % NRAW of CTA op[1]
+                key = (op[1], op[2] % self.NRAW)
+                prev = self.rawslot[key]
+                assert prev is None or prev == ("converted", op[2] - self.NRAW), \
+                    f"{k}: raw slot overwritten before its conversion"
+                self.rawslot[key] = ("issued", op[2])
+            elif op[0] == "raw_take":  # tile op[2] converted out of its raw slot
+                key = (op[1], op[2] % self.NRAW)
+                assert self.rawslot[key] == ("issued", op[2]), f"{k}: raw slot does not hold the tile"
+                self.rawslot[key] = ("converted", op[2])
             elif op[0] == "publish":  # the claimer writes unit use op[2] into slot op[1] of both CTAs
                 for c in (0, 1):
                     prev = self.uring[(c, op[1])]
@@ -661,6 +678,39 @@ class _MlaPairModel:
                 yield self._wait(f"{c}KE{ks}", kc // self.NK - 1)
             kc += 1
 
+        if self.raw:
+            issued = conv = 0
+
+            def convert():
+                nonlocal conv
+                ks = conv % self.NK
+                if conv >= self.NK and self.mistake != "stage converted into before its release":
+                    yield self._wait(f"{c}KE{ks}", conv // self.NK - 1)
+                yield ("raw_take", c, conv)
+                yield ("arrive", f"{c}KF{ks}")
+                conv += 1
+
+            lag = self.NRAW if self.mistake == "raw slot reused before its conversion" else self.NRAW - 1
+            for uc, u in enumerate(self.units):
+                yield from self._take(c, "copy", uc)
+                for _ in range(u["nt"]):
+                    si = ic % self.NI
+                    yield self._wait(f"{c}IF{si}", ic // self.NI)
+                    yield ("arrive", f"{c}IE{si}")
+                    ic += 1
+                    yield ("raw_put", c, issued)
+                    issued += 1
+                    if issued - conv > lag:
+                        yield from convert()
+                # the unit's last tiles before the next unit: its claim may
+                # wait for this unit's products, which wait for these tiles
+                if self.mistake != "conversions carried across units":
+                    while conv < issued:
+                        yield from convert()
+            while conv < issued:
+                yield from convert()
+            yield from self._take(c, "copy", len(self.units))
+            return
         for uc, u in enumerate(self.units):
             yield from self._take(c, "copy", uc)
             nt = u["nt"]
@@ -796,7 +846,7 @@ class _MlaPairModel:
         yield from self._take(c, "mma", len(self.units))
 
 
-def _mla_trials(n, mistake=None, mma_q=False):
+def _mla_trials(n, mistake=None, mma_q=False, raw=False):
     rng = random.Random(2)
     for t in range(n):
         # every third trial has runs of empty units, which the softmax of one
@@ -804,7 +854,8 @@ def _mla_trials(n, mistake=None, mma_q=False):
         sizes = [0, 0, 0, 1, 2, 5] if t % 3 == 2 else [0, 1, 1, 2, 3, 5, 8]
         units = [{"nt": rng.choice(sizes)} for _ in range(rng.randint(1, 12))]
         # and in every other one CTA 0 runs ahead
-        _MlaPairModel(units, seed=t, mistake=mistake, lead=8 if t % 2 else 1, mma_q=mma_q).run()
+        _MlaPairModel(units, seed=t, mistake=mistake, lead=8 if t % 2 else 1, mma_q=mma_q,
+                      raw=raw).run()
 
 
 def test_mla_protocol_has_no_deadlock_and_no_parity_aliasing():
@@ -814,6 +865,22 @@ def test_mla_protocol_has_no_deadlock_and_no_parity_aliasing():
 def test_mla_small_group_decode_protocol():
     """Decode of at most 32 rows: the MMA warp writes each unit's Q itself."""
     _mla_trials(150, mma_q=True)
+
+
+def test_mla_small_group_fp8_decode_protocol():
+    """... and over an fp8 pool: codes staged in private raw slots, converted
+    into one of three stages three tiles later; a unit's last tiles are
+    converted before the next unit is taken (carried across units, they
+    deadlock: the next claim waits for this unit's products)."""
+    _mla_trials(150, mma_q=True, raw=True)
+
+
+@pytest.mark.parametrize("mistake", ["raw slot reused before its conversion",
+                                     "stage converted into before its release",
+                                     "conversions carried across units"])
+def test_mla_raw_ring_model_catches_planted_mistakes(mistake):
+    with pytest.raises(AssertionError):
+        _mla_trials(150, mistake, mma_q=True, raw=True)
 
 
 def test_mla_model_catches_q_written_under_products():
