@@ -1652,6 +1652,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
         const uint32_t bytes = r >= 0 ? 16u : 0u;
         const bf16 *src = base + (int64_t)max(r, 0) * stride;
         if constexpr (!C::SPLIT) {
+          static_assert(L == C::LQ || L == C::HDV, "row length");
           cp_async_16_at<i * KPP * 128, 0>(stage + dthr, src, bytes);
         } else {
           static_for<0, (L + 63) / 64>([&](auto a_c) {
@@ -1664,7 +1665,8 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     };
     constexpr std::integral_constant<int, C::LQ> K_LEN{};
     constexpr std::integral_constant<int, C::HDV> V_LEN{};
-    uint32_t kc = 0, vc = 0, ic = 0, qc = 0;
+    uint32_t kc = 0, vc = 0, ic = 0;
+    [[maybe_unused]] uint32_t qc = 0;
     bool ok = true;
     if constexpr (FMT == 0) {
       for (uint32_t uc = 0; ok && !*abort_flag; ++uc) {
