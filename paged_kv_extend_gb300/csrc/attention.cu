@@ -79,9 +79,10 @@ struct SchedParams {
                    // streams into the two halves of their slot
   int n_dsplit;  // units per (block, split): value-dim slices (1, or 4 for MLA)
   int unit_target, qb_max, unit_max, comb_max, slot_max;
-  // Stream partition (parts > 0; one KV head): the blocks' key tiles laid
-  // end to end are cut into `parts` equal shares, a block is split where a
-  // share ends, each piece is claimed by its share's pair of CTAs, and
+  // Stream partition (parts > 0, a multiple of hkv): per KV head, the
+  // blocks' key tiles laid end to end are cut into parts / hkv equal shares
+  // (the same cuts for every head), a block is split where a share ends,
+  // each piece is claimed by its share's CTA (or CTA pair), and
   // part_first[k] is the first claim position of share k (k <= parts).
   int parts;
   int32_t *part_first;
@@ -343,7 +344,8 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     const long long total_tiles = (long long)tiles_all * p.hkv * p.n_dsplit;
     const long long c = (total_tiles + p.unit_target - 1) / p.unit_target;
     s_c = (int)max((long long)kMinSplitTiles, c);
-    s_share = stream ? max(1, (tiles_all + p.parts - 1) / p.parts) : 0;
+    const int ppk = stream ? p.parts / p.hkv : 1;  // shares per KV head
+    s_share = stream ? max(1, (tiles_all + ppk - 1) / ppk) : 0;
     p.hdr->split_tiles = stream ? s_share : s_c;
   }
   __syncthreads();
@@ -455,10 +457,11 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     int t0 = (int)((long long)sp * nt / S), t1 = (int)((long long)(sp + 1) * nt / S);
     int part = 0;
     if (stream) {
-      const int g0 = bTo[qb];
-      part = min(g0 / share + sp, p.parts - 1);
-      t0 = max(0, part * share - g0);
-      t1 = min(nt, (part + 1) * share - g0);
+      const int g0 = bTo[qb], ppk = p.parts / p.hkv;
+      const int k = min(g0 / share + sp, ppk - 1);  // the share within the head
+      t0 = max(0, k * share - g0);
+      t1 = min(nt, (k + 1) * share - g0);
+      part = kvh * ppk + k;
     }
     WorkUnit w;
     w.q_tok0 = d.qbase + i0;
@@ -1365,8 +1368,13 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
       // claim the next unit and hand it to the other warps
       int u = -1;
       if (lane == 0) {
-        const int pos = atomicAdd(p.next_unit, 1);
-        u = pos < n_units ? pos : -1;
+        if (p.part_first) {  // stream partition: this CTA's share, in order
+          const int pos = p.part_first[blockIdx.x] + (int)uc;
+          u = pos < p.part_first[blockIdx.x + 1] ? pos : -1;
+        } else {
+          const int pos = atomicAdd(p.next_unit, 1);
+          u = pos < n_units ? pos : -1;
+        }
       }
       u = __shfl_sync(0xffffffffu, u, 0);
       {
@@ -2277,8 +2285,14 @@ int launch_attention(const AttnArgs &a) {
   // MLA decode with one KV head: a stream partition, one share of the key
   // tiles per CTA pair (equal shares, where run-time claims of equal units
   // leave some pairs one unit more than others)
-  const bool stream = mla && decode && a.hkv == 1 && pairs <= kMaxStreamParts;
-  sp.parts = stream ? pairs : 0;
+  // GQA decode over a bf16 pool: one share per CTA, nsm / hkv per KV head
+  // (over an fp8 pool the conversion-bound pipeline does better with the
+  // run-time claims of smaller units: 0.48 against 0.54 ms on decode_gqa)
+  const bool stream =
+      decode && (mla ? a.hkv == 1 && pairs <= kMaxStreamParts
+                     : !split && a.kv_fmt == kKvBf16 && nsm <= kMaxStreamParts &&
+                           nsm % a.hkv == 0);
+  sp.parts = stream ? (mla ? pairs : nsm) : 0;
   sp.part_first = reinterpret_cast<int32_t *>(ws + L.part_off);
   sp.qb_max = L.qb_max;
   sp.unit_max = L.unit_max;
