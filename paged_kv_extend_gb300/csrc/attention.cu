@@ -80,8 +80,9 @@ struct SchedParams {
   int n_dsplit;  // units per (block, split): value-dim slices (1, or 4 for MLA)
   int unit_target, qb_max, unit_max, comb_max, slot_max;
   // Stream partition (parts > 0, a multiple of hkv): per KV head, the
-  // blocks' key tiles laid end to end are cut into parts / hkv equal shares
-  // (the same cuts for every head), a block is split where a share ends,
+  // blocks' key tiles laid end to end, each weighted by its block's Q tiles,
+  // are cut into parts / hkv equal shares of that cost (the same cuts for
+  // every head), a block is split at the first tile boundary of each share,
   // each piece is claimed by its share's CTA (or CTA pair), and
   // part_first[k] is the first claim position of share k (k <= parts).
   int parts;
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
   __syncthreads();
   const int total_qb = block_exclusive_scan(sOff, sOff, B, sh);
   if (tid == 0) sOff[B] = total_qb;
-  if (total_qb > p.qb_max) {  // cannot happen for consistent indptrs
+  if (total_qb >= p.qb_max) {  // cannot happen for consistent indptrs (one entry spare)
     if (tid == 0) {
       record_status(&p.hdr->status, PKX_EDEVICE);
       p.hdr->n_units = 0;
@@ -335,17 +336,26 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     bNt[qb] = nt;
     bSeq[qb] = b;
     my_tiles = min(my_tiles + nt, 0x1fffff);
+    // stream partition: the block's cost, its tiles times its Q tiles
+    if (p.parts > 0) bTo[qb] = nt * max(1, (i1 - i0 + p.q_tile_tok - 1) / p.q_tile_tok);
   }
   int tiles_all;
   block_scan_value(my_tiles, sh, tiles_all);
   const bool stream = p.parts > 0;
-  if (stream) block_exclusive_scan(bNt, bTo, total_qb, sh);
+  int cost_all = 0;
+  if (stream) {
+    __syncthreads();
+    cost_all = block_exclusive_scan(bTo, bTo, total_qb, sh);  // first cost of each block
+    if (tid == 0) bTo[total_qb] = cost_all;
+  }
   if (tid == 0) {
     const long long total_tiles = (long long)tiles_all * p.hkv * p.n_dsplit;
     const long long c = (total_tiles + p.unit_target - 1) / p.unit_target;
     s_c = (int)max((long long)kMinSplitTiles, c);
     const int ppk = stream ? p.parts / p.hkv : 1;  // shares per KV head
-    s_share = stream ? max(1, (tiles_all + ppk - 1) / ppk) : 0;
+    // at least two, the largest tile cost, so that every share holds a tile
+    // boundary and no piece is empty
+    s_share = stream ? max(2, (cost_all + ppk - 1) / ppk) : 0;
     p.hdr->split_tiles = stream ? s_share : s_c;
   }
   __syncthreads();
@@ -359,8 +369,9 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     const int nt = bNt[qb];
     if (nt <= 0) return 1;
     if (!stream) return (nt + C - 1) / C;
-    const int g0 = bTo[qb];
-    return (g0 + nt - 1) / share - g0 / share + 1;
+    // a tile belongs to the share its first cost falls in
+    const int g0 = bTo[qb], wq = (bTo[qb + 1] - g0) / nt;
+    return (g0 + (nt - 1) * wq) / share - g0 / share + 1;
   };
   // two key streams: every decode unit has two partial slots and every
   // block a combine entry
@@ -457,10 +468,15 @@ __global__ void __launch_bounds__(1024, 1) sched_kernel(SchedParams p) {
     int t0 = (int)((long long)sp * nt / S), t1 = (int)((long long)(sp + 1) * nt / S);
     int part = 0;
     if (stream) {
+      // share k of the head takes the block's tiles whose first cost lies
+      // in [k share, (k + 1) share); a tile costs wq (the block's Q tiles),
+      // at most share, so every share between the first and the last tile's
+      // holds a tile
       const int g0 = bTo[qb], ppk = p.parts / p.hkv;
+      const int wq = nt > 0 ? (bTo[qb + 1] - g0) / nt : 1;
       const int k = min(g0 / share + sp, ppk - 1);  // the share within the head
-      t0 = max(0, k * share - g0);
-      t1 = min(nt, (k + 1) * share - g0);
+      t0 = sp == 0 ? 0 : min(nt, (k * share - g0 + wq - 1) / wq);
+      t1 = sp == S - 1 ? nt : min(nt, ((k + 1) * share - g0 + wq - 1) / wq);
       part = kvh * ppk + k;
     }
     WorkUnit w;
