@@ -69,8 +69,10 @@ extern "C" {
  * elements are one byte); the 16-byte alignment rule for rows still
  * applies.  Built for Lq = Lv = 64 or 128 and for the MLA head Lq / Lv =
  * 576 / 512 (v_buffer a view of k_buffer's codes), with or without a custom
- * mask; other fp8 calls return PKX_EUNSUPPORTED.  The extend rows of the
- * two-stage form (k_extend / v_extend) stay bf16.
+ * mask, and for the split head dims 192 / 128 and 288 / 256 in the two
+ * extend forms (no mask, no decode); other fp8 calls return
+ * PKX_EUNSUPPORTED.  The extend rows of the two-stage form (k_extend /
+ * v_extend) stay bf16.
  */
 #define PKX_KV_BF16 0
 #define PKX_KV_FP8_E4M3 1
@@ -183,7 +185,8 @@ void pkx_set_stall_injection(int on);
  *   lse_out    nullable fp32 [num_q_tokens, hq] (natural log)
  *   workspace  >= pkx_extend_workspace_size(...) bytes
  * Supported (lq, lv): (64, 64), (128, 128), (576, 512), and the split head
- * dims (192, 128) and (288, 256) (no custom mask and no fp8 pool for those);
+ * dims (192, 128) and (288, 256) (no custom mask for those; an fp8 pool in
+ * the extend forms only);
  * hq % hkv == 0 and hq / hkv <= 128.
  */
 int pkx_extend_attention_fwd(

@@ -67,15 +67,18 @@ static int check_mask_sinks(const uint8_t *custom_mask, const int32_t *mask_indp
 
 // The pool's element format and its scales (an fp8 pool: Lq = Lv = 64 or
 // 128, or the MLA head 576 / 512; with or without a custom mask).
-static int check_kv_format(int kv_dtype, float k_scale, float v_scale, int lq, int lv) {
+static int check_kv_format(int kv_dtype, float k_scale, float v_scale, int lq, int lv,
+                           bool decode) {
   if (kv_dtype == kKvBf16) return PKX_OK;
   if (kv_dtype != kKvFp8E4M3 && kv_dtype != kKvFp8E5M2)
     return set_error(PKX_EINVAL, "kv_dtype %d is not a PKX_KV_* value", kv_dtype);
   if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
     return set_error(PKX_EINVAL, "k_scale and v_scale must be positive and finite");
-  if (!((lq == 64 && lv == 64) || (lq == 128 && lv == 128) || (lq == 576 && lv == 512)))
+  if (!((lq == 64 && lv == 64) || (lq == 128 && lv == 128) || (lq == 576 && lv == 512) ||
+        (split_head_dims(lq, lv) && !decode)))
     return set_error(PKX_EUNSUPPORTED,
-                     "an fp8 pool is built for Lq = Lv = 64 or 128 and for Lq / Lv = 576 / 512");
+                     "an fp8 pool is built for Lq = Lv = 64 or 128, for Lq / Lv = 576 / 512 and, "
+                     "in extend, for the split head dims 192 / 128 and 288 / 256");
   return PKX_OK;
 }
 
@@ -157,7 +160,7 @@ static int two_stage_args(AttnArgs &a, const void *q_extend, const void *k_exten
   if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
   if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
   if ((rc = check_mask_sinks(custom_mask, mask_indptr, sinks))) return rc;
-  if ((rc = check_kv_format(kv_dtype, k_scale, v_scale, lq, lv))) return rc;
+  if ((rc = check_kv_format(kv_dtype, k_scale, v_scale, lq, lv, false))) return rc;
   if (batch == 0 || num_q_tokens == 0) {
     *nothing_to_do = true;
     return PKX_OK;
@@ -351,7 +354,7 @@ int pkx_extend_attention_fwd_unified(const void *q, void *o, const void *k_buffe
   if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
   if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
   if ((rc = check_mask_sinks(custom_mask, mask_indptr, sinks))) return rc;
-  if ((rc = check_kv_format(kv_dtype, k_scale, v_scale, lq, lv))) return rc;
+  if ((rc = check_kv_format(kv_dtype, k_scale, v_scale, lq, lv, false))) return rc;
   if (batch == 0 || num_q_tokens == 0) return PKX_OK;
   if ((rc = check_rows("q", q, 8, 8))) return rc;
   if ((rc = check_rows("o", o, 8, 8))) return rc;
@@ -396,7 +399,7 @@ int pkx_decode_attention_fwd(const void *q, void *o, const void *k_buffer, const
   if (batch < 0) return set_error(PKX_EINVAL, "negative batch");
   if ((rc = check_heads(hq, hkv, lq, lv))) return rc;
   if ((rc = check_scalars(sm_scale, logit_cap))) return rc;
-  if ((rc = check_kv_format(kv_dtype, k_scale, v_scale, lq, lv))) return rc;
+  if ((rc = check_kv_format(kv_dtype, k_scale, v_scale, lq, lv, true))) return rc;
   if (batch == 0) return PKX_OK;
   if ((rc = check_rows("q", q, 8, 8))) return rc;
   if ((rc = check_rows("o", o, 8, 8))) return rc;

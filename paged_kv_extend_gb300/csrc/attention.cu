@@ -1762,19 +1762,43 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
     // V(j-1), which the tensor core frees only after K(j) is full.  Extend
     // tiles (bf16 rows of the two-stage form) take the plain copy.  One
     // cp.async group is committed per issued tile.
-    auto issue_raw = [&](uint32_t stage, const uint8_t *base, int64_t stride, const int *rows) {
+    // (split head dims: by 64-dim atom, as copy_rows does; a row of L codes)
+    auto issue_raw = [&](uint32_t stage, const uint8_t *base, int64_t stride, const int *rows,
+                         auto l_c) {
+      constexpr int L = decltype(l_c)::value;
       static_for<0, NKEYS>([&](auto i_c) {
         constexpr int i = decltype(i_c)::value;
         const int r = rows[i];
         const uint8_t *src = base + (int64_t)max(r, 0) * stride;
-        cp_async_8_at<i * KPP * 128>(stage + dthr, src, r >= 0 ? 8u : 0u);
+        if constexpr (!C::SPLIT) {
+          static_assert(L == C::LQ || L == C::HDV, "row length");
+          cp_async_8_at<i * KPP * 128>(stage + dthr, src, r >= 0 ? 8u : 0u);
+        } else {
+          static_for<0, (L + 63) / 64>([&](auto a_c) {
+            constexpr int a = decltype(a_c)::value;
+            if (a * 8 + ch < L / 8)
+              cp_async_8_at<a * C::BN * 128 + i * KPP * 128>(stage + dthr, src + a * 64,
+                                                             r >= 0 ? 8u : 0u);
+          });
+        }
       });
     };
-    auto convert = [&](uint32_t stage) {
+    auto convert = [&](uint32_t stage, auto l_c) {
+      constexpr int L = decltype(l_c)::value;
       static_for<0, NKEYS>([&](auto i_c) {
         constexpr int i = decltype(i_c)::value;
-        const uint32_t a = stage + dthr + i * KPP * 128;
-        st_shared_u4(a, fp8x8_to_bf16x8<FMT>(ld_shared_u2(a)));
+        if constexpr (!C::SPLIT) {
+          const uint32_t a = stage + dthr + i * KPP * 128;
+          st_shared_u4(a, fp8x8_to_bf16x8<FMT>(ld_shared_u2(a)));
+        } else {
+          static_for<0, (L + 63) / 64>([&](auto a_c) {
+            constexpr int a = decltype(a_c)::value;
+            if (a * 8 + ch < L / 8) {
+              const uint32_t at = stage + dthr + a * C::BN * 128 + i * KPP * 128;
+              st_shared_u4(at, fp8x8_to_bf16x8<FMT>(ld_shared_u2(at)));
+            }
+          });
+        }
       });
       fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
     };
@@ -1824,7 +1848,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           copy_rows(stage, kx, p.ke_st, rows, K_LEN);
           cp_async_arrive_noinc(&k_full[ks]);
         } else {
-          issue_raw(stage, kp8, p.kb_ss, rows);
+          issue_raw(stage, kp8, p.kb_ss, rows, K_LEN);
         }
         cp_async_commit();
         ++kc;
@@ -1840,12 +1864,41 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           copy_rows(stage, vx, p.ve_st, rows, V_LEN);
           cp_async_arrive_noinc(&v_full[vs]);
         } else {
-          issue_raw(stage, vp8, p.vb_ss, rows);
+          issue_raw(stage, vp8, p.vb_ss, rows, V_LEN);
         }
         cp_async_commit();
         ++vc;
         return true;
       };
+      if constexpr (NK_ < 2 || C::NV < 2) {
+        // one K or one V stage (the 288 / 256 layout): the next tile's codes
+        // could only go into the stage this tile holds, so each tile's codes
+        // are converted as soon as they land
+        for (int j = 0; j < nt; ++j) {
+          const bool ext = tile_from_ext(j);
+          if (!fetch() || !issue_k(ext)) {
+            ok = false;
+            break;
+          }
+          if (!ext) {
+            cp_async_wait_group<0>();
+            const int ks = (kc - 1) % NK_;
+            convert(sbase + K0 + ks * C::K_BYTES, K_LEN);
+            mbar_arrive(&k_full[ks]);
+          }
+          if (!issue_v(ext)) {
+            ok = false;
+            break;
+          }
+          if (!ext) {
+            cp_async_wait_group<0>();
+            const int vs = (vc - 1) % C::NV;
+            convert(sbase + C::OFF_V + vs * C::V_BYTES, V_LEN);
+            mbar_arrive(&v_full[vs]);
+          }
+        }
+        continue;
+      }
       bool ext_j = tile_from_ext(0);
       if (!fetch() || !issue_k(ext_j) || !issue_v(ext_j)) {
         ok = false;
@@ -1863,7 +1916,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           // groups issued after K(j): V(j), and K(j+1) if there is one
           if (more) cp_async_wait_group<2>();
           else cp_async_wait_group<1>();
-          convert(sbase + K0 + ks_j * C::K_BYTES);
+          convert(sbase + K0 + ks_j * C::K_BYTES, K_LEN);
           mbar_arrive(&k_full[ks_j]);
         }
         if (more && !issue_v(ext_n)) {
@@ -1874,7 +1927,7 @@ __global__ void __launch_bounds__(Cfg<HD>::THREADS, 1)
           // groups issued after V(j): K(j+1) and V(j+1) if there are
           if (more) cp_async_wait_group<2>();
           else cp_async_wait_group<0>();
-          convert(sbase + C::OFF_V + vs_j * C::V_BYTES);
+          convert(sbase + C::OFF_V + vs_j * C::V_BYTES, V_LEN);
           mbar_arrive(&v_full[vs_j]);
         }
         ext_j = ext_n;
@@ -2419,10 +2472,27 @@ int launch_attention(const AttnArgs &a) {
     else
       rc = e4 ? launch_mla_pair<kDecode, false, 1>(kp, pairs, a.stream)
               : launch_mla_pair<kDecode, false, 2>(kp, pairs, a.stream);
+  } else if (a.kv_fmt != kKvBf16 && split) {
+    // the split head dims over an fp8 pool: the two extend forms, no mask
+    if (a.mode == kDecode || masked)
+      return set_error(PKX_EUNSUPPORTED,
+                       "an fp8 pool with split head dims is built for extend without a mask");
+    const bool e4 = a.kv_fmt == kKvFp8E4M3, two = a.mode == kTwoStage;
+    if (a.lq == 192)
+      rc = two ? (e4 ? launch_attn_kernel<192, kTwoStage, false, 1>(tm, kp, grid, a.stream)
+                     : launch_attn_kernel<192, kTwoStage, false, 2>(tm, kp, grid, a.stream))
+               : (e4 ? launch_attn_kernel<192, kUnified, false, 1>(tm, kp, grid, a.stream)
+                     : launch_attn_kernel<192, kUnified, false, 2>(tm, kp, grid, a.stream));
+    else
+      rc = two ? (e4 ? launch_attn_kernel<288, kTwoStage, false, 1>(tm, kp, grid, a.stream)
+                     : launch_attn_kernel<288, kTwoStage, false, 2>(tm, kp, grid, a.stream))
+               : (e4 ? launch_attn_kernel<288, kUnified, false, 1>(tm, kp, grid, a.stream)
+                     : launch_attn_kernel<288, kUnified, false, 2>(tm, kp, grid, a.stream));
   } else if (a.kv_fmt != kKvBf16) {
     if (!((a.lq == 128 && a.lv == 128) || (a.lq == 64 && a.lv == 64)))
       return set_error(PKX_EUNSUPPORTED,
-                       "an fp8 pool is built for Lq = Lv = 64 or 128 and for Lq / Lv = 576 / 512");
+                       "an fp8 pool is built for Lq = Lv = 64 or 128, for Lq / Lv = 576 / 512 and "
+                       "for the split head dims in extend");
     const bool e4 = a.kv_fmt == kKvFp8E4M3;
     if (a.lq == 128)
       rc = e4 ? launch_attn_fp8<128, 1>(a.mode, masked, tm, kp, grid, a.stream)

@@ -63,6 +63,17 @@ def _extend(lib, **over):
         a["ksc"], a["vsc"], a["lse"], a["ws"], a["wsb"], a["stream"])
 
 
+def _decode(lib, **over):
+    a = dict(q=None, o=None, kb=None, vb=None, kvp=None, kvi=None, batch=1, hq=8, hkv=2, lq=128,
+             lv=128, st=(1024, 128, 1024, 128), slots=16, scale=0.0, cap=0.0, win=-1, kvd=0,
+             ksc=1.0, vsc=1.0, lse=None, ws=None, wsb=0, stream=None)
+    a.update(over)
+    return lib.pkx_decode_attention_fwd(
+        a["q"], a["o"], a["kb"], a["vb"], a["kvp"], a["kvi"], a["batch"], a["hq"], a["hkv"],
+        a["lq"], a["lv"], *a["st"], a["slots"], a["scale"], a["cap"], a["win"], a["kvd"],
+        a["ksc"], a["vsc"], a["lse"], a["ws"], a["wsb"], a["stream"])
+
+
 def test_host_validation_rejects_bad_arguments(lib):
     assert _extend(lib, hq=6, hkv=4) == pkx.PKX_EINVAL
     assert b"multiple" in lib.pkx_last_error_string()
@@ -73,8 +84,13 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _extend(lib, lq=288, lv=256, hq=16, hkv=1) == pkx.PKX_EINVAL
     assert _extend(lib, lq=192, lv=256) == pkx.PKX_EUNSUPPORTED
     assert b"lq=192" in lib.pkx_last_error_string()
-    # an fp8 pool is built for Lq = Lv = 64 / 128 only
-    assert _extend(lib, lq=192, lv=128, kvd=1) == pkx.PKX_EUNSUPPORTED
+    # an fp8 pool with the split head dims is built for extend (past the
+    # format check, the null tensors stop the call), not for decode
+    assert _extend(lib, lq=192, lv=128, kvd=1) == pkx.PKX_EINVAL
+    assert b"q_extend" in lib.pkx_last_error_string()
+    assert _decode(lib, lq=192, lv=128, kvd=1) == pkx.PKX_EUNSUPPORTED
+    assert _decode(lib, lq=288, lv=256, hq=16, hkv=1, kvd=2) == pkx.PKX_EUNSUPPORTED
+    assert _decode(lib, kvd=1) == pkx.PKX_EINVAL  # D = 128: built, null tensors
     assert _extend(lib, hq=256, hkv=1) == pkx.PKX_EUNSUPPORTED
     assert _extend(lib, batch=-1) == pkx.PKX_EINVAL
     assert _extend(lib, scale=float("nan")) == pkx.PKX_EINVAL
@@ -94,7 +110,7 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _extend(lib, kvd=3) == pkx.PKX_EINVAL
     assert _extend(lib, kvd=1, ksc=0.0) == pkx.PKX_EINVAL
     assert _extend(lib, kvd=2, vsc=float("inf")) == pkx.PKX_EINVAL
-    assert _extend(lib, kvd=1, lq=192, lv=128) == pkx.PKX_EUNSUPPORTED
+    assert _extend(lib, kvd=1, lq=96, lv=96) == pkx.PKX_EUNSUPPORTED
     # the MLA head over an fp8 pool is built: past the format check, the null
     # tensors stop the call
     assert _extend(lib, kvd=1, lq=576, lv=512, hq=16, hkv=1) == pkx.PKX_EINVAL

@@ -281,6 +281,18 @@ class _Model:
             nt = u["nt"]
             if nt == 0:
                 continue
+            if (self.NK < 2 or self.NV < 2) and self.mistake != "one stage converted one tile behind":
+                # one K or one V stage (the 288 / 256 layout): a tile's codes
+                # are converted as soon as they land, before the next tile
+                for _ in range(nt):
+                    yield from fetch()
+                    yield from issue("K", kc, self.NK)
+                    yield ("arrive", f"KF{kc % self.NK}")
+                    kc += 1
+                    yield from issue("V", vc, self.NV)
+                    yield ("arrive", f"VF{vc % self.NV}")
+                    vc += 1
+                continue
             yield from fetch()
             yield from issue("K", kc, self.NK)
             yield from issue("V", vc, self.NV)
@@ -436,6 +448,24 @@ def test_fp8_protocols_have_no_deadlock_and_no_parity_aliasing():
         kind = rng.choice(["two", "one"])
         units = [{"kind": kind, "nt": rng.choice([0, 1, 2, 3, 6])} for _ in range(rng.randint(1, 10))]
         _Model(units, seed=t, f16_decode=True, stages=stages).run()
+
+
+def test_split_head_dim_fp8_protocol():
+    """The split head dims over an fp8 pool (extend): 192 / 128 (two stages
+    each) converts a tile after the next one is issued; 288 / 256 (one stage
+    each) converts a tile as soon as it lands, since the one-behind order
+    would wait for its own stage."""
+    rng = random.Random(8)
+    for stages in ((2, 2, 3), (1, 1, 3)):
+        for t in range(150):
+            units = [{"kind": "one", "nt": rng.choice([0, 1, 2, 3, 5, 8])}
+                     for _ in range(rng.randint(1, 12))]
+            _Model(units, seed=t, fp8=True, stages=stages).run()
+    with pytest.raises(AssertionError):  # the one-behind order on one stage deadlocks
+        for t in range(150):
+            units = [{"kind": "one", "nt": rng.choice([1, 2, 3])} for _ in range(rng.randint(1, 6))]
+            _Model(units, seed=t, fp8=True, stages=(1, 1, 3),
+                   mistake="one stage converted one tile behind").run()
 
 
 @pytest.mark.parametrize("mistake", ["raw slot reused before its conversion",

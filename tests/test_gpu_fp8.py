@@ -56,7 +56,8 @@ def test_fp8_write_bit_exact(dt, n, hkv, d, ks, vs, amp):
 
 # ------------------------------------------------------- attention over fp8
 def _extend_case(dt, lq, hq, hkv, prefix, extend, cap, window, ks, vs, seed):
-    spec = W.small_spec(batch=len(prefix), hq=hq, hkv=hkv, lq=lq, lv=lq, prefix=prefix,
+    lv = {192: 128, 288: 256}.get(lq, lq)  # the split head dims
+    spec = W.small_spec(batch=len(prefix), hq=hq, hkv=hkv, lq=lq, lv=lv, prefix=prefix,
                         extend=extend, logit_cap=cap, sliding_window=window, seed=seed)
     wl = W.draw(spec)
     kb, vb = wl.pool_fp8(dt, ks, vs)
@@ -69,6 +70,11 @@ CASES = [
     (128, 28, 4, [600, 0, 90, 3000], [200, 1, 19, 5], 20.0, 100, 0.05, 0.02),
     (64, 12, 3, [0, 999, 45], [500, 2, 129], 0.0, 250, 0.5, 2.0),
     (64, 8, 8, [40, 1300], [70, 33], 5.0, -1, 0.25, 0.125),
+    # the split head dims (one Q tile per unit)
+    (192, 16, 16, [0, 70, 300], [9, 1, 130], 0.0, -1, 0.5, 0.25),
+    (192, 32, 8, [129, 5, 1000], [17, 300, 3], 20.0, 100, 0.05, 0.02),
+    (288, 16, 1, [0, 2000, 33], [64, 1, 200], 0.0, -1, 1.0, 2.0),
+    (288, 8, 2, [500, 7], [3, 150], 5.0, 64, 0.25, 0.125),
 ]
 
 
@@ -86,7 +92,7 @@ def test_extend_over_fp8_pool(dt, lq, hq, hkv, prefix, extend, cap, window, ks, 
                                      k_scale=ks, v_scale=vs)
     dkb, dvb = kb.to(DEV), vb.to(DEV)
     n = wl.n_q_tokens
-    o = torch.full((n, hq, lq), float("nan"), dtype=torch.bfloat16, device=DEV)
+    o = torch.full((n, hq, s.lv), float("nan"), dtype=torch.bfloat16, device=DEV)
     lse = torch.full((n, hq), float("nan"), dtype=torch.float32, device=DEV)
     ws = pkx.extend_attention_fwd(wl.q.to(DEV), k_ext.to(DEV), v_ext.to(DEV), o, dkb, dvb,
                                   wl.qo_indptr.to(DEV), wl.kv_indptr.to(DEV),
